@@ -1,0 +1,156 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+This package is the checker, not the product.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may load
+it.  It shares no code with the CUDA library and imports nothing from it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, two passes per query
+row: scores and max, then weights, sum and weighted V).  This module only
+compiles that file with the host C compiler and marshals numpy arrays through
+ctypes.
+
+Definition followed (the "ThunderKittens" attention forward as printed on
+10100.com/article/71410160, section "writing a kernel with TK",
+attn_fwd_template consumer::compute / consumer::finish, and the inner-loop
+excerpt on alanwu.xyz/posts/thunderkittens):
+
+    s_ij   = scale * <Q_i, K_j>            j in J_i  (all keys, or j <= i if causal)
+    LSE_i  = max_j s_ij + ln(sum_j exp(s_ij - max_j s_ij))
+    O_i    = sum_j exp(s_ij - LSE_i) V_j
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libtk_attn_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libtk_attn_oracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        # -O2 without -ffast-math: IEEE fp64 semantics are kept.
+        cmd = ["gcc", "-O2", "-std=gnu11", "-Wall", "-fPIC", "-shared", "-pthread",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def bind(path: str):
+    """Load a compiled oracle library from ``path`` and declare its entry
+    points.  ``_load`` uses it for the default build; the oracle's own
+    mutation tests use it for deliberately broken copies."""
+    lib = ctypes.CDLL(path)
+    _declare(lib)
+    return lib
+
+
+def _declare(lib) -> None:
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.tkor_attn_fwd.argtypes = [P, P, P, P, P, i64, i64, i64, i64,
+                                  ctypes.c_int, ctypes.c_double, ctypes.c_int]
+    lib.tkor_attn_fwd.restype = ctypes.c_int
+    lib.tkor_attn_fwd_rows.argtypes = [P, P, P, i64, i64, ctypes.c_int,
+                                       ctypes.c_double, P, i64, P, P, ctypes.c_int]
+    lib.tkor_attn_fwd_rows.restype = ctypes.c_int
+    lib.tkor_attn_weights.argtypes = [P, P, i64, i64, ctypes.c_int,
+                                      ctypes.c_double, P]
+    lib.tkor_attn_weights.restype = ctypes.c_int
+    lib.tkor_last_threads.argtypes = []
+    lib.tkor_last_threads.restype = ctypes.c_int
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = bind(build())
+    return _lib
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 input as a C-contiguous uint16 array of its bit patterns.
+
+    Accepts a numpy uint16 array (already bit patterns) or a torch bfloat16
+    tensor on the CPU.
+    """
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint16:
+            raise TypeError("numpy inputs must be uint16 bf16 bit patterns")
+        return np.ascontiguousarray(a)
+    import torch  # only for the bfloat16 -> bits view
+    if not isinstance(a, torch.Tensor) or a.dtype != torch.bfloat16:
+        raise TypeError("expected a torch.bfloat16 tensor or uint16 bit patterns")
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy()
+                                .view(np.uint16))
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, threads: int = 0, lib=None):
+    """Whole problem.  q, k, v: [B,H,N,D] bf16.  Returns (O, LSE) as float64
+    arrays of shapes [B,H,N,D] and [B,H,N]."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 4 or qb.shape != kb.shape or qb.shape != vb.shape:
+        raise ValueError("q, k, v must share one [B,H,N,D] shape")
+    B, H, N, D = qb.shape
+    O = np.empty((B, H, N, D), dtype=np.float64)
+    L = np.empty((B, H, N), dtype=np.float64)
+    rc = (lib or _load()).tkor_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(O), _ptr(L),
+                               B, H, N, D, int(bool(causal)), float(scale), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return O, L
+
+
+def attn_fwd_rows(q, k, v, rows, causal: bool, scale: float, threads: int = 0):
+    """Selected query rows of ONE head.  q, k, v: [N,D] bf16; rows: int
+    indices.  Returns (O[len(rows),D], LSE[len(rows)]) as float64."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    if qb.ndim != 2 or qb.shape != kb.shape or qb.shape != vb.shape:
+        raise ValueError("q, k, v must share one [N,D] shape")
+    N, D = qb.shape
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    O = np.empty((r.size, D), dtype=np.float64)
+    L = np.empty((r.size,), dtype=np.float64)
+    rc = _load().tkor_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), N, D, int(bool(causal)),
+                                    float(scale), _ptr(r), r.size, _ptr(O), _ptr(L),
+                                    int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return O, L
+
+
+def attn_weights(q, k, causal: bool, scale: float) -> np.ndarray:
+    """Attention weight matrix of ONE head (tiny N only): float64 [N,N]."""
+    qb, kb = _bits(q), _bits(k)
+    N, D = qb.shape
+    P = np.empty((N, N), dtype=np.float64)
+    rc = _load().tkor_attn_weights(_ptr(qb), _ptr(kb), N, D, int(bool(causal)),
+                                   float(scale), _ptr(P))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return P
+
+
+def last_threads() -> int:
+    """Threads the last oracle call actually ran on."""
+    return int(_load().tkor_last_threads())

@@ -1,0 +1,238 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of the attention forward pass that the
+ * fused GPU kernel computes.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark load it; the product path never does.
+ * It shares no code, header or helper with the CUDA library.
+ *
+ * What it computes (per batch b, head h, query row i), written out as the
+ * plain definition of softmax attention with a per-row log-sum-exp:
+ *
+ *   J_i    = {0..N-1}            (non-causal)
+ *          = {0..i}              (causal: key j may be seen by query i iff j <= i)
+ *   s_ij   = scale * sum_d Q[i,d] * K[j,d]                 for j in J_i
+ *   m_i    = max_j s_ij
+ *   l_i    = sum_j exp(s_ij - m_i)
+ *   LSE_i  = m_i + ln(l_i)                                 (natural log, scale included)
+ *   O[i,d] = (sum_j exp(s_ij - m_i) * V[j,d]) / l_i
+ *
+ * Sources: "ThunderKittens" attention kernel as printed on the page
+ * 10100.com/article/71410160, section "writing a kernel with TK"
+ * (attn_fwd_template, consumer::compute forms Q K^T, takes the row max,
+ * exponentiates, accumulates the row sum and P V; consumer::finish divides
+ * by the row sum once); alanwu.xyz/posts/thunderkittens, the attention inner
+ * loop excerpt (same steps, with the ragged key tail filled with -inf so that
+ * keys past the sequence end take no weight).  The pages compute the
+ * exponentials in base 2 with scale*log2(e) folded in; that is the same
+ * number as exp() of the scaled score, so the definition is written with
+ * exp/log here.  The pages store no LSE; the reading taken is
+ * LSE = scale*max + ln(sum), in natural log.  The causal mask is not on the
+ * pages; the reading taken is top-left aligned, key j <= query i.
+ *
+ * Two passes, no streaming, no tiling, no blocking: pass 1 forms every score
+ * of the row and its maximum, pass 2 forms the weights, their sum and the
+ * weighted sum of V.  Inputs are bf16 bit patterns, converted exactly to
+ * double.  Outputs are double.
+ *
+ * Parallelism: independent rows are handed to POSIX threads; each row is
+ * computed by exactly one thread with the same loop order, so the result
+ * does not depend on the thread count.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_bits_to_double(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One query row of one head.  q: D values; K, V: N x D (double, row-major).
+ * s: scratch of N doubles. */
+static void attention_row(const double *q, const double *K, const double *V,
+                          int64_t N, int64_t D, int causal, double scale, int64_t i,
+                          double *s, double *o_row, double *lse_out) {
+    int64_t nkeys = causal ? (i + 1) : N;
+    if (nkeys > N) nkeys = N;
+
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        const double *k = K + j * D;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d) dot += q[d] * k[d];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+
+    /* pass 2: weights, their sum, and the weighted sum of V rows */
+    double l = 0.0;
+    for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        const double *v = V + j * D;
+        for (int64_t d = 0; d < D; ++d) o_row[d] += p * v[d];
+    }
+    for (int64_t d = 0; d < D; ++d) o_row[d] /= l;
+    *lse_out = m + log(l);
+}
+
+/* ------------------------------------------------------------------------ */
+/* work distribution                                                         */
+
+typedef struct {
+    /* one head, already widened to double */
+    const double *Q, *K, *V;
+    int64_t N, D;
+    int causal;
+    double scale;
+    const int64_t *rows; /* NULL: all rows 0..N-1 */
+    int64_t nrows;
+    double *O;   /* nrows x D */
+    double *LSE; /* nrows */
+    int64_t next;
+    pthread_mutex_t lock;
+} head_job;
+
+static void *head_worker(void *arg) {
+    head_job *job = (head_job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(job->N > 0 ? job->N : 1));
+    if (!s) return NULL;
+    const int64_t chunk = 8;
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        int64_t begin = job->next;
+        job->next += chunk;
+        pthread_mutex_unlock(&job->lock);
+        if (begin >= job->nrows) break;
+        int64_t end = begin + chunk < job->nrows ? begin + chunk : job->nrows;
+        for (int64_t r = begin; r < end; ++r) {
+            int64_t i = job->rows ? job->rows[r] : r;
+            attention_row(job->Q + i * job->D, job->K, job->V, job->N, job->D, job->causal,
+                          job->scale, i, s, job->O + r * job->D, job->LSE + r);
+        }
+    }
+    free(s);
+    return NULL;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static int g_last_threads = 0;
+
+/* Computes the listed rows of one head.  Returns 0, or -1 on bad arguments or
+ * allocation failure. */
+static int run_head(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, int64_t N,
+                    int64_t D, int causal, double scale, const int64_t *rows, int64_t nrows,
+                    double *O, double *LSE, int nthreads) {
+    size_t n = (size_t)N * (size_t)D;
+    double *Q = (double *)malloc(sizeof(double) * n);
+    double *K = (double *)malloc(sizeof(double) * n);
+    double *V = (double *)malloc(sizeof(double) * n);
+    if (!Q || !K || !V) {
+        free(Q); free(K); free(V);
+        return -1;
+    }
+    for (size_t t = 0; t < n; ++t) {
+        Q[t] = bf16_bits_to_double(Qb[t]);
+        K[t] = bf16_bits_to_double(Kb[t]);
+        V[t] = bf16_bits_to_double(Vb[t]);
+    }
+    head_job job;
+    job.Q = Q; job.K = K; job.V = V;
+    job.N = N; job.D = D; job.causal = causal; job.scale = scale;
+    job.rows = rows; job.nrows = nrows; job.O = O; job.LSE = LSE;
+    job.next = 0;
+    pthread_mutex_init(&job.lock, NULL);
+
+    int T = resolve_threads(nthreads);
+    if ((int64_t)T > (nrows + 7) / 8) T = (int)((nrows + 7) / 8);
+    if (T < 1) T = 1;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)T);
+    int started = 0;
+    for (int t = 1; tid && t < T; ++t) {
+        if (pthread_create(&tid[started], NULL, head_worker, &job) != 0) break;
+        ++started;
+    }
+    if (started + 1 > g_last_threads) g_last_threads = started + 1;
+    head_worker(&job); /* the calling thread works too */
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    free(tid);
+    pthread_mutex_destroy(&job.lock);
+    free(Q); free(K); free(V);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* exported entry points                                                     */
+
+/* Whole problem.  Q, K, V: bf16 bits, contiguous [B,H,N,D].
+ * O: double [B,H,N,D].  LSE: double [B,H,N].  nthreads <= 0: all online CPUs. */
+int tkor_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O,
+                  double *LSE, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                  double scale, int nthreads) {
+    if (!Q || !K || !V || !O || !LSE || B < 1 || H < 1 || N < 1 || D < 1) return -1;
+    g_last_threads = 0;
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        size_t off = (size_t)bh * (size_t)N * (size_t)D;
+        if (run_head(Q + off, K + off, V + off, N, D, causal, scale, NULL, N, O + off,
+                     LSE + (size_t)bh * (size_t)N, nthreads))
+            return -1;
+    }
+    return 0;
+}
+
+/* Selected rows of one head.  Q, K, V: bf16 bits [N,D] of that head.
+ * rows: nrows query indices in [0,N).  O: double [nrows,D]; LSE: double [nrows]. */
+int tkor_attn_fwd_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int64_t N,
+                       int64_t D, int causal, double scale, const int64_t *rows,
+                       int64_t nrows, double *O, double *LSE, int nthreads) {
+    if (!Q || !K || !V || !O || !LSE || !rows || N < 1 || D < 1 || nrows < 0) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+    g_last_threads = 0;
+    return run_head(Q, K, V, N, D, causal, scale, rows, nrows, O, LSE, nthreads);
+}
+
+/* The attention weights of one head, P[i,j] = exp(s_ij - m_i) / l_i, with
+ * P[i,j] = 0 for masked keys.  Q, K: bf16 bits [N,D].  P: double [N,N].
+ * Meant for tiny N (it materialises the N x N matrix). */
+int tkor_attn_weights(const uint16_t *Qb, const uint16_t *Kb, int64_t N, int64_t D,
+                      int causal, double scale, double *P) {
+    if (!Qb || !Kb || !P || N < 1 || D < 1) return -1;
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t nkeys = causal ? i + 1 : N;
+        double m = -INFINITY;
+        double *row = P + i * N;
+        for (int64_t j = 0; j < N; ++j) row[j] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                dot += bf16_bits_to_double(Qb[i * D + d]) * bf16_bits_to_double(Kb[j * D + d]);
+            row[j] = scale * dot;
+            if (row[j] > m) m = row[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            row[j] = exp(row[j] - m);
+            l += row[j];
+        }
+        for (int64_t j = 0; j < nkeys; ++j) row[j] /= l;
+    }
+    return 0;
+}
+
+/* Largest number of threads used by the last call. */
+int tkor_last_threads(void) { return g_last_threads; }

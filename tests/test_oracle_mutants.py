@@ -1,0 +1,72 @@
+"""The oracle's pins must be strong enough to catch a plausible mistake
+anywhere in it.  Each case below plants one mistake in a temporary copy of
+the oracle source, compiles it with the host C compiler and runs the pins on
+the copy: at least one pin must fail.  CPU only; the real oracle is
+untouched."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("scale dropped", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("scale applied twice", "s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
+    ("max not subtracted in the weights", "double p = exp(s[j] - m);", "double p = exp(s[j]);"),
+    ("max dropped from LSE", "*lse_out = m + log(l);", "*lse_out = log(l);"),
+    ("base-2 LSE", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    ("sign of the exponent flipped", "double p = exp(s[j] - m);", "double p = exp(m - s[j]);"),
+    ("minimum instead of maximum", "if (s[j] > m) m = s[j];", "if (s[j] < m || j == 0) m = s[j];"),
+    ("causal mask excludes the diagonal", "int64_t nkeys = causal ? (i + 1) : N;",
+     "int64_t nkeys = causal ? (i > 0 ? i : 1) : N;"),
+    ("causal mask ignored", "int64_t nkeys = causal ? (i + 1) : N;", "int64_t nkeys = N;"),
+    ("causal mask one key too wide", "int64_t nkeys = causal ? (i + 1) : N;",
+     "int64_t nkeys = causal ? (i + 2) : N;"),
+    ("output not normalised", "for (int64_t d = 0; d < D; ++d) o_row[d] /= l;", ""),
+    ("value row of the query instead of the key", "const double *v = V + j * D;",
+     "const double *v = V + i * D;"),
+    ("transposed key index", "dot += q[d] * k[d];", "dot += q[d] * K[(d % N) * D + (j % D)];"),
+    ("query element reused", "dot += q[d] * k[d];", "dot += q[0] * k[d];"),
+    ("last key skipped", "for (int64_t j = 0; j < nkeys; ++j) {\n        double p",
+     "for (int64_t j = 0; j + 1 < nkeys || (nkeys == 1 && j == 0); ++j) {\n        double p"),
+    ("sum not reset per row", "double l = 0.0;\n    for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;",
+     "static double l = 0.0;\n    for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;"),
+]
+
+
+def _compile(src_text: str, tmp_path, tag: str) -> str:
+    c = tmp_path / f"mut_{tag}.c"
+    so = tmp_path / f"libmut_{tag}.so"
+    c.write_text(src_text)
+    subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-pthread", str(c),
+                    "-o", str(so), "-lm"], check=True, capture_output=True)
+    return str(so)
+
+
+def _fwd_for(lib):
+    return lambda q, k, v, causal, scale: oracle.attn_fwd(q, k, v, causal, scale, lib=lib)
+
+
+def test_unmutated_copy_passes(tmp_path):
+    lib = oracle.bind(_compile(open(SRC).read(), tmp_path, "clean"))
+    for check in pins.ALL_CHECKS:
+        check(_fwd_for(lib))
+
+
+@pytest.mark.parametrize("name,orig,mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation anchor for '{name}' not unique in the oracle"
+    lib = oracle.bind(_compile(text.replace(orig, mutant), tmp_path, str(abs(hash(name)))))
+    caught = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(_fwd_for(lib))
+        except AssertionError as e:  # a pin failed, as it should
+            caught.append((check.__name__, str(e)[:80]))
+    assert caught, f"no pin caught the planted mistake: {name}"
