@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--all]
+
+One step = one tk_attn_fwd launch over the whole workload (every (b,h) head,
+every query row), inputs resident in HBM.  Default workload: B16 H32 N1024
+D128 non-causal, Q,K ~ N(0,3^2), V ~ U(-1,1) (the non-causal D=128 shape the
+>=60%-of-peak target is stated for).  Its inputs (3 x 128 MiB) and output
+exceed the 126 MiB L2, so no explicit flush is needed between steps.
+
+Prints ONE JSON line on rank 0 (``--all``: one line per workload).  Metric:
+attention forward TFLOP/s, algorithmic flops 4*B*H*N^2*D (halved under the
+causal mask).  Extra objects: ``roofline`` (tensor-bound, against the measured
+dense bf16 peak), ``cpu_baseline`` (the fp64 CPU oracle timed on a bounded
+sample on this host), ``e2e`` (the same metric through the public API with
+pinned host buffers, copies inside the timed region), ``clocks`` (sampled
+with nvidia-smi during the timed region) and ``gpu_launches``.
+
+``--impl reference``: the comparison arm is the fp64 CPU oracle (there is no
+runnable reference implementation), timed on this host's cores on a bounded
+sample of the same workload per step.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the full workload on
+its own GPU (independent problems, no data-path collective); the step time is
+the max over ranks and ``value`` counts the flops of all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 (fraction of dense BF16 peak) vs CPU oracle"
+FALLBACK_BF16_TFLOPS = 1900.0  # one earlier GB300 measurement, used only without MEASURED_PEAKS.json
+L2_BYTES = 126 * 1024 * 1024
+KERNEL_SOURCES = ["tiled_attention_tk_gb300/csrc/attn_fwd.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh"]
+DEFAULT_WORKLOAD = 4
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def max_over_ranks(value: float, dist_mod, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity on one rank)."""
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    """(bf16 burst TF/s, label) from MEASURED_PEAKS.json, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            v = d.get("bf16_tflops")
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v:
+                return float(v), "of measured"
+        except (OSError, ValueError, TypeError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "of fallback"
+
+
+def traffic_for(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while it runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={interval_ms}"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def time_oracle_sample(w, q, k, v, budget_s: float, min_rows: int = 64):
+    """Times the fp64 oracle on whole heads of the workload, one after another,
+    until ``budget_s`` of work has been done (at least ``min_rows`` rows).
+    Returns (TFLOP/s, cores, description)."""
+    import oracle
+    oracle.build()
+    flops_per_row_full = 4.0 * w.N * w.D  # non-causal per-row flops
+    done_flops, rows_done, t_total, heads = 0.0, 0, 0.0, 0
+    start = time.perf_counter()
+    bh_total = w.B * w.H
+    while True:
+        b, h = divmod(heads % bh_total, w.H)
+        # whole head, but at most enough rows to stay near the budget
+        remaining = max(budget_s - (time.perf_counter() - start), 0.0)
+        rows = list(range(w.N))
+        if rows_done and t_total > 0:
+            rate = rows_done / t_total
+            rows = rows[: max(min_rows, min(w.N, int(rate * remaining)))]
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        if w.causal:
+            done_flops += sum(4.0 * (r + 1) * w.D for r in rows)
+        else:
+            done_flops += flops_per_row_full * len(rows)
+        rows_done += len(rows)
+        heads += 1
+        if time.perf_counter() - start >= budget_s or heads >= bh_total:
+            break
+    cores = oracle.last_threads()
+    desc = (f"{rows_done} query rows of {heads} head(s) of {w.name} "
+            f"({done_flops / 1e9:.2f} GFLOP fp64, {t_total:.1f} s)")
+    return done_flops / t_total / 1e12, cores, desc
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import torch
+    import tiled_attention_tk_gb300 as tk
+    from tiled_attention_tk_gb300.inputs import workload_inputs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_mod = init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+
+    q, k, v = workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    qp, kp, vp, op, lp = qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr()
+
+    def step():
+        tk.fwd_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.D, w.causal, w.scale, sh)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 or True else None
+    if dist_mod:
+        dist_mod.barrier()
+    torch.cuda.synchronize(dev)
+    start_ev.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist_mod:
+        dist_mod.barrier()
+    clocks = sampler.stop()
+    total_ms = start_ev.elapsed_time(end_ev)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
+    total_ms = max_over_ranks(total_ms, dist_mod, dev)
+    ms_per_step = total_ms / args.steps
+    value = w.flops * ws / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    e2e_steps = max(3, min(20, args.steps // 50))
+    tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)  # warm
+    if dist_mod:
+        dist_mod.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = max_over_ranks(e2e_s, dist_mod, dev)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    if rank != 0:
+        if dist_mod:
+            dist_mod.barrier()
+        return None
+    peak, peak_label = peaks()
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
+        "config": dict(w.describe(), l2="inputs 384 MiB + output 128 MiB > 126 MiB L2, no flush"
+                       if w.index == DEFAULT_WORKLOAD else
+                       ("inputs > L2, no flush" if 3 * w.B * w.H * w.N * w.D * 2 > L2_BYTES
+                        else "inputs fit in L2: warm-L2 number")),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_label, "traffic": traffic_for(w.name),
+                     "kernel": f"attn_fwd_kernel<{w.D}>", "kernel_ms": round(kernel_ms, 5)},
+        "e2e": {"value": round(w.flops * ws / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, desc = time_oracle_sample(w, q, k, v, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle", "sample": desc}
+    if dist_mod:
+        dist_mod.barrier()
+    return line
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    from tiled_attention_tk_gb300.inputs import workload_inputs
+    oracle.build()
+    q, k, v = workload_inputs(w)
+    # Rows per step: sized from a measured rate so K steps take ~budget seconds.
+    probe_rows = list(range(min(w.N, 64)))
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q[0, 0], k[0, 0], v[0, 0], probe_rows, w.causal, w.scale)
+    rate = len(probe_rows) / max(time.perf_counter() - t0, 1e-6)
+    rows_per_step = int(max(8, min(w.N, rate * args.reference_budget / max(1, args.steps + args.warmup))))
+
+    def step(i):
+        bh = i % (w.B * w.H)
+        b, h = divmod(bh, w.H)
+        start = (i * rows_per_step) % w.N
+        rows = [(start + r) % w.N for r in range(rows_per_step)]
+        oracle.attn_fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
+        if w.causal:
+            return sum(4.0 * (r + 1) * w.D for r in rows)
+        return 4.0 * w.N * w.D * len(rows)
+
+    for i in range(args.warmup):
+        step(i)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = oracle.last_threads()
+    sample = (f"{rows_per_step} query rows of one (b,h) head of {w.name} per step "
+              f"(a 1/{w.B * w.H * w.N / rows_per_step:.0f} share of the workload), fp64")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
+        "config": w.describe(),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--reference-budget", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, _ = dist_env()
+    if ws != args.gpus and ws != 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
+
+    from tiled_attention_tk_gb300.inputs import WORKLOADS
+    idxs = [1, 2, 3, 4, 5] if args.all else [args.workload]
+    for idx in idxs:
+        w = WORKLOADS[idx]
+        line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

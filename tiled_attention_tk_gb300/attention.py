@@ -1,0 +1,106 @@
+"""Python entry points over the C ABI (argument marshalling only: every step
+of the attention forward runs in the CUDA library)."""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+            N: int, D: int, causal: bool, scale: float, stream_handle: int) -> None:
+    """tk_attn_fwd on raw device pointers; raises TkError on a non-zero status."""
+    rc = _lib.load().tk_attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, D,
+                                 int(bool(causal)), float(scale), stream_handle)
+    _lib.check(rc, "tk_attn_fwd")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: float | None = None, out: torch.Tensor | None = None,
+        lse: torch.Tensor | None = None, stream=None):
+    """Fused attention forward.
+
+    q, k, v: bf16 [B, H, N, D], D in {64, 128}.  Returns (O bf16 [B,H,N,D],
+    LSE fp32 [B,H,N]) with O = softmax(scale QK^T [+causal]) V and LSE the
+    natural-log row log-sum-exp.  ``scale`` defaults to 1/sqrt(D).
+
+    CUDA inputs: the kernel is enqueued on ``stream`` (default: the current
+    stream) and the call returns without synchronising.  CPU inputs (ideally
+    pinned): they are copied to the current CUDA device, the kernel runs, and
+    O and LSE are copied back into CPU tensors (pinned when the inputs are);
+    the call then returns after the stream has finished.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{n} must be bfloat16")
+        if t.dim() != 4:
+            raise ValueError(f"{n} must be [B, H, N, D]")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+
+    if q.device.type == "cpu":
+        return _fwd_from_host(q, k, v, bool(causal), float(scale), stream)
+    if q.device.type != "cuda":
+        raise ValueError("inputs must be CUDA or CPU tensors")
+
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    with torch.cuda.device(q.device):
+        fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                B, H, N, D, causal, scale, _stream_handle(stream))
+    return out, lse
+
+
+def _fwd_from_host(q, k, v, causal, scale, stream):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    pinned = q.is_pinned()
+    with torch.cuda.stream(s):
+        qd = q.to(dev, non_blocking=True)
+        kd = k.to(dev, non_blocking=True)
+        vd = v.to(dev, non_blocking=True)
+        o, lse = fwd(qd, kd, vd, causal, scale, stream=s)
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=pinned)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=pinned)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+    s.synchronize()
+    return o_h, l_h
+
+
+def device_status(stream=None) -> tuple[int, int]:
+    """(status, detail): synchronises the stream, reads and clears the device
+    status word.  status is 0 or TK_ERR_DEVICE_TIMEOUT."""
+    detail = ctypes.c_uint32(0)
+    rc = _lib.load().tk_attn_device_status(_stream_handle(stream), ctypes.byref(detail))
+    if rc not in (_lib.TK_OK, _lib.STATUS["TK_ERR_DEVICE_TIMEOUT"]):
+        _lib.check(rc, "tk_attn_device_status")
+    return rc, detail.value
+
+
+def selftest_timeout(limit_ns: int, stream=None) -> None:
+    """Enqueue the bounded-wait self test (a wait nothing ends, given up after
+    ``limit_ns``)."""
+    _lib.check(_lib.load().tk_attn_selftest_timeout(int(limit_ns), _stream_handle(stream)),
+               "tk_attn_selftest_timeout")

@@ -1,0 +1,218 @@
+// tk_attn_api.cpp -- the C ABI declared in include/tk_attn.h: argument
+// validation, TMA tensor-map encoding, per-device caches and the launch.
+//
+// The call sequence follows the launcher idiom of the ThunderKittens blog
+// post (alanwu.xyz/posts/thunderkittens, run_add_kernel: launch, then read
+// cudaGetLastError and report it), minus the synchronisation: the launch is
+// asynchronous on the caller's stream and errors come back as status codes.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime_api.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "tk_attn.h"
+#include "tk_attn_internal.h"
+
+namespace {
+
+constexpr int kVersionMajor = 0;
+constexpr int kVersionMinor = 1;
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda_error = 0;
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return TK_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime so the
+// library does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else if (g_encode_err == cudaSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+    });
+    return g_encode;
+}
+
+struct DeviceInfo {
+    bool checked = false;
+    bool supported = false;
+    int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+// Checks (once per device) that the current device is compute capability
+// 10.3, the only target the kernels are compiled for.
+int current_device(int *num_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return TK_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_devices_mu);
+    DeviceInfo &info = g_devices[dev];
+    if (!info.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e);
+        info.supported = (major == 10 && minor == 3);
+        info.num_sms = sms;
+        info.checked = true;
+    }
+    if (!info.supported) return TK_ERR_UNSUPPORTED_DEVICE;
+    *num_sms = info.num_sms;
+    return TK_OK;
+}
+
+bool overlaps(const void *a, uint64_t na, const void *b, uint64_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_device_memory(const void *p) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // clear the sticky-free error state of this query
+        return TK_ERR_NOT_DEVICE_MEMORY;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return TK_ERR_NOT_DEVICE_MEMORY;
+    return TK_OK;
+}
+
+// 3-D view {D, N, B*H} of a contiguous [B,H,N,D] bf16 tensor, loaded as
+// 128-row x 64-column boxes with the 128-byte swizzle; rows past N read as 0.
+int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int64_t BH) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail_cuda(g_encode_err);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                     box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+    return TK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                int64_t H, int64_t N, int64_t D, int causal, float scale, cudaStream_t stream) {
+    // ---- host-side validation: nothing is enqueued unless all of it passes
+    if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
+    if (D != 64 && D != 128) return TK_ERR_UNSUPPORTED_D;
+    // TMA coordinates and the launch grid are 32-bit.
+    if (N > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
+    const int64_t BH = B * H;
+    if (BH > INT64_MAX / N / D / 2) return TK_ERR_BAD_SHAPE;
+    const int64_t n_tiles = (N + 127) / 128;
+    if (n_tiles * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    if (causal != 0 && causal != 1) return TK_ERR_BAD_FLAG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return TK_ERR_BAD_SCALE;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+        return TK_ERR_MISALIGNED;
+    const uint64_t tensor_bytes = static_cast<uint64_t>(BH) * N * D * 2;
+    const uint64_t lse_bytes = static_cast<uint64_t>(BH) * N * 4;
+    if (overlaps(O, tensor_bytes, Q, tensor_bytes) || overlaps(O, tensor_bytes, K, tensor_bytes) ||
+        overlaps(O, tensor_bytes, V, tensor_bytes) || overlaps(LSE, lse_bytes, Q, tensor_bytes) ||
+        overlaps(LSE, lse_bytes, K, tensor_bytes) || overlaps(LSE, lse_bytes, V, tensor_bytes) ||
+        overlaps(LSE, lse_bytes, O, tensor_bytes))
+        return TK_ERR_ALIAS;
+
+    int num_sms = 0;
+    int rc = current_device(&num_sms);
+    if (rc != TK_OK) return rc;
+    const void *ptrs[5] = {Q, K, V, O, LSE};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+
+    tk::AttnParams p;
+    if ((rc = encode_qkv_map(&p.tmQ, Q, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmK, K, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmV, V, N, D, BH)) != TK_OK) return rc;
+    p.O = O;
+    p.LSE = LSE;
+    p.N = static_cast<int>(N);
+    p.BH = static_cast<int>(BH);
+    p.causal = causal;
+    p.n_qtiles = static_cast<int>(n_tiles);
+    p.n_kvtiles = static_cast<int>(n_tiles);
+    p.scale = scale;
+    p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    cudaError_t e = tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
+
+int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
+    uint32_t status = 0, where = 0;
+    cudaError_t e = tk::read_and_clear_status(stream, &status, &where);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail) *detail = where;
+    return status == 0 ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
+}
+
+int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000ull) limit_ns = 1000ull;
+    if (limit_ns > 5000000000ull) limit_ns = 5000000000ull;
+    int num_sms = 0;
+    int rc = current_device(&num_sms);
+    if (rc != TK_OK) return rc;
+    cudaError_t e = tk::launch_selftest_timeout(limit_ns, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
+
+const char *tk_attn_strerror(int code) {
+    switch (code) {
+        case TK_OK: return "success";
+        case TK_ERR_NULL_PTR: return "a required pointer is NULL";
+        case TK_ERR_BAD_SHAPE: return "invalid shape (B, H, N must be >= 1 and sizes must fit)";
+        case TK_ERR_UNSUPPORTED_D: return "unsupported head dimension (64 or 128)";
+        case TK_ERR_MISALIGNED: return "misaligned pointer (Q, K, V, O: 16 bytes; LSE: 4 bytes)";
+        case TK_ERR_BAD_SCALE: return "scale must be finite and > 0";
+        case TK_ERR_ALIAS: return "outputs overlap inputs or each other";
+        case TK_ERR_BAD_FLAG: return "causal must be 0 or 1";
+        case TK_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+        case TK_ERR_CUDA: return "a CUDA call or the kernel launch failed";
+        case TK_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case TK_ERR_NOT_DEVICE_MEMORY: return "a pointer is not device or managed memory";
+        default: return "unknown status code";
+    }
+}
+
+int tk_attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int tk_attn_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// tk_attn_internal.h -- types shared by the C-ABI layer and the kernel
+// translation unit.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <cstdint>
+
+namespace tk {
+
+// Everything one launch of the fused forward kernel needs.  Passed by value
+// as a __grid_constant__ kernel parameter (the tensor maps must stay in
+// parameter space for TMA).
+struct AttnParams {
+    CUtensorMap tmQ;  // 3-D {D, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK;
+    CUtensorMap tmV;
+    void *O;          // bf16 [B*H, N, D]
+    float *LSE;       // fp32 [B*H, N]
+    int N;            // sequence length
+    int BH;           // B * H
+    int causal;       // 0 / 1
+    int n_qtiles;     // ceil(N / 128)
+    int n_kvtiles;    // ceil(N / 128)
+    float scale;      // multiplier of Q K^T
+    float scale_log2e;  // scale * log2(e): the exp2-domain factor
+};
+
+// Launches the fused forward kernel for head dim D (64 or 128).
+cudaError_t launch_attn_fwd(int D, const AttnParams &p, int num_sms, cudaStream_t stream);
+
+// Launches the one-CTA bounded-wait self test.
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+// Synchronises `stream`, reads and clears the device status word.
+cudaError_t read_and_clear_status(cudaStream_t stream, uint32_t *status, uint32_t *detail);
+
+}  // namespace tk
