@@ -125,12 +125,19 @@ class ClockSampler:
     def __init__(self, gpu_index: int, interval_ms: int = 100):
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        gpu_id = str(gpu_index)
+        try:  # the UUID names the right GPU whatever CUDA_VISIBLE_DEVICES says
+            import torch
+            u = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", f"-lms={interval_ms}"],
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"--loop-ms={interval_ms}"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -237,7 +244,7 @@ def run_ours(args, w):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 or True else None
+    sampler = ClockSampler(local)
     if dist_mod:
         dist_mod.barrier()
     torch.cuda.synchronize(dev)
@@ -261,18 +268,23 @@ def run_ours(args, w):
     value = w.flops * ws / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API with pinned host buffers
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    e2e_steps = max(3, min(20, args.steps // 50))
-    tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)  # warm
-    if dist_mod:
-        dist_mod.barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_s = max_over_ranks(e2e_s, dist_mod, dev)
-    h2d = 3 * q.numel() * q.element_size()
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        e2e_steps = max(3, min(20, args.steps // 50))
+        tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)  # warm
+        if dist_mod:
+            dist_mod.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e_s = max_over_ranks(e2e_s, dist_mod, dev)
+        h2d = 3 * q.numel() * q.element_size()
+        d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+        e2e = {"value": round(w.flops * ws / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3, 3), "steps": e2e_steps}
 
     if rank != 0:
         if dist_mod:
@@ -301,9 +313,7 @@ def run_ours(args, w):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_label, "traffic": traffic_for(w.name),
                      "kernel": f"attn_fwd_kernel<{w.D}>", "kernel_ms": round(kernel_ms, 5)},
-        "e2e": {"value": round(w.flops * ws / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3, 3)},
+        "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
@@ -385,6 +395,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--shape", type=str, default=None,
+                    help="B,H,N,D,causal: a custom N(0,1) workload instead of a named one")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -395,10 +408,13 @@ def main(argv=None):
     if ws != args.gpus and ws != 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
 
-    from tiled_attention_tk_gb300.inputs import WORKLOADS
-    idxs = [1, 2, 3, 4, 5] if args.all else [args.workload]
-    for idx in idxs:
-        w = WORKLOADS[idx]
+    from tiled_attention_tk_gb300.inputs import WORKLOADS, Workload
+    if args.shape:
+        B, H, N, D, causal = (int(x) for x in args.shape.split(","))
+        todo = [Workload(0, B, H, N, D, bool(causal), "normal")]
+    else:
+        todo = [WORKLOADS[i] for i in ([1, 2, 3, 4, 5] if args.all else [args.workload])]
+    for w in todo:
         line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
         if line is not None and rank == 0:
             print(json.dumps(line), flush=True)

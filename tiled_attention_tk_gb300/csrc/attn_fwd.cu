@@ -11,20 +11,28 @@
 // ragged key tail from alanwu.xyz/posts/thunderkittens (attention inner loop).
 //
 // The Hopper design on that page (three consumer warpgroups of 64-row Q
-// tiles, register accumulators, wgmma, two pipeline stages) is replaced by
-// the Blackwell one:
-//   warp 4      TMA producer: Q once, then K/V tiles through a STAGES-deep
-//               shared-memory ring (full/empty mbarriers).
-//   warp 5      MMA issuer: S = Q K^T (tcgen05.mma, smem x smem -> TMEM fp32)
-//               into one of two S buffers, O += P V (P read from TMEM, V from
-//               smem) into the O accumulator in TMEM.  Also owns TMEM.
-//   warps 0-3   softmax + correction + epilogue: thread t owns query row t of
-//               the 128-row tile (TMEM lane t); reads its S row with
-//               tcgen05.ld, masks, updates m and l, writes P as bf16 over the
-//               S columns, rescales its O row in TMEM, and at the end writes
-//               O / l (bf16) and LSE.
-// One CTA handles one 128-row Q tile of one head; CTAs are ordered heaviest
-// (causal) tile first.
+// tiles, register accumulators, wgmma, two pipeline stages, one CTA per Q
+// block) is replaced by a Blackwell one.  A persistent CTA per SM walks a
+// list of work units; a unit is one head and a pair of consecutive 128-row Q
+// tiles, Q0 and Q1.  Roles:
+//   warp 9      TMA producer: Q0 and Q1 once per unit, then K_j and V_j into
+//               separate slots of a shared-memory ring (full/empty mbarriers).
+//   warp 8      MMA issuer (one thread): S_i = Q_i K_j^T (tcgen05.mma, smem x
+//               smem -> TMEM fp32) and O_i += P_i V_j (P_i read from TMEM, V
+//               from smem) into O_i in TMEM, ordered S0, S1, PV0, S0', PV1,
+//               S1', ... so the tensor core works on one Q tile while the
+//               other tile's softmax runs.  Also owns TMEM.
+//   warps 0-3   softmax warpgroup of Q0, warps 4-7 of Q1: thread t owns query
+//               row t of its tile (TMEM lane t); reads its S row with
+//               tcgen05.ld, masks the last key tile, takes the row max,
+//               writes P = exp2(c*s - c*m_ref) as bf16 over the S columns,
+//               updates l, rescales its O row only when the row max has grown
+//               by more than 2^8 since the reference max was set (lazy
+//               rescale; O and l always share the same reference, so the
+//               result is exact), and at the end of the unit writes O / l
+//               (bf16) and LSE while the MMA warp already starts the next
+//               unit.
+// TMEM (512 columns): S0/P0, S1/P1 (128 each), O0, O1 (D each).
 //
 // Every wait on an mbarrier is bounded in time: if it gives up, the CTA
 // records TK_ERR_DEVICE_TIMEOUT in a device status word, lets in-flight
@@ -78,41 +86,72 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 
 // ------------------------------------------------------------------ layout
 
-constexpr int BM = 128;          // query rows per tile (one TMEM lane each)
-constexpr int BN = 128;          // keys per tile
-constexpr int NUM_THREADS = 192; // 4 softmax warps + TMA warp + MMA warp
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
+constexpr int BM = 128;            // query rows per Q tile (one TMEM lane each)
+constexpr int BN = 128;            // keys per key tile
+constexpr int NUM_THREADS = 320;   // 2 softmax warpgroups + MMA warp + TMA warp
+constexpr int WARP_MMA = 8;
+constexpr int WARP_TMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_S0 = 0;    // S / P buffer 0: 128 fp32 columns
-constexpr uint32_t TMEM_S1 = 128;  // S / P buffer 1
-constexpr uint32_t TMEM_O = 256;   // O accumulator: D fp32 columns
+// Lazy rescale: the reference max of a row is moved (and O, l rescaled) only
+// when the new row max exceeds it by more than this many powers of two.
+constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct Layout {
     static constexpr int KATOMS = D / 64;                 // 128-byte swizzle atoms along D
-    static constexpr int STAGES = 2;                      // K/V ring depth
     static constexpr uint32_t BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
     static constexpr uint32_t TILE_BYTES = BM * D * 2;    // one 128-row tile
-    static constexpr uint32_t Q_OFF = 0;
-    static constexpr uint32_t KV_OFF = TILE_BYTES;        // stage s: K, then V
-    static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = KV_OFF + STAGES * STAGE_BYTES;
+    static constexpr int NSLOTS = D == 128 ? 4 : 8;       // K/V ring slots (K_j, V_j alternate)
+    static constexpr uint32_t Q_OFF = 0;                  // Q tile i at Q_OFF + i * TILE_BYTES
+    static constexpr uint32_t SLOT_OFF = 2 * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = SLOT_OFF + NSLOTS * TILE_BYTES;
     // barriers
     static constexpr int B_QFULL = 0;
-    static constexpr int B_KVFULL = 1;                    // + stage
-    static constexpr int B_KVEMPTY = B_KVFULL + STAGES;   // + stage
-    static constexpr int B_SFULL = B_KVEMPTY + STAGES;    // + buffer (2)
-    static constexpr int B_PFULL = B_SFULL + 2;
-    static constexpr int B_ODONE = B_PFULL + 1;
-    static constexpr int B_MMADONE = B_ODONE + 1;
+    static constexpr int B_QEMPTY = 1;
+    static constexpr int B_SLOTFULL = 2;                  // + slot
+    static constexpr int B_SLOTEMPTY = B_SLOTFULL + NSLOTS;
+    static constexpr int B_SFULL = B_SLOTEMPTY + NSLOTS;  // + Q tile (2)
+    static constexpr int B_PFULL = B_SFULL + 2;           // + Q tile
+    static constexpr int B_PVDONE = B_PFULL + 2;          // + Q tile
+    static constexpr int B_OFREE = B_PVDONE + 2;          // + Q tile
+    static constexpr int B_MMADONE = B_OFREE + 2;
     static constexpr int NUM_BARS = B_MMADONE + 1;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
-    // +1024: slack for 1024-byte alignment.  At least 116 KB so that only one
-    // CTA is resident per SM: each CTA allocates all 512 TMEM columns.
-    static constexpr uint32_t SMEM_ALLOC =
-        SMEM_USED + 1024 > 116u * 1024u ? SMEM_USED + 1024 : 116u * 1024u;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+    static_assert(SMEM_ALLOC > 116u * 1024u, "one CTA per SM: each CTA holds all 512 TMEM columns");
+    static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+    // TMEM columns: S / P of Q tile i, O of Q tile i
+    __host__ __device__ static constexpr uint32_t tmem_s(int i) { return static_cast<uint32_t>(i) * 128u; }
+    __host__ __device__ static constexpr uint32_t tmem_o(int i) { return 256u + static_cast<uint32_t>(i) * D; }
 };
+
+// Work unit = (head bh, pair of consecutive 128-row Q tiles).  Units are
+// handed to the persistent CTAs round by round; odd rounds run in reverse
+// CTA order (snake) so that no CTA always gets the heaviest unit of a round.
+struct Unit {
+    int bh;
+    int pair;
+};
+
+__device__ __forceinline__ Unit unit_at(int idx, const AttnParams &p) {
+    if (p.causal) {
+        // Heaviest first: the last pair of every head, then the one before...
+        const int r = idx / p.BH;
+        return {idx % p.BH, p.n_pairs - 1 - r};
+    }
+    // Equal cost: the pairs of one head are adjacent, so CTAs running at
+    // the same time share that head's K/V in L2.
+    return {idx / p.n_pairs, idx % p.n_pairs};
+}
+
+__device__ __forceinline__ int unit_index(int round, int cta, int grid) {
+    return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+// Key tiles Q tile `qt` must visit.
+__device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
+    return p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
+}
 
 // ------------------------------------------------------------------ kernel
 
@@ -130,13 +169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-
-    // Work unit: heaviest query tiles first (matters under the causal mask),
-    // consecutive CTAs on different heads.
-    const int rank = blockIdx.x / p.BH;
-    const int bh = blockIdx.x % p.BH;
-    const int qt = p.n_qtiles - 1 - rank;
-    const int n_kv = p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
+    const int total_units = p.BH * p.n_pairs;
+    const int grid = gridDim.x;
+    const int rounds = (total_units + grid - 1) / grid;
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -144,14 +179,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
     if (threadIdx.x == 0) {
         mbar_init(bar(L::B_QFULL), 1);
-        for (int s = 0; s < L::STAGES; ++s) {
-            mbar_init(bar(L::B_KVFULL + s), 1);
-            mbar_init(bar(L::B_KVEMPTY + s), 1);
+        mbar_init(bar(L::B_QEMPTY), 1);
+        for (int s = 0; s < L::NSLOTS; ++s) {
+            mbar_init(bar(L::B_SLOTFULL + s), 1);
+            mbar_init(bar(L::B_SLOTEMPTY + s), 1);
         }
-        mbar_init(bar(L::B_SFULL + 0), 1);
-        mbar_init(bar(L::B_SFULL + 1), 1);
-        mbar_init(bar(L::B_PFULL), BM);
-        mbar_init(bar(L::B_ODONE), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::B_SFULL + i), 1);
+            mbar_init(bar(L::B_PFULL + i), BM);
+            mbar_init(bar(L::B_PVDONE + i), 1);
+            mbar_init(bar(L::B_OFREE + i), BM);
+        }
         mbar_init(bar(L::B_MMADONE), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -167,34 +205,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             tma_prefetch_desc(&p.tmQ);
             tma_prefetch_desc(&p.tmK);
             tma_prefetch_desc(&p.tmV);
-            mbar_arrive_expect_tx(bar(L::B_QFULL), L::TILE_BYTES);
-            for (int c = 0; c < L::KATOMS; ++c)
-                tma_load_3d(sbase + L::Q_OFF + c * L::BOX_BYTES, &p.tmQ, bar(L::B_QFULL), c * 64,
-                            qt * BM, bh);
-            int issued = 0;
+            uint32_t loads = 0;  // K/V slot loads issued (K_j and V_j alternate)
+            int k_unit = 0;
             bool ok = true;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % L::STAGES;
-                if (j >= L::STAGES &&
-                    !wait_bounded(bar(L::B_KVEMPTY + s), ((j / L::STAGES) - 1) & 1, abort_flag,
-                                  (ROLE_PRODUCER << 24) | (L::B_KVEMPTY << 16) | j)) {
+            for (int r = 0; ok && r < rounds; ++r) {
+                const int idx = unit_index(r, blockIdx.x, grid);
+                if (idx >= total_units) continue;
+                const Unit u = unit_at(idx, p);
+                if (k_unit > 0 && !wait_bounded(bar(L::B_QEMPTY), (k_unit - 1) & 1, abort_flag,
+                                                (ROLE_PRODUCER << 24) | (L::B_QEMPTY << 16) | k_unit)) {
                     ok = false;
                     break;
                 }
-                const uint32_t kdst = sbase + L::KV_OFF + s * L::STAGE_BYTES;
-                mbar_arrive_expect_tx(bar(L::B_KVFULL + s), 2 * L::TILE_BYTES);
-                for (int c = 0; c < L::KATOMS; ++c)
-                    tma_load_3d(kdst + c * L::BOX_BYTES, &p.tmK, bar(L::B_KVFULL + s), c * 64, j * BN, bh);
-                for (int c = 0; c < L::KATOMS; ++c)
-                    tma_load_3d(kdst + L::TILE_BYTES + c * L::BOX_BYTES, &p.tmV, bar(L::B_KVFULL + s),
-                                c * 64, j * BN, bh);
-                ++issued;
+                mbar_arrive_expect_tx(bar(L::B_QFULL), 2 * L::TILE_BYTES);
+                for (int i = 0; i < 2; ++i)
+                    for (int c = 0; c < L::KATOMS; ++c)
+                        tma_load_3d(sbase + L::Q_OFF + i * L::TILE_BYTES + c * L::BOX_BYTES, &p.tmQ,
+                                    bar(L::B_QFULL), c * 64, (2 * u.pair + i) * BM, u.bh);
+                const int n_kv = kv_tiles(2 * u.pair + 1, p);
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int s = loads % L::NSLOTS;
+                        if (loads >= static_cast<uint32_t>(L::NSLOTS) &&
+                            !wait_bounded(bar(L::B_SLOTEMPTY + s), ((loads / L::NSLOTS) - 1) & 1, abort_flag,
+                                          (ROLE_PRODUCER << 24) | ((L::B_SLOTEMPTY + s) << 16) | (j & 0xFFFF))) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = sbase + L::SLOT_OFF + s * L::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(L::B_SLOTFULL + s), L::TILE_BYTES);
+                        for (int c = 0; c < L::KATOMS; ++c)
+                            tma_load_3d(dst + c * L::BOX_BYTES, kv ? &p.tmV : &p.tmK, bar(L::B_SLOTFULL + s),
+                                        c * 64, j * BN, u.bh);
+                        ++loads;
+                    }
+                }
+                ++k_unit;
             }
             if (!ok) {
-                // Let the copies already in flight land before the CTA exits.
-                for (int j = issued - L::STAGES < 0 ? 0 : issued - L::STAGES; j < issued; ++j) {
+                // Let the copies in flight land before the CTA exits.
+                const uint32_t first = loads > static_cast<uint32_t>(L::NSLOTS) ? loads - L::NSLOTS : 0;
+                for (uint32_t n = first; n < loads; ++n) {
                     const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bar(L::B_KVFULL + j % L::STAGES), (j / L::STAGES) & 1) &&
+                    while (!mbar_try_wait(bar(L::B_SLOTFULL + n % L::NSLOTS), (n / L::NSLOTS) & 1) &&
                            global_timer_ns() - t0 < kDrainLimitNs) {
                     }
                 }
@@ -206,160 +259,215 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);  // K-major Q and K
             constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 0, 1);   // P from TMEM, V MN-major
-            bool ok = wait_bounded(bar(L::B_QFULL), 0, abort_flag, (ROLE_MMA << 24) | (L::B_QFULL << 16));
+            uint32_t taken = 0;            // K/V slots consumed, in load order
+            uint32_t p_seen[2] = {0, 0};   // P hand-offs consumed per Q tile
+            bool ok = true;
+            int k_unit = 0;
 
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % L::STAGES;
-                if (!wait_bounded(bar(L::B_KVFULL + s), (j / L::STAGES) & 1, abort_flag,
-                                  (ROLE_MMA << 24) | (L::B_KVFULL << 16) | j))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t kbase = sbase + L::KV_OFF + s * L::STAGE_BYTES;
-                const uint32_t dcol = tmem + ((j & 1) ? TMEM_S1 : TMEM_S0);
+            auto take_slot = [&](uint32_t &slot) -> bool {
+                slot = taken % L::NSLOTS;
+                const bool r = wait_bounded(bar(L::B_SLOTFULL + slot), (taken / L::NSLOTS) & 1, abort_flag,
+                                            (ROLE_MMA << 24) | ((L::B_SLOTFULL + slot) << 16) | (taken & 0xFFFF));
+                ++taken;
+                return r;
+            };
+            auto issue_s = [&](int i, uint32_t kslot) {
+                const uint32_t kbase = sbase + L::SLOT_OFF + kslot * L::TILE_BYTES;
+                const uint32_t qbase = sbase + L::Q_OFF + i * L::TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k / 4) * L::BOX_BYTES + (k % 4) * 32;
-                    umma_ss(dcol, smem_desc_sw128(sbase + L::Q_OFF + off, 16, 1024),
+                    umma_ss(tmem + L::tmem_s(i), smem_desc_sw128(qbase + off, 16, 1024),
                             smem_desc_sw128(kbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(L::B_SFULL + (j & 1)));
-                return true;
+                umma_commit(bar(L::B_SFULL + i));
             };
-
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    // S buffer (j+1)&1 last held P_{j-1}: PV_{j-1} must be done.
-                    if (j >= 1 && !wait_bounded(bar(L::B_ODONE), (j - 1) & 1, abort_flag,
-                                                (ROLE_MMA << 24) | (L::B_ODONE << 16) | j)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!issue_s(j + 1)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!wait_bounded(bar(L::B_PFULL), j & 1, abort_flag,
-                                  (ROLE_MMA << 24) | (L::B_PFULL << 16) | j)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const int s = j % L::STAGES;
-                const uint32_t vbase = sbase + L::KV_OFF + s * L::STAGE_BYTES + L::TILE_BYTES;
-                const uint32_t pcol = tmem + ((j & 1) ? TMEM_S1 : TMEM_S0);
+            auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
+                const uint32_t vbase = sbase + L::SLOT_OFF + vslot * L::TILE_BYTES;
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     // 16 keys per step: P columns advance by 8 (two bf16 per
                     // 32-bit column), V rows by 16 * 128 bytes.
-                    umma_ts(tmem + TMEM_O, pcol + k * 8,
+                    umma_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + k * 8,
                             smem_desc_sw128(vbase + k * 2048, L::BOX_BYTES, 1024), IDESC_O,
-                            (j > 0 || k > 0) ? 1u : 0u);
+                            (accumulate || k > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(L::B_KVEMPTY + s));
-                umma_commit(bar(L::B_ODONE));
+                umma_commit(bar(L::B_PVDONE + i));
+            };
+            auto wait_p = [&](int i, int j) -> bool {
+                const bool r = wait_bounded(bar(L::B_PFULL + i), p_seen[i] & 1, abort_flag,
+                                            (ROLE_MMA << 24) | ((L::B_PFULL + i) << 16) | (j & 0xFFFF));
+                ++p_seen[i];
+                return r;
+            };
+
+            for (int r = 0; ok && r < rounds; ++r) {
+                const int idx = unit_index(r, blockIdx.x, grid);
+                if (idx >= total_units) continue;
+                const Unit u = unit_at(idx, p);
+                const int n0 = kv_tiles(2 * u.pair, p);
+                const int n1 = kv_tiles(2 * u.pair + 1, p);  // n1 >= n0 >= 1
+                uint32_t ks = 0, vs = 0;
+                if (!(ok = wait_bounded(bar(L::B_QFULL), k_unit & 1, abort_flag,
+                                        (ROLE_MMA << 24) | (L::B_QFULL << 16) | k_unit)))
+                    break;
+                if (!(ok = take_slot(ks))) break;
+                tc_fence_after_sync();
+                issue_s(0, ks);
+                issue_s(1, ks);
+                umma_commit(bar(L::B_SLOTEMPTY + ks));
+                // Q is free once the unit's last S MMA has completed, so the
+                // next unit's Q load overlaps this unit's last P V products.
+                if (n1 == 1) umma_commit(bar(L::B_QEMPTY));
+                for (int j = 0; j < n1; ++j) {
+                    const bool has_next = j + 1 < n1;
+                    if (!(ok = take_slot(vs))) break;  // V_j
+                    if (j < n0) {
+                        if (!(ok = wait_p(0, j))) break;
+                        if (j == 0 && k_unit > 0 &&
+                            !(ok = wait_bounded(bar(L::B_OFREE + 0), (k_unit - 1) & 1, abort_flag,
+                                                (ROLE_MMA << 24) | (L::B_OFREE << 16) | k_unit)))
+                            break;
+                        tc_fence_after_sync();
+                        issue_pv(0, vs, j > 0);
+                    }
+                    if (has_next) {
+                        if (!(ok = take_slot(ks))) break;  // K_{j+1}
+                        tc_fence_after_sync();
+                        if (j + 1 < n0) issue_s(0, ks);
+                    }
+                    if (!(ok = wait_p(1, j))) break;
+                    if (j == 0 && k_unit > 0 &&
+                        !(ok = wait_bounded(bar(L::B_OFREE + 1), (k_unit - 1) & 1, abort_flag,
+                                            (ROLE_MMA << 24) | ((L::B_OFREE + 1) << 16) | k_unit)))
+                        break;
+                    tc_fence_after_sync();
+                    issue_pv(1, vs, j > 0);
+                    umma_commit(bar(L::B_SLOTEMPTY + vs));
+                    if (has_next) {
+                        issue_s(1, ks);
+                        umma_commit(bar(L::B_SLOTEMPTY + ks));
+                        if (j + 2 == n1) umma_commit(bar(L::B_QEMPTY));
+                    }
+                }
+                if (!ok) break;
+                ++k_unit;
             }
             // Every MMA issued so far has completed before TMEM is released.
             umma_commit(bar(L::B_MMADONE));
-            {
-                const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
-                       global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
-                }
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
+                   global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ softmax / correction / epilogue
-        const int t = threadIdx.x;  // row within the tile == TMEM lane
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int row = qt * BM + t;
+        const int tile = warp / 4;                 // which Q tile of the unit this warpgroup owns
+        const int t = threadIdx.x % 128;           // row within the tile == TMEM lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+        const uint32_t s_addr = lane_base + L::tmem_s(tile);
+        const uint32_t o_addr = lane_base + L::tmem_o(tile);
         const float c = p.scale_log2e;
-        float m = -INFINITY;  // running max of raw scores
-        float l = 0.0f;       // running sum of exp2(c*(s - m))
+        uint32_t s_seen = 0;    // S hand-offs consumed
+        uint32_t pv_base = 0;   // PV MMAs of this Q tile in earlier units
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const uint32_t sbuf = lane_base + ((j & 1) ? TMEM_S1 : TMEM_S0);
-            if (!wait_bounded(bar(L::B_SFULL + (j & 1)), (j >> 1) & 1, abort_flag,
-                              (ROLE_SOFTMAX << 24) | (L::B_SFULL << 16) | j)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            float s[BN];
-#pragma unroll
-            for (int q = 0; q < BN / 32; ++q) {
-                uint32_t r[32];
-                tmem_ld32(sbuf + q * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(r[i]);
-            }
-            if (j == n_kv - 1) {
-                // Last key tile: the ragged tail (keys >= N) and, under the
-                // causal mask, the diagonal (keys > row) take -inf.
-                const int limit = p.causal ? min(row + 1, p.N) : p.N;
-                const int kmax = limit - j * BN;
-#pragma unroll
-                for (int i = 0; i < BN; ++i) s[i] = (i < kmax) ? s[i] : -INFINITY;
-            }
-            float mx = m;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) mx = fmaxf(mx, s[i]);
-            const float ms = (mx == -INFINITY) ? 0.0f : mx * c;
-            const float alpha = ex2(m * c - ms);
-            float sum = 0.0f;
-#pragma unroll
-            for (int q = 0; q < BN / 32; ++q) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[q * 32 + 2 * i], c, -ms));
-                    const float p1 = ex2(fmaf(s[q * 32 + 2 * i + 1], c, -ms));
-                    sum += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(sbuf + q * 16, pk);  // P (bf16) over the first 64 S columns
-            }
-            l = l * alpha + sum;
-            m = mx;
-            if (j > 0) {
-                // O holds PV_0..PV_{j-1}; it must be complete before rescaling.
-                if (!wait_bounded(bar(L::B_ODONE), (j - 1) & 1, abort_flag,
-                                  (ROLE_SOFTMAX << 24) | (L::B_ODONE << 16) | j)) {
-                    ok = false;
+        for (int r = 0; ok && r < rounds; ++r) {
+            const int idx = unit_index(r, blockIdx.x, grid);
+            if (idx >= total_units) continue;
+            const Unit u = unit_at(idx, p);
+            const int qt = 2 * u.pair + tile;
+            const int row = qt * BM + t;
+            const int n_kv = kv_tiles(qt, p);
+            float m_ref = -INFINITY;  // reference max of raw scores (lazy)
+            float l = 0.0f;           // sum of exp2(c * (s - m_ref))
+            for (int j = 0; j < n_kv; ++j) {
+                if (!(ok = wait_bounded(bar(L::B_SFULL + tile), s_seen & 1, abort_flag,
+                                        (ROLE_SOFTMAX << 24) | ((L::B_SFULL + tile) << 16) | (j & 0xFFFF))))
                     break;
-                }
+                ++s_seen;
                 tc_fence_after_sync();
+                float s[BN];
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + TMEM_O + q * 32, r);
+                for (int q = 0; q < BN / 32; ++q) {
+                    uint32_t rr[32];
+                    tmem_ld32(s_addr + q * 32, rr);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(lane_base + TMEM_O + q * 32, r);
+                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(rr[i]);
                 }
+                if (j == n_kv - 1) {
+                    // Last key tile of this Q tile: the ragged tail (keys >= N)
+                    // and, under the causal mask, keys past the row take -inf.
+                    const int limit = p.causal ? min(row + 1, p.N) : p.N;
+                    const int kmax = limit - j * BN;
+#pragma unroll
+                    for (int i = 0; i < BN; ++i) s[i] = (i < kmax) ? s[i] : -INFINITY;
+                }
+                // row max, as a tree
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+                for (int i = 8; i < BN; ++i) mx8[i % 8] = fmaxf(mx8[i % 8], s[i]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const bool need = (mx - m_ref) * c > kRescaleLog2;  // true when m_ref = -inf
+                const float new_ref = need ? mx : m_ref;
+                const float alpha = need ? ex2((m_ref - mx) * c) : 1.0f;
+                const float neg = (new_ref == -INFINITY) ? 0.0f : -new_ref * c;
+                float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int q = 0; q < BN / 32; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(s[q * 32 + 2 * i], c, neg));
+                        const float p1 = ex2(fmaf(s[q * 32 + 2 * i + 1], c, neg));
+                        sum4[i % 4] += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + q * 16, pk);  // P (bf16) over the first 64 S columns
+                }
+                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                m_ref = new_ref;
+                if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
+                    // O holds PV_0..PV_{j-1} of this tile; it must be complete.
+                    if (!(ok = wait_bounded(bar(L::B_PVDONE + tile), (pv_base + j - 1) & 1, abort_flag,
+                                            (ROLE_SOFTMAX << 24) | ((L::B_PVDONE + tile) << 16) | (j & 0xFFFF))))
+                        break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t rr[32];
+                        tmem_ld32(o_addr + q * 32, rr);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        tmem_st32(o_addr + q * 32, rr);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::B_PFULL + tile));
             }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(bar(L::B_PFULL));
-        }
-        if (ok && wait_bounded(bar(L::B_ODONE), (n_kv - 1) & 1, abort_flag,
-                               (ROLE_SOFTMAX << 24) | (L::B_ODONE << 16) | 0xFFFF)) {
+            if (!ok) break;
+            // ---- epilogue: O / l in bf16, LSE in fp32
+            if (!(ok = wait_bounded(bar(L::B_PVDONE + tile), (pv_base + n_kv - 1) & 1, abort_flag,
+                                    (ROLE_SOFTMAX << 24) | ((L::B_PVDONE + tile) << 16) | 0xFFFF)))
+                break;
+            pv_base += n_kv;
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
             const bool store = row < p.N;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) +
-                                  (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+                                  (static_cast<size_t>(u.bh) * p.N + (store ? row : 0)) * D;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + TMEM_O + q * 32, r);
+                uint32_t rr[32];
+                tmem_ld32(o_addr + q * 32, rr);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
-                                        __uint_as_float(r[2 * i + 1]) * inv_l);
+                    pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
                 if (store) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
 #pragma unroll
@@ -367,7 +475,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                         dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if (store) p.LSE[static_cast<size_t>(bh) * p.N + row] = m * p.scale + logf(l);
+            if (store) p.LSE[static_cast<size_t>(u.bh) * p.N + row] = m_ref * p.scale + logf(l);
+            tc_fence_before_sync();
+            mbar_arrive(bar(L::B_OFREE + tile));  // O of this tile may be overwritten
         }
     }
 
@@ -400,7 +510,7 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 // ------------------------------------------------------------------ host side
 
 template <int D>
-static cudaError_t launch_d(const AttnParams &p, cudaStream_t stream) {
+static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t stream) {
     using L = Layout<D>;
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -412,7 +522,8 @@ static cudaError_t launch_d(const AttnParams &p, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
         configured_device = dev;
     }
-    const long long blocks = static_cast<long long>(p.n_qtiles) * p.BH;
+    const long long units = static_cast<long long>(p.n_pairs) * p.BH;
+    const long long blocks = units < num_sms ? units : num_sms;  // persistent: <= one CTA per SM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -423,9 +534,10 @@ static cudaError_t launch_d(const AttnParams &p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, p);
 }
 
-cudaError_t launch_attn_fwd(int D, const AttnParams &p, int /*num_sms*/, cudaStream_t stream) {
-    if (D == 64) return launch_d<64>(p, stream);
-    if (D == 128) return launch_d<128>(p, stream);
+cudaError_t launch_attn_fwd(int D, const AttnParams &p, int num_sms, cudaStream_t stream) {
+    if (num_sms < 1) return cudaErrorInvalidValue;
+    if (D == 64) return launch_d<64>(p, num_sms, stream);
+    if (D == 128) return launch_d<128>(p, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -166,6 +166,7 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
     p.causal = causal;
     p.n_qtiles = static_cast<int>(n_tiles);
     p.n_kvtiles = static_cast<int>(n_tiles);
+    p.n_pairs = static_cast<int>((n_tiles + 1) / 2);
     p.scale = scale;
     p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 

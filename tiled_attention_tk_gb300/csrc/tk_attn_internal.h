@@ -22,6 +22,7 @@ struct AttnParams {
     int causal;       // 0 / 1
     int n_qtiles;     // ceil(N / 128)
     int n_kvtiles;    // ceil(N / 128)
+    int n_pairs;      // ceil(n_qtiles / 2): work units per head
     float scale;      // multiplier of Q K^T
     float scale_log2e;  // scale * log2(e): the exp2-domain factor
 };
