@@ -102,9 +102,13 @@ struct Layout {
     static constexpr uint32_t BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
     static constexpr uint32_t TILE_BYTES = BM * D * 2;    // one 128-row tile
     static constexpr int NSLOTS = D == 128 ? 4 : 8;       // K/V ring slots (K_j, V_j alternate)
+    static_assert(D % 64 == 0, "head dim in whole 128-byte swizzle atoms");
     static constexpr uint32_t Q_OFF = 0;                  // Q tile i at Q_OFF + i * TILE_BYTES
     static constexpr uint32_t SLOT_OFF = 2 * TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = SLOT_OFF + NSLOTS * TILE_BYTES;
+    // O staging for the TMA store: one 128-row x 64-column box per softmax
+    // warpgroup (the epilogue writes D/64 boxes through it one after another).
+    static constexpr uint32_t STAGE_OFF = SLOT_OFF + NSLOTS * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = STAGE_OFF + 2 * BOX_BYTES;
     // barriers
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
@@ -114,7 +118,8 @@ struct Layout {
     static constexpr int B_PFULL = B_SFULL + 2;           // + Q tile
     static constexpr int B_PVDONE = B_PFULL + 2;          // + Q tile
     static constexpr int B_OFREE = B_PVDONE + 2;          // + Q tile
-    static constexpr int B_MMADONE = B_OFREE + 2;
+    static constexpr int B_WGSYNC = B_OFREE + 2;          // + Q tile: warpgroup-internal sync
+    static constexpr int B_MMADONE = B_WGSYNC + 2;
     static constexpr int NUM_BARS = B_MMADONE + 1;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             mbar_init(bar(L::B_PFULL + i), BM);
             mbar_init(bar(L::B_PVDONE + i), 1);
             mbar_init(bar(L::B_OFREE + i), BM);
+            mbar_init(bar(L::B_WGSYNC + i), BM);
         }
         mbar_init(bar(L::B_MMADONE), 1);
         *abort_flag = 0;
@@ -212,34 +218,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 const int idx = unit_index(r, blockIdx.x, grid);
                 if (idx >= total_units) continue;
                 const Unit u = unit_at(idx, p);
-                if (k_unit > 0 && !wait_bounded(bar(L::B_QEMPTY), (k_unit - 1) & 1, abort_flag,
-                                                (ROLE_PRODUCER << 24) | (L::B_QEMPTY << 16) | k_unit)) {
-                    ok = false;
+                const int n_kv = kv_tiles(2 * u.pair + 1, p);
+                auto load_kv = [&](int j, int kv) -> bool {
+                    const int s = loads % L::NSLOTS;
+                    if (loads >= static_cast<uint32_t>(L::NSLOTS) &&
+                        !wait_bounded(bar(L::B_SLOTEMPTY + s), ((loads / L::NSLOTS) - 1) & 1, abort_flag,
+                                      (ROLE_PRODUCER << 24) | ((L::B_SLOTEMPTY + s) << 16) | (j & 0xFFFF)))
+                        return false;
+                    const uint32_t dst = sbase + L::SLOT_OFF + s * L::TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_SLOTFULL + s), L::TILE_BYTES);
+                    for (int c = 0; c < L::KATOMS; ++c)
+                        tma_load_3d(dst + c * L::BOX_BYTES, kv ? &p.tmV : &p.tmK, bar(L::B_SLOTFULL + s),
+                                    c * 64, j * BN, u.bh);
+                    ++loads;
+                    return true;
+                };
+                // K_0 and V_0 only need free ring slots: start them before
+                // waiting for the previous unit to release the Q buffers.
+                if (!(ok = load_kv(0, 0) && load_kv(0, 1))) break;
+                if (k_unit > 0 && !(ok = wait_bounded(bar(L::B_QEMPTY), (k_unit - 1) & 1, abort_flag,
+                                                      (ROLE_PRODUCER << 24) | (L::B_QEMPTY << 16) | k_unit)))
                     break;
-                }
                 mbar_arrive_expect_tx(bar(L::B_QFULL), 2 * L::TILE_BYTES);
                 for (int i = 0; i < 2; ++i)
                     for (int c = 0; c < L::KATOMS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + i * L::TILE_BYTES + c * L::BOX_BYTES, &p.tmQ,
                                     bar(L::B_QFULL), c * 64, (2 * u.pair + i) * BM, u.bh);
-                const int n_kv = kv_tiles(2 * u.pair + 1, p);
-                for (int j = 0; ok && j < n_kv; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const int s = loads % L::NSLOTS;
-                        if (loads >= static_cast<uint32_t>(L::NSLOTS) &&
-                            !wait_bounded(bar(L::B_SLOTEMPTY + s), ((loads / L::NSLOTS) - 1) & 1, abort_flag,
-                                          (ROLE_PRODUCER << 24) | ((L::B_SLOTEMPTY + s) << 16) | (j & 0xFFFF))) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t dst = sbase + L::SLOT_OFF + s * L::TILE_BYTES;
-                        mbar_arrive_expect_tx(bar(L::B_SLOTFULL + s), L::TILE_BYTES);
-                        for (int c = 0; c < L::KATOMS; ++c)
-                            tma_load_3d(dst + c * L::BOX_BYTES, kv ? &p.tmV : &p.tmK, bar(L::B_SLOTFULL + s),
-                                        c * 64, j * BN, u.bh);
-                        ++loads;
-                    }
-                }
+                for (int j = 1; ok && j < n_kv; ++j) ok = load_kv(j, 0) && load_kv(j, 1);
                 ++k_unit;
             }
             if (!ok) {
@@ -371,7 +376,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         const float c = p.scale_log2e;
         uint32_t s_seen = 0;    // S hand-offs consumed
         uint32_t pv_base = 0;   // PV MMAs of this Q tile in earlier units
+        uint32_t syncs = 0;     // warpgroup syncs done
         bool ok = true;
+        // Warpgroup-wide sync on an mbarrier: unlike a named barrier its wait
+        // is bounded, so an aborting CTA cannot hang here.
+        auto wg_sync = [&](int tl) -> bool {
+            mbar_arrive(bar(L::B_WGSYNC + tl));
+            const bool r = wait_bounded(bar(L::B_WGSYNC + tl), syncs & 1, abort_flag,
+                                        (ROLE_SOFTMAX << 24) | ((L::B_WGSYNC + tl) << 16) | (syncs & 0xFFFF));
+            ++syncs;
+            return r;
+        };
         for (int r = 0; ok && r < rounds; ++r) {
             const int idx = unit_index(r, blockIdx.x, grid);
             if (idx >= total_units) continue;
@@ -387,14 +402,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     break;
                 ++s_seen;
                 tc_fence_after_sync();
+                // The whole S row in one TMEM load (one round trip).
+                uint32_t sr[BN];
+                tmem_ld128(s_addr, sr);
                 float s[BN];
 #pragma unroll
-                for (int q = 0; q < BN / 32; ++q) {
-                    uint32_t rr[32];
-                    tmem_ld32(s_addr + q * 32, rr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(rr[i]);
-                }
+                for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
                 if (j == n_kv - 1) {
                     // Last key tile of this Q tile: the ragged tail (keys >= N)
                     // and, under the causal mask, keys past the row take -inf.
@@ -403,32 +416,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
 #pragma unroll
                     for (int i = 0; i < BN; ++i) s[i] = (i < kmax) ? s[i] : -INFINITY;
                 }
-                // row max, as a tree
+                // Row max: eight independent chains of three-input maxima.
                 float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+                for (int k = 0; k < 8; ++k) {
+                    float a = s[k];
 #pragma unroll
-                for (int i = 8; i < BN; ++i) mx8[i % 8] = fmaxf(mx8[i % 8], s[i]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                    for (int t = 1; t < 15; t += 2) a = fmax3(a, s[k + 8 * t], s[k + 8 * (t + 1)]);
+                    mx8[k] = fmaxf(a, s[k + 120]);
+                }
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmax3(mx8[6], mx8[7], m_ref));
                 const bool need = (mx - m_ref) * c > kRescaleLog2;  // true when m_ref = -inf
                 const float new_ref = need ? mx : m_ref;
                 const float alpha = need ? ex2((m_ref - mx) * c) : 1.0f;
                 const float neg = (new_ref == -INFINITY) ? 0.0f : -new_ref * c;
-                float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // P = exp2(c*s - c*m_ref): packed FMA for the argument, MUFU
+                // ex2, packed adds for the row sum, bf16x2 packing for TMEM.
+                const float2 c2 = make_float2(c, c);
+                const float2 n2 = make_float2(neg, neg);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int q = 0; q < BN / 32; ++q) {
-                    uint32_t pk[16];
+                for (int h = 0; h < 2; ++h) {  // two halves keep the register peak low
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(s[q * 32 + 2 * i], c, neg));
-                        const float p1 = ex2(fmaf(s[q * 32 + 2 * i + 1], c, neg));
-                        sum4[i % 4] += p0 + p1;
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = h * 64 + 2 * i;
+                        const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, n2);
+                        const float p0 = ex2(x.x);
+                        const float p1 = ex2(x.y);
+                        acc[i % 4] = __fadd2_rn(acc[i % 4], make_float2(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st16(s_addr + q * 16, pk);  // P (bf16) over the first 64 S columns
+                    tmem_st32(s_addr + h * 32, pk);  // P (bf16) over the first 64 S columns
                 }
-                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+                const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+                const float2 a = __fadd2_rn(a01, a23);
+                l = l * alpha + (a.x + a.y);
                 m_ref = new_ref;
                 if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
                     // O holds PV_0..PV_{j-1} of this tile; it must be complete.
@@ -457,28 +483,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             pv_base += n_kv;
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
-            const bool store = row < p.N;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) +
-                                  (static_cast<size_t>(u.bh) * p.N + (store ? row : 0)) * D;
+            // O / l as bf16 through shared memory to TMA stores, 64 columns
+            // (one 128-byte row of a TMA box) at a time: coalesced full-line
+            // writes, and rows past N are clipped by the tensor map.
+            uint8_t *stage = smem + L::STAGE_OFF + tile * L::BOX_BYTES;
+            const uint32_t stage_addr = sbase + L::STAGE_OFF + tile * L::BOX_BYTES;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t rr[32];
-                tmem_ld32(o_addr + q * 32, rr);
-                uint32_t pk[16];
+            for (int h = 0; h < L::KATOMS; ++h) {
+                uint32_t ob[32];
+                {
+                    uint32_t rr[64];
+                    tmem_ld64(o_addr + h * 64, rr);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 32);
+                    for (int i = 0; i < 32; ++i)
+                        ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                                            __uint_as_float(rr[2 * i + 1]) * inv_l);
+                }
+                if (h == L::KATOMS - 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(L::B_OFREE + tile));  // O of this tile may be overwritten
+                }
+                if (t == 0) tma_store_wait_read_all();  // the staging box is free again
+                if (!(ok = wg_sync(tile))) break;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(stage + t * 128 + ((c ^ (t & 7)) << 4)) =
+                        make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                fence_proxy_async_smem();
+                if (!(ok = wg_sync(tile))) break;
+                if (t == 0) {
+                    tma_store_3d(&p.tmO, stage_addr, h * 64, qt * BM, u.bh);
+                    tma_store_commit();
                 }
             }
-            if (store) p.LSE[static_cast<size_t>(u.bh) * p.N + row] = m_ref * p.scale + logf(l);
-            tc_fence_before_sync();
-            mbar_arrive(bar(L::B_OFREE + tile));  // O of this tile may be overwritten
+            if (row < p.N) p.LSE[static_cast<size_t>(u.bh) * p.N + row] = m_ref * p.scale + logf(l);
         }
+        if (t == 0) tma_store_wait_all();  // every store of this warpgroup has landed
     }
 
     tc_fence_before_sync();

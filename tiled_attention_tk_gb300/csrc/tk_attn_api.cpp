@@ -102,8 +102,9 @@ int check_device_memory(const void *p) {
     return TK_OK;
 }
 
-// 3-D view {D, N, B*H} of a contiguous [B,H,N,D] bf16 tensor, loaded as
-// 128-row x 64-column boxes with the 128-byte swizzle; rows past N read as 0.
+// 3-D view {D, N, B*H} of a contiguous [B,H,N,D] bf16 tensor, moved as
+// 128-row x 64-column boxes with the 128-byte swizzle; loads read rows past
+// N as 0, stores skip them.
 int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int64_t BH) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return fail_cuda(g_encode_err);
@@ -159,6 +160,7 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
     if ((rc = encode_qkv_map(&p.tmQ, Q, N, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmK, K, N, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmV, V, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmO, O, N, D, BH)) != TK_OK) return rc;
     p.O = O;
     p.LSE = LSE;
     p.N = static_cast<int>(N);

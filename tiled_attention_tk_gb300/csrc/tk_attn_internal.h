@@ -15,6 +15,7 @@ struct AttnParams {
     CUtensorMap tmQ;  // 3-D {D, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
     CUtensorMap tmK;
     CUtensorMap tmV;
+    CUtensorMap tmO;  // same view of O, for TMA stores
     void *O;          // bf16 [B*H, N, D]
     float *LSE;       // fp32 [B*H, N]
     int N;            // sequence length
