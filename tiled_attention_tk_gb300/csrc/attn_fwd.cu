@@ -93,8 +93,11 @@ constexpr int WARP_MMA = 8;
 constexpr int WARP_TMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 // Lazy rescale: the reference max of a row is moved (and O, l rescaled) only
-// when the new row max exceeds it by more than this many powers of two.
-constexpr float kRescaleLog2 = 8.0f;
+// when the new row max exceeds it by more than this many powers of two.  P
+// then stays below 2^24 (fine for bf16 P and fp32 l and O: the product of
+// N, 2^24 and max|V| stays far from the fp32 limit for any bf16 V below
+// 2^64), and O and l always share the reference, so O / l is exact.
+constexpr float kRescaleLog2 = 24.0f;
 
 template <int D>
 struct Layout {
@@ -158,6 +161,14 @@ __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
     return p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
 }
 
+// One arrival per warp: the warp's lanes first synchronise (ordering their
+// earlier writes, and after a tcgen05 fence their TMEM stores), then lane 0
+// arrives.  Barriers fed this way count 4 arrivals per warpgroup.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int D>
@@ -191,10 +202,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(L::B_SFULL + i), 1);
-            mbar_init(bar(L::B_PFULL + i), BM);
+            // hand-offs from a warpgroup: one arrival per warp (after __syncwarp)
+            mbar_init(bar(L::B_PFULL + i), 4);
             mbar_init(bar(L::B_PVDONE + i), 1);
-            mbar_init(bar(L::B_OFREE + i), BM);
-            mbar_init(bar(L::B_WGSYNC + i), BM);
+            mbar_init(bar(L::B_OFREE + i), 4);
+            mbar_init(bar(L::B_WGSYNC + i), 4);
         }
         mbar_init(bar(L::B_MMADONE), 1);
         *abort_flag = 0;
@@ -381,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         // Warpgroup-wide sync on an mbarrier: unlike a named barrier its wait
         // is bounded, so an aborting CTA cannot hang here.
         auto wg_sync = [&](int tl) -> bool {
-            mbar_arrive(bar(L::B_WGSYNC + tl));
+            warp_arrive(bar(L::B_WGSYNC + tl), lane);
             const bool r = wait_bounded(bar(L::B_WGSYNC + tl), syncs & 1, abort_flag,
                                         (ROLE_SOFTMAX << 24) | ((L::B_WGSYNC + tl) << 16) | (syncs & 0xFFFF));
             ++syncs;
@@ -473,7 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
                 tmem_st_wait();
                 tc_fence_before_sync();
-                mbar_arrive(bar(L::B_PFULL + tile));
+                warp_arrive(bar(L::B_PFULL + tile), lane);
             }
             if (!ok) break;
             // ---- epilogue: O / l in bf16, LSE in fp32
@@ -501,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
                 if (h == L::KATOMS - 1) {
                     tc_fence_before_sync();
-                    mbar_arrive(bar(L::B_OFREE + tile));  // O of this tile may be overwritten
+                    warp_arrive(bar(L::B_OFREE + tile), lane);  // O of this tile may be overwritten
                 }
                 if (t == 0) tma_store_wait_read_all();  // the staging box is free again
                 if (!(ok = wg_sync(tile))) break;
