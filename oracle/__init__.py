@@ -72,6 +72,9 @@ def _declare(lib) -> None:
     lib.tkor_attn_weights.argtypes = [P, P, i64, i64, ctypes.c_int,
                                       ctypes.c_double, P]
     lib.tkor_attn_weights.restype = ctypes.c_int
+    lib.tkor_attn_bwd.argtypes = [P, P, P, P, P, P, P, i64, i64, i64, i64,
+                                  ctypes.c_int, ctypes.c_double, ctypes.c_int]
+    lib.tkor_attn_bwd.restype = ctypes.c_int
     lib.tkor_last_threads.argtypes = []
     lib.tkor_last_threads.restype = ctypes.c_int
 
@@ -149,6 +152,28 @@ def attn_weights(q, k, causal: bool, scale: float) -> np.ndarray:
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return P
+
+
+def attn_bwd(q, k, v, do, causal: bool, scale: float, threads: int = 0, lib=None):
+    """Gradient of sum(O * dO) with respect to q, k, v for O = attention(q, k,
+    v).  All inputs bf16 [B,H,N,D].  Returns (dQ, dK, dV) float64 arrays.
+
+    Chain rule through the softmax, written out:  dV_j = sum_i p_ij dO_i;
+    dS_ij = p_ij (<dO_i, V_j> - sum_k p_ik <dO_i, V_k>);
+    dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_i dS_ij Q_i."""
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(do)
+    if qb.ndim != 4 or not (qb.shape == kb.shape == vb.shape == gb.shape):
+        raise ValueError("q, k, v, do must share one [B,H,N,D] shape")
+    B, H, N, D = qb.shape
+    dQ = np.empty((B, H, N, D), dtype=np.float64)
+    dK = np.empty((B, H, N, D), dtype=np.float64)
+    dV = np.empty((B, H, N, D), dtype=np.float64)
+    rc = (lib or _load()).tkor_attn_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), _ptr(dQ), _ptr(dK),
+                                        _ptr(dV), B, H, N, D, int(bool(causal)), float(scale),
+                                        int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return dQ, dK, dV
 
 
 def last_threads() -> int:

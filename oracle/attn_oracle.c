@@ -236,3 +236,153 @@ int tkor_attn_weights(const uint16_t *Qb, const uint16_t *Kb, int64_t N, int64_t
 
 /* Largest number of threads used by the last call. */
 int tkor_last_threads(void) { return g_last_threads; }
+
+/* ======================================================================== */
+/* Backward pass                                                             */
+/*
+ * The gradient of L = sum_{i,d} O[i,d] * dO[i,d] with respect to Q, K, V,
+ * where O is the forward output above.  Written out from the definition of
+ * softmax attention (the pages list attention backwards among the kernels
+ * built with the same tiles: groovesquid.com summary of the ThunderKittens
+ * paper; the quantities are the plain chain rule through the softmax):
+ *
+ *   p_ij   = exp(s_ij - m_i) / l_i            (the forward weights, j in J_i)
+ *   dV_j   = sum_i p_ij dO_i
+ *   dP_ij  = <dO_i, V_j>
+ *   dS_ij  = p_ij (dP_ij - sum_k p_ik dP_ik)   (softmax Jacobian applied to dP)
+ *   dQ_i   = scale * sum_j dS_ij K_j
+ *   dK_j   = scale * sum_i dS_ij Q_i
+ *
+ * Computed per head, one query row at a time, in fp64 from the bf16 inputs
+ * widened exactly.  Rows are split over threads; each thread accumulates
+ * its own dK and dV partial sums, which are added at the end in thread
+ * order (so the result does not depend on scheduling, only on the thread
+ * count through the final summation order, to within rounding).
+ */
+
+typedef struct {
+    const double *Q, *K, *V, *dO;
+    int64_t N, D;
+    int causal;
+    double scale;
+    double *dQ;            /* N x D, written by the thread owning the row */
+    double *dK_part;       /* T x N x D */
+    double *dV_part;       /* T x N x D */
+    int T;
+    int tid;
+} bwd_job;
+
+static void *bwd_worker(void *arg) {
+    bwd_job *job = (bwd_job *)arg;
+    const int64_t N = job->N, D = job->D;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s || !dp) {
+        free(s); free(dp);
+        return NULL;
+    }
+    double *dK = job->dK_part + (size_t)job->tid * (size_t)N * (size_t)D;
+    double *dV = job->dV_part + (size_t)job->tid * (size_t)N * (size_t)D;
+    for (int64_t i = job->tid; i < N; i += job->T) {
+        const double *q = job->Q + i * D;
+        const double *g = job->dO + i * D;
+        int64_t nkeys = job->causal ? i + 1 : N;
+        /* forward weights of row i */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += q[d] * job->K[j * D + d];
+            s[j] = job->scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            s[j] = exp(s[j] - m);
+            l += s[j];
+        }
+        for (int64_t j = 0; j < nkeys; ++j) s[j] /= l; /* s now holds p_ij */
+        /* dP and the softmax Jacobian term */
+        double pdp = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += g[d] * job->V[j * D + d];
+            dp[j] = dot;
+            pdp += s[j] * dot;
+        }
+        double *dq = job->dQ + i * D;
+        for (int64_t d = 0; d < D; ++d) dq[d] = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double ds = s[j] * (dp[j] - pdp);
+            for (int64_t d = 0; d < D; ++d) {
+                dq[d] += job->scale * ds * job->K[j * D + d];
+                dK[j * D + d] += job->scale * ds * q[d];
+                dV[j * D + d] += s[j] * g[d];
+            }
+        }
+    }
+    free(s); free(dp);
+    return NULL;
+}
+
+/* Q, K, V, dO: bf16 bits [B,H,N,D].  dQ, dK, dV: double [B,H,N,D]. */
+int tkor_attn_bwd(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, const uint16_t *dOb,
+                  double *dQ, double *dK, double *dV, int64_t B, int64_t H, int64_t N, int64_t D,
+                  int causal, double scale, int nthreads) {
+    if (!Qb || !Kb || !Vb || !dOb || !dQ || !dK || !dV || B < 1 || H < 1 || N < 1 || D < 1)
+        return -1;
+    int T = resolve_threads(nthreads);
+    if ((int64_t)T > N) T = (int)N;
+    const size_t n = (size_t)N * (size_t)D;
+    double *buf = (double *)malloc(sizeof(double) * n * 4);
+    double *dKp = (double *)malloc(sizeof(double) * n * (size_t)T);
+    double *dVp = (double *)malloc(sizeof(double) * n * (size_t)T);
+    bwd_job *jobs = (bwd_job *)malloc(sizeof(bwd_job) * (size_t)T);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)T);
+    if (!buf || !dKp || !dVp || !jobs || !tid) {
+        free(buf); free(dKp); free(dVp); free(jobs); free(tid);
+        return -1;
+    }
+    g_last_threads = T;
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const size_t off = (size_t)bh * n;
+        double *Q = buf, *K = buf + n, *V = buf + 2 * n, *G = buf + 3 * n;
+        for (size_t t = 0; t < n; ++t) {
+            Q[t] = bf16_bits_to_double(Qb[off + t]);
+            K[t] = bf16_bits_to_double(Kb[off + t]);
+            V[t] = bf16_bits_to_double(Vb[off + t]);
+            G[t] = bf16_bits_to_double(dOb[off + t]);
+        }
+        memset(dKp, 0, sizeof(double) * n * (size_t)T);
+        memset(dVp, 0, sizeof(double) * n * (size_t)T);
+        for (int t = 0; t < T; ++t) {
+            jobs[t].Q = Q; jobs[t].K = K; jobs[t].V = V; jobs[t].dO = G;
+            jobs[t].N = N; jobs[t].D = D; jobs[t].causal = causal; jobs[t].scale = scale;
+            jobs[t].dQ = dQ + off; jobs[t].dK_part = dKp; jobs[t].dV_part = dVp;
+            jobs[t].T = T; jobs[t].tid = t;
+        }
+        /* thread t >= 1 runs on its own pthread when one can be started,
+           otherwise inline; each writes only its own partial buffers */
+        unsigned char *spawned = (unsigned char *)calloc((size_t)T, 1);
+        for (int t = 1; t < T; ++t) {
+            if (spawned && pthread_create(&tid[t], NULL, bwd_worker, &jobs[t]) == 0)
+                spawned[t] = 1;
+            else
+                bwd_worker(&jobs[t]);
+        }
+        bwd_worker(&jobs[0]);
+        for (int t = 1; t < T; ++t)
+            if (spawned && spawned[t]) pthread_join(tid[t], NULL);
+        free(spawned);
+        for (size_t e = 0; e < n; ++e) {
+            double a = 0.0, b = 0.0;
+            for (int t = 0; t < T; ++t) {
+                a += dKp[(size_t)t * n + e];
+                b += dVp[(size_t)t * n + e];
+            }
+            dK[off + e] = a;
+            dV[off + e] = b;
+        }
+    }
+    free(buf); free(dKp); free(dVp); free(jobs); free(tid);
+    return 0;
+}

@@ -21,7 +21,8 @@ MUTANTS = [
     ("max dropped from LSE", "*lse_out = m + log(l);", "*lse_out = log(l);"),
     ("base-2 LSE", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     ("sign of the exponent flipped", "double p = exp(s[j] - m);", "double p = exp(m - s[j]);"),
-    ("minimum instead of maximum", "if (s[j] > m) m = s[j];", "if (s[j] < m || j == 0) m = s[j];"),
+    ("minimum instead of maximum", "s[j] = scale * dot;\n        if (s[j] > m) m = s[j];",
+     "s[j] = scale * dot;\n        if (s[j] < m || j == 0) m = s[j];"),
     ("causal mask excludes the diagonal", "int64_t nkeys = causal ? (i + 1) : N;",
      "int64_t nkeys = causal ? (i > 0 ? i : 1) : N;"),
     ("causal mask ignored", "int64_t nkeys = causal ? (i + 1) : N;", "int64_t nkeys = N;"),
@@ -70,3 +71,33 @@ def test_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
         except AssertionError as e:  # a pin failed, as it should
             caught.append((check.__name__, str(e)[:80]))
     assert caught, f"no pin caught the planted mistake: {name}"
+
+
+from tests import oracle_bwd_pins as bwd_pins  # noqa: E402
+
+BWD_MUTANTS = [
+    ("softmax term dropped", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * dp[j];"),
+    ("softmax term sign", "double ds = s[j] * (dp[j] - pdp);", "double ds = s[j] * (dp[j] + pdp);"),
+    ("scale missing in dQ", "dq[d] += job->scale * ds * job->K[j * D + d];", "dq[d] += ds * job->K[j * D + d];"),
+    ("dK from K instead of Q", "dK[j * D + d] += job->scale * ds * q[d];",
+     "dK[j * D + d] += job->scale * ds * job->K[j * D + d];"),
+    ("dV weighted by dS", "dV[j * D + d] += s[j] * g[d];", "dV[j * D + d] += ds * g[d];"),
+    ("dP against K", "for (int64_t d = 0; d < D; ++d) dot += g[d] * job->V[j * D + d];",
+     "for (int64_t d = 0; d < D; ++d) dot += g[d] * job->K[j * D + d];"),
+    ("weights not normalised", "for (int64_t j = 0; j < nkeys; ++j) s[j] /= l; /* s now holds p_ij */", ""),
+    ("causal mask dropped in backward", "int64_t nkeys = job->causal ? i + 1 : N;", "int64_t nkeys = N;"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mutant", BWD_MUTANTS, ids=[m[0] for m in BWD_MUTANTS])
+def test_bwd_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation anchor for '{name}' not unique in the oracle"
+    lib = oracle.bind(_compile(text.replace(orig, mutant), tmp_path, str(abs(hash(name)))))
+    caught = []
+    for check in bwd_pins.ALL_BWD_CHECKS:
+        try:
+            check(lambda q, k, v, do, c, s: oracle.attn_bwd(q, k, v, do, c, s, lib=lib))
+        except AssertionError as e:
+            caught.append((check.__name__, str(e)[:80]))
+    assert caught, f"no backward pin caught the planted mistake: {name}"

@@ -65,3 +65,22 @@ def test_oracle_regression_fixture(oracle_mod):
         L_ref = np.array([float(x) for x in case["LSE"]]).reshape(L.shape)
         assert np.max(np.abs(O - O_ref)) <= 1e-13
         assert np.max(np.abs(L - L_ref)) <= 1e-13
+
+
+from tests import oracle_bwd_pins as bwd_pins  # noqa: E402
+
+
+@pytest.mark.parametrize("check", bwd_pins.ALL_BWD_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_bwd_pin(oracle_mod, check):
+    check(oracle_mod.attn_bwd)
+
+
+def test_oracle_bwd_thread_count(oracle_mod):
+    import numpy as np
+    from tiled_attention_tk_gb300.inputs import make_qkv
+    q, k, v = make_qkv(1, 2, 40, 16, 51)
+    do = make_qkv(1, 2, 40, 16, 52)[0]
+    a = oracle_mod.attn_bwd(q, k, v, do, True, 0.25, threads=1)
+    b = oracle_mod.attn_bwd(q, k, v, do, True, 0.25, threads=3)
+    for x, y in zip(a, b):
+        assert np.max(np.abs(x - y)) <= 1e-13
