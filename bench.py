@@ -43,7 +43,8 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd TFLOP/s on 1 GB300 (fraction of dense BF16 peak) vs CPU oracle"
 FALLBACK_BF16_TFLOPS = 1900.0  # one earlier GB300 measurement, used only without MEASURED_PEAKS.json
 L2_BYTES = 126 * 1024 * 1024
-KERNEL_SOURCES = ["tiled_attention_tk_gb300/csrc/attn_fwd.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh"]
+KERNEL_SOURCES = ["tiled_attention_tk_gb300/csrc/attn_fwd.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
+                  "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
 DEFAULT_WORKLOAD = 4
 
 

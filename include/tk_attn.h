@@ -32,6 +32,7 @@
 #ifndef TK_ATTN_H
 #define TK_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -52,7 +53,8 @@ enum {
     TK_ERR_UNSUPPORTED_DEVICE = 8, /* current device is not compute capability 10.3       */
     TK_ERR_CUDA = 9,               /* a CUDA runtime/driver call or the launch failed     */
     TK_ERR_DEVICE_TIMEOUT = 10,    /* a bounded wait inside a kernel gave up (see below) */
-    TK_ERR_NOT_DEVICE_MEMORY = 11  /* a pointer is not device (or managed) memory        */
+    TK_ERR_NOT_DEVICE_MEMORY = 11, /* a pointer is not device (or managed) memory        */
+    TK_ERR_WORKSPACE = 12          /* workspace too small or not 256-byte aligned         */
 };
 
 /*
@@ -93,6 +95,49 @@ enum {
 int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                 int64_t B, int64_t H, int64_t N, int64_t D, int causal, float scale,
                 cudaStream_t stream);
+
+/*
+ * tk_attn_bwd_workspace_bytes -- device workspace tk_attn_bwd needs for a
+ * problem of this shape: an fp32 dQ accumulator [B,H,N,D] and the fp32 row
+ * values Delta_i = <dO_i, O_i> [B,H,N], each section 256-byte aligned.
+ * Returns 0 for shapes tk_attn_fwd would reject as TK_ERR_BAD_SHAPE or
+ * TK_ERR_UNSUPPORTED_D.
+ */
+size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
+
+/*
+ * tk_attn_bwd -- attention backward: the gradients of L = sum(O * dO) with
+ * respect to Q, K and V for O = softmax(scale * Q K^T [+ causal mask]) V.
+ * The pages list attention backwards among the kernels built with the same
+ * tiles (groovesquid.com summary of the ThunderKittens paper, "attention
+ * backwards"); it is the chain rule through the forward above:
+ *     P_ij  = exp(scale <Q_i,K_j> - LSE_i)   (LSE from tk_attn_fwd)
+ *     dV_j  = sum_i P_ij dO_i
+ *     dS_ij = scale * P_ij (<dO_i,V_j> - <dO_i,O_i>)
+ *     dQ_i  = sum_j dS_ij K_j,   dK_j = sum_i dS_ij Q_i
+ * P and dS are rounded to bf16 for the tensor-core products (as the forward
+ * rounds P); dQ accumulates in fp32 across key tiles.
+ *
+ * Arguments
+ *   Q, K, V   the forward's inputs (device, bf16 [B,H,N,D], 16-byte aligned).
+ *   O, LSE    the forward's outputs for them (bf16 [B,H,N,D]; fp32 [B,H,N]).
+ *   dO        gradient of the loss with respect to O (bf16 [B,H,N,D]).
+ *   dQ, dK, dV  outputs, bf16 [B,H,N,D], 16-byte aligned, written in full.
+ *   workspace device memory of at least tk_attn_bwd_workspace_bytes(B,H,N,D)
+ *             bytes, 256-byte aligned; owned by the caller, overwritten.
+ *   B, H, N, D, causal, scale, stream: as for tk_attn_fwd.
+ *
+ * Semantics: asynchronous on `stream` (three kernels: row values, main,
+ * dQ rounding).  dK and dV are deterministic; dQ sums fp32 contributions of
+ * the key tiles with atomic adds, so its last bits may vary between runs.
+ * Errors: as tk_attn_fwd, plus TK_ERR_NULL_PTR for a NULL workspace and
+ * TK_ERR_WORKSPACE (too small or misaligned).  Outputs must not overlap the
+ * inputs, each other or the workspace (TK_ERR_ALIAS).
+ */
+int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
+                size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                float scale, cudaStream_t stream);
 
 /*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the

@@ -35,8 +35,8 @@ def test_library_loads_and_exports_every_declared_symbol():
 
 def test_version_and_strerror():
     lib = tk.load()
-    assert lib.tk_attn_version() == (0 << 16) | 1
-    for code in range(0, 12):
+    assert lib.tk_attn_version() == (0 << 16) | 2
+    for code in range(0, 13):
         assert tk.strerror(code) and tk.strerror(code) != "unknown status code"
     assert tk.strerror(999) == "unknown status code"
 
@@ -94,3 +94,44 @@ def test_python_wrapper_rejects_bad_tensors():
 def test_error_carries_status_name():
     e = tk.TkError(tk.STATUS["TK_ERR_BAD_SCALE"], "tk_attn_fwd")
     assert "TK_ERR_BAD_SCALE" in str(e) and e.code == 5
+
+
+# ---------------------------------------------------------------- backward ABI
+
+Bdo, BdQ, BdK, BdV, Bws, Bo = (A + 0x5000000, A + 0x6000000, A + 0x7000000, A + 0x8000000,
+                               A + 0x9000000, A + 0xA000000)
+
+
+def _bwd(q=Bq, k=Bk, v=Bv, o=Bo, do=Bdo, l=Bl, dq=BdQ, dk=BdK, dv=BdV, ws=Bws, ws_bytes=None,
+         B=1, H=1, N=128, D=64, causal=0, scale=0.125):
+    lib = tk.load()
+    if ws_bytes is None:
+        ws_bytes = lib.tk_attn_bwd_workspace_bytes(B, H, N, D)
+    return lib.tk_attn_bwd(q, k, v, o, do, l, dq, dk, dv, ws, ws_bytes, B, H, N, D, causal, scale, None)
+
+
+def test_bwd_workspace_size():
+    lib = tk.load()
+    rows = 2 * 3 * 100
+    expect = -(-rows * 64 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+    assert lib.tk_attn_bwd_workspace_bytes(2, 3, 100, 64) == expect
+    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 96) == 0
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(do=None), "TK_ERR_NULL_PTR"),
+    (dict(ws=None), "TK_ERR_NULL_PTR"),
+    (dict(N=0), "TK_ERR_BAD_SHAPE"),
+    (dict(D=32), "TK_ERR_UNSUPPORTED_D"),
+    (dict(causal=3), "TK_ERR_BAD_FLAG"),
+    (dict(scale=-0.5), "TK_ERR_BAD_SCALE"),
+    (dict(dk=BdK + 8), "TK_ERR_MISALIGNED"),
+    (dict(ws=Bws + 16), "TK_ERR_WORKSPACE"),
+    (dict(ws_bytes=1024), "TK_ERR_WORKSPACE"),
+    (dict(dq=Bq), "TK_ERR_ALIAS"),
+    (dict(dv=BdK + 256), "TK_ERR_ALIAS"),
+    (dict(ws=Bdo), "TK_ERR_ALIAS"),
+])
+def test_bwd_host_validation(kwargs, code):
+    assert _bwd(**kwargs) == tk.STATUS[code]

@@ -1,0 +1,86 @@
+"""Parity of the CUDA backward (through the C ABI) with the fp64 backward
+oracle, on the forward outputs of the CUDA forward.
+
+Bar, per gradient G in (dQ, dK, dV), over every element:
+    max |G_gpu - G_ref|  <= 0.02 * max |G_ref|  + 1e-4
+    mean|G_gpu - G_ref|  <= 0.01 * mean|G_ref| + 1e-5
+sized from a CPU emulation of the kernel's roundings (bf16 P and dS, Delta
+from the bf16 forward output, fp32 LSE, bf16 outputs), whose errors stay
+below 0.0063 and 0.006 of those scales; the bar leaves about 3x for the fp32
+summation order of the tensor cores and the dQ atomics.  The absolute floor
+covers gradients that are exactly zero (a single key: dQ = dK = 0), where the
+kernel leaves fp32 rounding noise of order 1e-6 (Delta from the bf16 output
+against dP from the tensor core).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import tiled_attention_tk_gb300 as tk
+from tiled_attention_tk_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, do, causal, scale):
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, do))
+    o, lse = tk.fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = tk.bwd(qd, kd, vd, o, lse, gd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    status, detail = tk.device_status()
+    assert status == 0, f"device status {status} detail {detail:#x}"
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def _check(oracle_mod, q, k, v, do, causal, scale, what):
+    got = _run(q, k, v, do, causal, scale)
+    ref = oracle_mod.attn_bwd(q, k, v, do, causal, scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.double().numpy()
+        assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+        err = np.abs(g - r)
+        assert err.max() <= 0.02 * np.abs(r).max() + 1e-4, (
+            f"{what} {name}: max err {err.max():.3e} vs max|ref| {np.abs(r).max():.3e}")
+        assert err.mean() <= 0.01 * np.abs(r).mean() + 1e-5, (
+            f"{what} {name}: mean err {err.mean():.3e} vs mean|ref| {np.abs(r).mean():.3e}")
+    return got
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 128, 129, 300])
+def test_bwd_shape_sweep(oracle_mod, N, D, causal):
+    q, k, v = make_qkv(1, 2, N, D, 9000 + N + D)
+    do = make_qkv(1, 2, N, D, 9500 + N)[0]
+    _check(oracle_mod, q, k, v, do, causal, 1.0 / math.sqrt(D), f"N={N} D={D} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_several_tiles(oracle_mod, causal):
+    q, k, v = make_qkv(2, 3, 640, 128, 9100)
+    do = make_qkv(2, 3, 640, 128, 9101)[0]
+    _check(oracle_mod, q, k, v, do, causal, 1.0 / math.sqrt(128), f"B2H3N640 causal={causal}")
+
+
+def test_bwd_wide_logits(oracle_mod):
+    q, k, v = make_qkv(1, 4, 512, 128, 9200, "wide")
+    do = make_qkv(1, 4, 512, 128, 9201)[0]
+    _check(oracle_mod, q, k, v, do, False, 1.0 / math.sqrt(128), "wide logits")
+
+
+def test_bwd_invariants_and_determinism():
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold for the exact gradient;
+    dK and dV are also bitwise reproducible (dQ sums atomically)."""
+    q, k, v = make_qkv(1, 2, 384, 64, 9300)
+    do = make_qkv(1, 2, 384, 64, 9301)[0]
+    dq, dk, dv = _run(q, k, v, do, True, 0.125)
+    scale_k = dk.double().abs().sum(dim=2)
+    assert (dk.double().sum(dim=2).abs() <= 0.02 * scale_k + 1e-3).all()
+    sv = dv.double().sum(dim=2)
+    sd = do.double().sum(dim=2)
+    assert (sv - sd).abs().max().item() <= 0.02 * sd.abs().max().item() + 1e-2
+    dq2, dk2, dv2 = _run(q, k, v, do, True, 0.125)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert (dq.double() - dq2.double()).abs().max().item() <= 1e-2

@@ -89,6 +89,44 @@ def _fwd_from_host(q, k, v, causal, scale, stream):
     return o_h, l_h
 
 
+def bwd_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    """Device workspace bytes tk_attn_bwd needs (0 for an unsupported shape)."""
+    return int(_lib.load().tk_attn_bwd_workspace_bytes(B, H, N, D))
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        do: torch.Tensor, causal: bool = False, scale: float | None = None, workspace=None,
+        stream=None):
+    """Attention backward: (dQ, dK, dV), bf16 like q, for O = fwd(q, k, v)
+    with its LSE and the incoming gradient dO.  CUDA tensors only; enqueued
+    on ``stream`` (default: current) without synchronising.  ``workspace``
+    (optional) is a CUDA uint8 tensor of at least ``bwd_workspace_bytes``;
+    otherwise one is allocated with torch for the call."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA bf16 [B,H,N,D] tensor")
+        if t.shape != q.shape:
+            raise ValueError("q, k, v, o, do must have the same shape")
+    B, H, N, D = q.shape
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N):
+        raise ValueError("lse must be fp32 [B,H,N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    q, k, v, o, do, lse = (t.contiguous() for t in (q, k, v, o, do, lse))
+    need = bwd_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        rc = _lib.load().tk_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                     dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                     B, H, N, D, int(bool(causal)), float(scale),
+                                     _stream_handle(stream))
+    _lib.check(rc, "tk_attn_bwd")
+    return dq, dk, dv
+
+
 def device_status(stream=None) -> tuple[int, int]:
     """(status, detail): synchronises the stream, reads and clears the device
     status word.  status is 0 or TK_ERR_DEVICE_TIMEOUT."""

@@ -47,42 +47,9 @@
 #include "tk_attn.h"
 #include "tk_attn_internal.h"
 #include "tk_ptx.cuh"
+#include "tk_sync.cuh"
 
 namespace tk {
-
-// ------------------------------------------------------------------ status
-
-__device__ unsigned int g_status;  // 0 or TK_ERR_DEVICE_TIMEOUT
-__device__ unsigned int g_detail;  // where the first wait gave up
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
-constexpr uint64_t kDrainLimitNs = 50000000ull;   // 50 ms for draining after an abort
-
-enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_SOFTMAX = 3, ROLE_SELFTEST = 4 };
-
-__device__ __forceinline__ void record_timeout(uint32_t where) {
-    if (atomicCAS(&g_status, 0u, (unsigned)TK_ERR_DEVICE_TIMEOUT) == 0u) atomicExch(&g_detail, where);
-}
-
-// Waits for the phase `parity` of `bar`.  Returns false (and raises the
-// CTA's abort flag) if the wait exceeds `limit_ns`, or if another thread of
-// the CTA has raised the abort flag.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             uint32_t where, uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > limit_ns || spin > 0x7FFFFFF0u) {
-                *abort_flag = 1;
-                record_timeout(where);
-                return false;
-            }
-        }
-    }
-}
 
 // ------------------------------------------------------------------ layout
 
@@ -159,14 +126,6 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
 // Key tiles Q tile `qt` must visit.
 __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
     return p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
-}
-
-// One arrival per warp: the warp's lanes first synchronise (ordering their
-// earlier writes, and after a tcgen05 fence their TMEM stores), then lane 0
-// arrives.  Barriers fed this way count 4 arrivals per warpgroup.
-__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
 }
 
 // ------------------------------------------------------------------ kernel

@@ -20,7 +20,7 @@
 namespace {
 
 constexpr int kVersionMajor = 0;
-constexpr int kVersionMinor = 1;
+constexpr int kVersionMinor = 2;
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
@@ -121,9 +121,91 @@ int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int6
     return TK_OK;
 }
 
+// Shape checks shared by the forward and backward entry points.
+int check_shape(int64_t B, int64_t H, int64_t N, int64_t D) {
+    if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
+    if (D != 64 && D != 128) return TK_ERR_UNSUPPORTED_D;
+    // TMA coordinates and the launch grid are 32-bit.
+    if (N > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
+    const int64_t BH = B * H;
+    if (BH > INT64_MAX / N / D / 4) return TK_ERR_BAD_SHAPE;
+    const int64_t n_tiles = (N + 127) / 128;
+    if (n_tiles * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    return TK_OK;
+}
+
+constexpr uint64_t kWorkspaceAlign = 256;
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
 }  // namespace
 
 extern "C" {
+
+size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
+    if (check_shape(B, H, N, D) != TK_OK) return 0;
+    const uint64_t rows = static_cast<uint64_t>(B) * H * N;
+    return static_cast<size_t>(round_up(rows * D * 4, kWorkspaceAlign) + round_up(rows * 4, kWorkspaceAlign));
+}
+
+int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                void *dQ, void *dK, void *dV, void *workspace, size_t workspace_bytes, int64_t B, int64_t H,
+                int64_t N, int64_t D, int causal, float scale, cudaStream_t stream) {
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace) return TK_ERR_NULL_PTR;
+    int rc = check_shape(B, H, N, D);
+    if (rc != TK_OK) return rc;
+    if (causal != 0 && causal != 1) return TK_ERR_BAD_FLAG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return TK_ERR_BAD_SCALE;
+    const void *tensors[8] = {Q, K, V, O, dO, dQ, dK, dV};
+    for (const void *t : tensors)
+        if (!aligned(t, 16)) return TK_ERR_MISALIGNED;
+    if (!aligned(LSE, 4)) return TK_ERR_MISALIGNED;
+    const uint64_t need = tk_attn_bwd_workspace_bytes(B, H, N, D);
+    if (!aligned(workspace, kWorkspaceAlign) || workspace_bytes < need) return TK_ERR_WORKSPACE;
+    const int64_t BH = B * H;
+    const uint64_t tb = static_cast<uint64_t>(BH) * N * D * 2;
+    const uint64_t lb = static_cast<uint64_t>(BH) * N * 4;
+    // Outputs (dQ, dK, dV, workspace) must not overlap any input or each other.
+    const void *outs[4] = {dQ, dK, dV, workspace};
+    const uint64_t out_bytes[4] = {tb, tb, tb, need};
+    const void *ins[6] = {Q, K, V, O, dO, LSE};
+    const uint64_t in_bytes[6] = {tb, tb, tb, tb, tb, lb};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return TK_ERR_ALIAS;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return TK_ERR_ALIAS;
+    }
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const void *ptrs[11] = {Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, nullptr};
+    for (int i = 0; i < 10; ++i)
+        if ((rc = check_device_memory(ptrs[i])) != TK_OK) return rc;
+
+    tk::BwdParams p;
+    if ((rc = encode_qkv_map(&p.tmQ, Q, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmK, K, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmV, V, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmDO, dO, N, D, BH)) != TK_OK) return rc;
+    const uint64_t rows = static_cast<uint64_t>(BH) * N;
+    p.O = O;
+    p.dO = dO;
+    p.LSE = LSE;
+    p.dq_acc = static_cast<float *>(workspace);
+    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + round_up(rows * D * 4, kWorkspaceAlign));
+    p.dQ = dQ;
+    p.dK = dK;
+    p.dV = dV;
+    p.N = static_cast<int>(N);
+    p.BH = static_cast<int>(BH);
+    p.causal = causal;
+    p.n_tiles = static_cast<int>((N + 127) / 128);
+    p.scale = scale;
+    p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    cudaError_t e = tk::launch_attn_bwd(static_cast<int>(D), p, num_sms, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
 
 int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
                 int64_t H, int64_t N, int64_t D, int causal, float scale, cudaStream_t stream) {
@@ -178,11 +260,13 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
 }
 
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
-    uint32_t status = 0, where = 0;
-    cudaError_t e = tk::read_and_clear_status(stream, &status, &where);
+    uint32_t status = 0, where = 0, status_b = 0, where_b = 0;
+    cudaError_t e = tk::read_and_clear_status(stream, &status, &where);  // synchronises the stream
     if (e != cudaSuccess) return fail_cuda(e);
-    if (detail) *detail = where;
-    return status == 0 ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
+    e = tk::read_and_clear_bwd_status(&status_b, &where_b);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail) *detail = status ? where : where_b;
+    return (status == 0 && status_b == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
 }
 
 int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {
@@ -210,6 +294,7 @@ const char *tk_attn_strerror(int code) {
         case TK_ERR_CUDA: return "a CUDA call or the kernel launch failed";
         case TK_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
         case TK_ERR_NOT_DEVICE_MEMORY: return "a pointer is not device or managed memory";
+        case TK_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
         default: return "unknown status code";
     }
 }

@@ -28,6 +28,34 @@ struct AttnParams {
     float scale_log2e;  // scale * log2(e): the exp2-domain factor
 };
 
+// Everything the backward kernels need.
+struct BwdParams {
+    CUtensorMap tmQ;   // 3-D {D, N, B*H} bf16 views, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK;
+    CUtensorMap tmV;
+    CUtensorMap tmDO;
+    const void *O;     // bf16 [B*H, N, D] (forward output)
+    const void *dO;    // bf16 [B*H, N, D]
+    const float *LSE;  // fp32 [B*H, N] (forward log-sum-exp)
+    float *delta;      // workspace: fp32 [B*H, N], <dO_i, O_i>
+    float *dq_acc;     // workspace: fp32 [B*H, N, D], dQ accumulator
+    void *dQ;          // bf16 [B*H, N, D]
+    void *dK;
+    void *dV;
+    int N;
+    int BH;
+    int causal;
+    int n_tiles;       // ceil(N / 128)
+    float scale;
+    float scale_log2e;
+};
+
+// Launches the backward pass (prep, main, dQ conversion) for head dim D.
+cudaError_t launch_attn_bwd(int D, const BwdParams &p, int num_sms, cudaStream_t stream);
+
+// Reads and clears the backward translation unit's status word (no sync).
+cudaError_t read_and_clear_bwd_status(uint32_t *status, uint32_t *detail);
+
 // Launches the fused forward kernel for head dim D (64 or 128).
 cudaError_t launch_attn_fwd(int D, const AttnParams &p, int num_sms, cudaStream_t stream);
 
