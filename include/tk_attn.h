@@ -54,7 +54,8 @@ enum {
     TK_ERR_CUDA = 9,               /* a CUDA runtime/driver call or the launch failed     */
     TK_ERR_DEVICE_TIMEOUT = 10,    /* a bounded wait inside a kernel gave up (see below) */
     TK_ERR_NOT_DEVICE_MEMORY = 11, /* a pointer is not device (or managed) memory        */
-    TK_ERR_WORKSPACE = 12          /* workspace too small or not 256-byte aligned         */
+    TK_ERR_WORKSPACE = 12,         /* workspace too small or not 256-byte aligned         */
+    TK_ERR_NOALLOC_TOO_LARGE = 13  /* tk_attn_bwd_noalloc: workspace need above 32 MiB    */
 };
 
 /*
@@ -138,6 +139,33 @@ int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
                 const float *LSE, void *dQ, void *dK, void *dV, void *workspace,
                 size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
                 float scale, cudaStream_t stream);
+
+/*
+ * tk_attn_bwd_noalloc -- tk_attn_bwd without a caller workspace.  The paper
+ * has no counterpart: this entry point exists for callers that cannot
+ * allocate device memory, for instance code running under a framework or
+ * pool allocator that owns all of the device's memory (a raw cudaMalloc
+ * would fail or fragment it), or a latency-critical path that cannot take
+ * cudaMalloc's implicit device-wide synchronisation.  It allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The workspace is a fixed 32 MiB array inside the library (every device
+ * that loads the library holds it until the process exits).  Problems whose
+ * workspace (tk_attn_bwd_workspace_bytes) exceeds 32 MiB are rejected with
+ * TK_ERR_NOALLOC_TOO_LARGE before anything is enqueued; with D = 128 that is
+ * B*H*N above about 64 thousand rows.
+ *
+ * Arguments, results and errors are those of tk_attn_bwd without
+ * `workspace` and `workspace_bytes`.  The first call on a device looks up
+ * the array's device address (once per device, with that device current);
+ * make that first call before any stream capture.  All calls share the one
+ * array and it keeps the last call's contents (each call re-zeroes what it
+ * accumulates into), so calls whose work overlaps on the GPU -- on
+ * different streams without ordering between them -- race: serialise them.
+ */
+int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        const float *LSE, void *dQ, void *dK, void *dV, int64_t B, int64_t H,
+                        int64_t N, int64_t D, int causal, float scale, cudaStream_t stream);
 
 /*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the

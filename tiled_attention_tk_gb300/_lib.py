@@ -16,7 +16,7 @@ STATUS_NAMES = {
     0: "TK_OK", 1: "TK_ERR_NULL_PTR", 2: "TK_ERR_BAD_SHAPE", 3: "TK_ERR_UNSUPPORTED_D",
     4: "TK_ERR_MISALIGNED", 5: "TK_ERR_BAD_SCALE", 6: "TK_ERR_ALIAS", 7: "TK_ERR_BAD_FLAG",
     8: "TK_ERR_UNSUPPORTED_DEVICE", 9: "TK_ERR_CUDA", 10: "TK_ERR_DEVICE_TIMEOUT",
-    11: "TK_ERR_NOT_DEVICE_MEMORY", 12: "TK_ERR_WORKSPACE",
+    11: "TK_ERR_NOT_DEVICE_MEMORY", 12: "TK_ERR_WORKSPACE", 13: "TK_ERR_NOALLOC_TOO_LARGE",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 
@@ -27,6 +27,7 @@ SIGNATURES = {
     "tk_attn_bwd_workspace_bytes": ([_I64, _I64, _I64, _I64], ctypes.c_size_t),
     "tk_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64,
                      _I, _F, _P], _I),
+    "tk_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
     "tk_attn_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _I),
     "tk_attn_selftest_timeout": ([_U64, _P], _I),
     "tk_attn_strerror": ([_I], ctypes.c_char_p),

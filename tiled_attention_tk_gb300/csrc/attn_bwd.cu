@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "tk_attn.h"
 #include "tk_attn_internal.h"
@@ -419,6 +420,35 @@ cudaError_t launch_attn_bwd(int D, const BwdParams &p, int num_sms, cudaStream_t
     if (D == 64) return bwd::launch_d<64>(p, num_sms, stream);
     if (D == 128) return bwd::launch_d<128>(p, num_sms, stream);
     return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ fixed workspace
+// A workspace that lives in the library itself, for tk_attn_bwd_noalloc:
+// callers that cannot allocate device memory still get a backward pass for
+// problems whose workspace fits.  Every device that loads the library holds
+// this array until the process exits; every call on a device shares it.
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
+// The device address of the array on the current device.  Host code cannot
+// use the symbol itself (on the host it names a host-side stand-in), so the
+// address is looked up once per device, with that device current, and
+// cached.
+cudaError_t noalloc_workspace(void **ptr) {
+    static std::mutex mu;
+    static void *cached[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void *addr = nullptr;
+        err = cudaGetSymbolAddress(&addr, g_noalloc_workspace);
+        if (err != cudaSuccess) return err;
+        cached[dev] = addr;
+    }
+    *ptr = cached[dev];
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_bwd_status(uint32_t *status, uint32_t *detail) {

@@ -259,6 +259,23 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
     return TK_OK;
 }
 
+int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        const float *LSE, void *dQ, void *dK, void *dV, int64_t B, int64_t H, int64_t N,
+                        int64_t D, int causal, float scale, cudaStream_t stream) {
+    // The problem must fit the fixed workspace; this is decided on the host,
+    // before anything touches the device.
+    int rc = check_shape(B, H, N, D);
+    if (rc != TK_OK) return rc;
+    if (tk_attn_bwd_workspace_bytes(B, H, N, D) > tk::kNoAllocWorkspaceBytes) return TK_ERR_NOALLOC_TOO_LARGE;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    void *ws = nullptr;
+    const cudaError_t e = tk::noalloc_workspace(&ws);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return tk_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, ws, tk::kNoAllocWorkspaceBytes, B, H, N, D, causal,
+                       scale, stream);
+}
+
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     uint32_t status = 0, where = 0, status_b = 0, where_b = 0;
     cudaError_t e = tk::read_and_clear_status(stream, &status, &where);  // synchronises the stream
@@ -295,6 +312,8 @@ const char *tk_attn_strerror(int code) {
         case TK_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
         case TK_ERR_NOT_DEVICE_MEMORY: return "a pointer is not device or managed memory";
         case TK_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+        case TK_ERR_NOALLOC_TOO_LARGE:
+            return "problem needs more workspace than the 32 MiB built into tk_attn_bwd_noalloc";
         default: return "unknown status code";
     }
 }

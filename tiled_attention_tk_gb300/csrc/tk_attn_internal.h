@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime_api.h>
+#include <cstddef>
 #include <cstdint>
 
 namespace tk {
@@ -52,6 +53,13 @@ struct BwdParams {
 
 // Launches the backward pass (prep, main, dQ conversion) for head dim D.
 cudaError_t launch_attn_bwd(int D, const BwdParams &p, int num_sms, cudaStream_t stream);
+
+// Size of the library-owned workspace behind tk_attn_bwd_noalloc.
+constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
+
+// Device address of that workspace on the current device (looked up once
+// per device, then cached).  Allocates nothing.
+cudaError_t noalloc_workspace(void **ptr);
 
 // Reads and clears the backward translation unit's status word (no sync).
 cudaError_t read_and_clear_bwd_status(uint32_t *status, uint32_t *detail);
