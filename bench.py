@@ -2,7 +2,7 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..5] [--all]
+                    [--workload 1..5] [--all] [--bwd]
 
 One step = one tk_attn_fwd launch over the whole workload (every (b,h) head,
 every query row), inputs resident in HBM.  Default workload: B16 H32 N1024
@@ -17,6 +17,10 @@ dense bf16 peak), ``cpu_baseline`` (the fp64 CPU oracle timed on a bounded
 sample on this host), ``e2e`` (the same metric through the public API with
 pinned host buffers, copies inside the timed region), ``clocks`` (sampled
 with nvidia-smi during the timed region) and ``gpu_launches``.
+
+``--bwd``: the same line for the backward pass (tk_attn_bwd; flops
+10*B*H*N^2*D, halved under the causal mask), with the fp64 backward oracle as
+the CPU baseline.
 
 ``--impl reference``: the comparison arm is the fp64 CPU oracle (there is no
 runnable reference implementation), timed on this host's cores on a bounded
@@ -327,6 +331,95 @@ def run_ours(args, w):
     return line
 
 
+# ---------------------------------------------------------------- backward
+
+BWD_METRIC = "attention bwd TFLOP/s on 1 GB300 (fraction of dense BF16 peak) vs CPU oracle"
+
+
+def time_oracle_bwd_sample(w, q, k, v, do, budget_s: float):
+    """The fp64 backward oracle on whole heads until ``budget_s`` is spent.
+    Returns (TFLOP/s, cores, description); flops counted as 10*N^2*D per head
+    (halved under the causal mask), the same count as the GPU line."""
+    import oracle
+    oracle.build()
+    per_head = 10.0 * w.N * w.N * w.D / (2.0 if w.causal else 1.0)
+    done, t_total, heads = 0.0, 0.0, 0
+    while heads < w.B * w.H:
+        b, h = divmod(heads, w.H)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        t0 = time.perf_counter()
+        oracle.attn_bwd(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(), do[sl].contiguous(),
+                        w.causal, w.scale)
+        t_total += time.perf_counter() - t0
+        done += per_head
+        heads += 1
+        if t_total >= budget_s:
+            break
+    return (done / t_total / 1e12, oracle.last_threads(),
+            f"{heads} head(s) of {w.name} ({done / 1e9:.1f} GFLOP fp64, {t_total:.1f} s)")
+
+
+def run_bwd(args, w):
+    """One step = tk_attn_bwd over the whole workload (three launches: row
+    values, main kernel, dQ rounding), inputs and forward outputs resident."""
+    import torch
+    import tiled_attention_tk_gb300 as tk
+    from tiled_attention_tk_gb300.inputs import make_qkv, workload_inputs
+
+    _, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = workload_inputs(w)
+    do = make_qkv(w.B, w.H, w.N, w.D, 1000 * w.index + 500, "normal")[0]
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, do))
+    o, lse = tk.fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    ws = torch.empty(tk.bwd_workspace_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return tk.bwd(qd, kd, vd, o, lse, gd, causal=w.causal, scale=w.scale, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
+    flops = 2.5 * w.flops
+    peak, peak_label = peaks()
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": BWD_METRIC, "value": round(achieved, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
+        "config": dict(w.describe(), flops="10*B*H*N^2*D (halved causal): S, dP, dV, dK, dQ"),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_label, "traffic": None,
+                     "kernel": f"attn_bwd_kernel<{w.D}> + prep + dQ rounding (whole step)"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, desc = time_oracle_bwd_sample(w, q, k, v, do, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    return line
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args, w):
@@ -399,6 +492,7 @@ def main(argv=None):
     ap.add_argument("--shape", type=str, default=None,
                     help="B,H,N,D,causal: a custom N(0,1) workload instead of a named one")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -416,7 +510,12 @@ def main(argv=None):
     else:
         todo = [WORKLOADS[i] for i in ([1, 2, 3, 4, 5] if args.all else [args.workload])]
     for w in todo:
-        line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+        if args.impl == "reference":
+            line = run_reference(args, w)
+        elif args.bwd:
+            line = run_bwd(args, w)
+        else:
+            line = run_ours(args, w)
         if line is not None and rank == 0:
             print(json.dumps(line), flush=True)
 
