@@ -99,8 +99,10 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
 
 /*
  * tk_attn_bwd_workspace_bytes -- device workspace tk_attn_bwd needs for a
- * problem of this shape: an fp32 dQ accumulator [B,H,N,D] and the fp32 row
- * values Delta_i = <dO_i, O_i> [B,H,N], each section 256-byte aligned.
+ * problem of this shape: an fp32 dQ accumulator over whole 128-row query
+ * tiles (B*H*ceil(N/128)*128*D floats) and two fp32 row values over the
+ * same padded rows, Delta_i = <dO_i, O_i> and -LSE_i*log2(e); each section
+ * 256-byte aligned.
  * Returns 0 for shapes tk_attn_fwd would reject as TK_ERR_BAD_SHAPE or
  * TK_ERR_UNSUPPORTED_D.
  */
@@ -130,7 +132,8 @@ size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
  *
  * Semantics: asynchronous on `stream` (three kernels: row values, main,
  * dQ rounding).  dK and dV are deterministic; dQ sums fp32 contributions of
- * the key tiles with atomic adds, so its last bits may vary between runs.
+ * the key tiles with bulk atomic adds, so its last bits may vary between
+ * runs.
  * Errors: as tk_attn_fwd, plus TK_ERR_NULL_PTR for a NULL workspace and
  * TK_ERR_WORKSPACE (too small or misaligned).  Outputs must not overlap the
  * inputs, each other or the workspace (TK_ERR_ALIAS).

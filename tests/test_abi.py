@@ -113,7 +113,9 @@ def _bwd(q=Bq, k=Bk, v=Bv, o=Bo, do=Bdo, l=Bl, dq=BdQ, dk=BdK, dv=BdV, ws=Bws, w
 def test_bwd_workspace_size():
     lib = tk.load()
     rows = 2 * 3 * 100
-    expect = -(-rows * 64 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+    acc = 2 * 3 * 128 * 64 * 4  # fp32 dQ accumulator over whole 128-row query tiles
+    padded = 2 * 3 * 128 * 4    # Delta and -LSE*log2(e), one float per padded row each
+    expect = -(-acc // 256) * 256 + 2 * (-(-padded // 256) * 256)
     assert lib.tk_attn_bwd_workspace_bytes(2, 3, 100, 64) == expect
     assert lib.tk_attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
     assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 96) == 0

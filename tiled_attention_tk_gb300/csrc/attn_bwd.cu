@@ -15,21 +15,25 @@
 // tcgen05 tensor cores.
 //
 // Three kernels on the caller's stream:
-//   bwd_prep_kernel    Delta_i = <dO_i, O_i> (fp32) and a zeroed fp32 dQ
-//                      accumulator, one warp per row.
+//   bwd_prep_kernel    Delta_i = <dO_i, O_i> (fp32), one warp per row, and a
+//                      zeroed fp32 dQ accumulator.
 //   attn_bwd_kernel<D> one CTA per (head, 128-key tile).  K_j and V_j stay in
-//                      shared memory; for every 128-row query tile that sees
-//                      the keys, the MMA warp forms S = Q K^T and dP = dO V^T
-//                      in TMEM, four compute warps turn them into P and dS
-//                      (bf16, written to 128-byte-swizzled shared memory),
-//                      and the MMA warp accumulates dV += P^T dO and
-//                      dK += dS^T Q in TMEM and forms dQ_part = dS K, which
-//                      the compute warps add into the fp32 dQ accumulator
-//                      (vector reductions).  At the end dK and dV are written
-//                      as bf16.
+//                      shared memory and Q_i, dO_i of the query tiles that
+//                      see the keys stream through two buffers.  The MMA
+//                      warp forms S^T = K Q^T and dP^T = V dO^T in TMEM (one
+//                      key per TMEM lane); four compute warps turn them into
+//                      P^T and then dS^T, 32 queries at a time, written back
+//                      over them as bf16 (dS^T also into 128-byte-swizzled
+//                      shared memory).  The MMA warp accumulates
+//                      dV += P^T dO and dK += dS^T Q chunk by chunk with P^T
+//                      and dS^T read from TMEM, then forms dQ_part = dS K,
+//                      which the compute warps stage in shared memory and
+//                      add into the fp32 dQ accumulator with bulk (TMA)
+//                      reductions.  At the end dK and dV are written as bf16.
 //   bwd_dq_kernel      dQ = bf16(accumulator).
 // The same shared-memory tiles serve as K-major and MN-major MMA operands
-// through different descriptors (e.g. P for dV as P^T, dS as both).
+// through different descriptors (Q and dO are K-major B operands of S^T and
+// dP^T and MN-major B operands of dK and dV).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -37,6 +41,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "tk_attn.h"
 #include "tk_attn_internal.h"
@@ -48,9 +53,10 @@ namespace tk {
 namespace bwd {
 
 constexpr int BT = 128;             // rows per query tile and per key tile
-constexpr int NUM_THREADS = 192;    // 4 compute warps, TMA warp, MMA warp
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
+constexpr int NUM_THREADS = 448;    // 8 compute warps, 4 dQ warps, TMA warp, MMA warp
+constexpr int WARP_DQ = 8;          // first of the four dQ warps
+constexpr int WARP_TMA = 12;
+constexpr int WARP_MMA = 13;
 constexpr uint32_t TMEM_COLS = 512;
 
 template <int D>
@@ -60,36 +66,39 @@ struct Layout {
     static constexpr uint32_t TILE = BT * D * 2;         // a 128 x D tile
     static constexpr uint32_t K_OFF = 0;
     static constexpr uint32_t V_OFF = K_OFF + TILE;
-    static constexpr uint32_t Q_OFF = V_OFF + TILE;
-    static constexpr uint32_t DO_OFF = Q_OFF + TILE;
-    static constexpr uint32_t P_OFF = DO_OFF + TILE;      // 128 queries x 128 keys bf16 (2 boxes)
-    static constexpr uint32_t DS_OFF = P_OFF + 2 * BOX;
+    // Q and dO of a query tile, double-buffered: buffer b holds Q at
+    // QB_OFF + b * 2 * TILE and dO right after it.
+    static constexpr uint32_t QB_OFF = V_OFF + TILE;
+    static constexpr uint32_t DS_OFF = QB_OFF + 4 * TILE;   // dS^T: 128 keys x 128 queries bf16 (2 boxes)
     static constexpr uint32_t BAR_OFF = DS_OFF + 2 * BOX;
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_QFULL = 1;
-    static constexpr int B_SFULL = 2;      // S and dP in TMEM (MMA commit)
-    static constexpr int B_PREADY = 3;     // P and dS in shared memory (compute warps, 4)
-    static constexpr int B_GDONE = 4;      // dV, dK, dQ_part MMAs done (MMA commit)
-    static constexpr int B_DQREAD = 5;     // dQ_part read out of TMEM (compute warps, 4)
-    static constexpr int B_MMADONE = 6;
-    static constexpr int NUM_BARS = 7;
+    static constexpr int B_QFULL = 1;      // + buffer (2): Q and dO loaded
+    static constexpr int B_QEMPTY = 3;     // + buffer (2): the products that read them are done (MMA commit)
+    static constexpr int B_SFULL = 5;      // S^T in TMEM (MMA commit)
+    static constexpr int B_DPFULL = 6;     // dP^T in TMEM (MMA commit)
+    static constexpr int B_PRDY = 7;       // + chunk (4): 32 queries of P^T in TMEM (a compute group, 4)
+    static constexpr int B_DSRDY = 11;     // + chunk (4): 32 queries of dS^T in TMEM and smem (a compute group, 4)
+    static constexpr int B_GDONE = 15;     // dQ_part product done (MMA commit)
+    static constexpr int B_DQREAD = 16;    // dQ_part read out of TMEM (dQ warps, 4)
+    static constexpr int B_MMADONE = 17;
+    static constexpr int NUM_BARS = 18;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     static constexpr uint32_t SMEM_ALLOC =
         SMEM_USED + 1024 > 116u * 1024u ? SMEM_USED + 1024 : 116u * 1024u;  // one CTA per SM
     static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
-    // TMEM columns
-    static constexpr uint32_t T_S = 0;           // S, then dQ_part (D columns)
-    static constexpr uint32_t T_DP = 128;        // dP
+    // TMEM columns; lane = key of this CTA's key tile, except dQ_part
+    // (lane = query of the current query tile).
+    static constexpr uint32_t T_S = 0;           // S^T, then bf16 P^T (see pcol)
+    static constexpr uint32_t T_DP = 128;        // dP^T, then bf16 dS^T (see pcol); then dQ_part
+    static constexpr uint32_t T_DQ = T_DP + 128 - D;  // dQ_part (D columns)
     static constexpr uint32_t T_DV = 256;        // dV accumulator (D columns)
     static constexpr uint32_t T_DK = 256 + D;    // dK accumulator (D columns)
+    // Column (within the S^T / dP^T block) of the bf16 results of query
+    // chunk c (32 queries, 16 columns): each compute group writes only over
+    // its own inputs (group 0: columns 0..63, group 1: 64..127), after
+    // reading them.
+    __host__ __device__ static constexpr uint32_t pcol(int c) { return c < 2 ? 16 * c : 64 + 16 * (c - 2); }
 };
-
-// Adds four floats to global memory with one vector reduction.
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
 
 // Shared-memory address of 16-byte chunk `c` (0..7) of row `r` in a
 // 128-byte-swizzled box (the layout TMA writes with the 128-byte swizzle).
@@ -97,6 +106,37 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t box, int r, int c) {
     return box + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
+// Adds four floats to global memory with one vector reduction.
+__device__ __forceinline__ void red_add_v4(float *addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// The two floats of a packed bf16 pair (low half first).
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
+// Keys sit on the TMEM lanes: the MMA warp forms S^T = K Q^T and
+// dP^T = V dO^T, so that each key row of the tile belongs to one TMEM lane.
+// Two groups of four compute warps (queries 0..63 and 64..127) write P^T
+// and then dS^T back over S^T and dP^T as bf16, 32 queries at a time, and
+// the MMA warp consumes each chunk as soon as it is ready: dV += P^T dO and
+// dK += dS^T Q read P^T and dS^T from TMEM.  dS^T also goes to shared
+// memory, where it is the MN-major A operand of dQ_part = dS K.  The next
+// query tile's S^T is issued before this tile's dQ_part, so the compute
+// warps start on it while the tensor core finishes this tile; four dQ warps
+// add dQ_part into the fp32 accumulator and write dK and dV at the end.
+//
+// The unscaled dS' = P (dP - Delta) is what the products see; dK and dQ are
+// multiplied by `scale` when they are rounded to bf16.
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = Layout<D>;
@@ -111,12 +151,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    // Work: key tile kt of head bh; key tile 0 first (it sees the most query
-    // tiles under the causal mask).
-    const int kt = blockIdx.x / p.BH;
-    const int bh = blockIdx.x % p.BH;
+    // Work: key tile kt of head bh.  The key tiles of one head are adjacent
+    // in launch order, so they run together and share Q and dO through L2.
+    const int kt = blockIdx.x % p.n_tiles;
+    const int bh = blockIdx.x / p.n_tiles;
     const int qt_first = p.causal ? kt : 0;
     const int n_q = p.n_tiles - qt_first;
+    const size_t head_rows = static_cast<size_t>(bh) * p.N;
+    const size_t head_tiles = static_cast<size_t>(bh) * p.n_tiles;
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -124,9 +166,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
     }
     if (threadIdx.x == 0) {
         mbar_init(bar(L::B_KVFULL), 1);
-        mbar_init(bar(L::B_QFULL), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_QFULL + b), 1);
+            mbar_init(bar(L::B_QEMPTY + b), 1);
+        }
         mbar_init(bar(L::B_SFULL), 1);
-        mbar_init(bar(L::B_PREADY), 4);
+        mbar_init(bar(L::B_DPFULL), 1);
+        for (int c = 0; c < 4; ++c) {
+            mbar_init(bar(L::B_PRDY + c), 4);
+            mbar_init(bar(L::B_DSRDY + c), 4);
+        }
         mbar_init(bar(L::B_GDONE), 1);
         mbar_init(bar(L::B_DQREAD), 4);
         mbar_init(bar(L::B_MMADONE), 1);
@@ -152,75 +201,120 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             }
             int issued = 0;
             for (int it = 0; it < n_q; ++it) {
-                // Q, dO, P and dS of the previous query tile are free once its
-                // gradient MMAs have completed.
-                if (it > 0 && !wait_bounded(bar(L::B_GDONE), (it - 1) & 1, abort_flag,
-                                            (ROLE_BWD_PRODUCER << 24) | (L::B_GDONE << 16) | it)) {
+                const int b = it & 1;
+                // Buffer b was last used by query tile it-2.
+                if (it >= 2 && !wait_bounded(bar(L::B_QEMPTY + b), ((it >> 1) - 1) & 1, abort_flag,
+                                             (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | it)) {
                     // Let the copies in flight land before the CTA exits.
                     const uint64_t t0 = global_timer_ns();
-                    while (!(mbar_try_wait(bar(L::B_KVFULL), 0) && mbar_try_wait(bar(L::B_QFULL), (issued - 1) & 1)) &&
-                           global_timer_ns() - t0 < kDrainLimitNs) {
+                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                        while (!mbar_try_wait(bar(L::B_QFULL + (j & 1)), (j >> 1) & 1) &&
+                               global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    while (!mbar_try_wait(bar(L::B_KVFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
                     }
                     break;
                 }
-                ++issued;
                 const int qt = qt_first + it;
-                mbar_arrive_expect_tx(bar(L::B_QFULL), 2 * L::TILE);
+                const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE);
                 for (int c = 0; c < L::KATOMS; ++c) {
-                    tma_load_3d(sbase + L::Q_OFF + c * L::BOX, &p.tmQ, bar(L::B_QFULL), c * 64, qt * BT, bh);
-                    tma_load_3d(sbase + L::DO_OFF + c * L::BOX, &p.tmDO, bar(L::B_QFULL), c * 64, qt * BT, bh);
+                    tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
+                    tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
                 }
+                ++issued;
             }
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
+        // Per query tile i: dV(i) and dK(i) chunk by chunk, S^T(i+1),
+        // dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.  Each
+        // product that overwrites TMEM columns an earlier product reads (S^T
+        // over P^T, dQ_part over dS^T) is issued after it; the tensor core
+        // runs one thread's products in issue order.
         if (lane == 0) {
-            constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S, dP: K-major A and B
-            constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dV, dK: MN-major A and B
-            constexpr uint32_t IDESC_KM = idesc_bf16_f32(BT, D, 0, 1);   // dQ: K-major A, MN-major B
-            bool ok = wait_bounded(bar(L::B_KVFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16));
-            for (int it = 0; ok && it < n_q; ++it) {
-                if (!(ok = wait_bounded(bar(L::B_QFULL), it & 1, abort_flag,
-                                        (ROLE_BWD_MMA << 24) | (L::B_QFULL << 16) | it)))
-                    break;
-                // S / dQ_part columns are free once the previous dQ_part was read.
-                if (it > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (it - 1) & 1, abort_flag,
-                                                  (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | it)))
-                    break;
-                tc_fence_after_sync();
+            constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S^T, dP^T: K-major A and B
+            constexpr uint32_t IDESC_TS = idesc_bf16_f32(BT, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
+            constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dQ_part: MN-major A and B
+            auto issue_s = [&](uint32_t qb) {  // S^T = K Q^T
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k / 4) * L::BOX + (k % 4) * 32;
-                    umma_ss(tmem + L::T_S, smem_desc_sw128(sbase + L::Q_OFF + off, 16, 1024),
-                            smem_desc_sw128(sbase + L::K_OFF + off, 16, 1024), IDESC_KK, k > 0);
-                    umma_ss(tmem + L::T_DP, smem_desc_sw128(sbase + L::DO_OFF + off, 16, 1024),
-                            smem_desc_sw128(sbase + L::V_OFF + off, 16, 1024), IDESC_KK, k > 0);
+                    umma_ss(tmem + L::T_S, smem_desc_sw128(sbase + L::K_OFF + off, 16, 1024),
+                            smem_desc_sw128(qb + off, 16, 1024), IDESC_KK, k > 0);
                 }
                 umma_commit(bar(L::B_SFULL));
-                if (!(ok = wait_bounded(bar(L::B_PREADY), it & 1, abort_flag,
-                                        (ROLE_BWD_MMA << 24) | (L::B_PREADY << 16) | it)))
-                    break;
+            };
+            auto issue_dp = [&](uint32_t dob) {  // dP^T = V dO^T
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * L::BOX + (k % 4) * 32;
+                    umma_ss(tmem + L::T_DP, smem_desc_sw128(sbase + L::V_OFF + off, 16, 1024),
+                            smem_desc_sw128(dob + off, 16, 1024), IDESC_KK, k > 0);
+                }
+                umma_commit(bar(L::B_DPFULL));
+            };
+            bool ok = wait_bounded(bar(L::B_KVFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16)) &&
+                      wait_bounded(bar(L::B_QFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_QFULL << 16));
+            if (ok) {
                 tc_fence_after_sync();
-                // 16 queries per step: P / dS (MN-major, rows = queries) and
-                // dO / Q (MN-major, rows = queries) advance by 16 rows.
+                issue_s(sbase + L::QB_OFF);
+                issue_dp(sbase + L::QB_OFF + L::TILE);
+            }
+            for (int it = 0; ok && it < n_q; ++it) {
+                const int b = it & 1;
+                const uint32_t ph = it & 1;
+                const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                const uint32_t dob = qb + L::TILE;
+                // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
+                // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
+                for (int c = 0; ok && c < 4; ++c) {
+                    if (!(ok = wait_bounded(bar(L::B_PRDY + c), ph, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | it)))
+                        break;
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int k = 0; k < BT / 16; ++k) {
-                    const uint32_t roff = k * 2048;
-                    const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-                    umma_ss(tmem + L::T_DV, smem_desc_sw128(sbase + L::P_OFF + roff, L::BOX, 1024),
-                            smem_desc_sw128(sbase + L::DO_OFF + roff, L::BOX, 1024), IDESC_MM, acc);
-                    umma_ss(tmem + L::T_DK, smem_desc_sw128(sbase + L::DS_OFF + roff, L::BOX, 1024),
-                            smem_desc_sw128(sbase + L::Q_OFF + roff, L::BOX, 1024), IDESC_MM, acc);
+                    for (int k = 2 * c; k < 2 * c + 2; ++k)
+                        umma_ts(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + (k % 2) * 8,
+                                smem_desc_sw128(dob + k * 2048, L::BOX, 1024), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
                 }
-                // dQ_part = dS K: 16 keys per step; dS K-major, K MN-major.
+                // dK += dS'^T Q likewise.
+                for (int c = 0; ok && c < 4; ++c) {
+                    if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | it)))
+                        break;
+                    tc_fence_after_sync();
 #pragma unroll
-                for (int k = 0; k < BT / 16; ++k) {
-                    const uint32_t aoff = (k / 4) * L::BOX + (k % 4) * 32;
-                    umma_ss(tmem + L::T_S, smem_desc_sw128(sbase + L::DS_OFF + aoff, 16, 1024),
-                            smem_desc_sw128(sbase + L::K_OFF + k * 2048, L::BOX, 1024), IDESC_KM, k > 0);
+                    for (int k = 2 * c; k < 2 * c + 2; ++k)
+                        umma_ts(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + (k % 2) * 8,
+                                smem_desc_sw128(qb + k * 2048, L::BOX, 1024), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
                 }
+                if (!ok) break;
+                umma_commit(bar(L::B_QEMPTY + b));  // Q, dO of this tile are no longer read
+                const bool has_next = it + 1 < n_q;
+                const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
+                if (has_next) {
+                    if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((it + 1) >> 1) & 1, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | it)))
+                        break;
+                    tc_fence_after_sync();
+                    issue_s(qn);
+                }
+                // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
+                // the dS^T buffer (MN-major A) and K MN-major.
+#pragma unroll
+                for (int k = 0; k < BT / 16; ++k)
+                    umma_ss(tmem + L::T_DQ, smem_desc_sw128(sbase + L::DS_OFF + k * 2048, L::BOX, 1024),
+                            smem_desc_sw128(sbase + L::K_OFF + k * 2048, L::BOX, 1024), IDESC_MM, k > 0);
                 umma_commit(bar(L::B_GDONE));
+                if (has_next) {
+                    if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | it)))
+                        break;
+                    tc_fence_after_sync();
+                    issue_dp(qn + L::TILE);
+                }
             }
             umma_commit(bar(L::B_MMADONE));
             const uint64_t t0 = global_timer_ns();
@@ -229,101 +323,175 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ compute warps: P, dS, dQ reduction
-        const int t = threadIdx.x;  // row of the query tile == TMEM lane (S, dP, dQ_part),
-                                    // row of the key tile for dK, dV
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float c = p.scale_log2e;
-        const size_t head_rows = static_cast<size_t>(bh) * p.N;
+    } else if (warp < WARP_DQ) {
+        // ------------------------------------------------ compute warps
+        const int grp = warp / 4;              // queries 64*grp .. 64*grp + 63
+        const int t = (warp % 4) * 32 + lane;  // TMEM lane: key row t of the key tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+        const float2 c2 = make_float2(p.scale_log2e, p.scale_log2e);
+        const int key = kt * BT + t;
         bool ok = true;
         for (int it = 0; it < n_q; ++it) {
             const int qt = qt_first + it;
-            const int row = qt * BT + t;
-            const bool valid_row = row < p.N;
-            // Rows past N: P = exp2(-inf) = 0 and Delta = 0, so they add nothing.
-            const float lse2 = valid_row ? p.LSE[head_rows + row] * 1.4426950408889634f : INFINITY;
-            const float delta = valid_row ? p.delta[head_rows + row] : 0.0f;
-            // keys the row may see in this key tile: [0, kmax)
-            int kmax = p.N - kt * BT;
-            if (p.causal) kmax = min(kmax, row - kt * BT + 1);
-            if (!(ok = wait_bounded(bar(L::B_SFULL), it & 1, abort_flag,
+            const uint32_t ph = it & 1;
+            // -LSE*log2(e) and -Delta of this group's 64 queries (padded
+            // rows: -inf and 0, so their weights and gradients are 0)
+            const size_t row0 = (head_tiles + qt) * BT + grp * 64;
+            const float4 *nl4 = reinterpret_cast<const float4 *>(p.neg_lse2 + row0);
+            const float4 *dl4 = reinterpret_cast<const float4 *>(p.neg_delta + row0);
+            // Only the causal diagonal tile and a ragged last key tile hold
+            // weights to zero: the queries below qmin do not see this key
+            // (keys past N are seen by none).
+            const bool diag = p.causal && qt == kt;
+            const bool masked = diag || kt * BT + BT > p.N;
+            const int qmin = key >= p.N ? BT : (diag ? key - qt * BT : 0);
+
+            // P^T = exp2(S^T c - LSE log2 e), bf16, 32 queries per chunk
+            auto p_chunk = [&](const uint32_t(&sr)[32], int cc, uint32_t(&pp)[16], auto mask_tag) {
+                const int q0 = (2 * grp + cc) * 32;
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 l4 = __ldg(nl4 + cc * 8 + e4);
+                    float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * e4]), __uint_as_float(sr[4 * e4 + 1])),
+                                           c2, make_float2(l4.x, l4.y));
+                    float2 x1 = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[4 * e4 + 2]), __uint_as_float(sr[4 * e4 + 3])), c2,
+                        make_float2(l4.z, l4.w));
+                    float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                    float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                    if constexpr (decltype(mask_tag)::value) {
+                        const int q = q0 + 4 * e4;
+                        if (q + 0 < qmin) p0.x = 0.0f;
+                        if (q + 1 < qmin) p0.y = 0.0f;
+                        if (q + 2 < qmin) p1.x = 0.0f;
+                        if (q + 3 < qmin) p1.y = 0.0f;
+                    }
+                    pp[2 * e4] = pack2(p0);
+                    pp[2 * e4 + 1] = pack2(p1);
+                }
+            };
+            // dS' = P (dP - Delta), bf16
+            auto ds_chunk = [&](const uint32_t(&dr)[32], const uint32_t(&pr)[16], int cc, uint32_t(&ds)[16]) {
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 d4 = __ldg(dl4 + cc * 8 + e4);
+                    const float2 g0 = __fadd2_rn(
+                        make_float2(__uint_as_float(dr[4 * e4]), __uint_as_float(dr[4 * e4 + 1])),
+                        make_float2(d4.x, d4.y));
+                    const float2 g1 = __fadd2_rn(
+                        make_float2(__uint_as_float(dr[4 * e4 + 2]), __uint_as_float(dr[4 * e4 + 3])),
+                        make_float2(d4.z, d4.w));
+                    ds[2 * e4] = pack2(__fmul2_rn(unpack_bf16x2(pr[2 * e4]), g0));
+                    ds[2 * e4 + 1] = pack2(__fmul2_rn(unpack_bf16x2(pr[2 * e4 + 1]), g1));
+                }
+            };
+
+            if (!(ok = wait_bounded(bar(L::B_SFULL), ph, abort_flag,
                                     (ROLE_BWD_COMPUTE << 24) | (L::B_SFULL << 16) | it)))
                 break;
             tc_fence_after_sync();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 32 keys at a time
-                uint32_t sr[32], dr[32];
-                tmem_ld32(lane_base + L::T_S + q * 32, sr);
-                tmem_ld32(lane_base + L::T_DP + q * 32, dr);
-                uint32_t pp[16], ds[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int key = q * 32 + 2 * e + h;
-                        const float x = fmaf(__uint_as_float(sr[2 * e + h]), c, -lse2);
-                        pv[h] = key < kmax ? ex2(x) : 0.0f;
-                        dv[h] = p.scale * pv[h] * (__uint_as_float(dr[2 * e + h]) - delta);
-                    }
-                    pp[e] = pack_bf16x2(pv[0], pv[1]);
-                    ds[e] = pack_bf16x2(dv[0], dv[1]);
-                }
-                // keys q*32 .. q*32+31 = chunks 4(q%2) .. 4(q%2)+3 of box q/2, row t
-                const uint32_t pbox = sbase + L::P_OFF + (q / 2) * L::BOX;
-                const uint32_t dbox = sbase + L::DS_OFF + (q / 2) * L::BOX;
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int chunk = (q % 2) * 4 + v;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128_chunk(pbox, t, chunk)),
-                                 "r"(pp[4 * v]), "r"(pp[4 * v + 1]), "r"(pp[4 * v + 2]), "r"(pp[4 * v + 3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128_chunk(dbox, t, chunk)),
-                                 "r"(ds[4 * v]), "r"(ds[4 * v + 1]), "r"(ds[4 * v + 2]), "r"(ds[4 * v + 3])
-                                 : "memory");
-                }
+            {
+                const int ca = 2 * grp, cb = 2 * grp + 1;
+                uint32_t sa[32], sb[32], pp[16];
+                tmem_ld32_async(lane_base + L::T_S + ca * 32, sa);
+                tmem_ld32_async(lane_base + L::T_S + cb * 32, sb);
+                tmem_ld_wait();
+                reg_fence(sa);
+                reg_fence(sb);
+                if (masked) p_chunk(sa, 0, pp, std::true_type());
+                else p_chunk(sa, 0, pp, std::false_type());
+                tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
+                if (masked) p_chunk(sb, 1, pp, std::true_type());
+                else p_chunk(sb, 1, pp, std::false_type());
+                tmem_st16(lane_base + L::T_S + L::pcol(cb), pp);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                warp_arrive(bar(L::B_PRDY + ca), lane);
+                warp_arrive(bar(L::B_PRDY + cb), lane);
             }
+
+            if (!(ok = wait_bounded(bar(L::B_DPFULL), ph, abort_flag,
+                                    (ROLE_BWD_COMPUTE << 24) | (L::B_DPFULL << 16) | it)))
+                break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int ch = 2 * grp + cc;
+                uint32_t dr[32], pr[16], ds[16];
+                tmem_ld32_async(lane_base + L::T_DP + ch * 32, dr);
+                tmem_ld16_async(lane_base + L::T_S + L::pcol(ch), pr);
+                tmem_ld_wait();
+                reg_fence(dr);
+                reg_fence(pr);
+                ds_chunk(dr, pr, cc, ds);
+                tmem_st16(lane_base + L::T_DP + L::pcol(ch), ds);
+                // dS'^T row t (key), queries ch*32 .. ch*32+31 = pieces 4cc.. of box grp
+                const uint32_t dbox = sbase + L::DS_OFF + grp * L::BOX;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    st_shared_v4(sw128_chunk(dbox, t, cc * 4 + v), ds[4 * v], ds[4 * v + 1], ds[4 * v + 2],
+                                 ds[4 * v + 3]);
+            }
+            tmem_st_wait();
             fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
             tc_fence_before_sync();
-            warp_arrive(bar(L::B_PREADY), lane);
+            warp_arrive(bar(L::B_DSRDY + 2 * grp), lane);
+            warp_arrive(bar(L::B_DSRDY + 2 * grp + 1), lane);
+        }
+    } else {
+        // ------------------------------------------------ dQ warps
+        const int t = (warp - WARP_DQ) * 32 + lane;  // TMEM lane: query row t (dQ_part), key row t (dK, dV)
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - WARP_DQ) * 32) << 16);
+        bool ok = true;
+        for (int it = 0; it < n_q; ++it) {
+            const int qt = qt_first + it;
             if (!(ok = wait_bounded(bar(L::B_GDONE), it & 1, abort_flag,
                                     (ROLE_BWD_COMPUTE << 24) | (L::B_GDONE << 16) | it)))
                 break;
             tc_fence_after_sync();
-            float *dq = p.dq_acc + (head_rows + (valid_row ? row : 0)) * D;
+            // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
+            // reduction of one 4-column group covers 512 contiguous bytes.
+            float *dq_tile = p.dq_acc + (head_tiles + qt) * BT * D + t * 4;
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + L::T_S + q * 32, r);
-                if (valid_row) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dq + q * 32 + 4 * v, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32_async(lane_base + L::T_DQ + 64 * h, r0);
+                tmem_ld32_async(lane_base + L::T_DQ + 64 * h + 32, r1);
+                tmem_ld_wait();
+                reg_fence(r0);
+                reg_fence(r1);
+                if (h == D / 64 - 1) {
+                    tc_fence_before_sync();
+                    warp_arrive(bar(L::B_DQREAD), lane);
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    red_add_v4(dq_tile + (16 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    red_add_v4(dq_tile + (16 * h + 8 + j) * BT * 4, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
+                               r1[4 * j + 3]);
             }
-            tc_fence_before_sync();
-            warp_arrive(bar(L::B_DQREAD), lane);
         }
         if (ok) {
-            // dK, dV of this key tile: TMEM lane t = key kt*128 + t.  The last
-            // GDONE wait above covers every gradient MMA.
+            // dK = scale * (dS'^T Q), dV of this key tile (lane t = key).
+            // The last GDONE wait covers every product.
             const int key = kt * BT + t;
-            const bool store = key < p.N;
-            __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (store ? key : 0)) * D;
-            __nv_bfloat16 *dvrow = static_cast<__nv_bfloat16 *>(p.dV) + (head_rows + (store ? key : 0)) * D;
+            const bool valid_key = key < p.N;
+            const float scale = p.scale;
+            __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (valid_key ? key : 0)) * D;
+            __nv_bfloat16 *dvrow = static_cast<__nv_bfloat16 *>(p.dV) + (head_rows + (valid_key ? key : 0)) * D;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 // every lane takes part in the TMEM loads; only the stores are guarded
                 uint32_t rk[32], rv[32];
                 tmem_ld32(lane_base + L::T_DK + q * 32, rk);
                 tmem_ld32(lane_base + L::T_DV + q * 32, rv);
-                if (store) {
+                if (valid_key) {
                     uint32_t pk[16], pv[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        pk[e] = pack_bf16x2(__uint_as_float(rk[2 * e]), __uint_as_float(rk[2 * e + 1]));
+                        pk[e] = pack_bf16x2(scale * __uint_as_float(rk[2 * e]), scale * __uint_as_float(rk[2 * e + 1]));
                         pv[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
                     }
 #pragma unroll
@@ -346,39 +514,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
     }
 }
 
-// Delta_i = <dO_i, O_i> in fp32 and a zeroed fp32 dQ accumulator row; one
-// warp per row, rows = B*H*N.
+// Per padded query row (n_tiles * 128 rows per head, one warp per row):
+// -Delta = -<dO, O> in fp32 and -LSE * log2(e); rows past N get 0 and -inf.
+// Also zeroes the dQ accumulator (acc_vec4 float4s, grid-stride).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
-                                                      float *__restrict__ delta, float *__restrict__ dq_acc,
-                                                      int64_t rows) {
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+                                                      const float *__restrict__ LSE, float *__restrict__ neg_delta,
+                                                      float *__restrict__ neg_lse2, float *__restrict__ dq_acc,
+                                                      int64_t padded_rows, int N, int n_tiles, int64_t acc_vec4) {
+    const int64_t prow = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (row >= rows) return;
-    constexpr int PER = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
-    const __nv_bfloat16 *o = O + row * D + lane * PER;
-    const __nv_bfloat16 *g = dO + row * D + lane * PER;
-    float s = 0.0f;
+    if (prow < padded_rows) {
+        const int64_t bh = prow / (static_cast<int64_t>(n_tiles) * BT);
+        const int n = static_cast<int>(prow % (static_cast<int64_t>(n_tiles) * BT));
+        float s = 0.0f, nl = -INFINITY;
+        if (n < N) {
+            const int64_t row = bh * N + n;
+            constexpr int PER = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
+            const __nv_bfloat16 *o = O + row * D + lane * PER;
+            const __nv_bfloat16 *g = dO + row * D + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) s = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), s);
+            for (int e = 0; e < PER; ++e) s = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), s);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-    if (lane == 0) delta[row] = s;
-    float *acc = dq_acc + row * D + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+            nl = -LSE[row] * 1.4426950408889634f;
+        }
+        if (lane == 0) {
+            neg_delta[prow] = -s;
+            neg_lse2[prow] = nl;
+        }
+    }
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < acc_vec4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        reinterpret_cast<float4 *>(dq_acc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 }
 
-// dQ = bf16(dq_acc), eight elements per thread.
+// dQ = bf16(scale * accumulator), eight elements per thread.  The
+// accumulator of a head is [query tile][D/4][128 rows][4 floats], the order
+// the main kernel's vector reductions write.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dQ,
-                                                     int64_t n8) {
+                                                     int64_t rows, int N, int n_tiles, float scale) {
+    const int64_t n8 = rows * (D / 8);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float4 a = reinterpret_cast<const float4 *>(dq_acc)[2 * i];
-        const float4 b = reinterpret_cast<const float4 *>(dq_acc)[2 * i + 1];
+        const int64_t r = i / (D / 8);
+        const int g = static_cast<int>(i % (D / 8));
+        const int64_t bh = r / N;
+        const int n = static_cast<int>(r % N);
+        const int qt = n / BT, t = n % BT;
+        const float4 *tile = reinterpret_cast<const float4 *>(dq_acc + (bh * n_tiles + qt) * BT * D);
+        const float4 a = tile[(2 * g) * BT + t];
+        const float4 b = tile[(2 * g + 1) * BT + t];
         reinterpret_cast<uint4 *>(dQ)[i] =
-            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+            make_uint4(pack_bf16x2(scale * a.x, scale * a.y), pack_bf16x2(scale * a.z, scale * a.w),
+                       pack_bf16x2(scale * b.x, scale * b.y), pack_bf16x2(scale * b.z, scale * b.w));
     }
 }
 
@@ -395,8 +586,11 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         configured_device = dev;
     }
     const int64_t rows = static_cast<int64_t>(p.BH) * p.N;
-    bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(p.O), static_cast<const __nv_bfloat16 *>(p.dO), p.delta, p.dq_acc, rows);
+    const int64_t padded_rows = static_cast<int64_t>(p.BH) * p.n_tiles * BT;
+    const int64_t acc_vec4 = padded_rows * D / 4;
+    bwd_prep_kernel<D><<<static_cast<unsigned>((padded_rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(p.O), static_cast<const __nv_bfloat16 *>(p.dO), p.LSE, p.neg_delta,
+        p.neg_lse2, p.dq_acc, padded_rows, p.N, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     cudaLaunchConfig_t cfg = {};
@@ -409,7 +603,8 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     const int64_t n8 = rows * D / 8;
     int64_t blocks = (n8 + 255) / 256;
     if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
-    bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), n8);
+    bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), rows, p.N, p.n_tiles, p.scale);
     return cudaGetLastError();
 }
 

@@ -142,10 +142,21 @@ uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 extern "C" {
 
+// The fp32 dQ accumulator covers whole 128-row query tiles of every head.
+static uint64_t dq_acc_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
+    const uint64_t tiles = (static_cast<uint64_t>(N) + 127) / 128;
+    return static_cast<uint64_t>(B) * H * tiles * 128 * D * 4;
+}
+
+// One fp32 value per query row, over whole 128-row tiles of every head.
+static uint64_t row_bytes(int64_t B, int64_t H, int64_t N) {
+    return static_cast<uint64_t>(B) * H * ((static_cast<uint64_t>(N) + 127) / 128) * 128 * 4;
+}
+
 size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
     if (check_shape(B, H, N, D) != TK_OK) return 0;
-    const uint64_t rows = static_cast<uint64_t>(B) * H * N;
-    return static_cast<size_t>(round_up(rows * D * 4, kWorkspaceAlign) + round_up(rows * 4, kWorkspaceAlign));
+    return static_cast<size_t>(round_up(dq_acc_bytes(B, H, N, D), kWorkspaceAlign) +
+                               2 * round_up(row_bytes(B, H, N), kWorkspaceAlign));
 }
 
 int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
@@ -187,12 +198,14 @@ int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
     if ((rc = encode_qkv_map(&p.tmK, K, N, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmV, V, N, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmDO, dO, N, D, BH)) != TK_OK) return rc;
-    const uint64_t rows = static_cast<uint64_t>(BH) * N;
     p.O = O;
     p.dO = dO;
     p.LSE = LSE;
     p.dq_acc = static_cast<float *>(workspace);
-    p.delta = reinterpret_cast<float *>(static_cast<char *>(workspace) + round_up(rows * D * 4, kWorkspaceAlign));
+    char *ws = static_cast<char *>(workspace);
+    p.neg_delta = reinterpret_cast<float *>(ws + round_up(dq_acc_bytes(B, H, N, D), kWorkspaceAlign));
+    p.neg_lse2 = reinterpret_cast<float *>(ws + round_up(dq_acc_bytes(B, H, N, D), kWorkspaceAlign) +
+                                           round_up(row_bytes(B, H, N), kWorkspaceAlign));
     p.dQ = dQ;
     p.dK = dK;
     p.dV = dV;

@@ -38,8 +38,9 @@ struct BwdParams {
     const void *O;     // bf16 [B*H, N, D] (forward output)
     const void *dO;    // bf16 [B*H, N, D]
     const float *LSE;  // fp32 [B*H, N] (forward log-sum-exp)
-    float *delta;      // workspace: fp32 [B*H, N], <dO_i, O_i>
-    float *dq_acc;     // workspace: fp32 [B*H, N, D], dQ accumulator
+    float *neg_delta;  // workspace: fp32 [B*H, n_tiles*128], -<dO_i, O_i> (0 past N)
+    float *neg_lse2;   // workspace: fp32 [B*H, n_tiles*128], -LSE_i * log2(e) (-inf past N)
+    float *dq_acc;     // workspace: fp32 dQ accumulator, per head [n_tiles][D/4][128][4]
     void *dQ;          // bf16 [B*H, N, D]
     void *dK;
     void *dV;
