@@ -70,7 +70,10 @@ struct Layout {
     // QB_OFF + b * 2 * TILE and dO right after it.
     static constexpr uint32_t QB_OFF = V_OFF + TILE;
     static constexpr uint32_t DS_OFF = QB_OFF + 4 * TILE;   // dS^T: 128 keys x 128 queries bf16 (2 boxes)
-    static constexpr uint32_t BAR_OFF = DS_OFF + 2 * BOX;
+    // Per Q/dO buffer b, the query tile's row values: -LSE*log2(e) at
+    // RB_OFF + b * 1024 and -Delta 512 bytes further (128 floats each).
+    static constexpr uint32_t RB_OFF = DS_OFF + 2 * BOX;
+    static constexpr uint32_t BAR_OFF = RB_OFF + 2048;
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;      // + buffer (2): Q and dO loaded
     static constexpr int B_QEMPTY = 3;     // + buffer (2): the products that read them are done (MMA commit)
@@ -83,8 +86,9 @@ struct Layout {
     static constexpr int B_MMADONE = 17;
     static constexpr int NUM_BARS = 18;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
-    static constexpr uint32_t SMEM_ALLOC =
-        SMEM_USED + 1024 > 116u * 1024u ? SMEM_USED + 1024 : 116u * 1024u;  // one CTA per SM
+    // No alignment slack: the dynamic shared memory of a kernel without
+    // static shared memory starts 1024-byte aligned (the kernel checks).
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED > 116u * 1024u ? SMEM_USED : 116u * 1024u;  // one CTA per SM
     static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
     // TMEM columns; lane = key of this CTA's key tile, except dQ_part
     // (lane = query of the current query tile).
@@ -110,6 +114,14 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t box, int r, int c) {
 __device__ __forceinline__ void red_add_v4(float *addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
                  "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                 : "memory");
+}
+
+// Copies `bytes` (a multiple of 16) from global to shared memory with the
+// bulk-copy unit, completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
 
@@ -140,10 +152,12 @@ __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = Layout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
+    if (sbase & 1023u) {  // the 128-byte-swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) record_timeout(ROLE_BWD_LAYOUT << 24);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -217,11 +231,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
                 const int qt = qt_first + it;
                 const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE);
+                const uint32_t rb = sbase + L::RB_OFF + b * 1024;
+                const size_t row0 = (head_tiles + qt) * BT;
+                mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
                 for (int c = 0; c < L::KATOMS; ++c) {
                     tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
                     tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
                 }
+                bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
+                bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
                 ++issued;
             }
         }
@@ -334,11 +352,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         for (int it = 0; it < n_q; ++it) {
             const int qt = qt_first + it;
             const uint32_t ph = it & 1;
-            // -LSE*log2(e) and -Delta of this group's 64 queries (padded
-            // rows: -inf and 0, so their weights and gradients are 0)
-            const size_t row0 = (head_tiles + qt) * BT + grp * 64;
-            const float4 *nl4 = reinterpret_cast<const float4 *>(p.neg_lse2 + row0);
-            const float4 *dl4 = reinterpret_cast<const float4 *>(p.neg_delta + row0);
+            // -LSE*log2(e) and -Delta of this group's 64 queries, loaded with
+            // Q and dO (padded rows: -inf and 0, so their weights and
+            // gradients are 0)
+            const float *rows = reinterpret_cast<const float *>(smem + L::RB_OFF + (it & 1) * 1024) + grp * 64;
+            const float4 *nl4 = reinterpret_cast<const float4 *>(rows);
+            const float4 *dl4 = reinterpret_cast<const float4 *>(rows + 128);
             // Only the causal diagonal tile and a ragged last key tile hold
             // weights to zero: the queries below qmin do not see this key
             // (keys past N are seen by none).
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 const int q0 = (2 * grp + cc) * 32;
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 l4 = __ldg(nl4 + cc * 8 + e4);
+                    const float4 l4 = nl4[cc * 8 + e4];
                     float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * e4]), __uint_as_float(sr[4 * e4 + 1])),
                                            c2, make_float2(l4.x, l4.y));
                     float2 x1 = __ffma2_rn(
@@ -374,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             auto ds_chunk = [&](const uint32_t(&dr)[32], const uint32_t(&pr)[16], int cc, uint32_t(&ds)[16]) {
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 d4 = __ldg(dl4 + cc * 8 + e4);
+                    const float4 d4 = dl4[cc * 8 + e4];
                     const float2 g0 = __fadd2_rn(
                         make_float2(__uint_as_float(dr[4 * e4]), __uint_as_float(dr[4 * e4 + 1])),
                         make_float2(d4.x, d4.y));
@@ -392,17 +411,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             tc_fence_after_sync();
             {
                 const int ca = 2 * grp, cb = 2 * grp + 1;
-                uint32_t sa[32], sb[32], pp[16];
-                tmem_ld32_async(lane_base + L::T_S + ca * 32, sa);
-                tmem_ld32_async(lane_base + L::T_S + cb * 32, sb);
-                tmem_ld_wait();
-                reg_fence(sa);
-                reg_fence(sb);
-                if (masked) p_chunk(sa, 0, pp, std::true_type());
-                else p_chunk(sa, 0, pp, std::false_type());
+                uint32_t sr[32], pp[16];
+                tmem_ld32(lane_base + L::T_S + ca * 32, sr);
+                if (masked) p_chunk(sr, 0, pp, std::true_type());
+                else p_chunk(sr, 0, pp, std::false_type());
                 tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
-                if (masked) p_chunk(sb, 1, pp, std::true_type());
-                else p_chunk(sb, 1, pp, std::false_type());
+                tmem_ld32(lane_base + L::T_S + cb * 32, sr);
+                if (masked) p_chunk(sr, 1, pp, std::true_type());
+                else p_chunk(sr, 1, pp, std::false_type());
                 tmem_st16(lane_base + L::T_S + L::pcol(cb), pp);
                 tmem_st_wait();
                 tc_fence_before_sync();

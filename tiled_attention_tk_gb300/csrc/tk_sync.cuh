@@ -28,7 +28,8 @@ enum : uint32_t {
     ROLE_SELFTEST = 4,
     ROLE_BWD_PRODUCER = 5,
     ROLE_BWD_MMA = 6,
-    ROLE_BWD_COMPUTE = 7
+    ROLE_BWD_COMPUTE = 7,
+    ROLE_BWD_LAYOUT = 8  // not a wait: the backward kernel found its shared memory misaligned
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t where) {
