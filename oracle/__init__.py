@@ -14,7 +14,9 @@ Definition followed (the "ThunderKittens" attention forward as printed on
 attn_fwd_template consumer::compute / consumer::finish, and the inner-loop
 excerpt on alanwu.xyz/posts/thunderkittens):
 
-    s_ij   = scale * <Q_i, K_j>            j in J_i  (all keys, or j <= i if causal)
+    s_ij   = scale * <Q_i, K_j>            j in J_i  (all Nkv keys, or, if causal,
+                                                     j <= i + Nkv - Nq: the Nq queries
+                                                     stand at the end of the key sequence)
     LSE_i  = max_j s_ij + ln(sum_j exp(s_ij - max_j s_ij))
     O_i    = sum_j exp(s_ij - LSE_i) V_j
 """
@@ -69,6 +71,12 @@ def _declare(lib) -> None:
     lib.tkor_attn_fwd_rows.argtypes = [P, P, P, i64, i64, ctypes.c_int,
                                        ctypes.c_double, P, i64, P, P, ctypes.c_int]
     lib.tkor_attn_fwd_rows.restype = ctypes.c_int
+    lib.tkor_attn_fwd_kv.argtypes = [P, P, P, P, P, i64, i64, i64, i64, i64,
+                                     ctypes.c_int, ctypes.c_double, ctypes.c_int]
+    lib.tkor_attn_fwd_kv.restype = ctypes.c_int
+    lib.tkor_attn_fwd_kv_rows.argtypes = [P, P, P, i64, i64, i64, ctypes.c_int,
+                                          ctypes.c_double, P, i64, P, P, ctypes.c_int]
+    lib.tkor_attn_fwd_kv_rows.restype = ctypes.c_int
     lib.tkor_attn_weights.argtypes = [P, P, i64, i64, ctypes.c_int,
                                       ctypes.c_double, P]
     lib.tkor_attn_weights.restype = ctypes.c_int
@@ -109,34 +117,38 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def attn_fwd(q, k, v, causal: bool, scale: float, threads: int = 0, lib=None):
-    """Whole problem.  q, k, v: [B,H,N,D] bf16.  Returns (O, LSE) as float64
-    arrays of shapes [B,H,N,D] and [B,H,N]."""
+    """Whole problem.  q: [B,H,Nq,D], k, v: [B,H,Nkv,D] bf16 (Nq = Nkv for
+    the same-length problem).  Returns (O, LSE) as float64 arrays of shapes
+    [B,H,Nq,D] and [B,H,Nq]."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
-    if qb.ndim != 4 or qb.shape != kb.shape or qb.shape != vb.shape:
-        raise ValueError("q, k, v must share one [B,H,N,D] shape")
-    B, H, N, D = qb.shape
-    O = np.empty((B, H, N, D), dtype=np.float64)
-    L = np.empty((B, H, N), dtype=np.float64)
-    rc = (lib or _load()).tkor_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(O), _ptr(L),
-                               B, H, N, D, int(bool(causal)), float(scale), int(threads))
+    if qb.ndim != 4 or kb.shape != vb.shape or qb.shape[:2] + qb.shape[3:] != kb.shape[:2] + kb.shape[3:]:
+        raise ValueError("q [B,H,Nq,D] and k, v [B,H,Nkv,D] must agree in B, H, D")
+    B, H, Nq, D = qb.shape
+    Nkv = kb.shape[2]
+    O = np.empty((B, H, Nq, D), dtype=np.float64)
+    L = np.empty((B, H, Nq), dtype=np.float64)
+    rc = (lib or _load()).tkor_attn_fwd_kv(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(O), _ptr(L),
+                                           B, H, Nq, Nkv, D, int(bool(causal)), float(scale),
+                                           int(threads))
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return O, L
 
 
 def attn_fwd_rows(q, k, v, rows, causal: bool, scale: float, threads: int = 0):
-    """Selected query rows of ONE head.  q, k, v: [N,D] bf16; rows: int
-    indices.  Returns (O[len(rows),D], LSE[len(rows)]) as float64."""
+    """Selected query rows of ONE head.  q: [Nq,D], k, v: [Nkv,D] bf16; rows:
+    int indices into q.  Returns (O[len(rows),D], LSE[len(rows)]) as float64."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
-    if qb.ndim != 2 or qb.shape != kb.shape or qb.shape != vb.shape:
-        raise ValueError("q, k, v must share one [N,D] shape")
-    N, D = qb.shape
+    if qb.ndim != 2 or kb.shape != vb.shape or qb.shape[1] != kb.shape[1]:
+        raise ValueError("q [Nq,D] and k, v [Nkv,D] must agree in D")
+    Nq, D = qb.shape
+    Nkv = kb.shape[0]
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     O = np.empty((r.size, D), dtype=np.float64)
     L = np.empty((r.size,), dtype=np.float64)
-    rc = _load().tkor_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), N, D, int(bool(causal)),
-                                    float(scale), _ptr(r), r.size, _ptr(O), _ptr(L),
-                                    int(threads))
+    rc = _load().tkor_attn_fwd_kv_rows(_ptr(qb), _ptr(kb), _ptr(vb), Nq, Nkv, D,
+                                       int(bool(causal)), float(scale), _ptr(r), r.size,
+                                       _ptr(O), _ptr(L), int(threads))
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return O, L

@@ -9,8 +9,9 @@
  * What it computes (per batch b, head h, query row i), written out as the
  * plain definition of softmax attention with a per-row log-sum-exp:
  *
- *   J_i    = {0..N-1}            (non-causal)
- *          = {0..i}              (causal: key j may be seen by query i iff j <= i)
+ *   J_i    = {0..Nkv-1}                  (non-causal)
+ *          = {0..i + Nkv - Nq}           (causal: key j may be seen by query i iff
+ *                                          j <= i + Nkv - Nq)
  *   s_ij   = scale * sum_d Q[i,d] * K[j,d]                 for j in J_i
  *   m_i    = max_j s_ij
  *   l_i    = sum_j exp(s_ij - m_i)
@@ -28,7 +29,12 @@
  * number as exp() of the scaled score, so the definition is written with
  * exp/log here.  The pages store no LSE; the reading taken is
  * LSE = scale*max + ln(sum), in natural log.  The causal mask is not on the
- * pages; the reading taken is top-left aligned, key j <= query i.
+ * pages; the reading taken is key j <= query i when queries and keys have
+ * the same length N.  Nq queries against a longer sequence of Nkv keys
+ * (attention inference over a cache, listed among the kernels on the
+ * groovesquid.com summary of the ThunderKittens paper) place the queries at
+ * the end of the key sequence: query i stands at position i + Nkv - Nq.
+ * Causal problems need Nkv >= Nq, so that every query sees a key.
  *
  * Two passes, no streaming, no tiling, no blocking: pass 1 forms every score
  * of the row and its maximum, pass 2 forms the weights, their sum and the
@@ -54,13 +60,13 @@ static double bf16_bits_to_double(uint16_t bits) {
     return (double)f;
 }
 
-/* One query row of one head.  q: D values; K, V: N x D (double, row-major).
- * s: scratch of N doubles. */
+/* One query row of one head.  q: D values; K, V: Nkv x D (double, row-major);
+ * offset = Nkv - Nq.  s: scratch of Nkv doubles. */
 static void attention_row(const double *q, const double *K, const double *V,
-                          int64_t N, int64_t D, int causal, double scale, int64_t i,
-                          double *s, double *o_row, double *lse_out) {
-    int64_t nkeys = causal ? (i + 1) : N;
-    if (nkeys > N) nkeys = N;
+                          int64_t Nkv, int64_t D, int causal, int64_t offset, double scale,
+                          int64_t i, double *s, double *o_row, double *lse_out) {
+    int64_t nkeys = causal ? (i + offset + 1) : Nkv;
+    if (nkeys > Nkv) nkeys = Nkv;
 
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
@@ -91,10 +97,10 @@ static void attention_row(const double *q, const double *K, const double *V,
 typedef struct {
     /* one head, already widened to double */
     const double *Q, *K, *V;
-    int64_t N, D;
+    int64_t Nq, Nkv, D;
     int causal;
     double scale;
-    const int64_t *rows; /* NULL: all rows 0..N-1 */
+    const int64_t *rows; /* NULL: all rows 0..Nq-1 */
     int64_t nrows;
     double *O;   /* nrows x D */
     double *LSE; /* nrows */
@@ -104,7 +110,7 @@ typedef struct {
 
 static void *head_worker(void *arg) {
     head_job *job = (head_job *)arg;
-    double *s = (double *)malloc(sizeof(double) * (size_t)(job->N > 0 ? job->N : 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(job->Nkv > 0 ? job->Nkv : 1));
     if (!s) return NULL;
     const int64_t chunk = 8;
     for (;;) {
@@ -116,8 +122,8 @@ static void *head_worker(void *arg) {
         int64_t end = begin + chunk < job->nrows ? begin + chunk : job->nrows;
         for (int64_t r = begin; r < end; ++r) {
             int64_t i = job->rows ? job->rows[r] : r;
-            attention_row(job->Q + i * job->D, job->K, job->V, job->N, job->D, job->causal,
-                          job->scale, i, s, job->O + r * job->D, job->LSE + r);
+            attention_row(job->Q + i * job->D, job->K, job->V, job->Nkv, job->D, job->causal,
+                          job->Nkv - job->Nq, job->scale, i, s, job->O + r * job->D, job->LSE + r);
         }
     }
     free(s);
@@ -134,25 +140,25 @@ static int g_last_threads = 0;
 
 /* Computes the listed rows of one head.  Returns 0, or -1 on bad arguments or
  * allocation failure. */
-static int run_head(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, int64_t N,
-                    int64_t D, int causal, double scale, const int64_t *rows, int64_t nrows,
-                    double *O, double *LSE, int nthreads) {
-    size_t n = (size_t)N * (size_t)D;
-    double *Q = (double *)malloc(sizeof(double) * n);
-    double *K = (double *)malloc(sizeof(double) * n);
-    double *V = (double *)malloc(sizeof(double) * n);
+static int run_head(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, int64_t Nq,
+                    int64_t Nkv, int64_t D, int causal, double scale, const int64_t *rows,
+                    int64_t nrows, double *O, double *LSE, int nthreads) {
+    size_t nq = (size_t)Nq * (size_t)D, nkv = (size_t)Nkv * (size_t)D;
+    double *Q = (double *)malloc(sizeof(double) * nq);
+    double *K = (double *)malloc(sizeof(double) * nkv);
+    double *V = (double *)malloc(sizeof(double) * nkv);
     if (!Q || !K || !V) {
         free(Q); free(K); free(V);
         return -1;
     }
-    for (size_t t = 0; t < n; ++t) {
-        Q[t] = bf16_bits_to_double(Qb[t]);
+    for (size_t t = 0; t < nq; ++t) Q[t] = bf16_bits_to_double(Qb[t]);
+    for (size_t t = 0; t < nkv; ++t) {
         K[t] = bf16_bits_to_double(Kb[t]);
         V[t] = bf16_bits_to_double(Vb[t]);
     }
     head_job job;
     job.Q = Q; job.K = K; job.V = V;
-    job.N = N; job.D = D; job.causal = causal; job.scale = scale;
+    job.Nq = Nq; job.Nkv = Nkv; job.D = D; job.causal = causal; job.scale = scale;
     job.rows = rows; job.nrows = nrows; job.O = O; job.LSE = LSE;
     job.next = 0;
     pthread_mutex_init(&job.lock, NULL);
@@ -178,32 +184,51 @@ static int run_head(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, 
 /* ------------------------------------------------------------------------ */
 /* exported entry points                                                     */
 
-/* Whole problem.  Q, K, V: bf16 bits, contiguous [B,H,N,D].
- * O: double [B,H,N,D].  LSE: double [B,H,N].  nthreads <= 0: all online CPUs. */
-int tkor_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O,
-                  double *LSE, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
-                  double scale, int nthreads) {
-    if (!Q || !K || !V || !O || !LSE || B < 1 || H < 1 || N < 1 || D < 1) return -1;
+/* Whole problem.  Q: bf16 bits, contiguous [B,H,Nq,D]; K, V: [B,H,Nkv,D].
+ * O: double [B,H,Nq,D].  LSE: double [B,H,Nq].  nthreads <= 0: all online CPUs.
+ * Causal problems need Nkv >= Nq. */
+int tkor_attn_fwd_kv(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O,
+                     double *LSE, int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D,
+                     int causal, double scale, int nthreads) {
+    if (!Q || !K || !V || !O || !LSE || B < 1 || H < 1 || Nq < 1 || Nkv < 1 || D < 1) return -1;
+    if (causal && Nkv < Nq) return -1;
     g_last_threads = 0;
     for (int64_t bh = 0; bh < B * H; ++bh) {
-        size_t off = (size_t)bh * (size_t)N * (size_t)D;
-        if (run_head(Q + off, K + off, V + off, N, D, causal, scale, NULL, N, O + off,
-                     LSE + (size_t)bh * (size_t)N, nthreads))
+        size_t qoff = (size_t)bh * (size_t)Nq * (size_t)D;
+        size_t kvoff = (size_t)bh * (size_t)Nkv * (size_t)D;
+        if (run_head(Q + qoff, K + kvoff, V + kvoff, Nq, Nkv, D, causal, scale, NULL, Nq,
+                     O + qoff, LSE + (size_t)bh * (size_t)Nq, nthreads))
             return -1;
     }
     return 0;
 }
 
-/* Selected rows of one head.  Q, K, V: bf16 bits [N,D] of that head.
- * rows: nrows query indices in [0,N).  O: double [nrows,D]; LSE: double [nrows]. */
+/* The same-length problem: Nq = Nkv = N. */
+int tkor_attn_fwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O,
+                  double *LSE, int64_t B, int64_t H, int64_t N, int64_t D, int causal,
+                  double scale, int nthreads) {
+    return tkor_attn_fwd_kv(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, nthreads);
+}
+
+/* Selected rows of one head.  Q: bf16 bits [Nq,D] of that head; K, V:
+ * [Nkv,D].  rows: nrows query indices in [0,Nq).  O: double [nrows,D];
+ * LSE: double [nrows]. */
+int tkor_attn_fwd_kv_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int64_t Nq,
+                          int64_t Nkv, int64_t D, int causal, double scale, const int64_t *rows,
+                          int64_t nrows, double *O, double *LSE, int nthreads) {
+    if (!Q || !K || !V || !O || !LSE || !rows || Nq < 1 || Nkv < 1 || D < 1 || nrows < 0)
+        return -1;
+    if (causal && Nkv < Nq) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= Nq) return -1;
+    g_last_threads = 0;
+    return run_head(Q, K, V, Nq, Nkv, D, causal, scale, rows, nrows, O, LSE, nthreads);
+}
+
 int tkor_attn_fwd_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int64_t N,
                        int64_t D, int causal, double scale, const int64_t *rows,
                        int64_t nrows, double *O, double *LSE, int nthreads) {
-    if (!Q || !K || !V || !O || !LSE || !rows || N < 1 || D < 1 || nrows < 0) return -1;
-    for (int64_t r = 0; r < nrows; ++r)
-        if (rows[r] < 0 || rows[r] >= N) return -1;
-    g_last_threads = 0;
-    return run_head(Q, K, V, N, D, causal, scale, rows, nrows, O, LSE, nthreads);
+    return tkor_attn_fwd_kv_rows(Q, K, V, N, N, D, causal, scale, rows, nrows, O, LSE, nthreads);
 }
 
 /* The attention weights of one head, P[i,j] = exp(s_ij - m_i) / l_i, with

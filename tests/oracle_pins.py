@@ -11,6 +11,9 @@ Definition pinned (the "ThunderKittens" attention forward on
 attn_fwd_template consumer::compute and consumer::finish; the inner loop on
 alanwu.xyz/posts/thunderkittens): O_i = sum_j softmax_j(scale <Q_i,K_j>) V_j,
 LSE_i = ln sum_j exp(scale <Q_i,K_j>), j over all keys, or j <= i (causal).
+With Nq queries against Nkv >= Nq keys the causal queries stand at the end
+of the key sequence: j <= i + Nkv - Nq (attention inference over a cache,
+listed on the groovesquid.com summary of the ThunderKittens paper).
 """
 from __future__ import annotations
 
@@ -212,10 +215,67 @@ def check_key_shift(fwd):
         _close(L2[0, 0], L1[0, 0] + shift, 1e-12, "key shift LSE")
 
 
+# --- queries against a longer key sequence (Nq != Nkv) ------------------------
+
+def check_rect_zero_queries(fwd):
+    """Q = 0 with Nq = 7 queries over Nkv = 20 keys: every allowed key weighs
+    1/|J_i|.  Non-causal: LSE_i = ln 20 and O_i = mean of all V rows.
+    Causal, queries at the end of the key sequence: query i sees keys
+    0..i+13, so LSE_i = ln(i + 14) and O_i is the mean of V_0..V_{i+13}."""
+    B, H, Nq, Nkv, D = 1, 2, 7, 20, 16
+    _, k, v = make_qkv(B, H, Nkv, D, 6)
+    q = torch.zeros((B, H, Nq, D), dtype=torch.bfloat16)
+    vd = v.double().numpy()
+    O, L = fwd(q, k, v, False, 0.7)
+    _close(L, np.full((B, H, Nq), math.log(Nkv)), 1e-13, "rect Q=0 LSE non-causal")
+    _close(O, np.broadcast_to(vd.mean(axis=2, keepdims=True), O.shape), 1e-13,
+           "rect Q=0 output non-causal")
+    O, L = fwd(q, k, v, True, 0.7)
+    counts = np.arange(Nkv - Nq + 1, Nkv + 1, dtype=np.float64)
+    _close(L, np.broadcast_to(np.log(counts), (B, H, Nq)), 1e-13, "rect Q=0 LSE causal")
+    prefix_mean = (np.cumsum(vd, axis=2) / np.arange(1, Nkv + 1)[None, None, :, None])[:, :, Nkv - Nq:]
+    _close(O, prefix_mean, 1e-13, "rect Q=0 output causal")
+
+
+def check_rect_against_library(fwd):
+    """Non-causal Nq != Nkv (both Nq < Nkv and Nq > Nkv) against fp64 PyTorch
+    scaled_dot_product_attention and scipy's logsumexp; and one query
+    against Nkv keys under the causal mask, which sees every key, against the
+    same routines without a mask."""
+    cases = [(1, 2, 5, 23, 8, False), (2, 1, 31, 9, 16, False), (1, 1, 1, 37, 64, True),
+             (1, 2, 1, 130, 128, True)]
+    for idx, (B, H, Nq, Nkv, D, causal) in enumerate(cases):
+        q = make_qkv(B, H, Nq, D, 500 + idx)[0]
+        _, k, v = make_qkv(B, H, Nkv, D, 600 + idx)
+        scale = 1.0 / math.sqrt(D)
+        O, L = fwd(q, k, v, causal, scale)
+        qd, kd, vd = q.double(), k.double(), v.double()
+        O_ref = F.scaled_dot_product_attention(qd, kd, vd, scale=scale)
+        L_ref = logsumexp((scale * torch.matmul(qd, kd.transpose(-1, -2))).numpy(), axis=-1)
+        _close(O, O_ref.numpy(), 1e-12, f"rect O vs torch SDPA {B,H,Nq,Nkv,D,causal}")
+        _close(L, L_ref, 1e-12, f"rect LSE vs scipy logsumexp {B,H,Nq,Nkv,D,causal}")
+
+
+def check_rect_is_suffix_of_square(fwd):
+    """Causal queries at the end of the key sequence are the last Nq rows of
+    the square causal problem whose first Nkv - Nq queries are anything:
+    row i of the rectangular problem equals row i + Nkv - Nq of the square
+    one, computed with the same arithmetic (exactly equal)."""
+    B, H, Nq, Nkv, D = 1, 2, 9, 30, 16
+    _, k, v = make_qkv(B, H, Nkv, D, 71)
+    qfull = make_qkv(B, H, Nkv, D, 72)[0]
+    q = qfull[:, :, Nkv - Nq:].contiguous()
+    O, L = fwd(q, k, v, True, 0.3)
+    Of, Lf = fwd(qfull, k, v, True, 0.3)
+    _close(O, Of[:, :, Nkv - Nq:], 0.0, "rect causal rows = square causal suffix (O)")
+    _close(L, Lf[:, :, Nkv - Nq:], 0.0, "rect causal rows = square causal suffix (LSE)")
+
+
 ALL_CHECKS = [check_constant_values, check_single_key, check_causal_first_row,
               check_zero_queries, check_two_keys, check_against_library,
               check_key_permutation, check_head_independence, check_scale_homogeneity,
-              check_key_shift]
+              check_key_shift, check_rect_zero_queries, check_rect_against_library,
+              check_rect_is_suffix_of_square]
 
 
 def check_weights(weights_fn):

@@ -23,15 +23,21 @@ MUTANTS = [
     ("sign of the exponent flipped", "double p = exp(s[j] - m);", "double p = exp(m - s[j]);"),
     ("minimum instead of maximum", "s[j] = scale * dot;\n        if (s[j] > m) m = s[j];",
      "s[j] = scale * dot;\n        if (s[j] < m || j == 0) m = s[j];"),
-    ("causal mask excludes the diagonal", "int64_t nkeys = causal ? (i + 1) : N;",
-     "int64_t nkeys = causal ? (i > 0 ? i : 1) : N;"),
-    ("causal mask ignored", "int64_t nkeys = causal ? (i + 1) : N;", "int64_t nkeys = N;"),
-    ("causal mask one key too wide", "int64_t nkeys = causal ? (i + 1) : N;",
-     "int64_t nkeys = causal ? (i + 2) : N;"),
+    ("causal mask excludes the diagonal", "int64_t nkeys = causal ? (i + offset + 1) : Nkv;",
+     "int64_t nkeys = causal ? (i + offset > 0 ? i + offset : 1) : Nkv;"),
+    ("causal mask ignored", "int64_t nkeys = causal ? (i + offset + 1) : Nkv;", "int64_t nkeys = Nkv;"),
+    ("causal mask one key too wide", "int64_t nkeys = causal ? (i + offset + 1) : Nkv;",
+     "int64_t nkeys = causal ? (i + offset + 2) : Nkv;"),
+    ("causal queries placed at the start of the keys", "int64_t nkeys = causal ? (i + offset + 1) : Nkv;",
+     "int64_t nkeys = causal ? (i + 1) : Nkv;"),
+    ("causal offset sign flipped", "int64_t nkeys = causal ? (i + offset + 1) : Nkv;",
+     "int64_t nkeys = causal ? (i - offset + 1 > 0 ? i - offset + 1 : 1) : Nkv;"),
+    ("key count from the query length", "double *s = (double *)malloc(sizeof(double) * (size_t)(job->Nkv > 0 ? job->Nkv : 1));",
+     "double *s = (double *)malloc(sizeof(double) * (size_t)(job->Nkv > 0 ? job->Nkv : 1)); job->Nkv = job->Nq;"),
     ("output not normalised", "for (int64_t d = 0; d < D; ++d) o_row[d] /= l;", ""),
     ("value row of the query instead of the key", "const double *v = V + j * D;",
      "const double *v = V + i * D;"),
-    ("transposed key index", "dot += q[d] * k[d];", "dot += q[d] * K[(d % N) * D + (j % D)];"),
+    ("transposed key index", "dot += q[d] * k[d];", "dot += q[d] * K[(d % Nkv) * D + (j % D)];"),
     ("query element reused", "dot += q[d] * k[d];", "dot += q[0] * k[d];"),
     ("last key skipped", "for (int64_t j = 0; j < nkeys; ++j) {\n        double p",
      "for (int64_t j = 0; j + 1 < nkeys || (nkeys == 1 && j == 0); ++j) {\n        double p"),

@@ -26,6 +26,14 @@ def test_rows_entry_matches_whole_head(oracle_mod):
         Or, Lr = oracle_mod.attn_fwd_rows(q[0, 0], k[0, 0], v[0, 0], rows, causal, 0.125)
         assert np.array_equal(Or, O[0, 0, rows])
         assert np.array_equal(Lr, L[0, 0, rows])
+    # 130 queries at the end of 300 keys
+    qs = q[:, :, :130].contiguous()
+    rows = [0, 1, 127, 128, 129]
+    for causal in (False, True):
+        O, L = oracle_mod.attn_fwd(qs, k, v, causal, 0.125)
+        Or, Lr = oracle_mod.attn_fwd_rows(qs[0, 0], k[0, 0], v[0, 0], rows, causal, 0.125)
+        assert np.array_equal(Or, O[0, 0, rows])
+        assert np.array_equal(Lr, L[0, 0, rows])
 
 
 def test_thread_count_does_not_change_results(oracle_mod):
@@ -45,6 +53,10 @@ def test_oracle_rejects_bad_arguments(oracle_mod):
         oracle_mod.attn_fwd(z, z, np.zeros((1, 1, 5, 8), dtype=np.uint16), False, 1.0)
     with pytest.raises(RuntimeError):
         oracle_mod.attn_fwd_rows(z[0, 0], z[0, 0], z[0, 0], [4], False, 1.0)
+    # causal with fewer keys than queries: some query would see no key
+    with pytest.raises(RuntimeError):
+        oracle_mod.attn_fwd(z, z[:, :, :3].copy(), z[:, :, :3].copy(), True, 1.0)
+    oracle_mod.attn_fwd(z, z[:, :, :3].copy(), z[:, :, :3].copy(), False, 1.0)
 
 
 def test_oracle_regression_fixture(oracle_mod):
