@@ -2,7 +2,7 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..5] [--all] [--bwd]
+                    [--workload 1..6] [--all] [--bwd]
 
 One step = one tk_attn_fwd launch over the whole workload (every (b,h) head,
 every query row), inputs resident in HBM.  Default workload: B16 H32 N1024
@@ -180,13 +180,18 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
+def row_flops(w, r: int) -> float:
+    """Algorithmic flops of query row r: 4*D per key it sees."""
+    keys = min(r + 1 + w.Nkv - w.N, w.Nkv) if w.causal else w.Nkv
+    return 4.0 * keys * w.D
+
+
 def time_oracle_sample(w, q, k, v, budget_s: float, min_rows: int = 64):
     """Times the fp64 oracle on whole heads of the workload, one after another,
     until ``budget_s`` of work has been done (at least ``min_rows`` rows).
     Returns (TFLOP/s, cores, description)."""
     import oracle
     oracle.build()
-    flops_per_row_full = 4.0 * w.N * w.D  # non-causal per-row flops
     done_flops, rows_done, t_total, heads = 0.0, 0, 0.0, 0
     start = time.perf_counter()
     bh_total = w.B * w.H
@@ -202,10 +207,7 @@ def time_oracle_sample(w, q, k, v, budget_s: float, min_rows: int = 64):
         oracle.attn_fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
         dt = time.perf_counter() - t0
         t_total += dt
-        if w.causal:
-            done_flops += sum(4.0 * (r + 1) * w.D for r in rows)
-        else:
-            done_flops += flops_per_row_full * len(rows)
+        done_flops += sum(row_flops(w, r) for r in rows)
         rows_done += len(rows)
         heads += 1
         if time.perf_counter() - start >= budget_s or heads >= bh_total:
@@ -237,7 +239,10 @@ def run_ours(args, w):
     qp, kp, vp, op, lp = qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr()
 
     def step():
-        tk.fwd_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.D, w.causal, w.scale, sh)
+        if w.Nkv == w.N:
+            tk.fwd_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.D, w.causal, w.scale, sh)
+        else:
+            tk.fwd_kv_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.Nkv, w.D, w.causal, w.scale, sh)
 
     for _ in range(args.warmup):
         step()
@@ -285,7 +290,7 @@ def run_ours(args, w):
             oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
         e2e_s = max_over_ranks(e2e_s, dist_mod, dev)
-        h2d = 3 * q.numel() * q.element_size()
+        h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
         d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
         e2e = {"value": round(w.flops * ws / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -312,7 +317,7 @@ def run_ours(args, w):
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
         "config": dict(w.describe(), l2="inputs 384 MiB + output 128 MiB > 126 MiB L2, no flush"
                        if w.index == DEFAULT_WORKLOAD else
-                       ("inputs > L2, no flush" if 3 * w.B * w.H * w.N * w.D * 2 > L2_BYTES
+                       ("inputs > L2, no flush" if w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2 > L2_BYTES
                         else "inputs fit in L2: warm-L2 number")),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -443,9 +448,7 @@ def run_reference(args, w):
         start = (i * rows_per_step) % w.N
         rows = [(start + r) % w.N for r in range(rows_per_step)]
         oracle.attn_fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
-        if w.causal:
-            return sum(4.0 * (r + 1) * w.D for r in rows)
-        return 4.0 * w.N * w.D * len(rows)
+        return sum(row_flops(w, r) for r in rows)
 
     for i in range(args.warmup):
         step(i)
@@ -487,10 +490,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[1, 2, 3, 4, 5])
+    from tiled_attention_tk_gb300.inputs import WORKLOADS, Workload
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--shape", type=str, default=None,
-                    help="B,H,N,D,causal: a custom N(0,1) workload instead of a named one")
+                    help="B,H,N,D,causal[,Nkv]: a custom N(0,1) workload instead of a named one")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
@@ -503,12 +507,15 @@ def main(argv=None):
     if ws != args.gpus and ws != 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
 
-    from tiled_attention_tk_gb300.inputs import WORKLOADS, Workload
     if args.shape:
-        B, H, N, D, causal = (int(x) for x in args.shape.split(","))
-        todo = [Workload(0, B, H, N, D, bool(causal), "normal")]
+        f = [int(x) for x in args.shape.split(",")]
+        if len(f) not in (5, 6):
+            ap.error("--shape wants B,H,N,D,causal[,Nkv]")
+        todo = [Workload(0, f[0], f[1], f[2], f[3], bool(f[4]), "normal", f[5] if len(f) == 6 else None)]
     else:
-        todo = [WORKLOADS[i] for i in ([1, 2, 3, 4, 5] if args.all else [args.workload])]
+        todo = [WORKLOADS[i] for i in (sorted(WORKLOADS) if args.all else [args.workload])]
+    if args.bwd:
+        todo = [w for w in todo if w.Nkv == w.N]  # the backward takes Nq = Nkv only
     for w in todo:
         if args.impl == "reference":
             line = run_reference(args, w)

@@ -98,6 +98,26 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
                 cudaStream_t stream);
 
 /*
+ * tk_attn_fwd_kv -- the same forward for Nq queries against Nkv keys
+ * (attention inference over a cache: a block of new queries attends to every
+ * earlier key and to itself; the groovesquid.com summary of the
+ * ThunderKittens paper lists "attention inference" among its kernels).
+ *
+ * Arguments as tk_attn_fwd, except
+ *   Q, O     bf16 [B, H, Nq, D];  LSE fp32 [B, H, Nq].
+ *   K, V     bf16 [B, H, Nkv, D].
+ *   Nq, Nkv  query and key rows, each >= 1 (any values, ragged tails masked).
+ *   causal   0: every query sees every key.  1: the queries stand at the end
+ *            of the key sequence, query i at position i + Nkv - Nq, and see
+ *            keys j <= i + Nkv - Nq; needs Nkv >= Nq (else TK_ERR_BAD_SHAPE).
+ * With Nq = Nkv = N it is tk_attn_fwd.  Semantics, ownership and errors as
+ * tk_attn_fwd.
+ */
+int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                   int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal,
+                   float scale, cudaStream_t stream);
+
+/*
  * tk_attn_bwd_workspace_bytes -- device workspace tk_attn_bwd needs for a
  * problem of this shape: an fp32 dQ accumulator over whole 128-row query
  * tiles (B*H*ceil(N/128)*128*D floats) and two fp32 row values over the

@@ -77,6 +77,35 @@ def test_host_validation(kwargs, code):
     assert _call(**kwargs) == tk.STATUS[code]
 
 
+def _call_kv(q=Bq, k=Bk, v=Bv, o=Bo, l=Bl, B=1, H=1, Nq=128, Nkv=256, D=64, causal=0, scale=0.125):
+    return tk.load().tk_attn_fwd_kv(q, k, v, o, l, B, H, Nq, Nkv, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(k=None), "TK_ERR_NULL_PTR"),
+    (dict(Nq=0), "TK_ERR_BAD_SHAPE"),
+    (dict(Nkv=0), "TK_ERR_BAD_SHAPE"),
+    (dict(Nkv=2**31), "TK_ERR_BAD_SHAPE"),
+    (dict(Nq=300, Nkv=200, causal=1), "TK_ERR_BAD_SHAPE"),  # a causal query would see no key
+    (dict(D=32), "TK_ERR_UNSUPPORTED_D"),
+    (dict(causal=3), "TK_ERR_BAD_FLAG"),
+    (dict(scale=-0.5), "TK_ERR_BAD_SCALE"),
+    (dict(v=Bv + 4), "TK_ERR_MISALIGNED"),
+    (dict(o=Bk + 0x4000), "TK_ERR_ALIAS"),        # inside K: 256 keys x 64 x 2 B = 32 KB
+    (dict(l=Bq + 0x2000), "TK_ERR_ALIAS"),        # inside Q: 128 x 64 x 2 B = 16 KB
+])
+def test_host_validation_kv(kwargs, code):
+    assert _call_kv(**kwargs) == tk.STATUS[code]
+
+
+def test_kv_validation_sizes_by_each_length():
+    """K ends 32 KB after its start for Nkv = 256; an O placed just past it
+    is accepted by validation (it then stops at the device-memory check,
+    since the addresses are fake)."""
+    rc = _call_kv(o=Bk + 256 * 64 * 2)
+    assert rc != tk.STATUS["TK_ERR_ALIAS"]
+
+
 def test_validation_order_null_before_shape():
     assert _call(q=None, N=0) == tk.STATUS["TK_ERR_NULL_PTR"]
 

@@ -2,12 +2,13 @@
 
 ``fwd(q, k, v, causal, scale) -> (O, LSE)`` computes, per (batch, head),
 O = softmax(scale QK^T [+ causal mask]) V and the natural-log row
-log-sum-exp in one CUDA kernel (TMA producer, tcgen05 MMAs into tensor
+log-sum-exp (queries and keys of equal length, or Nq queries at the end of
+Nkv keys) in one CUDA kernel (TMA producer, tcgen05 MMAs into tensor
 memory, online softmax), through the C ABI declared in include/tk_attn.h.
 PyTorch only provides device memory and streams.
 """
 from ._lib import STATUS, STATUS_NAMES, TkError, library_path, load, strerror
-from .attention import bwd, bwd_workspace_bytes, device_status, fwd, fwd_raw, selftest_timeout
+from .attention import bwd, bwd_workspace_bytes, device_status, fwd, fwd_kv_raw, fwd_raw, selftest_timeout
 
-__all__ = ["fwd", "fwd_raw", "bwd", "bwd_workspace_bytes", "device_status", "selftest_timeout", "TkError", "STATUS",
+__all__ = ["fwd", "fwd_raw", "fwd_kv_raw", "bwd", "bwd_workspace_bytes", "device_status", "selftest_timeout", "TkError", "STATUS",
            "STATUS_NAMES", "library_path", "load", "strerror"]

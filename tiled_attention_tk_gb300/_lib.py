@@ -24,6 +24,7 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 _P, _I64, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_uint64
 SIGNATURES = {
     "tk_attn_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
+    "tk_attn_fwd_kv": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
     "tk_attn_bwd_workspace_bytes": ([_I64, _I64, _I64, _I64], ctypes.c_size_t),
     "tk_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64,
                      _I, _F, _P], _I),

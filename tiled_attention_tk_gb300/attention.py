@@ -24,14 +24,25 @@ def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int
     _lib.check(rc, "tk_attn_fwd")
 
 
+def fwd_kv_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+               Nq: int, Nkv: int, D: int, causal: bool, scale: float, stream_handle: int) -> None:
+    """tk_attn_fwd_kv on raw device pointers; raises TkError on a non-zero status."""
+    rc = _lib.load().tk_attn_fwd_kv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nkv, D,
+                                    int(bool(causal)), float(scale), stream_handle)
+    _lib.check(rc, "tk_attn_fwd_kv")
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: float | None = None, out: torch.Tensor | None = None,
         lse: torch.Tensor | None = None, stream=None):
     """Fused attention forward.
 
-    q, k, v: bf16 [B, H, N, D], D in {64, 128}.  Returns (O bf16 [B,H,N,D],
-    LSE fp32 [B,H,N]) with O = softmax(scale QK^T [+causal]) V and LSE the
-    natural-log row log-sum-exp.  ``scale`` defaults to 1/sqrt(D).
+    q: bf16 [B, H, Nq, D]; k, v: bf16 [B, H, Nkv, D] (Nkv = Nq usually), D
+    in {64, 128}.  Returns (O bf16 [B,H,Nq,D], LSE fp32 [B,H,Nq]) with
+    O = softmax(scale QK^T [+causal]) V and LSE the natural-log row
+    log-sum-exp.  Under the causal mask the queries stand at the end of the
+    key sequence (query i sees keys j <= i + Nkv - Nq; needs Nkv >= Nq).
+    ``scale`` defaults to 1/sqrt(D).
 
     CUDA inputs: the kernel is enqueued on ``stream`` (default: the current
     stream) and the call returns without synchronising.  CPU inputs (ideally
@@ -44,11 +55,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
             raise TypeError(f"{n} must be bfloat16")
         if t.dim() != 4:
             raise ValueError(f"{n} must be [B, H, N, D]")
-    if q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must have the same shape")
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,D] and k, v [B,H,Nkv,D] must agree in B, H, D")
     if not (q.device == k.device == v.device):
         raise ValueError("q, k, v must be on one device")
     B, H, N, D = q.shape
+    Nkv = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
 
@@ -67,8 +79,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
     with torch.cuda.device(q.device):
-        fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                B, H, N, D, causal, scale, _stream_handle(stream))
+        if Nkv == N:
+            fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, N, D, causal, scale, _stream_handle(stream))
+        else:
+            fwd_kv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, Nkv, D, causal, scale, _stream_handle(stream))
     return out, lse
 
 

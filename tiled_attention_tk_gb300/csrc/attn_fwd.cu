@@ -123,9 +123,12 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
     return round * grid + ((round & 1) ? grid - 1 - cta : cta);
 }
 
-// Key tiles Q tile `qt` must visit.
+// Key tiles Q tile `qt` must visit: all of them, or under the causal mask
+// those up to the last key its last row sees (row + offset).
 __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
-    return p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
+    if (!p.causal) return p.n_kvtiles;
+    const int last_key = min(qt * BM + BM, p.Nq) - 1 + p.offset;
+    return min(last_key / BN + 1, p.n_kvtiles);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -379,10 +382,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 float s[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
-                if (j == n_kv - 1) {
-                    // Last key tile of this Q tile: the ragged tail (keys >= N)
-                    // and, under the causal mask, keys past the row take -inf.
-                    const int limit = p.causal ? min(row + 1, p.N) : p.N;
+                if (j == n_kv - 1 || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
+                    // A key tile that some row of this Q tile does not see in
+                    // full: the ragged tail (keys >= Nkv) and, under the
+                    // causal mask, keys past row + offset take -inf.
+                    const int limit = p.causal ? min(row + 1 + p.offset, p.Nkv) : p.Nkv;
                     const int kmax = limit - j * BN;
 #pragma unroll
                     for (int i = 0; i < BN; ++i) s[i] = (i < kmax) ? s[i] : -INFINITY;
@@ -487,7 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     tma_store_commit();
                 }
             }
-            if (row < p.N) p.LSE[static_cast<size_t>(u.bh) * p.N + row] = m_ref * p.scale + logf(l);
+            if (row < p.Nq) p.LSE[static_cast<size_t>(u.bh) * p.Nq + row] = m_ref * p.scale + logf(l);
         }
         if (t == 0) tma_store_wait_all();  // every store of this warpgroup has landed
     }

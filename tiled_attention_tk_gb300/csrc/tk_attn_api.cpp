@@ -220,28 +220,34 @@ int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
     return TK_OK;
 }
 
-int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
-                int64_t H, int64_t N, int64_t D, int causal, float scale, cudaStream_t stream) {
+int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                   int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal, float scale,
+                   cudaStream_t stream) {
     // ---- host-side validation: nothing is enqueued unless all of it passes
     if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
-    if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
+    if (B < 1 || H < 1 || Nq < 1 || Nkv < 1) return TK_ERR_BAD_SHAPE;
     if (D != 64 && D != 128) return TK_ERR_UNSUPPORTED_D;
     // TMA coordinates and the launch grid are 32-bit.
-    if (N > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
+    if (Nq > INT32_MAX || Nkv > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
     const int64_t BH = B * H;
-    if (BH > INT64_MAX / N / D / 2) return TK_ERR_BAD_SHAPE;
-    const int64_t n_tiles = (N + 127) / 128;
-    if (n_tiles * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    const int64_t Nmax = Nq > Nkv ? Nq : Nkv;
+    if (BH > INT64_MAX / Nmax / D / 2) return TK_ERR_BAD_SHAPE;
+    const int64_t n_qtiles = (Nq + 127) / 128;
+    const int64_t n_kvtiles = (Nkv + 127) / 128;
+    if (n_qtiles * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
     if (causal != 0 && causal != 1) return TK_ERR_BAD_FLAG;
+    // Causal queries stand at the end of the key sequence; each must see a key.
+    if (causal && Nkv < Nq) return TK_ERR_BAD_SHAPE;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return TK_ERR_BAD_SCALE;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
         return TK_ERR_MISALIGNED;
-    const uint64_t tensor_bytes = static_cast<uint64_t>(BH) * N * D * 2;
-    const uint64_t lse_bytes = static_cast<uint64_t>(BH) * N * 4;
-    if (overlaps(O, tensor_bytes, Q, tensor_bytes) || overlaps(O, tensor_bytes, K, tensor_bytes) ||
-        overlaps(O, tensor_bytes, V, tensor_bytes) || overlaps(LSE, lse_bytes, Q, tensor_bytes) ||
-        overlaps(LSE, lse_bytes, K, tensor_bytes) || overlaps(LSE, lse_bytes, V, tensor_bytes) ||
-        overlaps(LSE, lse_bytes, O, tensor_bytes))
+    const uint64_t q_bytes = static_cast<uint64_t>(BH) * Nq * D * 2;
+    const uint64_t kv_bytes = static_cast<uint64_t>(BH) * Nkv * D * 2;
+    const uint64_t lse_bytes = static_cast<uint64_t>(BH) * Nq * 4;
+    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+        overlaps(O, q_bytes, V, kv_bytes) || overlaps(LSE, lse_bytes, Q, q_bytes) ||
+        overlaps(LSE, lse_bytes, K, kv_bytes) || overlaps(LSE, lse_bytes, V, kv_bytes) ||
+        overlaps(LSE, lse_bytes, O, q_bytes))
         return TK_ERR_ALIAS;
 
     int num_sms = 0;
@@ -252,24 +258,31 @@ int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE
         if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
 
     tk::AttnParams p;
-    if ((rc = encode_qkv_map(&p.tmQ, Q, N, D, BH)) != TK_OK) return rc;
-    if ((rc = encode_qkv_map(&p.tmK, K, N, D, BH)) != TK_OK) return rc;
-    if ((rc = encode_qkv_map(&p.tmV, V, N, D, BH)) != TK_OK) return rc;
-    if ((rc = encode_qkv_map(&p.tmO, O, N, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmQ, Q, Nq, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmK, K, Nkv, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmV, V, Nkv, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmO, O, Nq, D, BH)) != TK_OK) return rc;
     p.O = O;
     p.LSE = LSE;
-    p.N = static_cast<int>(N);
+    p.Nq = static_cast<int>(Nq);
+    p.Nkv = static_cast<int>(Nkv);
+    p.offset = static_cast<int>(Nkv - Nq);
     p.BH = static_cast<int>(BH);
     p.causal = causal;
-    p.n_qtiles = static_cast<int>(n_tiles);
-    p.n_kvtiles = static_cast<int>(n_tiles);
-    p.n_pairs = static_cast<int>((n_tiles + 1) / 2);
+    p.n_qtiles = static_cast<int>(n_qtiles);
+    p.n_kvtiles = static_cast<int>(n_kvtiles);
+    p.n_pairs = static_cast<int>((n_qtiles + 1) / 2);
     p.scale = scale;
     p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
     cudaError_t e = tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
+}
+
+int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                int64_t H, int64_t N, int64_t D, int causal, float scale, cudaStream_t stream) {
+    return tk_attn_fwd_kv(Q, K, V, O, LSE, B, H, N, N, D, causal, scale, stream);
 }
 
 int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void *O, const void *dO,

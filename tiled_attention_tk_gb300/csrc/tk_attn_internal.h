@@ -13,17 +13,19 @@ namespace tk {
 // as a __grid_constant__ kernel parameter (the tensor maps must stay in
 // parameter space for TMA).
 struct AttnParams {
-    CUtensorMap tmQ;  // 3-D {D, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
-    CUtensorMap tmK;
+    CUtensorMap tmQ;  // 3-D {D, Nq, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK;  // 3-D {D, Nkv, B*H}, same box and swizzle
     CUtensorMap tmV;
-    CUtensorMap tmO;  // same view of O, for TMA stores
-    void *O;          // bf16 [B*H, N, D]
-    float *LSE;       // fp32 [B*H, N]
-    int N;            // sequence length
+    CUtensorMap tmO;  // the view of Q for O, for TMA stores
+    void *O;          // bf16 [B*H, Nq, D]
+    float *LSE;       // fp32 [B*H, Nq]
+    int Nq;           // query rows
+    int Nkv;          // key / value rows
+    int offset;       // Nkv - Nq: causal query i sees keys j <= i + offset
     int BH;           // B * H
     int causal;       // 0 / 1
-    int n_qtiles;     // ceil(N / 128)
-    int n_kvtiles;    // ceil(N / 128)
+    int n_qtiles;     // ceil(Nq / 128)
+    int n_kvtiles;    // ceil(Nkv / 128)
     int n_pairs;      // ceil(n_qtiles / 2): work units per head
     float scale;      // multiplier of Q K^T
     float scale_log2e;  // scale * log2(e): the exp2-domain factor

@@ -9,8 +9,8 @@ fp32 and rounded to bf16 (round to nearest even) with ``.to(torch.bfloat16)``.
 Q, K and V of workload ``c`` take seeds ``1000*c + 0``, ``+1`` and ``+2``.
 Layout: contiguous ``[B, H, N, D]``.
 
-The five workloads below are the attention-forward shapes this library is
-measured on; the pages that describe the method print no shapes of their own
+The workloads below are the attention-forward shapes this library is
+measured on (the sixth: queries against a longer key sequence); the pages that describe the method print no shapes of their own
 besides head dims 64 and 128 (the "ThunderKittens" attention kernel on
 10100.com/article/71410160, section "writing a kernel with TK",
 attn_fwd_layout).
@@ -32,6 +32,11 @@ class Workload:
     D: int
     causal: bool
     dist: str  # "normal": Q,K,V ~ N(0,1); "wide": Q,K ~ N(0,3^2), V ~ U(-1,1)
+    kv_len: int | None = None  # key/value rows when they differ from the N query rows
+
+    @property
+    def Nkv(self) -> int:
+        return self.N if self.kv_len is None else self.kv_len
 
     @property
     def scale(self) -> float:
@@ -39,22 +44,27 @@ class Workload:
 
     @property
     def name(self) -> str:
-        return (f"B{self.B}H{self.H}N{self.N}D{self.D}"
+        kv = f"Nkv{self.Nkv}" if self.Nkv != self.N else ""
+        return (f"B{self.B}H{self.H}N{self.N}{kv}D{self.D}"
                 f"{'-causal' if self.causal else ''}{'-wide' if self.dist == 'wide' else ''}")
 
     @property
     def flops(self) -> float:
-        """Algorithmic flops of the two contractions: 4*B*H*N^2*D, halved for
-        the causal mask (masked products are not counted)."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.D
-        return f / 2.0 if self.causal else f
+        """Algorithmic flops of the two contractions: 4*B*H*N*Nkv*D, with the
+        causal mask 4*B*H*D*(N*(Nkv-N) + N^2/2) (masked products are not
+        counted; for Nkv = N that is half of the unmasked count)."""
+        if self.causal:
+            return 4.0 * self.B * self.H * self.D * (self.N * (self.Nkv - self.N) + self.N * self.N / 2.0)
+        return 4.0 * self.B * self.H * self.N * self.Nkv * self.D
 
     def describe(self) -> dict:
-        return {"workload": self.name, "B": self.B, "H": self.H, "N": self.N, "D": self.D,
-                "causal": self.causal,
+        d = {"workload": self.name, "B": self.B, "H": self.H, "N": self.N}
+        if self.Nkv != self.N:
+            d["Nkv"] = self.Nkv
+        return dict(d, **{"D": self.D, "causal": self.causal,
                 "dist": ("Q,K,V~N(0,1)" if self.dist == "normal"
                          else "Q,K~N(0,3^2), V~U(-1,1)"),
-                "scale": f"1/sqrt({self.D})"}
+                "scale": f"1/sqrt({self.D})"})
 
 
 WORKLOADS = {
@@ -63,6 +73,9 @@ WORKLOADS = {
     3: Workload(3, 4, 16, 4096, 128, True, "normal"),
     4: Workload(4, 16, 32, 1024, 128, False, "wide"),
     5: Workload(5, 1, 32, 16384, 128, True, "normal"),
+    # 2048 new queries at the end of a 16384-key sequence (attention
+    # inference over a cache)
+    6: Workload(6, 1, 32, 2048, 128, True, "normal", kv_len=16384),
 }
 
 
@@ -94,8 +107,24 @@ def make_qkv(B: int, H: int, N: int, D: int, seed_base: int, dist: str = "normal
     raise ValueError(dist)
 
 
+def make_qkv_rect(B: int, H: int, Nq: int, Nkv: int, D: int, seed_base: int, dist: str = "normal"):
+    """Q [B,H,Nq,D] and K, V [B,H,Nkv,D], contiguous bf16 CPU tensors, drawn
+    like make_qkv (same seeds and distributions)."""
+    if dist == "normal":
+        return (_draw((B, H, Nq, D), seed_base + 0, "normal"),
+                _draw((B, H, Nkv, D), seed_base + 1, "normal"),
+                _draw((B, H, Nkv, D), seed_base + 2, "normal"))
+    if dist == "wide":
+        return (_draw((B, H, Nq, D), seed_base + 0, "normal", 3.0),
+                _draw((B, H, Nkv, D), seed_base + 1, "normal", 3.0),
+                _draw((B, H, Nkv, D), seed_base + 2, "uniform"))
+    raise ValueError(dist)
+
+
 def workload_inputs(w: Workload):
-    """The seeded inputs of one of the five named workloads."""
+    """The seeded inputs of one of the named workloads."""
+    if w.Nkv != w.N:
+        return make_qkv_rect(w.B, w.H, w.N, w.Nkv, w.D, 1000 * w.index, w.dist)
     return make_qkv(w.B, w.H, w.N, w.D, 1000 * w.index, w.dist)
 
 
