@@ -530,62 +530,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
     }
 }
 
-// Per padded query row (n_tiles * 128 rows per head, one warp per row):
-// -Delta = -<dO, O> in fp32 and -LSE * log2(e); rows past N get 0 and -inf.
-// Also zeroes the dQ accumulator (acc_vec4 float4s, grid-stride).
+// Per padded query row (n_tiles * 128 rows per head): -Delta = -<dO, O> in
+// fp32 and -LSE * log2(e); rows past N get 0 and -inf.  D/8 lanes share a
+// row, 16 bytes of O and of dO each.  Also zeroes the dQ accumulator
+// (acc_vec4 float4s, grid-stride).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ LSE, float *__restrict__ neg_delta,
                                                       float *__restrict__ neg_lse2, float *__restrict__ dq_acc,
                                                       int64_t padded_rows, int N, int n_tiles, int64_t acc_vec4) {
-    const int64_t prow = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (prow < padded_rows) {
-        const int64_t bh = prow / (static_cast<int64_t>(n_tiles) * BT);
-        const int n = static_cast<int>(prow % (static_cast<int64_t>(n_tiles) * BT));
-        float s = 0.0f, nl = -INFINITY;
-        if (n < N) {
-            const int64_t row = bh * N + n;
-            constexpr int PER = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
-            const __nv_bfloat16 *o = O + row * D + lane * PER;
-            const __nv_bfloat16 *g = dO + row * D + lane * PER;
+    constexpr int LPR = D / 8;            // lanes per row
+    constexpr int RPB = 256 / LPR;        // rows per block
+    const int64_t prow = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / LPR;
+    const int sub = threadIdx.x % LPR;
+    const bool live = prow < padded_rows;
+    const int64_t bh = prow / (static_cast<int64_t>(n_tiles) * BT);
+    const int n = static_cast<int>(prow % (static_cast<int64_t>(n_tiles) * BT));
+    float s = 0.0f;
+    if (live && n < N) {
+        const int64_t row = bh * N + n;
+        const uint4 o = reinterpret_cast<const uint4 *>(O + row * D)[sub];
+        const uint4 g = reinterpret_cast<const uint4 *>(dO + row * D)[sub];
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-            for (int e = 0; e < PER; ++e) s = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), s);
+        for (int e = 0; e < 4; ++e) {
+            const float2 a = unpack_bf16x2(ow[e]), c = unpack_bf16x2(gw[e]);
+            s = fmaf(a.x, c.x, s);
+            s = fmaf(a.y, c.y, s);
+        }
+    }
+    // every lane of the warp takes part in the reduction
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-            nl = -LSE[row] * 1.4426950408889634f;
-        }
-        if (lane == 0) {
-            neg_delta[prow] = -s;
-            neg_lse2[prow] = nl;
-        }
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    if (live && sub == 0) {
+        neg_delta[prow] = -s;
+        neg_lse2[prow] = n < N ? -LSE[bh * N + n] * 1.4426950408889634f : -INFINITY;
     }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < acc_vec4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         reinterpret_cast<float4 *>(dq_acc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 }
 
-// dQ = bf16(scale * accumulator), eight elements per thread.  The
-// accumulator of a head is [query tile][D/4][128 rows][4 floats], the order
-// the main kernel's vector reductions write.
+// dQ = bf16(scale * accumulator), one 128-row query tile per block.  The
+// accumulator of a tile is [D/4][128 rows][4 floats] (the order the main
+// kernel's vector reductions write): it is read with consecutive threads on
+// consecutive rows, turned into bf16 rows in shared memory, and written out
+// row by row, so both sides are coalesced.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dQ,
-                                                     int64_t rows, int N, int n_tiles, float scale) {
-    const int64_t n8 = rows * (D / 8);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / (D / 8);
-        const int g = static_cast<int>(i % (D / 8));
-        const int64_t bh = r / N;
-        const int n = static_cast<int>(r % N);
-        const int qt = n / BT, t = n % BT;
-        const float4 *tile = reinterpret_cast<const float4 *>(dq_acc + (bh * n_tiles + qt) * BT * D);
-        const float4 a = tile[(2 * g) * BT + t];
-        const float4 b = tile[(2 * g + 1) * BT + t];
-        reinterpret_cast<uint4 *>(dQ)[i] =
-            make_uint4(pack_bf16x2(scale * a.x, scale * a.y), pack_bf16x2(scale * a.z, scale * a.w),
-                       pack_bf16x2(scale * b.x, scale * b.y), pack_bf16x2(scale * b.z, scale * b.w));
+                                                     int N, int n_tiles, float scale) {
+    constexpr int STRIDE = D / 2 + 1;  // 32-bit words per staged row (odd: no bank conflicts)
+    __shared__ uint32_t rows[BT * STRIDE];
+    const int64_t tile = blockIdx.x;   // bh * n_tiles + qt
+    const float4 *acc = reinterpret_cast<const float4 *>(dq_acc + tile * BT * D);
+    for (int i = threadIdx.x; i < BT * (D / 4); i += blockDim.x) {
+        const int t = i % BT, grp = i / BT;
+        const float4 a = acc[i];  // columns 4*grp .. 4*grp+3 of row t
+        rows[t * STRIDE + 2 * grp] = pack_bf16x2(scale * a.x, scale * a.y);
+        rows[t * STRIDE + 2 * grp + 1] = pack_bf16x2(scale * a.z, scale * a.w);
+    }
+    __syncthreads();
+    const int qt = static_cast<int>(tile % n_tiles);
+    const int64_t bh = tile / n_tiles;
+    for (int i = threadIdx.x; i < BT * (D / 8); i += blockDim.x) {
+        const int t = i / (D / 8), g = i % (D / 8);
+        const int n = qt * BT + t;
+        if (n >= N) continue;
+        const uint32_t *r = rows + t * STRIDE + 4 * g;
+        reinterpret_cast<uint4 *>(dQ + (bh * N + n) * D)[g] = make_uint4(r[0], r[1], r[2], r[3]);
     }
 }
 
@@ -601,10 +614,10 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         if (err != cudaSuccess) return err;
         configured_device = dev;
     }
-    const int64_t rows = static_cast<int64_t>(p.BH) * p.N;
     const int64_t padded_rows = static_cast<int64_t>(p.BH) * p.n_tiles * BT;
     const int64_t acc_vec4 = padded_rows * D / 4;
-    bwd_prep_kernel<D><<<static_cast<unsigned>((padded_rows + 7) / 8), 256, 0, stream>>>(
+    constexpr int RPB = 256 / (D / 8);  // rows per prep block
+    bwd_prep_kernel<D><<<static_cast<unsigned>((padded_rows + RPB - 1) / RPB), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(p.O), static_cast<const __nv_bfloat16 *>(p.dO), p.LSE, p.neg_delta,
         p.neg_lse2, p.dq_acc, padded_rows, p.N, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -616,11 +629,8 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     cfg.stream = stream;
     if ((err = cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D>, p)) != cudaSuccess) return err;
 
-    const int64_t n8 = rows * D / 8;
-    int64_t blocks = (n8 + 255) / 256;
-    if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
-    bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), rows, p.N, p.n_tiles, p.scale);
+    bwd_dq_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.n_tiles), 256, 0, stream>>>(
+        p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), p.N, p.n_tiles, p.scale);
     return cudaGetLastError();
 }
 
