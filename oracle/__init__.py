@@ -1,6 +1,7 @@
 """fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
 
-This package is the checker, not the product.  Only ``tests/``,
+This package is the checker, not the product (attention forward and backward,
+and the plain GEMM the same tile pipeline runs).  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may load
 it.  It shares no code with the CUDA library and imports nothing from it.
 
@@ -83,6 +84,10 @@ def _declare(lib) -> None:
     lib.tkor_attn_bwd.argtypes = [P, P, P, P, P, P, P, i64, i64, i64, i64,
                                   ctypes.c_int, ctypes.c_double, ctypes.c_int]
     lib.tkor_attn_bwd.restype = ctypes.c_int
+    lib.tkor_gemm.argtypes = [P, P, P, i64, i64, i64, ctypes.c_int, ctypes.c_int]
+    lib.tkor_gemm.restype = ctypes.c_int
+    lib.tkor_gemm_rows.argtypes = [P, P, i64, i64, i64, ctypes.c_int, P, i64, P, ctypes.c_int]
+    lib.tkor_gemm_rows.restype = ctypes.c_int
     lib.tkor_last_threads.argtypes = []
     lib.tkor_last_threads.restype = ctypes.c_int
 
@@ -186,6 +191,31 @@ def attn_bwd(q, k, v, do, causal: bool, scale: float, threads: int = 0, lib=None
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return dQ, dK, dV
+
+
+def gemm(a, b, b_kmajor: bool = True, rows=None, threads: int = 0, lib=None) -> np.ndarray:
+    """C = a @ b.T (b_kmajor: b is [N,K]) or a @ b (b is [K,N]) in fp64 from
+    the bf16 inputs; ``rows``: only those rows of C.  Returns float64
+    [len(rows) or M, N]."""
+    ab, bb = _bits(a), _bits(b)
+    if ab.ndim != 2 or bb.ndim != 2:
+        raise ValueError("a and b must be 2-D")
+    M, K = ab.shape
+    N, Kb = (bb.shape if b_kmajor else bb.shape[::-1])
+    if Kb != K:
+        raise ValueError("inner dimensions differ")
+    lib = lib or _load()
+    if rows is None:
+        C = np.empty((M, N), dtype=np.float64)
+        rc = lib.tkor_gemm(_ptr(ab), _ptr(bb), _ptr(C), M, N, K, int(bool(b_kmajor)), int(threads))
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        C = np.empty((r.size, N), dtype=np.float64)
+        rc = lib.tkor_gemm_rows(_ptr(ab), _ptr(bb), M, N, K, int(bool(b_kmajor)), _ptr(r), r.size,
+                                _ptr(C), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return C
 
 
 def last_threads() -> int:

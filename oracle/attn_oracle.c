@@ -44,6 +44,9 @@
  * Parallelism: independent rows are handed to POSIX threads; each row is
  * computed by exactly one thread with the same loop order, so the result
  * does not depend on the thread count.
+ *
+ * The file also holds the backward's chain rule and the plain GEMM that the
+ * same tile pipeline runs (at the end).
  */
 #include <math.h>
 #include <pthread.h>
@@ -410,4 +413,87 @@ int tkor_attn_bwd(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, co
     }
     free(buf); free(dKp); free(dVp); free(jobs); free(tid);
     return 0;
+}
+
+/* ======================================================================== */
+/* GEMM: C = A op(B), the second workload of the same tile pipeline          */
+/*                                                                          */
+/* The pages name GEMM as the workload the tile abstractions are built      */
+/* around (10100.com/article/71410160, section on grid-level abstraction).  */
+/* Definition, fp64 from the exact bf16 inputs, one plain dot product per   */
+/* output element in k order:                                               */
+/*   C[m,n] = sum_k A[m,k] * B'[k,n],  B' = B^T (B stored [N,K], b_kmajor)  */
+/*                                     or B (B stored [K,N]).               */
+
+typedef struct {
+    const uint16_t *A, *B;
+    int64_t M, N, K;
+    int b_kmajor;
+    const int64_t *rows; /* NULL: rows 0..M-1 */
+    int64_t nrows;
+    double *C;           /* nrows x N */
+    int64_t next;
+    pthread_mutex_t lock;
+} gemm_job;
+
+static void gemm_row(const gemm_job *job, int64_t m, double *c_row) {
+    const int64_t N = job->N, K = job->K;
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = bf16_bits_to_double(job->A[m * K + k]);
+            double b = job->b_kmajor ? bf16_bits_to_double(job->B[n * K + k])
+                                     : bf16_bits_to_double(job->B[k * N + n]);
+            acc += a * b;
+        }
+        c_row[n] = acc;
+    }
+}
+
+static void *gemm_worker(void *arg) {
+    gemm_job *job = (gemm_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        int64_t r = job->next++;
+        pthread_mutex_unlock(&job->lock);
+        if (r >= job->nrows) break;
+        int64_t m = job->rows ? job->rows[r] : r;
+        gemm_row(job, m, job->C + r * job->N);
+    }
+    return NULL;
+}
+
+/* Selected rows of C (rows == NULL: all M rows).  A: bf16 bits [M,K];
+ * B: [N,K] if b_kmajor else [K,N].  C: double [nrows, N]. */
+int tkor_gemm_rows(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K,
+                   int b_kmajor, const int64_t *rows, int64_t nrows, double *C, int nthreads) {
+    if (!A || !B || !C || M < 1 || N < 1 || K < 1 || nrows < 0) return -1;
+    if (b_kmajor != 0 && b_kmajor != 1) return -1;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= M) return -1;
+    gemm_job job;
+    job.A = A; job.B = B; job.M = M; job.N = N; job.K = K; job.b_kmajor = b_kmajor;
+    job.rows = rows; job.nrows = nrows; job.C = C; job.next = 0;
+    pthread_mutex_init(&job.lock, NULL);
+    g_last_threads = 0;
+    int T = resolve_threads(nthreads);
+    if ((int64_t)T > nrows) T = (int)(nrows > 0 ? nrows : 1);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)T);
+    int started = 0;
+    for (int t = 1; tid && t < T; ++t) {
+        if (pthread_create(&tid[started], NULL, gemm_worker, &job) != 0) break;
+        ++started;
+    }
+    g_last_threads = started + 1;
+    gemm_worker(&job);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    free(tid);
+    pthread_mutex_destroy(&job.lock);
+    return 0;
+}
+
+int tkor_gemm(const uint16_t *A, const uint16_t *B, double *C, int64_t M, int64_t N, int64_t K,
+              int b_kmajor, int nthreads) {
+    return tkor_gemm_rows(A, B, M, N, K, b_kmajor, NULL, M, C, nthreads);
 }

@@ -107,3 +107,34 @@ def test_bwd_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
         except AssertionError as e:
             caught.append((check.__name__, str(e)[:80]))
     assert caught, f"no backward pin caught the planted mistake: {name}"
+
+
+from tests import oracle_gemm_pins as gemm_pins  # noqa: E402
+
+GEMM_MUTANTS = [
+    ("B index transposed for [N,K]", "bf16_bits_to_double(job->B[n * K + k])",
+     "bf16_bits_to_double(job->B[k * N + n])"),
+    ("B index transposed for [K,N]", "bf16_bits_to_double(job->B[k * N + n]);",
+     "bf16_bits_to_double(job->B[n * K + k]);"),
+    ("last k dropped", "for (int64_t k = 0; k < K; ++k) {\n            double a",
+     "for (int64_t k = 0; k + 1 < K || K == 1; ++k) {\n            double a"),
+    ("accumulator not reset per element", "        double acc = 0.0;\n        for (int64_t k",
+     "        static double acc = 0.0;\n        for (int64_t k"),
+    ("A row index from n", "double a = bf16_bits_to_double(job->A[m * K + k]);",
+     "double a = bf16_bits_to_double(job->A[(n % job->M) * K + k]);"),
+    ("layout flag ignored", "double b = job->b_kmajor ?", "double b = 1 ?"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mutant", GEMM_MUTANTS, ids=[m[0] for m in GEMM_MUTANTS])
+def test_gemm_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation anchor for '{name}' not unique in the oracle"
+    lib = oracle.bind(_compile(text.replace(orig, mutant), tmp_path, "g" + str(abs(hash(name)))))
+    caught = []
+    for check in gemm_pins.GEMM_CHECKS:
+        try:
+            check(lambda a, b, km, rows=None: oracle.gemm(a, b, km, rows=rows, lib=lib))
+        except AssertionError as e:
+            caught.append((check.__name__, str(e)[:80]))
+    assert caught, f"no pin caught the planted mistake: {name}"

@@ -96,3 +96,11 @@ def test_oracle_bwd_thread_count(oracle_mod):
     b = oracle_mod.attn_bwd(q, k, v, do, True, 0.25, threads=3)
     for x, y in zip(a, b):
         assert np.max(np.abs(x - y)) <= 1e-13
+
+
+from tests import oracle_gemm_pins as gemm_pins  # noqa: E402
+
+
+@pytest.mark.parametrize("check", gemm_pins.GEMM_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_gemm_pin(oracle_mod, check):
+    check(oracle_mod.gemm)
