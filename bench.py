@@ -22,6 +22,11 @@ with nvidia-smi during the timed region) and ``gpu_launches``.
 10*B*H*N^2*D, halved under the causal mask), with the fp64 backward oracle as
 the CPU baseline.
 
+``--gemm``: the same line for the GEMM on the same pipeline (tk_gemm,
+C = A B^T, M = N = K = 8192 unless ``--gemm-shape M,N,K``; flops 2*M*N*K), with
+the fp64 oracle GEMM on sampled rows as the CPU baseline and cuBLAS (through
+torch.matmul) timed beside it for context.
+
 ``--impl reference``: the comparison arm is the fp64 CPU oracle (there is no
 runnable reference implementation), timed on this host's cores on a bounded
 sample of the same workload per step.
@@ -425,6 +430,192 @@ def run_bwd(args, w):
     return line
 
 
+# ---------------------------------------------------------------- GEMM
+
+GEMM_METRIC = "GEMM bf16 TFLOP/s on 1 GB300 (C = A B^T, fp32 accumulate; fraction of dense BF16 peak) vs CPU oracle"
+GEMM_SOURCES = ["tiled_attention_tk_gb300/csrc/gemm.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
+                "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_inputs(M: int, N: int, K: int):
+    """Seeded bf16 A [M,K] and B [N,K] on the host (N(0,1) draws rounded to bf16)."""
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(7000)
+    a = torch.randn((M, K), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    g.manual_seed(7001)
+    b = torch.randn((N, K), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return a, b
+
+
+def time_oracle_gemm_sample(a, b, budget_s: float):
+    """The fp64 oracle GEMM on rows of C until ``budget_s`` is spent."""
+    import oracle
+    oracle.build()
+    M, K = a.shape
+    N = b.shape[0]
+    rows_done, t_total, start = 0, 0.0, time.perf_counter()
+    chunk = 8
+    while time.perf_counter() - start < budget_s and rows_done < M:
+        rows = list(range(rows_done, min(M, rows_done + chunk)))
+        t0 = time.perf_counter()
+        oracle.gemm(a, b, True, rows=rows)
+        t_total += time.perf_counter() - t0
+        rows_done += len(rows)
+        chunk = min(chunk * 2, 256)
+    flops = 2.0 * rows_done * N * K
+    return flops / t_total / 1e12, oracle.last_threads(), (
+        f"{rows_done} of {M} rows of C ({flops / 1e9:.1f} GFLOP fp64, {t_total:.1f} s)")
+
+
+def run_gemm(args):
+    import torch
+    import tiled_attention_tk_gb300 as tk
+    M, N, K = (int(x) for x in args.gemm_shape.split(","))
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_mod = init_dist(ws_n, "nccl")
+    dev = torch.device("cuda", local)
+    a, b = gemm_inputs(M, N, K)
+    ad, bd = a.to(dev), b.to(dev)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    need = tk.gemm_workspace_bytes(M, N, K, True)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tk.gemm(ad, bd, b_kmajor=True, stream_k=True, out=c, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if dist_mod:
+        dist_mod.barrier()
+    torch.cuda.synchronize(dev)
+    start_ev.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist_mod:
+        dist_mod.barrier()
+    clocks = sampler.stop()
+    kernel_ms = sum(x.elapsed_time(y) for x, y in ev) / args.steps
+    total_ms = max_over_ranks(start_ev.elapsed_time(end_ev), dist_mod, dev)
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
+    flops = 2.0 * M * N * K
+    ms_per_step = total_ms / args.steps
+    value = flops * ws_n / (ms_per_step * 1e-3) / 1e12
+
+    # cuBLAS on the same operands, for context (not the target, not a bench value)
+    bt = bd.t()
+    for _ in range(3):
+        torch.matmul(ad, bt, out=c)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        torch.matmul(ad, bt, out=c)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    cublas = flops / (e0.elapsed_time(e1) / args.steps * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        ah, bh = a.pin_memory(), b.pin_memory()
+        ch = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+        steps = max(3, min(10, args.steps // 10))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                ad.copy_(ah, non_blocking=True)
+                bd.copy_(bh, non_blocking=True)
+                tk.gemm(ad, bd, b_kmajor=True, stream_k=True, out=c, workspace=ws, stream=stream)
+                ch.copy_(c, non_blocking=True)
+            stream.synchronize()
+        e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            e2e_step()
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, dist_mod, dev)
+        e2e = {"value": round(flops * ws_n / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (a.numel() + b.numel()) * 2, "d2h_bytes_per_step": M * N * 2,
+               "ms_per_step": round(e2e_s * 1e3, 3), "steps": steps}
+    if rank != 0:
+        return None
+    peak, peak_label = peaks()
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    name = f"gemm-M{M}N{N}K{K}"
+    line = {
+        "metric": GEMM_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch.Generator, N(0,1) fp32 draws rounded to bf16)",
+        "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": "[N,K] (C = A B^T)",
+                   "stream_k": "on where the schedule uses it",
+                   "workspace_bytes": need,
+                   "l2": "inputs > L2, no flush" if (M + N) * K * 2 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_label,
+                     "traffic": gemm_traffic_for(name), "kernel": "gemm_kernel<true>",
+                     "kernel_ms": round(kernel_ms, 5)},
+        "cublas_context_tflops": round(cublas, 2),
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, desc = time_oracle_gemm_sample(a, b, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    return line
+
+
+def gemm_traffic_for(name: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            e = json.load(f).get(name)
+        if e and e.get("kernel_source_hash") == gemm_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError, AttributeError):
+        pass
+    return None
+
+
+def run_reference_gemm(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    M, N, K = (int(x) for x in args.gemm_shape.split(","))
+    a, b = gemm_inputs(M, N, K)
+    tf, cores, desc = time_oracle_gemm_sample(a, b, budget_s=args.reference_budget)
+    return {"impl": "reference", "metric": GEMM_METRIC, "value": round(tf, 6), "unit": "TFLOP/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"gemm-M{M}N{N}K{K}", "M": M, "N": N, "K": K},
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": desc, "value": round(tf, 6)},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args, w):
@@ -497,6 +688,8 @@ def main(argv=None):
                     help="B,H,N,D,causal[,Nkv]: a custom N(0,1) workload instead of a named one")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
+    ap.add_argument("--gemm", action="store_true", help="time the GEMM on the same pipeline instead")
+    ap.add_argument("--gemm-shape", type=str, default="8192,8192,8192", help="M,N,K for --gemm")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -514,6 +707,11 @@ def main(argv=None):
         todo = [Workload(0, f[0], f[1], f[2], f[3], bool(f[4]), "normal", f[5] if len(f) == 6 else None)]
     else:
         todo = [WORKLOADS[i] for i in (sorted(WORKLOADS) if args.all else [args.workload])]
+    if args.gemm:
+        line = run_reference_gemm(args) if args.impl == "reference" else run_gemm(args)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.bwd:
         todo = [w for w in todo if w.Nkv == w.N]  # the backward takes Nq = Nkv only
     for w in todo:

@@ -191,6 +191,48 @@ int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
                         int64_t N, int64_t D, int causal, float scale, cudaStream_t stream);
 
 /*
+ * tk_gemm_workspace_bytes -- device workspace tk_gemm needs on the current
+ * device for this shape: 0 when the schedule has no stream-K part (or for a
+ * shape tk_gemm rejects), else one 128 x 256 fp32 partial-sum slot per SM
+ * plus one counter per stream-K tile, each section 256-byte aligned.
+ */
+size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k);
+
+/*
+ * tk_gemm -- C = A op(B) on the same TMA + tcgen05 pipeline as the attention
+ * kernels, with a persistent grid, an L2-grouped tile order and stream-K for
+ * the last wave.  The pages name GEMM as the workload the tile abstractions
+ * are built around and threadblock swizzle plus persistent grid + stream-K
+ * as the cures for its L2 hit rate and wave quantisation
+ * (10100.com/article/71410160, section on grid-level abstraction).
+ *
+ *   C[m,n] = sum_k A[m,k] * B'[k,n],  fp32 accumulation, C rounded to bf16
+ *            (round to nearest even), where B' = B^T if b_kmajor else B.
+ *
+ * Arguments
+ *   A          device bf16 [M, K] row-major, 16-byte aligned.
+ *   B          device bf16 [N, K] row-major if b_kmajor = 1 (C = A B^T), or
+ *              [K, N] row-major if b_kmajor = 0 (C = A B); 16-byte aligned.
+ *   C          device bf16 [M, N] row-major, 16-byte aligned, written in full.
+ *   workspace  device memory of at least tk_gemm_workspace_bytes(M,N,K,
+ *              stream_k) bytes, 256-byte aligned (may be NULL when that is 0).
+ *   M, N, K    >= 1; K and N multiples of 8 (16-byte row strides).
+ *   b_kmajor   0 or 1, as above.
+ *   stream_k   1: split the last wave's tiles in K over all SMs when the
+ *              tiles do not fill whole waves; 0: whole tiles only.
+ *   stream     CUDA stream (0 = legacy default).
+ * Semantics: asynchronous on `stream` (a memset of the stream-K counters and
+ * one kernel).  Deterministic: the stream-K partial sums are added in a fixed
+ * order.  Errors: TK_ERR_NULL_PTR, TK_ERR_BAD_SHAPE, TK_ERR_BAD_FLAG,
+ * TK_ERR_MISALIGNED, TK_ERR_ALIAS (C or the workspace overlapping an input or
+ * each other), TK_ERR_WORKSPACE, TK_ERR_NOT_DEVICE_MEMORY,
+ * TK_ERR_UNSUPPORTED_DEVICE, TK_ERR_CUDA; all reported before anything is
+ * enqueued.  Bounded waits as for the attention kernels.
+ */
+int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t workspace_bytes, int64_t M,
+            int64_t N, int64_t K, int b_kmajor, int stream_k, cudaStream_t stream);
+
+/*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the
  * current device's kernel status word.  Returns TK_OK if no bounded wait of
  * any kernel of this library on this device has given up since the last

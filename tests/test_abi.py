@@ -166,3 +166,32 @@ def test_bwd_workspace_size():
 ])
 def test_bwd_host_validation(kwargs, code):
     assert _bwd(**kwargs) == tk.STATUS[code]
+
+
+# ---------------------------------------------------------------- GEMM ABI
+
+def _gemm(a=Bq, b=Bk, c=Bo, ws=None, ws_bytes=0, M=256, N=256, K=256, b_kmajor=1, stream_k=1):
+    return tk.load().tk_gemm(a, b, c, ws, ws_bytes, M, N, K, b_kmajor, stream_k, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(a=None), "TK_ERR_NULL_PTR"),
+    (dict(c=None), "TK_ERR_NULL_PTR"),
+    (dict(M=0), "TK_ERR_BAD_SHAPE"),
+    (dict(K=12), "TK_ERR_BAD_SHAPE"),     # row strides must be multiples of 16 bytes
+    (dict(N=100), "TK_ERR_BAD_SHAPE"),
+    (dict(K=2**31), "TK_ERR_BAD_SHAPE"),
+    (dict(b_kmajor=2), "TK_ERR_BAD_FLAG"),
+    (dict(stream_k=-1), "TK_ERR_BAD_FLAG"),
+    (dict(b=Bk + 8), "TK_ERR_MISALIGNED"),
+    (dict(c=Bq + 0x1000), "TK_ERR_ALIAS"),  # inside A (256 x 256 x 2 bytes)
+])
+def test_gemm_host_validation(kwargs, code):
+    assert _gemm(**kwargs) == tk.STATUS[code]
+
+
+def test_gemm_workspace_bytes_rejects_bad_shapes():
+    lib = tk.load()
+    assert lib.tk_gemm_workspace_bytes(0, 8, 8, 1) == 0
+    assert lib.tk_gemm_workspace_bytes(8, 8, 12, 1) == 0
+    assert lib.tk_gemm_workspace_bytes(8, 8, 8, 3) == 0

@@ -158,3 +158,35 @@ def selftest_timeout(limit_ns: int, stream=None) -> None:
     ``limit_ns``)."""
     _lib.check(_lib.load().tk_attn_selftest_timeout(int(limit_ns), _stream_handle(stream)),
                "tk_attn_selftest_timeout")
+
+
+def gemm_workspace_bytes(M: int, N: int, K: int, stream_k: bool = True) -> int:
+    """Device workspace bytes tk_gemm needs on the current device (0: none)."""
+    return int(_lib.load().tk_gemm_workspace_bytes(M, N, K, int(bool(stream_k))))
+
+
+def gemm(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool = True, stream_k: bool = True,
+         out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """C = a @ b.T (b_kmajor: b is [N, K]) or a @ b (b is [K, N]); bf16 CUDA
+    tensors, fp32 accumulation, bf16 result [M, N].  Enqueued on ``stream``
+    (default: current) without synchronising."""
+    for t, n in ((a, "a"), (b, "b")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.device.type != "cuda":
+            raise ValueError(f"{n} must be a 2-D CUDA bf16 tensor")
+    M, K = a.shape
+    N = b.shape[0] if b_kmajor else b.shape[1]
+    if (b.shape[1] if b_kmajor else b.shape[0]) != K:
+        raise ValueError("inner dimensions of a and b differ")
+    a, b = a.contiguous(), b.contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    need = gemm_workspace_bytes(M, N, K, stream_k)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=a.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    with torch.cuda.device(a.device):
+        rc = _lib.load().tk_gemm(a.data_ptr(), b.data_ptr(), out.data_ptr(), ws_ptr, ws_len, M, N, K,
+                                 int(bool(b_kmajor)), int(bool(stream_k)), _stream_handle(stream))
+    _lib.check(rc, "tk_gemm")
+    return out

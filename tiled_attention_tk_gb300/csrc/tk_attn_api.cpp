@@ -121,6 +121,23 @@ int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int6
     return TK_OK;
 }
 
+// 3-D view {d0, d1, 1} of a contiguous row-major [d1, d0] bf16 matrix, moved
+// as box0 x box1 boxes with the 128-byte swizzle (box0 * 2 = 128 bytes).
+int encode_matrix_map(CUtensorMap *map, const void *ptr, int64_t d0, int64_t d1, uint32_t box0, uint32_t box1) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail_cuda(g_encode_err);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), 1};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d0) * 2,
+                                   static_cast<cuuint64_t>(d0) * static_cast<cuuint64_t>(d1) * 2};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                     box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+    return TK_OK;
+}
+
 // Shape checks shared by the forward and backward entry points.
 int check_shape(int64_t B, int64_t H, int64_t N, int64_t D) {
     if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
@@ -302,14 +319,134 @@ int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
                        scale, stream);
 }
 
+// ------------------------------------------------------------------ GEMM
+
+namespace {
+
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmGroupM = 8;
+constexpr int kGemmMinSkIters = 4;  // K iterations per stream-K range at least
+// Stream-K pays only when a tile's K loop is long against the fp32 partial
+// it writes and the finisher reads (128 KB each way): measured on the GB300,
+// it gains about 8% at K = 4096 over 3.2 waves and loses at K = 1024 and
+// when there are fewer tiles than SMs, where one tile's partials are summed
+// by a single CTA.
+constexpr int kGemmSkMinKIters = 48;
+constexpr uint64_t kGemmSlotBytes = static_cast<uint64_t>(kGemmBM) * kGemmBN * 4;
+
+struct GemmPlan {
+    int tiles_m, tiles_n, k_iters, grid, dp_tiles, sk_tiles, sk_iters_per_cta;
+    uint64_t workspace;  // bytes: partial slots, then the counters
+};
+
+int gemm_shape(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1) return TK_ERR_BAD_SHAPE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    // Row strides of A, B and C must be multiples of 16 bytes (TMA).
+    if (K % 8 != 0 || N % 8 != 0) return TK_ERR_BAD_SHAPE;
+    return TK_OK;
+}
+
+// Data-parallel waves of whole tiles; when the tiles do not fill the last
+// wave (and there is more than one wave), the last partial wave plus one full
+// wave are split in K over all CTAs (stream-K): every CTA gets at least one
+// tile's worth of K iterations, so a tile has at most two K segments.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
+    GemmPlan g = {};
+    g.tiles_m = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
+    g.tiles_n = static_cast<int>((N + kGemmBN - 1) / kGemmBN);
+    g.k_iters = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
+    const int64_t T = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
+    const int P = num_sms;
+    if (!stream_k || g.k_iters < kGemmSkMinKIters || T <= P || T % P == 0) {
+        g.dp_tiles = static_cast<int>(T);
+        g.grid = static_cast<int>(T < P ? T : P);
+        return g;
+    }
+    g.sk_tiles = static_cast<int>(P + T % P);  // the partial wave plus one full wave
+    g.dp_tiles = static_cast<int>(T - g.sk_tiles);
+    const int64_t total = static_cast<int64_t>(g.sk_tiles) * g.k_iters;
+    int64_t L = (total + P - 1) / P;
+    if (L < kGemmMinSkIters) L = kGemmMinSkIters;
+    g.sk_iters_per_cta = static_cast<int>(L);
+    g.grid = P;
+    g.workspace = round_up(static_cast<uint64_t>(P) * kGemmSlotBytes, kWorkspaceAlign) +
+                  round_up(static_cast<uint64_t>(g.sk_tiles) * 4, kWorkspaceAlign);
+    return g;
+}
+
+}  // namespace
+
+size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k) {
+    if (gemm_shape(M, N, K) != TK_OK || (stream_k != 0 && stream_k != 1)) return 0;
+    int num_sms = 0;
+    if (current_device(&num_sms) != TK_OK) return 0;
+    return static_cast<size_t>(plan_gemm(M, N, K, num_sms, stream_k).workspace);
+}
+
+int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t workspace_bytes, int64_t M,
+            int64_t N, int64_t K, int b_kmajor, int stream_k, cudaStream_t stream) {
+    if (!A || !B || !C) return TK_ERR_NULL_PTR;
+    int rc = gemm_shape(M, N, K);
+    if (rc != TK_OK) return rc;
+    if ((b_kmajor != 0 && b_kmajor != 1) || (stream_k != 0 && stream_k != 1)) return TK_ERR_BAD_FLAG;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return TK_ERR_MISALIGNED;
+    const uint64_t a_bytes = static_cast<uint64_t>(M) * K * 2, b_bytes = static_cast<uint64_t>(N) * K * 2,
+                   c_bytes = static_cast<uint64_t>(M) * N * 2;
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return TK_ERR_ALIAS;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const GemmPlan g = plan_gemm(M, N, K, num_sms, stream_k);
+    if (g.workspace > 0) {
+        if (!workspace) return TK_ERR_NULL_PTR;
+        if (!aligned(workspace, kWorkspaceAlign) || workspace_bytes < g.workspace) return TK_ERR_WORKSPACE;
+        if (overlaps(workspace, g.workspace, A, a_bytes) || overlaps(workspace, g.workspace, B, b_bytes) ||
+            overlaps(workspace, g.workspace, C, c_bytes))
+            return TK_ERR_ALIAS;
+    }
+    const void *ptrs[4] = {A, B, C, g.workspace > 0 ? workspace : C};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+
+    tk::GemmParams p;
+    if ((rc = encode_matrix_map(&p.tmA, A, K, M, 64, 128)) != TK_OK) return rc;
+    if (b_kmajor) {
+        if ((rc = encode_matrix_map(&p.tmB, B, K, N, 64, 256)) != TK_OK) return rc;
+    } else {
+        if ((rc = encode_matrix_map(&p.tmB, B, N, K, 64, 64)) != TK_OK) return rc;
+    }
+    if ((rc = encode_matrix_map(&p.tmC, C, N, M, 64, 32)) != TK_OK) return rc;
+    char *ws = static_cast<char *>(workspace);
+    p.partials = g.workspace > 0 ? reinterpret_cast<float *>(ws) : nullptr;
+    p.counters = g.workspace > 0
+                     ? reinterpret_cast<unsigned *>(ws + round_up(static_cast<uint64_t>(g.grid) * kGemmSlotBytes,
+                                                                  kWorkspaceAlign))
+                     : nullptr;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.b_kmajor = b_kmajor;
+    p.tiles_m = g.tiles_m;
+    p.tiles_n = g.tiles_n;
+    p.k_iters = g.k_iters;
+    p.group_m = kGemmGroupM;
+    p.dp_tiles = g.dp_tiles;
+    p.sk_tiles = g.sk_tiles;
+    p.sk_iters_per_cta = g.sk_iters_per_cta;
+    cudaError_t e = tk::launch_gemm(p, g.grid, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
+
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
-    uint32_t status = 0, where = 0, status_b = 0, where_b = 0;
+    uint32_t status = 0, where = 0, status_b = 0, where_b = 0, status_g = 0, where_g = 0;
     cudaError_t e = tk::read_and_clear_status(stream, &status, &where);  // synchronises the stream
     if (e != cudaSuccess) return fail_cuda(e);
     e = tk::read_and_clear_bwd_status(&status_b, &where_b);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (detail) *detail = status ? where : where_b;
-    return (status == 0 && status_b == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
+    e = tk::read_and_clear_gemm_status(&status_g, &where_g);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail) *detail = status ? where : (status_b ? where_b : where_g);
+    return (status == 0 && status_b == 0 && status_g == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
 }
 
 int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {

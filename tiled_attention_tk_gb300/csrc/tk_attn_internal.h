@@ -57,6 +57,25 @@ struct BwdParams {
 // Launches the backward pass (prep, main, dQ conversion) for head dim D.
 cudaError_t launch_attn_bwd(int D, const BwdParams &p, int num_sms, cudaStream_t stream);
 
+// Everything the GEMM kernel needs (C = A op(B), bf16 in and out, fp32 accumulation).
+struct GemmParams {
+    CUtensorMap tmA;   // 3-D {K, M, 1} bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmB;   // b_kmajor: {K, N, 1}, box {64, 256, 1}; else {N, K, 1}, box {64, 64, 1}
+    CUtensorMap tmC;   // {N, M, 1}, box {64, 32, 1}, for TMA stores
+    float *partials;   // workspace: one 128 x 256 fp32 stream-K partial slot per CTA
+    unsigned *counters;  // workspace: per stream-K tile, partials published (x4 warps)
+    int M, N, K;
+    int b_kmajor;      // 1: B is [N, K] (C = A B^T); 0: B is [K, N] (C = A B)
+    int tiles_m, tiles_n, k_iters;
+    int group_m;       // tile rows per L2 group of the tile order
+    int dp_tiles;      // tiles [0, dp_tiles): whole tiles, round-robin over the CTAs
+    int sk_tiles;      // tiles [dp_tiles, dp_tiles + sk_tiles): split in K (stream-K)
+    int sk_iters_per_cta;  // K iterations of the stream-K range of each CTA
+};
+
+cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream);
+cudaError_t read_and_clear_gemm_status(uint32_t *status, uint32_t *detail);
+
 // Size of the library-owned workspace behind tk_attn_bwd_noalloc.
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 
