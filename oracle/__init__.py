@@ -1,7 +1,7 @@
 """fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
 
 This package is the checker, not the product (attention forward and backward,
-and the plain GEMM the same tile pipeline runs).  Only ``tests/``,
+the plain GEMM the same tile pipeline runs, and Based linear attention).  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may load
 it.  It shares no code with the CUDA library and imports nothing from it.
 
@@ -88,6 +88,10 @@ def _declare(lib) -> None:
     lib.tkor_gemm.restype = ctypes.c_int
     lib.tkor_gemm_rows.argtypes = [P, P, i64, i64, i64, ctypes.c_int, P, i64, P, ctypes.c_int]
     lib.tkor_gemm_rows.restype = ctypes.c_int
+    lib.tkor_based.argtypes = [P, P, P, P, P, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int]
+    lib.tkor_based.restype = ctypes.c_int
+    lib.tkor_based_rows.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, i64, P, P, ctypes.c_int]
+    lib.tkor_based_rows.restype = ctypes.c_int
     lib.tkor_last_threads.argtypes = []
     lib.tkor_last_threads.restype = ctypes.c_int
 
@@ -216,6 +220,38 @@ def gemm(a, b, b_kmajor: bool = True, rows=None, threads: int = 0, lib=None) -> 
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return C
+
+
+def based(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
+    """Causal Based linear attention, plain quadratic form in fp64:
+    w_ij = 1 + s + s^2/2 with s = scale <q_i, k_j>, j <= i;
+    O_i = sum_j w_ij v_j / DEN_i, DEN_i = sum_j w_ij.
+    Whole problem: q, k [B,H,N,Dqk], v [B,H,N,Dv] -> (O [B,H,N,Dv], DEN [B,H,N]).
+    With ``rows``: q, k [N,Dqk], v [N,Dv] of ONE head -> (O [len,Dv], DEN [len])."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    lib = lib or _load()
+    if rows is None:
+        if qb.ndim != 4 or qb.shape != kb.shape or vb.shape[:3] != qb.shape[:3]:
+            raise ValueError("q, k [B,H,N,Dqk] and v [B,H,N,Dv] expected")
+        B, H, N, Dqk = qb.shape
+        Dv = vb.shape[3]
+        O = np.empty((B, H, N, Dv), dtype=np.float64)
+        DEN = np.empty((B, H, N), dtype=np.float64)
+        rc = lib.tkor_based(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(O), _ptr(DEN), B, H, N, Dqk, Dv,
+                            float(scale), int(threads))
+    else:
+        if qb.ndim != 2 or qb.shape != kb.shape or vb.shape[0] != qb.shape[0]:
+            raise ValueError("q, k [N,Dqk] and v [N,Dv] expected")
+        N, Dqk = qb.shape
+        Dv = vb.shape[1]
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        O = np.empty((r.size, Dv), dtype=np.float64)
+        DEN = np.empty((r.size,), dtype=np.float64)
+        rc = lib.tkor_based_rows(_ptr(qb), _ptr(kb), _ptr(vb), N, Dqk, Dv, float(scale), _ptr(r), r.size,
+                                 _ptr(O), _ptr(DEN), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return O, DEN
 
 
 def last_threads() -> int:

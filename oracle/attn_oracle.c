@@ -497,3 +497,99 @@ int tkor_gemm(const uint16_t *A, const uint16_t *B, double *C, int64_t M, int64_
               int b_kmajor, int nthreads) {
     return tkor_gemm_rows(A, B, M, N, K, b_kmajor, NULL, M, C, nthreads);
 }
+
+/* ======================================================================== */
+/* Based linear attention (causal), the linear-attention variant the pages */
+/* list ("Based Linear Attention", thebeat.tech "ThunderKittens 2.0", New    */
+/* Kernels).  The pages name it without a formula; the reading taken is the */
+/* Based feature map, the second-order Taylor expansion of exp, on query and */
+/* key features of dimension Dqk:                                           */
+/*   s_ij  = scale * <Q_i, K_j>                                             */
+/*   w_ij  = 1 + s_ij + s_ij^2 / 2          (= phi(q_i) . phi(k_j))          */
+/*   DEN_i = sum_{j <= i} w_ij                                              */
+/*   O_i   = sum_{j <= i} w_ij V_j / DEN_i                                  */
+/* written here in its plain quadratic form: one pass over the keys of each */
+/* row, fp64 from the exact bf16 inputs.  w_ij >= 1/2, so DEN_i > 0.         */
+
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    int64_t N, Dqk, Dv;
+    double scale;
+    const int64_t *rows; /* NULL: rows 0..N-1 */
+    int64_t nrows;
+    double *O, *DEN;     /* nrows x Dv, nrows */
+    int64_t next;
+    pthread_mutex_t lock;
+} based_job;
+
+static void based_row(const based_job *job, int64_t i, double *o_row, double *den_out) {
+    const int64_t Dqk = job->Dqk, Dv = job->Dv;
+    double den = 0.0;
+    for (int64_t d = 0; d < Dv; ++d) o_row[d] = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+        double dot = 0.0;
+        for (int64_t d = 0; d < Dqk; ++d)
+            dot += bf16_bits_to_double(job->Q[i * Dqk + d]) * bf16_bits_to_double(job->K[j * Dqk + d]);
+        double s = job->scale * dot;
+        double w = 1.0 + s + 0.5 * s * s;
+        den += w;
+        for (int64_t d = 0; d < Dv; ++d) o_row[d] += w * bf16_bits_to_double(job->V[j * Dv + d]);
+    }
+    for (int64_t d = 0; d < Dv; ++d) o_row[d] /= den;
+    *den_out = den;
+}
+
+static void *based_worker(void *arg) {
+    based_job *job = (based_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        int64_t r = job->next++;
+        pthread_mutex_unlock(&job->lock);
+        if (r >= job->nrows) break;
+        int64_t i = job->rows ? job->rows[r] : r;
+        based_row(job, i, job->O + r * job->Dv, job->DEN + r);
+    }
+    return NULL;
+}
+
+/* Selected rows of one head (rows == NULL: all N).  Q, K: bf16 bits [N,Dqk];
+ * V: [N,Dv].  O: double [nrows,Dv]; DEN: double [nrows]. */
+int tkor_based_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int64_t N, int64_t Dqk,
+                    int64_t Dv, double scale, const int64_t *rows, int64_t nrows, double *O, double *DEN,
+                    int nthreads) {
+    if (!Q || !K || !V || !O || !DEN || N < 1 || Dqk < 1 || Dv < 1 || nrows < 0) return -1;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= N) return -1;
+    based_job job;
+    job.Q = Q; job.K = K; job.V = V; job.N = N; job.Dqk = Dqk; job.Dv = Dv; job.scale = scale;
+    job.rows = rows; job.nrows = nrows; job.O = O; job.DEN = DEN; job.next = 0;
+    pthread_mutex_init(&job.lock, NULL);
+    g_last_threads = 0;
+    int T = resolve_threads(nthreads);
+    if ((int64_t)T > nrows) T = (int)(nrows > 0 ? nrows : 1);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)T);
+    int started = 0;
+    for (int t = 1; tid && t < T; ++t) {
+        if (pthread_create(&tid[started], NULL, based_worker, &job) != 0) break;
+        ++started;
+    }
+    g_last_threads = started + 1;
+    based_worker(&job);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    free(tid);
+    pthread_mutex_destroy(&job.lock);
+    return 0;
+}
+
+/* Whole problem: Q, K [B,H,N,Dqk]; V [B,H,N,Dv]; O [B,H,N,Dv]; DEN [B,H,N]. */
+int tkor_based(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *O, double *DEN, int64_t B,
+               int64_t H, int64_t N, int64_t Dqk, int64_t Dv, double scale, int nthreads) {
+    if (B < 1 || H < 1) return -1;
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        if (tkor_based_rows(Q + (size_t)bh * N * Dqk, K + (size_t)bh * N * Dqk, V + (size_t)bh * N * Dv, N, Dqk,
+                            Dv, scale, NULL, N, O + (size_t)bh * N * Dv, DEN + (size_t)bh * N, nthreads))
+            return -1;
+    }
+    return 0;
+}

@@ -138,3 +138,34 @@ def test_gemm_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
         except AssertionError as e:
             caught.append((check.__name__, str(e)[:80]))
     assert caught, f"no pin caught the planted mistake: {name}"
+
+
+from tests import oracle_based_pins as based_pins  # noqa: E402
+
+BASED_MUTANTS = [
+    ("quadratic term dropped", "double w = 1.0 + s + 0.5 * s * s;", "double w = 1.0 + s;"),
+    ("quadratic term not halved", "double w = 1.0 + s + 0.5 * s * s;", "double w = 1.0 + s + s * s;"),
+    ("constant term dropped", "double w = 1.0 + s + 0.5 * s * s;", "double w = s + 0.5 * s * s;"),
+    ("diagonal excluded", "for (int64_t j = 0; j <= i; ++j) {\n        double dot",
+     "for (int64_t j = 0; j < (i > 0 ? i : 1); ++j) {\n        double dot"),
+    ("not causal", "for (int64_t j = 0; j <= i; ++j) {\n        double dot",
+     "for (int64_t j = 0; j < job->N; ++j) {\n        double dot"),
+    ("output not normalised", "for (int64_t d = 0; d < Dv; ++d) o_row[d] /= den;", ""),
+    ("scale ignored", "double s = job->scale * dot;", "double s = dot;"),
+    ("value row of the query", "o_row[d] += w * bf16_bits_to_double(job->V[j * Dv + d]);",
+     "o_row[d] += w * bf16_bits_to_double(job->V[i * Dv + d]);"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mutant", BASED_MUTANTS, ids=[m[0] for m in BASED_MUTANTS])
+def test_based_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation anchor for '{name}' not unique in the oracle"
+    lib = oracle.bind(_compile(text.replace(orig, mutant), tmp_path, "b" + str(abs(hash(name)))))
+    caught = []
+    for check in based_pins.BASED_CHECKS:
+        try:
+            check(lambda q, k, v, scale, rows=None: oracle.based(q, k, v, scale, rows=rows, lib=lib))
+        except AssertionError as e:
+            caught.append((check.__name__, str(e)[:80]))
+    assert caught, f"no pin caught the planted mistake: {name}"

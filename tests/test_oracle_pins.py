@@ -104,3 +104,11 @@ from tests import oracle_gemm_pins as gemm_pins  # noqa: E402
 @pytest.mark.parametrize("check", gemm_pins.GEMM_CHECKS, ids=lambda c: c.__name__)
 def test_oracle_gemm_pin(oracle_mod, check):
     check(oracle_mod.gemm)
+
+
+from tests import oracle_based_pins as based_pins  # noqa: E402
+
+
+@pytest.mark.parametrize("check", based_pins.BASED_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_based_pin(oracle_mod, check):
+    check(oracle_mod.based)
