@@ -233,6 +233,29 @@ int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t works
             int64_t N, int64_t K, int b_kmajor, int stream_k, cudaStream_t stream);
 
 /*
+ * tk_based_fwd -- causal Based linear attention (the linear-attention kernel
+ * the pages list as "Based Linear Attention", thebeat.tech "ThunderKittens
+ * 2.0", New Kernels; the formula is the Based feature map, the second-order
+ * Taylor expansion of exp):
+ *     s_ij  = scale <Q_i, K_j>,   w_ij = 1 + s_ij + s_ij^2 / 2   (j <= i)
+ *     DEN_i = sum_j w_ij,         O_i  = sum_j w_ij V_j / DEN_i
+ * computed in linear time: chunks of 128 rows, a running state of the
+ * feature map's 153 features in TMEM, tensor-core products for the
+ * in-chunk and carried parts.
+ *
+ * Arguments
+ *   Q, K   device bf16 [B, H, N, Dqk], Dqk = 16, 16-byte aligned.
+ *   V, O   device bf16 [B, H, N, Dv], Dv = 64, 16-byte aligned (O written).
+ *   DEN    device fp32 [B, H, N], 4-byte aligned (written): the normaliser,
+ *          so O_i * DEN_i is the unnormalised sum.
+ *   scale  finite, > 0 (usually 1/sqrt(Dqk) = 0.25).
+ * Semantics, ownership and errors as tk_attn_fwd (TK_ERR_UNSUPPORTED_D for
+ * any other Dqk, Dv).  Deterministic.
+ */
+int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H,
+                 int64_t N, int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream);
+
+/*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the
  * current device's kernel status word.  Returns TK_OK if no bounded wait of
  * any kernel of this library on this device has given up since the last

@@ -195,3 +195,23 @@ def test_gemm_workspace_bytes_rejects_bad_shapes():
     assert lib.tk_gemm_workspace_bytes(0, 8, 8, 1) == 0
     assert lib.tk_gemm_workspace_bytes(8, 8, 12, 1) == 0
     assert lib.tk_gemm_workspace_bytes(8, 8, 8, 3) == 0
+
+
+# ---------------------------------------------------------------- Based ABI
+
+def _based(q=Bq, k=Bk, v=Bv, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=16, Dv=64, scale=0.25):
+    return tk.load().tk_based_fwd(q, k, v, o, d, B, H, N, Dqk, Dv, scale, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(v=None), "TK_ERR_NULL_PTR"),
+    (dict(N=0), "TK_ERR_BAD_SHAPE"),
+    (dict(Dqk=32), "TK_ERR_UNSUPPORTED_D"),
+    (dict(Dv=128), "TK_ERR_UNSUPPORTED_D"),
+    (dict(scale=0.0), "TK_ERR_BAD_SCALE"),
+    (dict(o=Bo + 8), "TK_ERR_MISALIGNED"),
+    (dict(o=Bv + 1024), "TK_ERR_ALIAS"),
+    (dict(d=Bo + 64), "TK_ERR_ALIAS"),
+])
+def test_based_host_validation(kwargs, code):
+    assert _based(**kwargs) == tk.STATUS[code]

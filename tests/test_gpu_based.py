@@ -1,0 +1,80 @@
+"""Parity of the Based linear attention (tk_based_fwd, through the C ABI) with
+the fp64 oracle's quadratic form.
+
+The kernel runs the linear (chunked, running-state) form with bf16 operands:
+the in-chunk weights P, the feature maps phi(q), phi(k) and the carried
+state enter the tensor-core products as bf16 (relative rounding 2^-9 each),
+accumulation is fp32, O is stored as bf16.  Bar: O within max-abs 2e-2 and
+mean-abs 2e-3 (the attention forward's bar: O is again a weighted mean of
+V rows); DEN within relative 1e-2 (max) and 2e-3 (mean).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import tiled_attention_tk_gb300 as tk
+
+pytestmark = pytest.mark.gpu
+
+
+def _qkv(B, H, N, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, N, 16), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, N, 16), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, N, 64), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+def _run(q, k, v, scale):
+    o, den = tk.based(q.cuda(), k.cuda(), v.cuda(), scale=scale)
+    torch.cuda.synchronize()
+    status, detail = tk.device_status()
+    assert status == 0, f"device status {status} detail {detail:#x}"
+    return o.cpu().double().numpy(), den.cpu().double().numpy()
+
+
+def _assert_close(o, den, O_ref, D_ref, what):
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(den)), f"{what}: non-finite output"
+    err = np.abs(o - O_ref)
+    rel = np.abs(den - D_ref) / np.abs(D_ref)
+    assert err.max() <= 2e-2, f"{what}: O max-abs {err.max():.3e}"
+    assert err.mean() <= 2e-3, f"{what}: O mean-abs {err.mean():.3e}"
+    assert rel.max() <= 1e-2, f"{what}: DEN max-rel {rel.max():.3e}"
+    assert rel.mean() <= 2e-3, f"{what}: DEN mean-rel {rel.mean():.3e}"
+
+
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 300, 1000])
+def test_based_shapes(oracle_mod, N):
+    q, k, v = _qkv(1, 2, N, 300 + N)
+    o, den = _run(q, k, v, 0.25)
+    O_ref, D_ref = oracle_mod.based(q, k, v, 0.25)
+    _assert_close(o, den, O_ref, D_ref, f"N={N}")
+
+
+@pytest.mark.parametrize("scale", [0.1, 0.5])
+def test_based_scales_and_heads(oracle_mod, scale):
+    q, k, v = _qkv(2, 3, 700, 400)
+    o, den = _run(q, k, v, scale)
+    O_ref, D_ref = oracle_mod.based(q, k, v, scale)
+    _assert_close(o, den, O_ref, D_ref, f"B2 H3 N700 scale={scale}")
+
+
+def test_based_deterministic():
+    q, k, v = _qkv(1, 4, 1000, 401)
+    o1, d1 = _run(q, k, v, 0.25)
+    o2, d2 = _run(q, k, v, 0.25)
+    assert np.array_equal(o1, o2) and np.array_equal(d1, d2)
+
+
+def test_based_bench_workload_sampled(oracle_mod):
+    """The benchmark's B8 H16 N4096 launch, sampled heads and rows (the last
+    rows of a head carry the longest state)."""
+    B, H, N = 8, 16, 4096
+    q, k, v = _qkv(B, H, N, 402)
+    o, den = _run(q, k, v, 0.25)
+    rows = [0, 1, 127, 128, 129, 2047, 2048, 4000, 4094, 4095]
+    for b, h in [(0, 0), (3, 7), (7, 15)]:
+        O_ref, D_ref = oracle_mod.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
+        _assert_close(o[b, h, rows], den[b, h, rows], O_ref, D_ref, f"B8H16N4096 head ({b},{h})")

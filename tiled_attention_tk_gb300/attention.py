@@ -190,3 +190,30 @@ def gemm(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool = True, stream_k: bool
                                  int(bool(b_kmajor)), int(bool(stream_k)), _stream_handle(stream))
     _lib.check(rc, "tk_gemm")
     return out
+
+
+def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+          out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None):
+    """Causal Based linear attention.  q, k: bf16 [B,H,N,16]; v: bf16
+    [B,H,N,64] (CUDA).  Returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]) with
+    w_ij = 1 + s + s^2/2, s = scale <q_i,k_j>, O_i = sum_{j<=i} w_ij v_j / DEN_i.
+    ``scale`` defaults to 1/sqrt(16).  Enqueued without synchronising."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA bf16 [B,H,N,D] tensor")
+    if q.shape != k.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k [B,H,N,Dqk] and v [B,H,N,Dv] must agree in B, H, N")
+    B, H, N, Dqk = q.shape
+    Dv = v.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dqk)
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=torch.bfloat16, device=q.device)
+    if den is None:
+        den = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = _lib.load().tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), den.data_ptr(),
+                                      B, H, N, Dqk, Dv, float(scale), _stream_handle(stream))
+    _lib.check(rc, "tk_based_fwd")
+    return out, den

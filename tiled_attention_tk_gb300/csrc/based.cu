@@ -1,0 +1,417 @@
+// based.cu -- causal Based linear attention on tcgen05 (sm_103a, GB300).
+//
+// The pages list "Based Linear Attention" among the kernels built with the
+// same tiles (thebeat.tech "ThunderKittens 2.0", New Kernels) without a
+// formula.  The reading taken is the Based feature map, the second-order
+// Taylor expansion of exp, on query/key features of dimension 16:
+//
+//   w_ij  = 1 + s_ij + s_ij^2 / 2,  s_ij = scale <q_i, k_j>   (= phi(q_i) . phi(k_j))
+//   O_i   = sum_{j<=i} w_ij v_j / DEN_i,   DEN_i = sum_{j<=i} w_ij      (v_j in R^64)
+//
+// with phi(x) = [1, sqrt(scale) x, scale/sqrt(2) x_a^2, scale x_a x_b (a < b)]
+// (153 features, padded with zeros to F = 192).  The kernel runs the chunked
+// linear form: one CTA per (batch, head) walks the sequence in chunks of 128
+// rows and keeps the running state
+//
+//   S^T = sum_j [v_j | 1] phi(k_j)^T      (65 live rows x 192 features, fp32 in TMEM)
+//
+// so that per chunk c, for the rows i of the chunk:
+//   intra:  [num | den]_i  = sum_{j in c, j<=i} w_ij [v_j | 1]     (tensor core: P [V | 1])
+//   inter:  [num | den]_i += phi(q_i) . S_{<c}                      (tensor core: phi(Q) S)
+//   state:  S^T += [V | 1]^T phi(K)                                 (tensor core)
+//   O_i = num_i / den_i.
+//
+// 192 threads: four compute warps (row i of the chunk = TMEM lane i), a TMA
+// warp and an MMA warp.  Q and K arrive as 128 x 64 boxes of which the first
+// 16 columns are the tensor (the rest zero-filled by TMA), so the same
+// 128-byte-swizzled layouts and descriptors as the attention kernels serve
+// every operand.  The "1" column is a constant shared-memory box.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tk_attn.h"
+#include "tk_attn_internal.h"
+#include "tk_ptx.cuh"
+#include "tk_sync.cuh"
+
+namespace tk {
+namespace based {
+
+constexpr int C = 128;             // rows per chunk
+constexpr int DQK = 16;
+constexpr int DV = 64;
+constexpr int F = 192;             // feature columns (153 live)
+constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
+constexpr int NUM_THREADS = 192;
+constexpr int WARP_TMA = 4;
+constexpr int WARP_MMA = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ROLE_BASED_PRODUCER = 12;
+constexpr uint32_t ROLE_BASED_MMA = 13;
+constexpr uint32_t ROLE_BASED_COMPUTE = 14;
+
+constexpr uint32_t BOX = 128 * 128;                   // 128 rows x 128 bytes
+constexpr uint32_t QKV_OFF = 0;                       // buffer b: Q, K, V boxes at + b * 3 * BOX
+constexpr uint32_t ONES_OFF = QKV_OFF + 6 * BOX;      // [row][col]: 1 in column 0
+constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 192 features (3 boxes)
+constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
+constexpr uint32_t SPREV_OFF = PHIK_OFF + 3 * BOX;    // S (bf16, K-major): 80 rows x 192 features (3 boxes)
+constexpr uint32_t BAR_OFF = SPREV_OFF + 3 * SBOX;
+constexpr int B_FULL = 0;          // + buffer (2)
+constexpr int B_EMPTY = 2;         // + buffer (2)
+constexpr int B_SFULL = 4;         // Q K^T in TMEM
+constexpr int B_PREADY = 5;        // P, phi(Q) in TMEM, phi(K) in smem (4 warps)
+constexpr int B_ODONE = 6;         // intra + inter products done
+constexpr int B_STDONE = 7;        // state product done
+constexpr int B_SREADY = 8;        // bf16 copy of the state in smem (4 warps)
+constexpr int B_MMADONE = 9;
+constexpr int NUM_BARS = 10;
+constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+static_assert(SBOX % 1024 == 0 && SPREV_OFF % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+
+constexpr uint32_t T_S = 0;        // Q K^T (fp32, 128 cols); P (bf16) over cols 0..63
+constexpr uint32_t T_PHIQ = 128;   // phi(Q) bf16: 96 cols
+constexpr uint32_t T_O = 224;      // [num | den] fp32: 80 cols
+constexpr uint32_t T_ST = 320;     // S^T fp32: 192 cols (lane = value column, 64 = the "1" row)
+
+__device__ __forceinline__ uint32_t sw128(uint32_t box, int r, int c) { return box + r * 128 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// phi(x) as 96 packed bf16 pairs: [1, r x_a (16), h x_a^2 (16),
+// g x_a x_b for a < b in order (120), 0 (39)].  Every index is a compile-time
+// constant once the loops are unrolled.
+__device__ __forceinline__ void phi_packed(const float (&x)[DQK], float r, float h, float g, uint32_t (&pk)[F / 2]) {
+    float f[F];
+    f[0] = 1.0f;
+#pragma unroll
+    for (int a = 0; a < DQK; ++a) f[1 + a] = r * x[a];
+#pragma unroll
+    for (int a = 0; a < DQK; ++a) f[17 + a] = h * x[a] * x[a];
+#pragma unroll
+    for (int a = 0; a < DQK; ++a)
+#pragma unroll
+        for (int b = a + 1; b < DQK; ++b) f[33 + a * 15 - a * (a - 1) / 2 + (b - a - 1)] = g * x[a] * x[b];
+#pragma unroll
+    for (int q = 153; q < F; ++q) f[q] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < F / 2; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+}
+
+// The 16 features of row r of a 128-byte-swizzled 128 x 64 bf16 box (its
+// first two 16-byte chunks).
+__device__ __forceinline__ void load_row16(uint32_t box, int r, float (&x)[DQK]) {
+    const uint4 lo = ld_shared_v4(sw128(box, r, 0));
+    const uint4 hi = ld_shared_v4(sw128(box, r, 1));
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int bh = blockIdx.x;
+    const int n_chunks = (p.N + C - 1) / C;
+
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_FULL + b), 1);
+            mbar_init(bar(B_EMPTY + b), 1);
+        }
+        mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_PREADY), 4);
+        mbar_init(bar(B_ODONE), 1);
+        mbar_init(bar(B_STDONE), 1);
+        mbar_init(bar(B_SREADY), 4);
+        mbar_init(bar(B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp < 4) {
+        // the constant box: 1 in column 0 of every row, 0 elsewhere
+        const int r = threadIdx.x;
+        const uint32_t one = 0x3F80u;  // bf16 1.0 in the low half (column 0)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(sw128(sbase + ONES_OFF, r, c), c == 0 ? one : 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmQ);
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            int issued = 0;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int b = c & 1;
+                if (c >= 2 && !wait_bounded(bar(B_EMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
+                                            (ROLE_BASED_PRODUCER << 24) | ((B_EMPTY + b) << 16) | c)) {
+                    const uint64_t t0 = global_timer_ns();
+                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                        while (!mbar_try_wait(bar(B_FULL + (j & 1)), (j >> 1) & 1) &&
+                               global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    break;
+                }
+                // Q and K boxes carry 16 real columns; TMA fills the rest with 0
+                // but still counts the full box.
+                const uint32_t dst = sbase + QKV_OFF + b * 3 * BOX;
+                mbar_arrive_expect_tx(bar(B_FULL + b), 3 * BOX);
+                tma_load_3d(dst, &p.tmQ, bar(B_FULL + b), 0, c * C, bh);
+                tma_load_3d(dst + BOX, &p.tmK, bar(B_FULL + b), 0, c * C, bh);
+                tma_load_3d(dst + 2 * BOX, &p.tmV, bar(B_FULL + b), 0, c * C, bh);
+                ++issued;
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);       // Q K^T
+            constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
+            constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
+            constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
+            bool ok = true;
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int b = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX, vb = qb + 2 * BOX;
+                if (!(ok = wait_bounded(bar(B_FULL + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | ((B_FULL + b) << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                umma_ss(tmem + T_S, smem_desc_sw128(qb, 16, 1024), smem_desc_sw128(kb, 16, 1024), ID_S, 0);
+                umma_commit(bar(B_SFULL));
+                if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | c)))
+                    break;
+                // the bf16 state of the previous chunks is in smem
+                if (c > 0 && !(ok = wait_bounded(bar(B_SREADY), ph ^ 1, abort_flag,
+                                                 (ROLE_BASED_MMA << 24) | (B_SREADY << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                // intra: [num | den] = P [V | 1]; 16 chunk rows per step
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ts(tmem + T_O, tmem + T_S + k * 8,
+                            smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
+                // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
+                if (c > 0) {
+#pragma unroll
+                    for (int k = 0; k < F / 16; ++k)
+                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8,
+                                smem_desc_sw128(sbase + SPREV_OFF + (k / 4) * SBOX + (k % 4) * 32, 16, 1024),
+                                ID_INTER, 1);
+                }
+                umma_commit(bar(B_ODONE));
+                // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
+                            smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE, (c > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(B_STDONE));
+                umma_commit(bar(B_EMPTY + b));
+            }
+            umma_commit(bar(B_MMADONE));
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ compute warps
+        const int i = threadIdx.x;  // row of the chunk = TMEM lane; also row i of S^T
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float scale = p.scale;
+        const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
+        const size_t head_row0 = static_cast<size_t>(bh) * p.N;
+        bool ok = true;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int b = c & 1;
+            const uint32_t ph = c & 1;
+            const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX;
+            const int row = c * C + i;  // sequence position of this thread's query and key
+            if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | c)))
+                break;
+            tc_fence_after_sync();
+            // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N)
+            {
+                const int jmax = min(i, p.N - 1 - c * C);  // last key of the chunk this row sees
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[64];
+                    tmem_ld64(lane_base + T_S + half * 64, sr);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j0 = half * 64 + 2 * e;
+                        const float s0 = scale * __uint_as_float(sr[2 * e]);
+                        const float s1 = scale * __uint_as_float(sr[2 * e + 1]);
+                        const float w0 = j0 <= jmax ? fmaf(0.5f * s0, s0, s0 + 1.0f) : 0.0f;
+                        const float w1 = j0 + 1 <= jmax ? fmaf(0.5f * s1, s1, s1 + 1.0f) : 0.0f;
+                        pk[e] = pack_bf16x2(w0, w1);
+                    }
+                    tmem_st32(lane_base + T_S + half * 32, pk);  // P over the first 64 columns
+                }
+            }
+            // --- phi(q_i) into TMEM (the A operand of the inter product)
+            {
+                float x[DQK];
+                load_row16(qb, i, x);
+                uint32_t pk[F / 2];
+                phi_packed(x, r, h, g, pk);
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+                    tmem_st32(lane_base + T_PHIQ + part * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * part));
+            }
+            // --- phi(k_i) into row i of the phi(K) boxes (0 for keys past N)
+            {
+                float x[DQK];
+                load_row16(kb, i, x);
+                if (row >= p.N) {
+#pragma unroll
+                    for (int a = 0; a < DQK; ++a) x[a] = 0.0f;
+                }
+                uint32_t pk[F / 2];
+                phi_packed(x, r, h, g, pk);
+                if (row >= p.N) pk[0] = 0u;  // the constant feature too: this key does not exist
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t box = sbase + PHIK_OFF + part * BOX;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(sw128(box, i, q), pk[32 * part + 4 * q], pk[32 * part + 4 * q + 1],
+                                     pk[32 * part + 4 * q + 2], pk[32 * part + 4 * q + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PREADY), lane);
+
+            // --- O_i = num_i / den_i
+            if (!(ok = wait_bounded(bar(B_ODONE), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | c)))
+                break;
+            tc_fence_after_sync();
+            {
+                uint32_t o[64], d[16];
+                tmem_ld64(lane_base + T_O, o);
+                tmem_ld16(lane_base + T_O + 64, d);
+                const float den = __uint_as_float(d[0]);
+                if (row < p.N) {
+                    const float inv = 1.0f / den;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                    p.DEN[head_row0 + row] = den;
+                }
+            }
+            // --- bf16 copy of the state S_{<=c} (rows 0..79 of S^T) for the next chunk
+            if (!(ok = wait_bounded(bar(B_STDONE), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
+                break;
+            tc_fence_after_sync();
+            if (c + 1 < n_chunks) {
+#pragma unroll
+                for (int part = 0; part < 3; ++part) {
+                    uint32_t sv[64];
+                    tmem_ld64(lane_base + T_ST + part * 64, sv);  // every lane loads; rows >= 80 are not stored
+                    if (i < NV) {
+                        const uint32_t box = sbase + SPREV_OFF + part * SBOX;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(sw128(box, i, q),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                warp_arrive(bar(B_SREADY), lane);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace based
+
+cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        if ((err = cudaFuncSetAttribute(based::based_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        based::SMEM_ALLOC)) != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH), 1, 1);
+    cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = based::SMEM_ALLOC;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, based::based_kernel, p);
+}
+
+cudaError_t read_and_clear_based_status(uint32_t *status, uint32_t *detail) {
+    unsigned int vals[2] = {0, 0};
+    cudaError_t err = cudaMemcpyFromSymbol(&vals[0], g_status, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpyFromSymbol(&vals[1], g_detail, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    const unsigned int zero[1] = {0};
+    if ((err = cudaMemcpyToSymbol(g_status, zero, sizeof(unsigned int))) != cudaSuccess) return err;
+    if ((err = cudaMemcpyToSymbol(g_detail, zero, sizeof(unsigned int))) != cudaSuccess) return err;
+    *status = vals[0];
+    *detail = vals[1];
+    return cudaSuccess;
+}
+
+}  // namespace tk

@@ -437,6 +437,47 @@ int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t works
     return TK_OK;
 }
 
+// ------------------------------------------------------------------ Based linear attention
+
+int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H, int64_t N,
+                 int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream) {
+    if (!Q || !K || !V || !O || !DEN) return TK_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
+    if (Dqk != 16 || Dv != 64) return TK_ERR_UNSUPPORTED_D;
+    if (N > INT32_MAX || B > INT32_MAX / H || B * H > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    const int64_t BH = B * H;
+    if (BH > INT64_MAX / N / 64 / 2) return TK_ERR_BAD_SHAPE;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return TK_ERR_BAD_SCALE;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(DEN, 4))
+        return TK_ERR_MISALIGNED;
+    const uint64_t qk_bytes = static_cast<uint64_t>(BH) * N * 16 * 2, v_bytes = static_cast<uint64_t>(BH) * N * 64 * 2,
+                   den_bytes = static_cast<uint64_t>(BH) * N * 4;
+    const void *ins[3] = {Q, K, V};
+    const uint64_t in_bytes[3] = {qk_bytes, qk_bytes, v_bytes};
+    for (int a = 0; a < 3; ++a)
+        if (overlaps(O, v_bytes, ins[a], in_bytes[a]) || overlaps(DEN, den_bytes, ins[a], in_bytes[a]))
+            return TK_ERR_ALIAS;
+    if (overlaps(O, v_bytes, DEN, den_bytes)) return TK_ERR_ALIAS;
+    int num_sms = 0;
+    int rc = current_device(&num_sms);
+    if (rc != TK_OK) return rc;
+    const void *ptrs[5] = {Q, K, V, O, DEN};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    tk::BasedParams p;
+    if ((rc = encode_qkv_map(&p.tmQ, Q, N, 16, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmK, K, N, 16, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmV, V, N, 64, BH)) != TK_OK) return rc;
+    p.O = O;
+    p.DEN = DEN;
+    p.N = static_cast<int>(N);
+    p.BH = static_cast<int>(BH);
+    p.scale = scale;
+    cudaError_t e = tk::launch_based(p, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
+
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     uint32_t status = 0, where = 0, status_b = 0, where_b = 0, status_g = 0, where_g = 0;
     cudaError_t e = tk::read_and_clear_status(stream, &status, &where);  // synchronises the stream
@@ -445,8 +486,11 @@ int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     if (e != cudaSuccess) return fail_cuda(e);
     e = tk::read_and_clear_gemm_status(&status_g, &where_g);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (detail) *detail = status ? where : (status_b ? where_b : where_g);
-    return (status == 0 && status_b == 0 && status_g == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
+    uint32_t status_l = 0, where_l = 0;
+    e = tk::read_and_clear_based_status(&status_l, &where_l);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail) *detail = status ? where : (status_b ? where_b : (status_g ? where_g : where_l));
+    return (status == 0 && status_b == 0 && status_g == 0 && status_l == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
 }
 
 int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {

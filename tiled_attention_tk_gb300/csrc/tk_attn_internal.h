@@ -76,6 +76,21 @@ struct GemmParams {
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream);
 cudaError_t read_and_clear_gemm_status(uint32_t *status, uint32_t *detail);
 
+// Everything the Based linear-attention kernel needs (Dqk = 16, Dv = 64).
+struct BasedParams {
+    CUtensorMap tmQ;   // 3-D {16, N, B*H} bf16, box {64, 128, 1} (columns 16..63 read as 0), 128-byte swizzle
+    CUtensorMap tmK;
+    CUtensorMap tmV;   // 3-D {64, N, B*H} bf16, box {64, 128, 1}
+    void *O;           // bf16 [B*H, N, 64]
+    float *DEN;        // fp32 [B*H, N]
+    int N;
+    int BH;
+    float scale;
+};
+
+cudaError_t launch_based(const BasedParams &p, cudaStream_t stream);
+cudaError_t read_and_clear_based_status(uint32_t *status, uint32_t *detail);
+
 // Size of the library-owned workspace behind tk_attn_bwd_noalloc.
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 
