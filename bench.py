@@ -22,6 +22,11 @@ with nvidia-smi during the timed region) and ``gpu_launches``.
 10*B*H*N^2*D, halved under the causal mask), with the fp64 backward oracle as
 the CPU baseline.
 
+``--based``: causal Based linear attention (tk_based_fwd, B8 H16 N4096, feature
+dim 16, value dim 64), reported as GB/s of algorithmic HBM traffic against the
+measured HBM bandwidth (the linear form's arithmetic intensity is below the
+ridge).
+
 ``--gemm``: the same line for the GEMM on the same pipeline (tk_gemm,
 C = A B^T, M = N = K = 8192 unless ``--gemm-shape M,N,K``; flops 2*M*N*K), with
 the fp64 oracle GEMM on sampled rows as the CPU baseline and cuBLAS (through
@@ -616,6 +621,122 @@ def run_reference_gemm(args):
             "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- Based linear attention
+
+BASED_METRIC = ("Based linear attention GB/s of algorithmic HBM traffic on 1 GB300 "
+                "(fraction of measured HBM bandwidth) vs CPU oracle")
+BASED_SOURCES = ["tiled_attention_tk_gb300/csrc/based.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
+                 "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
+
+
+def hbm_peak():
+    """(HBM GB/s, label) from MEASURED_PEAKS.json, else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = json.load(f).get("hbm_gbs")
+        if isinstance(v, dict):
+            v = v.get("value")
+        if v:
+            return float(v), "of measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return 6800.0, "of fallback"
+
+
+def based_inputs(B, H, N):
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(8000)
+    q = torch.randn((B, H, N, 16), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, N, 16), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, N, 64), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+def run_based(args):
+    """One step = tk_based_fwd over B8 H16 N4096 (Dqk 16, Dv 64) unless
+    --based-shape B,H,N.  Value: algorithmic bytes (Q, K, V read once, O and
+    DEN written once) per second; the chunked linear form's flops are reported
+    beside it."""
+    import torch
+    import tiled_attention_tk_gb300 as tk
+    B, H, N = (int(x) for x in args.based_shape.split(","))
+    _, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = based_inputs(B, H, N)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+    den = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        tk.based(qd, kd, vd, scale=0.25, out=o, den=den, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = sum(x.elapsed_time(y) for x, y in ev) / args.steps
+    st, detail = tk.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
+    tokens = B * H * N
+    alg_bytes = tokens * (16 * 2 + 16 * 2 + 64 * 2 + 64 * 2 + 4)
+    # chunked linear form per token: in-chunk Q K^T and P [V|1] (causal half of
+    # 128 rows), carried phi(Q) S and state update [V|1]^T phi(K) (153 x 65)
+    flops = tokens * (2 * 16 * 64 + 2 * 65 * 64 + 2 * (2 * 153 * 65))
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    peak, label = hbm_peak()
+    if rank != 0:
+        return None
+    line = {
+        "metric": BASED_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch.Generator, N(0,1) fp32 draws rounded to bf16)",
+        "config": {"workload": f"based-B{B}H{H}N{N}", "B": B, "H": H, "N": N, "Dqk": 16, "Dv": 64,
+                   "scale": 0.25, "causal": True, "alg_bytes": alg_bytes,
+                   "l2": "inputs > L2, no flush" if tokens * 192 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_source": label, "traffic": None,
+                     "kernel": "based_kernel", "kernel_ms": round(ms, 5)},
+        "linear_form_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t_total, rows_done, heads = 0.0, 0, 0
+        start = time.perf_counter()
+        while time.perf_counter() - start < args.cpu_budget and heads < B * H:
+            b, h = divmod(heads, H)
+            rows = list(range(N - 256, N))  # the longest rows of the head
+            t0 = time.perf_counter()
+            oracle.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
+            t_total += time.perf_counter() - t0
+            rows_done += len(rows)
+            heads += 1
+        # the quadratic form reads every earlier key once per row: bytes of the
+        # rows' own inputs/outputs, scaled to the workload by rows
+        cpu_gbs = rows_done * (alg_bytes / tokens) / t_total / 1e9
+        line["cpu_baseline"] = {"value": round(cpu_gbs, 6), "unit": "GB/s", "cores": oracle.last_threads(),
+                                "kind": "oracle",
+                                "sample": f"the last 256 rows of {heads} head(s), quadratic form in fp64 "
+                                          f"({t_total:.1f} s)"}
+    return line
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args, w):
@@ -690,6 +811,8 @@ def main(argv=None):
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
     ap.add_argument("--gemm", action="store_true", help="time the GEMM on the same pipeline instead")
     ap.add_argument("--gemm-shape", type=str, default="8192,8192,8192", help="M,N,K for --gemm")
+    ap.add_argument("--based", action="store_true", help="time the Based linear attention instead")
+    ap.add_argument("--based-shape", type=str, default="8,16,4096", help="B,H,N for --based")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -707,6 +830,11 @@ def main(argv=None):
         todo = [Workload(0, f[0], f[1], f[2], f[3], bool(f[4]), "normal", f[5] if len(f) == 6 else None)]
     else:
         todo = [WORKLOADS[i] for i in (sorted(WORKLOADS) if args.all else [args.workload])]
+    if args.based:
+        line = run_based(args)
+        if line is not None and rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.gemm:
         line = run_reference_gemm(args) if args.impl == "reference" else run_gemm(args)
         if line is not None and rank == 0:
