@@ -595,11 +595,21 @@ def run_gemm(args):
 
 
 def gemm_traffic_for(name: str):
+    return sources_traffic_for(name, GEMM_SOURCES)
+
+
+def sources_traffic_for(name: str, sources):
+    """DRAM bytes per launch recorded in profiles/traffic.json for workload
+    `name`, if taken on the current source of the kernel's files; else None."""
+    h = hashlib.sha256()
+    for rel in sources:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             e = json.load(f).get(name)
-        if e and e.get("kernel_source_hash") == gemm_source_hash():
+        if e and e.get("kernel_source_hash") == h.hexdigest()[:16]:
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError, TypeError, AttributeError):
         pass
@@ -707,7 +717,8 @@ def run_based(args):
                    "scale": 0.25, "causal": True, "alg_bytes": alg_bytes,
                    "l2": "inputs > L2, no flush" if tokens * 192 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "peak_source": label, "traffic": None,
+                     "frac": round(gbs / peak, 4), "peak_source": label,
+                     "traffic": sources_traffic_for(f"based-B{B}H{H}N{N}", BASED_SOURCES),
                      "kernel": "based_kernel", "kernel_ms": round(ms, 5)},
         "linear_form_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
         "tokens_per_s": round(tokens / (ms * 1e-3), 1),
