@@ -84,3 +84,27 @@ def test_bwd_invariants_and_determinism():
     dq2, dk2, dv2 = _run(q, k, v, do, True, 0.125)
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
     assert (dq.double() - dq2.double()).abs().max().item() <= 1e-2
+
+
+@pytest.mark.parametrize("idx,heads", [(4, [(0, 0), (15, 31)]), (3, [(3, 15)])])
+def test_bwd_bench_workload_sampled(oracle_mod, idx, heads):
+    """The benchmark's backward launches at full size (B16 H32 N1024 D128 wide
+    logits; B4 H16 N4096 D128 causal), with the incoming gradient the
+    benchmark draws, checked on sampled heads against the oracle's backward of
+    those heads."""
+    from tiled_attention_tk_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[idx]
+    q, k, v = workload_inputs(w)
+    do = make_qkv(w.B, w.H, w.N, w.D, 1000 * w.index + 500, "normal")[0]
+    got = _run(q, k, v, do, w.causal, w.scale)
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle_mod.attn_bwd(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(),
+                                  do[sl].contiguous(), w.causal, w.scale)
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            g = g[sl].double().numpy()
+            err = np.abs(g - r)
+            assert err.max() <= 0.02 * np.abs(r).max() + 1e-4, (
+                f"{w.name} head ({b},{h}) {name}: max err {err.max():.3e} vs max|ref| {np.abs(r).max():.3e}")
+            assert err.mean() <= 0.01 * np.abs(r).mean() + 1e-5, (
+                f"{w.name} head ({b},{h}) {name}: mean err {err.mean():.3e}")
