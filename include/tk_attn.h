@@ -45,7 +45,7 @@ enum {
     TK_OK = 0,
     TK_ERR_NULL_PTR = 1,           /* a required pointer is NULL                       */
     TK_ERR_BAD_SHAPE = 2,          /* B, H or N < 1, or B*H*N*D overflows               */
-    TK_ERR_UNSUPPORTED_D = 3,      /* head dim other than 64 or 128                      */
+    TK_ERR_UNSUPPORTED_D = 3,      /* head dim the entry point does not take              */
     TK_ERR_MISALIGNED = 4,         /* Q, K, V or O not 16-byte aligned, LSE not 4-byte   */
     TK_ERR_BAD_SCALE = 5,          /* scale not finite or not > 0                         */
     TK_ERR_ALIAS = 6,              /* O or LSE overlaps an input, or O overlaps LSE       */
@@ -72,7 +72,7 @@ enum {
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 1.
  *            Any N >= 1: the last key tile is masked, the last query tile's
  *            extra rows are neither computed into nor stored.
- *   D        head dimension: 64 or 128.
+ *   D        head dimension: 32, 64, 96 or 128 (the backward: 64 or 128).
  *   causal   0: every query sees every key; 1: query i sees keys j <= i.
  *   scale    multiplier of Q K^T, finite and > 0 (usually 1/sqrt(D)).
  *   stream   CUDA stream the kernel is enqueued on (0 = legacy default).

@@ -50,6 +50,8 @@ def _assert_close(o, lse, O_ref, L_ref, what):
     (1, 2, 257, 128, 64, False),    # more queries than keys (non-causal)
     (1, 2, 1000, 17, 128, False),
     (1, 2, 384, 384, 64, True),     # equal lengths through the same entry point
+    (1, 2, 200, 700, 96, True),     # half-box head dims
+    (2, 2, 130, 260, 32, True),
 ])
 def test_kv_parity(oracle_mod, B, H, Nq, Nkv, D, causal):
     q, k, v = make_qkv_rect(B, H, Nq, Nkv, D, 7000 + Nq + Nkv + D)

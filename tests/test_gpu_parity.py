@@ -7,7 +7,8 @@ bf16 at the end (as the "ThunderKittens" kernel on 10100.com/article/71410160
 does, section "writing a kernel with TK", consumer::compute "convert to bf16
 for mma"); both roundings stay well inside the bar.
 
-Small cases are compared in full.  The five named workloads run at full size,
+Small cases are compared in full (head dims 32, 64, 96 and 128; 32 and 96
+fill half of the last 64-column box).  The five named workloads run at full size,
 in the same single launch the benchmark times, and are compared on sampled
 heads (and, for the longest one, sampled rows) that the oracle computes.
 """
@@ -58,7 +59,7 @@ def _check_full(oracle_mod, q, k, v, causal, scale, what):
 
 # ---------------------------------------------------------------- shape sweep
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 255, 256, 384, 1000])
 def test_shape_sweep(oracle_mod, N, D, causal):

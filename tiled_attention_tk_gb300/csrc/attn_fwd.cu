@@ -68,11 +68,13 @@ constexpr float kRescaleLog2 = 24.0f;
 
 template <int D>
 struct Layout {
-    static constexpr int KATOMS = D / 64;                 // 128-byte swizzle atoms along D
+    // 128-byte swizzle atoms (TMA boxes of 64 columns) along D; for D = 32
+    // and 96 the last box is half full (TMA fills the columns past D with 0).
+    static constexpr int KATOMS = (D + 63) / 64;
     static constexpr uint32_t BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
-    static constexpr uint32_t TILE_BYTES = BM * D * 2;    // one 128-row tile
-    static constexpr int NSLOTS = D == 128 ? 4 : 8;       // K/V ring slots (K_j, V_j alternate)
-    static_assert(D % 64 == 0, "head dim in whole 128-byte swizzle atoms");
+    static constexpr uint32_t TILE_BYTES = KATOMS * BOX_BYTES;  // one 128-row tile, whole boxes
+    static constexpr int NSLOTS = D > 64 ? 4 : 8;         // K/V ring slots (K_j, V_j alternate)
+    static_assert(D % 32 == 0 && D >= 32 && D <= 128, "head dim 32, 64, 96 or 128");
     static constexpr uint32_t Q_OFF = 0;                  // Q tile i at Q_OFF + i * TILE_BYTES
     static constexpr uint32_t SLOT_OFF = 2 * TILE_BYTES;
     // O staging for the TMA store: one 128-row x 64-column box per softmax
@@ -466,13 +468,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
 #pragma unroll
             for (int h = 0; h < L::KATOMS; ++h) {
                 uint32_t ob[32];
-                {
+                if (D - h * 64 >= 64) {
                     uint32_t rr[64];
                     tmem_ld64(o_addr + h * 64, rr);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
                                             __uint_as_float(rr[2 * i + 1]) * inv_l);
+                } else {
+                    // a half box (D = 32, 96): the other 32 columns are not
+                    // this tile's, and the store clips them at D
+                    uint32_t rr[32];
+                    tmem_ld32(o_addr + h * 64, rr);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                                            __uint_as_float(rr[2 * i + 1]) * inv_l);
+#pragma unroll
+                    for (int i = 16; i < 32; ++i) ob[i] = 0u;
                 }
                 if (h == L::KATOMS - 1) {
                     tc_fence_before_sync();
@@ -551,7 +564,9 @@ static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t strea
 
 cudaError_t launch_attn_fwd(int D, const AttnParams &p, int num_sms, cudaStream_t stream) {
     if (num_sms < 1) return cudaErrorInvalidValue;
+    if (D == 32) return launch_d<32>(p, num_sms, stream);
     if (D == 64) return launch_d<64>(p, num_sms, stream);
+    if (D == 96) return launch_d<96>(p, num_sms, stream);
     if (D == 128) return launch_d<128>(p, num_sms, stream);
     return cudaErrorInvalidValue;
 }

@@ -243,7 +243,7 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     // ---- host-side validation: nothing is enqueued unless all of it passes
     if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
     if (B < 1 || H < 1 || Nq < 1 || Nkv < 1) return TK_ERR_BAD_SHAPE;
-    if (D != 64 && D != 128) return TK_ERR_UNSUPPORTED_D;
+    if (D != 32 && D != 64 && D != 96 && D != 128) return TK_ERR_UNSUPPORTED_D;
     // TMA coordinates and the launch grid are 32-bit.
     if (Nq > INT32_MAX || Nkv > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
     const int64_t BH = B * H;
@@ -509,7 +509,8 @@ const char *tk_attn_strerror(int code) {
         case TK_OK: return "success";
         case TK_ERR_NULL_PTR: return "a required pointer is NULL";
         case TK_ERR_BAD_SHAPE: return "invalid shape (B, H, N must be >= 1 and sizes must fit)";
-        case TK_ERR_UNSUPPORTED_D: return "unsupported head dimension (64 or 128)";
+        case TK_ERR_UNSUPPORTED_D:
+            return "unsupported head dimension (forward: 32, 64, 96, 128; backward: 64, 128; Based: 16 / 64)";
         case TK_ERR_MISALIGNED: return "misaligned pointer (Q, K, V, O: 16 bytes; LSE: 4 bytes)";
         case TK_ERR_BAD_SCALE: return "scale must be finite and > 0";
         case TK_ERR_ALIAS: return "outputs overlap inputs or each other";
