@@ -1,7 +1,8 @@
 """fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
 
 This package is the checker, not the product (attention forward and backward,
-the plain GEMM the same tile pipeline runs, and Based linear attention).  Only ``tests/``,
+the plain GEMM the same tile pipeline runs, and Based and Hedgehog linear
+attention).  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may load
 it.  It shares no code with the CUDA library and imports nothing from it.
 
@@ -92,6 +93,8 @@ def _declare(lib) -> None:
     lib.tkor_based.restype = ctypes.c_int
     lib.tkor_based_rows.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, i64, P, P, ctypes.c_int]
     lib.tkor_based_rows.restype = ctypes.c_int
+    lib.tkor_hedgehog_rows.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, i64, P, P]
+    lib.tkor_hedgehog_rows.restype = ctypes.c_int
     lib.tkor_last_threads.argtypes = []
     lib.tkor_last_threads.restype = ctypes.c_int
 
@@ -249,6 +252,29 @@ def based(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
         DEN = np.empty((r.size,), dtype=np.float64)
         rc = lib.tkor_based_rows(_ptr(qb), _ptr(kb), _ptr(vb), N, Dqk, Dv, float(scale), _ptr(r), r.size,
                                  _ptr(O), _ptr(DEN), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return O, DEN
+
+
+def hedgehog(q, k, v, wq, wk, rows=None, lib=None):
+    """Causal Hedgehog linear attention, plain quadratic form in fp64, for ONE
+    head: q, k [N,d], v [N,Dv], wq, wk [d,f] (bf16).  phi(x) =
+    [softmax(x W), softmax(-x W)], w_ij = phi_q(q_i) . phi_k(k_j),
+    O_i = sum_{j<=i} w_ij v_j / DEN_i.  Returns (O [len,Dv], DEN [len]) for
+    ``rows`` (default: all rows)."""
+    qb, kb, vb, wqb, wkb = _bits(q), _bits(k), _bits(v), _bits(wq), _bits(wk)
+    if qb.ndim != 2 or qb.shape != kb.shape or vb.shape[0] != qb.shape[0] or wqb.shape != wkb.shape \
+            or wqb.shape[0] != qb.shape[1]:
+        raise ValueError("q, k [N,d], v [N,Dv], wq, wk [d,f] expected")
+    N, d = qb.shape
+    f = wqb.shape[1]
+    Dv = vb.shape[1]
+    r = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    O = np.empty((r.size, Dv), dtype=np.float64)
+    DEN = np.empty((r.size,), dtype=np.float64)
+    rc = (lib or _load()).tkor_hedgehog_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(wqb), _ptr(wkb), N, d, f, Dv,
+                                             _ptr(r), r.size, _ptr(O), _ptr(DEN))
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return O, DEN

@@ -593,3 +593,77 @@ int tkor_based(const uint16_t *Q, const uint16_t *K, const uint16_t *V, double *
     }
     return 0;
 }
+
+/* ======================================================================== */
+/* Hedgehog linear attention (causal), the other linear-attention variant   */
+/* the pages list ("LoLCATS Hedgehog Linear Attention", thebeat.tech        */
+/* "ThunderKittens 2.0", New Kernels), named without a formula.  Reading:   */
+/* the Hedgehog feature map, a softmax over a learned projection and over   */
+/* its negation, on queries and keys of dimension d with f features each:   */
+/*   phi_q(x) = [softmax(x Wq), softmax(-x Wq)],  phi_k likewise with Wk    */
+/*   w_ij  = phi_q(q_i) . phi_k(k_j)                      (> 0)             */
+/*   DEN_i = sum_{j <= i} w_ij,   O_i = sum_{j <= i} w_ij V_j / DEN_i       */
+/* in its plain quadratic form, fp64 from the exact bf16 inputs; every      */
+/* softmax is taken with its maximum subtracted.                             */
+
+static void hedgehog_phi(const uint16_t *x, const uint16_t *W, int64_t d, int64_t f, double *phi) {
+    /* z = x W (f values), then the two softmaxes */
+    double zmax = -INFINITY, zmin = INFINITY;
+    for (int64_t c = 0; c < f; ++c) {
+        double z = 0.0;
+        for (int64_t a = 0; a < d; ++a) z += bf16_bits_to_double(x[a]) * bf16_bits_to_double(W[a * f + c]);
+        phi[c] = z;
+        if (z > zmax) zmax = z;
+        if (z < zmin) zmin = z;
+    }
+    double sp = 0.0, sn = 0.0;
+    for (int64_t c = 0; c < f; ++c) {
+        double z = phi[c];
+        phi[c] = exp(z - zmax);
+        phi[f + c] = exp(zmin - z);
+        sp += phi[c];
+        sn += phi[f + c];
+    }
+    for (int64_t c = 0; c < f; ++c) {
+        phi[c] /= sp;
+        phi[f + c] /= sn;
+    }
+}
+
+/* One head, selected rows (rows == NULL: all).  Q, K: bf16 bits [N,d];
+ * Wq, Wk: [d,f]; V: [N,Dv].  O: double [nrows,Dv]; DEN: double [nrows]. */
+int tkor_hedgehog_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const uint16_t *Wq,
+                       const uint16_t *Wk, int64_t N, int64_t d, int64_t f, int64_t Dv, const int64_t *rows,
+                       int64_t nrows, double *O, double *DEN) {
+    if (!Q || !K || !V || !Wq || !Wk || !O || !DEN || N < 1 || d < 1 || f < 1 || Dv < 1 || nrows < 0) return -1;
+    int64_t maxrow = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= N) return -1;
+        if (i > maxrow) maxrow = i;
+    }
+    double *phik = (double *)malloc(sizeof(double) * (size_t)(maxrow + 1) * (size_t)(2 * f));
+    double *phiq = (double *)malloc(sizeof(double) * (size_t)(2 * f));
+    if (!phik || !phiq) {
+        free(phik); free(phiq);
+        return -1;
+    }
+    for (int64_t j = 0; j <= maxrow && nrows > 0; ++j) hedgehog_phi(K + j * d, Wk, d, f, phik + j * 2 * f);
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        hedgehog_phi(Q + i * d, Wq, d, f, phiq);
+        double den = 0.0;
+        double *o = O + r * Dv;
+        for (int64_t e = 0; e < Dv; ++e) o[e] = 0.0;
+        for (int64_t j = 0; j <= i; ++j) {
+            double w = 0.0;
+            for (int64_t c = 0; c < 2 * f; ++c) w += phiq[c] * phik[j * 2 * f + c];
+            den += w;
+            for (int64_t e = 0; e < Dv; ++e) o[e] += w * bf16_bits_to_double(V[j * Dv + e]);
+        }
+        for (int64_t e = 0; e < Dv; ++e) o[e] /= den;
+        DEN[r] = den;
+    }
+    free(phik); free(phiq);
+    return 0;
+}

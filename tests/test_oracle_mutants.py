@@ -169,3 +169,31 @@ def test_based_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
         except AssertionError as e:
             caught.append((check.__name__, str(e)[:80]))
     assert caught, f"no pin caught the planted mistake: {name}"
+
+
+from tests import oracle_hedgehog_pins as hh_pins  # noqa: E402
+
+HEDGEHOG_MUTANTS = [
+    ("negated half dropped", "phi[f + c] = exp(zmin - z);", "phi[f + c] = 0.0;"),
+    ("negated half not negated", "phi[f + c] = exp(zmin - z);", "phi[f + c] = exp(z - zmax);"),
+    ("softmax not normalised", "phi[c] /= sp;", ""),
+    ("projection transposed", "bf16_bits_to_double(W[a * f + c])", "bf16_bits_to_double(W[(c % d) * f + (a % f)])"),
+    ("key map used for queries", "hedgehog_phi(Q + i * d, Wq, d, f, phiq);", "hedgehog_phi(Q + i * d, Wk, d, f, phiq);"),
+    ("not causal", "for (int64_t j = 0; j <= i; ++j) {\n            double w = 0.0;",
+     "for (int64_t j = 0; j <= (i > 0 ? i - 1 : 0); ++j) {\n            double w = 0.0;"),
+    ("output not normalised", "for (int64_t e = 0; e < Dv; ++e) o[e] /= den;", ""),
+]
+
+
+@pytest.mark.parametrize("name,orig,mutant", HEDGEHOG_MUTANTS, ids=[m[0] for m in HEDGEHOG_MUTANTS])
+def test_hedgehog_pins_catch_planted_mistake(tmp_path, name, orig, mutant):
+    text = open(SRC).read()
+    assert text.count(orig) == 1, f"mutation anchor for '{name}' not unique in the oracle"
+    lib = oracle.bind(_compile(text.replace(orig, mutant), tmp_path, "h" + str(abs(hash(name)))))
+    caught = []
+    for check in hh_pins.HEDGEHOG_CHECKS:
+        try:
+            check(lambda q, k, v, wq, wk, rows=None: oracle.hedgehog(q, k, v, wq, wk, rows=rows, lib=lib))
+        except AssertionError as e:
+            caught.append((check.__name__, str(e)[:80]))
+    assert caught, f"no pin caught the planted mistake: {name}"

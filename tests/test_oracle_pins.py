@@ -112,3 +112,11 @@ from tests import oracle_based_pins as based_pins  # noqa: E402
 @pytest.mark.parametrize("check", based_pins.BASED_CHECKS, ids=lambda c: c.__name__)
 def test_oracle_based_pin(oracle_mod, check):
     check(oracle_mod.based)
+
+
+from tests import oracle_hedgehog_pins as hh_pins  # noqa: E402
+
+
+@pytest.mark.parametrize("check", hh_pins.HEDGEHOG_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_hedgehog_pin(oracle_mod, check):
+    check(oracle_mod.hedgehog)
