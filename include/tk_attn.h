@@ -256,6 +256,27 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
                  int64_t N, int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream);
 
 /*
+ * tk_hedgehog_fwd -- causal Hedgehog linear attention (the pages list
+ * "LoLCATS Hedgehog Linear Attention", thebeat.tech "ThunderKittens 2.0", New
+ * Kernels; the formula is the Hedgehog feature map):
+ *     phi_q(x) = [softmax(x Wq), softmax(-x Wq)],  phi_k likewise with Wk
+ *     w_ij = phi_q(Q_i) . phi_k(K_j)  (j <= i),   DEN_i = sum_j w_ij,
+ *     O_i  = sum_j w_ij V_j / DEN_i
+ * in linear time (128-row chunks, running state of the 128 features).
+ *
+ * Arguments
+ *   Q, K, V, O   device bf16 [B, H, N, 64], 16-byte aligned (O written).
+ *   Wq, Wk       device bf16 [H, Dqk = 64, F = 64] (the projection of head h
+ *                is Wq[h], row-major [64][64]), 16-byte aligned.
+ *   DEN          device fp32 [B, H, N] (written).
+ *   Dqk, F, Dv   must be 64, 64, 64 (else TK_ERR_UNSUPPORTED_D).
+ * Semantics, ownership and errors as tk_attn_fwd.  Deterministic.
+ */
+int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O,
+                    float *DEN, int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t F, int64_t Dv,
+                    cudaStream_t stream);
+
+/*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the
  * current device's kernel status word.  Returns TK_OK if no bounded wait of
  * any kernel of this library on this device has given up since the last

@@ -217,3 +217,31 @@ def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None
                                       B, H, N, Dqk, Dv, float(scale), _stream_handle(stream))
     _lib.check(rc, "tk_based_fwd")
     return out, den
+
+
+def hedgehog(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
+             out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None):
+    """Causal Hedgehog linear attention.  q, k, v: bf16 [B,H,N,64]; wq, wk:
+    bf16 [H,64,64] (CUDA).  phi(x) = [softmax(x W), softmax(-x W)];
+    returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]).  Enqueued without
+    synchronising."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA bf16 [B,H,N,D] tensor")
+    for t, n in ((wq, "wq"), (wk, "wk")):
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or t.device.type != "cuda":
+            raise ValueError(f"{n} must be a CUDA bf16 [H,d,f] tensor")
+    if q.shape != k.shape or v.shape[:3] != q.shape[:3] or wq.shape != wk.shape or wq.shape[0] != q.shape[1]:
+        raise ValueError("q, k [B,H,N,d], v [B,H,N,Dv], wq, wk [H,d,f] must agree")
+    B, H, N, d = q.shape
+    f, Dv = wq.shape[2], v.shape[3]
+    q, k, v, wq, wk = (t.contiguous() for t in (q, k, v, wq, wk))
+    if out is None:
+        out = torch.empty((B, H, N, Dv), dtype=torch.bfloat16, device=q.device)
+    if den is None:
+        den = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = _lib.load().tk_hedgehog_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                         out.data_ptr(), den.data_ptr(), B, H, N, d, f, Dv, _stream_handle(stream))
+    _lib.check(rc, "tk_hedgehog_fwd")
+    return out, den

@@ -1,0 +1,409 @@
+// hedgehog.cu -- causal Hedgehog linear attention on tcgen05 (sm_103a, GB300).
+//
+// The pages list "LoLCATS Hedgehog Linear Attention" among the kernels built
+// with the same tiles (thebeat.tech "ThunderKittens 2.0", New Kernels) without
+// a formula.  The reading taken is the Hedgehog feature map, a softmax over a
+// learned projection of the query (key) and over its negation:
+//
+//   phi_q(x) = [softmax(x Wq), softmax(-x Wq)],  phi_k(x) likewise with Wk
+//   w_ij = phi_q(q_i) . phi_k(k_j),  O_i = sum_{j<=i} w_ij v_j / DEN_i,
+//   DEN_i = sum_{j<=i} w_ij
+//
+// for d = 64 query/key dims, f = 64 features per half (128 in all) and
+// value dim 64.  Same chunked linear form as the Based kernel: per 128-row
+// chunk, Z = Q Wq and K Wk on the tensor core, the feature maps in the
+// compute warps (into shared memory), S = phi(Q) phi(K)^T on the tensor core,
+// the causal mask (P over S in TMEM), then [num | den] = P [V | 1] +
+// phi(Q) S_{<c} and the state update S^T += [V | 1]^T phi(K).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tk_attn.h"
+#include "tk_attn_internal.h"
+#include "tk_ptx.cuh"
+#include "tk_sync.cuh"
+
+namespace tk {
+namespace hedgehog {
+
+constexpr int C = 128;             // rows per chunk
+constexpr int DQK = 64;            // query / key dims
+constexpr int FH = 64;             // features per half
+constexpr int F = 2 * FH;          // feature dims of phi
+constexpr int DV = 64;
+constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
+constexpr int NUM_THREADS = 192;
+constexpr int WARP_TMA = 4;
+constexpr int WARP_MMA = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ROLE_HH_PRODUCER = 15;
+constexpr uint32_t ROLE_HH_MMA = 16;
+constexpr uint32_t ROLE_HH_COMPUTE = 17;
+
+constexpr uint32_t BOX = 128 * 128;                   // 128 rows x 128 bytes
+constexpr uint32_t WBOX = 64 * 128;                   // 64 rows x 128 bytes
+constexpr uint32_t QKV_OFF = 0;                       // buffer b: Q, K, V boxes at + b * 3 * BOX
+constexpr uint32_t WQ_OFF = QKV_OFF + 6 * BOX;        // Wq [d][f]
+constexpr uint32_t WK_OFF = WQ_OFF + WBOX;            // Wk [d][f]
+constexpr uint32_t ONES_OFF = WK_OFF + WBOX;          // [row][col]: 1 in column 0
+constexpr uint32_t PHIQ_OFF = ONES_OFF + BOX;         // phi(Q): 128 rows x 128 features (2 boxes)
+constexpr uint32_t PHIK_OFF = PHIQ_OFF + 2 * BOX;     // phi(K): same
+constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
+constexpr uint32_t SPREV_OFF = PHIK_OFF + 2 * BOX;    // S (bf16, K-major): 80 rows x 128 features (2 boxes)
+constexpr uint32_t BAR_OFF = SPREV_OFF + 2 * SBOX;
+constexpr int B_FULL = 0;          // + buffer (2)
+constexpr int B_EMPTY = 2;         // + buffer (2)
+constexpr int B_WFULL = 4;         // Wq, Wk loaded
+constexpr int B_ZFULL = 5;         // Q Wq, K Wk in TMEM
+constexpr int B_PHIREADY = 6;      // phi(Q), phi(K) in smem (4 warps)
+constexpr int B_SFULL = 7;         // phi(Q) phi(K)^T in TMEM
+constexpr int B_PREADY = 8;        // P in TMEM (4 warps)
+constexpr int B_ODONE = 9;         // intra + inter products done
+constexpr int B_STDONE = 10;       // state product done
+constexpr int B_SREADY = 11;       // bf16 state in smem (4 warps)
+constexpr int B_MMADONE = 12;
+constexpr int NUM_BARS = 13;
+constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+static_assert(WQ_OFF % 1024 == 0 && ONES_OFF % 1024 == 0 && SPREV_OFF % 1024 == 0 && SBOX % 1024 == 0,
+              "swizzled boxes need 1024-byte alignment");
+
+constexpr uint32_t T_Z = 0;        // Q Wq (cols 0..63), K Wk (64..127); then S; P (bf16) over 0..63
+constexpr uint32_t T_O = 128;      // [num | den] fp32: 80 cols
+constexpr uint32_t T_ST = 256;     // S^T fp32: 128 cols (lane = value column, 64 = the "1" row)
+
+__device__ __forceinline__ uint32_t sw128(uint32_t box, int r, int c) { return box + r * 128 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// phi(z) = [softmax(z), softmax(-z)] of one row's 64 projections, as 64
+// packed bf16 pairs (zeros when `live` is false), written to row r of a
+// two-box 128-feature K-major tile.
+__device__ __forceinline__ void write_phi(const uint32_t (&zr)[64], bool live, uint32_t tile, int r) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    float zmax = __uint_as_float(zr[0]), zmin = zmax;
+#pragma unroll
+    for (int c = 1; c < FH; ++c) {
+        const float z = __uint_as_float(zr[c]);
+        zmax = fmaxf(zmax, z);
+        zmin = fminf(zmin, z);
+    }
+    float ep[FH], en[FH];
+    float sp = 0.0f, sn = 0.0f;
+#pragma unroll
+    for (int c = 0; c < FH; ++c) {
+        const float z = __uint_as_float(zr[c]);
+        ep[c] = ex2((z - zmax) * kLog2e);
+        en[c] = ex2((zmin - z) * kLog2e);
+        sp += ep[c];
+        sn += en[c];
+    }
+    const float ip = live ? 1.0f / sp : 0.0f, in = live ? 1.0f / sn : 0.0f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const float *e = half == 0 ? ep : en;
+        const float sc = half == 0 ? ip : in;
+        const uint32_t box = tile + half * BOX;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            st_shared_v4(sw128(box, r, q), pack_bf16x2(e[8 * q] * sc, e[8 * q + 1] * sc),
+                         pack_bf16x2(e[8 * q + 2] * sc, e[8 * q + 3] * sc),
+                         pack_bf16x2(e[8 * q + 4] * sc, e[8 * q + 5] * sc),
+                         pack_bf16x2(e[8 * q + 6] * sc, e[8 * q + 7] * sc));
+    }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_constant__ HedgehogParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int bh = blockIdx.x;
+    const int head = bh % p.H;
+    const int n_chunks = (p.N + C - 1) / C;
+
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_FULL + b), 1);
+            mbar_init(bar(B_EMPTY + b), 1);
+        }
+        mbar_init(bar(B_WFULL), 1);
+        mbar_init(bar(B_ZFULL), 1);
+        mbar_init(bar(B_PHIREADY), 4);
+        mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_PREADY), 4);
+        mbar_init(bar(B_ODONE), 1);
+        mbar_init(bar(B_STDONE), 1);
+        mbar_init(bar(B_SREADY), 4);
+        mbar_init(bar(B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const uint32_t one = 0x3F80u;  // bf16 1.0 in the low half (column 0)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(sw128(sbase + ONES_OFF, r, c), c == 0 ? one : 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmQ);
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            tma_prefetch_desc(&p.tmWq);
+            tma_prefetch_desc(&p.tmWk);
+            mbar_arrive_expect_tx(bar(B_WFULL), 2 * WBOX);
+            tma_load_3d(sbase + WQ_OFF, &p.tmWq, bar(B_WFULL), 0, 0, head);
+            tma_load_3d(sbase + WK_OFF, &p.tmWk, bar(B_WFULL), 0, 0, head);
+            int issued = 0;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int b = c & 1;
+                if (c >= 2 && !wait_bounded(bar(B_EMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
+                                            (ROLE_HH_PRODUCER << 24) | ((B_EMPTY + b) << 16) | c)) {
+                    const uint64_t t0 = global_timer_ns();
+                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                        while (!mbar_try_wait(bar(B_FULL + (j & 1)), (j >> 1) & 1) &&
+                               global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    while (!mbar_try_wait(bar(B_WFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                    break;
+                }
+                const uint32_t dst = sbase + QKV_OFF + b * 3 * BOX;
+                mbar_arrive_expect_tx(bar(B_FULL + b), 3 * BOX);
+                tma_load_3d(dst, &p.tmQ, bar(B_FULL + b), 0, c * C, bh);
+                tma_load_3d(dst + BOX, &p.tmK, bar(B_FULL + b), 0, c * C, bh);
+                tma_load_3d(dst + 2 * BOX, &p.tmV, bar(B_FULL + b), 0, c * C, bh);
+                ++issued;
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_Z = idesc_bf16_f32(C, FH, 0, 1);       // X W: X K-major, W MN-major
+            constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);        // phi(Q) phi(K)^T
+            constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);   // P [V | 1]: A in TMEM
+            constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);   // phi(Q) S: both K-major
+            constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);    // [V | 1]^T phi(K): both MN-major
+            bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16));
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int b = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX, vb = qb + 2 * BOX;
+                if (!(ok = wait_bounded(bar(B_FULL + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_HH_MMA << 24) | ((B_FULL + b) << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                // Z = Q Wq, K Wk: 16 of the 64 dims per step
+#pragma unroll
+                for (int k = 0; k < DQK / 16; ++k) {
+                    umma_ss(tmem + T_Z, smem_desc_sw128(qb + k * 32, 16, 1024),
+                            smem_desc_sw128(sbase + WQ_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
+                    umma_ss(tmem + T_Z + FH, smem_desc_sw128(kb + k * 32, 16, 1024),
+                            smem_desc_sw128(sbase + WK_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
+                }
+                umma_commit(bar(B_ZFULL));
+                if (!(ok = wait_bounded(bar(B_PHIREADY), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_PHIREADY << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                // S = phi(Q) phi(K)^T over the 128 features (2 boxes)
+#pragma unroll
+                for (int k = 0; k < F / 16; ++k) {
+                    const uint32_t off = (k / 4) * BOX + (k % 4) * 32;
+                    umma_ss(tmem + T_Z, smem_desc_sw128(sbase + PHIQ_OFF + off, 16, 1024),
+                            smem_desc_sw128(sbase + PHIK_OFF + off, 16, 1024), ID_S, k > 0);
+                }
+                umma_commit(bar(B_SFULL));
+                if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_PREADY << 16) | c)))
+                    break;
+                if (c > 0 && !(ok = wait_bounded(bar(B_SREADY), ph ^ 1, abort_flag,
+                                                 (ROLE_HH_MMA << 24) | (B_SREADY << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                // intra: [num | den] = P [V | 1]
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ts(tmem + T_O, tmem + T_Z + k * 8,
+                            smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
+                // inter: [num | den] += phi(Q) S_{<c}
+                if (c > 0) {
+#pragma unroll
+                    for (int k = 0; k < F / 16; ++k)
+                        umma_ss(tmem + T_O, smem_desc_sw128(sbase + PHIQ_OFF + (k / 4) * BOX + (k % 4) * 32, 16, 1024),
+                                smem_desc_sw128(sbase + SPREV_OFF + (k / 4) * SBOX + (k % 4) * 32, 16, 1024),
+                                ID_INTER, 1);
+                }
+                umma_commit(bar(B_ODONE));
+                // state: S^T += [V | 1]^T phi(K)
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
+                            smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE,
+                            (c > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(B_STDONE));
+                umma_commit(bar(B_EMPTY + b));
+            }
+            umma_commit(bar(B_MMADONE));
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ compute warps
+        const int i = threadIdx.x;  // row of the chunk = TMEM lane; also row i of S^T
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const size_t head_row0 = static_cast<size_t>(bh) * p.N;
+        for (int c = 0; c < n_chunks; ++c) {
+            const uint32_t ph = c & 1;
+            const int row = c * C + i;
+            // --- feature maps phi(q_i), phi(k_i) (0 for keys past N)
+            if (!wait_bounded(bar(B_ZFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16) | c)) break;
+            tc_fence_after_sync();
+            {
+                uint32_t zr[64];
+                tmem_ld64(lane_base + T_Z, zr);
+                write_phi(zr, true, sbase + PHIQ_OFF, i);
+                tmem_ld64(lane_base + T_Z + FH, zr);
+                write_phi(zr, row < p.N, sbase + PHIK_OFF, i);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PHIREADY), lane);
+            // --- P = S under the causal mask (keys j <= i of the chunk and j < N)
+            if (!wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_SFULL << 16) | c)) break;
+            tc_fence_after_sync();
+            {
+                const int jmax = min(i, p.N - 1 - c * C);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[64];
+                    tmem_ld64(lane_base + T_Z + half * 64, sr);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j0 = half * 64 + 2 * e;
+                        pk[e] = pack_bf16x2(j0 <= jmax ? __uint_as_float(sr[2 * e]) : 0.0f,
+                                            j0 + 1 <= jmax ? __uint_as_float(sr[2 * e + 1]) : 0.0f);
+                    }
+                    tmem_st32(lane_base + T_Z + half * 32, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PREADY), lane);
+            // --- O_i = num_i / den_i
+            if (!wait_bounded(bar(B_ODONE), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ODONE << 16) | c)) break;
+            tc_fence_after_sync();
+            {
+                uint32_t o[64], d[16];
+                tmem_ld64(lane_base + T_O, o);
+                tmem_ld16(lane_base + T_O + 64, d);
+                const float den = __uint_as_float(d[0]);
+                if (row < p.N) {
+                    const float inv = 1.0f / den;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                    p.DEN[head_row0 + row] = den;
+                }
+            }
+            // --- bf16 copy of the state S_{<=c} (rows 0..79 of S^T) for the next chunk
+            if (!wait_bounded(bar(B_STDONE), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_STDONE << 16) | c)) break;
+            tc_fence_after_sync();
+            if (c + 1 < n_chunks) {
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t sv[64];
+                    tmem_ld64(lane_base + T_ST + part * 64, sv);  // every lane loads; rows >= 80 are not stored
+                    if (i < NV) {
+                        const uint32_t box = sbase + SPREV_OFF + part * SBOX;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            st_shared_v4(sw128(box, i, q),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
+                                         pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                warp_arrive(bar(B_SREADY), lane);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace hedgehog
+
+cudaError_t launch_hedgehog(const HedgehogParams &p, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        if ((err = cudaFuncSetAttribute(hedgehog::hedgehog_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        hedgehog::SMEM_ALLOC)) != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH), 1, 1);
+    cfg.blockDim = dim3(hedgehog::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = hedgehog::SMEM_ALLOC;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, hedgehog::hedgehog_kernel, p);
+}
+
+cudaError_t read_and_clear_hedgehog_status(uint32_t *status, uint32_t *detail) {
+    unsigned int vals[2] = {0, 0};
+    cudaError_t err = cudaMemcpyFromSymbol(&vals[0], g_status, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpyFromSymbol(&vals[1], g_detail, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    const unsigned int zero[1] = {0};
+    if ((err = cudaMemcpyToSymbol(g_status, zero, sizeof(unsigned int))) != cudaSuccess) return err;
+    if ((err = cudaMemcpyToSymbol(g_detail, zero, sizeof(unsigned int))) != cudaSuccess) return err;
+    *status = vals[0];
+    *detail = vals[1];
+    return cudaSuccess;
+}
+
+}  // namespace tk

@@ -478,6 +478,66 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
     return TK_OK;
 }
 
+// ------------------------------------------------------------------ Hedgehog linear attention
+
+// 3-D view {c, r, n} of a contiguous [n, r, c] bf16 tensor, moved as
+// box_c x box_r x 1 boxes with the 128-byte swizzle.
+int encode_batched_map(CUtensorMap *map, const void *ptr, int64_t c, int64_t r, int64_t n, uint32_t box_c,
+                       uint32_t box_r) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail_cuda(g_encode_err);
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c), static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c) * 2, static_cast<cuuint64_t>(c) * r * 2};
+    const cuuint32_t box[3] = {box_c, box_r, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                       elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+    return TK_OK;
+}
+
+int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O, float *DEN,
+                    int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t F, int64_t Dv, cudaStream_t stream) {
+    if (!Q || !K || !V || !Wq || !Wk || !O || !DEN) return TK_ERR_NULL_PTR;
+    if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
+    if (Dqk != 64 || F != 64 || Dv != 64) return TK_ERR_UNSUPPORTED_D;
+    if (N > INT32_MAX || B > INT32_MAX / H || B * H > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    const int64_t BH = B * H;
+    if (BH > INT64_MAX / N / 64 / 2) return TK_ERR_BAD_SHAPE;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(Wq, 16) || !aligned(Wk, 16) ||
+        !aligned(O, 16) || !aligned(DEN, 4))
+        return TK_ERR_MISALIGNED;
+    const uint64_t t_bytes = static_cast<uint64_t>(BH) * N * 64 * 2, w_bytes = static_cast<uint64_t>(H) * 64 * 64 * 2,
+                   den_bytes = static_cast<uint64_t>(BH) * N * 4;
+    const void *ins[5] = {Q, K, V, Wq, Wk};
+    const uint64_t in_bytes[5] = {t_bytes, t_bytes, t_bytes, w_bytes, w_bytes};
+    for (int a = 0; a < 5; ++a)
+        if (overlaps(O, t_bytes, ins[a], in_bytes[a]) || overlaps(DEN, den_bytes, ins[a], in_bytes[a]))
+            return TK_ERR_ALIAS;
+    if (overlaps(O, t_bytes, DEN, den_bytes)) return TK_ERR_ALIAS;
+    int num_sms = 0;
+    int rc = current_device(&num_sms);
+    if (rc != TK_OK) return rc;
+    const void *ptrs[7] = {Q, K, V, Wq, Wk, O, DEN};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    tk::HedgehogParams p;
+    if ((rc = encode_qkv_map(&p.tmQ, Q, N, 64, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmK, K, N, 64, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmV, V, N, 64, BH)) != TK_OK) return rc;
+    if ((rc = encode_batched_map(&p.tmWq, Wq, 64, 64, H, 64, 64)) != TK_OK) return rc;
+    if ((rc = encode_batched_map(&p.tmWk, Wk, 64, 64, H, 64, 64)) != TK_OK) return rc;
+    p.O = O;
+    p.DEN = DEN;
+    p.N = static_cast<int>(N);
+    p.H = static_cast<int>(H);
+    p.BH = static_cast<int>(BH);
+    cudaError_t e = tk::launch_hedgehog(p, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TK_OK;
+}
+
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     uint32_t status = 0, where = 0, status_b = 0, where_b = 0, status_g = 0, where_g = 0;
     cudaError_t e = tk::read_and_clear_status(stream, &status, &where);  // synchronises the stream
@@ -486,11 +546,14 @@ int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     if (e != cudaSuccess) return fail_cuda(e);
     e = tk::read_and_clear_gemm_status(&status_g, &where_g);
     if (e != cudaSuccess) return fail_cuda(e);
-    uint32_t status_l = 0, where_l = 0;
+    uint32_t status_l = 0, where_l = 0, status_h = 0, where_h = 0;
     e = tk::read_and_clear_based_status(&status_l, &where_l);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (detail) *detail = status ? where : (status_b ? where_b : (status_g ? where_g : where_l));
-    return (status == 0 && status_b == 0 && status_g == 0 && status_l == 0) ? TK_OK : TK_ERR_DEVICE_TIMEOUT;
+    e = tk::read_and_clear_hedgehog_status(&status_h, &where_h);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail) *detail = status ? where : (status_b ? where_b : (status_g ? where_g : (status_l ? where_l : where_h)));
+    return (status == 0 && status_b == 0 && status_g == 0 && status_l == 0 && status_h == 0) ? TK_OK
+                                                                                             : TK_ERR_DEVICE_TIMEOUT;
 }
 
 int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {
@@ -510,7 +573,8 @@ const char *tk_attn_strerror(int code) {
         case TK_ERR_NULL_PTR: return "a required pointer is NULL";
         case TK_ERR_BAD_SHAPE: return "invalid shape (B, H, N must be >= 1 and sizes must fit)";
         case TK_ERR_UNSUPPORTED_D:
-            return "unsupported head dimension (forward: 32, 64, 96, 128; backward: 64, 128; Based: 16 / 64)";
+            return "unsupported head dimension (forward: 32, 64, 96, 128; backward: 64, 128; Based: 16 / 64; "
+                   "Hedgehog: 64 / 64 / 64)";
         case TK_ERR_MISALIGNED: return "misaligned pointer (Q, K, V, O: 16 bytes; LSE: 4 bytes)";
         case TK_ERR_BAD_SCALE: return "scale must be finite and > 0";
         case TK_ERR_ALIAS: return "outputs overlap inputs or each other";

@@ -91,6 +91,23 @@ struct BasedParams {
 cudaError_t launch_based(const BasedParams &p, cudaStream_t stream);
 cudaError_t read_and_clear_based_status(uint32_t *status, uint32_t *detail);
 
+// Everything the Hedgehog linear-attention kernel needs (d = f = Dv = 64).
+struct HedgehogParams {
+    CUtensorMap tmQ;   // 3-D {64, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmK;
+    CUtensorMap tmV;
+    CUtensorMap tmWq;  // 3-D {f, d, H} bf16 (W of head h: [d][f]), box {64, 64, 1}
+    CUtensorMap tmWk;
+    void *O;           // bf16 [B*H, N, 64]
+    float *DEN;        // fp32 [B*H, N]
+    int N;
+    int H;
+    int BH;
+};
+
+cudaError_t launch_hedgehog(const HedgehogParams &p, cudaStream_t stream);
+cudaError_t read_and_clear_hedgehog_status(uint32_t *status, uint32_t *detail);
+
 // Size of the library-owned workspace behind tk_attn_bwd_noalloc.
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 
