@@ -27,6 +27,9 @@ dim 16, value dim 64), reported as GB/s of algorithmic HBM traffic against the
 measured HBM bandwidth (the linear form's arithmetic intensity is below the
 ridge).
 
+``--hedgehog``: the same for causal Hedgehog linear attention (tk_hedgehog_fwd,
+B8 H16 N4096, query/key dim 64, 64 + 64 softmax features, value dim 64).
+
 ``--gemm``: the same line for the GEMM on the same pipeline (tk_gemm,
 C = A B^T, M = N = K = 8192 unless ``--gemm-shape M,N,K``; flops 2*M*N*K), with
 the fp64 oracle GEMM on sampled rows as the CPU baseline and cuBLAS (through
@@ -663,8 +666,26 @@ def based_inputs(B, H, N):
     return q, k, v
 
 
-def run_based(args):
-    """One step = tk_based_fwd over B8 H16 N4096 (Dqk 16, Dv 64) unless
+HEDGEHOG_METRIC = ("Hedgehog linear attention GB/s of algorithmic HBM traffic on 1 GB300 "
+                   "(fraction of measured HBM bandwidth) vs CPU oracle")
+HEDGEHOG_SOURCES = ["tiled_attention_tk_gb300/csrc/hedgehog.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
+                    "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
+
+
+def hedgehog_inputs(B, H, N):
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(8100)
+    q = torch.randn((B, H, N, 64), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, N, 64), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, N, 64), generator=g).to(torch.bfloat16)
+    wq = (torch.randn((H, 64, 64), generator=g) * 0.2).to(torch.bfloat16)
+    wk = (torch.randn((H, 64, 64), generator=g) * 0.2).to(torch.bfloat16)
+    return q, k, v, wq, wk
+
+
+def run_based(args, kind: str = "based"):
+    """One step = tk_based_fwd (or tk_hedgehog_fwd) over B8 H16 N4096 unless
     --based-shape B,H,N.  Value: algorithmic bytes (Q, K, V read once, O and
     DEN written once) per second; the chunked linear form's flops are reported
     beside it."""
@@ -674,14 +695,22 @@ def run_based(args):
     _, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    q, k, v = based_inputs(B, H, N)
+    hh = kind == "hedgehog"
+    if hh:
+        q, k, v, wq, wk = hedgehog_inputs(B, H, N)
+        wqd, wkd = wq.to(dev), wk.to(dev)
+    else:
+        q, k, v = based_inputs(B, H, N)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
     den = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        tk.based(qd, kd, vd, scale=0.25, out=o, den=den, stream=stream)
+        if hh:
+            tk.hedgehog(qd, kd, vd, wqd, wkd, out=o, den=den, stream=stream)
+        else:
+            tk.based(qd, kd, vd, scale=0.25, out=o, den=den, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -700,26 +729,34 @@ def run_based(args):
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
     tokens = B * H * N
-    alg_bytes = tokens * (16 * 2 + 16 * 2 + 64 * 2 + 64 * 2 + 4)
-    # chunked linear form per token: in-chunk Q K^T and P [V|1] (causal half of
-    # 128 rows), carried phi(Q) S and state update [V|1]^T phi(K) (153 x 65)
-    flops = tokens * (2 * 16 * 64 + 2 * 65 * 64 + 2 * (2 * 153 * 65))
+    dqk = 64 if hh else 16
+    alg_bytes = tokens * (dqk * 2 + dqk * 2 + 64 * 2 + 64 * 2 + 4) + (2 * H * 64 * 64 * 2 if hh else 0)
+    # chunked linear form per token: in-chunk phi(Q) phi(K)^T (Hedgehog, after
+    # the two 64 x 64 projections) or Q K^T (Based) and P [V|1] over the
+    # causal half of 128 rows; carried phi(Q) S and the state update
+    # [V|1]^T phi(K) (features x 65)
+    nf = 128 if hh else 153
+    flops = tokens * ((2 * 2 * 64 * 64 if hh else 0) + 2 * (nf if hh else 16) * 64 + 2 * 65 * 64 +
+                      2 * (2 * nf * 65))
     gbs = alg_bytes / (ms * 1e-3) / 1e9
     peak, label = hbm_peak()
     if rank != 0:
         return None
     line = {
-        "metric": BASED_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "metric": HEDGEHOG_METRIC if hh else BASED_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded torch.Generator, N(0,1) fp32 draws rounded to bf16)",
-        "config": {"workload": f"based-B{B}H{H}N{N}", "B": B, "H": H, "N": N, "Dqk": 16, "Dv": 64,
-                   "scale": 0.25, "causal": True, "alg_bytes": alg_bytes,
+        "config": {"workload": f"{kind}-B{B}H{H}N{N}", "B": B, "H": H, "N": N, "Dqk": dqk, "Dv": 64,
+                   **({"F": 64, "W": "N(0,0.2^2) per head"} if hh else {"scale": 0.25}),
+                   "causal": True, "alg_bytes": alg_bytes,
                    "l2": "inputs > L2, no flush" if tokens * 192 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "peak_source": label,
-                     "traffic": sources_traffic_for(f"based-B{B}H{H}N{N}", BASED_SOURCES),
-                     "kernel": "based_kernel", "kernel_ms": round(ms, 5)},
+                     "traffic": sources_traffic_for(f"{kind}-B{B}H{H}N{N}",
+                                                    HEDGEHOG_SOURCES if hh else BASED_SOURCES),
+                     "kernel": f"{kind}_kernel", "kernel_ms": round(ms, 5)},
         "linear_form_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
         "tokens_per_s": round(tokens / (ms * 1e-3), 1),
         "gpu_launches": args.steps,
@@ -734,7 +771,10 @@ def run_based(args):
             b, h = divmod(heads, H)
             rows = list(range(N - 256, N))  # the longest rows of the head
             t0 = time.perf_counter()
-            oracle.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
+            if hh:
+                oracle.hedgehog(q[b, h], k[b, h], v[b, h], wq[h], wk[h], rows=rows)
+            else:
+                oracle.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
             t_total += time.perf_counter() - t0
             rows_done += len(rows)
             heads += 1
@@ -823,7 +863,8 @@ def main(argv=None):
     ap.add_argument("--gemm", action="store_true", help="time the GEMM on the same pipeline instead")
     ap.add_argument("--gemm-shape", type=str, default="8192,8192,8192", help="M,N,K for --gemm")
     ap.add_argument("--based", action="store_true", help="time the Based linear attention instead")
-    ap.add_argument("--based-shape", type=str, default="8,16,4096", help="B,H,N for --based")
+    ap.add_argument("--hedgehog", action="store_true", help="time the Hedgehog linear attention instead")
+    ap.add_argument("--based-shape", type=str, default="8,16,4096", help="B,H,N for --based / --hedgehog")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -841,8 +882,8 @@ def main(argv=None):
         todo = [Workload(0, f[0], f[1], f[2], f[3], bool(f[4]), "normal", f[5] if len(f) == 6 else None)]
     else:
         todo = [WORKLOADS[i] for i in (sorted(WORKLOADS) if args.all else [args.workload])]
-    if args.based:
-        line = run_based(args)
+    if args.based or args.hedgehog:
+        line = run_based(args, "hedgehog" if args.hedgehog else "based")
         if line is not None and rank == 0:
             print(json.dumps(line), flush=True)
         return

@@ -216,3 +216,22 @@ def _based(q=Bq, k=Bk, v=Bv, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=16, Dv=64, scale=0
 ])
 def test_based_host_validation(kwargs, code):
     assert _based(**kwargs) == tk.STATUS[code]
+
+
+# ---------------------------------------------------------------- Hedgehog ABI
+
+def _hh(q=Bq, k=Bk, v=Bv, wq=Bdo, wk=BdQ, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=64, F=64, Dv=64):
+    return tk.load().tk_hedgehog_fwd(q, k, v, wq, wk, o, d, B, H, N, Dqk, F, Dv, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(wk=None), "TK_ERR_NULL_PTR"),
+    (dict(N=0), "TK_ERR_BAD_SHAPE"),
+    (dict(Dqk=128), "TK_ERR_UNSUPPORTED_D"),
+    (dict(F=32), "TK_ERR_UNSUPPORTED_D"),
+    (dict(wq=Bdo + 8), "TK_ERR_MISALIGNED"),
+    (dict(o=Bq + 4096), "TK_ERR_ALIAS"),
+    (dict(d=Bdo + 64), "TK_ERR_ALIAS"),     # inside Wq
+])
+def test_hedgehog_host_validation(kwargs, code):
+    assert _hh(**kwargs) == tk.STATUS[code]
