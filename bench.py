@@ -133,8 +133,53 @@ def traffic_for(workload_name: str):
     return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver): SM clock, its maximum and the clock-event reason bits."""
+
+    CLOCK_SM = 1
+    # clock-event reason bits, as nvml.h numbers them
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    GPU_IDLE = 0x1
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML device for " + uuid)
+        try:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        m = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.dev, self.CLOCK_SM, ctypes.byref(m))
+        self.max_mhz = float(m.value)
+
+    def sample(self):
+        clk, bits = self.c.c_uint(), self.c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, self.CLOCK_SM, self.c.byref(clk)) != 0:
+            return None
+        if self.reasons_fn(self.dev, self.c.byref(bits)) != 0:
+            return None
+        return float(clk.value), int(bits.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while it runs."""
+    """SM clock and clock-event reasons while the timed region runs.
+
+    A host thread queries NVML every ~2 ms between start (the constructor) and
+    stop(), so even a timed region of a few milliseconds gets samples; the
+    samples also go to gpurun_out/clocks_gpu<i>.csv.  Where NVML cannot be
+    loaded it falls back to `nvidia-smi --loop-ms`, whose start-up takes
+    longer than short timed regions."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -142,6 +187,7 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int, interval_ms: int = 100):
         self.proc = None
+        self.nvml = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
         gpu_id = str(gpu_index)
         try:  # the UUID names the right GPU whatever CUDA_VISIBLE_DEVICES says
@@ -152,6 +198,28 @@ class ClockSampler:
             pass
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        except OSError:
+            pass
+        try:
+            self.nvml = _Nvml(gpu_id)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.samples = []
+            self.stop_flag = threading.Event()
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    r = self.nvml.sample()
+                    if r is not None:
+                        self.samples.append((time.perf_counter(), r[0], r[1]))
+                    self.stop_flag.wait(0.002)
+            self.first = self.nvml.sample()
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return
+        try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.QUERY}",
@@ -160,7 +228,33 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def _stop_nvml(self):
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        last = self.nvml.sample()
+        self.nvml.close()
+        pts = list(self.samples)
+        try:
+            with open(self.path, "w") as f:
+                f.write("t_s,sm_mhz,max_sm_mhz,reason_bits\n")
+                for t, mhz, bits in pts:
+                    f.write(f"{t:.6f},{mhz:.0f},{self.nvml.max_mhz:.0f},{bits:#x}\n")
+        except OSError:
+            pass
+        if not pts:
+            pts = [(0.0, r[0], r[1]) for r in (self.first, last) if r is not None]
+        if not pts:
+            return {"sm_mhz": None, "sm_max_mhz": self.nvml.max_mhz, "reasons": ["no samples"], "samples": 0,
+                    "source": "nvml"}
+        busy = [p for p in pts if not p[2] & _Nvml.GPU_IDLE] or pts
+        mhz = sorted(p[1] for p in busy)
+        reasons = sorted({name for p in pts for bit, name in _Nvml.REASONS.items() if p[2] & bit})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": self.nvml.max_mhz, "reasons": reasons,
+                "samples": len(pts), "samples_busy": len(busy) if busy is not pts else 0, "source": "nvml"}
+
     def stop(self):
+        if self.nvml is not None:
+            return self._stop_nvml()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -185,10 +279,23 @@ class ClockSampler:
                     if val.lower() == "active":
                         reasons.add(n)
         if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": "nvidia-smi"}
         sms.sort()
         return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
-                "samples": len(sms)}
+                "samples": len(sms), "source": "nvidia-smi"}
+
+
+def l2_flusher(in_bytes: int, dev):
+    """(buffer, description): where the timed launch's inputs fit in L2, a
+    buffer of twice L2 that is written before every timed launch, outside its
+    event pair, so that no launch starts on operands left in L2 by the last."""
+    import torch
+    if in_bytes > L2_BYTES:
+        return None, f"inputs {in_bytes / 2**20:.0f} MiB > {L2_BYTES >> 20} MiB L2, no flush"
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    return buf, (f"inputs {in_bytes / 2**20:.0f} MiB fit in L2: a {2 * L2_BYTES >> 20} MiB write flushes L2 "
+                 "before every timed launch (outside its events)")
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -267,12 +374,15 @@ def run_ours(args, w):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush, l2_desc = l2_flusher(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2, dev)
     sampler = ClockSampler(local)
     if dist_mod:
         dist_mod.barrier()
     torch.cuda.synchronize(dev)
     start_ev.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -286,7 +396,8 @@ def run_ours(args, w):
     st, detail = tk.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
-    total_ms = max_over_ranks(total_ms, dist_mod, dev)
+    # with flushes in the region, a step is its own event pair
+    total_ms = max_over_ranks(total_ms if flush is None else kernel_ms * args.steps, dist_mod, dev)
     ms_per_step = total_ms / args.steps
     value = w.flops * ws / (ms_per_step * 1e-3) / 1e12
 
@@ -328,10 +439,7 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
-        "config": dict(w.describe(), l2="inputs 384 MiB + output 128 MiB > 126 MiB L2, no flush"
-                       if w.index == DEFAULT_WORKLOAD else
-                       ("inputs > L2, no flush" if w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2 > L2_BYTES
-                        else "inputs fit in L2: warm-L2 number")),
+        "config": dict(w.describe(), l2=l2_desc),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_label, "traffic": traffic_for(w.name),
@@ -404,9 +512,12 @@ def run_bwd(args, w):
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    flush, l2_desc = l2_flusher(w.B * w.H * (3 * w.N + 2 * w.Nkv) * w.D * 2, dev)
     sampler = ClockSampler(local)
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -424,7 +535,7 @@ def run_bwd(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
-        "config": dict(w.describe(), flops="10*B*H*N^2*D (halved causal): S, dP, dV, dK, dQ"),
+        "config": dict(w.describe(), flops="10*B*H*N^2*D (halved causal): S, dP, dV, dK, dQ", l2=l2_desc),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_label, "traffic": None,
                      "kernel": f"attn_bwd_kernel<{w.D}> + prep + dQ rounding (whole step)"},
@@ -510,12 +621,15 @@ def run_gemm(args):
         raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush, l2_desc = l2_flusher((M + N) * K * 2, dev)
     sampler = ClockSampler(local)
     if dist_mod:
         dist_mod.barrier()
     torch.cuda.synchronize(dev)
     start_ev.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -525,7 +639,8 @@ def run_gemm(args):
         dist_mod.barrier()
     clocks = sampler.stop()
     kernel_ms = sum(x.elapsed_time(y) for x, y in ev) / args.steps
-    total_ms = max_over_ranks(start_ev.elapsed_time(end_ev), dist_mod, dev)
+    total_ms = max_over_ranks(start_ev.elapsed_time(end_ev) if flush is None else kernel_ms * args.steps,
+                              dist_mod, dev)
     st, detail = tk.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
@@ -580,7 +695,7 @@ def run_gemm(args):
         "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": "[N,K] (C = A B^T)",
                    "stream_k": "on where the schedule uses it",
                    "workspace_bytes": need,
-                   "l2": "inputs > L2, no flush" if (M + N) * K * 2 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
+                   "l2": l2_desc},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_label,
                      "traffic": gemm_traffic_for(name), "kernel": "gemm_kernel<true>",
@@ -716,9 +831,13 @@ def run_based(args, kind: str = "based"):
         step()
     torch.cuda.synchronize(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    dqk = 64 if hh else 16
+    flush, l2_desc = l2_flusher(B * H * N * (2 * dqk + 64) * 2, dev)
     sampler = ClockSampler(local)
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -729,7 +848,6 @@ def run_based(args, kind: str = "based"):
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
     tokens = B * H * N
-    dqk = 64 if hh else 16
     alg_bytes = tokens * (dqk * 2 + dqk * 2 + 64 * 2 + 64 * 2 + 4) + (2 * H * 64 * 64 * 2 if hh else 0)
     # chunked linear form per token: in-chunk phi(Q) phi(K)^T (Hedgehog, after
     # the two 64 x 64 projections) or Q K^T (Based) and P [V|1] over the
@@ -751,7 +869,7 @@ def run_based(args, kind: str = "based"):
         "config": {"workload": f"{kind}-B{B}H{H}N{N}", "B": B, "H": H, "N": N, "Dqk": dqk, "Dv": 64,
                    **({"F": 64, "W": "N(0,0.2^2) per head"} if hh else {"scale": 0.25}),
                    "causal": True, "alg_bytes": alg_bytes,
-                   "l2": "inputs > L2, no flush" if tokens * 192 > L2_BYTES else "inputs fit in L2: warm-L2 number"},
+                   "l2": l2_desc},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 4), "peak_source": label,
                      "traffic": sources_traffic_for(f"{kind}-B{B}H{H}N{N}",

@@ -665,5 +665,6 @@ int tkor_hedgehog_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, 
         DEN[r] = den;
     }
     free(phik); free(phiq);
+    g_last_threads = 1;
     return 0;
 }
