@@ -21,8 +21,11 @@
 //   state:  S^T += [V | 1]^T phi(K)                                 (tensor core)
 //   O_i = num_i / den_i.
 //
-// 192 threads: four compute warps (row i of the chunk = TMEM lane i), a TMA
-// warp and an MMA warp.  Q and K arrive as 128 x 64 boxes of which the first
+// 320 threads: two compute warpgroups over the same 128 rows (row i of the
+// chunk = TMEM lane i; they split the columns of every step), a TMA warp and
+// an MMA warp.  The tensor core forms chunk c+1's Q K^T right after chunk
+// c's P [V|1], so the compute warps form P of c+1 while the rest of chunk c's
+// products run.  Q and K arrive as 128 x 64 boxes of which the first
 // 16 columns are the tensor (the rest zero-filled by TMA), so the same
 // 128-byte-swizzled layouts and descriptors as the attention kernels serve
 // every operand.  The "1" column is a constant shared-memory box.
@@ -45,9 +48,9 @@ constexpr int DQK = 16;
 constexpr int DV = 64;
 constexpr int F = 192;             // feature columns (153 live)
 constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
-constexpr int NUM_THREADS = 192;
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ROLE_BASED_PRODUCER = 12;
 constexpr uint32_t ROLE_BASED_MMA = 13;
@@ -63,12 +66,13 @@ constexpr uint32_t BAR_OFF = SPREV_OFF + 3 * SBOX;
 constexpr int B_FULL = 0;          // + buffer (2)
 constexpr int B_EMPTY = 2;         // + buffer (2)
 constexpr int B_SFULL = 4;         // Q K^T in TMEM
-constexpr int B_PREADY = 5;        // P, phi(Q) in TMEM, phi(K) in smem (4 warps)
-constexpr int B_ODONE = 6;         // intra + inter products done
-constexpr int B_STDONE = 7;        // state product done
-constexpr int B_SREADY = 8;        // bf16 copy of the state in smem (4 warps)
-constexpr int B_MMADONE = 9;
-constexpr int NUM_BARS = 10;
+constexpr int B_PREADY = 5;        // P, phi(Q) in TMEM, the bf16 state in smem, the last O read out (8 warps)
+constexpr int B_SREAD = 6;         // both groups hold their half of S in registers (8 warps)
+constexpr int B_ODONE = 7;         // [num | den] of the chunk complete
+constexpr int B_PHIKREADY = 8;     // phi(K) in smem (8 warps)
+constexpr int B_STDONE = 9;        // state product done
+constexpr int B_MMADONE = 10;
+constexpr int NUM_BARS = 11;
 constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
@@ -124,6 +128,58 @@ __device__ __forceinline__ void load_row16(uint32_t box, int r, float (&x)[DQK])
     }
 }
 
+// phi of one row (16 features from a swizzled box) into the 64-feature parts
+// of PARTS (bit k = features 64k .. 64k+63): into TMEM as the A operand of
+// the inter product, or into row r of the phi(K) boxes.  `live` false zeroes
+// the row (a key past N, the constant feature included).
+template <int PARTS, bool TO_TMEM>
+__device__ __forceinline__ void phi_store(uint32_t box16, int r, bool live, float rs, float hs, float gs,
+                                          uint32_t dst) {
+    float x[DQK];
+    load_row16(box16, r, x);
+    if (!live) {
+#pragma unroll
+        for (int a = 0; a < DQK; ++a) x[a] = 0.0f;
+    }
+    uint32_t pk[F / 2];
+    phi_packed(x, rs, hs, gs, pk);
+    if (!live) pk[0] = 0u;
+#pragma unroll
+    for (int part = 0; part < 3; ++part) {
+        if (!(PARTS & (1 << part))) continue;
+        if constexpr (TO_TMEM) {
+            tmem_st32(dst + part * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * part));
+        } else {
+            const uint32_t box = dst + part * BOX;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(sw128(box, r, q), pk[32 * part + 4 * q], pk[32 * part + 4 * q + 1],
+                             pk[32 * part + 4 * q + 2], pk[32 * part + 4 * q + 3]);
+        }
+    }
+}
+
+// O_i = num_i / den_i for 32 columns from `col` of the [num | den] accumulator;
+// DEN written when `den_out` is set.
+__device__ __forceinline__ void write_o(uint32_t lane_taddr, int col, bool live, __nv_bfloat16 *o_row,
+                                        float *den_out) {
+    uint32_t o[32], d[16];
+    tmem_ld32(lane_taddr + T_O + col, o);
+    tmem_ld16(lane_taddr + T_O + 64, d);
+    const float den = __uint_as_float(d[0]);
+    if (live) {
+        const float inv = 1.0f / den;
+        uint4 *dst = reinterpret_cast<uint4 *>(o_row + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+        if (den_out) *den_out = den;
+    }
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -148,10 +204,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             mbar_init(bar(B_EMPTY + b), 1);
         }
         mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_PREADY), 4);
+        mbar_init(bar(B_PREADY), 8);
+        mbar_init(bar(B_SREAD), 8);
         mbar_init(bar(B_ODONE), 1);
+        mbar_init(bar(B_PHIKREADY), 8);
         mbar_init(bar(B_STDONE), 1);
-        mbar_init(bar(B_SREADY), 4);
         mbar_init(bar(B_MMADONE), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -205,22 +262,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
             constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
             constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
-            bool ok = true;
+            // Per chunk c: P [V|1], then Q K^T of chunk c+1 (its P is formed while
+            // this chunk's other products run), phi(Q) S_{<c}, and the state
+            // update once phi(K) is in smem.
+            auto issue_s = [&](int c) {
+                const uint32_t qb = sbase + QKV_OFF + (c & 1) * 3 * BOX;
+                umma_ss(tmem + T_S, smem_desc_sw128(qb, 16, 1024), smem_desc_sw128(qb + BOX, 16, 1024), ID_S, 0);
+                umma_commit(bar(B_SFULL));
+            };
+            bool ok = wait_bounded(bar(B_FULL), 0, abort_flag, (ROLE_BASED_MMA << 24) | (B_FULL << 16));
+            if (ok) {
+                tc_fence_after_sync();
+                issue_s(0);
+            }
             for (int c = 0; ok && c < n_chunks; ++c) {
                 const int b = c & 1;
                 const uint32_t ph = c & 1;
-                const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX, vb = qb + 2 * BOX;
-                if (!(ok = wait_bounded(bar(B_FULL + b), (c >> 1) & 1, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | ((B_FULL + b) << 16) | c)))
-                    break;
-                tc_fence_after_sync();
-                umma_ss(tmem + T_S, smem_desc_sw128(qb, 16, 1024), smem_desc_sw128(kb, 16, 1024), ID_S, 0);
-                umma_commit(bar(B_SFULL));
+                const uint32_t vb = sbase + QKV_OFF + b * 3 * BOX + 2 * BOX;
                 if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | c)))
-                    break;
-                // the bf16 state of the previous chunks is in smem
-                if (c > 0 && !(ok = wait_bounded(bar(B_SREADY), ph ^ 1, abort_flag,
-                                                 (ROLE_BASED_MMA << 24) | (B_SREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]; 16 chunk rows per step
@@ -228,6 +287,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 for (int k = 0; k < C / 16; ++k)
                     umma_ts(tmem + T_O, tmem + T_S + k * 8,
                             smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
+                // S of the next chunk over P of this one (the tensor core runs them in order)
+                if (c + 1 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(B_FULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | ((B_FULL + (b ^ 1)) << 16) | (c + 1))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_s(c + 1);
+                }
                 // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
                 if (c > 0) {
 #pragma unroll
@@ -238,6 +305,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 }
                 umma_commit(bar(B_ODONE));
                 // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
+                if (!(ok = wait_bounded(bar(B_PHIKREADY), ph, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | c)))
+                    break;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
                     umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
@@ -253,11 +324,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         __syncwarp();
     } else {
         // ------------------------------------------------ compute warps
-        const int i = threadIdx.x;  // row of the chunk = TMEM lane; also row i of S^T
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Two warpgroups over the same 128 rows (warp w reads TMEM lanes
+        // 32 (w % 4) ..); each takes half of every step.  Per chunk c, once
+        // S(c) is in TMEM (while chunk c-1's phi(Q) S and state products may
+        // still run): P(c); O of chunk c-1; the bf16 state copy of chunk c-1;
+        // phi(Q) of chunk c (group 0: features 0..127, group 1: 128..191);
+        // PREADY; then phi(K) of chunk c (the other split) for the state
+        // product, which the tensor core takes last.
+        const int i = threadIdx.x % 128;  // row of the chunk = TMEM lane; also row i of S^T
+        const int grp = warp / 4;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const float scale = p.scale;
         const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
         const size_t head_row0 = static_cast<size_t>(bh) * p.N;
+        __nv_bfloat16 *const Obase = static_cast<__nv_bfloat16 *>(p.O);
         bool ok = true;
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
@@ -267,107 +347,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | c)))
                 break;
             tc_fence_after_sync();
-            // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N)
+            // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this
+            // group's 64 keys.  P columns 32..63 lie over S columns group 0
+            // reads, so both groups load their S first.
             {
                 const int jmax = min(i, p.N - 1 - c * C);  // last key of the chunk this row sees
+                uint32_t sr[64];
+                tmem_ld64(lane_base + T_S + grp * 64, sr);
+                tc_fence_before_sync();
+                warp_arrive(bar(B_SREAD), lane);
+                uint32_t pk[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sr[64];
-                    tmem_ld64(lane_base + T_S + half * 64, sr);
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j0 = half * 64 + 2 * e;
-                        const float s0 = scale * __uint_as_float(sr[2 * e]);
-                        const float s1 = scale * __uint_as_float(sr[2 * e + 1]);
-                        const float w0 = j0 <= jmax ? fmaf(0.5f * s0, s0, s0 + 1.0f) : 0.0f;
-                        const float w1 = j0 + 1 <= jmax ? fmaf(0.5f * s1, s1, s1 + 1.0f) : 0.0f;
-                        pk[e] = pack_bf16x2(w0, w1);
-                    }
-                    tmem_st32(lane_base + T_S + half * 32, pk);  // P over the first 64 columns
+                for (int e = 0; e < 32; ++e) {
+                    const int j0 = grp * 64 + 2 * e;
+                    const float s0 = scale * __uint_as_float(sr[2 * e]);
+                    const float s1 = scale * __uint_as_float(sr[2 * e + 1]);
+                    const float w0 = j0 <= jmax ? fmaf(0.5f * s0, s0, s0 + 1.0f) : 0.0f;
+                    const float w1 = j0 + 1 <= jmax ? fmaf(0.5f * s1, s1, s1 + 1.0f) : 0.0f;
+                    pk[e] = pack_bf16x2(w0, w1);
                 }
+                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SREAD << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                tmem_st32(lane_base + T_S + grp * 32, pk);  // P over the first 64 columns
             }
-            // --- phi(q_i) into TMEM (the A operand of the inter product)
-            {
-                float x[DQK];
-                load_row16(qb, i, x);
-                uint32_t pk[F / 2];
-                phi_packed(x, r, h, g, pk);
+            if (c > 0) {
+                // --- O of chunk c-1, this group's 32 columns
+                if (!(ok = wait_bounded(bar(B_ODONE), ph ^ 1, abort_flag,
+                                        (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+                write_o(lane_base, grp * 32, row - C < p.N, Obase + (head_row0 + row - C) * DV,
+                        grp == 0 ? p.DEN + head_row0 + row - C : nullptr);
+                // --- bf16 copy of the state S_{<c} (rows 0..79 of S^T): 96 of the 192 features
+                if (!(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
+                                        (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
+                    break;
+                tc_fence_after_sync();
 #pragma unroll
-                for (int part = 0; part < 3; ++part)
-                    tmem_st32(lane_base + T_PHIQ + part * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * part));
-            }
-            // --- phi(k_i) into row i of the phi(K) boxes (0 for keys past N)
-            {
-                float x[DQK];
-                load_row16(kb, i, x);
-                if (row >= p.N) {
-#pragma unroll
-                    for (int a = 0; a < DQK; ++a) x[a] = 0.0f;
-                }
-                uint32_t pk[F / 2];
-                phi_packed(x, r, h, g, pk);
-                if (row >= p.N) pk[0] = 0u;  // the constant feature too: this key does not exist
-#pragma unroll
-                for (int part = 0; part < 3; ++part) {
-                    const uint32_t box = sbase + PHIK_OFF + part * BOX;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_shared_v4(sw128(box, i, q), pk[32 * part + 4 * q], pk[32 * part + 4 * q + 1],
-                                     pk[32 * part + 4 * q + 2], pk[32 * part + 4 * q + 3]);
-                }
-            }
-            tmem_st_wait();
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            warp_arrive(bar(B_PREADY), lane);
-
-            // --- O_i = num_i / den_i
-            if (!(ok = wait_bounded(bar(B_ODONE), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | c)))
-                break;
-            tc_fence_after_sync();
-            {
-                uint32_t o[64], d[16];
-                tmem_ld64(lane_base + T_O, o);
-                tmem_ld16(lane_base + T_O + 64, d);
-                const float den = __uint_as_float(d[0]);
-                if (row < p.N) {
-                    const float inv = 1.0f / den;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-                    p.DEN[head_row0 + row] = den;
-                }
-            }
-            // --- bf16 copy of the state S_{<=c} (rows 0..79 of S^T) for the next chunk
-            if (!(ok = wait_bounded(bar(B_STDONE), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
-                break;
-            tc_fence_after_sync();
-            if (c + 1 < n_chunks) {
-#pragma unroll
-                for (int part = 0; part < 3; ++part) {
-                    uint32_t sv[64];
-                    tmem_ld64(lane_base + T_ST + part * 64, sv);  // every lane loads; rows >= 80 are not stored
+                for (int blk = 0; blk < 3; ++blk) {
+                    const int col = grp * 96 + blk * 32;
+                    uint32_t sv[32];
+                    tmem_ld32(lane_base + T_ST + col, sv);  // every lane loads; rows >= 80 are not stored
                     if (i < NV) {
-                        const uint32_t box = sbase + SPREV_OFF + part * SBOX;
+                        const uint32_t box = sbase + SPREV_OFF + (col / 64) * SBOX;
+                        const int q0 = (col % 64) / 8;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_shared_v4(sw128(box, i, q),
+                        for (int q = 0; q < 4; ++q)
+                            st_shared_v4(sw128(box, i, q0 + q),
                                          pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
                     }
                 }
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                warp_arrive(bar(B_SREADY), lane);
             }
+            // --- phi(Q) of chunk c into TMEM (its last reader, chunk c-1's phi(Q) S, is done)
+            if (grp == 0)
+                phi_store<3, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
+            else
+                phi_store<4, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PREADY), lane);
+            // --- phi(K) of chunk c into smem (0 for keys past N); its last reader,
+            // chunk c-1's state product, is done
+            if (grp == 0)
+                phi_store<4, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
+            else
+                phi_store<3, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PHIKREADY), lane);
+        }
+        // --- O of the last chunk
+        if (ok && n_chunks > 0 &&
+            wait_bounded(bar(B_ODONE), (n_chunks - 1) & 1, abort_flag,
+                         (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | n_chunks)) {
+            tc_fence_after_sync();
+            const int row = (n_chunks - 1) * C + i;
+            write_o(lane_base, grp * 32, row < p.N, Obase + (head_row0 + row) * DV,
+                    grp == 0 ? p.DEN + head_row0 + row : nullptr);
         }
     }
 

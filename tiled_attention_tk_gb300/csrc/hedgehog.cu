@@ -35,9 +35,9 @@ constexpr int FH = 64;             // features per half
 constexpr int F = 2 * FH;          // feature dims of phi
 constexpr int DV = 64;
 constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
-constexpr int NUM_THREADS = 192;
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
+constexpr int NUM_THREADS = 320;   // two compute warpgroups, a TMA warp, an MMA warp
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ROLE_HH_PRODUCER = 15;
 constexpr uint32_t ROLE_HH_MMA = 16;
@@ -58,23 +58,24 @@ constexpr int B_FULL = 0;          // + buffer (2)
 constexpr int B_EMPTY = 2;         // + buffer (2)
 constexpr int B_WFULL = 4;         // Wq, Wk loaded
 constexpr int B_ZFULL = 5;         // Q Wq, K Wk in TMEM
-constexpr int B_PHIREADY = 6;      // phi(Q), phi(K) in smem (4 warps)
+constexpr int B_PHIREADY = 6;      // phi(Q), phi(K) and the bf16 state of the chunks before in smem (8 warps)
 constexpr int B_SFULL = 7;         // phi(Q) phi(K)^T in TMEM
-constexpr int B_PREADY = 8;        // P in TMEM (4 warps)
-constexpr int B_ODONE = 9;         // intra + inter products done
-constexpr int B_STDONE = 10;       // state product done
-constexpr int B_SREADY = 11;       // bf16 state in smem (4 warps)
-constexpr int B_MMADONE = 12;
-constexpr int NUM_BARS = 13;
+constexpr int B_PREADY = 8;        // P in TMEM, the last O read out (8 warps)
+constexpr int B_ODONE = 9;         // [num | den] of the chunk complete
+constexpr int B_STDONE = 10;       // all products of the chunk done
+constexpr int B_MMADONE = 11;
+constexpr int NUM_BARS = 12;
 constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
 static_assert(WQ_OFF % 1024 == 0 && ONES_OFF % 1024 == 0 && SPREV_OFF % 1024 == 0 && SBOX % 1024 == 0,
               "swizzled boxes need 1024-byte alignment");
 
-constexpr uint32_t T_Z = 0;        // Q Wq (cols 0..63), K Wk (64..127); then S; P (bf16) over 0..63
+constexpr uint32_t T_Z = 0;        // Q Wq (cols 0..63), K Wk (64..127); then S
 constexpr uint32_t T_O = 128;      // [num | den] fp32: 80 cols
 constexpr uint32_t T_ST = 256;     // S^T fp32: 128 cols (lane = value column, 64 = the "1" row)
+constexpr uint32_t T_P = 384;      // P (bf16, 64 cols): apart from S, so the two groups need no
+                                   // order between one's reads of S and the other's writes of P
 
 __device__ __forceinline__ uint32_t sw128(uint32_t box, int r, int c) { return box + r * 128 + ((c ^ (r & 7)) << 4); }
 
@@ -82,11 +83,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// phi(z) = [softmax(z), softmax(-z)] of one row's 64 projections, as 64
-// packed bf16 pairs (zeros when `live` is false), written to row r of a
-// two-box 128-feature K-major tile.
-__device__ __forceinline__ void write_phi(const uint32_t (&zr)[64], bool live, uint32_t tile, int r) {
+// phi(z) = [softmax(z), softmax(-z)] of one row's 64 projections (TMEM
+// columns from `zcol`), as 64 packed bf16 pairs (zeros when `live` is false).
+// The projections are read again for the second half, so that only one
+// half's 64 exponentials are live at a time.
+__device__ __forceinline__ void phi_regs(uint32_t zcol, bool live, uint32_t (&pk)[64]) {
     constexpr float kLog2e = 1.4426950408889634f;
+    uint32_t zr[64];
+    tmem_ld64(zcol, zr);
     float zmax = __uint_as_float(zr[0]), zmin = zmax;
 #pragma unroll
     for (int c = 1; c < FH; ++c) {
@@ -94,29 +98,44 @@ __device__ __forceinline__ void write_phi(const uint32_t (&zr)[64], bool live, u
         zmax = fmaxf(zmax, z);
         zmin = fminf(zmin, z);
     }
-    float ep[FH], en[FH];
-    float sp = 0.0f, sn = 0.0f;
-#pragma unroll
-    for (int c = 0; c < FH; ++c) {
-        const float z = __uint_as_float(zr[c]);
-        ep[c] = ex2((z - zmax) * kLog2e);
-        en[c] = ex2((zmin - z) * kLog2e);
-        sp += ep[c];
-        sn += en[c];
-    }
-    const float ip = live ? 1.0f / sp : 0.0f, in = live ? 1.0f / sn : 0.0f;
+    // exp(z - zmax) = 2^(z log2e - zmax log2e), exp(zmin - z) likewise
+    const float offp = -zmax * kLog2e, offn = zmin * kLog2e;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        const float *e = half == 0 ? ep : en;
-        const float sc = half == 0 ? ip : in;
-        const uint32_t box = tile + half * BOX;
+        float e[FH];
+        float sum = 0.0f;
+        if (half == 0) {
+#pragma unroll
+            for (int c = 0; c < FH; ++c) {
+                e[c] = ex2(fmaf(__uint_as_float(zr[c]), kLog2e, offp));
+                sum += e[c];
+            }
+        } else {
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {  // reloaded in two 32-column parts
+                uint32_t zp[32];
+                tmem_ld32(zcol + part * 32, zp);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    e[part * 32 + c] = ex2(fmaf(-__uint_as_float(zp[c]), kLog2e, offn));
+                    sum += e[part * 32 + c];
+                }
+            }
+        }
+        const float sc = live ? 1.0f / sum : 0.0f;
+#pragma unroll
+        for (int q = 0; q < FH / 2; ++q) pk[half * 32 + q] = pack_bf16x2(e[2 * q] * sc, e[2 * q + 1] * sc);
+    }
+}
+
+// Row r of a two-box 128-feature K-major tile from 64 packed bf16 pairs.
+__device__ __forceinline__ void phi_store(const uint32_t (&pk)[64], uint32_t tile, int r) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            st_shared_v4(sw128(box, r, q), pack_bf16x2(e[8 * q] * sc, e[8 * q + 1] * sc),
-                         pack_bf16x2(e[8 * q + 2] * sc, e[8 * q + 3] * sc),
-                         pack_bf16x2(e[8 * q + 4] * sc, e[8 * q + 5] * sc),
-                         pack_bf16x2(e[8 * q + 6] * sc, e[8 * q + 7] * sc));
-    }
+            st_shared_v4(sw128(tile + half * BOX, r, q), pk[half * 32 + 4 * q], pk[half * 32 + 4 * q + 1],
+                         pk[half * 32 + 4 * q + 2], pk[half * 32 + 4 * q + 3]);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_constant__ HedgehogParams p) {
@@ -145,12 +164,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         }
         mbar_init(bar(B_WFULL), 1);
         mbar_init(bar(B_ZFULL), 1);
-        mbar_init(bar(B_PHIREADY), 4);
+        mbar_init(bar(B_PHIREADY), 8);
         mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_PREADY), 4);
+        mbar_init(bar(B_PREADY), 8);
         mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_STDONE), 1);
-        mbar_init(bar(B_SREADY), 4);
         mbar_init(bar(B_MMADONE), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -209,16 +227,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);   // P [V | 1]: A in TMEM
             constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);   // phi(Q) S: both K-major
             constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);    // [V | 1]^T phi(K): both MN-major
-            bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16));
-            for (int c = 0; ok && c < n_chunks; ++c) {
-                const int b = c & 1;
-                const uint32_t ph = c & 1;
-                const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX, vb = qb + 2 * BOX;
-                if (!(ok = wait_bounded(bar(B_FULL + b), (c >> 1) & 1, abort_flag,
-                                        (ROLE_HH_MMA << 24) | ((B_FULL + b) << 16) | c)))
-                    break;
-                tc_fence_after_sync();
-                // Z = Q Wq, K Wk: 16 of the 64 dims per step
+            // Per chunk c: P [V|1], then Q Wq and K Wk of chunk c+1 (so that
+            // its feature maps are formed while this chunk's products run),
+            // phi(Q) S_{<c}, the state update, and phi(Q) phi(K)^T of c+1.
+            auto issue_z = [&](int c) {  // Z of chunk c: Q Wq, K Wk, 16 of the 64 dims per step
+                const uint32_t qb = sbase + QKV_OFF + (c & 1) * 3 * BOX, kb = qb + BOX;
 #pragma unroll
                 for (int k = 0; k < DQK / 16; ++k) {
                     umma_ss(tmem + T_Z, smem_desc_sw128(qb + k * 32, 16, 1024),
@@ -227,10 +240,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                             smem_desc_sw128(sbase + WK_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
                 }
                 umma_commit(bar(B_ZFULL));
-                if (!(ok = wait_bounded(bar(B_PHIREADY), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_PHIREADY << 16) | c)))
-                    break;
-                tc_fence_after_sync();
-                // S = phi(Q) phi(K)^T over the 128 features (2 boxes)
+            };
+            auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features (2 boxes)
 #pragma unroll
                 for (int k = 0; k < F / 16; ++k) {
                     const uint32_t off = (k / 4) * BOX + (k % 4) * 32;
@@ -238,17 +249,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                             smem_desc_sw128(sbase + PHIK_OFF + off, 16, 1024), ID_S, k > 0);
                 }
                 umma_commit(bar(B_SFULL));
+            };
+            bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16)) &&
+                      wait_bounded(bar(B_FULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_FULL << 16));
+            if (ok) {
+                tc_fence_after_sync();
+                issue_z(0);
+                if ((ok = wait_bounded(bar(B_PHIREADY), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_PHIREADY << 16)))) {
+                    tc_fence_after_sync();
+                    issue_s();
+                }
+            }
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int b = c & 1;
+                const uint32_t ph = c & 1;
+                const uint32_t vb = sbase + QKV_OFF + b * 3 * BOX + 2 * BOX;
                 if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_PREADY << 16) | c)))
-                    break;
-                if (c > 0 && !(ok = wait_bounded(bar(B_SREADY), ph ^ 1, abort_flag,
-                                                 (ROLE_HH_MMA << 24) | (B_SREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ts(tmem + T_O, tmem + T_Z + k * 8,
+                    umma_ts(tmem + T_O, tmem + T_P + k * 8,
                             smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
+                // Z of the next chunk (its S was read out before this chunk's PREADY)
+                if (c + 1 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(B_FULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
+                                            (ROLE_HH_MMA << 24) | ((B_FULL + (b ^ 1)) << 16) | (c + 1))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_z(c + 1);
+                }
                 // inter: [num | den] += phi(Q) S_{<c}
                 if (c > 0) {
 #pragma unroll
@@ -266,6 +297,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                             (c > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_EMPTY + b));
+                // S of the next chunk, once its features and this chunk's state are in smem
+                if (c + 1 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(B_PHIREADY), ph ^ 1, abort_flag,
+                                            (ROLE_HH_MMA << 24) | (B_PHIREADY << 16) | (c + 1))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_s();
+                }
             }
             umma_commit(bar(B_MMADONE));
             const uint64_t t0 = global_timer_ns();
@@ -275,90 +314,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         __syncwarp();
     } else {
         // ------------------------------------------------ compute warps
-        const int i = threadIdx.x;  // row of the chunk = TMEM lane; also row i of S^T
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Two warpgroups over the same 128 rows (warp w reads TMEM lanes
+        // 32 (w % 4) ..): group 0 forms phi(Q), the first half of P and of
+        // the state copy, O columns 0..31 and DEN; group 1 forms phi(K) and
+        // the second halves.  Per chunk c: P; chunk c+1's feature maps into
+        // registers while chunk c's products run; once they are done, the
+        // state copy and the feature maps into smem (they feed c+1's
+        // products); then O of chunk c.
+        const int i = threadIdx.x % 128;  // row of the chunk = TMEM lane; also row i of S^T
+        const int grp = warp / 4;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const size_t head_row0 = static_cast<size_t>(bh) * p.N;
-        for (int c = 0; c < n_chunks; ++c) {
-            const uint32_t ph = c & 1;
-            const int row = c * C + i;
-            // --- feature maps phi(q_i), phi(k_i) (0 for keys past N)
-            if (!wait_bounded(bar(B_ZFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16) | c)) break;
+        const uint32_t phi_tile = sbase + (grp == 0 ? PHIQ_OFF : PHIK_OFF);
+        const uint32_t zcol = lane_base + T_Z + grp * FH;
+        bool ok = wait_bounded(bar(B_ZFULL), 0, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16));
+        if (ok) {
             tc_fence_after_sync();
-            {
-                uint32_t zr[64];
-                tmem_ld64(lane_base + T_Z, zr);
-                write_phi(zr, true, sbase + PHIQ_OFF, i);
-                tmem_ld64(lane_base + T_Z + FH, zr);
-                write_phi(zr, row < p.N, sbase + PHIK_OFF, i);
-            }
+            uint32_t pk[64];
+            phi_regs(zcol, grp == 0 || i < p.N, pk);  // phi(Q) always live; phi(K) zero past N
+            phi_store(pk, phi_tile, i);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             warp_arrive(bar(B_PHIREADY), lane);
-            // --- P = S under the causal mask (keys j <= i of the chunk and j < N)
-            if (!wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_SFULL << 16) | c)) break;
+        }
+        for (int c = 0; ok && c < n_chunks; ++c) {
+            const uint32_t ph = c & 1;
+            const int row = c * C + i;
+            // --- this group's half of P = S under the causal mask (keys j <= i of the chunk and j < N)
+            if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_SFULL << 16) | c)))
+                break;
             tc_fence_after_sync();
             {
                 const int jmax = min(i, p.N - 1 - c * C);
+                uint32_t sr[64];
+                tmem_ld64(lane_base + T_Z + grp * 64, sr);
+                uint32_t pk[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sr[64];
-                    tmem_ld64(lane_base + T_Z + half * 64, sr);
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j0 = half * 64 + 2 * e;
-                        pk[e] = pack_bf16x2(j0 <= jmax ? __uint_as_float(sr[2 * e]) : 0.0f,
-                                            j0 + 1 <= jmax ? __uint_as_float(sr[2 * e + 1]) : 0.0f);
-                    }
-                    tmem_st32(lane_base + T_Z + half * 32, pk);
+                for (int e = 0; e < 32; ++e) {
+                    const int j0 = grp * 64 + 2 * e;
+                    pk[e] = pack_bf16x2(j0 <= jmax ? __uint_as_float(sr[2 * e]) : 0.0f,
+                                        j0 + 1 <= jmax ? __uint_as_float(sr[2 * e + 1]) : 0.0f);
                 }
+                tmem_st32(lane_base + T_P + grp * 32, pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
             warp_arrive(bar(B_PREADY), lane);
-            // --- O_i = num_i / den_i
-            if (!wait_bounded(bar(B_ODONE), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ODONE << 16) | c)) break;
-            tc_fence_after_sync();
-            {
-                uint32_t o[64], d[16];
-                tmem_ld64(lane_base + T_O, o);
-                tmem_ld16(lane_base + T_O + 64, d);
-                const float den = __uint_as_float(d[0]);
-                if (row < p.N) {
-                    const float inv = 1.0f / den;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[q] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-                    p.DEN[head_row0 + row] = den;
-                }
-            }
-            // --- bf16 copy of the state S_{<=c} (rows 0..79 of S^T) for the next chunk
-            if (!wait_bounded(bar(B_STDONE), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_STDONE << 16) | c)) break;
-            tc_fence_after_sync();
             if (c + 1 < n_chunks) {
+                // --- chunk c+1's feature maps into registers (Z of c+1 follows P [V|1] of c)
+                if (!(ok = wait_bounded(bar(B_ZFULL), ph ^ 1, abort_flag,
+                                        (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16) | (c + 1))))
+                    break;
+                tc_fence_after_sync();
+                uint32_t pk[64];
+                phi_regs(zcol, grp == 0 || row + C < p.N, pk);
+                // --- chunk c's products done: the state copy, then the feature maps into smem
+                if (!(ok = wait_bounded(bar(B_STDONE), ph, abort_flag,
+                                        (ROLE_HH_COMPUTE << 24) | (B_STDONE << 16) | c)))
+                    break;
+                tc_fence_after_sync();
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    uint32_t sv[64];
-                    tmem_ld64(lane_base + T_ST + part * 64, sv);  // every lane loads; rows >= 80 are not stored
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sv[32];
+                    tmem_ld32(lane_base + T_ST + grp * 64 + h2 * 32, sv);  // every lane loads; rows >= 80 are not stored
                     if (i < NV) {
-                        const uint32_t box = sbase + SPREV_OFF + part * SBOX;
+                        const uint32_t box = sbase + SPREV_OFF + grp * SBOX;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_shared_v4(sw128(box, i, q),
+                        for (int q = 0; q < 4; ++q)
+                            st_shared_v4(sw128(box, i, h2 * 4 + q),
                                          pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
                     }
                 }
+                phi_store(pk, phi_tile, i);
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
-                warp_arrive(bar(B_SREADY), lane);
+                warp_arrive(bar(B_PHIREADY), lane);
+            }
+            // --- O_i = num_i / den_i, this group's 32 columns (read before the
+            // group arrives on the next chunk's PREADY, after which the
+            // tensor core overwrites them)
+            if (!(ok = wait_bounded(bar(B_ODONE), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ODONE << 16) | c)))
+                break;
+            tc_fence_after_sync();
+            {
+                uint32_t o[32], d[16];
+                tmem_ld32(lane_base + T_O + grp * 32, o);
+                tmem_ld16(lane_base + T_O + 64, d);
+                const float den = __uint_as_float(d[0]);
+                if (row < p.N) {
+                    const float inv = 1.0f / den;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV +
+                                                           grp * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+                    if (grp == 0) p.DEN[head_row0 + row] = den;
+                }
             }
         }
     }
