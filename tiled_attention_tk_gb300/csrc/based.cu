@@ -46,7 +46,7 @@ namespace based {
 constexpr int C = 128;             // rows per chunk
 constexpr int DQK = 16;
 constexpr int DV = 64;
-constexpr int F = 192;             // feature columns (153 live)
+constexpr int F = 160;             // feature columns (153 live; ten 16-feature steps)
 constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_TMA = 8;
@@ -57,31 +57,40 @@ constexpr uint32_t ROLE_BASED_MMA = 13;
 constexpr uint32_t ROLE_BASED_COMPUTE = 14;
 
 constexpr uint32_t BOX = 128 * 128;                   // 128 rows x 128 bytes
-constexpr uint32_t QKV_OFF = 0;                       // buffer b: Q, K, V boxes at + b * 3 * BOX
-constexpr uint32_t ONES_OFF = QKV_OFF + 6 * BOX;      // [row][col]: 1 in column 0
+constexpr uint32_t QK_OFF = 0;                        // buffer b: Q, K boxes at + b * 2 * BOX
+constexpr uint32_t V_OFF = QK_OFF + 4 * BOX;          // buffer b: V box at + b * BOX
+constexpr uint32_t ONES_OFF = V_OFF + 2 * BOX;        // [row][col]: 1 in column 0
 constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 192 features (3 boxes)
 constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
 constexpr uint32_t SPREV_OFF = PHIK_OFF + 3 * BOX;    // S (bf16, K-major): 80 rows x 192 features (3 boxes)
-constexpr uint32_t BAR_OFF = SPREV_OFF + 3 * SBOX;
-constexpr int B_FULL = 0;          // + buffer (2)
-constexpr int B_EMPTY = 2;         // + buffer (2)
-constexpr int B_SFULL = 4;         // Q K^T in TMEM
-constexpr int B_PREADY = 5;        // P, phi(Q) in TMEM, the bf16 state in smem, the last O read out (8 warps)
-constexpr int B_SREAD = 6;         // both groups hold their half of S in registers (8 warps)
-constexpr int B_ODONE = 7;         // [num | den] of the chunk complete
-constexpr int B_PHIKREADY = 8;     // phi(K) in smem (8 warps)
-constexpr int B_STDONE = 9;        // state product done
-constexpr int B_MMADONE = 10;
-constexpr int NUM_BARS = 11;
+constexpr uint32_t OBOX = 32 * DV;                    // 32 rows x 64 bytes: one warp's O columns
+constexpr uint32_t OST_OFF = SPREV_OFF + 3 * SBOX;    // O staging: one 32 x 32 box per compute warp
+constexpr uint32_t BAR_OFF = OST_OFF + 8 * OBOX;
+constexpr int B_QKFULL = 0;        // + buffer (2): Q, K of a chunk loaded
+constexpr int B_QKEMPTY = 2;       // + buffer (2): its Q K^T and feature maps formed (8 warps)
+constexpr int B_VFULL = 4;         // + buffer (2): V of a chunk loaded
+constexpr int B_VEMPTY = 6;        // + buffer (2): its P [V|1] and state products done
+constexpr int B_SFULL = 8;         // Q K^T in TMEM
+constexpr int B_SREAD = 9;         // both groups hold their half of S in registers (8 warps)
+constexpr int B_PREADY = 10;       // P in TMEM, the last O read out (8 warps)
+constexpr int B_PHIQREADY = 11;    // phi(Q) in TMEM, the bf16 state of the chunks before in smem (8 warps)
+constexpr int B_PHIKREADY = 12;    // phi(K) in smem (8 warps)
+constexpr int B_ODONE = 13;        // [num | den] of the chunk complete
+constexpr int B_STDONE = 14;       // state product done
+constexpr int B_MMADONE = 15;
+constexpr int NUM_BARS = 16;
 constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
-static_assert(SBOX % 1024 == 0 && SPREV_OFF % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+static_assert(SBOX % 1024 == 0 && SPREV_OFF % 1024 == 0 && OST_OFF % 1024 == 0,
+              "swizzled boxes need 1024-byte alignment");
 
-constexpr uint32_t T_S = 0;        // Q K^T (fp32, 128 cols); P (bf16) over cols 0..63
-constexpr uint32_t T_PHIQ = 128;   // phi(Q) bf16: 96 cols
-constexpr uint32_t T_O = 224;      // [num | den] fp32: 80 cols
-constexpr uint32_t T_ST = 320;     // S^T fp32: 192 cols (lane = value column, 64 = the "1" row)
+constexpr uint32_t T_S = 0;        // Q K^T (fp32, 128 cols)
+constexpr uint32_t T_PHIQ = 128;   // phi(Q) bf16: 80 cols
+constexpr uint32_t T_O = 208;      // [num | den] fp32: 80 cols
+constexpr uint32_t T_ST = 288;     // S^T fp32: 160 cols (lane = value column, 64 = the "1" row)
+constexpr uint32_t T_P = 448;      // P bf16: 64 cols, apart from S so the next S can be formed early
+static_assert(T_P + 64 <= TMEM_COLS, "TMEM plan");
 
 __device__ __forceinline__ uint32_t sw128(uint32_t box, int r, int c) { return box + r * 128 + ((c ^ (r & 7)) << 4); }
 
@@ -95,8 +104,8 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// phi(x) as 96 packed bf16 pairs: [1, r x_a (16), h x_a^2 (16),
-// g x_a x_b for a < b in order (120), 0 (39)].  Every index is a compile-time
+// phi(x) as 80 packed bf16 pairs: [1, r x_a (16), h x_a^2 (16),
+// g x_a x_b for a < b in order (120), 0 (7)].  Every index is a compile-time
 // constant once the loops are unrolled.
 __device__ __forceinline__ void phi_packed(const float (&x)[DQK], float r, float h, float g, uint32_t (&pk)[F / 2]) {
     float f[F];
@@ -128,10 +137,10 @@ __device__ __forceinline__ void load_row16(uint32_t box, int r, float (&x)[DQK])
     }
 }
 
-// phi of one row (16 features from a swizzled box) into the 64-feature parts
-// of PARTS (bit k = features 64k .. 64k+63): into TMEM as the A operand of
-// the inter product, or into row r of the phi(K) boxes.  `live` false zeroes
-// the row (a key past N, the constant feature included).
+// phi of one row (16 features from a swizzled box) into the feature parts of
+// PARTS (bit k = features 64k .. 64k+63; part 2 holds 128..159): into TMEM as
+// the A operand of the inter product, or into row r of the phi(K) boxes.
+// `live` false zeroes the row (a key past N, the constant feature included).
 template <int PARTS, bool TO_TMEM>
 __device__ __forceinline__ void phi_store(uint32_t box16, int r, bool live, float rs, float hs, float gs,
                                           uint32_t dst) {
@@ -148,35 +157,52 @@ __device__ __forceinline__ void phi_store(uint32_t box16, int r, bool live, floa
     for (int part = 0; part < 3; ++part) {
         if (!(PARTS & (1 << part))) continue;
         if constexpr (TO_TMEM) {
-            tmem_st32(dst + part * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * part));
+            if (part < 2)
+                tmem_st32(dst + part * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * part));
+            else
+                tmem_st16(dst + 64, *reinterpret_cast<const uint32_t(*)[16]>(pk + 64));
         } else {
             const uint32_t box = dst + part * BOX;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < (part < 2 ? 8 : 4); ++q)
                 st_shared_v4(sw128(box, r, q), pk[32 * part + 4 * q], pk[32 * part + 4 * q + 1],
                              pk[32 * part + 4 * q + 2], pk[32 * part + 4 * q + 3]);
         }
     }
 }
 
-// O_i = num_i / den_i for 32 columns from `col` of the [num | den] accumulator;
-// DEN written when `den_out` is set.
-__device__ __forceinline__ void write_o(uint32_t lane_taddr, int col, bool live, __nv_bfloat16 *o_row,
-                                        float *den_out) {
+// O_i = num_i / den_i for the warp's 32 rows and its group's 32 columns of
+// the [num | den] accumulator: bf16 into the warp's staging box (64-byte
+// swizzle), then one TMA store by lane 0 (rows past N are clipped).  DEN is
+// written when `den_out` is set.
+__device__ __forceinline__ void write_o(uint32_t lane_taddr, int grp, int lane, uint32_t obox, const CUtensorMap *tmO,
+                                        int row0, int bh, int N, float *den_out) {
     uint32_t o[32], d[16];
-    tmem_ld32(lane_taddr + T_O + col, o);
+    tmem_ld32(lane_taddr + T_O + grp * 32, o);
     tmem_ld16(lane_taddr + T_O + 64, d);
     const float den = __uint_as_float(d[0]);
-    if (live) {
-        const float inv = 1.0f / den;
-        uint4 *dst = reinterpret_cast<uint4 *>(o_row + col);
+    const float inv = 1.0f / den;
+    const float2 inv2 = make_float2(inv, inv);
+    if (lane == 0) tma_store_wait_read_all();  // this warp's previous store has read the box
+    __syncwarp();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-        if (den_out) *den_out = den;
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 v =
+                __fmul2_rn(make_float2(__uint_as_float(o[8 * q + 2 * t]), __uint_as_float(o[8 * q + 2 * t + 1])), inv2);
+            w[t] = pack_bf16x2(v.x, v.y);
+        }
+        // 64-byte swizzle: 16-byte chunk q of row `lane` at chunk q ^ ((lane >> 1) & 3)
+        st_shared_v4(obox + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+    }
+    if (den_out && row0 + lane < N) *den_out = den;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < N) {
+        tma_store_3d(tmO, obox, grp * 32, row0, bh);
+        tma_store_commit();
     }
 }
 
@@ -200,14 +226,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     }
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_FULL + b), 1);
-            mbar_init(bar(B_EMPTY + b), 1);
+            mbar_init(bar(B_QKFULL + b), 1);
+            mbar_init(bar(B_QKEMPTY + b), 8);
+            mbar_init(bar(B_VFULL + b), 1);
+            mbar_init(bar(B_VEMPTY + b), 1);
         }
         mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_PREADY), 8);
         mbar_init(bar(B_SREAD), 8);
-        mbar_init(bar(B_ODONE), 1);
+        mbar_init(bar(B_PREADY), 8);
+        mbar_init(bar(B_PHIQREADY), 8);
         mbar_init(bar(B_PHIKREADY), 8);
+        mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_STDONE), 1);
         mbar_init(bar(B_MMADONE), 1);
         *abort_flag = 0;
@@ -232,26 +261,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             tma_prefetch_desc(&p.tmQ);
             tma_prefetch_desc(&p.tmK);
             tma_prefetch_desc(&p.tmV);
-            int issued = 0;
+            // Q, K of chunk c into buffer c & 1 once chunk c-2's Q K^T and
+            // feature maps are formed (early, so the next S never waits on
+            // HBM); V of chunk c once chunk c-2's products are done.
+            int qk_issued = 0, v_issued = 0;
+            bool ok = true;
             for (int c = 0; c < n_chunks; ++c) {
                 const int b = c & 1;
-                if (c >= 2 && !wait_bounded(bar(B_EMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
-                                            (ROLE_BASED_PRODUCER << 24) | ((B_EMPTY + b) << 16) | c)) {
-                    const uint64_t t0 = global_timer_ns();
-                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                        while (!mbar_try_wait(bar(B_FULL + (j & 1)), (j >> 1) & 1) &&
-                               global_timer_ns() - t0 < kDrainLimitNs) {
-                        }
+                if (c >= 2 && !(ok = wait_bounded(bar(B_QKEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_BASED_PRODUCER << 24) | ((B_QKEMPTY + b) << 16) | c)))
                     break;
-                }
                 // Q and K boxes carry 16 real columns; TMA fills the rest with 0
                 // but still counts the full box.
-                const uint32_t dst = sbase + QKV_OFF + b * 3 * BOX;
-                mbar_arrive_expect_tx(bar(B_FULL + b), 3 * BOX);
-                tma_load_3d(dst, &p.tmQ, bar(B_FULL + b), 0, c * C, bh);
-                tma_load_3d(dst + BOX, &p.tmK, bar(B_FULL + b), 0, c * C, bh);
-                tma_load_3d(dst + 2 * BOX, &p.tmV, bar(B_FULL + b), 0, c * C, bh);
-                ++issued;
+                const uint32_t dst = sbase + QK_OFF + b * 2 * BOX;
+                mbar_arrive_expect_tx(bar(B_QKFULL + b), 2 * BOX);
+                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, c * C, bh);
+                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, c * C, bh);
+                ++qk_issued;
+                if (c >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | c)))
+                    break;
+                mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
+                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, c * C, bh);
+                ++v_issued;
+            }
+            if (!ok) {
+                // let the loads in flight land before the CTA's shared memory goes away
+                const uint64_t t0 = global_timer_ns();
+                for (int j = qk_issued - 2 < 0 ? 0 : qk_issued - 2; j < qk_issued; ++j)
+                    while (!mbar_try_wait(bar(B_QKFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+                    while (!mbar_try_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
             }
         }
         __syncwarp();
@@ -262,15 +304,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
             constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
             constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
-            // Per chunk c: P [V|1], then Q K^T of chunk c+1 (its P is formed while
-            // this chunk's other products run), phi(Q) S_{<c}, and the state
-            // update once phi(K) is in smem.
+            // Per chunk c: Q K^T of chunk c+1 as soon as both groups hold S of
+            // chunk c in registers; then P [V|1], phi(Q) S_{<c} and the state
+            // update, each once its operands are in place.
             auto issue_s = [&](int c) {
-                const uint32_t qb = sbase + QKV_OFF + (c & 1) * 3 * BOX;
+                const uint32_t qb = sbase + QK_OFF + (c & 1) * 2 * BOX;
                 umma_ss(tmem + T_S, smem_desc_sw128(qb, 16, 1024), smem_desc_sw128(qb + BOX, 16, 1024), ID_S, 0);
                 umma_commit(bar(B_SFULL));
             };
-            bool ok = wait_bounded(bar(B_FULL), 0, abort_flag, (ROLE_BASED_MMA << 24) | (B_FULL << 16));
+            bool ok = wait_bounded(bar(B_QKFULL), 0, abort_flag, (ROLE_BASED_MMA << 24) | (B_QKFULL << 16));
             if (ok) {
                 tc_fence_after_sync();
                 issue_s(0);
@@ -278,24 +320,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             for (int c = 0; ok && c < n_chunks; ++c) {
                 const int b = c & 1;
                 const uint32_t ph = c & 1;
-                const uint32_t vb = sbase + QKV_OFF + b * 3 * BOX + 2 * BOX;
+                const uint32_t vb = sbase + V_OFF + b * BOX;
+                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | c)))
+                    break;
+                if (c + 1 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | (c + 1))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_s(c + 1);
+                }
                 if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | c)))
+                    break;
+                if (!(ok = wait_bounded(bar(B_VFULL + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | ((B_VFULL + b) << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]; 16 chunk rows per step
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ts(tmem + T_O, tmem + T_S + k * 8,
+                    umma_ts(tmem + T_O, tmem + T_P + k * 8,
                             smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
-                // S of the next chunk over P of this one (the tensor core runs them in order)
-                if (c + 1 < n_chunks) {
-                    if (!(ok = wait_bounded(bar(B_FULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
-                                            (ROLE_BASED_MMA << 24) | ((B_FULL + (b ^ 1)) << 16) | (c + 1))))
-                        break;
-                    tc_fence_after_sync();
-                    issue_s(c + 1);
-                }
                 // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
+                if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | c)))
+                    break;
+                tc_fence_after_sync();
                 if (c > 0) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
@@ -314,7 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                     umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
                             smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE, (c > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
-                umma_commit(bar(B_EMPTY + b));
+                umma_commit(bar(B_VEMPTY + b));
             }
             umma_commit(bar(B_MMADONE));
             const uint64_t t0 = global_timer_ns();
@@ -325,68 +375,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     } else {
         // ------------------------------------------------ compute warps
         // Two warpgroups over the same 128 rows (warp w reads TMEM lanes
-        // 32 (w % 4) ..); each takes half of every step.  Per chunk c, once
-        // S(c) is in TMEM (while chunk c-1's phi(Q) S and state products may
-        // still run): P(c); O of chunk c-1; the bf16 state copy of chunk c-1;
-        // phi(Q) of chunk c (group 0: features 0..127, group 1: 128..191);
-        // PREADY; then phi(K) of chunk c (the other split) for the state
-        // product, which the tensor core takes last.
+        // 32 (w % 4) ..); each takes half of every step.  Per chunk c: S(c)
+        // into registers (the tensor core may then form S(c+1)); P(c) once
+        // chunk c-1's [num | den] is complete; O of chunk c-1; PREADY; the
+        // bf16 state copy of chunk c-1 and phi(Q) of chunk c; PHIQREADY;
+        // phi(K) of chunk c; PHIKREADY.
         const int i = threadIdx.x % 128;  // row of the chunk = TMEM lane; also row i of S^T
         const int grp = warp / 4;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const float scale = p.scale;
         const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
         const size_t head_row0 = static_cast<size_t>(bh) * p.N;
-        __nv_bfloat16 *const Obase = static_cast<__nv_bfloat16 *>(p.O);
+        const uint32_t obox = sbase + OST_OFF + warp * OBOX;
         bool ok = true;
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
             const uint32_t ph = c & 1;
-            const uint32_t qb = sbase + QKV_OFF + b * 3 * BOX, kb = qb + BOX;
+            const uint32_t qb = sbase + QK_OFF + b * 2 * BOX, kb = qb + BOX;
             const int row = c * C + i;  // sequence position of this thread's query and key
             if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | c)))
                 break;
             tc_fence_after_sync();
-            // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this
-            // group's 64 keys.  P columns 32..63 lie over S columns group 0
-            // reads, so both groups load their S first.
+            // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this group's 64 keys
+            uint32_t pk[32];
             {
                 const int jmax = min(i, p.N - 1 - c * C);  // last key of the chunk this row sees
                 uint32_t sr[64];
                 tmem_ld64(lane_base + T_S + grp * 64, sr);
                 tc_fence_before_sync();
                 warp_arrive(bar(B_SREAD), lane);
-                uint32_t pk[32];
+                const float2 sc2 = make_float2(scale, scale), one2 = make_float2(1.0f, 1.0f),
+                             half2 = make_float2(0.5f, 0.5f);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int j0 = grp * 64 + 2 * e;
-                    const float s0 = scale * __uint_as_float(sr[2 * e]);
-                    const float s1 = scale * __uint_as_float(sr[2 * e + 1]);
-                    const float w0 = j0 <= jmax ? fmaf(0.5f * s0, s0, s0 + 1.0f) : 0.0f;
-                    const float w1 = j0 + 1 <= jmax ? fmaf(0.5f * s1, s1, s1 + 1.0f) : 0.0f;
-                    pk[e] = pack_bf16x2(w0, w1);
+                    const float2 s2 = __fmul2_rn(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2);
+                    const float2 w2 = __ffma2_rn(__fmul2_rn(half2, s2), s2, __fadd2_rn(s2, one2));
+                    pk[e] = pack_bf16x2(j0 <= jmax ? w2.x : 0.0f, j0 + 1 <= jmax ? w2.y : 0.0f);
                 }
-                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SREAD << 16) | c)))
-                    break;
-                tc_fence_after_sync();
-                tmem_st32(lane_base + T_S + grp * 32, pk);  // P over the first 64 columns
             }
             if (c > 0) {
-                // --- O of chunk c-1, this group's 32 columns
+                // chunk c-1's P [V|1] and phi(Q) S are done: T_P, T_O and T_PHIQ are free
                 if (!(ok = wait_bounded(bar(B_ODONE), ph ^ 1, abort_flag,
                                         (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | c)))
                     break;
                 tc_fence_after_sync();
-                write_o(lane_base, grp * 32, row - C < p.N, Obase + (head_row0 + row - C) * DV,
+            }
+            tmem_st32(lane_base + T_P + grp * 32, pk);
+            if (c > 0)  // --- O of chunk c-1, this group's 32 columns
+                write_o(lane_base, grp, lane, obox, &p.tmO, (c - 1) * C + (warp % 4) * 32, bh, p.N,
                         grp == 0 ? p.DEN + head_row0 + row - C : nullptr);
-                // --- bf16 copy of the state S_{<c} (rows 0..79 of S^T): 96 of the 192 features
+            tmem_st_wait();
+            tc_fence_before_sync();
+            warp_arrive(bar(B_PREADY), lane);
+            if (c > 0) {
+                // --- bf16 copy of the state S_{<c} (rows 0..79 of S^T): 32-feature blocks
+                // {0, 1} (group 0) and {2, 3, 4} (group 1) of the 160
                 if (!(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
                                         (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
                     break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int blk = 0; blk < 3; ++blk) {
-                    const int col = grp * 96 + blk * 32;
+                    if (grp == 0 && blk == 2) break;
+                    const int col = grp == 0 ? blk * 32 : 64 + blk * 32;
                     uint32_t sv[32];
                     tmem_ld32(lane_base + T_ST + col, sv);  // every lane loads; rows >= 80 are not stored
                     if (i < NV) {
@@ -402,24 +454,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                     }
                 }
             }
-            // --- phi(Q) of chunk c into TMEM (its last reader, chunk c-1's phi(Q) S, is done)
+            // --- phi(Q) of chunk c into TMEM (group 0: features 0..63; group 1: 64..159)
             if (grp == 0)
-                phi_store<3, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
+                phi_store<1, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
             else
-                phi_store<4, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
+                phi_store<6, true>(qb, i, true, r, h, g, lane_base + T_PHIQ);
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            warp_arrive(bar(B_PREADY), lane);
-            // --- phi(K) of chunk c into smem (0 for keys past N); its last reader,
-            // chunk c-1's state product, is done
+            warp_arrive(bar(B_PHIQREADY), lane);
+            // --- phi(K) of chunk c into smem, 0 for keys past N (group 0: features 64..159;
+            // group 1: 0..63); its last reader, chunk c-1's state product, is done
             if (grp == 0)
-                phi_store<4, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
+                phi_store<6, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
             else
-                phi_store<3, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
+                phi_store<1, false>(kb, i, row < p.N, r, h, g, sbase + PHIK_OFF);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             warp_arrive(bar(B_PHIKREADY), lane);
+            warp_arrive(bar(B_QKEMPTY + b), lane);  // this chunk's Q and K are no longer read here
         }
         // --- O of the last chunk
         if (ok && n_chunks > 0 &&
@@ -427,9 +480,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                          (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | n_chunks)) {
             tc_fence_after_sync();
             const int row = (n_chunks - 1) * C + i;
-            write_o(lane_base, grp * 32, row < p.N, Obase + (head_row0 + row) * DV,
+            write_o(lane_base, grp, lane, obox, &p.tmO, (n_chunks - 1) * C + (warp % 4) * 32, bh, p.N,
                     grp == 0 ? p.DEN + head_row0 + row : nullptr);
         }
+        if (lane == 0) tma_store_wait_all();
     }
 
     tc_fence_before_sync();

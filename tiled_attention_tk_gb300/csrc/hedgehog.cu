@@ -33,7 +33,7 @@ constexpr int C = 128;             // rows per chunk
 constexpr int DQK = 64;            // query / key dims
 constexpr int FH = 64;             // features per half
 constexpr int F = 2 * FH;          // feature dims of phi
-constexpr int DV = 64;
+constexpr int DV = 64;              // value dims: O rows leave as two 32-column boxes
 constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
 constexpr int NUM_THREADS = 320;   // two compute warpgroups, a TMA warp, an MMA warp
 constexpr int WARP_TMA = 8;
@@ -42,40 +42,51 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ROLE_HH_PRODUCER = 15;
 constexpr uint32_t ROLE_HH_MMA = 16;
 constexpr uint32_t ROLE_HH_COMPUTE = 17;
+constexpr uint32_t ROLE_HH_LAYOUT = 18;
 
 constexpr uint32_t BOX = 128 * 128;                   // 128 rows x 128 bytes
 constexpr uint32_t WBOX = 64 * 128;                   // 64 rows x 128 bytes
-constexpr uint32_t QKV_OFF = 0;                       // buffer b: Q, K, V boxes at + b * 3 * BOX
-constexpr uint32_t WQ_OFF = QKV_OFF + 6 * BOX;        // Wq [d][f]
+constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
+constexpr uint32_t OBOX = 32 * DV;                    // 32 rows x 64 bytes: one warp's O columns
+constexpr uint32_t QK_OFF = 0;                        // Q, K boxes of the chunk Z is formed from next
+constexpr uint32_t V_OFF = QK_OFF + 2 * BOX;          // V box of chunk c at + (c & 1) * BOX
+constexpr uint32_t WQ_OFF = V_OFF + 2 * BOX;          // Wq [d][f]
 constexpr uint32_t WK_OFF = WQ_OFF + WBOX;            // Wk [d][f]
 constexpr uint32_t ONES_OFF = WK_OFF + WBOX;          // [row][col]: 1 in column 0
-constexpr uint32_t PHIQ_OFF = ONES_OFF + BOX;         // phi(Q): 128 rows x 128 features (2 boxes)
-constexpr uint32_t PHIK_OFF = PHIQ_OFF + 2 * BOX;     // phi(K): same
-constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
+constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 128 features (2 boxes)
 constexpr uint32_t SPREV_OFF = PHIK_OFF + 2 * BOX;    // S (bf16, K-major): 80 rows x 128 features (2 boxes)
-constexpr uint32_t BAR_OFF = SPREV_OFF + 2 * SBOX;
-constexpr int B_FULL = 0;          // + buffer (2)
-constexpr int B_EMPTY = 2;         // + buffer (2)
-constexpr int B_WFULL = 4;         // Wq, Wk loaded
-constexpr int B_ZFULL = 5;         // Q Wq, K Wk in TMEM
-constexpr int B_PHIREADY = 6;      // phi(Q), phi(K) and the bf16 state of the chunks before in smem (8 warps)
-constexpr int B_SFULL = 7;         // phi(Q) phi(K)^T in TMEM
-constexpr int B_PREADY = 8;        // P in TMEM, the last O read out (8 warps)
-constexpr int B_ODONE = 9;         // [num | den] of the chunk complete
-constexpr int B_STDONE = 10;       // all products of the chunk done
-constexpr int B_MMADONE = 11;
-constexpr int NUM_BARS = 12;
+constexpr uint32_t OST_OFF = SPREV_OFF + 2 * SBOX;    // O staging: one 32 x 32 box per compute warp
+constexpr uint32_t BAR_OFF = OST_OFF + 8 * OBOX;
+constexpr int B_QKFULL = 0;        // Q, K of the next Z loaded
+constexpr int B_QKEMPTY = 1;       // Z has read them
+constexpr int B_VFULL = 2;         // + buffer (2)
+constexpr int B_VEMPTY = 4;        // + buffer (2)
+constexpr int B_WFULL = 6;         // Wq, Wk loaded
+constexpr int B_ZFULL = 7;         // Q Wq, K Wk in TMEM
+constexpr int B_PHIREADY = 8;      // phi(Q) in TMEM, phi(K) and the bf16 state of the chunks before in smem (8 warps)
+constexpr int B_SFULL = 9;         // phi(Q) phi(K)^T in TMEM
+constexpr int B_SREAD = 10;        // both groups hold their half of S in registers (8 warps)
+constexpr int B_PREADY = 11;       // P in TMEM, the last O read out (8 warps)
+constexpr int B_ODONE = 12;        // [num | den] of the chunk complete
+constexpr int B_STDONE = 13;       // all products of the chunk done
+constexpr int B_MMADONE = 14;
+constexpr int NUM_BARS = 15;
 constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+// The dynamic shared memory base is 1024-byte aligned (no static shared
+// memory in this kernel); the kernel checks it and reports ROLE_HH_LAYOUT.
+constexpr uint32_t SMEM_ALLOC = SMEM_USED;
 static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
-static_assert(WQ_OFF % 1024 == 0 && ONES_OFF % 1024 == 0 && SPREV_OFF % 1024 == 0 && SBOX % 1024 == 0,
-              "swizzled boxes need 1024-byte alignment");
+static_assert(WQ_OFF % 1024 == 0 && ONES_OFF % 1024 == 0 && PHIK_OFF % 1024 == 0 && SPREV_OFF % 1024 == 0 &&
+                  SBOX % 1024 == 0 &&
+                  OST_OFF % 1024 == 0 && OBOX % 512 == 0,
+              "swizzled boxes need 1024-byte (64-byte swizzle: 512-byte) alignment");
 
 constexpr uint32_t T_Z = 0;        // Q Wq (cols 0..63), K Wk (64..127); then S
 constexpr uint32_t T_O = 128;      // [num | den] fp32: 80 cols
 constexpr uint32_t T_ST = 256;     // S^T fp32: 128 cols (lane = value column, 64 = the "1" row)
-constexpr uint32_t T_P = 384;      // P (bf16, 64 cols): apart from S, so the two groups need no
-                                   // order between one's reads of S and the other's writes of P
+constexpr uint32_t T_P = 384;      // P (bf16, 64 cols): apart from S, so the next Z can be formed
+                                   // as soon as S is read out
+constexpr uint32_t T_PHIQ = 448;   // phi(Q) (bf16, 64 cols): the A operand of S and of the carried product
 
 __device__ __forceinline__ uint32_t sw128(uint32_t box, int r, int c) { return box + r * 128 + ((c ^ (r & 7)) << 4); }
 
@@ -83,52 +94,61 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // phi(z) = [softmax(z), softmax(-z)] of one row's 64 projections (TMEM
 // columns from `zcol`), as 64 packed bf16 pairs (zeros when `live` is false).
 // The projections are read again for the second half, so that only one
-// half's 64 exponentials are live at a time.
+// half's 64 exponentials are live at a time; pairs of columns go through the
+// packed fp32 pipe.
 __device__ __forceinline__ void phi_regs(uint32_t zcol, bool live, uint32_t (&pk)[64]) {
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t zr[64];
     tmem_ld64(zcol, zr);
     float zmax = __uint_as_float(zr[0]), zmin = zmax;
 #pragma unroll
-    for (int c = 1; c < FH; ++c) {
-        const float z = __uint_as_float(zr[c]);
-        zmax = fmaxf(zmax, z);
-        zmin = fminf(zmin, z);
+    for (int c = 1; c < FH; c += 2) {
+        zmax = fmax3(zmax, __uint_as_float(zr[c]), __uint_as_float(zr[c + 1 < FH ? c + 1 : c]));
+        zmin = fmin3(zmin, __uint_as_float(zr[c]), __uint_as_float(zr[c + 1 < FH ? c + 1 : c]));
     }
-    // exp(z - zmax) = 2^(z log2e - zmax log2e), exp(zmin - z) likewise
-    const float offp = -zmax * kLog2e, offn = zmin * kLog2e;
+    // exp(z - zmax) = 2^(z log2e - zmax log2e); exp(zmin - z) = 2^(-z log2e + zmin log2e)
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        float e[FH];
-        float sum = 0.0f;
-        if (half == 0) {
+        const float2 mul = half == 0 ? make_float2(kLog2e, kLog2e) : make_float2(-kLog2e, -kLog2e);
+        const float off = half == 0 ? -zmax * kLog2e : zmin * kLog2e;
+        const float2 add = make_float2(off, off);
+        float2 e[FH / 2];
+        float2 sum2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int c = 0; c < FH; ++c) {
-                e[c] = ex2(fmaf(__uint_as_float(zr[c]), kLog2e, offp));
-                sum += e[c];
-            }
-        } else {
+        for (int part = 0; part < 2; ++part) {
+            uint32_t zp[32];
+            if (half == 1) tmem_ld32(zcol + part * 32, zp);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {  // reloaded in two 32-column parts
-                uint32_t zp[32];
-                tmem_ld32(zcol + part * 32, zp);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    e[part * 32 + c] = ex2(fmaf(-__uint_as_float(zp[c]), kLog2e, offn));
-                    sum += e[part * 32 + c];
-                }
+            for (int q = 0; q < 16; ++q) {
+                const int c = part * 32 + 2 * q;
+                const float2 z2 = half == 0 ? make_float2(__uint_as_float(zr[c]), __uint_as_float(zr[c + 1]))
+                                            : make_float2(__uint_as_float(zp[2 * q]), __uint_as_float(zp[2 * q + 1]));
+                const float2 a = __ffma2_rn(z2, mul, add);
+                e[c / 2] = make_float2(ex2(a.x), ex2(a.y));
+                sum2 = __fadd2_rn(sum2, e[c / 2]);
             }
         }
-        const float sc = live ? 1.0f / sum : 0.0f;
+        const float sc = live ? 1.0f / (sum2.x + sum2.y) : 0.0f;
+        const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-        for (int q = 0; q < FH / 2; ++q) pk[half * 32 + q] = pack_bf16x2(e[2 * q] * sc, e[2 * q + 1] * sc);
+        for (int q = 0; q < FH / 2; ++q) {
+            const float2 v = __fmul2_rn(e[q], sc2);
+            pk[half * 32 + q] = pack_bf16x2(v.x, v.y);
+        }
     }
 }
 
-// Row r of a two-box 128-feature K-major tile from 64 packed bf16 pairs.
+// Row r of a two-box 128-feature K-major tile from 64 packed bf16 pairs (phi(K));
+// phi(Q) goes to TMEM instead.
 __device__ __forceinline__ void phi_store(const uint32_t (&pk)[64], uint32_t tile, int r) {
 #pragma unroll
     for (int half = 0; half < 2; ++half)
@@ -139,9 +159,7 @@ __device__ __forceinline__ void phi_store(const uint32_t (&pk)[64], uint32_t til
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_constant__ HedgehogParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
@@ -153,19 +171,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
     const int head = bh % p.H;
     const int n_chunks = (p.N + C - 1) / C;
 
+    if (sbase & 1023u) {  // the swizzled layouts need it; uniform over the CTA, so every thread returns
+        if (threadIdx.x == 0) record_timeout((ROLE_HH_LAYOUT << 24) | (sbase & 0xFFFFu));
+        return;
+    }
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
     if (threadIdx.x == 0) {
+        mbar_init(bar(B_QKFULL), 1);
+        mbar_init(bar(B_QKEMPTY), 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_FULL + b), 1);
-            mbar_init(bar(B_EMPTY + b), 1);
+            mbar_init(bar(B_VFULL + b), 1);
+            mbar_init(bar(B_VEMPTY + b), 1);
         }
         mbar_init(bar(B_WFULL), 1);
         mbar_init(bar(B_ZFULL), 1);
         mbar_init(bar(B_PHIREADY), 8);
         mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_SREAD), 8);
         mbar_init(bar(B_PREADY), 8);
         mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_STDONE), 1);
@@ -196,26 +221,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             mbar_arrive_expect_tx(bar(B_WFULL), 2 * WBOX);
             tma_load_3d(sbase + WQ_OFF, &p.tmWq, bar(B_WFULL), 0, 0, head);
             tma_load_3d(sbase + WK_OFF, &p.tmWk, bar(B_WFULL), 0, 0, head);
-            int issued = 0;
+            // Q, K of chunk c into the single Q/K buffer once Z of chunk c-1 has
+            // read it; V of chunk c into buffer c & 1 once chunk c-2's products have.
+            int qk_issued = 0, v_issued = 0;
+            bool ok = true;
             for (int c = 0; c < n_chunks; ++c) {
                 const int b = c & 1;
-                if (c >= 2 && !wait_bounded(bar(B_EMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
-                                            (ROLE_HH_PRODUCER << 24) | ((B_EMPTY + b) << 16) | c)) {
-                    const uint64_t t0 = global_timer_ns();
-                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                        while (!mbar_try_wait(bar(B_FULL + (j & 1)), (j >> 1) & 1) &&
-                               global_timer_ns() - t0 < kDrainLimitNs) {
-                        }
-                    while (!mbar_try_wait(bar(B_WFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
-                    }
+                if (c >= 1 && !(ok = wait_bounded(bar(B_QKEMPTY), (c - 1) & 1, abort_flag,
+                                                  (ROLE_HH_PRODUCER << 24) | (B_QKEMPTY << 16) | c)))
                     break;
+                mbar_arrive_expect_tx(bar(B_QKFULL), 2 * BOX);
+                tma_load_3d(sbase + QK_OFF, &p.tmQ, bar(B_QKFULL), 0, c * C, bh);
+                tma_load_3d(sbase + QK_OFF + BOX, &p.tmK, bar(B_QKFULL), 0, c * C, bh);
+                ++qk_issued;
+                if (c >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_HH_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | c)))
+                    break;
+                mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
+                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, c * C, bh);
+                ++v_issued;
+            }
+            if (!ok) {
+                // let the loads in flight land before the CTA's shared memory goes away
+                const uint64_t t0 = global_timer_ns();
+                if (qk_issued > 0)
+                    while (!mbar_try_wait(bar(B_QKFULL), (qk_issued - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+                    while (!mbar_try_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1) &&
+                           global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                while (!mbar_try_wait(bar(B_WFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
                 }
-                const uint32_t dst = sbase + QKV_OFF + b * 3 * BOX;
-                mbar_arrive_expect_tx(bar(B_FULL + b), 3 * BOX);
-                tma_load_3d(dst, &p.tmQ, bar(B_FULL + b), 0, c * C, bh);
-                tma_load_3d(dst + BOX, &p.tmK, bar(B_FULL + b), 0, c * C, bh);
-                tma_load_3d(dst + 2 * BOX, &p.tmV, bar(B_FULL + b), 0, c * C, bh);
-                ++issued;
             }
         }
         __syncwarp();
@@ -223,38 +260,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t ID_Z = idesc_bf16_f32(C, FH, 0, 1);       // X W: X K-major, W MN-major
-            constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);        // phi(Q) phi(K)^T
+            constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);        // phi(Q) phi(K)^T: A in TMEM
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);   // P [V | 1]: A in TMEM
-            constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);   // phi(Q) S: both K-major
+            constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);   // phi(Q) S: A in TMEM, B K-major
             constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);    // [V | 1]^T phi(K): both MN-major
-            // Per chunk c: P [V|1], then Q Wq and K Wk of chunk c+1 (so that
-            // its feature maps are formed while this chunk's products run),
-            // phi(Q) S_{<c}, the state update, and phi(Q) phi(K)^T of c+1.
-            auto issue_z = [&](int c) {  // Z of chunk c: Q Wq, K Wk, 16 of the 64 dims per step
-                const uint32_t qb = sbase + QKV_OFF + (c & 1) * 3 * BOX, kb = qb + BOX;
+            // Per chunk c, once both groups hold its S in registers: Q Wq and
+            // K Wk of chunk c+1 (its feature maps are then formed while this
+            // chunk's products run); once P is in TMEM: P [V|1], phi(Q) S_{<c},
+            // the state update; once c+1's features are in place, phi(Q)
+            // phi(K)^T of c+1.
+            auto issue_z = [&]() {  // Z = Q Wq, K Wk from the Q/K buffer, 16 of the 64 dims per step
 #pragma unroll
                 for (int k = 0; k < DQK / 16; ++k) {
-                    umma_ss(tmem + T_Z, smem_desc_sw128(qb + k * 32, 16, 1024),
+                    umma_ss(tmem + T_Z, smem_desc_sw128(sbase + QK_OFF + k * 32, 16, 1024),
                             smem_desc_sw128(sbase + WQ_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
-                    umma_ss(tmem + T_Z + FH, smem_desc_sw128(kb + k * 32, 16, 1024),
+                    umma_ss(tmem + T_Z + FH, smem_desc_sw128(sbase + QK_OFF + BOX + k * 32, 16, 1024),
                             smem_desc_sw128(sbase + WK_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
                 }
                 umma_commit(bar(B_ZFULL));
+                umma_commit(bar(B_QKEMPTY));
             };
-            auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features (2 boxes)
+            auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features
 #pragma unroll
-                for (int k = 0; k < F / 16; ++k) {
-                    const uint32_t off = (k / 4) * BOX + (k % 4) * 32;
-                    umma_ss(tmem + T_Z, smem_desc_sw128(sbase + PHIQ_OFF + off, 16, 1024),
-                            smem_desc_sw128(sbase + PHIK_OFF + off, 16, 1024), ID_S, k > 0);
-                }
+                for (int k = 0; k < F / 16; ++k)
+                    umma_ts(tmem + T_Z, tmem + T_PHIQ + k * 8,
+                            smem_desc_sw128(sbase + PHIK_OFF + (k / 4) * BOX + (k % 4) * 32, 16, 1024), ID_S, k > 0);
                 umma_commit(bar(B_SFULL));
             };
             bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16)) &&
-                      wait_bounded(bar(B_FULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_FULL << 16));
+                      wait_bounded(bar(B_QKFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_QKFULL << 16));
             if (ok) {
                 tc_fence_after_sync();
-                issue_z(0);
+                issue_z();
                 if ((ok = wait_bounded(bar(B_PHIREADY), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_PHIREADY << 16)))) {
                     tc_fence_after_sync();
                     issue_s();
@@ -263,8 +300,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             for (int c = 0; ok && c < n_chunks; ++c) {
                 const int b = c & 1;
                 const uint32_t ph = c & 1;
-                const uint32_t vb = sbase + QKV_OFF + b * 3 * BOX + 2 * BOX;
+                const uint32_t vb = sbase + V_OFF + b * BOX;
+                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_SREAD << 16) | c)))
+                    break;
+                // Z of the next chunk over this chunk's S, which both groups have read out
+                if (c + 1 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(B_QKFULL), (c + 1) & 1, abort_flag,
+                                            (ROLE_HH_MMA << 24) | (B_QKFULL << 16) | (c + 1))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_z();
+                }
                 if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_HH_MMA << 24) | (B_PREADY << 16) | c)))
+                    break;
+                if (!(ok = wait_bounded(bar(B_VFULL + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_HH_MMA << 24) | ((B_VFULL + b) << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]
@@ -272,19 +322,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 for (int k = 0; k < C / 16; ++k)
                     umma_ts(tmem + T_O, tmem + T_P + k * 8,
                             smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
-                // Z of the next chunk (its S was read out before this chunk's PREADY)
-                if (c + 1 < n_chunks) {
-                    if (!(ok = wait_bounded(bar(B_FULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
-                                            (ROLE_HH_MMA << 24) | ((B_FULL + (b ^ 1)) << 16) | (c + 1))))
-                        break;
-                    tc_fence_after_sync();
-                    issue_z(c + 1);
-                }
                 // inter: [num | den] += phi(Q) S_{<c}
                 if (c > 0) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
-                        umma_ss(tmem + T_O, smem_desc_sw128(sbase + PHIQ_OFF + (k / 4) * BOX + (k % 4) * 32, 16, 1024),
+                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8,
                                 smem_desc_sw128(sbase + SPREV_OFF + (k / 4) * SBOX + (k % 4) * 32, 16, 1024),
                                 ID_INTER, 1);
                 }
@@ -296,7 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                             smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE,
                             (c > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
-                umma_commit(bar(B_EMPTY + b));
+                umma_commit(bar(B_VEMPTY + b));
                 // S of the next chunk, once its features and this chunk's state are in smem
                 if (c + 1 < n_chunks) {
                     if (!(ok = wait_bounded(bar(B_PHIREADY), ph ^ 1, abort_flag,
@@ -317,22 +359,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         // Two warpgroups over the same 128 rows (warp w reads TMEM lanes
         // 32 (w % 4) ..): group 0 forms phi(Q), the first half of P and of
         // the state copy, O columns 0..31 and DEN; group 1 forms phi(K) and
-        // the second halves.  Per chunk c: P; chunk c+1's feature maps into
+        // the second halves.  Per chunk c: S into registers (the tensor core
+        // may then form Z of c+1) and P; chunk c+1's feature maps into
         // registers while chunk c's products run; once they are done, the
-        // state copy and the feature maps into smem (they feed c+1's
-        // products); then O of chunk c.
+        // state copy and the feature maps into TMEM / smem (they feed c+1's
+        // products); then O of chunk c through this warp's staging box and a
+        // TMA store.
         const int i = threadIdx.x % 128;  // row of the chunk = TMEM lane; also row i of S^T
         const int grp = warp / 4;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const size_t head_row0 = static_cast<size_t>(bh) * p.N;
-        const uint32_t phi_tile = sbase + (grp == 0 ? PHIQ_OFF : PHIK_OFF);
         const uint32_t zcol = lane_base + T_Z + grp * FH;
+        // phi(Q) (group 0) into TMEM, phi(K) (group 1) into its smem tile
+        auto put_phi = [&](const uint32_t (&pk)[64]) {
+            if (grp == 0) {
+                tmem_st32(lane_base + T_PHIQ, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                tmem_st32(lane_base + T_PHIQ + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                tmem_st_wait();
+            } else {
+                phi_store(pk, sbase + PHIK_OFF, i);
+            }
+        };
+        const uint32_t obox = sbase + OST_OFF + warp * OBOX;
         bool ok = wait_bounded(bar(B_ZFULL), 0, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16));
         if (ok) {
             tc_fence_after_sync();
             uint32_t pk[64];
             phi_regs(zcol, grp == 0 || i < p.N, pk);  // phi(Q) always live; phi(K) zero past N
-            phi_store(pk, phi_tile, i);
+            put_phi(pk);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             warp_arrive(bar(B_PHIREADY), lane);
@@ -348,6 +402,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 const int jmax = min(i, p.N - 1 - c * C);
                 uint32_t sr[64];
                 tmem_ld64(lane_base + T_Z + grp * 64, sr);
+                tc_fence_before_sync();
+                warp_arrive(bar(B_SREAD), lane);
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -361,18 +417,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             tc_fence_before_sync();
             warp_arrive(bar(B_PREADY), lane);
             if (c + 1 < n_chunks) {
-                // --- chunk c+1's feature maps into registers (Z of c+1 follows P [V|1] of c)
+                // --- chunk c+1's feature maps into registers (its Z follows this chunk's SREAD)
                 if (!(ok = wait_bounded(bar(B_ZFULL), ph ^ 1, abort_flag,
                                         (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16) | (c + 1))))
                     break;
                 tc_fence_after_sync();
                 uint32_t pk[64];
                 phi_regs(zcol, grp == 0 || row + C < p.N, pk);
-                // --- chunk c's products done: the state copy, then the feature maps into smem
+                // --- chunk c's products done: the feature maps into TMEM / smem, then the state copy
                 if (!(ok = wait_bounded(bar(B_STDONE), ph, abort_flag,
                                         (ROLE_HH_COMPUTE << 24) | (B_STDONE << 16) | c)))
                     break;
                 tc_fence_after_sync();
+                put_phi(pk);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     uint32_t sv[32];
@@ -388,7 +445,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
                     }
                 }
-                phi_store(pk, phi_tile, i);
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(bar(B_PHIREADY), lane);
@@ -404,21 +460,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 tmem_ld32(lane_base + T_O + grp * 32, o);
                 tmem_ld16(lane_base + T_O + 64, d);
                 const float den = __uint_as_float(d[0]);
-                if (row < p.N) {
-                    const float inv = 1.0f / den;
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.O) + (head_row0 + row) * DV +
-                                                           grp * 32);
+                const float inv = 1.0f / den;
+                const float2 inv2 = make_float2(inv, inv);
+                // this warp's previous store has read its staging box
+                if (lane == 0) tma_store_wait_read_all();
+                __syncwarp();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(
-                            pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
-                    if (grp == 0) p.DEN[head_row0 + row] = den;
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 v = __fmul2_rn(
+                            make_float2(__uint_as_float(o[8 * q + 2 * t]), __uint_as_float(o[8 * q + 2 * t + 1])), inv2);
+                        w[t] = pack_bf16x2(v.x, v.y);
+                    }
+                    // 64-byte swizzle: 16-byte chunk q of row `lane` at chunk q ^ ((lane >> 1) & 3)
+                    st_shared_v4(obox + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                if (grp == 0 && row < p.N) p.DEN[head_row0 + row] = den;
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int row0 = c * C + (warp % 4) * 32;
+                if (lane == 0 && row0 < p.N) {
+                    tma_store_3d(&p.tmO, obox, grp * 32, row0, bh);  // rows past N are clipped
+                    tma_store_commit();
                 }
             }
         }
+        if (lane == 0) tma_store_wait_all();
     }
 
     tc_fence_before_sync();

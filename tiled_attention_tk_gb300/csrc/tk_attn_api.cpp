@@ -138,6 +138,22 @@ int encode_matrix_map(CUtensorMap *map, const void *ptr, int64_t d0, int64_t d1,
     return TK_OK;
 }
 
+// 3-D view {64, N, BH} of a contiguous [BH, N, 64] bf16 output, stored as
+// 32 x 32 boxes (one warp's half rows) with the 64-byte swizzle.
+int encode_out32_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t BH) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail_cuda(g_encode_err);
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(N) * 64 * 2};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                     elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
+    return TK_OK;
+}
+
 // Shape checks shared by the forward and backward entry points.
 int check_shape(int64_t B, int64_t H, int64_t N, int64_t D) {
     if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
@@ -468,6 +484,7 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
     if ((rc = encode_qkv_map(&p.tmQ, Q, N, 16, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmK, K, N, 16, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmV, V, N, 64, BH)) != TK_OK) return rc;
+    if ((rc = encode_out32_map(&p.tmO, O, N, BH)) != TK_OK) return rc;
     p.O = O;
     p.DEN = DEN;
     p.N = static_cast<int>(N);
@@ -528,6 +545,7 @@ int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq,
     if ((rc = encode_qkv_map(&p.tmV, V, N, 64, BH)) != TK_OK) return rc;
     if ((rc = encode_batched_map(&p.tmWq, Wq, 64, 64, H, 64, 64)) != TK_OK) return rc;
     if ((rc = encode_batched_map(&p.tmWk, Wk, 64, 64, H, 64, 64)) != TK_OK) return rc;
+    if ((rc = encode_out32_map(&p.tmO, O, N, BH)) != TK_OK) return rc;
     p.O = O;
     p.DEN = DEN;
     p.N = static_cast<int>(N);

@@ -81,6 +81,7 @@ struct BasedParams {
     CUtensorMap tmQ;   // 3-D {16, N, B*H} bf16, box {64, 128, 1} (columns 16..63 read as 0), 128-byte swizzle
     CUtensorMap tmK;
     CUtensorMap tmV;   // 3-D {64, N, B*H} bf16, box {64, 128, 1}
+    CUtensorMap tmO;   // 3-D {64, N, B*H} bf16, box {32, 32, 1}, 64-byte swizzle (stores)
     void *O;           // bf16 [B*H, N, 64]
     float *DEN;        // fp32 [B*H, N]
     int N;
@@ -98,6 +99,7 @@ struct HedgehogParams {
     CUtensorMap tmV;
     CUtensorMap tmWq;  // 3-D {f, d, H} bf16 (W of head h: [d][f]), box {64, 64, 1}
     CUtensorMap tmWk;
+    CUtensorMap tmO;   // 3-D {64, N, B*H} bf16, box {32, 32, 1}, 64-byte swizzle (stores)
     void *O;           // bf16 [B*H, N, 64]
     float *DEN;        // fp32 [B*H, N]
     int N;
