@@ -22,7 +22,7 @@ with nvidia-smi during the timed region) and ``gpu_launches``.
 10*B*H*N^2*D, halved under the causal mask), with the fp64 backward oracle as
 the CPU baseline.
 
-``--based``: causal Based linear attention (tk_based_fwd, B8 H16 N4096, feature
+``--based``: causal Based linear attention (tk_based_fwd, B16 H16 N4096, feature
 dim 16, value dim 64), reported as GB/s of algorithmic HBM traffic against the
 measured HBM bandwidth (the linear form's arithmetic intensity is below the
 ridge).
@@ -800,13 +800,15 @@ def hedgehog_inputs(B, H, N):
 
 
 def run_based(args, kind: str = "based"):
-    """One step = tk_based_fwd (or tk_hedgehog_fwd) over B8 H16 N4096 unless
+    """One step = tk_based_fwd over B16 H16 N4096 (tk_hedgehog_fwd over B8 H16
+    N4096; both read 192 MiB of inputs, more than L2) unless
     --based-shape B,H,N.  Value: algorithmic bytes (Q, K, V read once, O and
     DEN written once) per second; the chunked linear form's flops are reported
     beside it."""
     import torch
     import tiled_attention_tk_gb300 as tk
-    B, H, N = (int(x) for x in args.based_shape.split(","))
+    shape = args.based_shape or ("8,16,4096" if kind == "hedgehog" else "16,16,4096")
+    B, H, N = (int(x) for x in shape.split(","))
     _, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -982,7 +984,8 @@ def main(argv=None):
     ap.add_argument("--gemm-shape", type=str, default="8192,8192,8192", help="M,N,K for --gemm")
     ap.add_argument("--based", action="store_true", help="time the Based linear attention instead")
     ap.add_argument("--hedgehog", action="store_true", help="time the Hedgehog linear attention instead")
-    ap.add_argument("--based-shape", type=str, default="8,16,4096", help="B,H,N for --based / --hedgehog")
+    ap.add_argument("--based-shape", type=str, default=None,
+                    help="B,H,N for --based (default 16,16,4096) / --hedgehog (default 8,16,4096)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

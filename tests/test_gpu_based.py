@@ -69,12 +69,12 @@ def test_based_deterministic():
 
 
 def test_based_bench_workload_sampled(oracle_mod):
-    """The benchmark's B8 H16 N4096 launch, sampled heads and rows (the last
-    rows of a head carry the longest state)."""
-    B, H, N = 8, 16, 4096
+    """The benchmark's B16 H16 N4096 launch (two waves of heads over the SMs),
+    sampled heads and rows (the last rows of a head carry the longest state)."""
+    B, H, N = 16, 16, 4096
     q, k, v = _qkv(B, H, N, 402)
     o, den = _run(q, k, v, 0.25)
     rows = [0, 1, 127, 128, 129, 2047, 2048, 4000, 4094, 4095]
-    for b, h in [(0, 0), (3, 7), (7, 15)]:
+    for b, h in [(0, 0), (3, 7), (9, 10), (15, 15)]:
         O_ref, D_ref = oracle_mod.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
-        _assert_close(o[b, h, rows], den[b, h, rows], O_ref, D_ref, f"B8H16N4096 head ({b},{h})")
+        _assert_close(o[b, h, rows], den[b, h, rows], O_ref, D_ref, f"B16H16N4096 head ({b},{h})")
