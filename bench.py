@@ -59,6 +59,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 (fraction of dense BF16 peak) vs CPU oracle"
 FALLBACK_BF16_TFLOPS = 1900.0  # one earlier GB300 measurement, used only without MEASURED_PEAKS.json
+FALLBACK_BF16_SUSTAINED_TFLOPS = 1700.0  # the same measurement held for seconds under the power limit
 L2_BYTES = 126 * 1024 * 1024
 KERNEL_SOURCES = ["tiled_attention_tk_gb300/csrc/attn_fwd.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
                   "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
@@ -99,21 +100,24 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def peaks():
-    """(bf16 burst TF/s, label) from MEASURED_PEAKS.json, else the fallback."""
+def peaks(sustained: bool = False):
+    """(bf16 TF/s, label) from MEASURED_PEAKS.json (the burst figure, or the
+    sustained one for a kernel that runs under the power limit through a
+    seconds-long timed region), else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             with open(path) as f:
                 d = json.load(f)
-            v = d.get("bf16_tflops")
+            v = d.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
             if isinstance(v, dict):
                 v = v.get("value")
             if v:
-                return float(v), "of measured"
+                return float(v), "of measured sustained" if sustained else "of measured"
         except (OSError, ValueError, TypeError):
             pass
-    return FALLBACK_BF16_TFLOPS, "of fallback"
+    return (FALLBACK_BF16_SUSTAINED_TFLOPS, "of fallback sustained") if sustained else \
+        (FALLBACK_BF16_TFLOPS, "of fallback")
 
 
 def traffic_for(workload_name: str):
@@ -684,7 +688,12 @@ def run_gemm(args):
                "ms_per_step": round(e2e_s * 1e3, 3), "steps": steps}
     if rank != 0:
         return None
-    peak, peak_label = peaks()
+    # A GEMM of this size runs the GPU into its power limit (sw_power_cap, SM
+    # clock well below maximum) over a timed region of about a second and a
+    # half: the sustained measured peak is its denominator; the burst one is
+    # reported beside it.
+    peak, peak_label = peaks(sustained=True)
+    burst, _ = peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     name = f"gemm-M{M}N{N}K{K}"
     line = {
@@ -698,6 +707,7 @@ def run_gemm(args):
                    "l2": l2_desc},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_label,
+                     "peak_burst": burst, "frac_of_burst": round(achieved / burst, 4),
                      "traffic": gemm_traffic_for(name), "kernel": "gemm_kernel<true>",
                      "kernel_ms": round(kernel_ms, 5)},
         "cublas_context_tflops": round(cublas, 2),
