@@ -256,6 +256,37 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
                  int64_t N, int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream);
 
 /*
+ * tk_based_workspace_bytes -- the workspace tk_based_fwd_ws needs on the
+ * current device for [B, H, N]: 0 when the B*H heads fill the SMs (one CTA
+ * walks each head, as in tk_based_fwd), else B*H * n_seg * 51,200 bytes
+ * (rounded up to 256) for the partial states of n_seg segments per head.
+ * 0 also for an invalid shape (tk_based_fwd_ws then reports it).
+ */
+size_t tk_based_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/*
+ * tk_based_fwd_ws -- tk_based_fwd with the sequence split into segments
+ * when the heads are fewer than the SMs: a first pass forms each segment's
+ * partial state sum_j [V_j | 1] phi(K_j)^T (fp32, into `workspace`), then
+ * one CTA per segment starts from the sum of the partial states before it.
+ * Same result as tk_based_fwd up to the order of fp32 additions.
+ *
+ * Arguments as tk_based_fwd, plus
+ *   workspace        device memory of at least tk_based_workspace_bytes(B,H,N)
+ *                    bytes, 256-byte aligned, not overlapping any other
+ *                    argument; may be NULL when that size is 0 (then this is
+ *                    tk_based_fwd).  Owned by the caller, overwritten.
+ *   workspace_bytes  its size.
+ * Semantics: asynchronous on `stream` (two kernels when segmented).
+ * Deterministic.  Errors as tk_based_fwd, plus TK_ERR_WORKSPACE (too small
+ * or misaligned), TK_ERR_NULL_PTR (NULL where one is needed) and
+ * TK_ERR_ALIAS (the workspace overlapping an argument).
+ */
+int tk_based_fwd_ws(const void *Q, const void *K, const void *V, void *O, float *DEN, void *workspace,
+                    size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t Dv, float scale,
+                    cudaStream_t stream);
+
+/*
  * tk_hedgehog_fwd -- causal Hedgehog linear attention (the pages list
  * "LoLCATS Hedgehog Linear Attention", thebeat.tech "ThunderKittens 2.0", New
  * Kernels; the formula is the Hedgehog feature map):

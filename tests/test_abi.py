@@ -218,6 +218,31 @@ def test_based_host_validation(kwargs, code):
     assert _based(**kwargs) == tk.STATUS[code]
 
 
+def _based_ws(q=Bq, k=Bk, v=Bv, o=Bo, d=Bl, ws=Bws, ws_bytes=1 << 20, B=1, H=1, N=128, Dqk=16, Dv=64, scale=0.25):
+    return tk.load().tk_based_fwd_ws(q, k, v, o, d, ws, ws_bytes, B, H, N, Dqk, Dv, scale, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(k=None), "TK_ERR_NULL_PTR"),
+    (dict(B=0), "TK_ERR_BAD_SHAPE"),
+    (dict(Dqk=64), "TK_ERR_UNSUPPORTED_D"),
+    (dict(scale=float("nan")), "TK_ERR_BAD_SCALE"),
+    (dict(q=Bq + 2), "TK_ERR_MISALIGNED"),
+    (dict(d=Bv + 256), "TK_ERR_ALIAS"),
+])
+def test_based_ws_host_validation(kwargs, code):
+    """The segmented entry point checks its arguments like tk_based_fwd, before
+    it looks at the device (the workspace checks need the device's SM count
+    and are covered on the GPU)."""
+    assert _based_ws(**kwargs) == tk.STATUS[code]
+
+
+def test_based_workspace_bytes_without_device():
+    lib = tk.load()
+    assert lib.tk_based_workspace_bytes(0, 1, 128) == 0
+    assert lib.tk_based_workspace_bytes(1, 1, 0) == 0
+
+
 # ---------------------------------------------------------------- Hedgehog ABI
 
 def _hh(q=Bq, k=Bk, v=Bv, wq=Bdo, wk=BdQ, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=64, F=64, Dv=64):

@@ -27,8 +27,8 @@ def _qkv(B, H, N, seed):
     return q, k, v
 
 
-def _run(q, k, v, scale):
-    o, den = tk.based(q.cuda(), k.cuda(), v.cuda(), scale=scale)
+def _run(q, k, v, scale, segments=True):
+    o, den = tk.based(q.cuda(), k.cuda(), v.cuda(), scale=scale, segments=segments)
     torch.cuda.synchronize()
     status, detail = tk.device_status()
     assert status == 0, f"device status {status} detail {detail:#x}"
@@ -78,3 +78,68 @@ def test_based_bench_workload_sampled(oracle_mod):
     for b, h in [(0, 0), (3, 7), (9, 10), (15, 15)]:
         O_ref, D_ref = oracle_mod.based(q[b, h], k[b, h], v[b, h], 0.25, rows=rows)
         _assert_close(o[b, h, rows], den[b, h, rows], O_ref, D_ref, f"B16H16N4096 head ({b},{h})")
+
+
+# ---------------------------------------------------------------- segmented sequences
+# With fewer heads than SMs (tk_based_fwd_ws, the binding's default), each
+# head is split into segments: a first pass forms every segment's partial
+# state in fp32, then one CTA per segment starts from the sum of those
+# before it.  The result is the same linear form; only the order of fp32
+# additions in the state differs.
+
+def test_based_segments_long_sequence(oracle_mod):
+    """B1 H2 N20000 (157 chunks, several dozen segments): sampled rows on
+    both sides of many chunk and segment boundaries and at the ragged end."""
+    B, H, N = 1, 2, 20000
+    assert tk.based_workspace_bytes(B, H, N) > 0
+    q, k, v = _qkv(B, H, N, 410)
+    o, den = _run(q, k, v, 0.25)
+    rows = sorted({0, 1, 127, 128, 639, 640, 641, 1279, 1280, 5119, 5120, 9999, 12799, 12800, 19199, 19200,
+                   19967, 19968, 19999} | {int(x) for x in np.random.default_rng(7).integers(0, N, 12)})
+    for h in range(H):
+        O_ref, D_ref = oracle_mod.based(q[0, h], k[0, h], v[0, h], 0.25, rows=rows)
+        _assert_close(o[0, h, rows], den[0, h, rows], O_ref, D_ref, f"segmented N={N} head {h}")
+
+
+@pytest.mark.parametrize("N", [1000, 2049, 9000])
+def test_based_segments_match_one_cta_per_head(oracle_mod, N):
+    """Segmented and whole-head runs agree (fp32 order only), and both meet the
+    oracle bar on the full output of a short case."""
+    q, k, v = _qkv(1, 3, N, 420 + N)
+    o1, d1 = _run(q, k, v, 0.25, segments=True)
+    o2, d2 = _run(q, k, v, 0.25, segments=False)
+    assert np.abs(o1 - o2).max() <= 1e-2 and (np.abs(d1 - d2) / np.abs(d2)).max() <= 2e-3
+    if N <= 2049:
+        O_ref, D_ref = oracle_mod.based(q, k, v, 0.25)
+        _assert_close(o1, d1, O_ref, D_ref, f"segmented N={N}")
+
+
+def test_based_segments_deterministic():
+    q, k, v = _qkv(1, 2, 12000, 430)
+    o1, d1 = _run(q, k, v, 0.25)
+    o2, d2 = _run(q, k, v, 0.25)
+    assert np.array_equal(o1, o2) and np.array_equal(d1, d2)
+
+
+def test_based_workspace_checks():
+    """tk_based_fwd_ws rejects a workspace that is missing, too small,
+    misaligned or overlapping an argument, before anything is enqueued."""
+    B, H, N = 1, 2, 20000
+    need = tk.based_workspace_bytes(B, H, N)
+    assert need > 0 and need % 256 == 0
+    q, k, v = (t.cuda() for t in _qkv(B, H, N, 440))
+    o = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device="cuda")
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    lib = tk.load()
+
+    def call(ws_ptr, ws_bytes, o_ptr=None):
+        return lib.tk_based_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_ptr or o.data_ptr(), den.data_ptr(),
+                                   ws_ptr, ws_bytes, B, H, N, 16, 64, 0.25, None)
+    assert call(None, 0) == tk.STATUS["TK_ERR_NULL_PTR"]
+    assert call(ws.data_ptr(), need - 256) == tk.STATUS["TK_ERR_WORKSPACE"]
+    assert call(ws.data_ptr() + 16, need) == tk.STATUS["TK_ERR_WORKSPACE"]
+    assert call(o.data_ptr(), need) == tk.STATUS["TK_ERR_ALIAS"]
+    assert call(ws.data_ptr(), need) == 0
+    torch.cuda.synchronize()
+    assert tk.device_status()[0] == 0

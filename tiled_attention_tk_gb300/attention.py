@@ -192,12 +192,22 @@ def gemm(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool = True, stream_k: bool
     return out
 
 
+def based_workspace_bytes(B: int, H: int, N: int) -> int:
+    """Workspace tk_based_fwd_ws needs on the current device (0: no segments)."""
+    return int(_lib.load().tk_based_workspace_bytes(B, H, N))
+
+
 def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
-          out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None):
+          out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None,
+          workspace: torch.Tensor | None = None, segments: bool = True):
     """Causal Based linear attention.  q, k: bf16 [B,H,N,16]; v: bf16
     [B,H,N,64] (CUDA).  Returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]) with
     w_ij = 1 + s + s^2/2, s = scale <q_i,k_j>, O_i = sum_{j<=i} w_ij v_j / DEN_i.
-    ``scale`` defaults to 1/sqrt(16).  Enqueued without synchronising."""
+    ``scale`` defaults to 1/sqrt(16).  With ``segments`` (the default) and
+    fewer heads than SMs, each head's sequence is split into segments
+    (tk_based_fwd_ws; ``workspace`` is allocated here unless given);
+    ``segments=False`` is tk_based_fwd (one CTA per head).  Enqueued without
+    synchronising."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
             raise ValueError(f"{n} must be a CUDA bf16 [B,H,N,D] tensor")
@@ -213,9 +223,19 @@ def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None
     if den is None:
         den = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        rc = _lib.load().tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), den.data_ptr(),
-                                      B, H, N, Dqk, Dv, float(scale), _stream_handle(stream))
-    _lib.check(rc, "tk_based_fwd")
+        if not segments:
+            rc = _lib.load().tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), den.data_ptr(),
+                                          B, H, N, Dqk, Dv, float(scale), _stream_handle(stream))
+            _lib.check(rc, "tk_based_fwd")
+            return out, den
+        need = based_workspace_bytes(B, H, N) if Dqk == 16 and Dv == 64 else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = _lib.load().tk_based_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), den.data_ptr(),
+                                         ws_ptr, ws_bytes, B, H, N, Dqk, Dv, float(scale), _stream_handle(stream))
+    _lib.check(rc, "tk_based_fwd_ws")
     return out, den
 
 

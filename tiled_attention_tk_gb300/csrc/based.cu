@@ -217,8 +217,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int bh = blockIdx.x;
-    const int n_chunks = (p.N + C - 1) / C;
+    // A CTA walks one segment of a head: its chunks c0 .. c0 + n_chunks - 1
+    // (the whole head unless the sequence is split into segments; then the
+    // state of the chunks before c0 comes from the segment-state pass in
+    // p.ws).  Chunk indices below are local to the segment.
+    const int seg = blockIdx.x % p.n_seg;
+    const int bh = blockIdx.x / p.n_seg;
+    const int c0 = seg * p.seg_chunks;
+    const int n_chunks = min(p.seg_chunks, (p.N + C - 1) / C - c0);
+    const bool has_prev = seg > 0;
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -275,14 +282,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 // but still counts the full box.
                 const uint32_t dst = sbase + QK_OFF + b * 2 * BOX;
                 mbar_arrive_expect_tx(bar(B_QKFULL + b), 2 * BOX);
-                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, c * C, bh);
-                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, c * C, bh);
+                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, (c0 + c) * C, bh);
+                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, (c0 + c) * C, bh);
                 ++qk_issued;
                 if (c >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
                                                   (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | c)))
                     break;
                 mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
-                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, c * C, bh);
+                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (c0 + c) * C, bh);
                 ++v_issued;
             }
             if (!ok) {
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                                         (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
-                if (c > 0) {
+                if (c > 0 || has_prev) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
                         umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8,
@@ -362,7 +369,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
                     umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
-                            smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE, (c > 0 || k > 0) ? 1u : 0u);
+                            smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE,
+                            (c > 0 || has_prev || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_VEMPTY + b));
             }
@@ -387,19 +395,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
         const size_t head_row0 = static_cast<size_t>(bh) * p.N;
         const uint32_t obox = sbase + OST_OFF + warp * OBOX;
+        if (has_prev) {
+            // --- the state of the segments before this one: the sum of their
+            // fp32 partial states, into the group's columns of S^T (rows >= 65 are 0)
+            const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;
+            for (int blk = 0; blk < ncol; blk += 16) {
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+                if (i < NV) {
+                    for (int sp = 0; sp < seg; ++sp) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.ws + ((static_cast<size_t>(bh) * p.n_seg + sp) * NV + i) * F + col0 + blk);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 v = src[q];
+                            acc[4 * q] += v.x;
+                            acc[4 * q + 1] += v.y;
+                            acc[4 * q + 2] += v.z;
+                            acc[4 * q + 3] += v.w;
+                        }
+                    }
+                }
+                uint32_t u[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(acc[e]);
+                tmem_st16(lane_base + T_ST + col0 + blk, u);
+            }
+            tmem_st_wait();
+        }
         bool ok = true;
         for (int c = 0; c < n_chunks; ++c) {
             const int b = c & 1;
             const uint32_t ph = c & 1;
             const uint32_t qb = sbase + QK_OFF + b * 2 * BOX, kb = qb + BOX;
-            const int row = c * C + i;  // sequence position of this thread's query and key
+            const int row = (c0 + c) * C + i;  // sequence position of this thread's query and key
             if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | c)))
                 break;
             tc_fence_after_sync();
             // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this group's 64 keys
             uint32_t pk[32];
             {
-                const int jmax = min(i, p.N - 1 - c * C);  // last key of the chunk this row sees
+                const int jmax = min(i, p.N - 1 - (c0 + c) * C);  // last key of the chunk this row sees
                 uint32_t sr[64];
                 tmem_ld64(lane_base + T_S + grp * 64, sr);
                 tc_fence_before_sync();
@@ -423,16 +460,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             }
             tmem_st32(lane_base + T_P + grp * 32, pk);
             if (c > 0)  // --- O of chunk c-1, this group's 32 columns
-                write_o(lane_base, grp, lane, obox, &p.tmO, (c - 1) * C + (warp % 4) * 32, bh, p.N,
+                write_o(lane_base, grp, lane, obox, &p.tmO, (c0 + c - 1) * C + (warp % 4) * 32, bh, p.N,
                         grp == 0 ? p.DEN + head_row0 + row - C : nullptr);
             tmem_st_wait();
             tc_fence_before_sync();
             warp_arrive(bar(B_PREADY), lane);
-            if (c > 0) {
+            if (c > 0 || has_prev) {
                 // --- bf16 copy of the state S_{<c} (rows 0..79 of S^T): 32-feature blocks
-                // {0, 1} (group 0) and {2, 3, 4} (group 1) of the 160
-                if (!(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
-                                        (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
+                // {0, 1} (group 0) and {2, 3, 4} (group 1) of the 160 (at a
+                // segment's first chunk: the state the group itself stored above)
+                if (c > 0 && !(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
+                                                 (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
                     break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -479,8 +517,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             wait_bounded(bar(B_ODONE), (n_chunks - 1) & 1, abort_flag,
                          (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | n_chunks)) {
             tc_fence_after_sync();
-            const int row = (n_chunks - 1) * C + i;
-            write_o(lane_base, grp, lane, obox, &p.tmO, (n_chunks - 1) * C + (warp % 4) * 32, bh, p.N,
+            const int row = (c0 + n_chunks - 1) * C + i;
+            write_o(lane_base, grp, lane, obox, &p.tmO, (c0 + n_chunks - 1) * C + (warp % 4) * 32, bh, p.N,
                     grp == 0 ? p.DEN + head_row0 + row : nullptr);
         }
         if (lane == 0) tma_store_wait_all();
@@ -491,6 +529,180 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     if (warp == WARP_MMA) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+
+// ------------------------------------------------------------------ segment states
+//
+// For a head split into segments, the state each segment starts from is the
+// sum of the partial states of the segments before it.  This pass forms, per
+// (head, segment) except the last, the segment's partial state
+//   dS^T = sum over its rows of [v_j | 1] phi(k_j)^T      (fp32, 65 live rows x 160)
+// with the same feature map and product as the main kernel's state update,
+// and stores it to ws[bh][seg] (rows 65..79 are zero).
+namespace st {
+constexpr uint32_t K_OFF = 0;                         // K box of chunk c at + (c & 1) * BOX
+constexpr uint32_t V_OFF = K_OFF + 2 * BOX;           // V box likewise
+constexpr uint32_t ONES_OFF = V_OFF + 2 * BOX;
+constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K) of chunk c at + (c & 1) * 3 * BOX
+constexpr uint32_t BAR_OFF = PHIK_OFF + 6 * BOX;
+constexpr int B_FULL = 0;          // + buffer (2): K, V loaded
+constexpr int B_FREE = 2;          // + buffer (2): the state product of the chunk in it is done
+constexpr int B_PHIKREADY = 4;     // + buffer (2): phi(K) in smem (8 warps)
+constexpr int B_STDONE = 6;
+constexpr int B_MMADONE = 7;
+constexpr int NUM_BARS = 8;
+constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+constexpr uint32_t TMEM_COLS = 256;
+static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+}  // namespace st
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) based_state_kernel(const __grid_constant__ BasedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + st::BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + st::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int seg = blockIdx.x % (p.n_seg - 1);   // every segment but the last
+    const int bh = blockIdx.x / (p.n_seg - 1);
+    const int c0 = seg * p.seg_chunks;
+    const int n_chunks = p.seg_chunks;
+
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_addr(tmem_slot), st::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(st::B_FULL + b), 1);
+            mbar_init(bar(st::B_FREE + b), 1);
+            mbar_init(bar(st::B_PHIKREADY + b), 8);
+        }
+        mbar_init(bar(st::B_STDONE), 1);
+        mbar_init(bar(st::B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const uint32_t one = 0x3F80u;  // bf16 1.0 in the low half (column 0)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(sw128(sbase + st::ONES_OFF, r, c), c == 0 ? one : 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            int issued = 0;
+            bool ok = true;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int b = c & 1;
+                if (c >= 2 && !(ok = wait_bounded(bar(st::B_FREE + b), ((c >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_BASED_PRODUCER << 24) | ((st::B_FREE + b) << 16) | c)))
+                    break;
+                mbar_arrive_expect_tx(bar(st::B_FULL + b), 2 * BOX);
+                tma_load_3d(sbase + st::K_OFF + b * BOX, &p.tmK, bar(st::B_FULL + b), 0, (c0 + c) * C, bh);
+                tma_load_3d(sbase + st::V_OFF + b * BOX, &p.tmV, bar(st::B_FULL + b), 0, (c0 + c) * C, bh);
+                ++issued;
+            }
+            if (!ok) {
+                const uint64_t t0 = global_timer_ns();
+                for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                    while (!mbar_try_wait(bar(st::B_FULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);  // [V | 1]^T phi(K): both MN-major
+            bool ok = true;
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int b = c & 1;
+                const uint32_t vb = sbase + st::V_OFF + b * BOX;
+                if (!(ok = wait_bounded(bar(st::B_FULL + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | ((st::B_FULL + b) << 16) | c)))
+                    break;
+                if (!(ok = wait_bounded(bar(st::B_PHIKREADY + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | ((st::B_PHIKREADY + b) << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ss(tmem, smem_desc_sw128(vb + k * 2048, st::ONES_OFF - (vb - sbase), 1024),
+                            smem_desc_sw128(sbase + st::PHIK_OFF + b * 3 * BOX + k * 2048, BOX, 1024), ID_STATE,
+                            (c > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(st::B_FREE + b));
+            }
+            if (ok) umma_commit(bar(st::B_STDONE));
+            umma_commit(bar(st::B_MMADONE));
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(st::B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+            }
+        }
+        __syncwarp();
+    } else {
+        const int i = threadIdx.x % 128;
+        const int grp = warp / 4;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+        const float scale = p.scale;
+        const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
+        bool ok = true;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int b = c & 1;
+            if (!(ok = wait_bounded(bar(st::B_FULL + b), (c >> 1) & 1, abort_flag,
+                                    (ROLE_BASED_COMPUTE << 24) | ((st::B_FULL + b) << 16) | c)))
+                break;
+            if (c >= 2 && !(ok = wait_bounded(bar(st::B_FREE + b), ((c >> 1) - 1) & 1, abort_flag,
+                                              (ROLE_BASED_COMPUTE << 24) | ((st::B_FREE + b) << 16) | c)))
+                break;
+            const uint32_t kb = sbase + st::K_OFF + b * BOX, dst = sbase + st::PHIK_OFF + b * 3 * BOX;
+            const bool live = (c0 + c) * C + i < p.N;
+            if (grp == 0)
+                phi_store<6, false>(kb, i, live, r, h, g, dst);
+            else
+                phi_store<1, false>(kb, i, live, r, h, g, dst);
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(st::B_PHIKREADY + b), lane);
+        }
+        if (ok && wait_bounded(bar(st::B_STDONE), 0, abort_flag, (ROLE_BASED_COMPUTE << 24) | (st::B_STDONE << 16))) {
+            tc_fence_after_sync();
+            // rows 0..79 of the partial state: group 0 columns 0..63, group 1 64..159
+            const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;
+            float *dst = p.ws + ((static_cast<size_t>(bh) * p.n_seg + seg) * NV + i) * F;
+            for (int blk = 0; blk < ncol; blk += 32) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + col0 + blk, v);  // every lane loads; rows >= 80 are not stored
+                if (i < NV) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + col0 + blk);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, st::TMEM_COLS);
     }
 }
 
@@ -508,11 +720,31 @@ cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
         configured_device = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.BH), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * p.n_seg), 1, 1);
     cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = based::SMEM_ALLOC;
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, based::based_kernel, p);
+}
+
+// The segment-state pass (n_seg > 1): one CTA per (head, segment) but the last.
+cudaError_t launch_based_states(const BasedParams &p, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        if ((err = cudaFuncSetAttribute(based::based_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        based::st::SMEM_ALLOC)) != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * (p.n_seg - 1)), 1, 1);
+    cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = based::st::SMEM_ALLOC;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, based::based_state_kernel, p);
 }
 
 cudaError_t read_and_clear_based_status(uint32_t *status, uint32_t *detail) {

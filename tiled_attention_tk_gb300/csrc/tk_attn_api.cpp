@@ -455,8 +455,38 @@ int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t works
 
 // ------------------------------------------------------------------ Based linear attention
 
-int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H, int64_t N,
-                 int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream) {
+namespace {
+
+// Segments per head for Based: one CTA per head leaves SMs idle when the
+// heads are fewer than the SMs; a head's chunks are then split into
+// segments (at least 4 chunks each), one CTA per segment, after a pass that
+// forms each segment's partial state.
+struct BasedPlan {
+    int n_seg;
+    int seg_chunks;
+    uint64_t workspace;
+};
+
+constexpr int kBasedMinSegChunks = 4;
+constexpr uint64_t kBasedSegStateBytes = 80ull * 160ull * 4ull;  // one segment's state, fp32
+
+BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
+    const int64_t n_chunks = (N + 127) / 128;
+    BasedPlan pl{1, static_cast<int>(n_chunks), 0};
+    if (BH >= num_sms) return pl;
+    int64_t n_seg = std::min<int64_t>(num_sms / BH, n_chunks / kBasedMinSegChunks);
+    if (n_seg < 2) return pl;
+    const int64_t seg_chunks = (n_chunks + n_seg - 1) / n_seg;
+    n_seg = (n_chunks + seg_chunks - 1) / seg_chunks;  // no empty segment
+    if (n_seg < 2) return pl;
+    pl.n_seg = static_cast<int>(n_seg);
+    pl.seg_chunks = static_cast<int>(seg_chunks);
+    pl.workspace = round_up(static_cast<uint64_t>(BH) * n_seg * kBasedSegStateBytes, kWorkspaceAlign);
+    return pl;
+}
+
+int based_checks(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H, int64_t N,
+                 int64_t Dqk, int64_t Dv, float scale) {
     if (!Q || !K || !V || !O || !DEN) return TK_ERR_NULL_PTR;
     if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
     if (Dqk != 16 || Dv != 64) return TK_ERR_UNSUPPORTED_D;
@@ -474,12 +504,12 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
         if (overlaps(O, v_bytes, ins[a], in_bytes[a]) || overlaps(DEN, den_bytes, ins[a], in_bytes[a]))
             return TK_ERR_ALIAS;
     if (overlaps(O, v_bytes, DEN, den_bytes)) return TK_ERR_ALIAS;
-    int num_sms = 0;
-    int rc = current_device(&num_sms);
-    if (rc != TK_OK) return rc;
-    const void *ptrs[5] = {Q, K, V, O, DEN};
-    for (const void *ptr : ptrs)
-        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    return TK_OK;
+}
+
+int based_launch(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t BH, int64_t N,
+                 float scale, const BasedPlan &pl, void *workspace, cudaStream_t stream) {
+    int rc;
     tk::BasedParams p;
     if ((rc = encode_qkv_map(&p.tmQ, Q, N, 16, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmK, K, N, 16, BH)) != TK_OK) return rc;
@@ -487,12 +517,64 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
     if ((rc = encode_out32_map(&p.tmO, O, N, BH)) != TK_OK) return rc;
     p.O = O;
     p.DEN = DEN;
+    p.ws = static_cast<float *>(workspace);
     p.N = static_cast<int>(N);
     p.BH = static_cast<int>(BH);
+    p.n_seg = pl.n_seg;
+    p.seg_chunks = pl.seg_chunks;
     p.scale = scale;
-    cudaError_t e = tk::launch_based(p, stream);
+    cudaError_t e = cudaSuccess;
+    if (pl.n_seg > 1) e = tk::launch_based_states(p, stream);
+    if (e == cudaSuccess) e = tk::launch_based(p, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
+}
+
+}  // namespace
+
+int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H, int64_t N,
+                 int64_t Dqk, int64_t Dv, float scale, cudaStream_t stream) {
+    int rc = based_checks(Q, K, V, O, DEN, B, H, N, Dqk, Dv, scale);
+    if (rc != TK_OK) return rc;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const void *ptrs[5] = {Q, K, V, O, DEN};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0};
+    return based_launch(Q, K, V, O, DEN, B * H, N, scale, whole, nullptr, stream);
+}
+
+size_t tk_based_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || B > INT32_MAX / H) return 0;
+    int num_sms = 0;
+    if (current_device(&num_sms) != TK_OK) return 0;
+    return static_cast<size_t>(plan_based(B * H, N, num_sms).workspace);
+}
+
+int tk_based_fwd_ws(const void *Q, const void *K, const void *V, void *O, float *DEN, void *workspace,
+                    size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t Dv, float scale,
+                    cudaStream_t stream) {
+    int rc = based_checks(Q, K, V, O, DEN, B, H, N, Dqk, Dv, scale);
+    if (rc != TK_OK) return rc;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const BasedPlan pl = plan_based(B * H, N, num_sms);
+    if (pl.workspace > 0) {
+        if (!workspace) return TK_ERR_NULL_PTR;
+        if (!aligned(workspace, kWorkspaceAlign) || workspace_bytes < pl.workspace) return TK_ERR_WORKSPACE;
+        const int64_t BH = B * H;
+        const uint64_t qk_bytes = static_cast<uint64_t>(BH) * N * 16 * 2, v_bytes = static_cast<uint64_t>(BH) * N * 64 * 2,
+                       den_bytes = static_cast<uint64_t>(BH) * N * 4;
+        const void *bufs[5] = {Q, K, V, O, DEN};
+        const uint64_t bytes[5] = {qk_bytes, qk_bytes, v_bytes, v_bytes, den_bytes};
+        for (int a = 0; a < 5; ++a)
+            if (overlaps(workspace, pl.workspace, bufs[a], bytes[a])) return TK_ERR_ALIAS;
+    }
+    const void *ptrs[6] = {Q, K, V, O, DEN, pl.workspace > 0 ? workspace : Q};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    return based_launch(Q, K, V, O, DEN, B * H, N, scale, pl, pl.workspace > 0 ? workspace : nullptr, stream);
 }
 
 // ------------------------------------------------------------------ Hedgehog linear attention

@@ -84,12 +84,16 @@ struct BasedParams {
     CUtensorMap tmO;   // 3-D {64, N, B*H} bf16, box {32, 32, 1}, 64-byte swizzle (stores)
     void *O;           // bf16 [B*H, N, 64]
     float *DEN;        // fp32 [B*H, N]
+    float *ws;         // segment states [B*H][n_seg][80][160] fp32 (n_seg > 1), else unused
     int N;
     int BH;
+    int n_seg;         // segments per head (1: one CTA walks the whole head)
+    int seg_chunks;    // 128-row chunks per segment
     float scale;
 };
 
 cudaError_t launch_based(const BasedParams &p, cudaStream_t stream);
+cudaError_t launch_based_states(const BasedParams &p, cudaStream_t stream);
 cudaError_t read_and_clear_based_status(uint32_t *status, uint32_t *detail);
 
 // Everything the Hedgehog linear-attention kernel needs (d = f = Dv = 64).
