@@ -308,6 +308,24 @@ int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq,
                     cudaStream_t stream);
 
 /*
+ * tk_hedgehog_workspace_bytes / tk_hedgehog_fwd_ws -- tk_hedgehog_fwd with
+ * the sequence split into segments when the B*H heads are fewer than the
+ * SMs, as tk_based_workspace_bytes / tk_based_fwd_ws describe for Based: a
+ * first pass forms each segment's fp32 partial state sum_j [V_j | 1]
+ * phi_k(K_j)^T (B*H * n_seg * 40,960 bytes of workspace, rounded up to 256;
+ * 0 when no split is needed or the shape is invalid), then one CTA per
+ * segment starts from the sum of those before it.  Arguments as
+ * tk_hedgehog_fwd plus `workspace` (device, 256-byte aligned, not
+ * overlapping any argument; NULL allowed when the size is 0) and its size.
+ * Errors as tk_hedgehog_fwd plus TK_ERR_WORKSPACE, TK_ERR_NULL_PTR and
+ * TK_ERR_ALIAS for the workspace.  Deterministic.
+ */
+size_t tk_hedgehog_workspace_bytes(int64_t B, int64_t H, int64_t N);
+int tk_hedgehog_fwd_ws(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O,
+                       float *DEN, void *workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+                       int64_t Dqk, int64_t F, int64_t Dv, cudaStream_t stream);
+
+/*
  * tk_attn_device_status -- synchronises `stream`, then reads and clears the
  * current device's kernel status word.  Returns TK_OK if no bounded wait of
  * any kernel of this library on this device has given up since the last

@@ -260,3 +260,23 @@ def _hh(q=Bq, k=Bk, v=Bv, wq=Bdo, wk=BdQ, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=64, F
 ])
 def test_hedgehog_host_validation(kwargs, code):
     assert _hh(**kwargs) == tk.STATUS[code]
+
+
+def _hh_ws(q=Bq, k=Bk, v=Bv, wq=Bdo, wk=BdQ, o=Bo, d=Bl, ws=Bws, ws_bytes=1 << 20, B=1, H=1, N=128, Dqk=64, F=64,
+           Dv=64):
+    return tk.load().tk_hedgehog_fwd_ws(q, k, v, wq, wk, o, d, ws, ws_bytes, B, H, N, Dqk, F, Dv, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(wq=None), "TK_ERR_NULL_PTR"),
+    (dict(H=0), "TK_ERR_BAD_SHAPE"),
+    (dict(F=128), "TK_ERR_UNSUPPORTED_D"),
+    (dict(wk=BdQ + 4), "TK_ERR_MISALIGNED"),
+    (dict(o=Bk + 2048), "TK_ERR_ALIAS"),
+])
+def test_hedgehog_ws_host_validation(kwargs, code):
+    assert _hh_ws(**kwargs) == tk.STATUS[code]
+
+
+def test_hedgehog_workspace_bytes_without_device():
+    assert tk.load().tk_hedgehog_workspace_bytes(1, 0, 128) == 0

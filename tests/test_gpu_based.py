@@ -108,7 +108,9 @@ def test_based_segments_match_one_cta_per_head(oracle_mod, N):
     q, k, v = _qkv(1, 3, N, 420 + N)
     o1, d1 = _run(q, k, v, 0.25, segments=True)
     o2, d2 = _run(q, k, v, 0.25, segments=False)
-    assert np.abs(o1 - o2).max() <= 1e-2 and (np.abs(d1 - d2) / np.abs(d2)).max() <= 2e-3
+    # the carried state enters the products as bf16: two fp32 states that differ in
+    # their last bits may round to neighbouring bf16 values (2^-8 apart at most)
+    assert np.abs(o1 - o2).max() <= 1e-2 and (np.abs(d1 - d2) / np.abs(d2)).max() <= 2.0 ** -8
     if N <= 2049:
         O_ref, D_ref = oracle_mod.based(q, k, v, 0.25)
         _assert_close(o1, d1, O_ref, D_ref, f"segmented N={N}")

@@ -28,8 +28,8 @@ def _inputs(B, H, N, seed, wscale=0.2):
     return q, k, v, wq, wk
 
 
-def _run(q, k, v, wq, wk):
-    o, den = tk.hedgehog(q.cuda(), k.cuda(), v.cuda(), wq.cuda(), wk.cuda())
+def _run(q, k, v, wq, wk, segments=True):
+    o, den = tk.hedgehog(q.cuda(), k.cuda(), v.cuda(), wq.cuda(), wk.cuda(), segments=segments)
     torch.cuda.synchronize()
     status, detail = tk.device_status()
     assert status == 0, f"device status {status} detail {detail:#x}"
@@ -79,3 +79,60 @@ def test_hedgehog_bench_workload_sampled(oracle_mod):
     o, den = _run(q, k, v, wq, wk)
     rows = [0, 1, 127, 128, 2047, 2048, 4094, 4095]
     _check_heads(oracle_mod, q, k, v, wq, wk, o, den, [(0, 0), (7, 15)], rows=rows, what="B8H16N4096")
+
+
+# ---------------------------------------------------------------- segmented sequences
+# Fewer heads than SMs (the binding's default path, tk_hedgehog_fwd_ws): each
+# head is split into segments that start from the sum of the fp32 partial
+# states before them (formed by a first pass with the same feature map).
+
+def test_hedgehog_segments_long_sequence(oracle_mod):
+    """B1 H2 N20000: sampled rows across many segment boundaries and the ragged end."""
+    B, H, N = 1, 2, 20000
+    assert tk.hedgehog_workspace_bytes(B, H, N) > 0
+    q, k, v, wq, wk = _inputs(B, H, N, 510)
+    o, den = _run(q, k, v, wq, wk)
+    rows = sorted({0, 1, 127, 128, 639, 640, 641, 1279, 1280, 5119, 5120, 12799, 12800, 19200, 19967, 19968,
+                   19999} | {int(x) for x in np.random.default_rng(8).integers(0, N, 10)})
+    _check_heads(oracle_mod, q, k, v, wq, wk, o, den, [(0, 0), (0, 1)], rows=rows, what="segmented N20000")
+
+
+@pytest.mark.parametrize("N", [1000, 2049, 9000])
+def test_hedgehog_segments_match_one_cta_per_head(oracle_mod, N):
+    q, k, v, wq, wk = _inputs(1, 3, N, 520 + N)
+    o1, d1 = _run(q, k, v, wq, wk, segments=True)
+    o2, d2 = _run(q, k, v, wq, wk, segments=False)
+    # the carried state enters the products as bf16: two fp32 states that differ in
+    # their last bits may round to neighbouring bf16 values (2^-8 apart at most)
+    assert np.abs(o1 - o2).max() <= 1e-2 and (np.abs(d1 - d2) / np.abs(d2)).max() <= 2.0 ** -8
+    if N <= 2049:
+        _check_heads(oracle_mod, q, k, v, wq, wk, o1, d1, [(0, 0), (0, 2)], what=f"segmented N={N}")
+
+
+def test_hedgehog_segments_deterministic():
+    q, k, v, wq, wk = _inputs(1, 2, 12000, 530)
+    o1, d1 = _run(q, k, v, wq, wk)
+    o2, d2 = _run(q, k, v, wq, wk)
+    assert np.array_equal(o1, o2) and np.array_equal(d1, d2)
+
+
+def test_hedgehog_workspace_checks():
+    B, H, N = 1, 2, 20000
+    need = tk.hedgehog_workspace_bytes(B, H, N)
+    assert need > 0 and need % 256 == 0
+    q, k, v, wq, wk = (t.cuda() for t in _inputs(B, H, N, 540))
+    o = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device="cuda")
+    den = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    lib = tk.load()
+
+    def call(ws_ptr, ws_bytes):
+        return lib.tk_hedgehog_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                      o.data_ptr(), den.data_ptr(), ws_ptr, ws_bytes, B, H, N, 64, 64, 64, None)
+    assert call(None, 0) == tk.STATUS["TK_ERR_NULL_PTR"]
+    assert call(ws.data_ptr(), need - 256) == tk.STATUS["TK_ERR_WORKSPACE"]
+    assert call(ws.data_ptr() + 16, need) == tk.STATUS["TK_ERR_WORKSPACE"]
+    assert call(den.data_ptr(), need) == tk.STATUS["TK_ERR_ALIAS"]
+    assert call(ws.data_ptr(), need) == 0
+    torch.cuda.synchronize()
+    assert tk.device_status()[0] == 0

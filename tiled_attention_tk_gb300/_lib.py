@@ -35,6 +35,9 @@ SIGNATURES = {
     "tk_based_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
     "tk_based_fwd_ws": ([_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64, _I64, _F, _P], _I),
     "tk_hedgehog_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P], _I),
+    "tk_hedgehog_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),
+    "tk_hedgehog_fwd_ws": ([_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64, _I64, _I64, _P],
+                           _I),
     "tk_attn_device_status": ([_P, ctypes.POINTER(ctypes.c_uint32)], _I),
     "tk_attn_selftest_timeout": ([_U64, _P], _I),
     "tk_attn_strerror": ([_I], ctypes.c_char_p),

@@ -239,11 +239,20 @@ def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None
     return out, den
 
 
+def hedgehog_workspace_bytes(B: int, H: int, N: int) -> int:
+    """Workspace tk_hedgehog_fwd_ws needs on the current device (0: no segments)."""
+    return int(_lib.load().tk_hedgehog_workspace_bytes(B, H, N))
+
+
 def hedgehog(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, wq: torch.Tensor, wk: torch.Tensor,
-             out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None):
+             out: torch.Tensor | None = None, den: torch.Tensor | None = None, stream=None,
+             workspace: torch.Tensor | None = None, segments: bool = True):
     """Causal Hedgehog linear attention.  q, k, v: bf16 [B,H,N,64]; wq, wk:
     bf16 [H,64,64] (CUDA).  phi(x) = [softmax(x W), softmax(-x W)];
-    returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]).  Enqueued without
+    returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]).  With ``segments`` (the
+    default) and fewer heads than SMs, each head's sequence is split into
+    segments (tk_hedgehog_fwd_ws; ``workspace`` is allocated here unless
+    given); ``segments=False`` is tk_hedgehog_fwd.  Enqueued without
     synchronising."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
@@ -261,7 +270,18 @@ def hedgehog(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, wq: torch.Tensor
     if den is None:
         den = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        rc = _lib.load().tk_hedgehog_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
-                                         out.data_ptr(), den.data_ptr(), B, H, N, d, f, Dv, _stream_handle(stream))
-    _lib.check(rc, "tk_hedgehog_fwd")
+        if not segments:
+            rc = _lib.load().tk_hedgehog_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                             out.data_ptr(), den.data_ptr(), B, H, N, d, f, Dv, _stream_handle(stream))
+            _lib.check(rc, "tk_hedgehog_fwd")
+            return out, den
+        need = hedgehog_workspace_bytes(B, H, N) if (d, f, Dv) == (64, 64, 64) else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = _lib.load().tk_hedgehog_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), wq.data_ptr(), wk.data_ptr(),
+                                            out.data_ptr(), den.data_ptr(), ws_ptr, ws_bytes, B, H, N, d, f, Dv,
+                                            _stream_handle(stream))
+    _lib.check(rc, "tk_hedgehog_fwd_ws")
     return out, den

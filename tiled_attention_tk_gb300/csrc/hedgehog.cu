@@ -167,9 +167,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int bh = blockIdx.x;
+    // A CTA walks one segment of a head: its chunks c0 .. c0 + n_chunks - 1
+    // (the whole head unless the sequence is split into segments; then the
+    // state of the chunks before c0 comes from the segment-state pass in
+    // p.ws).  Chunk indices below are local to the segment.
+    const int seg = blockIdx.x % p.n_seg;
+    const int bh = blockIdx.x / p.n_seg;
     const int head = bh % p.H;
-    const int n_chunks = (p.N + C - 1) / C;
+    const int c0 = seg * p.seg_chunks;
+    const int n_chunks = min(p.seg_chunks, (p.N + C - 1) / C - c0);
+    const bool has_prev = seg > 0;
 
     if (sbase & 1023u) {  // the swizzled layouts need it; uniform over the CTA, so every thread returns
         if (threadIdx.x == 0) record_timeout((ROLE_HH_LAYOUT << 24) | (sbase & 0xFFFFu));
@@ -231,14 +238,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                                                   (ROLE_HH_PRODUCER << 24) | (B_QKEMPTY << 16) | c)))
                     break;
                 mbar_arrive_expect_tx(bar(B_QKFULL), 2 * BOX);
-                tma_load_3d(sbase + QK_OFF, &p.tmQ, bar(B_QKFULL), 0, c * C, bh);
-                tma_load_3d(sbase + QK_OFF + BOX, &p.tmK, bar(B_QKFULL), 0, c * C, bh);
+                tma_load_3d(sbase + QK_OFF, &p.tmQ, bar(B_QKFULL), 0, (c0 + c) * C, bh);
+                tma_load_3d(sbase + QK_OFF + BOX, &p.tmK, bar(B_QKFULL), 0, (c0 + c) * C, bh);
                 ++qk_issued;
                 if (c >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
                                                   (ROLE_HH_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | c)))
                     break;
                 mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
-                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, c * C, bh);
+                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (c0 + c) * C, bh);
                 ++v_issued;
             }
             if (!ok) {
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                     umma_ts(tmem + T_O, tmem + T_P + k * 8,
                             smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
                 // inter: [num | den] += phi(Q) S_{<c}
-                if (c > 0) {
+                if (c > 0 || has_prev) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
                         umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8,
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 for (int k = 0; k < C / 16; ++k)
                     umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
                             smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE,
-                            (c > 0 || k > 0) ? 1u : 0u);
+                            (c > 0 || has_prev || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_VEMPTY + b));
                 // S of the next chunk, once its features and this chunk's state are in smem
@@ -381,11 +388,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             }
         };
         const uint32_t obox = sbase + OST_OFF + warp * OBOX;
+        // bf16 copy of the state (rows 0..79 of S^T, this group's 64 features)
+        // for the next chunk's carried product
+        auto copy_state = [&]() {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sv[32];
+                tmem_ld32(lane_base + T_ST + grp * 64 + h2 * 32, sv);  // every lane loads; rows >= 80 are not stored
+                if (i < NV) {
+                    const uint32_t box = sbase + SPREV_OFF + grp * SBOX;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_shared_v4(sw128(box, i, h2 * 4 + q),
+                                     pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
+                                     pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
+                                     pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
+                                     pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
+                }
+            }
+        };
+        if (has_prev) {
+            // --- the state of the segments before this one: the sum of their fp32
+            // partial states into the group's 64 columns of S^T (rows >= 65 are 0),
+            // and its bf16 copy for the first chunk's carried product
+            for (int blk = 0; blk < 64; blk += 16) {
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
+                if (i < NV) {
+                    for (int sp = 0; sp < seg; ++sp) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.ws + ((static_cast<size_t>(bh) * p.n_seg + sp) * NV + i) * F + grp * 64 + blk);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 v = src[q];
+                            acc[4 * q] += v.x;
+                            acc[4 * q + 1] += v.y;
+                            acc[4 * q + 2] += v.z;
+                            acc[4 * q + 3] += v.w;
+                        }
+                    }
+                }
+                uint32_t u[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(acc[e]);
+                tmem_st16(lane_base + T_ST + grp * 64 + blk, u);
+            }
+            tmem_st_wait();
+            copy_state();
+        }
         bool ok = wait_bounded(bar(B_ZFULL), 0, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_ZFULL << 16));
         if (ok) {
             tc_fence_after_sync();
             uint32_t pk[64];
-            phi_regs(zcol, grp == 0 || i < p.N, pk);  // phi(Q) always live; phi(K) zero past N
+            phi_regs(zcol, grp == 0 || c0 * C + i < p.N, pk);  // phi(Q) always live; phi(K) zero past N
             put_phi(pk);
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -393,13 +449,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         }
         for (int c = 0; ok && c < n_chunks; ++c) {
             const uint32_t ph = c & 1;
-            const int row = c * C + i;
+            const int row = (c0 + c) * C + i;
             // --- this group's half of P = S under the causal mask (keys j <= i of the chunk and j < N)
             if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_HH_COMPUTE << 24) | (B_SFULL << 16) | c)))
                 break;
             tc_fence_after_sync();
             {
-                const int jmax = min(i, p.N - 1 - c * C);
+                const int jmax = min(i, p.N - 1 - (c0 + c) * C);
                 uint32_t sr[64];
                 tmem_ld64(lane_base + T_Z + grp * 64, sr);
                 tc_fence_before_sync();
@@ -430,21 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                     break;
                 tc_fence_after_sync();
                 put_phi(pk);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t sv[32];
-                    tmem_ld32(lane_base + T_ST + grp * 64 + h2 * 32, sv);  // every lane loads; rows >= 80 are not stored
-                    if (i < NV) {
-                        const uint32_t box = sbase + SPREV_OFF + grp * SBOX;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            st_shared_v4(sw128(box, i, h2 * 4 + q),
-                                         pack_bf16x2(__uint_as_float(sv[8 * q]), __uint_as_float(sv[8 * q + 1])),
-                                         pack_bf16x2(__uint_as_float(sv[8 * q + 2]), __uint_as_float(sv[8 * q + 3])),
-                                         pack_bf16x2(__uint_as_float(sv[8 * q + 4]), __uint_as_float(sv[8 * q + 5])),
-                                         pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
-                    }
-                }
+                copy_state();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(bar(B_PHIREADY), lane);
@@ -480,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 if (grp == 0 && row < p.N) p.DEN[head_row0 + row] = den;
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int row0 = c * C + (warp % 4) * 32;
+                const int row0 = (c0 + c) * C + (warp % 4) * 32;
                 if (lane == 0 && row0 < p.N) {
                     tma_store_3d(&p.tmO, obox, grp * 32, row0, bh);  // rows past N are clipped
                     tma_store_commit();
@@ -498,6 +540,249 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
     }
 }
 
+
+// ------------------------------------------------------------------ segment states
+//
+// For a head split into segments, each segment starts from the sum of the
+// partial states of the segments before it.  This pass forms, per (head,
+// segment) except the last, the partial state
+//   dS^T = sum over the segment's rows of [v_j | 1] phi_k(k_j)^T   (fp32, 65 live rows x 128)
+// with the main kernel's arithmetic (Z = K Wk on the tensor core, the same
+// feature map, the same product), into ws[bh][seg].
+
+// One half of phi(z) for one row: softmax(z) (half 0) or softmax(-z) (half 1)
+// of the 64 projections at `zcol`, as 32 packed bf16 pairs, computed exactly
+// as phi_regs computes that half.
+__device__ __forceinline__ void phi_half(uint32_t zcol, bool live, int half, uint32_t (&pk)[32]) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    uint32_t zr[64];
+    tmem_ld64(zcol, zr);
+    float zmax = __uint_as_float(zr[0]), zmin = zmax;
+#pragma unroll
+    for (int c = 1; c < FH; c += 2) {
+        zmax = fmax3(zmax, __uint_as_float(zr[c]), __uint_as_float(zr[c + 1 < FH ? c + 1 : c]));
+        zmin = fmin3(zmin, __uint_as_float(zr[c]), __uint_as_float(zr[c + 1 < FH ? c + 1 : c]));
+    }
+    const float2 mul = half == 0 ? make_float2(kLog2e, kLog2e) : make_float2(-kLog2e, -kLog2e);
+    const float off = half == 0 ? -zmax * kLog2e : zmin * kLog2e;
+    const float2 add = make_float2(off, off);
+    float2 e[FH / 2];
+    float2 sum2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < FH / 2; ++q) {
+        const float2 a = __ffma2_rn(make_float2(__uint_as_float(zr[2 * q]), __uint_as_float(zr[2 * q + 1])), mul, add);
+        e[q] = make_float2(ex2(a.x), ex2(a.y));
+        sum2 = __fadd2_rn(sum2, e[q]);
+    }
+    const float sc = live ? 1.0f / (sum2.x + sum2.y) : 0.0f;
+    const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+    for (int q = 0; q < FH / 2; ++q) {
+        const float2 v = __fmul2_rn(e[q], sc2);
+        pk[q] = pack_bf16x2(v.x, v.y);
+    }
+}
+
+namespace st {
+constexpr uint32_t K_OFF = 0;                         // K box of chunk c at + (c & 1) * BOX
+constexpr uint32_t V_OFF = K_OFF + 2 * BOX;           // V box likewise
+constexpr uint32_t WK_OFF = V_OFF + 2 * BOX;          // Wk [d][f]
+constexpr uint32_t ONES_OFF = WK_OFF + WBOX;
+constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K) of chunk c at + (c & 1) * 2 * BOX
+constexpr uint32_t BAR_OFF = PHIK_OFF + 4 * BOX;
+constexpr int B_FULL = 0;          // + buffer (2): K, V loaded
+constexpr int B_FREE = 2;          // + buffer (2): the state product of the chunk in it is done
+constexpr int B_ZFULL = 4;         // + buffer (2): K Wk in TMEM
+constexpr int B_PHIKREADY = 6;     // + buffer (2): phi(K) in smem (8 warps)
+constexpr int B_WFULL = 8;
+constexpr int B_STDONE = 9;
+constexpr int B_MMADONE = 10;
+constexpr int NUM_BARS = 11;
+constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t T_ZK = 0;       // K Wk of chunk c at + (c & 1) * 64
+constexpr uint32_t T_STATE = 128;  // S^T fp32: 128 cols
+static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+static_assert(WK_OFF % 1024 == 0 && ONES_OFF % 1024 == 0 && PHIK_OFF % 1024 == 0, "swizzled boxes");
+}  // namespace st
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_state_kernel(const __grid_constant__ HedgehogParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + st::BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + st::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int seg = blockIdx.x % (p.n_seg - 1);   // every segment but the last
+    const int bh = blockIdx.x / (p.n_seg - 1);
+    const int head = bh % p.H;
+    const int c0 = seg * p.seg_chunks;
+    const int n_chunks = p.seg_chunks;
+
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_addr(tmem_slot), st::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(st::B_FULL + b), 1);
+            mbar_init(bar(st::B_FREE + b), 1);
+            mbar_init(bar(st::B_ZFULL + b), 1);
+            mbar_init(bar(st::B_PHIKREADY + b), 8);
+        }
+        mbar_init(bar(st::B_WFULL), 1);
+        mbar_init(bar(st::B_STDONE), 1);
+        mbar_init(bar(st::B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp < 4) {
+        const int r = threadIdx.x;
+        const uint32_t one = 0x3F80u;  // bf16 1.0 in the low half (column 0)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(sw128(sbase + st::ONES_OFF, r, c), c == 0 ? one : 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == WARP_TMA) {
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            tma_prefetch_desc(&p.tmWk);
+            mbar_arrive_expect_tx(bar(st::B_WFULL), WBOX);
+            tma_load_3d(sbase + st::WK_OFF, &p.tmWk, bar(st::B_WFULL), 0, 0, head);
+            int issued = 0;
+            bool ok = true;
+            for (int c = 0; c < n_chunks; ++c) {
+                const int b = c & 1;
+                if (c >= 2 && !(ok = wait_bounded(bar(st::B_FREE + b), ((c >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_HH_PRODUCER << 24) | ((st::B_FREE + b) << 16) | c)))
+                    break;
+                mbar_arrive_expect_tx(bar(st::B_FULL + b), 2 * BOX);
+                tma_load_3d(sbase + st::K_OFF + b * BOX, &p.tmK, bar(st::B_FULL + b), 0, (c0 + c) * C, bh);
+                tma_load_3d(sbase + st::V_OFF + b * BOX, &p.tmV, bar(st::B_FULL + b), 0, (c0 + c) * C, bh);
+                ++issued;
+            }
+            if (!ok) {
+                const uint64_t t0 = global_timer_ns();
+                for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+                    while (!mbar_try_wait(bar(st::B_FULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                while (!mbar_try_wait(bar(st::B_WFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t ID_Z = idesc_bf16_f32(C, FH, 0, 1);      // K Wk: K K-major, W MN-major
+            constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
+            auto issue_z = [&](int c) {
+                const int b = c & 1;
+                const uint32_t kb = sbase + st::K_OFF + b * BOX;
+#pragma unroll
+                for (int k = 0; k < DQK / 16; ++k)
+                    umma_ss(tmem + st::T_ZK + b * FH, smem_desc_sw128(kb + k * 32, 16, 1024),
+                            smem_desc_sw128(sbase + st::WK_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
+                umma_commit(bar(st::B_ZFULL + b));
+            };
+            bool ok = wait_bounded(bar(st::B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (st::B_WFULL << 16));
+            for (int c = 0; ok && c < 2 && c < n_chunks; ++c) {
+                if (!(ok = wait_bounded(bar(st::B_FULL + c), 0, abort_flag, (ROLE_HH_MMA << 24) | ((st::B_FULL + c) << 16))))
+                    break;
+                tc_fence_after_sync();
+                issue_z(c);
+            }
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int b = c & 1;
+                const uint32_t vb = sbase + st::V_OFF + b * BOX;
+                if (!(ok = wait_bounded(bar(st::B_PHIKREADY + b), (c >> 1) & 1, abort_flag,
+                                        (ROLE_HH_MMA << 24) | ((st::B_PHIKREADY + b) << 16) | c)))
+                    break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    umma_ss(tmem + st::T_STATE, smem_desc_sw128(vb + k * 2048, st::ONES_OFF - (vb - sbase), 1024),
+                            smem_desc_sw128(sbase + st::PHIK_OFF + b * 2 * BOX + k * 2048, BOX, 1024), ID_STATE,
+                            (c > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(st::B_FREE + b));
+                // Z of chunk c+2 into this buffer: its K is loaded once this chunk's products are done,
+                // and the compute warps read this chunk's Z before they handed over phi(K)
+                if (c + 2 < n_chunks) {
+                    if (!(ok = wait_bounded(bar(st::B_FULL + b), ((c + 2) >> 1) & 1, abort_flag,
+                                            (ROLE_HH_MMA << 24) | ((st::B_FULL + b) << 16) | (c + 2))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_z(c + 2);
+                }
+            }
+            if (ok) umma_commit(bar(st::B_STDONE));
+            umma_commit(bar(st::B_MMADONE));
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(st::B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // group 0 forms softmax(z), group 1 softmax(-z) of K Wk, each into its box of phi(K)
+        const int i = threadIdx.x % 128;
+        const int grp = warp / 4;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+        bool ok = true;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int b = c & 1;
+            if (!(ok = wait_bounded(bar(st::B_ZFULL + b), (c >> 1) & 1, abort_flag,
+                                    (ROLE_HH_COMPUTE << 24) | ((st::B_ZFULL + b) << 16) | c)))
+                break;
+            tc_fence_after_sync();
+            uint32_t pk[32];
+            phi_half(lane_base + st::T_ZK + b * FH, (c0 + c) * C + i < p.N, grp, pk);
+            if (c >= 2 && !(ok = wait_bounded(bar(st::B_FREE + b), ((c >> 1) - 1) & 1, abort_flag,
+                                              (ROLE_HH_COMPUTE << 24) | ((st::B_FREE + b) << 16) | c)))
+                break;
+            const uint32_t box = sbase + st::PHIK_OFF + b * 2 * BOX + grp * BOX;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_shared_v4(sw128(box, i, q), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            warp_arrive(bar(st::B_PHIKREADY + b), lane);
+        }
+        if (ok && wait_bounded(bar(st::B_STDONE), 0, abort_flag, (ROLE_HH_COMPUTE << 24) | (st::B_STDONE << 16))) {
+            tc_fence_after_sync();
+            float *dst = p.ws + ((static_cast<size_t>(bh) * p.n_seg + seg) * NV + i) * F + grp * 64;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + st::T_STATE + grp * 64 + h2 * 32, v);  // every lane loads; rows >= 80 are not stored
+                if (i < NV) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + h2 * 32);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, st::TMEM_COLS);
+    }
+}
+
 }  // namespace hedgehog
 
 cudaError_t launch_hedgehog(const HedgehogParams &p, cudaStream_t stream) {
@@ -512,11 +797,31 @@ cudaError_t launch_hedgehog(const HedgehogParams &p, cudaStream_t stream) {
         configured_device = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.BH), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * p.n_seg), 1, 1);
     cfg.blockDim = dim3(hedgehog::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = hedgehog::SMEM_ALLOC;
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, hedgehog::hedgehog_kernel, p);
+}
+
+// The segment-state pass (n_seg > 1): one CTA per (head, segment) but the last.
+cudaError_t launch_hedgehog_states(const HedgehogParams &p, cudaStream_t stream) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        if ((err = cudaFuncSetAttribute(hedgehog::hedgehog_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        hedgehog::st::SMEM_ALLOC)) != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * (p.n_seg - 1)), 1, 1);
+    cfg.blockDim = dim3(hedgehog::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = hedgehog::st::SMEM_ALLOC;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, hedgehog::hedgehog_state_kernel, p);
 }
 
 cudaError_t read_and_clear_hedgehog_status(uint32_t *status, uint32_t *detail) {

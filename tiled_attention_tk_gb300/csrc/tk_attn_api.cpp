@@ -468,9 +468,10 @@ struct BasedPlan {
 };
 
 constexpr int kBasedMinSegChunks = 4;
-constexpr uint64_t kBasedSegStateBytes = 80ull * 160ull * 4ull;  // one segment's state, fp32
+constexpr uint64_t kBasedSegStateBytes = 80ull * 160ull * 4ull;     // one segment's state, fp32
+constexpr uint64_t kHedgehogSegStateBytes = 80ull * 128ull * 4ull;  // likewise for Hedgehog
 
-BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
+BasedPlan plan_segments(int64_t BH, int64_t N, int num_sms, uint64_t seg_state_bytes) {
     const int64_t n_chunks = (N + 127) / 128;
     BasedPlan pl{1, static_cast<int>(n_chunks), 0};
     if (BH >= num_sms) return pl;
@@ -481,8 +482,12 @@ BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
     if (n_seg < 2) return pl;
     pl.n_seg = static_cast<int>(n_seg);
     pl.seg_chunks = static_cast<int>(seg_chunks);
-    pl.workspace = round_up(static_cast<uint64_t>(BH) * n_seg * kBasedSegStateBytes, kWorkspaceAlign);
+    pl.workspace = round_up(static_cast<uint64_t>(BH) * n_seg * seg_state_bytes, kWorkspaceAlign);
     return pl;
+}
+
+BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
+    return plan_segments(BH, N, num_sms, kBasedSegStateBytes);
 }
 
 int based_checks(const void *Q, const void *K, const void *V, void *O, float *DEN, int64_t B, int64_t H, int64_t N,
@@ -596,8 +601,10 @@ int encode_batched_map(CUtensorMap *map, const void *ptr, int64_t c, int64_t r, 
     return TK_OK;
 }
 
-int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O, float *DEN,
-                    int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t F, int64_t Dv, cudaStream_t stream) {
+namespace {
+
+int hedgehog_checks(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O, float *DEN,
+                    int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t F, int64_t Dv) {
     if (!Q || !K || !V || !Wq || !Wk || !O || !DEN) return TK_ERR_NULL_PTR;
     if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
     if (Dqk != 64 || F != 64 || Dv != 64) return TK_ERR_UNSUPPORTED_D;
@@ -615,12 +622,12 @@ int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq,
         if (overlaps(O, t_bytes, ins[a], in_bytes[a]) || overlaps(DEN, den_bytes, ins[a], in_bytes[a]))
             return TK_ERR_ALIAS;
     if (overlaps(O, t_bytes, DEN, den_bytes)) return TK_ERR_ALIAS;
-    int num_sms = 0;
-    int rc = current_device(&num_sms);
-    if (rc != TK_OK) return rc;
-    const void *ptrs[7] = {Q, K, V, Wq, Wk, O, DEN};
-    for (const void *ptr : ptrs)
-        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    return TK_OK;
+}
+
+int hedgehog_launch(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O, float *DEN,
+                    int64_t H, int64_t BH, int64_t N, const BasedPlan &pl, void *workspace, cudaStream_t stream) {
+    int rc;
     tk::HedgehogParams p;
     if ((rc = encode_qkv_map(&p.tmQ, Q, N, 64, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmK, K, N, 64, BH)) != TK_OK) return rc;
@@ -630,12 +637,64 @@ int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq,
     if ((rc = encode_out32_map(&p.tmO, O, N, BH)) != TK_OK) return rc;
     p.O = O;
     p.DEN = DEN;
+    p.ws = static_cast<float *>(workspace);
     p.N = static_cast<int>(N);
     p.H = static_cast<int>(H);
     p.BH = static_cast<int>(BH);
-    cudaError_t e = tk::launch_hedgehog(p, stream);
+    p.n_seg = pl.n_seg;
+    p.seg_chunks = pl.seg_chunks;
+    cudaError_t e = cudaSuccess;
+    if (pl.n_seg > 1) e = tk::launch_hedgehog_states(p, stream);
+    if (e == cudaSuccess) e = tk::launch_hedgehog(p, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
+}
+
+}  // namespace
+
+int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O, float *DEN,
+                    int64_t B, int64_t H, int64_t N, int64_t Dqk, int64_t F, int64_t Dv, cudaStream_t stream) {
+    int rc = hedgehog_checks(Q, K, V, Wq, Wk, O, DEN, B, H, N, Dqk, F, Dv);
+    if (rc != TK_OK) return rc;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const void *ptrs[7] = {Q, K, V, Wq, Wk, O, DEN};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0};
+    return hedgehog_launch(Q, K, V, Wq, Wk, O, DEN, H, B * H, N, whole, nullptr, stream);
+}
+
+size_t tk_hedgehog_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B < 1 || H < 1 || N < 1 || N > INT32_MAX || B > INT32_MAX / H) return 0;
+    int num_sms = 0;
+    if (current_device(&num_sms) != TK_OK) return 0;
+    return static_cast<size_t>(plan_segments(B * H, N, num_sms, kHedgehogSegStateBytes).workspace);
+}
+
+int tk_hedgehog_fwd_ws(const void *Q, const void *K, const void *V, const void *Wq, const void *Wk, void *O,
+                       float *DEN, void *workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+                       int64_t Dqk, int64_t F, int64_t Dv, cudaStream_t stream) {
+    int rc = hedgehog_checks(Q, K, V, Wq, Wk, O, DEN, B, H, N, Dqk, F, Dv);
+    if (rc != TK_OK) return rc;
+    int num_sms = 0;
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const BasedPlan pl = plan_segments(B * H, N, num_sms, kHedgehogSegStateBytes);
+    if (pl.workspace > 0) {
+        if (!workspace) return TK_ERR_NULL_PTR;
+        if (!aligned(workspace, kWorkspaceAlign) || workspace_bytes < pl.workspace) return TK_ERR_WORKSPACE;
+        const int64_t BH = B * H;
+        const uint64_t t_bytes = static_cast<uint64_t>(BH) * N * 64 * 2, w_bytes = static_cast<uint64_t>(H) * 64 * 64 * 2,
+                       den_bytes = static_cast<uint64_t>(BH) * N * 4;
+        const void *bufs[7] = {Q, K, V, Wq, Wk, O, DEN};
+        const uint64_t bytes[7] = {t_bytes, t_bytes, t_bytes, w_bytes, w_bytes, t_bytes, den_bytes};
+        for (int a = 0; a < 7; ++a)
+            if (overlaps(workspace, pl.workspace, bufs[a], bytes[a])) return TK_ERR_ALIAS;
+    }
+    const void *ptrs[8] = {Q, K, V, Wq, Wk, O, DEN, pl.workspace > 0 ? workspace : Q};
+    for (const void *ptr : ptrs)
+        if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
+    return hedgehog_launch(Q, K, V, Wq, Wk, O, DEN, H, B * H, N, pl, pl.workspace > 0 ? workspace : nullptr, stream);
 }
 
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {

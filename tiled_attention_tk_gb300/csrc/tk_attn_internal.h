@@ -106,12 +106,16 @@ struct HedgehogParams {
     CUtensorMap tmO;   // 3-D {64, N, B*H} bf16, box {32, 32, 1}, 64-byte swizzle (stores)
     void *O;           // bf16 [B*H, N, 64]
     float *DEN;        // fp32 [B*H, N]
+    float *ws;         // segment states [B*H][n_seg][80][128] fp32 (n_seg > 1), else unused
     int N;
     int H;
     int BH;
+    int n_seg;         // segments per head (1: one CTA walks the whole head)
+    int seg_chunks;    // 128-row chunks per segment
 };
 
 cudaError_t launch_hedgehog(const HedgehogParams &p, cudaStream_t stream);
+cudaError_t launch_hedgehog_states(const HedgehogParams &p, cudaStream_t stream);
 cudaError_t read_and_clear_hedgehog_status(uint32_t *status, uint32_t *detail);
 
 // Size of the library-owned workspace behind tk_attn_bwd_noalloc.
