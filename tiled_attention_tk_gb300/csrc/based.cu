@@ -206,6 +206,9 @@ __device__ __forceinline__ void write_o(uint32_t lane_taddr, int grp, int lane, 
     }
 }
 
+// SEG: the sequence is split into segments (compiled apart, so the whole-head
+// kernel carries none of the segment bookkeeping).
+template <bool SEG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -221,11 +224,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     // (the whole head unless the sequence is split into segments; then the
     // state of the chunks before c0 comes from the segment-state pass in
     // p.ws).  Chunk indices below are local to the segment.
-    const int seg = blockIdx.x % p.n_seg;
-    const int bh = blockIdx.x / p.n_seg;
-    const int c0 = seg * p.seg_chunks;
-    const int n_chunks = min(p.seg_chunks, (p.N + C - 1) / C - c0);
-    const bool has_prev = seg > 0;
+    const int seg = SEG ? static_cast<int>(blockIdx.x) % p.n_seg : 0;
+    const int bh = SEG ? static_cast<int>(blockIdx.x) / p.n_seg : static_cast<int>(blockIdx.x);
+    const int c0 = SEG ? seg * p.seg_chunks : 0;
+    const int n_chunks = SEG ? min(p.seg_chunks, (p.N + C - 1) / C - c0) : (p.N + C - 1) / C;
+    const bool has_prev = SEG && seg > 0;
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -714,7 +717,9 @@ cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        if ((err = cudaFuncSetAttribute(based::based_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncSetAttribute(based::based_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        based::SMEM_ALLOC)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(based::based_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         based::SMEM_ALLOC)) != cudaSuccess)
             return err;
         configured_device = dev;
@@ -724,7 +729,8 @@ cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
     cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = based::SMEM_ALLOC;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, based::based_kernel, p);
+    return p.n_seg > 1 ? cudaLaunchKernelEx(&cfg, based::based_kernel<true>, p)
+                       : cudaLaunchKernelEx(&cfg, based::based_kernel<false>, p);
 }
 
 // The segment-state pass (n_seg > 1): one CTA per (head, segment) but the last.
