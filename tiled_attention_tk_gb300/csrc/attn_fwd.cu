@@ -252,25 +252,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 ++taken;
                 return r;
             };
+            // Descriptors are formed once per operand tile; the k steps add
+            // their (compile-time) offsets to the start-address field, which
+            // cannot carry out of its 14 bits (shared memory is below 256 KB).
             auto issue_s = [&](int i, uint32_t kslot) {
-                const uint32_t kbase = sbase + L::SLOT_OFF + kslot * L::TILE_BYTES;
-                const uint32_t qbase = sbase + L::Q_OFF + i * L::TILE_BYTES;
+                const uint64_t qd = smem_desc_sw128(sbase + L::Q_OFF + i * L::TILE_BYTES, 16, 1024);
+                const uint64_t kd = smem_desc_sw128(sbase + L::SLOT_OFF + kslot * L::TILE_BYTES, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * L::BOX_BYTES + (k % 4) * 32;
-                    umma_ss(tmem + L::tmem_s(i), smem_desc_sw128(qbase + off, 16, 1024),
-                            smem_desc_sw128(kbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    const uint64_t off = ((k / 4) * L::BOX_BYTES + (k % 4) * 32) >> 4;
+                    umma_ss(tmem + L::tmem_s(i), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(L::B_SFULL + i));
             };
             auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
-                const uint32_t vbase = sbase + L::SLOT_OFF + vslot * L::TILE_BYTES;
+                const uint64_t vd = smem_desc_sw128(sbase + L::SLOT_OFF + vslot * L::TILE_BYTES, L::BOX_BYTES, 1024);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     // 16 keys per step: P columns advance by 8 (two bf16 per
                     // 32-bit column), V rows by 16 * 128 bytes.
-                    umma_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + k * 8,
-                            smem_desc_sw128(vbase + k * 2048, L::BOX_BYTES, 1024), IDESC_O,
+                    umma_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + k * 8, vd + ((k * 2048) >> 4), IDESC_O,
                             (accumulate || k > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(L::B_PVDONE + i));
