@@ -255,21 +255,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S^T, dP^T: K-major A and B
             constexpr uint32_t IDESC_TS = idesc_bf16_f32(BT, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
             constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dQ_part: MN-major A and B
+            // Descriptors are formed once per operand tile; a k step adds its
+            // compile-time offset to the start-address field, which cannot
+            // carry out of its 14 bits (shared memory is below 256 KB).
             auto issue_s = [&](uint32_t qb) {  // S^T = K Q^T
+                const uint64_t kd = smem_desc_sw128(sbase + L::K_OFF, 16, 1024), qd = smem_desc_sw128(qb, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * L::BOX + (k % 4) * 32;
-                    umma_ss(tmem + L::T_S, smem_desc_sw128(sbase + L::K_OFF + off, 16, 1024),
-                            smem_desc_sw128(qb + off, 16, 1024), IDESC_KK, k > 0);
+                    const uint64_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
+                    umma_ss(tmem + L::T_S, kd + off, qd + off, IDESC_KK, k > 0);
                 }
                 umma_commit(bar(L::B_SFULL));
             };
             auto issue_dp = [&](uint32_t dob) {  // dP^T = V dO^T
+                const uint64_t vd = smem_desc_sw128(sbase + L::V_OFF, 16, 1024), dd = smem_desc_sw128(dob, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * L::BOX + (k % 4) * 32;
-                    umma_ss(tmem + L::T_DP, smem_desc_sw128(sbase + L::V_OFF + off, 16, 1024),
-                            smem_desc_sw128(dob + off, 16, 1024), IDESC_KK, k > 0);
+                    const uint64_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
+                    umma_ss(tmem + L::T_DP, vd + off, dd + off, IDESC_KK, k > 0);
                 }
                 umma_commit(bar(L::B_DPFULL));
             };
@@ -285,6 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 const uint32_t ph = it & 1;
                 const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
                 const uint32_t dob = qb + L::TILE;
+                const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
                 // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
                 // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
                 for (int c = 0; ok && c < 4; ++c) {
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                     for (int k = 2 * c; k < 2 * c + 2; ++k)
                         umma_ts(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + (k % 2) * 8,
-                                smem_desc_sw128(dob + k * 2048, L::BOX, 1024), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
+                                dob_mn + ((k * 2048) >> 4), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
                 }
                 // dK += dS'^T Q likewise.
                 for (int c = 0; ok && c < 4; ++c) {
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                     for (int k = 2 * c; k < 2 * c + 2; ++k)
                         umma_ts(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + (k % 2) * 8,
-                                smem_desc_sw128(qb + k * 2048, L::BOX, 1024), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
+                                qb_mn + ((k * 2048) >> 4), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
                 umma_commit(bar(L::B_QEMPTY + b));  // Q, dO of this tile are no longer read
@@ -321,10 +325,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
                 // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
                 // the dS^T buffer (MN-major A) and K MN-major.
+                {
+                    const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
+                                   kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
 #pragma unroll
-                for (int k = 0; k < BT / 16; ++k)
-                    umma_ss(tmem + L::T_DQ, smem_desc_sw128(sbase + L::DS_OFF + k * 2048, L::BOX, 1024),
-                            smem_desc_sw128(sbase + L::K_OFF + k * 2048, L::BOX, 1024), IDESC_MM, k > 0);
+                    for (int k = 0; k < BT / 16; ++k)
+                        umma_ss(tmem + L::T_DQ, dsd + ((k * 2048) >> 4), kmd + ((k * 2048) >> 4), IDESC_MM, k > 0);
+                }
                 umma_commit(bar(L::B_GDONE));
                 if (has_next) {
                     if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,

@@ -276,13 +276,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             // chunk's products run); once P is in TMEM: P [V|1], phi(Q) S_{<c},
             // the state update; once c+1's features are in place, phi(Q)
             // phi(K)^T of c+1.
+            // Descriptors are formed once per operand; a k step adds its
+            // compile-time offset to the start-address field (no carry:
+            // shared memory is below 256 KB).
+            const uint64_t qd = smem_desc_sw128(sbase + QK_OFF, 16, 1024), kd = smem_desc_sw128(sbase + QK_OFF + BOX, 16, 1024);
+            const uint64_t wqd = smem_desc_sw128(sbase + WQ_OFF, WBOX, 1024), wkd = smem_desc_sw128(sbase + WK_OFF, WBOX, 1024);
+            const uint64_t phikd = smem_desc_sw128(sbase + PHIK_OFF, 16, 1024), sprevd = smem_desc_sw128(sbase + SPREV_OFF, 16, 1024);
+            const uint64_t phikmn = smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024);
             auto issue_z = [&]() {  // Z = Q Wq, K Wk from the Q/K buffer, 16 of the 64 dims per step
 #pragma unroll
                 for (int k = 0; k < DQK / 16; ++k) {
-                    umma_ss(tmem + T_Z, smem_desc_sw128(sbase + QK_OFF + k * 32, 16, 1024),
-                            smem_desc_sw128(sbase + WQ_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
-                    umma_ss(tmem + T_Z + FH, smem_desc_sw128(sbase + QK_OFF + BOX + k * 32, 16, 1024),
-                            smem_desc_sw128(sbase + WK_OFF + k * 2048, WBOX, 1024), ID_Z, k > 0);
+                    umma_ss(tmem + T_Z, qd + ((k * 32) >> 4), wqd + ((k * 2048) >> 4), ID_Z, k > 0);
+                    umma_ss(tmem + T_Z + FH, kd + ((k * 32) >> 4), wkd + ((k * 2048) >> 4), ID_Z, k > 0);
                 }
                 umma_commit(bar(B_ZFULL));
                 umma_commit(bar(B_QKEMPTY));
@@ -290,8 +295,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features
 #pragma unroll
                 for (int k = 0; k < F / 16; ++k)
-                    umma_ts(tmem + T_Z, tmem + T_PHIQ + k * 8,
-                            smem_desc_sw128(sbase + PHIK_OFF + (k / 4) * BOX + (k % 4) * 32, 16, 1024), ID_S, k > 0);
+                    umma_ts(tmem + T_Z, tmem + T_PHIQ + k * 8, phikd + (((k / 4) * BOX + (k % 4) * 32) >> 4), ID_S, k > 0);
                 umma_commit(bar(B_SFULL));
             };
             bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16)) &&
@@ -325,24 +329,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]
+                const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ts(tmem + T_O, tmem + T_P + k * 8,
-                            smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024), ID_INTRA, k > 0);
+                    umma_ts(tmem + T_O, tmem + T_P + k * 8, v1d + ((k * 2048) >> 4), ID_INTRA, k > 0);
                 // inter: [num | den] += phi(Q) S_{<c}
                 if (c > 0 || has_prev) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
-                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8,
-                                smem_desc_sw128(sbase + SPREV_OFF + (k / 4) * SBOX + (k % 4) * 32, 16, 1024),
+                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8, sprevd + (((k / 4) * SBOX + (k % 4) * 32) >> 4),
                                 ID_INTER, 1);
                 }
                 umma_commit(bar(B_ODONE));
                 // state: S^T += [V | 1]^T phi(K)
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ss(tmem + T_ST, smem_desc_sw128(vb + k * 2048, ONES_OFF - (vb - sbase), 1024),
-                            smem_desc_sw128(sbase + PHIK_OFF + k * 2048, BOX, 1024), ID_STATE,
+                    umma_ss(tmem + T_ST, v1d + ((k * 2048) >> 4), phikmn + ((k * 2048) >> 4), ID_STATE,
                             (c > 0 || has_prev || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_VEMPTY + b));
