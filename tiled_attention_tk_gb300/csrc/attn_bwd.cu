@@ -260,19 +260,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             // carry out of its 14 bits (shared memory is below 256 KB).
             auto issue_s = [&](uint32_t qb) {  // S^T = K Q^T
                 const uint64_t kd = smem_desc_sw128(sbase + L::K_OFF, 16, 1024), qd = smem_desc_sw128(qb, 16, 1024);
+                const uint32_t k_lo = static_cast<uint32_t>(kd), q_lo = static_cast<uint32_t>(qd),
+                               hi = static_cast<uint32_t>(kd >> 32);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
-                    umma_ss(tmem + L::T_S, kd + off, qd + off, IDESC_KK, k > 0);
+                    const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
+                    umma_ss_lo(tmem + L::T_S, k_lo + off, hi, q_lo + off, hi, IDESC_KK, k > 0);
                 }
                 umma_commit(bar(L::B_SFULL));
             };
             auto issue_dp = [&](uint32_t dob) {  // dP^T = V dO^T
                 const uint64_t vd = smem_desc_sw128(sbase + L::V_OFF, 16, 1024), dd = smem_desc_sw128(dob, 16, 1024);
+                const uint32_t v_lo = static_cast<uint32_t>(vd), d_lo = static_cast<uint32_t>(dd),
+                               hi = static_cast<uint32_t>(vd >> 32);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
-                    umma_ss(tmem + L::T_DP, vd + off, dd + off, IDESC_KK, k > 0);
+                    const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
+                    umma_ss_lo(tmem + L::T_DP, v_lo + off, hi, d_lo + off, hi, IDESC_KK, k > 0);
                 }
                 umma_commit(bar(L::B_DPFULL));
             };
@@ -289,6 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
                 const uint32_t dob = qb + L::TILE;
                 const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
+                const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
                 // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
                 // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
                 for (int c = 0; ok && c < 4; ++c) {
@@ -298,8 +303,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     tc_fence_after_sync();
 #pragma unroll
                     for (int k = 2 * c; k < 2 * c + 2; ++k)
-                        umma_ts(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + (k % 2) * 8,
-                                dob_mn + ((k * 2048) >> 4), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
+                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + (k % 2) * 8,
+                                   static_cast<uint32_t>(dob_mn) + ((k * 2048) >> 4), mn_hi, IDESC_TS,
+                                   (it > 0 || k > 0) ? 1u : 0u);
                 }
                 // dK += dS'^T Q likewise.
                 for (int c = 0; ok && c < 4; ++c) {
@@ -309,8 +315,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     tc_fence_after_sync();
 #pragma unroll
                     for (int k = 2 * c; k < 2 * c + 2; ++k)
-                        umma_ts(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + (k % 2) * 8,
-                                qb_mn + ((k * 2048) >> 4), IDESC_TS, (it > 0 || k > 0) ? 1u : 0u);
+                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + (k % 2) * 8,
+                                   static_cast<uint32_t>(qb_mn) + ((k * 2048) >> 4), mn_hi, IDESC_TS,
+                                   (it > 0 || k > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
                 umma_commit(bar(L::B_QEMPTY + b));  // Q, dO of this tile are no longer read
@@ -328,9 +335,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 {
                     const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
                                    kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
+                    const uint32_t ds_lo = static_cast<uint32_t>(dsd), km_lo = static_cast<uint32_t>(kmd),
+                                   hi = static_cast<uint32_t>(dsd >> 32);
 #pragma unroll
                     for (int k = 0; k < BT / 16; ++k)
-                        umma_ss(tmem + L::T_DQ, dsd + ((k * 2048) >> 4), kmd + ((k * 2048) >> 4), IDESC_MM, k > 0);
+                        umma_ss_lo(tmem + L::T_DQ, ds_lo + ((k * 2048) >> 4), hi, km_lo + ((k * 2048) >> 4), hi, IDESC_MM,
+                                   k > 0);
                 }
                 umma_commit(bar(L::B_GDONE));
                 if (has_next) {

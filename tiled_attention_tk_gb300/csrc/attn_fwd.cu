@@ -51,6 +51,7 @@
 
 namespace tk {
 
+
 // ------------------------------------------------------------------ layout
 
 constexpr int BM = 128;            // query rows per Q tile (one TMEM lane each)
@@ -258,21 +259,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             auto issue_s = [&](int i, uint32_t kslot) {
                 const uint64_t qd = smem_desc_sw128(sbase + L::Q_OFF + i * L::TILE_BYTES, 16, 1024);
                 const uint64_t kd = smem_desc_sw128(sbase + L::SLOT_OFF + kslot * L::TILE_BYTES, 16, 1024);
+                const uint32_t q_lo = static_cast<uint32_t>(qd), k_lo = static_cast<uint32_t>(kd);
+                const uint32_t d_hi = static_cast<uint32_t>(qd >> 32);  // the same for Q and K
+                const uint32_t dst = tmem + L::tmem_s(i);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t off = ((k / 4) * L::BOX_BYTES + (k % 4) * 32) >> 4;
-                    umma_ss(tmem + L::tmem_s(i), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+                    const uint32_t off = ((k / 4) * L::BOX_BYTES + (k % 4) * 32) >> 4;
+                    umma_ss_lo(dst, q_lo + off, d_hi, k_lo + off, d_hi, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(L::B_SFULL + i));
             };
             auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
                 const uint64_t vd = smem_desc_sw128(sbase + L::SLOT_OFF + vslot * L::TILE_BYTES, L::BOX_BYTES, 1024);
+                const uint32_t v_lo = static_cast<uint32_t>(vd), v_hi = static_cast<uint32_t>(vd >> 32);
+                const uint32_t dst = tmem + L::tmem_o(i), pa = tmem + L::tmem_s(i);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     // 16 keys per step: P columns advance by 8 (two bf16 per
                     // 32-bit column), V rows by 16 * 128 bytes.
-                    umma_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + k * 8, vd + ((k * 2048) >> 4), IDESC_O,
-                            (accumulate || k > 0) ? 1u : 0u);
+                    umma_ts_lo(dst, pa + k * 8, v_lo + ((k * 2048) >> 4), v_hi, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(L::B_PVDONE + i));
             };

@@ -350,20 +350,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 // are formed once per operand; a k step adds its compile-time
                 // offset to the start-address field (no carry: smem < 256 KB).
                 const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
+                const uint32_t v1_lo = static_cast<uint32_t>(v1d), hi = static_cast<uint32_t>(v1d >> 32);
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ts(tmem + T_O, tmem + T_P + k * 8, v1d + ((k * 2048) >> 4), ID_INTRA, k > 0);
+                    umma_ts_lo(tmem + T_O, tmem + T_P + k * 8, v1_lo + ((k * 2048) >> 4), hi, ID_INTRA, k > 0);
                 // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
                 if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
                                         (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 if (c > 0 || has_prev) {
-                    const uint64_t sd = smem_desc_sw128(sbase + SPREV_OFF, 16, 1024);
+                    const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
-                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8, sd + (((k / 4) * SBOX + (k % 4) * 32) >> 4),
-                                ID_INTER, 1);
+                        umma_ts_lo(tmem + T_O, tmem + T_PHIQ + k * 8, s_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4), hi,
+                                   ID_INTER, 1);
                 }
                 umma_commit(bar(B_ODONE));
                 // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
@@ -371,11 +372,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                                         (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
-                const uint64_t pkd = smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024);
+                const uint32_t pk_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024));
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ss(tmem + T_ST, v1d + ((k * 2048) >> 4), pkd + ((k * 2048) >> 4), ID_STATE,
-                            (c > 0 || has_prev || k > 0) ? 1u : 0u);
+                    umma_ss_lo(tmem + T_ST, v1_lo + ((k * 2048) >> 4), hi, pk_lo + ((k * 2048) >> 4), hi, ID_STATE,
+                               (c > 0 || has_prev || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_VEMPTY + b));
             }

@@ -283,11 +283,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             const uint64_t wqd = smem_desc_sw128(sbase + WQ_OFF, WBOX, 1024), wkd = smem_desc_sw128(sbase + WK_OFF, WBOX, 1024);
             const uint64_t phikd = smem_desc_sw128(sbase + PHIK_OFF, 16, 1024), sprevd = smem_desc_sw128(sbase + SPREV_OFF, 16, 1024);
             const uint64_t phikmn = smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024);
+            const uint32_t hi = static_cast<uint32_t>(qd >> 32);  // every descriptor here has SBO 1024
+            const uint32_t q_lo = static_cast<uint32_t>(qd), k_lo = static_cast<uint32_t>(kd);
+            const uint32_t wq_lo = static_cast<uint32_t>(wqd), wk_lo = static_cast<uint32_t>(wkd);
+            const uint32_t phik_lo = static_cast<uint32_t>(phikd), sprev_lo = static_cast<uint32_t>(sprevd);
+            const uint32_t phikmn_lo = static_cast<uint32_t>(phikmn);
             auto issue_z = [&]() {  // Z = Q Wq, K Wk from the Q/K buffer, 16 of the 64 dims per step
 #pragma unroll
                 for (int k = 0; k < DQK / 16; ++k) {
-                    umma_ss(tmem + T_Z, qd + ((k * 32) >> 4), wqd + ((k * 2048) >> 4), ID_Z, k > 0);
-                    umma_ss(tmem + T_Z + FH, kd + ((k * 32) >> 4), wkd + ((k * 2048) >> 4), ID_Z, k > 0);
+                    umma_ss_lo(tmem + T_Z, q_lo + ((k * 32) >> 4), hi, wq_lo + ((k * 2048) >> 4), hi, ID_Z, k > 0);
+                    umma_ss_lo(tmem + T_Z + FH, k_lo + ((k * 32) >> 4), hi, wk_lo + ((k * 2048) >> 4), hi, ID_Z, k > 0);
                 }
                 umma_commit(bar(B_ZFULL));
                 umma_commit(bar(B_QKEMPTY));
@@ -295,7 +300,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features
 #pragma unroll
                 for (int k = 0; k < F / 16; ++k)
-                    umma_ts(tmem + T_Z, tmem + T_PHIQ + k * 8, phikd + (((k / 4) * BOX + (k % 4) * 32) >> 4), ID_S, k > 0);
+                    umma_ts_lo(tmem + T_Z, tmem + T_PHIQ + k * 8, phik_lo + (((k / 4) * BOX + (k % 4) * 32) >> 4), hi, ID_S,
+                               k > 0);
                 umma_commit(bar(B_SFULL));
             };
             bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16)) &&
@@ -329,23 +335,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]
-                const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
+                const uint32_t v1_lo = static_cast<uint32_t>(smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024));
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ts(tmem + T_O, tmem + T_P + k * 8, v1d + ((k * 2048) >> 4), ID_INTRA, k > 0);
+                    umma_ts_lo(tmem + T_O, tmem + T_P + k * 8, v1_lo + ((k * 2048) >> 4), hi, ID_INTRA, k > 0);
                 // inter: [num | den] += phi(Q) S_{<c}
                 if (c > 0 || has_prev) {
 #pragma unroll
                     for (int k = 0; k < F / 16; ++k)
-                        umma_ts(tmem + T_O, tmem + T_PHIQ + k * 8, sprevd + (((k / 4) * SBOX + (k % 4) * 32) >> 4),
-                                ID_INTER, 1);
+                        umma_ts_lo(tmem + T_O, tmem + T_PHIQ + k * 8, sprev_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4), hi,
+                                   ID_INTER, 1);
                 }
                 umma_commit(bar(B_ODONE));
                 // state: S^T += [V | 1]^T phi(K)
 #pragma unroll
                 for (int k = 0; k < C / 16; ++k)
-                    umma_ss(tmem + T_ST, v1d + ((k * 2048) >> 4), phikmn + ((k * 2048) >> 4), ID_STATE,
-                            (c > 0 || has_prev || k > 0) ? 1u : 0u);
+                    umma_ss_lo(tmem + T_ST, v1_lo + ((k * 2048) >> 4), hi, phikmn_lo + ((k * 2048) >> 4), hi, ID_STATE,
+                               (c > 0 || has_prev || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_STDONE));
                 umma_commit(bar(B_VEMPTY + b));
                 // S of the next chunk, once its features and this chunk's state are in smem
