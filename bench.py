@@ -181,9 +181,10 @@ class ClockSampler:
 
     A host thread queries NVML every ~2 ms between start (the constructor) and
     stop(), so even a timed region of a few milliseconds gets samples; the
-    samples also go to gpurun_out/clocks_gpu<i>.csv.  Where NVML cannot be
-    loaded it falls back to `nvidia-smi --loop-ms`, whose start-up takes
-    longer than short timed regions."""
+    samples also go to the CSV file named by TK_BENCH_CLOCKS_CSV, when set
+    (with `<i>` replaced by the GPU index).  Where NVML cannot be loaded it
+    falls back to `nvidia-smi --loop-ms`, whose start-up takes longer than
+    short timed regions."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -192,7 +193,14 @@ class ClockSampler:
     def __init__(self, gpu_index: int, interval_ms: int = 100):
         self.proc = None
         self.nvml = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        want = os.environ.get("TK_BENCH_CLOCKS_CSV")
+        self.keep = bool(want)
+        if want:
+            self.path = want.replace("<i>", str(gpu_index))
+        else:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="tk_clocks_", suffix=".csv")
+            os.close(fd)
         gpu_id = str(gpu_index)
         try:  # the UUID names the right GPU whatever CUDA_VISIBLE_DEVICES says
             import torch
@@ -201,7 +209,7 @@ class ClockSampler:
         except Exception:
             pass
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
         except OSError:
             pass
         try:
@@ -239,10 +247,13 @@ class ClockSampler:
         self.nvml.close()
         pts = list(self.samples)
         try:
-            with open(self.path, "w") as f:
-                f.write("t_s,sm_mhz,max_sm_mhz,reason_bits\n")
-                for t, mhz, bits in pts:
-                    f.write(f"{t:.6f},{mhz:.0f},{self.nvml.max_mhz:.0f},{bits:#x}\n")
+            if self.keep:
+                with open(self.path, "w") as f:
+                    f.write("t_s,sm_mhz,max_sm_mhz,reason_bits\n")
+                    for t, mhz, bits in pts:
+                        f.write(f"{t:.6f},{mhz:.0f},{self.nvml.max_mhz:.0f},{bits:#x}\n")
+            else:
+                os.remove(self.path)
         except OSError:
             pass
         if not pts:
@@ -282,6 +293,11 @@ class ClockSampler:
                 for n, val in zip(names, parts[5:9]):
                     if val.lower() == "active":
                         reasons.add(n)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sms:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
                     "source": "nvidia-smi"}
