@@ -271,6 +271,11 @@ class ClockSampler:
         if self.nvml is not None:
             return self._stop_nvml()
         if self.proc is None:
+            if not self.keep:
+                try:
+                    os.remove(self.path)
+                except OSError:
+                    pass
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
