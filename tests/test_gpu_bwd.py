@@ -108,3 +108,39 @@ def test_bwd_bench_workload_sampled(oracle_mod, idx, heads):
                 f"{w.name} head ({b},{h}) {name}: max err {err.max():.3e} vs max|ref| {np.abs(r).max():.3e}")
             assert err.mean() <= 0.01 * np.abs(r).mean() + 1e-5, (
                 f"{w.name} head ({b},{h}) {name}: mean err {err.mean():.3e}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal):
+    """Every dQ row is written and the accumulator is re-zeroed per call: dQ
+    and the workspace start as NaN bytes (0xFF), the workspace is used twice
+    in a row, and every dQ row must come out finite and equal to the
+    oracle's, over several heads, six query tiles (a ragged last one) and,
+    under the causal mask, 1 to 6 key tiles adding into a query tile."""
+    B, H, N, D = 2, 3, 700, 128
+    scale = 1.0 / math.sqrt(D)
+    q, k, v = make_qkv(B, H, N, D, 9400 + causal)
+    do = make_qkv(B, H, N, D, 9402 + causal)[0]
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, do))
+    o, lse = tk.fwd(qd, kd, vd, causal=causal, scale=scale)
+    ws = torch.full((tk.bwd_workspace_bytes(B, H, N, D),), 0xFF, dtype=torch.uint8, device="cuda")
+    lib = tk.load()
+    outs = []
+    for _ in range(2):
+        dq = torch.full_like(qd, float("nan"))
+        dk, dv = torch.empty_like(qd), torch.empty_like(qd)
+        rc = lib.tk_attn_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), gd.data_ptr(),
+                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                             ws.numel(), B, H, N, D, int(causal), scale, None)
+        assert rc == 0, tk.strerror(rc)
+        torch.cuda.synchronize()
+        status, detail = tk.device_status()
+        assert status == 0, f"device status {status} detail {detail:#x}"
+        outs.append(dq.cpu())
+    ref = oracle_mod.attn_bwd(q, k, v, do, causal, scale)[0]
+    for dq in outs:
+        g = dq.double().numpy()
+        assert np.all(np.isfinite(g)), f"dQ rows left unwritten: {np.argwhere(~np.isfinite(g))[:4]}"
+        err = np.abs(g - ref)
+        assert err.max() <= 0.02 * np.abs(ref).max() + 1e-4
+        assert err.mean() <= 0.01 * np.abs(ref).mean() + 1e-5
