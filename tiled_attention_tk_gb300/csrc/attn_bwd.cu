@@ -15,22 +15,22 @@
 // tcgen05 tensor cores.
 //
 // Three kernels on the caller's stream:
-//   bwd_prep_kernel    Delta_i = <dO_i, O_i> (fp32), one warp per row, and a
-//                      zeroed fp32 dQ accumulator.
+//   bwd_prep_kernel    -Delta_i = -<dO_i, O_i> (fp32) and -LSE_i * log2(e)
+//                      per padded query row; zeroes the fp32 dQ accumulator.
 //   attn_bwd_kernel<D> one CTA per (head, 128-key tile).  K_j and V_j stay in
 //                      shared memory and Q_i, dO_i of the query tiles that
 //                      see the keys stream through two buffers.  The MMA
 //                      warp forms S^T = K Q^T and dP^T = V dO^T in TMEM (one
-//                      key per TMEM lane); four compute warps turn them into
-//                      P^T and then dS^T, 32 queries at a time, written back
-//                      over them as bf16 (dS^T also into 128-byte-swizzled
-//                      shared memory).  The MMA warp accumulates
-//                      dV += P^T dO and dK += dS^T Q chunk by chunk with P^T
-//                      and dS^T read from TMEM, then forms dQ_part = dS K,
-//                      which the compute warps stage in shared memory and
-//                      add into the fp32 dQ accumulator with bulk (TMA)
-//                      reductions.  At the end dK and dV are written as bf16.
-//   bwd_dq_kernel      dQ = bf16(accumulator).
+//                      key per TMEM lane); two groups of four compute warps
+//                      turn them into P^T and then dS^T, 32 queries at a
+//                      time, written back over them as bf16 (dS^T also into
+//                      128-byte-swizzled shared memory).  The MMA warp
+//                      accumulates dV += P^T dO and dK += dS^T Q chunk by
+//                      chunk with P^T and dS^T read from TMEM, then forms
+//                      dQ_part = dS K, which four dQ warps add into the fp32
+//                      accumulator with vector reductions; at the end they
+//                      write dK and dV as bf16.
+//   bwd_dq_kernel      dQ = bf16(scale * accumulator).
 // The same shared-memory tiles serve as K-major and MN-major MMA operands
 // through different descriptors (Q and dO are K-major B operands of S^T and
 // dP^T and MN-major B operands of dK and dV).

@@ -9,11 +9,11 @@
 //   O_i   = sum_{j<=i} w_ij v_j / DEN_i,   DEN_i = sum_{j<=i} w_ij      (v_j in R^64)
 //
 // with phi(x) = [1, sqrt(scale) x, scale/sqrt(2) x_a^2, scale x_a x_b (a < b)]
-// (153 features, padded with zeros to F = 192).  The kernel runs the chunked
+// (153 features, padded with zeros to F = 160).  The kernel runs the chunked
 // linear form: one CTA per (batch, head) walks the sequence in chunks of 128
 // rows and keeps the running state
 //
-//   S^T = sum_j [v_j | 1] phi(k_j)^T      (65 live rows x 192 features, fp32 in TMEM)
+//   S^T = sum_j [v_j | 1] phi(k_j)^T      (65 live rows x 160 features, fp32 in TMEM)
 //
 // so that per chunk c, for the rows i of the chunk:
 //   intra:  [num | den]_i  = sum_{j in c, j<=i} w_ij [v_j | 1]     (tensor core: P [V | 1])
@@ -60,9 +60,9 @@ constexpr uint32_t BOX = 128 * 128;                   // 128 rows x 128 bytes
 constexpr uint32_t QK_OFF = 0;                        // buffer b: Q, K boxes at + b * 2 * BOX
 constexpr uint32_t V_OFF = QK_OFF + 4 * BOX;          // buffer b: V box at + b * BOX
 constexpr uint32_t ONES_OFF = V_OFF + 2 * BOX;        // [row][col]: 1 in column 0
-constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 192 features (3 boxes)
+constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 160 features (3 boxes, the last half used)
 constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
-constexpr uint32_t SPREV_OFF = PHIK_OFF + 3 * BOX;    // S (bf16, K-major): 80 rows x 192 features (3 boxes)
+constexpr uint32_t SPREV_OFF = PHIK_OFF + 3 * BOX;    // S (bf16, K-major): 80 rows x 160 features (3 boxes, the last half used)
 constexpr uint32_t OBOX = 32 * DV;                    // 32 rows x 64 bytes: one warp's O columns
 constexpr uint32_t OST_OFF = SPREV_OFF + 3 * SBOX;    // O staging: one 32 x 32 box per compute warp
 constexpr uint32_t BAR_OFF = OST_OFF + 8 * OBOX;
@@ -104,37 +104,64 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// phi(x) as 80 packed bf16 pairs: [1, r x_a (16), h x_a^2 (16),
-// g x_a x_b for a < b in order (120), 0 (7)].  Every index is a compile-time
-// constant once the loops are unrolled.
-__device__ __forceinline__ void phi_packed(const float (&x)[DQK], float r, float h, float g, uint32_t (&pk)[F / 2]) {
-    float f[F];
-    f[0] = 1.0f;
-#pragma unroll
-    for (int a = 0; a < DQK; ++a) f[1 + a] = r * x[a];
-#pragma unroll
-    for (int a = 0; a < DQK; ++a) f[17 + a] = h * x[a] * x[a];
-#pragma unroll
-    for (int a = 0; a < DQK; ++a)
-#pragma unroll
-        for (int b = a + 1; b < DQK; ++b) f[33 + a * 15 - a * (a - 1) / 2 + (b - a - 1)] = g * x[a] * x[b];
-#pragma unroll
-    for (int q = 153; q < F; ++q) f[q] = 0.0f;
-#pragma unroll
-    for (int e = 0; e < F / 2; ++e) pk[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+// Two bf16 products in one instruction (each rounded to nearest even).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// The 16 features of row r of a 128-byte-swizzled 128 x 64 bf16 box (its
-// first two 16-byte chunks).
-__device__ __forceinline__ void load_row16(uint32_t box, int r, float (&x)[DQK]) {
-    const uint4 lo = ld_shared_v4(sw128(box, r, 0));
-    const uint4 hi = ld_shared_v4(sw128(box, r, 1));
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+// phi(x) as 80 packed bf16 pairs, from x as 8 packed bf16 pairs
+// w[n] = (x_2n, x_2n+1).  The order of the features is the kernel's own
+// (phi(q) . phi(k) does not depend on it, and every phi here comes from this
+// function):
+//   word 0        (1, 0)
+//   words 1..8    r (x_2n, x_2n+1)
+//   words 9..16   h (x_2n^2, x_2n+1^2)
+//   words 17..20  g (x_4n x_4n+1, x_4n+2 x_4n+3)
+//   words 21..76  g x_a (x_2m, x_2m+1) for a = 0..13 and every m with 2m > a,
+//                 a-major: the 112 products x_a x_b (a < b) not above
+//   words 77..79  0
+// The first 21 words are formed in fp32 and rounded once.  Each of the other
+// 56 is one bf16x2 multiply of bf16(g x_a), broadcast to both halves, by the
+// input pair w[m], so those features carry two roundings.  Every index is a
+// compile-time constant once the loops are unrolled.
+__device__ __forceinline__ void phi_words(const uint32_t (&w)[DQK / 2], float r, float h, float g,
+                                          uint32_t (&pk)[F / 2]) {
+    float x[DQK];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        x[2 * e] = __uint_as_float(w[e] << 16);
-        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    for (int n = 0; n < DQK / 2; ++n) {
+        x[2 * n] = __uint_as_float(w[n] << 16);
+        x[2 * n + 1] = __uint_as_float(w[n] & 0xFFFF0000u);
     }
+    pk[0] = pack_bf16x2(1.0f, 0.0f);
+    const float2 r2 = make_float2(r, r), h2 = make_float2(h, h), g2 = make_float2(g, g);
+    float y[DQK];  // g x_a in fp32
+#pragma unroll
+    for (int n = 0; n < DQK / 2; ++n) {
+        const float2 xp = make_float2(x[2 * n], x[2 * n + 1]);
+        const float2 lin = __fmul2_rn(r2, xp);
+        const float2 sq = __fmul2_rn(__fmul2_rn(h2, xp), xp);
+        const float2 yp = __fmul2_rn(g2, xp);
+        pk[1 + n] = pack_bf16x2(lin.x, lin.y);
+        pk[9 + n] = pack_bf16x2(sq.x, sq.y);
+        y[2 * n] = yp.x;
+        y[2 * n + 1] = yp.y;
+    }
+#pragma unroll
+    for (int n = 0; n < DQK / 4; ++n) {
+        const float2 u = __fmul2_rn(make_float2(y[4 * n], y[4 * n + 2]), make_float2(x[4 * n + 1], x[4 * n + 3]));
+        pk[17 + n] = pack_bf16x2(u.x, u.y);
+    }
+    int k = 21;
+#pragma unroll
+    for (int a = 0; a < DQK - 2; ++a) {
+        const uint32_t ya = pack_bf16x2(y[a], y[a]);
+#pragma unroll
+        for (int m = a / 2 + 1; m < DQK / 2; ++m) pk[k++] = mul_bf16x2(ya, w[m]);
+    }
+#pragma unroll
+    for (; k < F / 2; ++k) pk[k] = 0u;
 }
 
 // phi of one row (16 features from a swizzled box) into the feature parts of
@@ -144,14 +171,15 @@ __device__ __forceinline__ void load_row16(uint32_t box, int r, float (&x)[DQK])
 template <int PARTS, bool TO_TMEM>
 __device__ __forceinline__ void phi_store(uint32_t box16, int r, bool live, float rs, float hs, float gs,
                                           uint32_t dst) {
-    float x[DQK];
-    load_row16(box16, r, x);
+    const uint4 lo = ld_shared_v4(sw128(box16, r, 0));
+    const uint4 hi = ld_shared_v4(sw128(box16, r, 1));
+    uint32_t w[DQK / 2] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     if (!live) {
 #pragma unroll
-        for (int a = 0; a < DQK; ++a) x[a] = 0.0f;
+        for (int n = 0; n < DQK / 2; ++n) w[n] = 0u;
     }
     uint32_t pk[F / 2];
-    phi_packed(x, rs, hs, gs, pk);
+    phi_words(w, rs, hs, gs, pk);
     if (!live) pk[0] = 0u;
 #pragma unroll
     for (int part = 0; part < 3; ++part) {
@@ -447,13 +475,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 tmem_ld64(lane_base + T_S + grp * 64, sr);
                 tc_fence_before_sync();
                 warp_arrive(bar(B_SREAD), lane);
+                // w = 1 + c t + (c^2 / 2) t^2 for the raw score t, in Horner form:
+                // two packed FMAs per pair of keys
                 const float2 sc2 = make_float2(scale, scale), one2 = make_float2(1.0f, 1.0f),
-                             half2 = make_float2(0.5f, 0.5f);
+                             hc2 = make_float2(0.5f * scale * scale, 0.5f * scale * scale);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int j0 = grp * 64 + 2 * e;
-                    const float2 s2 = __fmul2_rn(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sc2);
-                    const float2 w2 = __ffma2_rn(__fmul2_rn(half2, s2), s2, __fadd2_rn(s2, one2));
+                    const float2 t2 = make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+                    const float2 w2 = __ffma2_rn(t2, __ffma2_rn(t2, hc2, sc2), one2);
                     pk[e] = pack_bf16x2(j0 <= jmax ? w2.x : 0.0f, j0 + 1 <= jmax ? w2.y : 0.0f);
                 }
             }
