@@ -463,17 +463,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 break;
             tc_fence_after_sync();
             {
-                const int jmax = min(i, p.N - 1 - (c0 + c) * C);
-                uint32_t sr[64];
-                tmem_ld64(lane_base + T_Z + grp * 64, sr);
-                tc_fence_before_sync();
-                warp_arrive(bar(B_SREAD), lane);
+                const int lim = p.N - 1 - (c0 + c) * C;  // last key of the chunk (j < N)
+                const int jmax = min(i, lim);              // last key of the chunk this row sees
+                // Per warp (rows r0 .. r0+31) and group (keys k0 .. k0+63): every key
+                // hidden, every key seen, or a mix (the diagonal block, a ragged tail)
+                const int r0 = (warp % 4) * 32, k0 = grp * 64;
+                const int jlo = min(r0, lim), jhi = min(r0 + 31, lim);
                 uint32_t pk[32];
+                if (jhi < k0) {
+                    tc_fence_before_sync();
+                    warp_arrive(bar(B_SREAD), lane);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j0 = grp * 64 + 2 * e;
-                    pk[e] = pack_bf16x2(j0 <= jmax ? __uint_as_float(sr[2 * e]) : 0.0f,
-                                        j0 + 1 <= jmax ? __uint_as_float(sr[2 * e + 1]) : 0.0f);
+                    for (int e = 0; e < 32; ++e) pk[e] = 0u;
+                } else {
+                    uint32_t sr[64];
+                    tmem_ld64(lane_base + T_Z + grp * 64, sr);
+                    tc_fence_before_sync();
+                    warp_arrive(bar(B_SREAD), lane);
+                    if (jlo >= k0 + 63) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            pk[e] = pack_bf16x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int j0 = k0 + 2 * e;
+                            pk[e] = pack_bf16x2(j0 <= jmax ? __uint_as_float(sr[2 * e]) : 0.0f,
+                                                j0 + 1 <= jmax ? __uint_as_float(sr[2 * e + 1]) : 0.0f);
+                        }
+                    }
                 }
                 tmem_st32(lane_base + T_P + grp * 32, pk);
             }
