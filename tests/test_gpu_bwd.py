@@ -110,17 +110,19 @@ def test_bwd_bench_workload_sampled(oracle_mod, idx, heads):
                 f"{w.name} head ({b},{h}) {name}: mean err {err.mean():.3e}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal):
+def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal, D):
     """Every dQ row is written and the accumulator is re-zeroed per call: dQ
     and the workspace start as NaN bytes (0xFF), the workspace is used twice
     in a row, and every dQ row must come out finite and equal to the
     oracle's, over several heads, six query tiles (a ragged last one) and,
-    under the causal mask, 1 to 6 key tiles adding into a query tile."""
-    B, H, N, D = 2, 3, 700, 128
+    under the causal mask, 1 to 6 key tiles adding into a query tile; at
+    D = 64 (bulk reductions of staged tiles) and D = 128 (vector reductions)."""
+    B, H, N = 2, 3, 700
     scale = 1.0 / math.sqrt(D)
-    q, k, v = make_qkv(B, H, N, D, 9400 + causal)
-    do = make_qkv(B, H, N, D, 9402 + causal)[0]
+    q, k, v = make_qkv(B, H, N, D, 9400 + causal + D)
+    do = make_qkv(B, H, N, D, 9402 + causal + D)[0]
     qd, kd, vd, gd = (t.cuda() for t in (q, k, v, do))
     o, lse = tk.fwd(qd, kd, vd, causal=causal, scale=scale)
     ws = torch.full((tk.bwd_workspace_bytes(B, H, N, D),), 0xFF, dtype=torch.uint8, device="cuda")

@@ -28,8 +28,9 @@
 //                      accumulates dV += P^T dO and dK += dS^T Q chunk by
 //                      chunk with P^T and dS^T read from TMEM, then forms
 //                      dQ_part = dS K, which four dQ warps add into the fp32
-//                      accumulator with vector reductions; at the end they
-//                      write dK and dV as bf16.
+//                      accumulator with vector reductions (at D = 64: staged
+//                      in shared memory, one bulk reduction per tile); at the
+//                      end they write dK and dV as bf16.
 //   bwd_dq_kernel      dQ = bf16(scale * accumulator).
 // The same shared-memory tiles serve as K-major and MN-major MMA operands
 // through different descriptors (Q and dO are K-major B operands of S^T and
@@ -73,7 +74,14 @@ struct Layout {
     // Per Q/dO buffer b, the query tile's row values: -LSE*log2(e) at
     // RB_OFF + b * 1024 and -Delta 512 bytes further (128 floats each).
     static constexpr uint32_t RB_OFF = DS_OFF + 2 * BOX;
-    static constexpr uint32_t BAR_OFF = RB_OFF + 2048;
+    // D = 64 leaves room for two fp32 staging copies of dQ_part, laid out like
+    // an accumulator tile ([D/4][128 rows][4]); each goes out as one bulk
+    // reduction (the TMA unit adds it into L2) instead of the dQ warps'
+    // vector reductions.  D = 128 has no room and keeps the vector reductions.
+    static constexpr bool DQ_BULK = D == 64;
+    static constexpr uint32_t DQST_BYTES = BT * D * 4;
+    static constexpr uint32_t DQST_OFF = RB_OFF + 2048;
+    static constexpr uint32_t BAR_OFF = DQST_OFF + (DQ_BULK ? 2 * DQST_BYTES : 0);
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;      // + buffer (2): Q and dO loaded
     static constexpr int B_QEMPTY = 3;     // + buffer (2): the products that read them are done (MMA commit)
@@ -84,7 +92,9 @@ struct Layout {
     static constexpr int B_GDONE = 15;     // dQ_part product done (MMA commit)
     static constexpr int B_DQREAD = 16;    // dQ_part read out of TMEM (dQ warps, 4)
     static constexpr int B_MMADONE = 17;
-    static constexpr int NUM_BARS = 18;
+    static constexpr int B_STAGED = 18;    // + buffer (2): dQ_part staged (dQ warps, 4)
+    static constexpr int B_STAGEFREE = 20; // + buffer (2): its bulk reduction has read it (one thread)
+    static constexpr int NUM_BARS = 22;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     // No alignment slack: the dynamic shared memory of a kernel without
     // static shared memory starts 1024-byte aligned (the kernel checks).
@@ -123,6 +133,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+// Adds `bytes` (a multiple of 16) of fp32 from shared memory into global
+// memory with the bulk-copy unit, in the current bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Waits until every bulk group but the newest has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -193,6 +216,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         mbar_init(bar(L::B_GDONE), 1);
         mbar_init(bar(L::B_DQREAD), 4);
         mbar_init(bar(L::B_MMADONE), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_STAGED + b), 4);
+            mbar_init(bar(L::B_STAGEFREE + b), 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -475,6 +502,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         // ------------------------------------------------ dQ warps
         const int t = (warp - WARP_DQ) * 32 + lane;  // TMEM lane: query row t (dQ_part), key row t (dK, dV)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - WARP_DQ) * 32) << 16);
+        const bool issuer = warp == WARP_DQ && lane == 0;  // issues the bulk reductions (D = 64)
+        int bulk_issued = 0;
         bool ok = true;
         for (int it = 0; it < n_q; ++it) {
             const int qt = qt_first + it;
@@ -482,30 +511,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                                     (ROLE_BWD_COMPUTE << 24) | (L::B_GDONE << 16) | it)))
                 break;
             tc_fence_after_sync();
-            // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
-            // reduction of one 4-column group covers 512 contiguous bytes.
-            float *dq_tile = p.dq_acc + (head_tiles + qt) * BT * D + t * 4;
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
+            if constexpr (L::DQ_BULK) {
+                // dQ_part into staging buffer it & 1 ([D/4][128 rows][4], the
+                // accumulator's layout), then one bulk reduction of the tile.
                 uint32_t r0[32], r1[32];
-                tmem_ld32_async(lane_base + L::T_DQ + 64 * h, r0);
-                tmem_ld32_async(lane_base + L::T_DQ + 64 * h + 32, r1);
+                tmem_ld32_async(lane_base + L::T_DQ, r0);
+                tmem_ld32_async(lane_base + L::T_DQ + 32, r1);
                 tmem_ld_wait();
                 reg_fence(r0);
                 reg_fence(r1);
-                if (h == D / 64 - 1) {
-                    tc_fence_before_sync();
-                    warp_arrive(bar(L::B_DQREAD), lane);
+                tc_fence_before_sync();
+                warp_arrive(bar(L::B_DQREAD), lane);
+                const int b = it & 1;
+                if (it >= 2 && !(ok = wait_bounded(bar(L::B_STAGEFREE + b), ((it >> 1) - 1) & 1, abort_flag,
+                                                   (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGEFREE + b) << 16) | it)))
+                    break;
+                const uint32_t stage = sbase + L::DQST_OFF + b * L::DQST_BYTES + t * 16;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    st_shared_v4(stage + g * BT * 16, r0[4 * g], r0[4 * g + 1], r0[4 * g + 2], r0[4 * g + 3]);
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    st_shared_v4(stage + (8 + g) * BT * 16, r1[4 * g], r1[4 * g + 1], r1[4 * g + 2], r1[4 * g + 3]);
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk-copy unit
+                warp_arrive(bar(L::B_STAGED + b), lane);
+                if (issuer) {
+                    if ((ok = wait_bounded(bar(L::B_STAGED + b), (it >> 1) & 1, abort_flag,
+                                           (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGED + b) << 16) | it))) {
+                        bulk_reduce_add_f32(p.dq_acc + (head_tiles + qt) * BT * D,
+                                            sbase + L::DQST_OFF + b * L::DQST_BYTES, L::DQST_BYTES);
+                        tma_store_commit();
+                        ++bulk_issued;
+                        if (it >= 1) {
+                            // the previous tile's reduction has read its buffer
+                            bulk_wait_read_all_but_one();
+                            mbar_arrive(bar(L::B_STAGEFREE + (b ^ 1)));
+                        }
+                    }
                 }
+                __syncwarp();
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the issuer's verdict holds for its warp
+                if (!ok) break;
+            } else {
+                // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
+                // reduction of one 4-column group covers 512 contiguous bytes.
+                float *dq_tile = p.dq_acc + (head_tiles + qt) * BT * D + t * 4;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    red_add_v4(dq_tile + (16 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+                for (int h = 0; h < D / 64; ++h) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32_async(lane_base + L::T_DQ + 64 * h, r0);
+                    tmem_ld32_async(lane_base + L::T_DQ + 64 * h + 32, r1);
+                    tmem_ld_wait();
+                    reg_fence(r0);
+                    reg_fence(r1);
+                    if (h == D / 64 - 1) {
+                        tc_fence_before_sync();
+                        warp_arrive(bar(L::B_DQREAD), lane);
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    red_add_v4(dq_tile + (16 * h + 8 + j) * BT * 4, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
-                               r1[4 * j + 3]);
+                    for (int j = 0; j < 8; ++j)
+                        red_add_v4(dq_tile + (16 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
+                                   r0[4 * j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        red_add_v4(dq_tile + (16 * h + 8 + j) * BT * 4, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
+                                   r1[4 * j + 3]);
+                }
             }
         }
+        // The bulk reductions complete before the CTA (and its shared memory) goes away.
+        if (issuer && bulk_issued > 0) tma_store_wait_all();
+        __syncwarp();
         if (ok) {
             // dK = scale * (dS'^T Q), dV of this key tile (lane t = key).
             // The last GDONE wait covers every product.
