@@ -469,7 +469,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             tc_fence_after_sync();
             // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this group's 64 keys
             uint32_t pk[32];
-            {
+            if (grp == 1 && warp % 4 < 2) {
+                // rows 0..63 see none of keys 64..127: nothing to read
+                tc_fence_before_sync();
+                warp_arrive(bar(B_SREAD), lane);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = 0u;
+            } else {
                 const int jmax = min(i, p.N - 1 - (c0 + c) * C);  // last key of the chunk this row sees
                 uint32_t sr[64];
                 tmem_ld64(lane_base + T_S + grp * 64, sr);
