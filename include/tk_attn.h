@@ -72,7 +72,7 @@ enum {
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 1.
  *            Any N >= 1: the last key tile is masked, the last query tile's
  *            extra rows are neither computed into nor stored.
- *   D        head dimension: 32, 64, 96 or 128 (the backward: 64 or 128).
+ *   D        head dimension: 32, 64, 96, 128 or 256 (the backward: 64 or 128).
  *   causal   0: every query sees every key; 1: query i sees keys j <= i.
  *   scale    multiplier of Q K^T, finite and > 0 (usually 1/sqrt(D)).
  *   stream   CUDA stream the kernel is enqueued on (0 = legacy default).

@@ -60,7 +60,8 @@ def _call(q=Bq, k=Bk, v=Bv, o=Bo, l=Bl, B=1, H=1, N=128, D=64, causal=0, scale=0
     (dict(N=2**31), "TK_ERR_BAD_SHAPE"),
     (dict(B=2**20, H=2**20, N=2**20, D=128), "TK_ERR_BAD_SHAPE"),
     (dict(D=80), "TK_ERR_UNSUPPORTED_D"),
-    (dict(D=256), "TK_ERR_UNSUPPORTED_D"),
+    (dict(D=192), "TK_ERR_UNSUPPORTED_D"),
+    (dict(D=512), "TK_ERR_UNSUPPORTED_D"),
     (dict(causal=2), "TK_ERR_BAD_FLAG"),
     (dict(scale=0.0), "TK_ERR_BAD_SCALE"),
     (dict(scale=-1.0), "TK_ERR_BAD_SCALE"),

@@ -38,7 +38,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     """Fused attention forward.
 
     q: bf16 [B, H, Nq, D]; k, v: bf16 [B, H, Nkv, D] (Nkv = Nq usually), D
-    in {64, 128}.  Returns (O bf16 [B,H,Nq,D], LSE fp32 [B,H,Nq]) with
+    in {32, 64, 96, 128, 256}.  Returns (O bf16 [B,H,Nq,D], LSE fp32 [B,H,Nq]) with
     O = softmax(scale QK^T [+causal]) V and LSE the natural-log row
     log-sum-exp.  Under the causal mask the queries stand at the end of the
     key sequence (query i sees keys j <= i + Nkv - Nq; needs Nkv >= Nq).

@@ -22,7 +22,7 @@ LIB_NAME = "libtk_attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "gemm.cu", "based.cu", "hedgehog.cu", "tk_attn_api.cpp"]
+SOURCES = ["attn_fwd.cu", "attn_fwd256.cu", "attn_bwd.cu", "gemm.cu", "based.cu", "hedgehog.cu", "tk_attn_api.cpp"]
 
 
 def _nvcc() -> str:

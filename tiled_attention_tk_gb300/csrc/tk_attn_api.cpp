@@ -259,7 +259,7 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     // ---- host-side validation: nothing is enqueued unless all of it passes
     if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
     if (B < 1 || H < 1 || Nq < 1 || Nkv < 1) return TK_ERR_BAD_SHAPE;
-    if (D != 32 && D != 64 && D != 96 && D != 128) return TK_ERR_UNSUPPORTED_D;
+    if (D != 32 && D != 64 && D != 96 && D != 128 && D != 256) return TK_ERR_UNSUPPORTED_D;
     // TMA coordinates and the launch grid are 32-bit.
     if (Nq > INT32_MAX || Nkv > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
     const int64_t BH = B * H;
@@ -308,7 +308,8 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     p.scale = scale;
     p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
-    cudaError_t e = tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
+    cudaError_t e = D == 256 ? tk::launch_attn_fwd256(p, num_sms, stream)
+                             : tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
 }
@@ -710,9 +711,19 @@ int tk_attn_device_status(cudaStream_t stream, uint32_t *detail) {
     if (e != cudaSuccess) return fail_cuda(e);
     e = tk::read_and_clear_hedgehog_status(&status_h, &where_h);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (detail) *detail = status ? where : (status_b ? where_b : (status_g ? where_g : (status_l ? where_l : where_h)));
-    return (status == 0 && status_b == 0 && status_g == 0 && status_l == 0 && status_h == 0) ? TK_OK
-                                                                                             : TK_ERR_DEVICE_TIMEOUT;
+    uint32_t status_w = 0, where_w = 0;
+    e = tk::read_and_clear_fwd256_status(&status_w, &where_w);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (detail)
+        *detail = status     ? where
+                  : status_b ? where_b
+                  : status_g ? where_g
+                  : status_l ? where_l
+                  : status_h ? where_h
+                             : where_w;
+    return (status == 0 && status_b == 0 && status_g == 0 && status_l == 0 && status_h == 0 && status_w == 0)
+               ? TK_OK
+               : TK_ERR_DEVICE_TIMEOUT;
 }
 
 int tk_attn_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {

@@ -128,8 +128,13 @@ cudaError_t noalloc_workspace(void **ptr);
 // Reads and clears the backward translation unit's status word (no sync).
 cudaError_t read_and_clear_bwd_status(uint32_t *status, uint32_t *detail);
 
-// Launches the fused forward kernel for head dim D (64 or 128).
+// Launches the fused forward kernel for head dim D (32, 64, 96 or 128).
 cudaError_t launch_attn_fwd(int D, const AttnParams &p, int num_sms, cudaStream_t stream);
+
+// The forward at head dim 256 (attn_fwd256.cu: one Q tile per unit, two S
+// slots), and its device status word.
+cudaError_t launch_attn_fwd256(const AttnParams &p, int num_sms, cudaStream_t stream);
+cudaError_t read_and_clear_fwd256_status(uint32_t *status, uint32_t *detail);
 
 // Launches the one-CTA bounded-wait self test.
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
