@@ -40,37 +40,45 @@
 namespace tk {
 namespace fwd256 {
 
-constexpr int D = 256;
 constexpr int BM = 128;            // query rows per unit (one TMEM lane each)
 constexpr int BN = 128;            // keys per key tile
-constexpr int KATOMS = D / 64;     // 64-column boxes (128-byte swizzle atoms) along D
 constexpr int NUM_THREADS = 192;   // softmax warpgroup, MMA warp, TMA warp
 constexpr int WARP_MMA = 4;
 constexpr int WARP_TMA = 5;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kRescaleLog2 = 24.0f;  // as attn_fwd.cu: P < 2^24 between rescales
+constexpr uint32_t BOX_BYTES = 128 * 64 * 2;  // one TMA box: 128 rows x 64 bf16
 
-constexpr uint32_t BOX_BYTES = 128 * 64 * 2;          // one TMA box: 128 rows x 64 bf16
-constexpr uint32_t TILE_BYTES = KATOMS * BOX_BYTES;   // a 128 x 256 tile: 64 KB
-constexpr uint32_t Q_OFF = 0;
-constexpr uint32_t SLOT_OFF = TILE_BYTES;             // two K/V slots
-constexpr uint32_t STAGE_OFF = SLOT_OFF + 2 * TILE_BYTES;  // O staging: one 128 x 64 box
-constexpr uint32_t BAR_OFF = STAGE_OFF + BOX_BYTES;
-constexpr int B_QFULL = 0;
-constexpr int B_QEMPTY = 1;        // the unit's last S product is done
-constexpr int B_SLOTFULL = 2;      // + slot (2)
-constexpr int B_SLOTEMPTY = 4;     // + slot (2): the product reading it is done
-constexpr int B_SFULL = 6;         // + S slot (2)
-constexpr int B_PFULL = 8;         // + S slot (2): P in the slot (4 warps)
-constexpr int B_PVDONE = 10;       // O += P V done
-constexpr int B_OFREE = 11;        // O read out by the epilogue (4 warps)
-constexpr int B_WGSYNC = 12;       // warpgroup-internal sync (4 warps)
-constexpr int B_MMADONE = 13;
-constexpr int NUM_BARS = 14;
-constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
-static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
-// TMEM columns: S slot s at 128 s, O at 256
+template <int D>
+struct Layout {
+    static constexpr int KATOMS = D / 64;                  // 64-column boxes along D
+    static constexpr uint32_t TILE_BYTES = KATOMS * BOX_BYTES;  // a 128 x D tile
+    static constexpr int NSLOTS = D == 256 ? 2 : 4;        // K/V slots
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t SLOT_OFF = TILE_BYTES;
+    static constexpr uint32_t STAGE_OFF = SLOT_OFF + NSLOTS * TILE_BYTES;  // O staging: one 128 x 64 box
+    static constexpr uint32_t BAR_OFF = STAGE_OFF + BOX_BYTES;
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_QEMPTY = 1;                     // the unit's last S product is done
+    static constexpr int B_SLOTFULL = 2;                   // + slot
+    static constexpr int B_SLOTEMPTY = B_SLOTFULL + NSLOTS;  // + slot: the product reading it is done
+    static constexpr int B_SFULL = B_SLOTEMPTY + NSLOTS;   // + S slot (2)
+    static constexpr int B_PFULL = B_SFULL + 2;            // + S slot (2): P in the slot (4 warps)
+    static constexpr int B_PVDONE = B_PFULL + 2;           // O += P V done
+    static constexpr int B_OFREE = B_PVDONE + 1;           // O read out by the epilogue (4 warps)
+    static constexpr int B_WGSYNC = B_OFREE + 1;           // warpgroup-internal sync (4 warps)
+    static constexpr int B_MMADONE = B_WGSYNC + 1;
+    static constexpr int NUM_BARS = B_MMADONE + 1;
+    static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+    // Built for 256.  At 128 the same plan (four K/V slots) measured 11 %
+    // slower than attn_fwd.cu's two Q tiles per unit: with one softmax
+    // warpgroup the softmax, not the tensor core, then sets the pace.
+    static_assert(D == 128 || D == 256, "head dim 128 or 256");
+    static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+    static_assert(SMEM_ALLOC > 116u * 1024u, "one CTA per SM: each CTA holds all 512 TMEM columns");
+};
+// TMEM columns: S slot s at 128 s, O at 256 (D columns)
 __host__ __device__ constexpr uint32_t tmem_s(uint32_t s) { return s * 128u; }
 constexpr uint32_t T_O = 256;
 
@@ -98,7 +106,16 @@ __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
     return min(last_key / BN + 1, p.n_kvtiles);
 }
 
+template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __grid_constant__ AttnParams p) {
+    using L = Layout<D>;
+    constexpr int KATOMS = L::KATOMS, NSLOTS = L::NSLOTS;
+    constexpr uint32_t TILE_BYTES = L::TILE_BYTES, Q_OFF = L::Q_OFF, SLOT_OFF = L::SLOT_OFF,
+                       STAGE_OFF = L::STAGE_OFF, BAR_OFF = L::BAR_OFF;
+    constexpr int B_QFULL = L::B_QFULL, B_QEMPTY = L::B_QEMPTY, B_SLOTFULL = L::B_SLOTFULL,
+                  B_SLOTEMPTY = L::B_SLOTEMPTY, B_SFULL = L::B_SFULL, B_PFULL = L::B_PFULL,
+                  B_PVDONE = L::B_PVDONE, B_OFREE = L::B_OFREE, B_WGSYNC = L::B_WGSYNC,
+                  B_MMADONE = L::B_MMADONE, NUM_BARS = L::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -121,9 +138,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QFULL), 1);
         mbar_init(bar(B_QEMPTY), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSLOTS; ++s) {
             mbar_init(bar(B_SLOTFULL + s), 1);
             mbar_init(bar(B_SLOTEMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_SFULL + s), 1);
             mbar_init(bar(B_PFULL + s), 4);
         }
@@ -155,9 +174,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                 const Unit u = unit_at(idx, p);
                 const int n_kv = kv_tiles(u.qt, p);
                 auto load_kv = [&](int j, bool v) -> bool {
-                    const int s = loads & 1;
-                    if (loads >= 2 && !wait_bounded(bar(B_SLOTEMPTY + s), ((loads >> 1) - 1) & 1, abort_flag,
-                                                    (ROLE_PRODUCER << 24) | ((B_SLOTEMPTY + s) << 16) | (j & 0xFFFF)))
+                    const int s = loads % NSLOTS;
+                    if (loads >= static_cast<uint32_t>(NSLOTS) &&
+                        !wait_bounded(bar(B_SLOTEMPTY + s), ((loads / NSLOTS) - 1) & 1, abort_flag,
+                                      (ROLE_PRODUCER << 24) | ((B_SLOTEMPTY + s) << 16) | (j & 0xFFFF)))
                         return false;
                     const uint32_t dst = sbase + SLOT_OFF + s * TILE_BYTES;
                     mbar_arrive_expect_tx(bar(B_SLOTFULL + s), TILE_BYTES);
@@ -186,10 +206,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
             }
             if (!ok) {
                 // Let the copies in flight land before the CTA exits.
-                const uint32_t first = loads > 2 ? loads - 2 : 0;
+                const uint32_t first = loads > static_cast<uint32_t>(NSLOTS) ? loads - NSLOTS : 0;
                 for (uint32_t n = first; n < loads; ++n) {
                     const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bar(B_SLOTFULL + (n & 1)), (n >> 1) & 1) &&
+                    while (!mbar_try_wait(bar(B_SLOTFULL + n % NSLOTS), (n / NSLOTS) & 1) &&
                            global_timer_ns() - t0 < kDrainLimitNs) {
                     }
                 }
@@ -211,8 +231,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
             bool ok = true;
             int k_unit = 0;
             auto take_slot = [&](uint32_t &slot) -> bool {
-                slot = taken & 1;
-                const bool r = wait_bounded(bar(B_SLOTFULL + slot), (taken >> 1) & 1, abort_flag,
+                slot = taken % NSLOTS;
+                const bool r = wait_bounded(bar(B_SLOTFULL + slot), (taken / NSLOTS) & 1, abort_flag,
                                             (ROLE_MMA << 24) | ((B_SLOTFULL + slot) << 16) | (taken & 0xFFFF));
                 ++taken;
                 return r;
@@ -457,17 +477,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
     }
 }
 
-}  // namespace fwd256
-
-cudaError_t launch_attn_fwd256(const AttnParams &p, int num_sms, cudaStream_t stream) {
-    if (num_sms < 1) return cudaErrorInvalidValue;
+template <int D>
+static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t stream) {
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        err = cudaFuncSetAttribute(fwd256::attn_fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   fwd256::SMEM_ALLOC);
+        err = cudaFuncSetAttribute(attn_fwd256_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Layout<D>::SMEM_ALLOC);
         if (err != cudaSuccess) return err;
         configured_device = dev;
     }
@@ -475,10 +493,17 @@ cudaError_t launch_attn_fwd256(const AttnParams &p, int num_sms, cudaStream_t st
     const long long blocks = units < num_sms ? units : num_sms;  // persistent: <= one CTA per SM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-    cfg.blockDim = dim3(fwd256::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = fwd256::SMEM_ALLOC;
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Layout<D>::SMEM_ALLOC;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, fwd256::attn_fwd256_kernel, p);
+    return cudaLaunchKernelEx(&cfg, attn_fwd256_kernel<D>, p);
+}
+
+}  // namespace fwd256
+
+cudaError_t launch_attn_fwd256(const AttnParams &p, int num_sms, cudaStream_t stream) {
+    if (num_sms < 1) return cudaErrorInvalidValue;
+    return fwd256::launch_d<256>(p, num_sms, stream);
 }
 
 cudaError_t read_and_clear_fwd256_status(uint32_t *status, uint32_t *detail) {
