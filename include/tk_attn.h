@@ -123,8 +123,8 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
  * tiles (B*H*ceil(N/128)*128*D floats) and two fp32 row values over the
  * same padded rows, Delta_i = <dO_i, O_i> and -LSE_i*log2(e); each section
  * 256-byte aligned.
- * Returns 0 for shapes tk_attn_fwd would reject as TK_ERR_BAD_SHAPE or
- * TK_ERR_UNSUPPORTED_D.
+ * Returns 0 for shapes tk_attn_bwd rejects: TK_ERR_BAD_SHAPE, or a head dim
+ * other than 64 and 128 (TK_ERR_UNSUPPORTED_D).
  */
 size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
 
