@@ -57,3 +57,24 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     args = type("A", (), {"steps": 1, "warmup": 3, "reference_budget": 1.0})()
     from tiled_attention_tk_gb300.inputs import WORKLOADS
     assert bench.run_reference(args, WORKLOADS[1]) is None
+
+
+def test_reference_arm_line_on_rank0(monkeypatch):
+    """On rank 0 the reference arm times the oracle on the host and returns
+    the contract's line: the metric, a positive value, impl "reference", a
+    cpu_baseline describing this run and an e2e entry with no copies."""
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    import bench
+    from tiled_attention_tk_gb300.inputs import WORKLOADS
+    args = type("A", (), {"steps": 2, "warmup": 3, "reference_budget": 0.5})()
+    line = bench.run_reference(args, WORKLOADS[1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["gpu_launches"] == 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == WORKLOADS[1].name
