@@ -14,24 +14,30 @@
 // tiles, register accumulators, wgmma, two pipeline stages, one CTA per Q
 // block) is replaced by a Blackwell one.  A persistent CTA per SM walks a
 // list of work units; a unit is one head and a pair of consecutive 128-row Q
-// tiles, Q0 and Q1.  Roles:
-//   warp 9      TMA producer: Q0 and Q1 once per unit, then K_j and V_j into
-//               separate slots of a shared-memory ring (full/empty mbarriers).
-//   warp 8      MMA issuer (one thread): S_i = Q_i K_j^T (tcgen05.mma, smem x
-//               smem -> TMEM fp32) and O_i += P_i V_j (P_i read from TMEM, V
-//               from smem) into O_i in TMEM, ordered S0, S1, PV0, S0', PV1,
-//               S1', ... so the tensor core works on one Q tile while the
-//               other tile's softmax runs.  Also owns TMEM.
+// tiles, Q0 and Q1.  Roles (512 threads, registers reallocated per
+// warpgroup):
+//   warp 13     TMA producer: Q0 and Q1 once per unit (each reloaded as soon
+//               as the unit's last S of that tile is done), then K_j and V_j
+//               into separate slots of a shared-memory ring (full/empty
+//               mbarriers).
+//   warp 12     MMA issuer: S_i = Q_i K_j^T (tcgen05.mma, smem x smem -> TMEM
+//               fp32) and O_i += P_i V_j (P_i read from TMEM, V from smem)
+//               into O_i in TMEM, ordered S0, S1, PV0, S0', PV1, S1', ... so
+//               the tensor core works on one Q tile while the other tile's
+//               softmax runs.  The order runs on across units: a unit's last
+//               P V of a tile is followed by the next unit's first S of it.
+//               Also owns TMEM.
 //   warps 0-3   softmax warpgroup of Q0, warps 4-7 of Q1: thread t owns query
 //               row t of its tile (TMEM lane t); reads its S row with
-//               tcgen05.ld, masks the last key tile, takes the row max,
-//               writes P = exp2(c*s - c*m_ref) as bf16 over the S columns,
-//               updates l, rescales its O row only when the row max has grown
-//               by more than 2^8 since the reference max was set (lazy
-//               rescale; O and l always share the same reference, so the
-//               result is exact), and at the end of the unit writes O / l
-//               (bf16) and LSE while the MMA warp already starts the next
-//               unit.
+//               tcgen05.ld, masks the key tiles its rows see in part, takes
+//               the row max, writes P = exp2(c*s - c*m_ref) as bf16 over the
+//               S columns, updates l, rescales its O row only when the row
+//               max has grown by more than 2^24 since the reference max was
+//               set (lazy rescale; O and l always share the same reference,
+//               so the result is exact), and at the end of a unit hands m_ref
+//               and l to the epilogue and goes on to the next unit.
+//   warps 8-11  epilogue: once a unit's last P V of a tile is done, O / l
+//               (bf16) through shared memory to TMA stores, and LSE.
 // TMEM (512 columns): S0/P0, S1/P1 (128 each), O0, O1 (D each).
 //
 // Every wait on an mbarrier is bounded in time: if it gives up, the CTA
@@ -56,10 +62,20 @@ namespace tk {
 
 constexpr int BM = 128;            // query rows per Q tile (one TMEM lane each)
 constexpr int BN = 128;            // keys per key tile
-constexpr int NUM_THREADS = 320;   // 2 softmax warpgroups + MMA warp + TMA warp
-constexpr int WARP_MMA = 8;
-constexpr int WARP_TMA = 9;
+constexpr int NUM_THREADS = 512;   // 2 softmax warpgroups, epilogue warpgroup, control warpgroup
+constexpr int WARP_EPI = 8;        // warps 8..11: epilogue (warp 8 + q reads TMEM lanes 32q..32q+31)
+constexpr int WARP_MMA = 12;
+constexpr int WARP_TMA = 13;       // warps 14 and 15 only take part in set-up and tear-down
 constexpr uint32_t TMEM_COLS = 512;
+// Registers per thread after the split.  The CTA is launched with 128 per
+// thread (512 threads fill the 64 K register file); the split hands the
+// control and epilogue warpgroups' spare registers to the softmax warps and
+// adds up to exactly the launch budget.
+constexpr uint32_t REGS_SOFTMAX = 184;
+constexpr uint32_t REGS_EPI = 80;
+constexpr uint32_t REGS_CTRL = 64;
+constexpr int LAUNCH_REGS = 128;
+static_assert(2 * REGS_SOFTMAX + REGS_EPI + REGS_CTRL == 4 * LAUNCH_REGS, "register split = launch budget");
 // Lazy rescale: the reference max of a row is moved (and O, l rescaled) only
 // when the new row max exceeds it by more than this many powers of two.  P
 // then stays below 2^24 (fine for bf16 P and fp32 l and O: the product of
@@ -78,24 +94,32 @@ struct Layout {
     static_assert(D % 32 == 0 && D >= 32 && D <= 128, "head dim 32, 64, 96 or 128");
     static constexpr uint32_t Q_OFF = 0;                  // Q tile i at Q_OFF + i * TILE_BYTES
     static constexpr uint32_t SLOT_OFF = 2 * TILE_BYTES;
-    // O staging for the TMA store: one 128-row x 64-column box per softmax
-    // warpgroup (the epilogue writes D/64 boxes through it one after another).
+    // O staging for the TMA stores: per epilogue warp, one 32-row x 64-column
+    // box (4 KB) per 64 columns of D.
+    static constexpr uint32_t STAGE_BOX = 32 * 64 * 2;
+    static constexpr uint32_t STAGE_WARP = KATOMS * STAGE_BOX;
     static constexpr uint32_t STAGE_OFF = SLOT_OFF + NSLOTS * TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = STAGE_OFF + 2 * BOX_BYTES;
+    // Row statistics (reference max, row sum) handed from a softmax
+    // warpgroup to the epilogue at the end of each unit: [tile][row][2].
+    static constexpr uint32_t STATS_OFF = STAGE_OFF + 4 * STAGE_WARP;
+    static constexpr uint32_t BAR_OFF = STATS_OFF + 2 * BM * 8;
     // barriers
-    static constexpr int B_QFULL = 0;
-    static constexpr int B_QEMPTY = 1;
-    static constexpr int B_SLOTFULL = 2;                  // + slot
+    static constexpr int B_QFULL = 0;                     // + Q tile (2)
+    static constexpr int B_QEMPTY = 2;                    // + Q tile
+    static constexpr int B_SLOTFULL = 4;                  // + slot
     static constexpr int B_SLOTEMPTY = B_SLOTFULL + NSLOTS;
-    static constexpr int B_SFULL = B_SLOTEMPTY + NSLOTS;  // + Q tile (2)
-    static constexpr int B_PFULL = B_SFULL + 2;           // + Q tile
-    static constexpr int B_PVDONE = B_PFULL + 2;          // + Q tile
-    static constexpr int B_OFREE = B_PVDONE + 2;          // + Q tile
-    static constexpr int B_WGSYNC = B_OFREE + 2;          // + Q tile: warpgroup-internal sync
-    static constexpr int B_MMADONE = B_WGSYNC + 2;
+    static constexpr int B_SFULL = B_SLOTEMPTY + NSLOTS;  // + Q tile: S in TMEM
+    static constexpr int B_PFULL = B_SFULL + 2;           // + Q tile: P in TMEM (softmax -> MMA)
+    static constexpr int B_ODONE = B_PFULL + 2;           // + Q tile: a unit's last P V is done
+    static constexpr int B_OFREE = B_ODONE + 2;           // + Q tile: the epilogue has read O
+    static constexpr int B_STFULL = B_OFREE + 2;          // + Q tile: row statistics written
+    static constexpr int B_STEMPTY = B_STFULL + 2;        // + Q tile: row statistics read
+    static constexpr int B_MMADONE = B_STEMPTY + 2;
     static constexpr int NUM_BARS = B_MMADONE + 1;
-    static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
-    static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+    // No alignment slack: the dynamic shared memory of a kernel without
+    // static shared memory starts 1024-byte aligned (the kernel checks).
+    static constexpr uint32_t SMEM_ALLOC = BAR_OFF + NUM_BARS * 8 + 16;
+    static_assert(STAGE_OFF % 1024 == 0 && STAGE_BOX % 1024 == 0, "swizzled staging boxes");
     static_assert(SMEM_ALLOC > 116u * 1024u, "one CTA per SM: each CTA holds all 512 TMEM columns");
     static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
     // TMEM columns: S / P of Q tile i, O of Q tile i
@@ -126,6 +150,20 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
     return round * grid + ((round & 1) ? grid - 1 - cta : cta);
 }
 
+// The k-th unit of this CTA (k < units_of_cta).
+__device__ __forceinline__ Unit cta_unit(int k, const AttnParams &p) {
+    return unit_at(unit_index(k, blockIdx.x, gridDim.x), p);
+}
+
+// Units this CTA runs: one per round, except that the last round may have
+// none for it.
+__device__ __forceinline__ int units_of_cta(const AttnParams &p) {
+    const int total = p.BH * p.n_pairs;
+    const int grid = gridDim.x;
+    const int rounds = (total + grid - 1) / grid;
+    return rounds - (unit_index(rounds - 1, blockIdx.x, grid) >= total ? 1 : 0);
+}
+
 // Key tiles Q tile `qt` must visit: all of them, or under the causal mask
 // those up to the last key its last row sees (row + offset).
 __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
@@ -139,39 +177,41 @@ __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
     using L = Layout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
+    if (sbase & 1023u) {  // the 128-byte-swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) record_timeout(ROLE_LAYOUT << 24);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + L::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float2 *stats = reinterpret_cast<float2 *>(smem + L::STATS_OFF);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int total_units = p.BH * p.n_pairs;
-    const int grid = gridDim.x;
-    const int rounds = (total_units + grid - 1) / grid;
+    const int my_units = units_of_cta(p);
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::B_QFULL), 1);
-        mbar_init(bar(L::B_QEMPTY), 1);
-        for (int s = 0; s < L::NSLOTS; ++s) {
-            mbar_init(bar(L::B_SLOTFULL + s), 1);
-            mbar_init(bar(L::B_SLOTEMPTY + s), 1);
-        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::B_QFULL + i), 1);
+            mbar_init(bar(L::B_QEMPTY + i), 1);
             mbar_init(bar(L::B_SFULL + i), 1);
             // hand-offs from a warpgroup: one arrival per warp (after __syncwarp)
             mbar_init(bar(L::B_PFULL + i), 4);
-            mbar_init(bar(L::B_PVDONE + i), 1);
+            mbar_init(bar(L::B_ODONE + i), 1);
             mbar_init(bar(L::B_OFREE + i), 4);
-            mbar_init(bar(L::B_WGSYNC + i), 4);
+            mbar_init(bar(L::B_STFULL + i), 4);
+            mbar_init(bar(L::B_STEMPTY + i), 4);
+        }
+        for (int s = 0; s < L::NSLOTS; ++s) {
+            mbar_init(bar(L::B_SLOTFULL + s), 1);
+            mbar_init(bar(L::B_SLOTEMPTY + s), 1);
         }
         mbar_init(bar(L::B_MMADONE), 1);
         *abort_flag = 0;
@@ -182,20 +222,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_TMA) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+    if (warp >= WARP_MMA) {
+        regs_dealloc<REGS_CTRL>();
+        if (warp == WARP_TMA && lane == 0) {
+            // ------------------------------------------------ TMA producer
+            // Loads in the order the MMA warp consumes them: per unit K_0,
+            // V_0, then Q0 and Q1 (each once the previous unit's last S of
+            // that tile has completed), then K_j, V_j.
             tma_prefetch_desc(&p.tmQ);
             tma_prefetch_desc(&p.tmK);
             tma_prefetch_desc(&p.tmV);
-            uint32_t loads = 0;  // K/V slot loads issued (K_j and V_j alternate)
-            int k_unit = 0;
+            uint32_t loads = 0;  // K/V slot loads issued
             bool ok = true;
-            for (int r = 0; ok && r < rounds; ++r) {
-                const int idx = unit_index(r, blockIdx.x, grid);
-                if (idx >= total_units) continue;
-                const Unit u = unit_at(idx, p);
+            for (int k = 0; ok && k < my_units; ++k) {
+                const Unit u = cta_unit(k, p);
                 const int n_kv = kv_tiles(2 * u.pair + 1, p);
+                if (k + 1 < my_units) {
+                    // the next unit's Q tiles into L2: they are read once, from
+                    // HBM, and the next unit's first S waits for them
+                    const Unit un = cta_unit(k + 1, p);
+                    for (int i = 0; i < 2 && (2 * un.pair + i) * BM < p.Nq; ++i)
+                        for (int c = 0; c < L::KATOMS; ++c)
+                            tma_prefetch_l2_3d(&p.tmQ, c * 64, (2 * un.pair + i) * BM, un.bh);
+                }
                 auto load_kv = [&](int j, int kv) -> bool {
                     const int s = loads % L::NSLOTS;
                     if (loads >= static_cast<uint32_t>(L::NSLOTS) &&
@@ -210,19 +259,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     ++loads;
                     return true;
                 };
-                // K_0 and V_0 only need free ring slots: start them before
-                // waiting for the previous unit to release the Q buffers.
                 if (!(ok = load_kv(0, 0) && load_kv(0, 1))) break;
-                if (k_unit > 0 && !(ok = wait_bounded(bar(L::B_QEMPTY), (k_unit - 1) & 1, abort_flag,
-                                                      (ROLE_PRODUCER << 24) | (L::B_QEMPTY << 16) | k_unit)))
-                    break;
-                mbar_arrive_expect_tx(bar(L::B_QFULL), 2 * L::TILE_BYTES);
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; ok && i < 2; ++i) {
+                    if (k > 0 && !(ok = wait_bounded(bar(L::B_QEMPTY + i), (k - 1) & 1, abort_flag,
+                                                     (ROLE_PRODUCER << 24) | ((L::B_QEMPTY + i) << 16) | k)))
+                        break;
+                    mbar_arrive_expect_tx(bar(L::B_QFULL + i), L::TILE_BYTES);
                     for (int c = 0; c < L::KATOMS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + i * L::TILE_BYTES + c * L::BOX_BYTES, &p.tmQ,
-                                    bar(L::B_QFULL), c * 64, (2 * u.pair + i) * BM, u.bh);
+                                    bar(L::B_QFULL + i), c * 64, (2 * u.pair + i) * BM, u.bh);
+                }
                 for (int j = 1; ok && j < n_kv; ++j) ok = load_kv(j, 0) && load_kv(j, 1);
-                ++k_unit;
             }
             if (!ok) {
                 // Let the copies in flight land before the CTA exits.
@@ -234,18 +281,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     }
                 }
             }
-        }
-        __syncwarp();
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------ MMA issuer
+            // The whole warp runs the loop: waits and operand arithmetic are
+            // warp-uniform, and one elected lane sends each block of MMAs and
+            // each commit.  The stream does not stop between units: the last
+            // key tile of a unit is followed at once by the next unit's first
+            // S of each Q tile.  S of key tile j+1 of a Q tile is issued after
+            // P V of key tile j of that tile, so its "S ready" commit also
+            // tells the softmax that every earlier P V of the tile is done.
             constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);  // K-major Q and K
             constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 0, 1);   // P from TMEM, V MN-major
+            constexpr int KS = D / 16;     // k steps of S = Q K^T
             uint32_t taken = 0;            // K/V slots consumed, in load order
             uint32_t p_seen[2] = {0, 0};   // P hand-offs consumed per Q tile
             bool ok = true;
-            int k_unit = 0;
 
+            auto commit = [&](int b) {
+                if (elect_one()) umma_commit(bar(b));
+                __syncwarp();
+            };
             auto take_slot = [&](uint32_t &slot) -> bool {
                 slot = taken % L::NSLOTS;
                 const bool r = wait_bounded(bar(L::B_SLOTFULL + slot), (taken / L::NSLOTS) & 1, abort_flag,
@@ -253,103 +308,201 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 ++taken;
                 return r;
             };
-            // Descriptors are formed once per operand tile; the k steps add
-            // their (compile-time) offsets to the start-address field, which
-            // cannot carry out of its 14 bits (shared memory is below 256 KB).
+            // S_i = Q_i K^T, then "S ready".  A k step moves 32 bytes along a
+            // 128-byte swizzled row; every four steps the next 64-column box.
             auto issue_s = [&](int i, uint32_t kslot) {
                 const uint64_t qd = smem_desc_sw128(sbase + L::Q_OFF + i * L::TILE_BYTES, 16, 1024);
                 const uint64_t kd = smem_desc_sw128(sbase + L::SLOT_OFF + kslot * L::TILE_BYTES, 16, 1024);
-                const uint32_t q_lo = static_cast<uint32_t>(qd), k_lo = static_cast<uint32_t>(kd);
-                const uint32_t d_hi = static_cast<uint32_t>(qd >> 32);  // the same for Q and K
-                const uint32_t dst = tmem + L::tmem_s(i);
+                const uint32_t hi = static_cast<uint32_t>(qd >> 32);  // the same for Q and K
+                uint32_t a[KS], b[KS];
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 0; k < KS; ++k) {
                     const uint32_t off = ((k / 4) * L::BOX_BYTES + (k % 4) * 32) >> 4;
-                    umma_ss_lo(dst, q_lo + off, d_hi, k_lo + off, d_hi, IDESC_S, k > 0 ? 1u : 0u);
+                    a[k] = static_cast<uint32_t>(qd) + off;
+                    b[k] = static_cast<uint32_t>(kd) + off;
                 }
-                umma_commit(bar(L::B_SFULL + i));
+                const uint32_t dst = tmem + L::tmem_s(i);
+                if (elect_one()) {
+#pragma unroll
+                    for (int k = 0; k + 4 <= KS; k += 4) umma_ss_x4(dst, a + k, b + k, hi, IDESC_S, k > 0 ? 1u : 0u);
+                    if constexpr (KS % 4 == 2) umma_ss_x2(dst, a + KS - 2, b + KS - 2, hi, IDESC_S, KS > 2 ? 1u : 0u);
+                    umma_commit(bar(L::B_SFULL + i));
+                }
+                __syncwarp();
             };
+            // O_i += P_i V over 128 keys in 8 k steps; P from the S columns
+            // of TMEM (two bf16 per column), V MN-major from the slot.
             auto issue_pv = [&](int i, uint32_t vslot, bool accumulate) {
                 const uint64_t vd = smem_desc_sw128(sbase + L::SLOT_OFF + vslot * L::TILE_BYTES, L::BOX_BYTES, 1024);
                 const uint32_t v_lo = static_cast<uint32_t>(vd), v_hi = static_cast<uint32_t>(vd >> 32);
-                const uint32_t dst = tmem + L::tmem_o(i), pa = tmem + L::tmem_s(i);
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    // 16 keys per step: P columns advance by 8 (two bf16 per
-                    // 32-bit column), V rows by 16 * 128 bytes.
-                    umma_ts_lo(dst, pa + k * 8, v_lo + ((k * 2048) >> 4), v_hi, IDESC_O, (accumulate || k > 0) ? 1u : 0u);
-                }
-                umma_commit(bar(L::B_PVDONE + i));
+                if (elect_one())
+                    umma_ts_x8(tmem + L::tmem_o(i), tmem + L::tmem_s(i), v_lo, v_hi, IDESC_O, accumulate ? 1u : 0u);
+                __syncwarp();
+            };
+            auto wait_bar = [&](int b, uint32_t parity, uint32_t step) -> bool {
+                return wait_bounded(bar(b), parity & 1, abort_flag, (ROLE_MMA << 24) | (b << 16) | (step & 0xFFFF));
             };
             auto wait_p = [&](int i, int j) -> bool {
-                const bool r = wait_bounded(bar(L::B_PFULL + i), p_seen[i] & 1, abort_flag,
-                                            (ROLE_MMA << 24) | ((L::B_PFULL + i) << 16) | (j & 0xFFFF));
+                const bool r = wait_bar(L::B_PFULL + i, p_seen[i], j);
                 ++p_seen[i];
                 return r;
             };
 
-            for (int r = 0; ok && r < rounds; ++r) {
-                const int idx = unit_index(r, blockIdx.x, grid);
-                if (idx >= total_units) continue;
-                const Unit u = unit_at(idx, p);
-                const int n0 = kv_tiles(2 * u.pair, p);
-                const int n1 = kv_tiles(2 * u.pair + 1, p);  // n1 >= n0 >= 1
+            if (my_units > 0) {
+                const Unit u0 = cta_unit(0, p);
+                int n0 = kv_tiles(2 * u0.pair, p);
+                int n1 = kv_tiles(2 * u0.pair + 1, p);  // n1 >= n0 >= 1
                 uint32_t ks = 0, vs = 0;
-                if (!(ok = wait_bounded(bar(L::B_QFULL), k_unit & 1, abort_flag,
-                                        (ROLE_MMA << 24) | (L::B_QFULL << 16) | k_unit)))
-                    break;
-                if (!(ok = take_slot(ks))) break;
-                tc_fence_after_sync();
-                issue_s(0, ks);
-                issue_s(1, ks);
-                umma_commit(bar(L::B_SLOTEMPTY + ks));
-                // Q is free once the unit's last S MMA has completed, so the
-                // next unit's Q load overlaps this unit's last P V products.
-                if (n1 == 1) umma_commit(bar(L::B_QEMPTY));
-                for (int j = 0; j < n1; ++j) {
-                    const bool has_next = j + 1 < n1;
-                    if (!(ok = take_slot(vs))) break;  // V_j
-                    if (j < n0) {
-                        if (!(ok = wait_p(0, j))) break;
-                        if (j == 0 && k_unit > 0 &&
-                            !(ok = wait_bounded(bar(L::B_OFREE + 0), (k_unit - 1) & 1, abort_flag,
-                                                (ROLE_MMA << 24) | (L::B_OFREE << 16) | k_unit)))
-                            break;
-                        tc_fence_after_sync();
-                        issue_pv(0, vs, j > 0);
-                    }
-                    if (has_next) {
-                        if (!(ok = take_slot(ks))) break;  // K_{j+1}
-                        tc_fence_after_sync();
-                        if (j + 1 < n0) issue_s(0, ks);
-                    }
-                    if (!(ok = wait_p(1, j))) break;
-                    if (j == 0 && k_unit > 0 &&
-                        !(ok = wait_bounded(bar(L::B_OFREE + 1), (k_unit - 1) & 1, abort_flag,
-                                            (ROLE_MMA << 24) | ((L::B_OFREE + 1) << 16) | k_unit)))
-                        break;
+                // The first unit's S of both Q tiles.
+                ok = wait_bar(L::B_QFULL, 0, 0) && take_slot(ks);
+                if (ok) {
                     tc_fence_after_sync();
-                    issue_pv(1, vs, j > 0);
-                    umma_commit(bar(L::B_SLOTEMPTY + vs));
-                    if (has_next) {
-                        issue_s(1, ks);
-                        umma_commit(bar(L::B_SLOTEMPTY + ks));
-                        if (j + 2 == n1) umma_commit(bar(L::B_QEMPTY));
-                    }
+                    issue_s(0, ks);
+                    if (n0 == 1) commit(L::B_QEMPTY);
+                    ok = wait_bar(L::B_QFULL + 1, 0, 0);
                 }
-                if (!ok) break;
-                ++k_unit;
+                if (ok) {
+                    tc_fence_after_sync();
+                    issue_s(1, ks);
+                    commit(L::B_SLOTEMPTY + ks);
+                    if (n1 == 1) commit(L::B_QEMPTY + 1);
+                }
+                for (int k = 0; ok && k < my_units; ++k) {
+                    const bool has_next = k + 1 < my_units;
+                    int m0 = 0, m1 = 0;
+                    if (has_next) {
+                        const Unit un = cta_unit(k + 1, p);
+                        m0 = kv_tiles(2 * un.pair, p);
+                        m1 = kv_tiles(2 * un.pair + 1, p);
+                    }
+                    for (int j = 0; j < n1; ++j) {
+                        const bool last = j + 1 == n1;
+                        if (!(ok = take_slot(vs))) break;  // V_j
+                        if (j < n0) {
+                            if (!(ok = wait_p(0, j))) break;
+                            // O of Q tile 0 is overwritten by the unit's first
+                            // P V: the epilogue must have read the previous one.
+                            if (j == 0 && k > 0 && !(ok = wait_bar(L::B_OFREE, k - 1, k))) break;
+                            tc_fence_after_sync();
+                            issue_pv(0, vs, j > 0);
+                            if (j == n0 - 1) commit(L::B_ODONE);
+                        }
+                        // The next S of Q tile 0: key tile j+1 of this unit, or
+                        // the next unit's first key tile.
+                        if (!last) {
+                            if (!(ok = take_slot(ks))) break;  // K_{j+1}
+                            if (j + 1 < n0) {
+                                tc_fence_after_sync();
+                                issue_s(0, ks);
+                                if (j + 2 == n0) commit(L::B_QEMPTY);
+                            }
+                        } else if (has_next) {
+                            if (!(ok = take_slot(ks) && wait_bar(L::B_QFULL, k + 1, k + 1))) break;
+                            tc_fence_after_sync();
+                            issue_s(0, ks);
+                            if (m0 == 1) commit(L::B_QEMPTY);
+                        }
+                        if (!(ok = wait_p(1, j))) break;
+                        if (j == 0 && k > 0 && !(ok = wait_bar(L::B_OFREE + 1, k - 1, k))) break;
+                        tc_fence_after_sync();
+                        issue_pv(1, vs, j > 0);
+                        commit(L::B_SLOTEMPTY + vs);
+                        if (last) commit(L::B_ODONE + 1);
+                        if (!last) {
+                            issue_s(1, ks);
+                            commit(L::B_SLOTEMPTY + ks);
+                            if (j + 2 == n1) commit(L::B_QEMPTY + 1);
+                        } else if (has_next) {
+                            if (!(ok = wait_bar(L::B_QFULL + 1, k + 1, k + 1))) break;
+                            tc_fence_after_sync();
+                            issue_s(1, ks);
+                            commit(L::B_SLOTEMPTY + ks);
+                            if (m1 == 1) commit(L::B_QEMPTY + 1);
+                        }
+                    }
+                    n0 = m0;
+                    n1 = m1;
+                }
             }
             // Every MMA issued so far has completed before TMEM is released.
-            umma_commit(bar(L::B_MMADONE));
+            commit(L::B_MMADONE);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
                    global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
             }
         }
         __syncwarp();
+    } else if (warp >= WARP_EPI) {
+        // ------------------------------------------------ epilogue
+        // Per unit and Q tile: O / l as bf16 through this warp's staging
+        // boxes to TMA stores of its 32 rows, and LSE.  Runs while the
+        // softmax warps are already on the next unit.
+        regs_dealloc<REGS_EPI>();
+        const int quarter = warp - WARP_EPI;           // TMEM lanes 32 * quarter ...
+        const int r = quarter * 32 + lane;             // row within the Q tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint8_t *stage = smem + L::STAGE_OFF + quarter * L::STAGE_WARP;
+        const uint32_t stage_addr = sbase + L::STAGE_OFF + quarter * L::STAGE_WARP;
+        bool ok = true;
+        auto wait_bar = [&](int b, uint32_t parity, uint32_t step) -> bool {
+            return wait_bounded(bar(b), parity & 1, abort_flag, (ROLE_EPILOGUE << 24) | (b << 16) | (step & 0xFFFF));
+        };
+        for (int k = 0; ok && k < my_units; ++k) {
+            const Unit u = cta_unit(k, p);
+            for (int tile = 0; tile < 2; ++tile) {
+                const int qt = 2 * u.pair + tile;
+                if (!(ok = wait_bar(L::B_STFULL + tile, k, k))) break;
+                const float2 st = stats[tile * BM + r];     // (reference max, row sum)
+                warp_arrive(bar(L::B_STEMPTY + tile), lane);
+                if (!(ok = wait_bar(L::B_ODONE + tile, k, k))) break;
+                tc_fence_after_sync();
+                // the staging boxes of this warp's previous stores are free
+                if (lane == 0) tma_store_wait_read_all();
+                __syncwarp();
+                const float inv_l = 1.0f / st.y;
+                const uint32_t o_addr = lane_base + L::tmem_o(tile);
+#pragma unroll
+                for (int h = 0; h < L::KATOMS; ++h) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        if (h * 64 + half * 32 >= D) continue;  // D = 32, 96: the store clips at D
+                        uint32_t rr[32];
+                        tmem_ld32(o_addr + h * 64 + half * 32, rr);
+                        uint32_t ob[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                                                __uint_as_float(rr[2 * i + 1]) * inv_l);
+                        // row `lane` of a 32-row box, 128-byte swizzle
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int chunk = half * 4 + c;
+                            *reinterpret_cast<uint4 *>(stage + h * L::STAGE_BOX + lane * 128 +
+                                                       ((chunk ^ (lane & 7)) << 4)) =
+                                make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                        }
+                    }
+                }
+                // All of O has left TMEM: the next unit's first P V may overwrite it.
+                tc_fence_before_sync();
+                warp_arrive(bar(L::B_OFREE + tile), lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int h = 0; h < L::KATOMS; ++h)
+                        tma_store_3d(&p.tmO32, stage_addr + h * L::STAGE_BOX, h * 64, qt * BM + quarter * 32, u.bh);
+                    tma_store_commit();
+                }
+                const int row = qt * BM + r;
+                if (row < p.Nq) p.LSE[static_cast<size_t>(u.bh) * p.Nq + row] = st.x * p.scale + logf(st.y);
+            }
+        }
+        if (lane == 0) tma_store_wait_all();  // every store of this warp has landed
+        __syncwarp();
     } else {
-        // ------------------------------------------------ softmax / correction / epilogue
+        // ------------------------------------------------ softmax / correction
+        regs_alloc<REGS_SOFTMAX>();
         const int tile = warp / 4;                 // which Q tile of the unit this warpgroup owns
         const int t = threadIdx.x % 128;           // row within the tile == TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
@@ -357,22 +510,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         const uint32_t o_addr = lane_base + L::tmem_o(tile);
         const float c = p.scale_log2e;
         uint32_t s_seen = 0;    // S hand-offs consumed
-        uint32_t pv_base = 0;   // PV MMAs of this Q tile in earlier units
-        uint32_t syncs = 0;     // warpgroup syncs done
         bool ok = true;
-        // Warpgroup-wide sync on an mbarrier: unlike a named barrier its wait
-        // is bounded, so an aborting CTA cannot hang here.
-        auto wg_sync = [&](int tl) -> bool {
-            warp_arrive(bar(L::B_WGSYNC + tl), lane);
-            const bool r = wait_bounded(bar(L::B_WGSYNC + tl), syncs & 1, abort_flag,
-                                        (ROLE_SOFTMAX << 24) | ((L::B_WGSYNC + tl) << 16) | (syncs & 0xFFFF));
-            ++syncs;
-            return r;
-        };
-        for (int r = 0; ok && r < rounds; ++r) {
-            const int idx = unit_index(r, blockIdx.x, grid);
-            if (idx >= total_units) continue;
-            const Unit u = unit_at(idx, p);
+        for (int k = 0; ok && k < my_units; ++k) {
+            const Unit u = cta_unit(k, p);
             const int qt = 2 * u.pair + tile;
             const int row = qt * BM + t;
             const int n_kv = kv_tiles(qt, p);
@@ -384,9 +524,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     break;
                 ++s_seen;
                 tc_fence_after_sync();
-                // The whole S row in one TMEM load (one round trip).
+                // The whole S row: two 64-column TMEM loads, one wait.
                 uint32_t sr[BN];
-                tmem_ld128(s_addr, sr);
+                tmem_ld64_async(s_addr, sr);
+                tmem_ld64_async(s_addr + 64, sr + 64);
+                tmem_ld_wait();
+                reg_fence(sr);
                 float s[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
@@ -402,11 +545,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 // Row max: eight independent chains of three-input maxima.
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float a = s[k];
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    float a = s[k8];
 #pragma unroll
-                    for (int t = 1; t < 15; t += 2) a = fmax3(a, s[k + 8 * t], s[k + 8 * (t + 1)]);
-                    mx8[k] = fmaxf(a, s[k + 120]);
+                    for (int t2 = 1; t2 < 15; t2 += 2) a = fmax3(a, s[k8 + 8 * t2], s[k8 + 8 * (t2 + 1)]);
+                    mx8[k8] = fmaxf(a, s[k8 + 120]);
                 }
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmax3(mx8[6], mx8[7], m_ref));
@@ -440,10 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 l = l * alpha + (a.x + a.y);
                 m_ref = new_ref;
                 if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
-                    // O holds PV_0..PV_{j-1} of this tile; it must be complete.
-                    if (!(ok = wait_bounded(bar(L::B_PVDONE + tile), (pv_base + j - 1) & 1, abort_flag,
-                                            (ROLE_SOFTMAX << 24) | ((L::B_PVDONE + tile) << 16) | (j & 0xFFFF))))
-                        break;
+                    // S_j was issued after P V of key tile j-1: O is complete.
                     tc_fence_after_sync();
 #pragma unroll
                     for (int q = 0; q < D / 32; ++q) {
@@ -459,60 +599,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 warp_arrive(bar(L::B_PFULL + tile), lane);
             }
             if (!ok) break;
-            // ---- epilogue: O / l in bf16, LSE in fp32
-            if (!(ok = wait_bounded(bar(L::B_PVDONE + tile), (pv_base + n_kv - 1) & 1, abort_flag,
-                                    (ROLE_SOFTMAX << 24) | ((L::B_PVDONE + tile) << 16) | 0xFFFF)))
+            // Row statistics to the epilogue (once it has read the last ones).
+            if (k > 0 && !(ok = wait_bounded(bar(L::B_STEMPTY + tile), (k - 1) & 1, abort_flag,
+                                             (ROLE_SOFTMAX << 24) | ((L::B_STEMPTY + tile) << 16) | (k & 0xFFFF))))
                 break;
-            pv_base += n_kv;
-            tc_fence_after_sync();
-            const float inv_l = 1.0f / l;
-            // O / l as bf16 through shared memory to TMA stores, 64 columns
-            // (one 128-byte row of a TMA box) at a time: coalesced full-line
-            // writes, and rows past N are clipped by the tensor map.
-            uint8_t *stage = smem + L::STAGE_OFF + tile * L::BOX_BYTES;
-            const uint32_t stage_addr = sbase + L::STAGE_OFF + tile * L::BOX_BYTES;
-#pragma unroll
-            for (int h = 0; h < L::KATOMS; ++h) {
-                uint32_t ob[32];
-                if (D - h * 64 >= 64) {
-                    uint32_t rr[64];
-                    tmem_ld64(o_addr + h * 64, rr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                                            __uint_as_float(rr[2 * i + 1]) * inv_l);
-                } else {
-                    // a half box (D = 32, 96): the other 32 columns are not
-                    // this tile's, and the store clips them at D
-                    uint32_t rr[32];
-                    tmem_ld32(o_addr + h * 64, rr);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                                            __uint_as_float(rr[2 * i + 1]) * inv_l);
-#pragma unroll
-                    for (int i = 16; i < 32; ++i) ob[i] = 0u;
-                }
-                if (h == L::KATOMS - 1) {
-                    tc_fence_before_sync();
-                    warp_arrive(bar(L::B_OFREE + tile), lane);  // O of this tile may be overwritten
-                }
-                if (t == 0) tma_store_wait_read_all();  // the staging box is free again
-                if (!(ok = wg_sync(tile))) break;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(stage + t * 128 + ((c ^ (t & 7)) << 4)) =
-                        make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-                fence_proxy_async_smem();
-                if (!(ok = wg_sync(tile))) break;
-                if (t == 0) {
-                    tma_store_3d(&p.tmO, stage_addr, h * 64, qt * BM, u.bh);
-                    tma_store_commit();
-                }
-            }
-            if (row < p.Nq) p.LSE[static_cast<size_t>(u.bh) * p.Nq + row] = m_ref * p.scale + logf(l);
+            stats[tile * BM + t] = make_float2(m_ref, l);
+            warp_arrive(bar(L::B_STFULL + tile), lane);
         }
-        if (t == 0) tma_store_wait_all();  // every store of this warpgroup has landed
     }
 
     tc_fence_before_sync();
@@ -551,6 +644,14 @@ static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t strea
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
+        // The register split of the kernel's warpgroups adds up to the
+        // launch budget of 128 registers per thread; a build that launched
+        // with fewer would leave the growing warpgroup waiting, so it is
+        // refused here instead.
+        cudaFuncAttributes attr;
+        err = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D>);
+        if (err != cudaSuccess) return err;
+        if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         err = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    L::SMEM_ALLOC);
         if (err != cudaSuccess) return err;

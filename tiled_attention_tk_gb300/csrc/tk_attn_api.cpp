@@ -105,14 +105,15 @@ int check_device_memory(const void *p) {
 // 3-D view {D, N, B*H} of a contiguous [B,H,N,D] bf16 tensor, moved as
 // 128-row x 64-column boxes with the 128-byte swizzle; loads read rows past
 // N as 0, stores skip them.
-int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int64_t BH) {
+int encode_qkv_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t D, int64_t BH,
+                   uint32_t box_rows = 128) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return fail_cuda(g_encode_err);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                      box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -295,6 +296,7 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     if ((rc = encode_qkv_map(&p.tmK, K, Nkv, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmV, V, Nkv, D, BH)) != TK_OK) return rc;
     if ((rc = encode_qkv_map(&p.tmO, O, Nq, D, BH)) != TK_OK) return rc;
+    if ((rc = encode_qkv_map(&p.tmO32, O, Nq, D, BH, 32)) != TK_OK) return rc;
     p.O = O;
     p.LSE = LSE;
     p.Nq = static_cast<int>(Nq);

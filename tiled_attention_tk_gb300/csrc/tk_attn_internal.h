@@ -17,6 +17,7 @@ struct AttnParams {
     CUtensorMap tmK;  // 3-D {D, Nkv, B*H}, same box and swizzle
     CUtensorMap tmV;
     CUtensorMap tmO;  // the view of Q for O, for TMA stores
+    CUtensorMap tmO32;  // the same view moved as 32-row boxes {64, 32, 1} (per-warp stores)
     void *O;          // bf16 [B*H, Nq, D]
     float *LSE;       // fp32 [B*H, Nq]
     int Nq;           // query rows

@@ -78,6 +78,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Hint: bring a 3-D box into L2 ahead of its load (no shared memory, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // 3-D tiled store shared -> global (rows outside the tensor are not written).
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1,
                                              int c2) {
@@ -190,6 +199,95 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
+}
+
+// An MMA-issuing warp runs its loop on all 32 lanes, so that the operands
+// it forms stay warp-uniform, and sends each block of MMAs from one elected
+// lane.  (A loop run by lane 0 alone measured about 35% slower per MMA when
+// busy warps share the issuing warp's SM sub-partition.)
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// Four SS MMAs (A and B from shared memory) from descriptor low halves
+// formed beforehand (a[k], b[k]; the high half `hi` is shared); the first
+// accumulates iff `acc_first`, the rest always.
+__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, const uint32_t *a, const uint32_t *b, uint32_t hi,
+                                           uint32_t idesc, uint32_t acc_first) {
+    asm volatile(
+        "{\n\t.reg .pred pt, pa;\n\t.reg .b64 ad0, ad1, ad2, ad3, bd0, bd1, bd2, bd3;\n\t"
+        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %11, 0;\n\t"
+        "mov.b64 ad0, {%1, %9};\n\tmov.b64 bd0, {%5, %9};\n\t"
+        "mov.b64 ad1, {%2, %9};\n\tmov.b64 bd1, {%6, %9};\n\t"
+        "mov.b64 ad2, {%3, %9};\n\tmov.b64 bd2, {%7, %9};\n\t"
+        "mov.b64 ad3, {%4, %9};\n\tmov.b64 bd3, {%8, %9};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad0, bd0, %10, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad1, bd1, %10, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad2, bd2, %10, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad3, bd3, %10, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(hi),
+        "r"(idesc), "r"(acc_first)
+        : "memory");
+}
+
+// Two SS MMAs, the same (for head dims whose k steps are not a multiple of 4).
+__device__ __forceinline__ void umma_ss_x2(uint32_t d_tmem, const uint32_t *a, const uint32_t *b, uint32_t hi,
+                                           uint32_t idesc, uint32_t acc_first) {
+    asm volatile(
+        "{\n\t.reg .pred pt, pa;\n\t.reg .b64 ad0, ad1, bd0, bd1;\n\t"
+        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %7, 0;\n\t"
+        "mov.b64 ad0, {%1, %5};\n\tmov.b64 bd0, {%3, %5};\n\t"
+        "mov.b64 ad1, {%2, %5};\n\tmov.b64 bd1, {%4, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad0, bd0, %6, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad1, bd1, %6, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(b[0]), "r"(b[1]), "r"(hi), "r"(idesc), "r"(acc_first)
+        : "memory");
+}
+
+// Eight TS MMAs (A from TMEM, B from shared memory) over 128 keys: A advances
+// 8 columns and B 2048 bytes (128 in 16-byte units) per k step.  The first
+// accumulates iff `acc_first`.
+__device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t acc_first) {
+    asm volatile(
+        "{\n\t.reg .pred pt, pa;\n\t.reg .b32 b1, b2, b3, b4, b5, b6, b7;\n\t"
+        ".reg .b64 bd0, bd1, bd2, bd3, bd4, bd5, bd6, bd7;\n\t"
+        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %5, 0;\n\t"
+        "add.u32 b1, %2, 128;\n\tadd.u32 b2, %2, 256;\n\tadd.u32 b3, %2, 384;\n\tadd.u32 b4, %2, 512;\n\t"
+        "add.u32 b5, %2, 640;\n\tadd.u32 b6, %2, 768;\n\tadd.u32 b7, %2, 896;\n\t"
+        "mov.b64 bd0, {%2, %3};\n\tmov.b64 bd1, {b1, %3};\n\tmov.b64 bd2, {b2, %3};\n\tmov.b64 bd3, {b3, %3};\n\t"
+        "mov.b64 bd4, {b4, %3};\n\tmov.b64 bd5, {b5, %3};\n\tmov.b64 bd6, {b6, %3};\n\tmov.b64 bd7, {b7, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd0, %4, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], bd1, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], bd2, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], bd3, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], bd4, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], bd5, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], bd6, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], bd7, %4, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc_first)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- registers
+
+// Per-warpgroup register reallocation (all four warps of a warpgroup run
+// the same one).  A warpgroup that gives registers up lets another one grow
+// within the registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
@@ -312,6 +410,17 @@ __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : TK_R8(0), TK_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+
+// 64 columns without the wait (a 64-column load is the widest that fits the
+// 128-register budget of a 512-thread CTA, whatever a later register
+// reallocation allows).
+__device__ __forceinline__ void tmem_ld64_async(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr)
         : "memory");
 }

@@ -29,7 +29,9 @@ enum : uint32_t {
     ROLE_BWD_PRODUCER = 5,
     ROLE_BWD_MMA = 6,
     ROLE_BWD_COMPUTE = 7,
-    ROLE_BWD_LAYOUT = 8  // not a wait: the backward kernel found its shared memory misaligned
+    ROLE_BWD_LAYOUT = 8,  // not a wait: the backward kernel found its shared memory misaligned
+    ROLE_EPILOGUE = 9,
+    ROLE_LAYOUT = 10      // not a wait: the forward kernel found its shared memory misaligned
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t where) {
