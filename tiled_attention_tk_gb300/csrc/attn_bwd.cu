@@ -277,36 +277,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         // dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.  Each
         // product that overwrites TMEM columns an earlier product reads (S^T
         // over P^T, dQ_part over dS^T) is issued after it; the tensor core
-        // runs one thread's products in issue order.
-        if (lane == 0) {
+        // runs one thread's products in issue order.  The whole warp runs
+        // the loop (operands stay warp-uniform); one elected lane sends each
+        // block of products and each commit.
+        {
             constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S^T, dP^T: K-major A and B
             constexpr uint32_t IDESC_TS = idesc_bf16_f32(BT, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
             constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dQ_part: MN-major A and B
             // Descriptors are formed once per operand tile; a k step adds its
             // compile-time offset to the start-address field, which cannot
             // carry out of its 14 bits (shared memory is below 256 KB).
-            auto issue_s = [&](uint32_t qb) {  // S^T = K Q^T
-                const uint64_t kd = smem_desc_sw128(sbase + L::K_OFF, 16, 1024), qd = smem_desc_sw128(qb, 16, 1024);
-                const uint32_t k_lo = static_cast<uint32_t>(kd), q_lo = static_cast<uint32_t>(qd),
-                               hi = static_cast<uint32_t>(kd >> 32);
+            auto commit = [&](int b) {
+                if (elect_one()) umma_commit(bar(b));
+                __syncwarp();
+            };
+            // A = (K or V) x B = (Q or dO), both K-major over D, into `dst`.
+            auto issue_kmajor = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile, int done_bar) {
+                const uint64_t ad = smem_desc_sw128(a_tile, 16, 1024), bd = smem_desc_sw128(b_tile, 16, 1024);
+                const uint32_t hi = static_cast<uint32_t>(ad >> 32);
+                uint32_t av[D / 16], bv[D / 16];
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
-                    umma_ss_lo(tmem + L::T_S, k_lo + off, hi, q_lo + off, hi, IDESC_KK, k > 0);
+                    av[k] = static_cast<uint32_t>(ad) + off;
+                    bv[k] = static_cast<uint32_t>(bd) + off;
                 }
-                umma_commit(bar(L::B_SFULL));
-            };
-            auto issue_dp = [&](uint32_t dob) {  // dP^T = V dO^T
-                const uint64_t vd = smem_desc_sw128(sbase + L::V_OFF, 16, 1024), dd = smem_desc_sw128(dob, 16, 1024);
-                const uint32_t v_lo = static_cast<uint32_t>(vd), d_lo = static_cast<uint32_t>(dd),
-                               hi = static_cast<uint32_t>(vd >> 32);
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
-                    umma_ss_lo(tmem + L::T_DP, v_lo + off, hi, d_lo + off, hi, IDESC_KK, k > 0);
+                if (elect_one()) {
+                    umma_ss_steps<D / 16>(dst, av, hi, bv, hi, IDESC_KK, 0u);
+                    umma_commit(bar(done_bar));
                 }
-                umma_commit(bar(L::B_DPFULL));
+                __syncwarp();
             };
+            auto issue_s = [&](uint32_t qb) { issue_kmajor(tmem + L::T_S, sbase + L::K_OFF, qb, L::B_SFULL); };     // S^T = K Q^T
+            auto issue_dp = [&](uint32_t dob) { issue_kmajor(tmem + L::T_DP, sbase + L::V_OFF, dob, L::B_DPFULL); };  // dP^T = V dO^T
             bool ok = wait_bounded(bar(L::B_KVFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16)) &&
                       wait_bounded(bar(L::B_QFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_QFULL << 16));
             if (ok) {
@@ -328,11 +331,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                                             (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | it)))
                         break;
                     tc_fence_after_sync();
-#pragma unroll
-                    for (int k = 2 * c; k < 2 * c + 2; ++k)
-                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + (k % 2) * 8,
-                                   static_cast<uint32_t>(dob_mn) + ((k * 2048) >> 4), mn_hi, IDESC_TS,
-                                   (it > 0 || k > 0) ? 1u : 0u);
+                    const uint32_t b0 = static_cast<uint32_t>(dob_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                    if (elect_one()) {
+                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                    }
+                    __syncwarp();
                 }
                 // dK += dS'^T Q likewise.
                 for (int c = 0; ok && c < 4; ++c) {
@@ -340,14 +344,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                                             (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | it)))
                         break;
                     tc_fence_after_sync();
-#pragma unroll
-                    for (int k = 2 * c; k < 2 * c + 2; ++k)
-                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + (k % 2) * 8,
-                                   static_cast<uint32_t>(qb_mn) + ((k * 2048) >> 4), mn_hi, IDESC_TS,
-                                   (it > 0 || k > 0) ? 1u : 0u);
+                    const uint32_t b0 = static_cast<uint32_t>(qb_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                    if (elect_one()) {
+                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                    }
+                    __syncwarp();
                 }
                 if (!ok) break;
-                umma_commit(bar(L::B_QEMPTY + b));  // Q, dO of this tile are no longer read
+                commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
                 const bool has_next = it + 1 < n_q;
                 const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
                 if (has_next) {
@@ -362,14 +367,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 {
                     const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
                                    kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
-                    const uint32_t ds_lo = static_cast<uint32_t>(dsd), km_lo = static_cast<uint32_t>(kmd),
-                                   hi = static_cast<uint32_t>(dsd >> 32);
+                    const uint32_t hi = static_cast<uint32_t>(dsd >> 32);
+                    uint32_t av[BT / 16], bv[BT / 16];
 #pragma unroll
-                    for (int k = 0; k < BT / 16; ++k)
-                        umma_ss_lo(tmem + L::T_DQ, ds_lo + ((k * 2048) >> 4), hi, km_lo + ((k * 2048) >> 4), hi, IDESC_MM,
-                                   k > 0);
+                    for (int k = 0; k < BT / 16; ++k) {
+                        av[k] = static_cast<uint32_t>(dsd) + ((k * 2048) >> 4);
+                        bv[k] = static_cast<uint32_t>(kmd) + ((k * 2048) >> 4);
+                    }
+                    if (elect_one()) {
+                        umma_ss_steps<BT / 16>(tmem + L::T_DQ, av, hi, bv, hi, IDESC_MM, 0u);
+                        umma_commit(bar(L::B_GDONE));
+                    }
+                    __syncwarp();
                 }
-                umma_commit(bar(L::B_GDONE));
                 if (has_next) {
                     if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
                                             (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | it)))
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     issue_dp(qn + L::TILE);
                 }
             }
-            umma_commit(bar(L::B_MMADONE));
+            commit(L::B_MMADONE);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
                    global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {

@@ -323,9 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
                 const uint32_t dst = tmem + L::tmem_s(i);
                 if (elect_one()) {
-#pragma unroll
-                    for (int k = 0; k + 4 <= KS; k += 4) umma_ss_x4(dst, a + k, b + k, hi, IDESC_S, k > 0 ? 1u : 0u);
-                    if constexpr (KS % 4 == 2) umma_ss_x2(dst, a + KS - 2, b + KS - 2, hi, IDESC_S, KS > 2 ? 1u : 0u);
+                    umma_ss_steps<KS>(dst, a, hi, b, hi, IDESC_S, 0u);
                     umma_commit(bar(L::B_SFULL + i));
                 }
                 __syncwarp();

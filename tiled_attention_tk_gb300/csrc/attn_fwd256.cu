@@ -223,7 +223,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (operands stay warp-uniform); one
+        // elected lane sends each block of MMAs and each commit.
+        {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);  // K-major Q and K
             constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 0, 1);   // P from TMEM, V MN-major
             uint32_t taken = 0;   // K/V tiles consumed, in load order
@@ -242,28 +244,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
             // shared memory is below 256 KB).
             const uint64_t qd = smem_desc_sw128(sbase + Q_OFF, 16, 1024);
             const uint32_t q_lo = static_cast<uint32_t>(qd), d_hi = static_cast<uint32_t>(qd >> 32);
+            auto commit = [&](int b) {
+                if (elect_one()) umma_commit(bar(b));
+                __syncwarp();
+            };
             auto issue_s = [&](uint32_t s, uint32_t kslot) {  // S = Q K^T into S slot s
                 const uint32_t k_lo =
                     static_cast<uint32_t>(smem_desc_sw128(sbase + SLOT_OFF + kslot * TILE_BYTES, 16, 1024));
-                const uint32_t dst = tmem + tmem_s(s);
+                uint32_t a[D / 16], b[D / 16];
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = ((k / 4) * BOX_BYTES + (k % 4) * 32) >> 4;
-                    umma_ss_lo(dst, q_lo + off, d_hi, k_lo + off, d_hi, IDESC_S, k > 0 ? 1u : 0u);
+                    a[k] = q_lo + off;
+                    b[k] = k_lo + off;
                 }
-                umma_commit(bar(B_SFULL + s));
-                umma_commit(bar(B_SLOTEMPTY + kslot));
+                if (elect_one()) {
+                    umma_ss_steps<D / 16>(tmem + tmem_s(s), a, d_hi, b, d_hi, IDESC_S, 0u);
+                    umma_commit(bar(B_SFULL + s));
+                    umma_commit(bar(B_SLOTEMPTY + kslot));
+                }
+                __syncwarp();
             };
             auto issue_pv = [&](uint32_t s, uint32_t vslot, bool accumulate) {  // O += P V, P in S slot s
                 const uint64_t vd = smem_desc_sw128(sbase + SLOT_OFF + vslot * TILE_BYTES, BOX_BYTES, 1024);
                 const uint32_t v_lo = static_cast<uint32_t>(vd), v_hi = static_cast<uint32_t>(vd >> 32);
-                const uint32_t pa = tmem + tmem_s(s);
+                uint32_t b[BN / 16];
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                    umma_ts_lo(tmem + T_O, pa + k * 8, v_lo + ((k * 2048) >> 4), v_hi, IDESC_O,
-                               (accumulate || k > 0) ? 1u : 0u);
-                umma_commit(bar(B_PVDONE));
-                umma_commit(bar(B_SLOTEMPTY + vslot));
+                for (int k = 0; k < BN / 16; ++k) b[k] = v_lo + ((k * 2048) >> 4);
+                if (elect_one()) {
+                    // 16 keys per step: P advances 8 TMEM columns (two bf16 each)
+                    umma_ts_steps<BN / 16, 8>(tmem + T_O, tmem + tmem_s(s), b, v_hi, IDESC_O, accumulate ? 1u : 0u);
+                    umma_commit(bar(B_PVDONE));
+                    umma_commit(bar(B_SLOTEMPTY + vslot));
+                }
+                __syncwarp();
             };
 
             for (int r = 0; ok && r < rounds; ++r) {
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                     tc_fence_after_sync();
                     issue_s(g & 1, ks);
                     ++g;
-                    if (j == n_kv - 1) umma_commit(bar(B_QEMPTY));  // the unit's last S
+                    if (j == n_kv - 1) commit(B_QEMPTY);  // the unit's last S
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
                     const uint32_t gj = g0 + j, s = gj & 1;
@@ -301,14 +315,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                         tc_fence_after_sync();
                         issue_s(s, ks);  // over P_j, after the product that reads it
                         ++g;
-                        if (j + 2 == n_kv - 1) umma_commit(bar(B_QEMPTY));
+                        if (j + 2 == n_kv - 1) commit(B_QEMPTY);
                     }
                 }
                 if (!ok) break;
                 ++k_unit;
             }
             // Every MMA issued so far has completed before TMEM is released.
-            umma_commit(bar(B_MMADONE));
+            commit(B_MMADONE);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(B_MMADONE), 0) &&
                    global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {

@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (operands stay warp-uniform); one
+        // elected lane sends each block of products and each commit.
+        {
             constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);       // Q K^T
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
             constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
@@ -347,8 +349,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             // update, each once its operands are in place.
             auto issue_s = [&](int c) {
                 const uint32_t qb = sbase + QK_OFF + (c & 1) * 2 * BOX;
-                umma_ss(tmem + T_S, smem_desc_sw128(qb, 16, 1024), smem_desc_sw128(qb + BOX, 16, 1024), ID_S, 0);
-                umma_commit(bar(B_SFULL));
+                const uint64_t qd = smem_desc_sw128(qb, 16, 1024), kd = smem_desc_sw128(qb + BOX, 16, 1024);
+                if (elect_one()) {
+                    umma_ss(tmem + T_S, qd, kd, ID_S, 0);
+                    umma_commit(bar(B_SFULL));
+                }
+                __syncwarp();
             };
             bool ok = wait_bounded(bar(B_QKFULL), 0, abort_flag, (ROLE_BASED_MMA << 24) | (B_QKFULL << 16));
             if (ok) {
@@ -379,36 +385,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 // offset to the start-address field (no carry: smem < 256 KB).
                 const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
                 const uint32_t v1_lo = static_cast<uint32_t>(v1d), hi = static_cast<uint32_t>(v1d >> 32);
+                uint32_t v1v[C / 16];
 #pragma unroll
-                for (int k = 0; k < C / 16; ++k)
-                    umma_ts_lo(tmem + T_O, tmem + T_P + k * 8, v1_lo + ((k * 2048) >> 4), hi, ID_INTRA, k > 0);
+                for (int k = 0; k < C / 16; ++k) v1v[k] = v1_lo + ((k * 2048) >> 4);
+                if (elect_one()) umma_ts_steps<C / 16, 8>(tmem + T_O, tmem + T_P, v1v, hi, ID_INTRA, 0u);
+                __syncwarp();
                 // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
                 if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
                                         (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
-                if (c > 0 || has_prev) {
-                    const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
+                const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
+                uint32_t sv[F / 16];
 #pragma unroll
-                    for (int k = 0; k < F / 16; ++k)
-                        umma_ts_lo(tmem + T_O, tmem + T_PHIQ + k * 8, s_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4), hi,
-                                   ID_INTER, 1);
+                for (int k = 0; k < F / 16; ++k) sv[k] = s_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4);
+                if (elect_one()) {
+                    if (c > 0 || has_prev) umma_ts_steps<F / 16, 8>(tmem + T_O, tmem + T_PHIQ, sv, hi, ID_INTER, 1u);
+                    umma_commit(bar(B_ODONE));
                 }
-                umma_commit(bar(B_ODONE));
+                __syncwarp();
                 // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
                 if (!(ok = wait_bounded(bar(B_PHIKREADY), ph, abort_flag,
                                         (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | c)))
                     break;
                 tc_fence_after_sync();
                 const uint32_t pk_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024));
+                uint32_t pkv[C / 16];
 #pragma unroll
-                for (int k = 0; k < C / 16; ++k)
-                    umma_ss_lo(tmem + T_ST, v1_lo + ((k * 2048) >> 4), hi, pk_lo + ((k * 2048) >> 4), hi, ID_STATE,
-                               (c > 0 || has_prev || k > 0) ? 1u : 0u);
-                umma_commit(bar(B_STDONE));
-                umma_commit(bar(B_VEMPTY + b));
+                for (int k = 0; k < C / 16; ++k) pkv[k] = pk_lo + ((k * 2048) >> 4);
+                if (elect_one()) {
+                    umma_ss_steps<C / 16>(tmem + T_ST, v1v, hi, pkv, hi, ID_STATE, (c > 0 || has_prev) ? 1u : 0u);
+                    umma_commit(bar(B_STDONE));
+                    umma_commit(bar(B_VEMPTY + b));
+                }
+                __syncwarp();
             }
-            umma_commit(bar(B_MMADONE));
+            if (elect_one()) umma_commit(bar(B_MMADONE));
+            __syncwarp();
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
             }

@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (operands stay warp-uniform); one
+        // elected lane sends each stage's MMAs and each commit.
+        {
             constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0, KMAJOR_B ? 0 : 1);
             uint32_t n = 0;     // stages consumed
             uint32_t items = 0; // accumulators used
@@ -231,20 +233,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     tc_fence_after_sync();
                     const uint32_t a_src = sbase + STAGE_OFF + s * STAGE_BYTES;
                     const uint32_t b_src = a_src + A_BYTES;
+                    const uint64_t ad = smem_desc_sw128(a_src, 16, 1024);
+                    const uint64_t bd = KMAJOR_B ? smem_desc_sw128(b_src, 16, 1024)
+                                                 : smem_desc_sw128(b_src, 64 * BK * 2, 1024);
+                    uint32_t av[BK / 16], bv[BK / 16];
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a_src + kk * 32, 16, 1024);
-                        const uint64_t bdesc = KMAJOR_B ? smem_desc_sw128(b_src + kk * 32, 16, 1024)
-                                                        : smem_desc_sw128(b_src + kk * 2048, 64 * BK * 2, 1024);
-                        umma_ss(d, adesc, bdesc, IDESC, (k > it.kb || kk > 0) ? 1u : 0u);
+                        av[kk] = static_cast<uint32_t>(ad) + ((kk * 32) >> 4);
+                        bv[kk] = static_cast<uint32_t>(bd) + ((KMAJOR_B ? kk * 32 : kk * 2048) >> 4);
                     }
-                    umma_commit(bar(B_EMPTY + s));  // the stage is free once these MMAs are done
+                    if (elect_one()) {
+                        umma_ss_steps<BK / 16>(d, av, static_cast<uint32_t>(ad >> 32), bv, static_cast<uint32_t>(bd >> 32),
+                                               IDESC, k > it.kb ? 1u : 0u);
+                        umma_commit(bar(B_EMPTY + s));  // the stage is free once these MMAs are done
+                    }
+                    __syncwarp();
                 }
                 if (!ok) break;
-                umma_commit(bar(B_ACC_FULL + acc));
+                if (elect_one()) umma_commit(bar(B_ACC_FULL + acc));
+                __syncwarp();
                 ++items;
             }
-            umma_commit(bar(B_MMADONE));
+            if (elect_one()) umma_commit(bar(B_MMADONE));
+            __syncwarp();
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(B_MMADONE), 0) &&
                    global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {

@@ -265,7 +265,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (operands stay warp-uniform); one
+        // elected lane sends each block of products and each commit.
+        {
             constexpr uint32_t ID_Z = idesc_bf16_f32(C, FH, 0, 1);       // X W: X K-major, W MN-major
             constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);        // phi(Q) phi(K)^T: A in TMEM
             constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);   // P [V | 1]: A in TMEM
@@ -289,20 +291,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
             const uint32_t phik_lo = static_cast<uint32_t>(phikd), sprev_lo = static_cast<uint32_t>(sprevd);
             const uint32_t phikmn_lo = static_cast<uint32_t>(phikmn);
             auto issue_z = [&]() {  // Z = Q Wq, K Wk from the Q/K buffer, 16 of the 64 dims per step
+                uint32_t qv[DQK / 16], kv[DQK / 16], wqv[DQK / 16], wkv[DQK / 16];
 #pragma unroll
                 for (int k = 0; k < DQK / 16; ++k) {
-                    umma_ss_lo(tmem + T_Z, q_lo + ((k * 32) >> 4), hi, wq_lo + ((k * 2048) >> 4), hi, ID_Z, k > 0);
-                    umma_ss_lo(tmem + T_Z + FH, k_lo + ((k * 32) >> 4), hi, wk_lo + ((k * 2048) >> 4), hi, ID_Z, k > 0);
+                    qv[k] = q_lo + ((k * 32) >> 4);
+                    kv[k] = k_lo + ((k * 32) >> 4);
+                    wqv[k] = wq_lo + ((k * 2048) >> 4);
+                    wkv[k] = wk_lo + ((k * 2048) >> 4);
                 }
-                umma_commit(bar(B_ZFULL));
-                umma_commit(bar(B_QKEMPTY));
+                if (elect_one()) {
+                    umma_ss_steps<DQK / 16>(tmem + T_Z, qv, hi, wqv, hi, ID_Z, 0u);
+                    umma_ss_steps<DQK / 16>(tmem + T_Z + FH, kv, hi, wkv, hi, ID_Z, 0u);
+                    umma_commit(bar(B_ZFULL));
+                    umma_commit(bar(B_QKEMPTY));
+                }
+                __syncwarp();
             };
             auto issue_s = [&]() {  // S = phi(Q) phi(K)^T over the 128 features
+                uint32_t phikv[F / 16];
 #pragma unroll
-                for (int k = 0; k < F / 16; ++k)
-                    umma_ts_lo(tmem + T_Z, tmem + T_PHIQ + k * 8, phik_lo + (((k / 4) * BOX + (k % 4) * 32) >> 4), hi, ID_S,
-                               k > 0);
-                umma_commit(bar(B_SFULL));
+                for (int k = 0; k < F / 16; ++k) phikv[k] = phik_lo + (((k / 4) * BOX + (k % 4) * 32) >> 4);
+                if (elect_one()) {
+                    umma_ts_steps<F / 16, 8>(tmem + T_Z, tmem + T_PHIQ, phikv, hi, ID_S, 0u);
+                    umma_commit(bar(B_SFULL));
+                }
+                __syncwarp();
             };
             bool ok = wait_bounded(bar(B_WFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_WFULL << 16)) &&
                       wait_bounded(bar(B_QKFULL), 0, abort_flag, (ROLE_HH_MMA << 24) | (B_QKFULL << 16));
@@ -336,24 +349,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]
                 const uint32_t v1_lo = static_cast<uint32_t>(smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024));
+                uint32_t v1v[C / 16], pkv[C / 16], sprevv[F / 16];
 #pragma unroll
-                for (int k = 0; k < C / 16; ++k)
-                    umma_ts_lo(tmem + T_O, tmem + T_P + k * 8, v1_lo + ((k * 2048) >> 4), hi, ID_INTRA, k > 0);
-                // inter: [num | den] += phi(Q) S_{<c}
-                if (c > 0 || has_prev) {
-#pragma unroll
-                    for (int k = 0; k < F / 16; ++k)
-                        umma_ts_lo(tmem + T_O, tmem + T_PHIQ + k * 8, sprev_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4), hi,
-                                   ID_INTER, 1);
+                for (int k = 0; k < C / 16; ++k) {
+                    v1v[k] = v1_lo + ((k * 2048) >> 4);
+                    pkv[k] = phikmn_lo + ((k * 2048) >> 4);
                 }
-                umma_commit(bar(B_ODONE));
-                // state: S^T += [V | 1]^T phi(K)
 #pragma unroll
-                for (int k = 0; k < C / 16; ++k)
-                    umma_ss_lo(tmem + T_ST, v1_lo + ((k * 2048) >> 4), hi, phikmn_lo + ((k * 2048) >> 4), hi, ID_STATE,
-                               (c > 0 || has_prev || k > 0) ? 1u : 0u);
-                umma_commit(bar(B_STDONE));
-                umma_commit(bar(B_VEMPTY + b));
+                for (int k = 0; k < F / 16; ++k) sprevv[k] = sprev_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4);
+                if (elect_one()) {
+                    umma_ts_steps<C / 16, 8>(tmem + T_O, tmem + T_P, v1v, hi, ID_INTRA, 0u);
+                    // inter: [num | den] += phi(Q) S_{<c}
+                    if (c > 0 || has_prev) umma_ts_steps<F / 16, 8>(tmem + T_O, tmem + T_PHIQ, sprevv, hi, ID_INTER, 1u);
+                    umma_commit(bar(B_ODONE));
+                    // state: S^T += [V | 1]^T phi(K)
+                    umma_ss_steps<C / 16>(tmem + T_ST, v1v, hi, pkv, hi, ID_STATE, (c > 0 || has_prev) ? 1u : 0u);
+                    umma_commit(bar(B_STDONE));
+                    umma_commit(bar(B_VEMPTY + b));
+                }
+                __syncwarp();
                 // S of the next chunk, once its features and this chunk's state are in smem
                 if (c + 1 < n_chunks) {
                     if (!(ok = wait_bounded(bar(B_PHIREADY), ph ^ 1, abort_flag,
@@ -363,7 +377,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) hedgehog_kernel(const __grid_c
                     issue_s();
                 }
             }
-            umma_commit(bar(B_MMADONE));
+            if (elect_one()) umma_commit(bar(B_MMADONE));
+            __syncwarp();
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
             }

@@ -216,38 +216,65 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 // Four SS MMAs (A and B from shared memory) from descriptor low halves
-// formed beforehand (a[k], b[k]; the high half `hi` is shared); the first
+// formed beforehand (a[k], b[k]; high halves a_hi, b_hi); the first
 // accumulates iff `acc_first`, the rest always.
-__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, const uint32_t *a, const uint32_t *b, uint32_t hi,
-                                           uint32_t idesc, uint32_t acc_first) {
+__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, const uint32_t *a, uint32_t a_hi, const uint32_t *b,
+                                           uint32_t b_hi, uint32_t idesc, uint32_t acc_first) {
     asm volatile(
         "{\n\t.reg .pred pt, pa;\n\t.reg .b64 ad0, ad1, ad2, ad3, bd0, bd1, bd2, bd3;\n\t"
-        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %11, 0;\n\t"
-        "mov.b64 ad0, {%1, %9};\n\tmov.b64 bd0, {%5, %9};\n\t"
-        "mov.b64 ad1, {%2, %9};\n\tmov.b64 bd1, {%6, %9};\n\t"
-        "mov.b64 ad2, {%3, %9};\n\tmov.b64 bd2, {%7, %9};\n\t"
-        "mov.b64 ad3, {%4, %9};\n\tmov.b64 bd3, {%8, %9};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad0, bd0, %10, pa;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad1, bd1, %10, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad2, bd2, %10, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad3, bd3, %10, pt;\n\t}" ::"r"(d_tmem),
-        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(hi),
-        "r"(idesc), "r"(acc_first)
+        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %12, 0;\n\t"
+        "mov.b64 ad0, {%1, %9};\n\tmov.b64 bd0, {%5, %10};\n\t"
+        "mov.b64 ad1, {%2, %9};\n\tmov.b64 bd1, {%6, %10};\n\t"
+        "mov.b64 ad2, {%3, %9};\n\tmov.b64 bd2, {%7, %10};\n\t"
+        "mov.b64 ad3, {%4, %9};\n\tmov.b64 bd3, {%8, %10};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad0, bd0, %11, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad1, bd1, %11, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad2, bd2, %11, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad3, bd3, %11, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(a_hi),
+        "r"(b_hi), "r"(idesc), "r"(acc_first)
         : "memory");
 }
 
-// Two SS MMAs, the same (for head dims whose k steps are not a multiple of 4).
-__device__ __forceinline__ void umma_ss_x2(uint32_t d_tmem, const uint32_t *a, const uint32_t *b, uint32_t hi,
+// SS MMAs over KS k steps (groups of four, then single ones), the first
+// accumulating iff `acc_first`.
+template <int KS>
+__device__ __forceinline__ void umma_ss_steps(uint32_t d_tmem, const uint32_t (&a)[KS], uint32_t a_hi,
+                                              const uint32_t (&b)[KS], uint32_t b_hi, uint32_t idesc,
+                                              uint32_t acc_first) {
+#pragma unroll
+    for (int k = 0; k + 4 <= KS; k += 4) umma_ss_x4(d_tmem, a + k, a_hi, b + k, b_hi, idesc, k > 0 ? 1u : acc_first);
+#pragma unroll
+    for (int k = KS - KS % 4; k < KS; ++k) umma_ss_lo(d_tmem, a[k], a_hi, b[k], b_hi, idesc, k > 0 ? 1u : acc_first);
+}
+
+// Four TS MMAs (A from TMEM at a_tmem + k * ASTEP columns, B from shared
+// memory at b[k]); the first accumulates iff `acc_first`.
+template <int ASTEP>
+__device__ __forceinline__ void umma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, const uint32_t *b, uint32_t b_hi,
                                            uint32_t idesc, uint32_t acc_first) {
     asm volatile(
-        "{\n\t.reg .pred pt, pa;\n\t.reg .b64 ad0, ad1, bd0, bd1;\n\t"
-        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %7, 0;\n\t"
-        "mov.b64 ad0, {%1, %5};\n\tmov.b64 bd0, {%3, %5};\n\t"
-        "mov.b64 ad1, {%2, %5};\n\tmov.b64 bd1, {%4, %5};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad0, bd0, %6, pa;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad1, bd1, %6, pt;\n\t}" ::"r"(d_tmem),
-        "r"(a[0]), "r"(a[1]), "r"(b[0]), "r"(b[1]), "r"(hi), "r"(idesc), "r"(acc_first)
+        "{\n\t.reg .pred pt, pa;\n\t.reg .b64 bd0, bd1, bd2, bd3;\n\t"
+        "setp.eq.u32 pt, 1, 1;\n\tsetp.ne.u32 pa, %8, 0;\n\t"
+        "mov.b64 bd0, {%2, %6};\n\tmov.b64 bd1, {%3, %6};\n\tmov.b64 bd2, {%4, %6};\n\tmov.b64 bd3, {%5, %6};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd0, %7, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+%9], bd1, %7, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+%10], bd2, %7, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+%11], bd3, %7, pt;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b_hi), "r"(idesc), "r"(acc_first),
+        "n"(ASTEP), "n"(2 * ASTEP), "n"(3 * ASTEP)
         : "memory");
+}
+
+// TS MMAs over KS k steps (groups of four, then single ones), A advancing
+// ASTEP columns per step; the first accumulates iff `acc_first`.
+template <int KS, int ASTEP>
+__device__ __forceinline__ void umma_ts_steps(uint32_t d_tmem, uint32_t a_tmem, const uint32_t (&b)[KS],
+                                              uint32_t b_hi, uint32_t idesc, uint32_t acc_first) {
+#pragma unroll
+    for (int k = 0; k + 4 <= KS; k += 4) umma_ts_x4<ASTEP>(d_tmem, a_tmem + k * ASTEP, b + k, b_hi, idesc, k > 0 ? 1u : acc_first);
+#pragma unroll
+    for (int k = KS - KS % 4; k < KS; ++k) umma_ts_lo(d_tmem, a_tmem + k * ASTEP, b[k], b_hi, idesc, k > 0 ? 1u : acc_first);
 }
 
 // Eight TS MMAs (A from TMEM, B from shared memory) over 128 keys: A advances
