@@ -39,9 +39,19 @@ torch.matmul) timed beside it for context.
 runnable reference implementation), timed on this host's cores on a bounded
 sample of the same workload per step.
 
-Multi-GPU (torchrun, one rank per GPU): every rank runs the full workload on
-its own GPU (independent problems, no data-path collective); the step time is
-the max over ranks and ``value`` counts the flops of all ranks (weak scaling).
+The forward line also carries ``parity`` (the timed launch's O and LSE
+against the fp64 oracle on sampled heads and rows, with the target's bars)
+and, for the default workload, ``configs``: kernel time, TFLOP/s, fraction of
+peak and parity of the other four workloads, measured in the same process.
+
+Multi-GPU (one rank per GPU; ``--gpus N`` alone re-runs the script under
+torchrun): the B*H heads of the one workload are split into contiguous
+slices, one per rank, and each rank runs tk_attn_fwd on its slice as a
+[1, heads, N, D] problem.  No data-path collective: the step time is the max
+over ranks and ``value`` is the whole workload's flops over that time
+(strong scaling).  ``--gather`` also times an NCCL all-gather of O and LSE,
+reported apart.  The backward, GEMM and linear-attention modes run the full
+problem on every rank (weak scaling).
 """
 from __future__ import annotations
 
@@ -311,16 +321,24 @@ class ClockSampler:
                 "samples": len(sms), "source": "nvidia-smi"}
 
 
+def l2_description(in_bytes: int) -> str:
+    """How the timed region treats L2 for inputs of `in_bytes` (the same text
+    in both arms' config)."""
+    if in_bytes > L2_BYTES:
+        return f"inputs {in_bytes / 2**20:.0f} MiB > {L2_BYTES >> 20} MiB L2, no flush"
+    return (f"inputs {in_bytes / 2**20:.0f} MiB fit in L2: a {2 * L2_BYTES >> 20} MiB write flushes L2 "
+            "before every timed launch (outside its events)")
+
+
 def l2_flusher(in_bytes: int, dev):
     """(buffer, description): where the timed launch's inputs fit in L2, a
     buffer of twice L2 that is written before every timed launch, outside its
     event pair, so that no launch starts on operands left in L2 by the last."""
     import torch
     if in_bytes > L2_BYTES:
-        return None, f"inputs {in_bytes / 2**20:.0f} MiB > {L2_BYTES >> 20} MiB L2, no flush"
+        return None, l2_description(in_bytes)
     buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
-    return buf, (f"inputs {in_bytes / 2**20:.0f} MiB fit in L2: a {2 * L2_BYTES >> 20} MiB write flushes L2 "
-                 "before every timed launch (outside its events)")
+    return buf, l2_description(in_bytes)
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -365,92 +383,258 @@ def time_oracle_sample(w, q, k, v, budget_s: float, min_rows: int = 64):
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, w):
+def shard(bh_total: int, world: int, rank: int):
+    """(first, count): the contiguous slice of the B*H heads that rank
+    `rank` of `world` computes.  The first bh_total % world ranks take one
+    head more; every head belongs to exactly one rank."""
+    base, extra = divmod(bh_total, world)
+    first = rank * base + min(rank, extra)
+    return first, base + (1 if rank < extra else 0)
+
+
+def parity_rows(w, limit: int = 320):
+    """Query rows compared with the oracle in one head: all of them for
+    short sequences, else the first and last 64, both sides of every fourth
+    128-row tile boundary and a seeded draw, `limit` rows at most."""
+    if w.N <= limit:
+        return list(range(w.N))
+    import random
+    rows = set(range(64)) | set(range(w.N - 64, w.N))
+    for t in range(128, w.N, 512):
+        rows.update((t - 1, t))
+    rnd = random.Random(1000 * w.index + w.N)
+    while len(rows) < limit:
+        rows.add(rnd.randrange(w.N))
+    return sorted(rows)
+
+
+def parity_check(w, q, k, v, o, lse, heads, first: int = 0):
+    """O and LSE of the given global heads (b*H + h, inside this rank's slice
+    that starts at head `first`) against the fp64 oracle on sampled rows.
+    Returns the error figures with the pass/fail of the target's bars."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    rows = parity_rows(w)
+    o_max = o_sum = lse_max = 0.0
+    count = 0
+    for gh in heads:
+        b, h = divmod(gh, w.H)
+        O_ref, L_ref = oracle.attn_fwd_rows(q[b, h], k[b, h], v[b, h], rows, w.causal, w.scale)
+        o_gpu = o[gh - first][rows].double().cpu().numpy()
+        l_gpu = lse[gh - first][rows].double().cpu().numpy()
+        e = np.abs(o_gpu - O_ref)
+        o_max = max(o_max, float(e.max()))
+        o_sum += float(e.sum())
+        count += e.size
+        lse_max = max(lse_max, float(np.abs(l_gpu - L_ref).max()))
+    o_mean = o_sum / max(count, 1)
+    return {"heads": len(heads), "rows_per_head": len(rows), "o_max": float(f"{o_max:.3e}"),
+            "o_mean": float(f"{o_mean:.3e}"), "lse_max": float(f"{lse_max:.3e}"),
+            "ok": bool(o_max <= 2e-2 and o_mean <= 2e-3 and lse_max <= 1e-3)}
+
+
+def parity_heads(first: int, count: int, n: int = 4, seed: int = 11):
+    """Up to n global heads of the slice [first, first+count): its first and
+    last head and a seeded draw of the rest."""
+    if count <= 0:
+        return []
+    if count <= n:
+        return list(range(first, first + count))
+    import random
+    chosen = {first, first + count - 1}
+    rnd = random.Random(seed + first)
+    while len(chosen) < n:
+        chosen.add(first + rnd.randrange(count))
+    return sorted(chosen)
+
+
+class ForwardRun:
+    """One workload on this rank: its slice of the heads resident on the
+    device, and the launch of tk_attn_fwd (tk_attn_fwd_kv when Nq != Nkv)
+    over that slice as one [1, count, N, D] problem."""
+
+    def __init__(self, w, dev, ws: int, rank: int):
+        import torch
+        from tiled_attention_tk_gb300.inputs import workload_inputs
+        self.w = w
+        self.first, self.count = shard(w.B * w.H, ws, rank)
+        q, k, v = workload_inputs(w)
+        self.q, self.k, self.v = q, k, v
+        sl = slice(self.first, self.first + self.count)
+        self.qd = q.reshape(w.B * w.H, w.N, w.D)[sl].to(dev)
+        self.kd = k.reshape(w.B * w.H, w.Nkv, w.D)[sl].to(dev)
+        self.vd = v.reshape(w.B * w.H, w.Nkv, w.D)[sl].to(dev)
+        self.o = torch.empty_like(self.qd)
+        self.lse = torch.empty((self.count, w.N), dtype=torch.float32, device=dev)
+        self.in_bytes = self.count * (w.N + 2 * w.Nkv) * w.D * 2
+
+    def launch(self, stream_handle: int):
+        import tiled_attention_tk_gb300 as tk
+        w = self.w
+        if self.count == 0:
+            return
+        ptrs = (self.qd.data_ptr(), self.kd.data_ptr(), self.vd.data_ptr(), self.o.data_ptr(), self.lse.data_ptr())
+        if w.Nkv == w.N:
+            tk.fwd_raw(*ptrs, 1, self.count, w.N, w.D, w.causal, w.scale, stream_handle)
+        else:
+            tk.fwd_kv_raw(*ptrs, 1, self.count, w.N, w.Nkv, w.D, w.causal, w.scale, stream_handle)
+
+
+def time_launches(run, steps: int, warmup: int, dev, stream, flush, dist_mod):
+    """Warm-up, then `steps` timed launches, each in its own event pair, with
+    the whole region in one more pair.  Returns (total ms of the region, mean
+    ms per launch); with an L2 flush between launches the region's time is the
+    sum of the launches' own times."""
     import torch
     import tiled_attention_tk_gb300 as tk
-    from tiled_attention_tk_gb300.inputs import workload_inputs
-
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dist_mod = init_dist(ws, "nccl")
-    dev = torch.device("cuda", local)
-
-    q, k, v = workload_inputs(w)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
-    qp, kp, vp, op, lp = qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr()
-
-    def step():
-        if w.Nkv == w.N:
-            tk.fwd_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.D, w.causal, w.scale, sh)
-        else:
-            tk.fwd_kv_raw(qp, kp, vp, op, lp, w.B, w.H, w.N, w.Nkv, w.D, w.causal, w.scale, sh)
-
-    for _ in range(args.warmup):
-        step()
+    for _ in range(warmup):
+        run.launch(sh)
     torch.cuda.synchronize(dev)
     st, detail = tk.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush, l2_desc = l2_flusher(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2, dev)
-    sampler = ClockSampler(local)
     if dist_mod:
         dist_mod.barrier()
     torch.cuda.synchronize(dev)
     start_ev.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             flush.zero_()
         ev[i][0].record(stream)
-        step()
+        run.launch(sh)
         ev[i][1].record(stream)
     end_ev.record(stream)
     torch.cuda.synchronize(dev)
     if dist_mod:
         dist_mod.barrier()
-    clocks = sampler.stop()
-    total_ms = start_ev.elapsed_time(end_ev)
-    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     st, detail = tk.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
-    # with flushes in the region, a step is its own event pair
-    total_ms = max_over_ranks(total_ms if flush is None else kernel_ms * args.steps, dist_mod, dev)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    total_ms = kernel_ms * steps if flush is not None else start_ev.elapsed_time(end_ev)
+    return total_ms, kernel_ms
+
+
+# Workloads measured beside the default line (kernel time, TFLOP/s, fraction
+# of peak, parity on sampled heads) within the same process.
+SIDE_WORKLOADS = (1, 2, 3, 5)
+
+
+def measure_side_configs(args, dev, stream, dist_mod, ws, rank, peak):
+    import torch
+    from tiled_attention_tk_gb300.inputs import WORKLOADS
+    out = {}
+    for idx in SIDE_WORKLOADS:
+        w = WORKLOADS[idx]
+        run = ForwardRun(w, dev, ws, rank)
+        flush, _ = l2_flusher(max(run.in_bytes, 1), dev)
+        steps = 200 if w.flops < 1e10 else 20
+        _, kernel_ms = time_launches(run, steps, 3, dev, stream, flush, dist_mod)
+        kernel_ms = max_over_ranks(kernel_ms, dist_mod, dev)
+        tf = w.flops / (kernel_ms * 1e-3) / 1e12
+        entry = {"kernel_ms": round(kernel_ms, 5), "tflops": round(tf, 2), "frac": round(tf / peak, 4),
+                 "l2_flush": flush is not None}
+        if rank == 0 and not args.no_parity:
+            entry["parity"] = parity_check(w, run.q, run.k, run.v, run.o, run.lse,
+                                           parity_heads(run.first, run.count, 2), run.first)
+        out[w.name] = entry
+        del run, flush
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, w):
+    import torch
+    import tiled_attention_tk_gb300 as tk
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_mod = init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    run = ForwardRun(w, dev, ws, rank)
+    flush, l2_desc = l2_flusher(max(run.in_bytes, 1), dev)
+    sampler = ClockSampler(local)
+    total_ms, kernel_ms = time_launches(run, args.steps, args.warmup, dev, stream, flush, dist_mod)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(total_ms, dist_mod, dev)
     ms_per_step = total_ms / args.steps
-    value = w.flops * ws / (ms_per_step * 1e-3) / 1e12
+    # strong scaling: the ranks share one workload, so the whole workload's
+    # flops count once against the slowest rank's time
+    value = w.flops / (ms_per_step * 1e-3) / 1e12
+
+    parity = None
+    if rank == 0 and not args.no_parity:
+        parity = parity_check(w, run.q, run.k, run.v, run.o, run.lse, parity_heads(run.first, run.count),
+                              run.first)
+
+    # ---- optional all-gather of every rank's O and LSE to all ranks (NCCL),
+    # timed on its own: the forward itself needs no exchange
+    gather = None
+    if dist_mod is not None and args.gather:
+        base, extra = divmod(w.B * w.H, ws)
+        cnt = base + (1 if extra else 0)  # the largest slice; smaller ones are padded
+        o_pad = torch.zeros((cnt, w.N, w.D), dtype=torch.bfloat16, device=dev)
+        l_pad = torch.zeros((cnt, w.N), dtype=torch.float32, device=dev)
+        o_pad[:run.count].copy_(run.o)
+        l_pad[:run.count].copy_(run.lse)
+        o_all = [torch.empty_like(o_pad) for _ in range(ws)]
+        l_all = [torch.empty_like(l_pad) for _ in range(ws)]
+        dist_mod.all_gather(o_all, o_pad)
+        dist_mod.all_gather(l_all, l_pad)
+        torch.cuda.synchronize(dev)
+        dist_mod.barrier()
+        t0 = time.perf_counter()
+        for _ in range(5):
+            dist_mod.all_gather(o_all, o_pad)
+            dist_mod.all_gather(l_all, l_pad)
+        torch.cuda.synchronize(dev)
+        g_ms = max_over_ranks((time.perf_counter() - t0) / 5 * 1e3, dist_mod, dev)
+        gather = {"ms_per_step": round(g_ms, 4), "bytes_per_rank": (o_pad.numel() * 2 + l_pad.numel() * 4),
+                  "collective": "all_gather (NCCL) of O and LSE"}
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        sl = slice(run.first, run.first + run.count)
+        qh = run.q.reshape(w.B * w.H, w.N, w.D)[sl].reshape(1, run.count, w.N, w.D).pin_memory()
+        kh = run.k.reshape(w.B * w.H, w.Nkv, w.D)[sl].reshape(1, run.count, w.Nkv, w.D).pin_memory()
+        vh = run.v.reshape(w.B * w.H, w.Nkv, w.D)[sl].reshape(1, run.count, w.Nkv, w.D).pin_memory()
         e2e_steps = max(3, min(20, args.steps // 50))
-        tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)  # warm
+        if run.count:
+            tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)  # warm
         if dist_mod:
             dist_mod.barrier()
         t0 = time.perf_counter()
+        oh = lh = None
         for _ in range(e2e_steps):
-            oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
+            if run.count:
+                oh, lh = tk.fwd(qh, kh, vh, causal=w.causal, scale=w.scale)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
         e2e_s = max_over_ranks(e2e_s, dist_mod, dev)
-        h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
-        d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
-        e2e = {"value": round(w.flops * ws / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+        h2d = (qh.numel() + kh.numel() + vh.numel()) * qh.element_size()
+        d2h = (oh.numel() * oh.element_size() + lh.numel() * lh.element_size()) if oh is not None else 0
+        e2e = {"value": round(w.flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s * 1e3, 3), "steps": e2e_steps}
+               "ms_per_step": round(e2e_s * 1e3, 3), "steps": e2e_steps,
+               "path": "tk.fwd on pinned host tensors: heads in chunks over two streams, copies in and out "
+                       "overlapping the kernels"}
+
+    peak, peak_label = peaks()
+    side = None
+    if args.side_configs and not args.all and not args.shape:
+        side = measure_side_configs(args, dev, stream, dist_mod, ws, rank, peak)
 
     if rank != 0:
         if dist_mod:
             dist_mod.barrier()
         return None
-    peak, peak_label = peaks()
-    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+    achieved = w.flops * (run.count / (w.B * w.H)) / (kernel_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -460,21 +644,31 @@ def run_ours(args, w):
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
-        "config": dict(w.describe(), l2=l2_desc),
+        "config": dict(w.describe(), l2=l2_description(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2)),
+        "sharding": {"ranks": ws, "heads": w.B * w.H,
+                     "rule": "rank r computes a contiguous slice of the B*H heads (the first B*H % ranks "
+                             "ranks one head more); no data-path collective",
+                     "rank0_heads": [run.first, run.first + run.count]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": peak_label, "traffic": traffic_for(w.name),
-                     "kernel": f"attn_fwd_kernel<{w.D}>", "kernel_ms": round(kernel_ms, 5)},
+                     "peak_source": peak_label, "traffic": traffic_for(w.name) if ws == 1 else None,
+                     "kernel": f"attn_fwd_kernel<{w.D}>" if w.D != 256 else "attn_fwd256_kernel<256>",
+                     "kernel_ms": round(kernel_ms, 5)},
+        "parity": parity,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps if run.count else 0,
         "clocks": clocks,
     }
+    if side is not None:
+        line["configs"] = side
+    if gather is not None:
+        line["gather"] = gather
     if not args.no_cpu_baseline:
-        tf, cores, desc = time_oracle_sample(w, q, k, v, budget_s=args.cpu_budget)
+        tf, cores, desc = time_oracle_sample(w, run.q, run.k, run.v, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores,
                                 "kind": "oracle", "sample": desc}
     if dist_mod:
@@ -985,17 +1179,36 @@ def run_reference(args, w):
         "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
-        "config": w.describe(),
+        "config": dict(w.describe(), l2=l2_description(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2)),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def relaunch_cmd(n: int, argv, port: int):
+    """The torchrun command that runs this script as n ranks on one node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+
+
+def relaunch_ranks(n: int, argv) -> int:
+    """Runs the benchmark as n ranks (rank 0 prints the line) and returns
+    their exit status."""
+    return subprocess.call(relaunch_cmd(n, argv, free_port()))
 
 
 def main(argv=None):
@@ -1020,12 +1233,21 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--reference-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the check of the timed launch's O/LSE against the oracle on sampled heads")
+    ap.add_argument("--no-side-configs", dest="side_configs", action="store_false",
+                    help="skip the other workloads measured beside the default line")
+    ap.add_argument("--gather", action="store_true",
+                    help="under several ranks, also time an all-gather of every rank's O and LSE")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, _ = dist_env()
     if ws != args.gpus and ws != 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: start the ranks under torchrun, same arguments
+        sys.exit(relaunch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv)))
 
     if args.shape:
         f = [int(x) for x in args.shape.split(",")]

@@ -332,6 +332,15 @@ int tk_hedgehog_fwd_ws(const void *Q, const void *K, const void *V, const void *
  * call, TK_ERR_DEVICE_TIMEOUT if one has, TK_ERR_CUDA if the synchronisation
  * itself failed.  *detail (may be NULL) receives the role and step at which
  * the first wait gave up (0 if none).
+ *
+ * Scope: the status word belongs to the library on one device, not to a
+ * stream or a call.  Kernels of every stream on that device record into it,
+ * and the first timeout since the last read wins (later ones are dropped).
+ * The call synchronises only `stream`: a timeout raised by a kernel still
+ * running on another stream is seen by whichever call reads the word after
+ * that kernel has finished, and reading clears it for every caller.  A
+ * program that needs per-stream attribution calls this once per stream with
+ * the other streams idle (for instance after cudaDeviceSynchronize()).
  */
 int tk_attn_device_status(cudaStream_t stream, uint32_t *detail);
 

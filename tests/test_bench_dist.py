@@ -1,7 +1,7 @@
 """The multi-rank host logic of bench.py on CPU: two gloo ranks, as torchrun
-would start them.  Every rank runs its own full workload (independent
-problems, no data-path collective); the step time reported is the max over
-ranks and the value counts the work of all ranks."""
+would start them.  The ranks split the B*H heads of one workload into
+contiguous slices (no data-path collective); the step time reported is the
+max over ranks."""
 import os
 import socket
 
@@ -78,3 +78,100 @@ def test_reference_arm_line_on_rank0(monkeypatch):
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"] == WORKLOADS[1].name
+
+
+@pytest.mark.parametrize("bh,world", [(512, 8), (32, 2), (7, 2), (5, 8), (1, 2), (64, 3), (100, 7)])
+def test_shard_covers_every_head_once(bh, world):
+    import bench
+    seen = []
+    for r in range(world):
+        first, count = bench.shard(bh, world, r)
+        assert count >= 0
+        seen.extend(range(first, first + count))
+    assert seen == list(range(bh))  # contiguous, in rank order, each head once
+    counts = [bench.shard(bh, world, r)[1] for r in range(world)]
+    assert max(counts) - min(counts) <= 1
+
+
+def _shard_oracle_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE=str(world))
+    import numpy as np
+    import torch
+    import bench
+    import oracle
+    from tiled_attention_tk_gb300.inputs import make_qkv
+    dist = bench.init_dist(world, "gloo")
+    B, H, N, D = 1, 5, 40, 16  # 5 heads over 2 ranks: 3 + 2
+    q, k, v = make_qkv(B, H, N, D, 9100)
+    first, count = bench.shard(B * H, world, rank)
+    sl = slice(first, first + count)
+    qs = q.reshape(B * H, N, D)[sl].reshape(1, count, N, D)
+    ks = k.reshape(B * H, N, D)[sl].reshape(1, count, N, D)
+    vs = v.reshape(B * H, N, D)[sl].reshape(1, count, N, D)
+    O, L = oracle.attn_fwd(qs, ks, vs, True, 0.25)
+    # every rank's slice to every rank (padded to the largest slice)
+    cnt = bench.shard(B * H, world, 0)[1]
+    o_pad = torch.zeros((cnt, N, D), dtype=torch.float64)
+    l_pad = torch.zeros((cnt, N), dtype=torch.float64)
+    o_pad[:count] = torch.from_numpy(O[0])
+    l_pad[:count] = torch.from_numpy(L[0])
+    o_all = [torch.empty_like(o_pad) for _ in range(world)]
+    l_all = [torch.empty_like(l_pad) for _ in range(world)]
+    dist.all_gather(o_all, o_pad)
+    dist.all_gather(l_all, l_pad)
+    if rank == 0:
+        parts_o, parts_l = [], []
+        for r in range(world):
+            c = bench.shard(B * H, world, r)[1]
+            parts_o.append(o_all[r][:c])
+            parts_l.append(l_all[r][:c])
+        o_cat = torch.cat(parts_o).numpy().reshape(B, H, N, D)
+        l_cat = torch.cat(parts_l).numpy().reshape(B, H, N)
+        O_full, L_full = oracle.attn_fwd(q, k, v, True, 0.25)
+        out["equal"] = bool(np.array_equal(o_cat, O_full) and np.array_equal(l_cat, L_full))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_sharded_oracle_results_reassemble_bitwise():
+    """Per-slice results of two gloo ranks, gathered and put back in head
+    order, equal the whole-problem oracle bit for bit."""
+    import oracle
+    oracle.build()
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_shard_oracle_worker, args=(world, port, out), nprocs=world, join=True)
+        assert out["equal"] is True
+
+
+def test_gpus_without_torchrun_relaunches_ranks(monkeypatch):
+    """--gpus N outside torchrun runs the script as N ranks rather than
+    printing a one-rank line."""
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    import bench
+    cmd = bench.relaunch_cmd(4, ["--gpus", "4", "--steps", "5"], 29500)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "5"]
+    calls = []
+    monkeypatch.setattr(bench, "relaunch_ranks", lambda n, argv: calls.append((n, list(argv))) or 0)
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2", "--steps", "3", "--warmup", "3"])
+    assert e.value.code == 0 and calls == [(2, ["--gpus", "2", "--steps", "3", "--warmup", "3"])]
+
+
+def test_parity_rows_cover_edges():
+    import bench
+    from tiled_attention_tk_gb300.inputs import WORKLOADS
+    w = WORKLOADS[5]
+    rows = bench.parity_rows(w)
+    assert rows[0] == 0 and rows[-1] == w.N - 1 and len(rows) <= 320 and len(set(rows)) == len(rows)
+    assert 127 in rows and 128 in rows
+    assert bench.parity_rows(WORKLOADS[1]) == list(range(128))
+    assert bench.parity_heads(10, 3) == [10, 11, 12]
+    h = bench.parity_heads(0, 512)
+    assert h[0] == 0 and h[-1] == 511 and len(h) == 4

@@ -88,20 +88,60 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     return out, lse
 
 
-def _fwd_from_host(q, k, v, causal, scale, stream):
+_side_streams = {}
+
+
+def _side_stream(dev: torch.device):
+    if dev.index not in _side_streams:
+        _side_streams[dev.index] = torch.cuda.Stream(dev)
+    return _side_streams[dev.index]
+
+
+def _fwd_from_host(q, k, v, causal, scale, stream, chunk_bytes: int = 32 << 20):
+    """Host tensors in and out.  With pinned inputs the heads go in chunks
+    over two streams, so that one chunk's copy in, another's kernel and a
+    third's copy out overlap; each chunk is one tk_attn_fwd launch over its
+    heads as a [1, heads, N, D] problem."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    pinned = q.is_pinned()
-    with torch.cuda.stream(s):
-        qd = q.to(dev, non_blocking=True)
-        kd = k.to(dev, non_blocking=True)
-        vd = v.to(dev, non_blocking=True)
-        o, lse = fwd(qd, kd, vd, causal, scale, stream=s)
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=pinned)
-        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=pinned)
-        o_h.copy_(o, non_blocking=True)
-        l_h.copy_(lse, non_blocking=True)
-    s.synchronize()
+    main = stream if stream is not None else torch.cuda.current_stream(dev)
+    B, H, N, D = q.shape
+    Nkv = k.shape[2]
+    BH = B * H
+    pinned = q.is_pinned() and k.is_pinned() and v.is_pinned()
+    o_h = torch.empty((B, H, N, D), dtype=torch.bfloat16, pin_memory=pinned)
+    l_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pinned)
+    per_head = (N + 2 * Nkv) * D * 2
+    n_chunks = max(1, min(BH, (BH * per_head) // chunk_bytes)) if pinned else 1
+    qf, kf, vf = q.reshape(BH, N, D), k.reshape(BH, Nkv, D), v.reshape(BH, Nkv, D)
+    of, lf = o_h.reshape(BH, N, D), l_h.reshape(BH, N)
+    streams = [main, _side_stream(dev)] if n_chunks > 1 else [main]
+    main_done = torch.cuda.Event()
+    main_done.record(torch.cuda.current_stream(dev))
+    for s in streams:
+        s.wait_event(main_done)
+    qd = torch.empty((BH, N, D), dtype=torch.bfloat16, device=dev)
+    kd = torch.empty((BH, Nkv, D), dtype=torch.bfloat16, device=dev)
+    vd = torch.empty((BH, Nkv, D), dtype=torch.bfloat16, device=dev)
+    od = torch.empty((BH, N, D), dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((BH, N), dtype=torch.float32, device=dev)
+    for c in range(n_chunks):
+        h0, h1 = c * BH // n_chunks, (c + 1) * BH // n_chunks
+        if h1 == h0:
+            continue
+        s = streams[c % len(streams)]
+        with torch.cuda.stream(s):
+            qd[h0:h1].copy_(qf[h0:h1], non_blocking=True)
+            kd[h0:h1].copy_(kf[h0:h1], non_blocking=True)
+            vd[h0:h1].copy_(vf[h0:h1], non_blocking=True)
+            ptrs = (qd[h0].data_ptr(), kd[h0].data_ptr(), vd[h0].data_ptr(), od[h0].data_ptr(), ld[h0].data_ptr())
+            if Nkv == N:
+                fwd_raw(*ptrs, 1, h1 - h0, N, D, causal, scale, int(s.cuda_stream))
+            else:
+                fwd_kv_raw(*ptrs, 1, h1 - h0, N, Nkv, D, causal, scale, int(s.cuda_stream))
+            of[h0:h1].copy_(od[h0:h1], non_blocking=True)
+            lf[h0:h1].copy_(ld[h0:h1], non_blocking=True)
+    for s in streams:
+        s.synchronize()
     return o_h, l_h
 
 
