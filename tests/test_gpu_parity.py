@@ -208,3 +208,24 @@ def test_bounded_wait_reports_timeout_and_context_survives(oracle_mod):
     assert tk.device_status()[0] == 0, "status must clear after reading"
     q, k, v = make_qkv(1, 1, 64, 64, 37)
     _check_full(oracle_mod, q, k, v, False, 0.125, "after timeout")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal,Nkv", [(False, 700), (True, 700), (True, 1100)])
+def test_host_inputs_in_chunks_equal_device_launch(causal, Nkv):
+    """Pinned host inputs go to the device in chunks of heads over two streams
+    (copies overlapping kernels); each chunk is its own launch over its heads.
+    Heads are independent and each launch is deterministic, so the result
+    equals one launch over all heads bit for bit."""
+    from tiled_attention_tk_gb300 import attention
+    from tiled_attention_tk_gb300.inputs import make_qkv_rect
+    B, H, Nq, D = 2, 5, 700, 128
+    q, k, v = make_qkv_rect(B, H, Nq, Nkv, D, 5150 + Nkv + causal)
+    o_dev, l_dev = tk.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, l_h = attention._fwd_from_host(qh, kh, vh, causal, 1.0 / math.sqrt(D), None, chunk_bytes=600_000)
+    torch.cuda.synchronize()
+    assert o_h.device.type == "cpu" and o_h.is_pinned()
+    assert torch.equal(o_h, o_dev.cpu()) and torch.equal(l_h, l_dev.cpu())
+    st, detail = tk.device_status()
+    assert st == 0, (st, detail)

@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 float s[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
-                if (j == n_kv - 1 || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
+                if ((j + 1) * BN > p.Nkv || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
                     // A key tile that some row of this Q tile does not see in
                     // full: the ragged tail (keys >= Nkv) and, under the
                     // causal mask, keys past row + offset take -inf.

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                 float sv[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) sv[i] = __uint_as_float(sr[i]);
-                if (j == n_kv - 1 || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
+                if ((j + 1) * BN > p.Nkv || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
                     // the ragged tail (keys >= Nkv) and, under the causal mask,
                     // keys past row + offset take -inf
                     const int limit = p.causal ? min(row + 1 + p.offset, p.Nkv) : p.Nkv;
