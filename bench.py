@@ -451,8 +451,9 @@ def parity_heads(first: int, count: int, n: int = 4, seed: int = 11):
 
 class ForwardRun:
     """One workload on this rank: its slice of the heads resident on the
-    device, and the launch of tk_attn_fwd (tk_attn_fwd_kv when Nq != Nkv)
-    over that slice as one [1, count, N, D] problem."""
+    device, and the launch of tk_attn_fwd_ws over that slice as one
+    [1, count, N, D] problem (with its workspace when the shape's last round
+    of work units is split by key tiles)."""
 
     def __init__(self, w, dev, ws: int, rank: int):
         import torch
@@ -468,6 +469,10 @@ class ForwardRun:
         self.o = torch.empty_like(self.qd)
         self.lse = torch.empty((self.count, w.N), dtype=torch.float32, device=dev)
         self.in_bytes = self.count * (w.N + 2 * w.Nkv) * w.D * 2
+        import tiled_attention_tk_gb300 as tk
+        with torch.cuda.device(dev):
+            self.ws_bytes = tk.fwd_workspace_bytes(1, self.count, w.N, w.Nkv, w.D, w.causal) if self.count else 0
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev) if self.ws_bytes else None
 
     def launch(self, stream_handle: int):
         import tiled_attention_tk_gb300 as tk
@@ -475,10 +480,8 @@ class ForwardRun:
         if self.count == 0:
             return
         ptrs = (self.qd.data_ptr(), self.kd.data_ptr(), self.vd.data_ptr(), self.o.data_ptr(), self.lse.data_ptr())
-        if w.Nkv == w.N:
-            tk.fwd_raw(*ptrs, 1, self.count, w.N, w.D, w.causal, w.scale, stream_handle)
-        else:
-            tk.fwd_kv_raw(*ptrs, 1, self.count, w.N, w.Nkv, w.D, w.causal, w.scale, stream_handle)
+        tk.fwd_ws_raw(*ptrs, self.ws.data_ptr() if self.ws is not None else None, self.ws_bytes, 1, self.count,
+                      w.N, w.Nkv, w.D, w.causal, w.scale, stream_handle)
 
 
 def time_launches(run, steps: int, warmup: int, dev, stream, flush, dist_mod):
@@ -648,7 +651,8 @@ def run_ours(args, w):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded torch.Generator, fp32 draws rounded to bf16)",
-        "config": dict(w.describe(), l2=l2_description(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2)),
+        "config": dict(w.describe(), l2=l2_description(w.B * w.H * (w.N + 2 * w.Nkv) * w.D * 2),
+                       tail_split=bool(run.ws_bytes)),
         "sharding": {"ranks": ws, "heads": w.B * w.H,
                      "rule": "rank r computes a contiguous slice of the B*H heads (the first B*H % ranks "
                              "ranks one head more); no data-path collective",

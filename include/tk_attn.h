@@ -118,6 +118,48 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
                    float scale, cudaStream_t stream);
 
 /*
+ * tk_attn_fwd_workspace_bytes -- device workspace tk_attn_fwd_ws needs on
+ * the current device for this shape: nonzero only without the causal mask,
+ * at a head dim below 256, with at least 4 key tiles (Nkv > 384), when the
+ * work units (pairs of 128-row query tiles, B*H*ceil(ceil(Nq/128)/2) of
+ * them) fill some rounds of one unit per SM and leave a last round at most
+ * half full.  Then each unit of that round is split in two by key tiles:
+ * 2*T pieces for T tail units need 2*T*2*128*(D+1)*4 bytes of partial
+ * results (rounded up to 256) plus T*64 bytes of counters (rounded up to
+ * 256).  0 for any other shape, including one tk_attn_fwd_ws rejects.
+ * There is no counterpart on the pages: it balances the last round on this
+ * GPU's SM count.
+ */
+size_t tk_attn_fwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal);
+
+/*
+ * tk_attn_fwd_ws -- tk_attn_fwd_kv with the last, partial round of work
+ * units split by key tiles when tk_attn_fwd_workspace_bytes says so.  A
+ * split unit's two pieces each leave O/l (fp32) and their LSE in the
+ * workspace; the piece that publishes second merges them,
+ *     LSE = m + ln(w_a + w_b),  w = exp(LSE_piece - m),  m = max(LSE_a, LSE_b)
+ *     O   = (w_a O_a + w_b O_b) / (w_a + w_b),
+ * the same combination of partial softmax sums the online softmax uses
+ * across key tiles, with unfused fp32 products and sums so that the result
+ * does not depend on which piece merges.  Deterministic.
+ *
+ * Arguments as tk_attn_fwd_kv, plus
+ *   workspace        device memory of at least tk_attn_fwd_workspace_bytes
+ *                    bytes for this shape, 256-byte aligned, not overlapping
+ *                    any other argument; may be NULL when that size is 0
+ *                    (then this is tk_attn_fwd_kv).  Owned by the caller,
+ *                    overwritten; no clearing is needed between calls.  Two
+ *                    calls in flight at once need two workspaces.
+ *   workspace_bytes  its size.
+ * Errors as tk_attn_fwd_kv, plus TK_ERR_WORKSPACE (too small or
+ * misaligned), TK_ERR_NULL_PTR (NULL where one is needed) and TK_ERR_ALIAS
+ * (the workspace overlapping an argument).
+ */
+int tk_attn_fwd_ws(const void *Q, const void *K, const void *V, void *O, float *LSE, void *workspace,
+                   size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D,
+                   int causal, float scale, cudaStream_t stream);
+
+/*
  * tk_attn_bwd_workspace_bytes -- device workspace tk_attn_bwd needs for a
  * problem of this shape: an fp32 dQ accumulator over whole 128-row query
  * tiles (B*H*ceil(N/128)*128*D floats) and two fp32 row values over the

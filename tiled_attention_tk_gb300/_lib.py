@@ -25,6 +25,8 @@ _P, _I64, _I, _F, _U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c
 SIGNATURES = {
     "tk_attn_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
     "tk_attn_fwd_kv": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
+    "tk_attn_fwd_workspace_bytes": ([_I64, _I64, _I64, _I64, _I64, _I], ctypes.c_size_t),
+    "tk_attn_fwd_ws": ([_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
     "tk_attn_bwd_workspace_bytes": ([_I64, _I64, _I64, _I64], ctypes.c_size_t),
     "tk_attn_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I64,
                      _I, _F, _P], _I),

@@ -32,9 +32,24 @@ def fwd_kv_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: 
     _lib.check(rc, "tk_attn_fwd_kv")
 
 
+def fwd_workspace_bytes(B: int, H: int, Nq: int, Nkv: int, D: int, causal: bool) -> int:
+    """Device workspace bytes tk_attn_fwd_ws needs on the current device for
+    this shape (0: the last round of work units is not split)."""
+    return int(_lib.load().tk_attn_fwd_workspace_bytes(B, H, Nq, Nkv, D, int(bool(causal))))
+
+
+def fwd_ws_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, ws_ptr, ws_bytes: int,
+               B: int, H: int, Nq: int, Nkv: int, D: int, causal: bool, scale: float,
+               stream_handle: int) -> None:
+    """tk_attn_fwd_ws on raw device pointers; raises TkError on a non-zero status."""
+    rc = _lib.load().tk_attn_fwd_ws(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H, Nq, Nkv, D,
+                                    int(bool(causal)), float(scale), stream_handle)
+    _lib.check(rc, "tk_attn_fwd_ws")
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: float | None = None, out: torch.Tensor | None = None,
-        lse: torch.Tensor | None = None, stream=None):
+        lse: torch.Tensor | None = None, stream=None, workspace: torch.Tensor | None = None):
     """Fused attention forward.
 
     q: bf16 [B, H, Nq, D]; k, v: bf16 [B, H, Nkv, D] (Nkv = Nq usually), D
@@ -49,6 +64,11 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     pinned): they are copied to the current CUDA device, the kernel runs, and
     O and LSE are copied back into CPU tensors (pinned when the inputs are);
     the call then returns after the stream has finished.
+
+    On CUDA inputs the call goes through tk_attn_fwd_ws: when the shape's last
+    round of work units is split (``fwd_workspace_bytes`` > 0) it uses
+    ``workspace`` (a CUDA uint8 tensor of at least that size) or allocates one
+    on ``q``'s device.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         if t.dtype != torch.bfloat16:
@@ -79,12 +99,13 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
     with torch.cuda.device(q.device):
-        if Nkv == N:
-            fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, H, N, D, causal, scale, _stream_handle(stream))
-        else:
-            fwd_kv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, N, Nkv, D, causal, scale, _stream_handle(stream))
+        need = fwd_workspace_bytes(B, H, N, Nkv, D, causal)
+        if need > 0 and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if need > 0 else None
+        ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
+        fwd_ws_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
+                   B, H, N, Nkv, D, causal, scale, _stream_handle(stream))
     return out, lse
 
 

@@ -127,14 +127,6 @@ __device__ __forceinline__ void red_add_v4(float *addr, uint32_t a, uint32_t b, 
                  : "memory");
 }
 
-// Copies `bytes` (a multiple of 16) from global to shared memory with the
-// bulk-copy unit, completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // Adds `bytes` (a multiple of 16) of fp32 from shared memory into global
 // memory with the bulk-copy unit, in the current bulk group.
 __device__ __forceinline__ void bulk_reduce_add_f32(float *dst, uint32_t src, uint32_t bytes) {

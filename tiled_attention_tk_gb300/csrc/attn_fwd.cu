@@ -115,7 +115,11 @@ struct Layout {
     static constexpr int B_STFULL = B_OFREE + 2;          // + Q tile: row statistics written
     static constexpr int B_STEMPTY = B_STFULL + 2;        // + Q tile: row statistics read
     static constexpr int B_MMADONE = B_STEMPTY + 2;
-    static constexpr int NUM_BARS = B_MMADONE + 1;
+    static constexpr int B_MERGE = B_MMADONE + 1;         // + epilogue warp: the other piece's block fetched
+    static constexpr int NUM_BARS = B_MERGE + 4;
+    // A split piece's merge fetches up to 8 blocks of 32 rows x (D + 1) fp32
+    // (per Q tile and epilogue warp) into the Q and K/V buffers.
+    static_assert(8u * 32u * (D + 1) * 4u <= STAGE_OFF - Q_OFF, "merge blocks fit the Q and K/V buffers");
     // No alignment slack: the dynamic shared memory of a kernel without
     // static shared memory starts 1024-byte aligned (the kernel checks).
     static constexpr uint32_t SMEM_ALLOC = BAR_OFF + NUM_BARS * 8 + 16;
@@ -130,20 +134,27 @@ struct Layout {
 // Work unit = (head bh, pair of consecutive 128-row Q tiles).  Units are
 // handed to the persistent CTAs round by round; odd rounds run in reverse
 // CTA order (snake) so that no CTA always gets the heaviest unit of a round.
+// Without the causal mask, when the last round is less than half full its
+// units are split in two pieces by key tiles (kv0 .. kv0 + nkv - 1), one
+// piece per CTA, so that the last round takes half a unit's time.
 struct Unit {
     int bh;
     int pair;
+    int kv0;    // first key tile
+    int nkv;    // key tiles of a piece (0 for a whole unit)
+    int piece;  // -1: a whole unit; 0 / 1: the first / second key range of tail unit `tail`
+    int tail;
 };
 
 __device__ __forceinline__ Unit unit_at(int idx, const AttnParams &p) {
     if (p.causal) {
         // Heaviest first: the last pair of every head, then the one before...
         const int r = idx / p.BH;
-        return {idx % p.BH, p.n_pairs - 1 - r};
+        return {idx % p.BH, p.n_pairs - 1 - r, 0, 0, -1, 0};
     }
     // Equal cost: the pairs of one head are adjacent, so CTAs running at
     // the same time share that head's K/V in L2.
-    return {idx / p.n_pairs, idx % p.n_pairs};
+    return {idx / p.n_pairs, idx % p.n_pairs, 0, 0, -1, 0};
 }
 
 __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
@@ -152,21 +163,33 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
 
 // The k-th unit of this CTA (k < units_of_cta).
 __device__ __forceinline__ Unit cta_unit(int k, const AttnParams &p) {
+    if (p.split_pieces > 0 && k == p.split_round) {
+        const int t = static_cast<int>(blockIdx.x) / 2, piece = static_cast<int>(blockIdx.x) % 2;
+        Unit u = unit_at(p.split_round * static_cast<int>(gridDim.x) + t, p);
+        u.kv0 = piece ? p.split_kv : 0;
+        u.nkv = piece ? p.n_kvtiles - p.split_kv : p.split_kv;
+        u.piece = piece;
+        u.tail = t;
+        return u;
+    }
     return unit_at(unit_index(k, blockIdx.x, gridDim.x), p);
 }
 
 // Units this CTA runs: one per round, except that the last round may have
 // none for it.
 __device__ __forceinline__ int units_of_cta(const AttnParams &p) {
+    if (p.split_pieces > 0) return p.split_round + (static_cast<int>(blockIdx.x) < p.split_pieces ? 1 : 0);
     const int total = p.BH * p.n_pairs;
     const int grid = gridDim.x;
     const int rounds = (total + grid - 1) / grid;
     return rounds - (unit_index(rounds - 1, blockIdx.x, grid) >= total ? 1 : 0);
 }
 
-// Key tiles Q tile `qt` must visit: all of them, or under the causal mask
-// those up to the last key its last row sees (row + offset).
-__device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
+// Key tiles Q tile `qt` of unit `u` must visit: the piece's, all of them,
+// or under the causal mask those up to the last key its last row sees
+// (row + offset).
+__device__ __forceinline__ int kv_tiles(const Unit &u, int qt, const AttnParams &p) {
+    if (u.piece >= 0) return u.nkv;
     if (!p.causal) return p.n_kvtiles;
     const int last_key = min(qt * BM + BM, p.Nq) - 1 + p.offset;
     return min(last_key / BN + 1, p.n_kvtiles);
@@ -214,6 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             mbar_init(bar(L::B_SLOTEMPTY + s), 1);
         }
         mbar_init(bar(L::B_MMADONE), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(L::B_MERGE + q), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             bool ok = true;
             for (int k = 0; ok && k < my_units; ++k) {
                 const Unit u = cta_unit(k, p);
-                const int n_kv = kv_tiles(2 * u.pair + 1, p);
+                const int n_kv = kv_tiles(u, 2 * u.pair + 1, p);
                 if (k + 1 < my_units) {
                     // the next unit's Q tiles into L2: they are read once, from
                     // HBM, and the next unit's first S waits for them
@@ -255,7 +279,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     mbar_arrive_expect_tx(bar(L::B_SLOTFULL + s), L::TILE_BYTES);
                     for (int c = 0; c < L::KATOMS; ++c)
                         tma_load_3d(dst + c * L::BOX_BYTES, kv ? &p.tmV : &p.tmK, bar(L::B_SLOTFULL + s),
-                                    c * 64, j * BN, u.bh);
+                                    c * 64, (u.kv0 + j) * BN, u.bh);
                     ++loads;
                     return true;
                 };
@@ -348,8 +372,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
 
             if (my_units > 0) {
                 const Unit u0 = cta_unit(0, p);
-                int n0 = kv_tiles(2 * u0.pair, p);
-                int n1 = kv_tiles(2 * u0.pair + 1, p);  // n1 >= n0 >= 1
+                int n0 = kv_tiles(u0, 2 * u0.pair, p);
+                int n1 = kv_tiles(u0, 2 * u0.pair + 1, p);  // n1 >= n0 >= 1
                 uint32_t ks = 0, vs = 0;
                 // The first unit's S of both Q tiles.
                 ok = wait_bar(L::B_QFULL, 0, 0) && take_slot(ks);
@@ -370,8 +394,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     int m0 = 0, m1 = 0;
                     if (has_next) {
                         const Unit un = cta_unit(k + 1, p);
-                        m0 = kv_tiles(2 * un.pair, p);
-                        m1 = kv_tiles(2 * un.pair + 1, p);
+                        m0 = kv_tiles(un, 2 * un.pair, p);
+                        m1 = kv_tiles(un, 2 * un.pair + 1, p);
                     }
                     for (int j = 0; j < n1; ++j) {
                         const bool last = j + 1 == n1;
@@ -445,55 +469,162 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         auto wait_bar = [&](int b, uint32_t parity, uint32_t step) -> bool {
             return wait_bounded(bar(b), parity & 1, abort_flag, (ROLE_EPILOGUE << 24) | (b << 16) | (step & 0xFFFF));
         };
-        for (int k = 0; ok && k < my_units; ++k) {
+        // O / l (bf16) of this warp's 32 rows of Q tile `qt` of head `bh`,
+        // from TMEM at o_addr, through its staging boxes (row `lane` of a
+        // 32-row box, 128-byte swizzle) to one TMA store per 64 columns, and
+        // LSE; "O free" once O has left TMEM.
+        auto store_tile = [&](int tile, int qt, int bh, float inv_l, float lse) {
+            // the staging boxes of this warp's previous stores are free
+            if (lane == 0) tma_store_wait_read_all();
+            __syncwarp();
+            const uint32_t o_addr = lane_base + L::tmem_o(tile);
+#pragma unroll
+            for (int h = 0; h < L::KATOMS; ++h) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (h * 64 + half * 32 >= D) continue;  // D = 32, 96: the store clips at D
+                    uint32_t rr[32];
+                    tmem_ld32(o_addr + h * 64 + half * 32, rr);
+                    uint32_t ob[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = half * 4 + c;
+                        *reinterpret_cast<uint4 *>(stage + h * L::STAGE_BOX + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                            make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                    }
+                }
+            }
+            // All of O has left TMEM: the next unit's first P V may overwrite it.
+            tc_fence_before_sync();
+            warp_arrive(bar(L::B_OFREE + tile), lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < L::KATOMS; ++h)
+                    tma_store_3d(&p.tmO32, stage_addr + h * L::STAGE_BOX, h * 64, qt * BM + quarter * 32, bh);
+                tma_store_commit();
+            }
+            const int row = qt * BM + r;
+            if (row < p.Nq) p.LSE[static_cast<size_t>(bh) * p.Nq + row] = lse;
+        };
+        // Whole units; a split piece is always a CTA's last unit (below).
+        const bool has_piece = p.split_pieces > 0 && my_units > p.split_round;
+        const int n_whole = my_units - (has_piece ? 1 : 0);
+        for (int k = 0; ok && k < n_whole; ++k) {
             const Unit u = cta_unit(k, p);
             for (int tile = 0; tile < 2; ++tile) {
-                const int qt = 2 * u.pair + tile;
                 if (!(ok = wait_bar(L::B_STFULL + tile, k, k))) break;
                 const float2 st = stats[tile * BM + r];     // (reference max, row sum)
                 warp_arrive(bar(L::B_STEMPTY + tile), lane);
                 if (!(ok = wait_bar(L::B_ODONE + tile, k, k))) break;
                 tc_fence_after_sync();
-                // the staging boxes of this warp's previous stores are free
-                if (lane == 0) tma_store_wait_read_all();
-                __syncwarp();
-                const float inv_l = 1.0f / st.y;
-                const uint32_t o_addr = lane_base + L::tmem_o(tile);
+                store_tile(tile, 2 * u.pair + tile, u.bh, 1.0f / st.y, st.x * p.scale + logf(st.y));
+            }
+        }
+        if (ok && has_piece) {
+            // ---- a piece of a split unit: both Q tiles at once.  Publish
+            // O / l and LSE of this warp's rows (column-major [D][32] then 32
+            // LSE, 128 contiguous bytes per column); the piece that publishes
+            // second fetches the other piece's block with one bulk copy into
+            // the Q / K / V buffers (idle once every MMA is done), merges into
+            // its own O in TMEM (weights exp(LSE - max), unfused products and
+            // sums: the same bits whichever piece merges) and alone stores O
+            // and LSE.
+            const int k = n_whole;
+            const Unit u = cta_unit(k, p);
+            constexpr uint32_t BLOCK = 32 * (D + 1);  // floats per warp block
+            float2 st0 = make_float2(0.f, 1.f), st1 = make_float2(0.f, 1.f);
+            ok = wait_bar(L::B_STFULL, k, k);
+            if (ok) {
+                st0 = stats[r];
+                warp_arrive(bar(L::B_STEMPTY), lane);
+                ok = wait_bar(L::B_STFULL + 1, k, k);
+            }
+            if (ok) {
+                st1 = stats[BM + r];
+                warp_arrive(bar(L::B_STEMPTY + 1), lane);
+                ok = wait_bar(L::B_ODONE, k, k) && wait_bar(L::B_ODONE + 1, k, k);
+            }
+            unsigned merge_mask = 0;  // bit t: this warp merges Q tile t
+            if (ok) {
+                tc_fence_after_sync();
+                float *mine = p.part + static_cast<size_t>((u.tail * 2 + u.piece) * 8 + quarter) * BLOCK + lane;
+#pragma unroll 1
+                for (int tile = 0; tile < 2; ++tile) {
+                    const float2 st = tile ? st1 : st0;
+                    const float inv_l = 1.0f / st.y;
+                    float *blk = mine + tile * 4 * BLOCK;
+                    const uint32_t o_addr = lane_base + L::tmem_o(tile);
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t rr[16];
+                        tmem_ld16(o_addr + c * 16, rr);
 #pragma unroll
-                for (int h = 0; h < L::KATOMS; ++h) {
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        if (h * 64 + half * 32 >= D) continue;  // D = 32, 96: the store clips at D
-                        uint32_t rr[32];
-                        tmem_ld32(o_addr + h * 64 + half * 32, rr);
-                        uint32_t ob[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ob[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                                                __uint_as_float(rr[2 * i + 1]) * inv_l);
-                        // row `lane` of a 32-row box, 128-byte swizzle
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int chunk = half * 4 + c;
-                            *reinterpret_cast<uint4 *>(stage + h * L::STAGE_BOX + lane * 128 +
-                                                       ((chunk ^ (lane & 7)) << 4)) =
-                                make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-                        }
+                        for (int i = 0; i < 16; ++i) blk[(c * 16 + i) * 32] = __fmul_rn(__uint_as_float(rr[i]), inv_l);
                     }
+                    blk[D * 32] = st.x * p.scale + logf(st.y);
                 }
-                // All of O has left TMEM: the next unit's first P V may overwrite it.
-                tc_fence_before_sync();
-                warp_arrive(bar(L::B_OFREE + tile), lane);
-                fence_proxy_async_smem();
+                __threadfence();
                 __syncwarp();
                 if (lane == 0) {
-#pragma unroll
-                    for (int h = 0; h < L::KATOMS; ++h)
-                        tma_store_3d(&p.tmO32, stage_addr + h * L::STAGE_BOX, h * 64, qt * BM + quarter * 32, u.bh);
-                    tma_store_commit();
+#pragma unroll 1
+                    for (int tile = 0; tile < 2; ++tile)
+                        if (atomicExch(p.ctr + (u.tail * 2 + tile) * 4 + quarter, p.epoch) == p.epoch)
+                            merge_mask |= 1u << tile;
                 }
-                const int row = qt * BM + r;
-                if (row < p.Nq) p.LSE[static_cast<size_t>(u.bh) * p.Nq + row] = st.x * p.scale + logf(st.y);
+                merge_mask = __shfl_sync(0xFFFFFFFFu, merge_mask, 0);
+            }
+            if (ok && merge_mask) {
+                __threadfence();
+                if (lane == 0) {
+                    fence_proxy_async_global();
+                    const uint32_t mb = bar(L::B_MERGE + quarter);
+                    mbar_arrive_expect_tx(mb, __popc(merge_mask) * BLOCK * 4);
+                    // the other piece's blocks: tile t at + t * 4 * BLOCK floats
+                    const float *src = p.part + static_cast<size_t>((u.tail * 2 + 1 - u.piece) * 8 + quarter) * BLOCK;
+#pragma unroll 1
+                    for (int tile = 0; tile < 2; ++tile)
+                        if (merge_mask & (1u << tile))
+                            bulk_load(sbase + L::Q_OFF + (tile * 4 + quarter) * BLOCK * 4, src + tile * 4 * BLOCK,
+                                      BLOCK * 4, mb);
+                }
+                __syncwarp();
+                ok = wait_bar(L::B_MERGE + quarter, 0, k);
+            }
+#pragma unroll 1
+            for (int tile = 0; ok && tile < 2; ++tile) {
+                if (!(merge_mask & (1u << tile))) {
+                    tc_fence_before_sync();
+                    warp_arrive(bar(L::B_OFREE + tile), lane);
+                    continue;
+                }
+                const float2 st = tile ? st1 : st0;
+                const float *oth =
+                    reinterpret_cast<const float *>(smem + L::Q_OFF + (tile * 4 + quarter) * BLOCK * 4) + lane;
+                const float lse_own = st.x * p.scale + logf(st.y), lse_oth = oth[D * 32];
+                const float m = fmaxf(lse_own, lse_oth);
+                const float w_own = expf(lse_own - m), w_oth = expf(lse_oth - m);
+                const float inv_w = 1.0f / (w_own + w_oth), inv_l = 1.0f / st.y;
+                const uint32_t o_addr = lane_base + L::tmem_o(tile);
+#pragma unroll 1
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t rr[16];
+                    tmem_ld16(o_addr + c * 16, rr);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        rr[i] = __float_as_uint(__fmul_rn(
+                            __fadd_rn(__fmul_rn(w_own, __fmul_rn(__uint_as_float(rr[i]), inv_l)),
+                                      __fmul_rn(w_oth, oth[(c * 16 + i) * 32])),
+                            inv_w));
+                    tmem_st16(o_addr + c * 16, rr);
+                }
+                tmem_st_wait();
+                // TMEM now holds the merged, normalised O
+                store_tile(tile, 2 * u.pair + tile, u.bh, 1.0f, m + logf(w_own + w_oth));
             }
         }
         if (lane == 0) tma_store_wait_all();  // every store of this warp has landed
@@ -513,7 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             const Unit u = cta_unit(k, p);
             const int qt = 2 * u.pair + tile;
             const int row = qt * BM + t;
-            const int n_kv = kv_tiles(qt, p);
+            const int n_kv = kv_tiles(u, qt, p);
             float m_ref = -INFINITY;  // reference max of raw scores (lazy)
             float l = 0.0f;           // sum of exp2(c * (s - m_ref))
             for (int j = 0; j < n_kv; ++j) {
@@ -531,12 +662,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 float s[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i]);
-                if ((j + 1) * BN > p.Nkv || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
+                const int jg = u.kv0 + j;  // key tile within the head
+                if ((jg + 1) * BN > p.Nkv || (p.causal && (jg + 1) * BN > qt * BM + p.offset + 1)) {
                     // A key tile that some row of this Q tile does not see in
                     // full: the ragged tail (keys >= Nkv) and, under the
                     // causal mask, keys past row + offset take -inf.
                     const int limit = p.causal ? min(row + 1 + p.offset, p.Nkv) : p.Nkv;
-                    const int kmax = limit - j * BN;
+                    const int kmax = limit - jg * BN;
 #pragma unroll
                     for (int i = 0; i < BN; ++i) s[i] = (i < kmax) ? s[i] : -INFINITY;
                 }

@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -254,11 +255,9 @@ int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
     return TK_OK;
 }
 
-int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
-                   int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal, float scale,
-                   cudaStream_t stream) {
-    // ---- host-side validation: nothing is enqueued unless all of it passes
-    if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
+namespace {
+
+int fwd_shape(int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal) {
     if (B < 1 || H < 1 || Nq < 1 || Nkv < 1) return TK_ERR_BAD_SHAPE;
     if (D != 32 && D != 64 && D != 96 && D != 128 && D != 256) return TK_ERR_UNSUPPORTED_D;
     // TMA coordinates and the launch grid are 32-bit.
@@ -266,12 +265,68 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     const int64_t BH = B * H;
     const int64_t Nmax = Nq > Nkv ? Nq : Nkv;
     if (BH > INT64_MAX / Nmax / D / 2) return TK_ERR_BAD_SHAPE;
-    const int64_t n_qtiles = (Nq + 127) / 128;
-    const int64_t n_kvtiles = (Nkv + 127) / 128;
-    if (n_qtiles * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
+    if ((Nq + 127) / 128 * BH > INT32_MAX) return TK_ERR_BAD_SHAPE;
     if (causal != 0 && causal != 1) return TK_ERR_BAD_FLAG;
     // Causal queries stand at the end of the key sequence; each must see a key.
     if (causal && Nkv < Nq) return TK_ERR_BAD_SHAPE;
+    return TK_OK;
+}
+
+// The forward's tail split.  Without the causal mask every unit costs the
+// same, so the last round of units is the only imbalance: when it is at most
+// half full, each of its units runs as two pieces (the first half of the key
+// tiles and the rest) on two CTAs, and the round takes half a unit's time.
+// Each piece leaves O / l and LSE in the workspace; the second to publish
+// merges.  The workspace holds, per piece and Q tile, 128 x D + 128 floats,
+// then one 8-byte counter per tail unit, Q tile and 32-row quarter.
+struct FwdSplit {
+    int round, pieces, kv_first;
+    uint64_t part_bytes, workspace;
+};
+
+constexpr int64_t kFwdSplitMinKvTiles = 4;  // each piece gets at least two key tiles
+
+FwdSplit plan_fwd_split(int64_t BH, int64_t Nq, int64_t Nkv, int64_t D, int causal, int num_sms) {
+    FwdSplit f = {0, 0, 0, 0, 0};
+    const int64_t n_kvtiles = (Nkv + 127) / 128;
+    if (causal || D == 256 || n_kvtiles < kFwdSplitMinKvTiles) return f;
+    const int64_t units = BH * (((Nq + 127) / 128 + 1) / 2);
+    if (units <= num_sms) return f;
+    const int64_t tail = units % num_sms;
+    if (tail == 0 || 2 * tail > num_sms) return f;
+    f.round = static_cast<int>(units / num_sms);
+    f.pieces = static_cast<int>(2 * tail);
+    f.kv_first = static_cast<int>((n_kvtiles + 1) / 2);
+    f.part_bytes = round_up(static_cast<uint64_t>(f.pieces) * 2 * 128 * (D + 1) * 4, kWorkspaceAlign);
+    f.workspace = f.part_bytes + round_up(static_cast<uint64_t>(tail) * 2 * 4 * 8, kWorkspaceAlign);
+    return f;
+}
+
+// Tags the split launches: a counter holds the tag of the last piece that
+// published on it, so no launch needs the counters cleared.
+std::atomic<unsigned long long> g_fwd_epoch{0};
+
+}  // namespace
+
+size_t tk_attn_fwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal) {
+    if (fwd_shape(B, H, Nq, Nkv, D, causal) != TK_OK) return 0;
+    int num_sms = 0;
+    if (current_device(&num_sms) != TK_OK) return 0;
+    return static_cast<size_t>(plan_fwd_split(B * H, Nq, Nkv, D, causal, num_sms).workspace);
+}
+
+// The forward behind every entry point; `allow_split` is false for the
+// entry points that take no workspace.
+static int attn_fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, void *workspace,
+                         size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D,
+                         int causal, float scale, bool allow_split, cudaStream_t stream) {
+    // ---- host-side validation: nothing is enqueued unless all of it passes
+    if (!Q || !K || !V || !O || !LSE) return TK_ERR_NULL_PTR;
+    int rc = fwd_shape(B, H, Nq, Nkv, D, causal);
+    if (rc != TK_OK) return rc;
+    const int64_t BH = B * H;
+    const int64_t n_qtiles = (Nq + 127) / 128;
+    const int64_t n_kvtiles = (Nkv + 127) / 128;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return TK_ERR_BAD_SCALE;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
         return TK_ERR_MISALIGNED;
@@ -285,9 +340,17 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
         return TK_ERR_ALIAS;
 
     int num_sms = 0;
-    int rc = current_device(&num_sms);
-    if (rc != TK_OK) return rc;
-    const void *ptrs[5] = {Q, K, V, O, LSE};
+    if ((rc = current_device(&num_sms)) != TK_OK) return rc;
+    const FwdSplit f = allow_split ? plan_fwd_split(BH, Nq, Nkv, D, causal, num_sms) : FwdSplit{0, 0, 0, 0, 0};
+    if (f.workspace > 0) {
+        if (!workspace) return TK_ERR_NULL_PTR;
+        if (!aligned(workspace, kWorkspaceAlign) || workspace_bytes < f.workspace) return TK_ERR_WORKSPACE;
+        if (overlaps(workspace, f.workspace, Q, q_bytes) || overlaps(workspace, f.workspace, K, kv_bytes) ||
+            overlaps(workspace, f.workspace, V, kv_bytes) || overlaps(workspace, f.workspace, O, q_bytes) ||
+            overlaps(workspace, f.workspace, LSE, lse_bytes))
+            return TK_ERR_ALIAS;
+    }
+    const void *ptrs[6] = {Q, K, V, O, LSE, f.workspace > 0 ? workspace : Q};
     for (const void *ptr : ptrs)
         if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
 
@@ -309,11 +372,31 @@ int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *
     p.n_pairs = static_cast<int>((n_qtiles + 1) / 2);
     p.scale = scale;
     p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.split_round = f.round;
+    p.split_pieces = f.pieces;
+    p.split_kv = f.kv_first;
+    char *ws = static_cast<char *>(workspace);
+    p.part = f.pieces > 0 ? reinterpret_cast<float *>(ws) : nullptr;
+    p.ctr = f.pieces > 0 ? reinterpret_cast<unsigned long long *>(ws + f.part_bytes) : nullptr;
+    p.epoch = f.pieces > 0 ? ++g_fwd_epoch : 0;
 
     cudaError_t e = D == 256 ? tk::launch_attn_fwd256(p, num_sms, stream)
                              : tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
+}
+
+int tk_attn_fwd_ws(const void *Q, const void *K, const void *V, void *O, float *LSE, void *workspace,
+                   size_t workspace_bytes, int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t D,
+                   int causal, float scale, cudaStream_t stream) {
+    return attn_fwd_impl(Q, K, V, O, LSE, workspace, workspace_bytes, B, H, Nq, Nkv, D, causal, scale, true,
+                         stream);
+}
+
+int tk_attn_fwd_kv(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,
+                   int64_t H, int64_t Nq, int64_t Nkv, int64_t D, int causal, float scale,
+                   cudaStream_t stream) {
+    return attn_fwd_impl(Q, K, V, O, LSE, nullptr, 0, B, H, Nq, Nkv, D, causal, scale, false, stream);
 }
 
 int tk_attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int64_t B,

@@ -30,6 +30,17 @@ struct AttnParams {
     int n_pairs;      // ceil(n_qtiles / 2): work units per head
     float scale;      // multiplier of Q K^T
     float scale_log2e;  // scale * log2(e): the exp2-domain factor
+    // Tail split (non-causal only; split_pieces = 0: none).  The units of the
+    // last, partial round run as two pieces each, over the first split_kv
+    // key tiles and over the rest, on CTAs 0 .. split_pieces - 1 (tail unit
+    // t on CTAs 2t and 2t + 1).  Each piece writes its O / l (fp32) and LSE
+    // to `part`; the piece that publishes second merges the two.
+    int split_round;                // the round whose units are split (= the full rounds)
+    int split_pieces;               // 2 x the tail units
+    int split_kv;                   // key tiles of the first piece
+    float *part;                    // per piece and Q tile: 128 x D floats of O / l, then 128 LSE
+    unsigned long long *ctr;        // per tail unit, Q tile and 32-row quarter: the last publisher's epoch
+    unsigned long long epoch;       // this launch's tag (distinct for every split launch)
 };
 
 // Everything the backward kernels need.
