@@ -66,8 +66,7 @@ struct Layout {
     static constexpr int B_PFULL = B_SFULL + 2;            // + S slot (2): P in the slot (4 warps)
     static constexpr int B_PVDONE = B_PFULL + 2;           // O += P V done
     static constexpr int B_OFREE = B_PVDONE + 1;           // O read out by the epilogue (4 warps)
-    static constexpr int B_WGSYNC = B_OFREE + 1;           // warpgroup-internal sync (4 warps)
-    static constexpr int B_MMADONE = B_WGSYNC + 1;
+    static constexpr int B_MMADONE = B_OFREE + 1;
     static constexpr int NUM_BARS = B_MMADONE + 1;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -114,8 +113,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                        STAGE_OFF = L::STAGE_OFF, BAR_OFF = L::BAR_OFF;
     constexpr int B_QFULL = L::B_QFULL, B_QEMPTY = L::B_QEMPTY, B_SLOTFULL = L::B_SLOTFULL,
                   B_SLOTEMPTY = L::B_SLOTEMPTY, B_SFULL = L::B_SFULL, B_PFULL = L::B_PFULL,
-                  B_PVDONE = L::B_PVDONE, B_OFREE = L::B_OFREE, B_WGSYNC = L::B_WGSYNC,
-                  B_MMADONE = L::B_MMADONE, NUM_BARS = L::NUM_BARS;
+                  B_PVDONE = L::B_PVDONE, B_OFREE = L::B_OFREE, B_MMADONE = L::B_MMADONE,
+                  NUM_BARS = L::NUM_BARS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -148,7 +147,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
         }
         mbar_init(bar(B_PVDONE), 1);
         mbar_init(bar(B_OFREE), 4);
-        mbar_init(bar(B_WGSYNC), 4);
         mbar_init(bar(B_MMADONE), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -337,17 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
         const float c = p.scale_log2e;
         uint32_t g = 0;         // S hand-offs consumed (all units)
         uint32_t pv_base = 0;   // O += P V products of earlier units
-        uint32_t syncs = 0;     // warpgroup syncs done
         bool ok = true;
-        // Warpgroup-wide sync on an mbarrier: its wait is bounded, so an
-        // aborting CTA cannot hang here.
-        auto wg_sync = [&]() -> bool {
-            warp_arrive(bar(B_WGSYNC), lane);
-            const bool r = wait_bounded(bar(B_WGSYNC), syncs & 1, abort_flag,
-                                        (ROLE_SOFTMAX << 24) | (B_WGSYNC << 16) | (syncs & 0xFFFF));
-            ++syncs;
-            return r;
-        };
         for (int r = 0; ok && r < rounds; ++r) {
             const int idx = unit_index(r, blockIdx.x, grid);
             if (idx >= total_units) continue;
@@ -449,8 +437,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
             // O / l as bf16 through shared memory to TMA stores, 64 columns at
-            // a time; rows past N are clipped by the tensor map.
-            uint8_t *stage = smem + STAGE_OFF;
+            // a time: each warp stages its own 32 rows in a 32 x 64 box (4 KB
+            // of the staging area) and issues its own store, so the warps never
+            // wait for one another; rows past N are clipped by the tensor map.
+            uint8_t *wstage = smem + STAGE_OFF + warp * 4096;
+            const uint32_t wstage_addr = sbase + STAGE_OFF + warp * 4096;
 #pragma unroll 1
             for (int h = 0; h < KATOMS; ++h) {
                 uint32_t ob[32];
@@ -465,22 +456,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                     tc_fence_before_sync();
                     warp_arrive(bar(B_OFREE), lane);  // O may be overwritten
                 }
-                if (t == 0) tma_store_wait_read_all();  // the staging box is free again
-                if (!(ok = wg_sync())) break;
+                if (lane == 0) tma_store_wait_read_all();  // this warp's box is free again
+                __syncwarp();
+                // row `lane` of a 32-row box, 128-byte swizzle
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(stage + t * 128 + ((q ^ (t & 7)) << 4)) =
+                    *reinterpret_cast<uint4 *>(wstage + lane * 128 + ((q ^ (lane & 7)) << 4)) =
                         make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
                 fence_proxy_async_smem();
-                if (!(ok = wg_sync())) break;
-                if (t == 0) {
-                    tma_store_3d(&p.tmO, sbase + STAGE_OFF, h * 64, qt * BM, u.bh);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&p.tmO32, wstage_addr, h * 64, qt * BM + warp * 32, u.bh);
                     tma_store_commit();
                 }
             }
             if (row < p.Nq) p.LSE[static_cast<size_t>(u.bh) * p.Nq + row] = m_ref * p.scale + logf(l);
         }
-        if (t == 0) tma_store_wait_all();  // every store of this CTA has landed
+        if (lane == 0) tma_store_wait_all();  // every store of this warp has landed
     }
 
     tc_fence_before_sync();
