@@ -487,8 +487,8 @@ class ForwardRun:
 def time_launches(run, steps: int, warmup: int, dev, stream, flush, dist_mod):
     """Warm-up, then `steps` timed launches, each in its own event pair, with
     the whole region in one more pair.  Returns (total ms of the region, mean
-    ms per launch); with an L2 flush between launches the region's time is the
-    sum of the launches' own times."""
+    ms per launch, {median, min, max} ms per launch); with an L2 flush between
+    launches the region's time is the sum of the launches' own times."""
     import torch
     import tiled_attention_tk_gb300 as tk
     sh = int(stream.cuda_stream)
@@ -517,9 +517,13 @@ def time_launches(run, steps: int, warmup: int, dev, stream, flush, dist_mod):
     st, detail = tk.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) after timing")
-    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    per_launch = sorted(a.elapsed_time(b) for a, b in ev)
+    kernel_ms = sum(per_launch) / steps
     total_ms = kernel_ms * steps if flush is not None else start_ev.elapsed_time(end_ev)
-    return total_ms, kernel_ms
+    mid = steps // 2
+    median = per_launch[mid] if steps % 2 else 0.5 * (per_launch[mid - 1] + per_launch[mid])
+    stats = {"median": round(median, 5), "min": round(per_launch[0], 5), "max": round(per_launch[-1], 5)}
+    return total_ms, kernel_ms, stats
 
 
 # Workloads measured beside the default line (kernel time, TFLOP/s, fraction
@@ -536,7 +540,7 @@ def measure_side_configs(args, dev, stream, dist_mod, ws, rank, peak):
         run = ForwardRun(w, dev, ws, rank)
         flush, _ = l2_flusher(max(run.in_bytes, 1), dev)
         steps = 200 if w.flops < 1e10 else 20
-        _, kernel_ms = time_launches(run, steps, 3, dev, stream, flush, dist_mod)
+        _, kernel_ms, _ = time_launches(run, steps, 3, dev, stream, flush, dist_mod)
         kernel_ms = max_over_ranks(kernel_ms, dist_mod, dev)
         tf = w.flops / (kernel_ms * 1e-3) / 1e12
         entry = {"kernel_ms": round(kernel_ms, 5), "tflops": round(tf, 2), "frac": round(tf / peak, 4),
@@ -563,7 +567,7 @@ def run_ours(args, w):
     run = ForwardRun(w, dev, ws, rank)
     flush, l2_desc = l2_flusher(max(run.in_bytes, 1), dev)
     sampler = ClockSampler(local)
-    total_ms, kernel_ms = time_launches(run, args.steps, args.warmup, dev, stream, flush, dist_mod)
+    total_ms, kernel_ms, launch_stats = time_launches(run, args.steps, args.warmup, dev, stream, flush, dist_mod)
     clocks = sampler.stop()
     total_ms = max_over_ranks(total_ms, dist_mod, dev)
     ms_per_step = total_ms / args.steps
@@ -662,6 +666,7 @@ def run_ours(args, w):
                      "peak_source": peak_label, "traffic": traffic_for(w.name) if ws == 1 else None,
                      "kernel": f"attn_fwd_kernel<{w.D}>" if w.D != 256 else "attn_fwd256_kernel<256>",
                      "kernel_ms": round(kernel_ms, 5)},
+        "launch_ms": launch_stats,  # this rank's per-launch CUDA-event times
         "parity": parity,
         "e2e": e2e,
         "gpu_launches": args.steps if run.count else 0,
