@@ -80,6 +80,56 @@ def test_based_bench_workload_sampled(oracle_mod):
         _assert_close(o[b, h, rows], den[b, h, rows], O_ref, D_ref, f"B16H16N4096 head ({b},{h})")
 
 
+# ---------------------------------------------------------------- balanced schedule
+# With more heads than SMs and a last wave of heads at most half full
+# (tk_based_fwd_ws, the binding's default), the heads' chunks, laid end to end, are cut into one run
+# per SM: a CTA walks the start of the head its run ends in first and
+# publishes that state, then its whole heads, then the end of the head its run
+# starts in from the state the CTA before it published.  The state passes in
+# fp32, exactly, so the result is bitwise that of one CTA per head.
+
+def _heads_over_sms(extra):
+    return torch.cuda.get_device_properties(0).multi_processor_count + extra
+
+
+@pytest.mark.parametrize("extra,N", [(5, 1024), (70, 1000), (1, 300), (48, 4096)])
+def test_based_balanced_bitwise_equals_one_cta_per_head(oracle_mod, extra, N):
+    H = _heads_over_sms(extra)
+    assert tk.based_workspace_bytes(1, H, N) > 0, "the balanced schedule is not taken"
+    q, k, v = _qkv(1, H, N, 450 + extra)
+    o1, d1 = _run(q, k, v, 0.25, segments=True)
+    o2, d2 = _run(q, k, v, 0.25, segments=False)
+    assert np.array_equal(o1, o2) and np.array_equal(d1, d2)
+    if N <= 1024:
+        for h in (0, H // 2, H - 1):
+            O_ref, D_ref = oracle_mod.based(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], 0.25)
+            _assert_close(o1[:, h:h + 1], d1[:, h:h + 1], O_ref, D_ref, f"balanced head {h}")
+
+
+def test_based_balanced_only_for_a_short_last_wave():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tk.based_workspace_bytes(1, sms + sms // 2, 1024) > 0
+    assert tk.based_workspace_bytes(1, sms + sms // 2 + 1, 1024) == 0   # a last wave more than half full
+    assert tk.based_workspace_bytes(1, 2 * sms, 1024) == 0              # whole waves
+    assert tk.based_workspace_bytes(1, sms + 5, 128) == 0               # one chunk per head
+
+
+def test_based_balanced_workspace_checks():
+    H, N = _heads_over_sms(3), 512
+    need = tk.based_workspace_bytes(1, H, N)
+    assert need > 0 and need % 256 == 0
+    q, k, v = (t.cuda() for t in _qkv(1, H, N, 460))
+    o = torch.empty((1, H, N, 64), dtype=torch.bfloat16, device="cuda")
+    den = torch.empty((1, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tk.TkError) as e:
+        tk.based(q, k, v, scale=0.25, out=o, den=den, workspace=ws[: need - 256])
+    assert e.value.name == "TK_ERR_WORKSPACE"
+    tk.based(q, k, v, scale=0.25, out=o, den=den, workspace=ws)
+    torch.cuda.synchronize()
+    assert tk.device_status()[0] == 0
+
+
 # ---------------------------------------------------------------- segmented sequences
 # With fewer heads than SMs (tk_based_fwd_ws, the binding's default), each
 # head is split into segments: a first pass forms every segment's partial

@@ -264,11 +264,12 @@ def based(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None
     """Causal Based linear attention.  q, k: bf16 [B,H,N,16]; v: bf16
     [B,H,N,64] (CUDA).  Returns (O bf16 [B,H,N,64], DEN fp32 [B,H,N]) with
     w_ij = 1 + s + s^2/2, s = scale <q_i,k_j>, O_i = sum_{j<=i} w_ij v_j / DEN_i.
-    ``scale`` defaults to 1/sqrt(16).  With ``segments`` (the default) and
-    fewer heads than SMs, each head's sequence is split into segments
-    (tk_based_fwd_ws; ``workspace`` is allocated here unless given);
-    ``segments=False`` is tk_based_fwd (one CTA per head).  Enqueued without
-    synchronising."""
+    ``scale`` defaults to 1/sqrt(16).  With ``segments`` (the default) the
+    work is balanced over the SMs (tk_based_fwd_ws; ``workspace`` is allocated
+    here unless given): with fewer heads than SMs each head's sequence is
+    split into segments; with more heads than SMs, not a multiple of them, the
+    heads' chunks are cut into one equal run per SM.  ``segments=False`` is
+    tk_based_fwd (one CTA per head).  Enqueued without synchronising."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         if t.dtype != torch.bfloat16 or t.dim() != 4 or t.device.type != "cuda":
             raise ValueError(f"{n} must be a CUDA bf16 [B,H,N,D] tensor")

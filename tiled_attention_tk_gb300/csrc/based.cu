@@ -234,10 +234,26 @@ __device__ __forceinline__ void write_o(uint32_t lane_taddr, int grp, int lane, 
     }
 }
 
-// SEG: the sequence is split into segments (compiled apart, so the whole-head
-// kernel carries none of the segment bookkeeping).
-template <bool SEG>
+// A piece of work: chunks c0 .. c0 + n - 1 of head bh, starting from no
+// state, from the sum of the partial states of the segments before it
+// (carry 1, from the segment-state pass), or from the state another CTA
+// published for the chunks before c0 (carry 2); `publish` stores the state
+// after the piece's last chunk for the CTA that walks the rest of the head.
+struct Piece {
+    int bh, c0, n, carry, publish, seg;
+};
+
+// MODE 0: one CTA per head.  MODE 1: one CTA per segment, after the
+// segment-state pass.  MODE 2 (balanced): the heads' chunks, laid end to end,
+// are cut into one run per CTA (at least a head long, so a run holds the end
+// of one head, whole heads and the start of another); a CTA walks the start
+// of the head it ends in first and publishes that state, then its whole
+// heads, then the end of the head it starts in, from the state the CTA before
+// it published.  Compiled apart, so the whole-head kernel carries none of the
+// bookkeeping.
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
+    constexpr bool SEG = MODE == 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -248,15 +264,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    // A CTA walks one segment of a head: its chunks c0 .. c0 + n_chunks - 1
-    // (the whole head unless the sequence is split into segments; then the
-    // state of the chunks before c0 comes from the segment-state pass in
-    // p.ws).  Chunk indices below are local to the segment.
-    const int seg = SEG ? static_cast<int>(blockIdx.x) % p.n_seg : 0;
-    const int bh = SEG ? static_cast<int>(blockIdx.x) / p.n_seg : static_cast<int>(blockIdx.x);
-    const int c0 = SEG ? seg * p.seg_chunks : 0;
-    const int n_chunks = SEG ? min(p.seg_chunks, (p.N + C - 1) / C - c0) : (p.N + C - 1) / C;
-    const bool has_prev = SEG && seg > 0;
+    // This CTA's pieces, in the order it walks them.  Chunk indices inside a
+    // piece are local to it; the barriers' phases run on over all pieces
+    // (g = chunks of earlier pieces + c).
+    const int n_ch = (p.N + C - 1) / C;
+    long long run_s = 0, run_e = 0;
+    if (MODE == 2) {
+        const long long total = static_cast<long long>(p.BH) * n_ch;
+        run_s = static_cast<long long>(blockIdx.x) * total / gridDim.x;
+        run_e = static_cast<long long>(blockIdx.x + 1) * total / gridDim.x;
+    }
+    const int hs = static_cast<int>(run_s / n_ch), cs = static_cast<int>(run_s % n_ch);
+    const int he = static_cast<int>(run_e / n_ch), ce = static_cast<int>(run_e % n_ch);
+    const int h_first = cs != 0 ? hs + 1 : hs;  // first whole head
+    const int n_pieces = MODE == 2 ? (ce != 0) + (he - h_first) + (cs != 0) : 1;
+    auto piece = [&](int k) -> Piece {
+        if (MODE == 0) return {static_cast<int>(blockIdx.x), 0, n_ch, 0, 0, 0};
+        if (MODE == 1) {
+            const int seg = static_cast<int>(blockIdx.x) % p.n_seg;
+            const int c0 = seg * p.seg_chunks;
+            return {static_cast<int>(blockIdx.x) / p.n_seg, c0, min(p.seg_chunks, n_ch - c0), seg > 0 ? 1 : 0, 0, seg};
+        }
+        if (ce != 0 && k == 0) return {he, 0, ce, 0, 1, 0};  // the start of the head the run ends in
+        const int kk = k - (ce != 0);
+        if (kk < he - h_first) return {h_first + kk, 0, n_ch, 0, 0, 0};
+        return {hs, cs, n_ch - cs, 2, 0, 0};  // the end of the head the run starts in
+    };
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -304,24 +337,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             // HBM); V of chunk c once chunk c-2's products are done.
             int qk_issued = 0, v_issued = 0;
             bool ok = true;
-            for (int c = 0; c < n_chunks; ++c) {
-                const int b = c & 1;
-                if (c >= 2 && !(ok = wait_bounded(bar(B_QKEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
-                                                  (ROLE_BASED_PRODUCER << 24) | ((B_QKEMPTY + b) << 16) | c)))
+            int g0 = 0;  // chunks of earlier pieces
+            for (int k = 0; ok && k < n_pieces; ++k) {
+            const Piece pc = piece(k);
+            for (int c = 0; c < pc.n; ++c) {
+                const int g = g0 + c;
+                const int b = g & 1;
+                if (g >= 2 && !(ok = wait_bounded(bar(B_QKEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_BASED_PRODUCER << 24) | ((B_QKEMPTY + b) << 16) | (g & 0xFFFF))))
                     break;
                 // Q and K boxes carry 16 real columns; TMA fills the rest with 0
                 // but still counts the full box.
                 const uint32_t dst = sbase + QK_OFF + b * 2 * BOX;
                 mbar_arrive_expect_tx(bar(B_QKFULL + b), 2 * BOX);
-                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, (c0 + c) * C, bh);
-                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, (c0 + c) * C, bh);
+                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
+                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
                 ++qk_issued;
-                if (c >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((c >> 1) - 1) & 1, abort_flag,
-                                                  (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | c)))
+                if (g >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                  (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | (g & 0xFFFF))))
                     break;
                 mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
-                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (c0 + c) * C, bh);
+                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (pc.c0 + c) * C, pc.bh);
                 ++v_issued;
+            }
+            g0 += pc.n;
             }
             if (!ok) {
                 // let the loads in flight land before the CTA's shared memory goes away
@@ -356,28 +395,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 }
                 __syncwarp();
             };
-            bool ok = wait_bounded(bar(B_QKFULL), 0, abort_flag, (ROLE_BASED_MMA << 24) | (B_QKFULL << 16));
+            bool ok = true;
+            int g0 = 0;  // chunks of earlier pieces
+            for (int k = 0; ok && k < n_pieces; ++k) {
+            const Piece pc = piece(k);
+            const bool has_prev = pc.carry != 0;
+            // the piece's first S
+            ok = wait_bounded(bar(B_QKFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag,
+                              (ROLE_BASED_MMA << 24) | ((B_QKFULL + (g0 & 1)) << 16) | (g0 & 0xFFFF));
             if (ok) {
                 tc_fence_after_sync();
-                issue_s(0);
+                issue_s(g0);
             }
-            for (int c = 0; ok && c < n_chunks; ++c) {
-                const int b = c & 1;
-                const uint32_t ph = c & 1;
+            for (int c = 0; ok && c < pc.n; ++c) {
+                const int g = g0 + c;
+                const int b = g & 1;
+                const uint32_t ph = g & 1;
                 const uint32_t vb = sbase + V_OFF + b * BOX;
-                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | c)))
+                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | (g & 0xFFFF))))
                     break;
-                if (c + 1 < n_chunks) {
-                    if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((c + 1) >> 1) & 1, abort_flag,
-                                            (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | (c + 1))))
+                if (c + 1 < pc.n) {
+                    if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | ((g + 1) & 0xFFFF))))
                         break;
                     tc_fence_after_sync();
-                    issue_s(c + 1);
+                    issue_s(g + 1);
                 }
-                if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag, (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | c)))
+                if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | (g & 0xFFFF))))
                     break;
-                if (!(ok = wait_bounded(bar(B_VFULL + b), (c >> 1) & 1, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | ((B_VFULL + b) << 16) | c)))
+                if (!(ok = wait_bounded(bar(B_VFULL + b), (g >> 1) & 1, abort_flag,
+                                        (ROLE_BASED_MMA << 24) | ((B_VFULL + b) << 16) | (g & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
                 // intra: [num | den] = P [V | 1]; 16 chunk rows per step.  Descriptors
@@ -392,7 +441,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 __syncwarp();
                 // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
                 if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | c)))
+                                        (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | (g & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
                 const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
@@ -406,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 __syncwarp();
                 // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
                 if (!(ok = wait_bounded(bar(B_PHIKREADY), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | c)))
+                                        (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | (g & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
                 const uint32_t pk_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024));
@@ -419,6 +468,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                     umma_commit(bar(B_VEMPTY + b));
                 }
                 __syncwarp();
+            }
+            g0 += pc.n;
             }
             if (elect_one()) umma_commit(bar(B_MMADONE));
             __syncwarp();
@@ -440,12 +491,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const float scale = p.scale;
         const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
-        const size_t head_row0 = static_cast<size_t>(bh) * p.N;
         const uint32_t obox = sbase + OST_OFF + warp * OBOX;
-        if (has_prev) {
+        const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;  // this group's state columns
+        bool ok = true;
+        int g0 = 0;  // chunks of earlier pieces
+        for (int kp = 0; ok && kp < n_pieces; ++kp) {
+        const Piece pc = piece(kp);
+        const int bh = pc.bh, c0 = pc.c0, n_chunks = pc.n;
+        const bool has_prev = pc.carry != 0;
+        const size_t head_row0 = static_cast<size_t>(bh) * p.N;
+        if (MODE == 2 && pc.carry == 2) {
+            // --- the state of the head's chunks before c0, published by the
+            // CTA that walked them: this warp's rows and columns of S^T, which
+            // the same warp of that CTA wrote (rows >= 80 are 0)
+            if (lane == 0) {
+                const volatile unsigned long long *flag = p.flags + static_cast<size_t>(bh) * 8 + warp;
+                const uint64_t t0 = global_timer_ns();
+                while (*flag != p.epoch) {
+                    if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                        if (!*abort_flag) {
+                            *abort_flag = 1;
+                            record_timeout((ROLE_BASED_COMPUTE << 24) | (0xFF << 16) | (bh & 0xFFFF));
+                        }
+                        ok = false;
+                        break;
+                    }
+                }
+                __threadfence();
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            for (int blk = 0; blk < ncol; blk += 16) {
+                uint32_t u[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) u[e] = 0u;
+                if (i < NV) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.carry + (static_cast<size_t>(bh) * NV + i) * F + col0 + blk);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v = __ldcg(src + q);
+                        u[4 * q] = __float_as_uint(v.x);
+                        u[4 * q + 1] = __float_as_uint(v.y);
+                        u[4 * q + 2] = __float_as_uint(v.z);
+                        u[4 * q + 3] = __float_as_uint(v.w);
+                    }
+                }
+                tmem_st16(lane_base + T_ST + col0 + blk, u);
+            }
+            tmem_st_wait();
+        }
+        if (SEG && has_prev) {
             // --- the state of the segments before this one: the sum of their
             // fp32 partial states, into the group's columns of S^T (rows >= 65 are 0)
-            const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;
+            const int seg = pc.seg;
             for (int blk = 0; blk < ncol; blk += 16) {
                 float acc[16];
 #pragma unroll
@@ -471,13 +569,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             }
             tmem_st_wait();
         }
-        bool ok = true;
         for (int c = 0; c < n_chunks; ++c) {
-            const int b = c & 1;
-            const uint32_t ph = c & 1;
+            const int gc = g0 + c;
+            const int b = gc & 1;
+            const uint32_t ph = gc & 1;
             const uint32_t qb = sbase + QK_OFF + b * 2 * BOX, kb = qb + BOX;
             const int row = (c0 + c) * C + i;  // sequence position of this thread's query and key
-            if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag, (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | c)))
+            if (!(ok = wait_bounded(bar(B_SFULL), ph, abort_flag,
+                                    (ROLE_BASED_COMPUTE << 24) | (B_SFULL << 16) | (gc & 0xFFFF))))
                 break;
             tc_fence_after_sync();
             // --- P: w_ij = 1 + s + s^2/2 for keys j <= i of the chunk (and j < N), this group's 64 keys
@@ -509,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             if (c > 0) {
                 // chunk c-1's P [V|1] and phi(Q) S are done: T_P, T_O and T_PHIQ are free
                 if (!(ok = wait_bounded(bar(B_ODONE), ph ^ 1, abort_flag,
-                                        (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | c)))
+                                        (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (gc & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
             }
@@ -525,7 +624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 // {0, 1} (group 0) and {2, 3, 4} (group 1) of the 160 (at a
                 // segment's first chunk: the state the group itself stored above)
                 if (c > 0 && !(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
-                                                 (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | c)))
+                                                 (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (gc & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -567,14 +666,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             warp_arrive(bar(B_PHIKREADY), lane);
             warp_arrive(bar(B_QKEMPTY + b), lane);  // this chunk's Q and K are no longer read here
         }
-        // --- O of the last chunk
-        if (ok && n_chunks > 0 &&
-            wait_bounded(bar(B_ODONE), (n_chunks - 1) & 1, abort_flag,
-                         (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | n_chunks)) {
-            tc_fence_after_sync();
+        if (!ok) break;
+        // --- O of the piece's last chunk
+        const int g_last = g0 + n_chunks - 1;
+        if (!(ok = wait_bounded(bar(B_ODONE), g_last & 1, abort_flag,
+                                (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (g_last & 0xFFFF))))
+            break;
+        tc_fence_after_sync();
+        {
             const int row = (c0 + n_chunks - 1) * C + i;
             write_o(lane_base, grp, lane, obox, &p.tmO, (c0 + n_chunks - 1) * C + (warp % 4) * 32, bh, p.N,
                     grp == 0 ? p.DEN + head_row0 + row : nullptr);
+        }
+        if (MODE == 2) {
+            // The piece's last state product has read phi(K) and written S^T:
+            // the next piece may write phi(K) again and start a new state.
+            if (!(ok = wait_bounded(bar(B_STDONE), g_last & 1, abort_flag,
+                                    (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (g_last & 0xFFFF))))
+                break;
+            tc_fence_after_sync();
+            if (pc.publish) {
+                // --- this warp's rows and columns of S^T (fp32) for the CTA that
+                // walks the rest of the head, then this warp's flag
+                for (int blk = 0; blk < ncol; blk += 16) {
+                    uint32_t u[16];
+                    tmem_ld16(lane_base + T_ST + col0 + blk, u);
+                    if (i < NV) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.carry + (static_cast<size_t>(bh) * NV + i) * F + col0 + blk);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                                 __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicExch(p.flags + static_cast<size_t>(bh) * 8 + warp, p.epoch);
+            }
+        }
+        g0 += n_chunks;
         }
         if (lane == 0) tma_store_wait_all();
     }
@@ -769,20 +899,35 @@ cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        if ((err = cudaFuncSetAttribute(based::based_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncSetAttribute(based::based_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         based::SMEM_ALLOC)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(based::based_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (err = cudaFuncSetAttribute(based::based_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        based::SMEM_ALLOC)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(based::based_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         based::SMEM_ALLOC)) != cudaSuccess)
             return err;
         configured_device = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * p.n_seg), 1, 1);
     cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = based::SMEM_ALLOC;
     cfg.stream = stream;
-    return p.n_seg > 1 ? cudaLaunchKernelEx(&cfg, based::based_kernel<true>, p)
-                       : cudaLaunchKernelEx(&cfg, based::based_kernel<false>, p);
+    if (p.balanced) {
+        // One CTA per SM, all resident at once (a CTA may wait for the state
+        // another publishes), which a cooperative launch guarantees.
+        int sms = 0;
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(sms), 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, based::based_kernel<2>, p);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(p.BH * p.n_seg), 1, 1);
+    return p.n_seg > 1 ? cudaLaunchKernelEx(&cfg, based::based_kernel<1>, p)
+                       : cudaLaunchKernelEx(&cfg, based::based_kernel<0>, p);
 }
 
 // The segment-state pass (n_seg > 1): one CTA per (head, segment) but the last.

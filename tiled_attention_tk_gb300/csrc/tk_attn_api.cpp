@@ -302,9 +302,11 @@ FwdSplit plan_fwd_split(int64_t BH, int64_t Nq, int64_t Nkv, int64_t D, int caus
     return f;
 }
 
-// Tags the split launches: a counter holds the tag of the last piece that
-// published on it, so no launch needs the counters cleared.
-std::atomic<unsigned long long> g_fwd_epoch{0};
+// Tags the launches whose CTAs hand results to one another through a caller
+// workspace (the forward's tail split, Based's balanced schedule): a counter
+// or flag holds the tag of the last launch that wrote it, so no launch needs
+// them cleared.
+std::atomic<unsigned long long> g_launch_epoch{0};
 
 }  // namespace
 
@@ -378,7 +380,7 @@ static int attn_fwd_impl(const void *Q, const void *K, const void *V, void *O, f
     char *ws = static_cast<char *>(workspace);
     p.part = f.pieces > 0 ? reinterpret_cast<float *>(ws) : nullptr;
     p.ctr = f.pieces > 0 ? reinterpret_cast<unsigned long long *>(ws + f.part_bytes) : nullptr;
-    p.epoch = f.pieces > 0 ? ++g_fwd_epoch : 0;
+    p.epoch = f.pieces > 0 ? ++g_launch_epoch : 0;
 
     cudaError_t e = D == 256 ? tk::launch_attn_fwd256(p, num_sms, stream)
                              : tk::launch_attn_fwd(static_cast<int>(D), p, num_sms, stream);
@@ -551,6 +553,7 @@ struct BasedPlan {
     int n_seg;
     int seg_chunks;
     uint64_t workspace;
+    int balanced;  // Based only: the balanced schedule (more heads than SMs, not a multiple)
 };
 
 constexpr int kBasedMinSegChunks = 4;
@@ -559,7 +562,7 @@ constexpr uint64_t kHedgehogSegStateBytes = 80ull * 128ull * 4ull;  // likewise 
 
 BasedPlan plan_segments(int64_t BH, int64_t N, int num_sms, uint64_t seg_state_bytes) {
     const int64_t n_chunks = (N + 127) / 128;
-    BasedPlan pl{1, static_cast<int>(n_chunks), 0};
+    BasedPlan pl{1, static_cast<int>(n_chunks), 0, 0};
     if (BH >= num_sms) return pl;
     int64_t n_seg = std::min<int64_t>(num_sms / BH, n_chunks / kBasedMinSegChunks);
     if (n_seg < 2) return pl;
@@ -572,7 +575,22 @@ BasedPlan plan_segments(int64_t BH, int64_t N, int num_sms, uint64_t seg_state_b
     return pl;
 }
 
+// More heads than SMs, and a last wave of heads at most half full: one CTA
+// per head would leave most SMs idle in that wave, so the heads' chunks are
+// cut into one equal run per CTA instead (balanced schedule); a head split
+// between two CTAs passes its state through the workspace (80 x 160 fp32 per
+// head, then eight 8-byte flags per head).  With a fuller last wave the
+// balanced runs measured no faster: fewer CTAs share the memory system there,
+// and each runs faster.
 BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
+    const int64_t n_chunks = (N + 127) / 128;
+    const int64_t last_wave = BH % num_sms;
+    if (BH > num_sms && last_wave != 0 && 2 * last_wave <= num_sms && n_chunks >= 2) {
+        BasedPlan pl{1, static_cast<int>(n_chunks), 0, 1};
+        pl.workspace = round_up(static_cast<uint64_t>(BH) * kBasedSegStateBytes, kWorkspaceAlign) +
+                       round_up(static_cast<uint64_t>(BH) * 8 * 8, kWorkspaceAlign);
+        return pl;
+    }
     return plan_segments(BH, N, num_sms, kBasedSegStateBytes);
 }
 
@@ -614,6 +632,13 @@ int based_launch(const void *Q, const void *K, const void *V, void *O, float *DE
     p.n_seg = pl.n_seg;
     p.seg_chunks = pl.seg_chunks;
     p.scale = scale;
+    p.balanced = pl.balanced;
+    p.carry = pl.balanced ? static_cast<float *>(workspace) : nullptr;
+    p.flags = pl.balanced ? reinterpret_cast<unsigned long long *>(
+                                static_cast<char *>(workspace) +
+                                round_up(static_cast<uint64_t>(BH) * kBasedSegStateBytes, kWorkspaceAlign))
+                          : nullptr;
+    p.epoch = pl.balanced ? ++g_launch_epoch : 0;
     cudaError_t e = cudaSuccess;
     if (pl.n_seg > 1) e = tk::launch_based_states(p, stream);
     if (e == cudaSuccess) e = tk::launch_based(p, stream);
@@ -632,7 +657,7 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
     const void *ptrs[5] = {Q, K, V, O, DEN};
     for (const void *ptr : ptrs)
         if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
-    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0};
+    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0, 0};
     return based_launch(Q, K, V, O, DEN, B * H, N, scale, whole, nullptr, stream);
 }
 
@@ -747,7 +772,7 @@ int tk_hedgehog_fwd(const void *Q, const void *K, const void *V, const void *Wq,
     const void *ptrs[7] = {Q, K, V, Wq, Wk, O, DEN};
     for (const void *ptr : ptrs)
         if ((rc = check_device_memory(ptr)) != TK_OK) return rc;
-    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0};
+    const BasedPlan whole{1, static_cast<int>((N + 127) / 128), 0, 0};
     return hedgehog_launch(Q, K, V, Wq, Wk, O, DEN, H, B * H, N, whole, nullptr, stream);
 }
 

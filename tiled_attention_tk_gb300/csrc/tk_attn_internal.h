@@ -102,6 +102,14 @@ struct BasedParams {
     int n_seg;         // segments per head (1: one CTA walks the whole head)
     int seg_chunks;    // 128-row chunks per segment
     float scale;
+    // Balanced schedule (balanced = 1): the chunks of all heads cut into one
+    // run per CTA; a head split between two CTAs passes its state through
+    // `carry` ([B*H][80][160] fp32), each of the 8 compute warps raising its
+    // own flag ([B*H][8], set to `epoch`, distinct for every launch).
+    int balanced;
+    float *carry;
+    unsigned long long *flags;
+    unsigned long long epoch;
 };
 
 cudaError_t launch_based(const BasedParams &p, cudaStream_t stream);
