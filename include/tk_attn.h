@@ -303,10 +303,11 @@ int tk_based_fwd(const void *Q, const void *K, const void *V, void *O, float *DE
  *   - B*H below the SM count: B*H * n_seg * 51,200 bytes (rounded up to 256)
  *     for the partial states of n_seg segments per head (0 when the heads
  *     are too short to split);
- *   - B*H above the SM count with B*H mod SMs at most half the SMs (a last
- *     wave of heads at most half full), N > 128: B*H * 51,200 bytes (rounded
- *     up to 256) for the states of heads split between two CTAs, plus B*H * 64
- *     bytes (rounded up to 256) of flags (balanced schedule);
+ *   - B*H above the SM count, where one CTA per head would leave more than
+ *     eight 128-row chunks per SM idle in the last wave ((waves * SMs - B*H)
+ *     * ceil(N/128) > 8 * SMs): B*H * 51,200 bytes (rounded up to 256) for
+ *     the states of heads split between two CTAs, plus B*H * 64 bytes
+ *     (rounded up to 256) of flags (balanced schedule);
  *   - otherwise 0 (one CTA walks each head, as in tk_based_fwd).
  * 0 also for an invalid shape (tk_based_fwd_ws then reports it).
  */
@@ -318,9 +319,9 @@ size_t tk_based_workspace_bytes(int64_t B, int64_t H, int64_t N);
  * pass forms each segment's partial state sum_j [V_j | 1] phi(K_j)^T (fp32,
  * into `workspace`), then one CTA per segment starts from the sum of the
  * partial states before it; same result as tk_based_fwd up to the order of
- * fp32 additions.  With more heads than SMs and a last wave of heads at
- * most half full, the heads' chunks, laid end to end, are cut into one equal
- * run per SM: a head
+ * fp32 additions.  With more heads than SMs and a last wave of heads that
+ * would leave SMs idle for long, the heads' chunks, laid end to end, are cut
+ * into one equal run per SM: a head
  * split between two CTAs passes its exact fp32 state from the first to the
  * second through `workspace`, and the result is bitwise that of
  * tk_based_fwd (one kernel, launched cooperatively so that every CTA is

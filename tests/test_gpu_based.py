@@ -81,7 +81,7 @@ def test_based_bench_workload_sampled(oracle_mod):
 
 
 # ---------------------------------------------------------------- balanced schedule
-# With more heads than SMs and a last wave of heads at most half full
+# With more heads than SMs and a last wave that would leave SMs idle for long
 # (tk_based_fwd_ws, the binding's default), the heads' chunks, laid end to end, are cut into one run
 # per SM: a CTA walks the start of the head its run ends in first and
 # publishes that state, then its whole heads, then the end of the head its run
@@ -92,7 +92,7 @@ def _heads_over_sms(extra):
     return torch.cuda.get_device_properties(0).multi_processor_count + extra
 
 
-@pytest.mark.parametrize("extra,N", [(5, 1024), (70, 1000), (1, 300), (48, 4096)])
+@pytest.mark.parametrize("extra,N", [(5, 2048), (10, 1500), (1, 1300), (48, 4096), (160, 2048)])
 def test_based_balanced_bitwise_equals_one_cta_per_head(oracle_mod, extra, N):
     H = _heads_over_sms(extra)
     assert tk.based_workspace_bytes(1, H, N) > 0, "the balanced schedule is not taken"
@@ -100,22 +100,29 @@ def test_based_balanced_bitwise_equals_one_cta_per_head(oracle_mod, extra, N):
     o1, d1 = _run(q, k, v, 0.25, segments=True)
     o2, d2 = _run(q, k, v, 0.25, segments=False)
     assert np.array_equal(o1, o2) and np.array_equal(d1, d2)
-    if N <= 1024:
+    if N <= 1500:
         for h in (0, H // 2, H - 1):
             O_ref, D_ref = oracle_mod.based(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], 0.25)
             _assert_close(o1[:, h:h + 1], d1[:, h:h + 1], O_ref, D_ref, f"balanced head {h}")
 
 
-def test_based_balanced_only_for_a_short_last_wave():
+def test_based_balanced_only_where_it_pays():
+    """Balanced when one CTA per head would leave more than eight chunks per SM
+    idle in the last wave."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert tk.based_workspace_bytes(1, sms + sms // 2, 1024) > 0
-    assert tk.based_workspace_bytes(1, sms + sms // 2 + 1, 1024) == 0   # a last wave more than half full
-    assert tk.based_workspace_bytes(1, 2 * sms, 1024) == 0              # whole waves
-    assert tk.based_workspace_bytes(1, sms + 5, 128) == 0               # one chunk per head
+
+    def idle_per_sm(bh, n):
+        waves = -(-bh // sms)
+        return (waves * sms - bh) * (-(-n // 128)) / sms
+
+    for bh, n in [(sms + 5, 1024), (sms + 5, 2048), (sms + sms // 2, 2048), (sms + sms // 2, 4096),
+                  (2 * sms - 8, 4096), (2 * sms - 40, 2048), (2 * sms, 4096), (2 * sms + 10, 2048), (sms + 3, 128)]:
+        expect = bh > sms and idle_per_sm(bh, n) > 8
+        assert (tk.based_workspace_bytes(1, bh, n) > 0) == expect, (bh, n)
 
 
 def test_based_balanced_workspace_checks():
-    H, N = _heads_over_sms(3), 512
+    H, N = _heads_over_sms(3), 2048
     need = tk.based_workspace_bytes(1, H, N)
     assert need > 0 and need % 256 == 0
     q, k, v = (t.cuda() for t in _qkv(1, H, N, 460))

@@ -400,12 +400,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             for (int k = 0; ok && k < n_pieces; ++k) {
             const Piece pc = piece(k);
             const bool has_prev = pc.carry != 0;
-            // the piece's first S
-            ok = wait_bounded(bar(B_QKFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag,
-                              (ROLE_BASED_MMA << 24) | ((B_QKFULL + (g0 & 1)) << 16) | (g0 & 0xFFFF));
-            if (ok) {
-                tc_fence_after_sync();
-                issue_s(g0);
+            if (k == 0) {  // the first S (a later piece's was issued during the piece before it)
+                ok = wait_bounded(bar(B_QKFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag,
+                                  (ROLE_BASED_MMA << 24) | ((B_QKFULL + (g0 & 1)) << 16) | (g0 & 0xFFFF));
+                if (ok) {
+                    tc_fence_after_sync();
+                    issue_s(g0);
+                }
             }
             for (int c = 0; ok && c < pc.n; ++c) {
                 const int g = g0 + c;
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag,
                                         (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | (g & 0xFFFF))))
                     break;
-                if (c + 1 < pc.n) {
+                if (c + 1 < pc.n || k + 1 < n_pieces) {  // S of the next chunk, in this piece or the next
                     if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
                                             (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | ((g + 1) & 0xFFFF))))
                         break;
@@ -495,15 +496,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;  // this group's state columns
         bool ok = true;
         int g0 = 0;  // chunks of earlier pieces
+        // The chunk before the current one (possibly the previous piece's
+        // last): its O is written while the current chunk's products run.
+        int prev_bh = 0, prev_row0 = 0, prev_publish = 0, pc_prev_bh = 0;
+        // --- this warp's rows and columns of S^T (fp32), once a piece's last
+        // state product is done, for the CTA that walks the rest of the head;
+        // then this warp's flag
+        auto publish = [&](int pbh) {
+            for (int blk = 0; blk < ncol; blk += 16) {
+                uint32_t u[16];
+                tmem_ld16(lane_base + T_ST + col0 + blk, u);
+                if (i < NV) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.carry + (static_cast<size_t>(pbh) * NV + i) * F + col0 + blk);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                             __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicExch(p.flags + static_cast<size_t>(pbh) * 8 + warp, p.epoch);
+        };
         for (int kp = 0; ok && kp < n_pieces; ++kp) {
         const Piece pc = piece(kp);
         const int bh = pc.bh, c0 = pc.c0, n_chunks = pc.n;
         const bool has_prev = pc.carry != 0;
-        const size_t head_row0 = static_cast<size_t>(bh) * p.N;
         if (MODE == 2 && pc.carry == 2) {
             // --- the state of the head's chunks before c0, published by the
             // CTA that walked them: this warp's rows and columns of S^T, which
-            // the same warp of that CTA wrote (rows >= 80 are 0)
+            // the same warp of that CTA wrote (rows >= 80 are 0).  S^T is
+            // free once the previous piece's last state product is done (and
+            // published, if that piece is the start of a head).
+            if (kp > 0) {
+                if (!(ok = wait_bounded(bar(B_STDONE), (g0 - 1) & 1, abort_flag,
+                                        (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | ((g0 - 1) & 0xFFFF))))
+                    break;
+                tc_fence_after_sync();
+                if (prev_publish) publish(prev_bh);
+                prev_publish = 0;
+            }
             if (lane == 0) {
                 const volatile unsigned long long *flag = p.flags + static_cast<size_t>(bh) * 8 + warp;
                 const uint64_t t0 = global_timer_ns();
@@ -521,22 +553,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            for (int blk = 0; blk < ncol; blk += 16) {
+            // all of this thread's 96 columns in flight at once (group 0 uses
+            // the first 64), then into TMEM
+            float4 v[24];
+            const float4 *src = reinterpret_cast<const float4 *>(p.carry + (static_cast<size_t>(bh) * NV + i) * F + col0);
+#pragma unroll
+            for (int q = 0; q < 24; ++q) v[q] = i < NV ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int blk = 0; blk < 6; ++blk) {
+                if (blk * 16 >= ncol) break;
                 uint32_t u[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) u[e] = 0u;
-                if (i < NV) {
-                    const float4 *src = reinterpret_cast<const float4 *>(p.carry + (static_cast<size_t>(bh) * NV + i) * F + col0 + blk);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 v = __ldcg(src + q);
-                        u[4 * q] = __float_as_uint(v.x);
-                        u[4 * q + 1] = __float_as_uint(v.y);
-                        u[4 * q + 2] = __float_as_uint(v.z);
-                        u[4 * q + 3] = __float_as_uint(v.w);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    u[4 * q] = __float_as_uint(v[4 * blk + q].x);
+                    u[4 * q + 1] = __float_as_uint(v[4 * blk + q].y);
+                    u[4 * q + 2] = __float_as_uint(v[4 * blk + q].z);
+                    u[4 * q + 3] = __float_as_uint(v[4 * blk + q].w);
                 }
-                tmem_st16(lane_base + T_ST + col0 + blk, u);
+                tmem_st16(lane_base + T_ST + col0 + blk * 16, u);
             }
             tmem_st_wait();
         }
@@ -605,17 +639,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                     pk[e] = pack_bf16x2(j0 <= jmax ? w2.x : 0.0f, j0 + 1 <= jmax ? w2.y : 0.0f);
                 }
             }
-            if (c > 0) {
-                // chunk c-1's P [V|1] and phi(Q) S are done: T_P, T_O and T_PHIQ are free
+            if (gc > 0) {
+                // the previous chunk's P [V|1] and phi(Q) S are done: T_P, T_O and T_PHIQ are free
                 if (!(ok = wait_bounded(bar(B_ODONE), ph ^ 1, abort_flag,
                                         (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (gc & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
             }
             tmem_st32(lane_base + T_P + grp * 32, pk);
-            if (c > 0)  // --- O of chunk c-1, this group's 32 columns
-                write_o(lane_base, grp, lane, obox, &p.tmO, (c0 + c - 1) * C + (warp % 4) * 32, bh, p.N,
-                        grp == 0 ? p.DEN + head_row0 + row - C : nullptr);
+            if (gc > 0)  // --- O of the previous chunk, this group's 32 columns
+                write_o(lane_base, grp, lane, obox, &p.tmO, prev_row0 + (warp % 4) * 32, prev_bh, p.N,
+                        grp == 0 ? p.DEN + static_cast<size_t>(prev_bh) * p.N + prev_row0 + i : nullptr);
+            prev_bh = bh;
+            prev_row0 = (c0 + c) * C;
             tmem_st_wait();
             tc_fence_before_sync();
             warp_arrive(bar(B_PREADY), lane);
@@ -645,6 +681,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                                          pack_bf16x2(__uint_as_float(sv[8 * q + 6]), __uint_as_float(sv[8 * q + 7])));
                     }
                 }
+            } else if (MODE == 2 && kp > 0) {
+                // a later piece's first chunk from no state: the previous
+                // piece's last state product must be done before phi(K) is
+                // written again (and publish S^T if that piece was the start
+                // of a head)
+                if (!(ok = wait_bounded(bar(B_STDONE), ph ^ 1, abort_flag,
+                                        (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (gc & 0xFFFF))))
+                    break;
+                tc_fence_after_sync();
+                if (prev_publish) publish(pc_prev_bh);
+                prev_publish = 0;
             }
             // --- phi(Q) of chunk c into TMEM (group 0: features 0..63; group 1: 64..159)
             if (grp == 0)
@@ -667,44 +714,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
             warp_arrive(bar(B_QKEMPTY + b), lane);  // this chunk's Q and K are no longer read here
         }
         if (!ok) break;
-        // --- O of the piece's last chunk
-        const int g_last = g0 + n_chunks - 1;
-        if (!(ok = wait_bounded(bar(B_ODONE), g_last & 1, abort_flag,
-                                (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (g_last & 0xFFFF))))
-            break;
-        tc_fence_after_sync();
-        {
-            const int row = (c0 + n_chunks - 1) * C + i;
-            write_o(lane_base, grp, lane, obox, &p.tmO, (c0 + n_chunks - 1) * C + (warp % 4) * 32, bh, p.N,
-                    grp == 0 ? p.DEN + head_row0 + row : nullptr);
-        }
-        if (MODE == 2) {
-            // The piece's last state product has read phi(K) and written S^T:
-            // the next piece may write phi(K) again and start a new state.
-            if (!(ok = wait_bounded(bar(B_STDONE), g_last & 1, abort_flag,
-                                    (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (g_last & 0xFFFF))))
-                break;
-            tc_fence_after_sync();
-            if (pc.publish) {
-                // --- this warp's rows and columns of S^T (fp32) for the CTA that
-                // walks the rest of the head, then this warp's flag
-                for (int blk = 0; blk < ncol; blk += 16) {
-                    uint32_t u[16];
-                    tmem_ld16(lane_base + T_ST + col0 + blk, u);
-                    if (i < NV) {
-                        float4 *dst = reinterpret_cast<float4 *>(p.carry + (static_cast<size_t>(bh) * NV + i) * F + col0 + blk);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
-                                                 __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
-                    }
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicExch(p.flags + static_cast<size_t>(bh) * 8 + warp, p.epoch);
-            }
-        }
+        prev_publish = pc.publish;
+        pc_prev_bh = bh;
         g0 += n_chunks;
+        }
+        // --- O of the last chunk (and the state, if that piece is the start
+        // of a head)
+        if (ok && g0 > 0) {
+            const int g_last = g0 - 1;
+            ok = wait_bounded(bar(B_ODONE), g_last & 1, abort_flag,
+                              (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (g_last & 0xFFFF));
+            if (ok) {
+                tc_fence_after_sync();
+                write_o(lane_base, grp, lane, obox, &p.tmO, prev_row0 + (warp % 4) * 32, prev_bh, p.N,
+                        grp == 0 ? p.DEN + static_cast<size_t>(prev_bh) * p.N + prev_row0 + i : nullptr);
+            }
+            if (ok && MODE == 2 && prev_publish &&
+                (ok = wait_bounded(bar(B_STDONE), g_last & 1, abort_flag,
+                                   (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (g_last & 0xFFFF)))) {
+                tc_fence_after_sync();
+                publish(pc_prev_bh);
+            }
         }
         if (lane == 0) tma_store_wait_all();
     }

@@ -575,17 +575,19 @@ BasedPlan plan_segments(int64_t BH, int64_t N, int num_sms, uint64_t seg_state_b
     return pl;
 }
 
-// More heads than SMs, and a last wave of heads at most half full: one CTA
-// per head would leave most SMs idle in that wave, so the heads' chunks are
-// cut into one equal run per CTA instead (balanced schedule); a head split
-// between two CTAs passes its state through the workspace (80 x 160 fp32 per
-// head, then eight 8-byte flags per head).  With a fuller last wave the
-// balanced runs measured no faster: fewer CTAs share the memory system there,
-// and each runs faster.
+// More heads than SMs, not a multiple of them: one CTA per head leaves SMs
+// idle in the last wave.  When those idle SM-chunks, (waves * SMs - heads) *
+// chunks, come to more than eight chunks per SM, the heads' chunks are cut
+// into one equal run per CTA instead (balanced schedule); a head split between
+// two CTAs passes its state through the workspace (80 x 160 fp32 per head,
+// then eight 8-byte flags per head).  The balanced runs cost a CTA about five
+// to nine chunks of its own (measured at 8 to 64 chunks per head), so below
+// that margin one CTA per head is kept.
 BasedPlan plan_based(int64_t BH, int64_t N, int num_sms) {
     const int64_t n_chunks = (N + 127) / 128;
-    const int64_t last_wave = BH % num_sms;
-    if (BH > num_sms && last_wave != 0 && 2 * last_wave <= num_sms && n_chunks >= 2) {
+    const int64_t waves = (BH + num_sms - 1) / num_sms;
+    const int64_t idle = (waves * num_sms - BH) * n_chunks;  // SM-chunks one CTA per head leaves idle
+    if (BH > num_sms && idle > 8 * static_cast<int64_t>(num_sms)) {
         BasedPlan pl{1, static_cast<int>(n_chunks), 0, 1};
         pl.workspace = round_up(static_cast<uint64_t>(BH) * kBasedSegStateBytes, kWorkspaceAlign) +
                        round_up(static_cast<uint64_t>(BH) * 8 * 8, kWorkspaceAlign);
