@@ -664,7 +664,7 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_label, "traffic": traffic_for(w.name) if ws == 1 else None,
-                     "kernel": f"attn_fwd_kernel<{w.D}>" if w.D != 256 else "attn_fwd256_kernel<256>",
+                     "kernel": f"attn_fwd_kernel<{w.D}>" if w.D != 256 else f"attn_fwd256_kernel<256, {str(bool(w.causal)).lower()}>",
                      "kernel_ms": round(kernel_ms, 5)},
         "launch_ms": launch_stats,  # this rank's per-launch CUDA-event times
         "parity": parity,

@@ -86,26 +86,85 @@ struct Unit {
     int qt;
 };
 
-// Causal: heaviest Q tiles first (the last tile of every head, then the one
-// before ...).  Otherwise the tiles of one head are adjacent, so CTAs running
-// together share its K/V in L2.
-__device__ __forceinline__ Unit unit_at(int idx, const AttnParams &p) {
-    if (p.causal) return {idx % p.BH, p.n_qtiles - 1 - idx / p.BH};
-    return {idx / p.n_qtiles, idx % p.n_qtiles};
-}
-
 // Odd rounds run in reverse CTA order (snake).
 __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
     return round * grid + ((round & 1) ? grid - 1 - cta : cta);
 }
 
+// Units sit in slots, one slot per CTA per round.  Without the mask a slot is
+// one Q tile, the tiles of a head adjacent, so CTAs running together share
+// that head's K/V in L2.  Under the causal mask, with an even number of Q
+// tiles, the first heads run in mirrored pairs: a slot holds a head's Q tile
+// n-1-i and then its tile i, which together visit n+1 key tiles whatever i
+// is, so these slots are balanced as they come and lie head by head (CTAs
+// running together then read the K/V of a few heads, not of every head).  The
+// heads left once fewer than a round of pairs would remain run one tile per
+// slot, heaviest first (their last tiles, then the ones before ...), which
+// evens out the last rounds.  Odd tile counts run that way throughout.
+struct Sched {
+    int heads_paired;  // heads whose tiles run in pairs (the first ones)
+    int pair_slots;    // heads_paired * n_qtiles / 2
+    int slots;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Sched schedule(const AttnParams &p, int grid) {
+    Sched s{0, 0, p.BH * p.n_qtiles};
+    if (CAUSAL && p.n_qtiles % 2 == 0) {
+        const int hp = p.n_qtiles / 2;
+        s.heads_paired = max(0, (p.BH * hp - grid) / hp);
+        s.pair_slots = s.heads_paired * hp;
+        s.slots = s.pair_slots + (p.BH - s.heads_paired) * p.n_qtiles;
+    }
+    return s;
+}
+
+// Unit `h` (0 or 1) of slot `idx`.
+template <bool CAUSAL>
+__device__ __forceinline__ Unit slot_unit(int idx, int h, const Sched &s, const AttnParams &p) {
+    if (CAUSAL && idx < s.pair_slots) {
+        const int hp = p.n_qtiles / 2, i = idx % hp;
+        return {idx / hp, h ? i : p.n_qtiles - 1 - i};
+    }
+    if (CAUSAL) {
+        const int j = idx - s.pair_slots, left = p.BH - s.heads_paired;
+        return {s.heads_paired + j % left, p.n_qtiles - 1 - j / left};
+    }
+    return {idx / p.n_qtiles, idx % p.n_qtiles};
+}
+
+// Slots of this CTA that hold pairs: every round before the first round with
+// single units, and that round's slot if it is still a pair.
+__device__ __forceinline__ int pair_rounds_of_cta(const Sched &s, int grid) {
+    const int r0 = s.pair_slots / grid;
+    return r0 + (unit_index(r0, blockIdx.x, grid) < s.pair_slots ? 1 : 0);
+}
+
+// Units this CTA runs: two per pair slot, one per other slot (the last round
+// may hold no slot for it).
+__device__ __forceinline__ int units_of_cta(const Sched &s, int grid) {
+    const int rounds = (s.slots + grid - 1) / grid;
+    const int mine = rounds - (unit_index(rounds - 1, blockIdx.x, grid) >= s.slots ? 1 : 0);
+    return mine + pair_rounds_of_cta(s, grid);
+}
+
+// The k-th unit of this CTA (k < units_of_cta).
+template <bool CAUSAL>
+__device__ __forceinline__ Unit cta_unit(int k, const Sched &s, int pair_rounds, const AttnParams &p) {
+    const int grid = gridDim.x;
+    if (CAUSAL && k < 2 * pair_rounds) return slot_unit<CAUSAL>(unit_index(k >> 1, blockIdx.x, grid), k & 1, s, p);
+    return slot_unit<CAUSAL>(unit_index(k - pair_rounds, blockIdx.x, grid), 0, s, p);
+}
+
+template <bool CAUSAL>
 __device__ __forceinline__ int kv_tiles(int qt, const AttnParams &p) {
-    if (!p.causal) return p.n_kvtiles;
+    if (!CAUSAL) return p.n_kvtiles;
     const int last_key = min(qt * BM + BM, p.Nq) - 1 + p.offset;
     return min(last_key / BN + 1, p.n_kvtiles);
 }
 
-template <int D>
+// CAUSAL is p.causal: each mask has its own instantiation.
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __grid_constant__ AttnParams p) {
     using L = Layout<D>;
     constexpr int KATOMS = L::KATOMS, NSLOTS = L::NSLOTS;
@@ -126,9 +185,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int total_units = p.BH * p.n_qtiles;
     const int grid = gridDim.x;
-    const int rounds = (total_units + grid - 1) / grid;
+    const Sched sched = schedule<CAUSAL>(p, grid);
+    const int pair_rounds = pair_rounds_of_cta(sched, grid);
+    const int my_units = units_of_cta(sched, grid);
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -166,11 +226,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
             uint32_t q_loads = 0;
             int k_unit = 0;
             bool ok = true;
-            for (int r = 0; ok && r < rounds; ++r) {
-                const int idx = unit_index(r, blockIdx.x, grid);
-                if (idx >= total_units) continue;
-                const Unit u = unit_at(idx, p);
-                const int n_kv = kv_tiles(u.qt, p);
+            for (int k = 0; ok && k < my_units; ++k) {
+                const Unit u = cta_unit<CAUSAL>(k, sched, pair_rounds, p);
+                const int n_kv = kv_tiles<CAUSAL>(u.qt, p);
                 auto load_kv = [&](int j, bool v) -> bool {
                     const int s = loads % NSLOTS;
                     if (loads >= static_cast<uint32_t>(NSLOTS) &&
@@ -278,11 +336,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                 __syncwarp();
             };
 
-            for (int r = 0; ok && r < rounds; ++r) {
-                const int idx = unit_index(r, blockIdx.x, grid);
-                if (idx >= total_units) continue;
-                const Unit u = unit_at(idx, p);
-                const int n_kv = kv_tiles(u.qt, p);
+            for (int k = 0; ok && k < my_units; ++k) {
+                const Unit u = cta_unit<CAUSAL>(k, sched, pair_rounds, p);
+                const int n_kv = kv_tiles<CAUSAL>(u.qt, p);
                 const uint32_t g0 = g;  // S number of key tile 0 of this unit
                 uint32_t ks = 0, vs = 0;
                 if (!(ok = wait_bounded(bar(B_QFULL), k_unit & 1, abort_flag,
@@ -336,13 +392,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
         uint32_t g = 0;         // S hand-offs consumed (all units)
         uint32_t pv_base = 0;   // O += P V products of earlier units
         bool ok = true;
-        for (int r = 0; ok && r < rounds; ++r) {
-            const int idx = unit_index(r, blockIdx.x, grid);
-            if (idx >= total_units) continue;
-            const Unit u = unit_at(idx, p);
+        for (int k = 0; ok && k < my_units; ++k) {
+            const Unit u = cta_unit<CAUSAL>(k, sched, pair_rounds, p);
             const int qt = u.qt;
             const int row = qt * BM + t;
-            const int n_kv = kv_tiles(qt, p);
+            const int n_kv = kv_tiles<CAUSAL>(qt, p);
             float m_ref = -INFINITY;  // reference max of raw scores (lazy)
             float l = 0.0f;           // sum of exp2(c * (s - m_ref))
             for (int j = 0; j < n_kv; ++j) {
@@ -358,10 +412,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd256_kernel(const __gri
                 float sv[BN];
 #pragma unroll
                 for (int i = 0; i < BN; ++i) sv[i] = __uint_as_float(sr[i]);
-                if ((j + 1) * BN > p.Nkv || (p.causal && (j + 1) * BN > qt * BM + p.offset + 1)) {
+                if ((j + 1) * BN > p.Nkv || (CAUSAL && (j + 1) * BN > qt * BM + p.offset + 1)) {
                     // the ragged tail (keys >= Nkv) and, under the causal mask,
                     // keys past row + offset take -inf
-                    const int limit = p.causal ? min(row + 1 + p.offset, p.Nkv) : p.Nkv;
+                    const int limit = CAUSAL ? min(row + 1 + p.offset, p.Nkv) : p.Nkv;
                     const int kmax = limit - j * BN;
 #pragma unroll
                     for (int i = 0; i < BN; ++i) sv[i] = (i < kmax) ? sv[i] : -INFINITY;
@@ -490,9 +544,10 @@ static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t strea
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        err = cudaFuncSetAttribute(attn_fwd256_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   Layout<D>::SMEM_ALLOC);
-        if (err != cudaSuccess) return err;
+        for (auto kern : {attn_fwd256_kernel<D, false>, attn_fwd256_kernel<D, true>}) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::SMEM_ALLOC);
+            if (err != cudaSuccess) return err;
+        }
         configured_device = dev;
     }
     const long long units = static_cast<long long>(p.n_qtiles) * p.BH;
@@ -502,7 +557,8 @@ static cudaError_t launch_d(const AttnParams &p, int num_sms, cudaStream_t strea
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Layout<D>::SMEM_ALLOC;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, attn_fwd256_kernel<D>, p);
+    return p.causal ? cudaLaunchKernelEx(&cfg, attn_fwd256_kernel<D, true>, p)
+                    : cudaLaunchKernelEx(&cfg, attn_fwd256_kernel<D, false>, p);
 }
 
 }  // namespace fwd256
