@@ -180,10 +180,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    // Work: key tile kt of head bh.  The key tiles of one head are adjacent
-    // in launch order, so they run together and share Q and dO through L2.
-    const int kt = blockIdx.x % p.n_tiles;
-    const int bh = blockIdx.x / p.n_tiles;
+    // Work: key tile kt of head bh.  The grid is (L, n_tiles, B*H / L) and
+    // blocks start roughly in launch order (x fastest): the heads run in
+    // groups of L, and a group's key tiles launch tile by tile across its
+    // heads.  The blocks running together then share a few heads' Q and dO
+    // through L2, and under the causal mask, where key tile kt sees n_tiles
+    // - kt query tiles, each group goes heaviest first (L = 1 without it).
+    const int kt = blockIdx.y;
+    const int bh = blockIdx.z * gridDim.x + blockIdx.x;
     const int qt_first = p.causal ? kt : 0;
     const int n_q = p.n_tiles - qt_first;
     const size_t head_rows = static_cast<size_t>(bh) * p.N;
@@ -559,25 +563,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 // reduction of one 4-column group covers 512 contiguous bytes.
                 float *dq_tile = p.dq_acc + (head_tiles + qt) * BT * D + t * 4;
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32_async(lane_base + L::T_DQ + 64 * h, r0);
-                    tmem_ld32_async(lane_base + L::T_DQ + 64 * h + 32, r1);
+                for (int h = 0; h < D / 32; ++h) {
+                    uint32_t r0[32];
+                    tmem_ld32_async(lane_base + L::T_DQ + 32 * h, r0);
                     tmem_ld_wait();
                     reg_fence(r0);
-                    reg_fence(r1);
-                    if (h == D / 64 - 1) {
+                    if (h == D / 32 - 1) {
                         tc_fence_before_sync();
                         warp_arrive(bar(L::B_DQREAD), lane);
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        red_add_v4(dq_tile + (16 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
+                        red_add_v4(dq_tile + (8 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
                                    r0[4 * j + 3]);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        red_add_v4(dq_tile + (16 * h + 8 + j) * BT * 4, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
-                                   r1[4 * j + 3]);
                 }
             }
         }
@@ -592,26 +590,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             const float scale = p.scale;
             __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (valid_key ? key : 0)) * D;
             __nv_bfloat16 *dvrow = static_cast<__nv_bfloat16 *>(p.dV) + (head_rows + (valid_key ? key : 0)) * D;
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
+            // dK then dV, 32 columns at a time (one set of registers at once)
+#pragma unroll 1
+            for (int q = 0; q < 2 * (D / 32); ++q) {
+                const bool is_v = q >= D / 32;
+                const int c = is_v ? q - D / 32 : q;
+                const float f = is_v ? 1.0f : scale;
                 // every lane takes part in the TMEM loads; only the stores are guarded
-                uint32_t rk[32], rv[32];
-                tmem_ld32(lane_base + L::T_DK + q * 32, rk);
-                tmem_ld32(lane_base + L::T_DV + q * 32, rv);
+                uint32_t r[32];
+                tmem_ld32(lane_base + (is_v ? L::T_DV : L::T_DK) + c * 32, r);
                 if (valid_key) {
-                    uint32_t pk[16], pv[16];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        pk[e] = pack_bf16x2(scale * __uint_as_float(rk[2 * e]), scale * __uint_as_float(rk[2 * e + 1]));
-                        pv[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(f * __uint_as_float(r[2 * e]), f * __uint_as_float(r[2 * e + 1]));
+                    __nv_bfloat16 *dst = (is_v ? dvrow : dkrow) + c * 32;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        reinterpret_cast<uint4 *>(dkrow + q * 32)[v] =
-                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                        reinterpret_cast<uint4 *>(dvrow + q * 32)[v] =
-                            make_uint4(pv[4 * v], pv[4 * v + 1], pv[4 * v + 2], pv[4 * v + 3]);
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        reinterpret_cast<uint4 *>(dst)[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
         }
@@ -717,8 +713,23 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         p.neg_lse2, p.dq_acc, padded_rows, p.N, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
+    // Causal: groups of L heads, L the largest divisor of B*H up to about
+    // three waves of blocks; the grid's z extent stays within its limit.
+    int64_t group = 1;
+    if (p.causal) {
+        const int64_t want = (3 * static_cast<int64_t>(num_sms) + p.n_tiles - 1) / p.n_tiles;
+        for (int64_t l = want < p.BH ? want : p.BH; l >= 1; --l)
+            if (p.BH % l == 0) {
+                group = l;
+                break;
+            }
+    }
+    while (p.BH / group > 65535)  // a divisor of B*H that keeps z in range (B*H itself at worst)
+        for (++group; p.BH % group != 0; ++group) {
+        }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(p.n_tiles) * p.BH), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(group), static_cast<unsigned>(p.n_tiles),
+                       static_cast<unsigned>(p.BH / group));
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM_ALLOC;
     cfg.stream = stream;
