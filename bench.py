@@ -781,7 +781,7 @@ def run_bwd(args, w):
 
 GEMM_METRIC = "GEMM bf16 TFLOP/s on 1 GB300 (C = A B^T, fp32 accumulate; fraction of dense BF16 peak) vs CPU oracle"
 GEMM_SOURCES = ["tiled_attention_tk_gb300/csrc/gemm.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
-                "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
+                "tiled_attention_tk_gb300/csrc/tk_ptx_pair.cuh", "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
 
 
 def gemm_source_hash() -> str:
@@ -920,6 +920,7 @@ def run_gemm(args):
     burst, _ = peaks()
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     name = f"gemm-M{M}N{N}K{K}"
+    pairs = tk.gemm_uses_pairs(M, N, K, True)
     line = {
         "metric": GEMM_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -927,12 +928,14 @@ def run_gemm(args):
         "data": "synthetic (seeded torch.Generator, N(0,1) fp32 draws rounded to bf16)",
         "config": {"workload": name, "M": M, "N": N, "K": K, "b_layout": "[N,K] (C = A B^T)",
                    "stream_k": "on where the schedule uses it",
+                   "cta_pairs": pairs,
                    "workspace_bytes": need,
                    "l2": l2_desc},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_label,
                      "peak_burst": burst, "frac_of_burst": round(achieved / burst, 4),
-                     "traffic": gemm_traffic_for(name), "kernel": "gemm_kernel<true>",
+                     "traffic": gemm_traffic_for(name),
+                     "kernel": "gemm_pair_kernel<true>" if pairs else "gemm_kernel<true>",
                      "kernel_ms": round(kernel_ms, 5)},
         "cublas_context_tflops": round(cublas, 2),
         "e2e": e2e,

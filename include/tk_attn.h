@@ -234,11 +234,19 @@ int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
 
 /*
  * tk_gemm_workspace_bytes -- device workspace tk_gemm needs on the current
- * device for this shape: 0 when the schedule has no stream-K part (or for a
- * shape tk_gemm rejects), else one 128 x 256 fp32 partial-sum slot per SM
- * plus one counter per stream-K tile, each section 256-byte aligned.
+ * device for this shape: 0 when the schedule has no stream-K part (the pair
+ * path never has; also for a shape tk_gemm rejects), else one 128 x 256 fp32
+ * partial-sum slot per SM plus one counter per stream-K tile, each section
+ * 256-byte aligned.
  */
 size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k);
+
+/*
+ * tk_gemm_uses_pairs -- 1 if tk_gemm runs this shape on CTA pairs on the
+ * current device (see tk_gemm), 0 if on single CTAs; 0 also for a shape or
+ * flag tk_gemm rejects, or when no device is usable.  Enqueues nothing.
+ */
+int tk_gemm_uses_pairs(int64_t M, int64_t N, int64_t K, int stream_k);
 
 /*
  * tk_gemm -- C = A op(B) on the same TMA + tcgen05 pipeline as the attention
@@ -247,6 +255,13 @@ size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k);
  * are built around and threadblock swizzle plus persistent grid + stream-K
  * as the cures for its L2 hit rate and wave quantisation
  * (10100.com/article/71410160, section on grid-level abstraction).
+ * Large problems (at least one wave of 256 x 256 tiles over pairs of SMs,
+ * K >= 1024) run on CTA pairs (two-SM tcgen05 products, each SM loading half
+ * of each operand tile), without stream-K, unless stream_k = 1 would split a
+ * partial last wave and the pairs' waves would be less than 80 % full; the
+ * pair path needs no workspace.  Either path gives the same C bit for bit
+ * when no tile is split in K (each output element is one fp32 dot product in
+ * k order).
  *
  *   C[m,n] = sum_k A[m,k] * B'[k,n],  fp32 accumulation, C rounded to bf16
  *            (round to nearest even), where B' = B^T if b_kmajor else B.

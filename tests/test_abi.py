@@ -199,6 +199,15 @@ def test_gemm_workspace_bytes_rejects_bad_shapes():
     assert lib.tk_gemm_workspace_bytes(8, 8, 8, 3) == 0
 
 
+def test_gemm_uses_pairs_rejects_bad_shapes():
+    """No device here: 0 for every query, valid or not, and nothing raises."""
+    lib = tk.load()
+    assert lib.tk_gemm_uses_pairs(0, 8, 8, 1) == 0
+    assert lib.tk_gemm_uses_pairs(8, 8, 12, 1) == 0
+    assert lib.tk_gemm_uses_pairs(8192, 8192, 8192, 3) == 0
+    assert lib.tk_gemm_uses_pairs(8192, 8192, 8192, 1) in (0, 1)
+
+
 # ---------------------------------------------------------------- Based ABI
 
 def _based(q=Bq, k=Bk, v=Bv, o=Bo, d=Bl, B=1, H=1, N=128, Dqk=16, Dv=64, scale=0.25):

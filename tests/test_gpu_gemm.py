@@ -7,7 +7,8 @@ neighbour); the second bounds the fp32 accumulation error by a margin of
 about 16x over K * 2^-24 * sum |a b| / sqrt(K) for these sizes.  Shapes cover
 one tile, ragged M, N and K, both B layouts, data-parallel-only schedules
 (fewer tiles than SMs among them), a stream-K schedule with a partial last
-wave, and the benchmark's 8192^3 launch on sampled rows.
+wave, the CTA-pair path (ragged and whole-wave shapes, both B layouts) and
+the benchmark's 8192^3 launch (pairs) on sampled rows.
 """
 import numpy as np
 import pytest
@@ -77,6 +78,8 @@ def test_gemm_stream_k_partial_wave(oracle_mod, b_kmajor):
     M, N, K = 3000, 5120, 4096
     a, b = _inputs(M, N, K, b_kmajor, 22)
     assert tk.gemm_workspace_bytes(M, N, K, True) > 0
+    # with stream-K the pairs' waves would be 79 % full: single CTAs and stream-K
+    assert not tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_uses_pairs(M, N, K, False)
     rows = sorted({r for blk in range(0, M, 128) for r in (blk + 3, min(blk + 127, M - 1))})
     for stream_k in (True, False):
         c = _run(a, b, b_kmajor, stream_k)
@@ -91,12 +94,56 @@ def test_gemm_deterministic():
 
 
 def test_gemm_bench_shape_sampled(oracle_mod):
-    """The benchmark's 8192 x 8192 x 8192 launch, checked on sampled rows."""
+    """The benchmark's 8192 x 8192 x 8192 launch (CTA pairs), checked on sampled rows."""
     M = N = K = 8192
+    assert tk.gemm_uses_pairs(M, N, K, True)
     a, b = _inputs(M, N, K, True, 24)
     c = _run(a, b, True, True)
     rows = [0, 1, 127, 128, 4095, 4096, 8190, 8191]
     _check(oracle_mod, a, b, True, c, rows=rows, what="8192^3")
+
+
+# ---------------------------------------------------------------- CTA pairs
+# At least one wave of 256 x 256 tiles over the SM pairs and K >= 1024 run on
+# pairs of CTAs: the leader's MMAs read both CTAs' halves of A and B, and each
+# CTA writes its own 128 rows of every tile.
+
+def _pair_shape_rows(M):
+    """Two rows of every 128-row half of every 256-row pair tile."""
+    return sorted({r for blk in range(0, M, 128) for r in (blk + 5, min(blk + 126, M - 1))})
+
+
+@pytest.mark.parametrize("b_kmajor", [True, False])
+def test_gemm_pairs_ragged(oracle_mod, b_kmajor):
+    """9 x 11 pair tiles with M, N and K all ragged (the last tile's second
+    CTA holds no row of C), against the oracle on two rows of every 128-row
+    block; stream-K on or off takes the same path."""
+    M, N, K = 2148, 2632, 1032
+    assert tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_uses_pairs(M, N, K, False)
+    assert tk.gemm_workspace_bytes(M, N, K, True) == 0 and tk.gemm_workspace_bytes(M, N, K, False) == 0
+    a, b = _inputs(M, N, K, b_kmajor, 31)
+    rows = _pair_shape_rows(M)
+    c1 = _run(a, b, b_kmajor, True)
+    _check(oracle_mod, a, b, b_kmajor, c1, rows=rows, what=f"pairs {M}x{N}x{K} kmajor={b_kmajor}")
+    c2 = _run(a, b, b_kmajor, False)
+    assert torch.equal(c1, c2)
+
+
+def test_gemm_pairs_full_wave_multiple(oracle_mod):
+    """4864 x 4096 x 2048: 19 x 16 = 304 pair tiles, four whole waves over 76
+    pairs; two rows of every 128-row block."""
+    M, N, K = 4864, 4096, 2048
+    assert tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_workspace_bytes(M, N, K, True) == 0
+    a, b = _inputs(M, N, K, True, 32)
+    c = _run(a, b, True, True)
+    _check(oracle_mod, a, b, True, c, rows=_pair_shape_rows(M)[::3], what="pairs 4864x4096x2048")
+
+
+def test_gemm_pairs_deterministic():
+    a, b = _inputs(2148, 2632, 1032, True, 33)
+    c1 = _run(a, b, True, True)
+    c2 = _run(a, b, True, True)
+    assert torch.equal(c1, c2)
 
 
 def test_gemm_rejects_small_workspace():

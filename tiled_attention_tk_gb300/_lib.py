@@ -32,6 +32,7 @@ SIGNATURES = {
                      _I, _F, _P], _I),
     "tk_attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _F, _P], _I),
     "tk_gemm_workspace_bytes": ([_I64, _I64, _I64, _I], ctypes.c_size_t),
+    "tk_gemm_uses_pairs": ([_I64, _I64, _I64, _I], _I),
     "tk_gemm": ([_P, _P, _P, _P, ctypes.c_size_t, _I64, _I64, _I64, _I, _I, _P], _I),
     "tk_based_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _F, _P], _I),
     "tk_based_workspace_bytes": ([_I64, _I64, _I64], ctypes.c_size_t),

@@ -226,6 +226,11 @@ def gemm_workspace_bytes(M: int, N: int, K: int, stream_k: bool = True) -> int:
     return int(_lib.load().tk_gemm_workspace_bytes(M, N, K, int(bool(stream_k))))
 
 
+def gemm_uses_pairs(M: int, N: int, K: int, stream_k: bool = True) -> bool:
+    """Whether tk_gemm runs this shape on CTA pairs on the current device."""
+    return bool(_lib.load().tk_gemm_uses_pairs(M, N, K, int(bool(stream_k))))
+
+
 def gemm(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool = True, stream_k: bool = True,
          out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
     """C = a @ b.T (b_kmajor: b is [N, K]) or a @ b (b is [K, N]); bf16 CUDA

@@ -39,6 +39,7 @@
 #include "tk_attn.h"
 #include "tk_attn_internal.h"
 #include "tk_ptx.cuh"
+#include "tk_ptx_pair.cuh"
 #include "tk_sync.cuh"
 
 namespace tk {
@@ -389,6 +390,283 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// The same GEMM on pairs of CTAs (a cluster of two, tcgen05 cta_group::2):
+// a pair computes a 256 x 256 output tile with M = 256 MMAs.  Each CTA loads
+// its own 128 rows of A and its own 128 rows (K-major B) or columns (B
+// [K, N]) of B into its shared memory, so every CTA reads half as much B per
+// MMA as a single CTA does on a 128 x 256 tile; the leader (cluster rank 0)
+// issues each MMA over both CTAs' operands, and each CTA's TMEM holds its 128
+// rows of the accumulator.  The peer's TMA loads complete on the leader's
+// stage barrier (which expects both CTAs' bytes); the leader's commits
+// arrive on the barriers of both CTAs, one commit per CTA; the epilogue warps
+// of both CTAs free an accumulator on the leader's barrier.  Tiles go whole
+// and round-robin over the pairs (no stream-K).
+namespace pair {
+
+constexpr int BM = 128;            // output rows per CTA (256 per pair)
+constexpr int BN = 256;            // output tile columns
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr uint32_t A_BYTES = BM * BK * 2;           // 16 KB
+constexpr uint32_t B_BYTES = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of B
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t STAGE_OFF = 0;
+constexpr uint32_t CSTAGE_OFF = STAGE_OFF + STAGES * STAGE_BYTES;
+constexpr uint32_t BAR_OFF = CSTAGE_OFF + 4 * 2 * C_BOX_BYTES;
+constexpr int B_FULL = 0;                       // + stage (leader): both CTAs' operands landed
+constexpr int B_EMPTY = STAGES;                 // + stage (each CTA): the pair's MMAs have read it
+constexpr int B_ACC_FULL = 2 * STAGES;          // + accumulator (each CTA)
+constexpr int B_ACC_EMPTY = 2 * STAGES + 2;     // + accumulator (leader): 4 epilogue warps x 2 CTAs
+constexpr int B_MMADONE = 2 * STAGES + 4;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
+
+}  // namespace pair
+
+template <bool KMAJOR_B>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+    // this kernel's layout (shadows the single-CTA kernel's constants)
+    constexpr int BM = pair::BM, BN = pair::BN, BK = pair::BK, STAGES = pair::STAGES;
+    constexpr uint32_t A_BYTES = pair::A_BYTES, STAGE_BYTES = pair::STAGE_BYTES, STAGE_OFF = pair::STAGE_OFF,
+                       CSTAGE_OFF = pair::CSTAGE_OFF, BAR_OFF = pair::BAR_OFF;
+    constexpr int B_FULL = pair::B_FULL, B_EMPTY = pair::B_EMPTY, B_ACC_FULL = pair::B_ACC_FULL,
+                  B_ACC_EMPTY = pair::B_ACC_EMPTY, B_MMADONE = pair::B_MMADONE, NUM_BARS = pair::NUM_BARS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    // The same barrier in the leader's and in this pair's other CTA.
+    auto lead_bar = [&](int i) { return cluster_addr(bar(i), 0); };
+    auto rank_bar = [&](int i, uint32_t r) { return cluster_addr(bar(i), r); };
+
+    if (warp == WARP_MMA) {
+        tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(B_FULL + s), 1);
+            mbar_init(bar(B_EMPTY + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(B_ACC_FULL + a), 1);
+            mbar_init(bar(B_ACC_EMPTY + a), 8);
+        }
+        mbar_init(bar(B_MMADONE), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other's
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int pair_id = static_cast<int>(blockIdx.x) / 2;
+    const int n_pairs = static_cast<int>(gridDim.x) / 2;
+    const int n_tiles = p.tiles_m * p.tiles_n;
+
+    if (warp == WARP_TMA) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmA);
+            tma_prefetch_desc(&p.tmB);
+            uint32_t n = 0;  // stages filled so far
+            bool ok = true;
+            for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+                int tm, tn;
+                tile_coords(tile, p, tm, tn);
+                for (int k = 0; k < p.k_iters; ++k, ++n) {
+                    const uint32_t s = n % STAGES;
+                    if (n >= STAGES &&
+                        !(ok = wait_bounded(bar(B_EMPTY + s), ((n / STAGES) - 1) & 1, abort_flag,
+                                            (ROLE_GEMM_PRODUCER << 24) | ((B_EMPTY + s) << 16) | (n & 0xFFFF))))
+                        break;
+                    const uint32_t a_dst = sbase + STAGE_OFF + s * STAGE_BYTES;
+                    const uint32_t b_dst = a_dst + A_BYTES;
+                    const uint32_t full = lead_bar(B_FULL + s);
+                    if (leader) mbar_arrive_expect_tx(bar(B_FULL + s), 2 * STAGE_BYTES);
+                    tma_load_3d_pair(a_dst, &p.tmA, full, k * BK, tm * (2 * BM) + static_cast<int>(rank) * BM, 0);
+                    const int n0 = tn * BN + static_cast<int>(rank) * (BN / 2);
+                    if (KMAJOR_B) {
+                        tma_load_3d_pair(b_dst, &p.tmB, full, k * BK, n0, 0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 2 / 64; ++j)
+                            tma_load_3d_pair(b_dst + j * (64 * BK * 2), &p.tmB, full, n0 + j * 64, k * BK, 0);
+                    }
+                }
+            }
+            if (!ok && leader) {
+                // let the copies in flight (both CTAs' land on the leader's
+                // barriers) arrive before the pair exits
+                const uint64_t t0 = global_timer_ns();
+                const uint32_t first = n > STAGES ? n - STAGES : 0;
+                for (uint32_t j = first; j < n; ++j)
+                    while (!mbar_try_wait_cluster(bar(B_FULL + j % STAGES), (j / STAGES) & 1) &&
+                           global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------ MMA issuer (the leader)
+        if (leader) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, 0, KMAJOR_B ? 0 : 1);
+            uint32_t n = 0;      // stages consumed
+            uint32_t items = 0;  // accumulators used
+            bool ok = true;
+            for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+                const uint32_t acc = items & 1;
+                // both CTAs' epilogues have read this accumulator's previous tile
+                if (items >= 2) {
+                    const uint32_t ph = ((items >> 1) - 1) & 1;
+                    bool done = mbar_try_wait_cluster(bar(B_ACC_EMPTY + acc), ph);
+                    const uint64_t t0 = global_timer_ns();
+                    while (!done) {
+                        done = mbar_try_wait_cluster(bar(B_ACC_EMPTY + acc), ph);
+                        if (!done && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) {
+                            if (!*abort_flag) record_timeout((ROLE_GEMM_MMA << 24) | ((B_ACC_EMPTY + acc) << 16) |
+                                                             (items & 0xFFFF));
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem + acc * BN;
+                for (int k = 0; k < p.k_iters; ++k, ++n) {
+                    const uint32_t s = n % STAGES;
+                    if (!(ok = wait_bounded(bar(B_FULL + s), (n / STAGES) & 1, abort_flag,
+                                            (ROLE_GEMM_MMA << 24) | ((B_FULL + s) << 16) | (n & 0xFFFF))))
+                        break;
+                    tc_fence_after_sync();
+                    const uint32_t a_src = sbase + STAGE_OFF + s * STAGE_BYTES;
+                    const uint32_t b_src = a_src + A_BYTES;
+                    const uint64_t ad = smem_desc_sw128(a_src, 16, 1024);
+                    const uint64_t bd = KMAJOR_B ? smem_desc_sw128(b_src, 16, 1024)
+                                                 : smem_desc_sw128(b_src, 64 * BK * 2, 1024);
+                    uint32_t av[BK / 16], bv[BK / 16];
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        av[kk] = static_cast<uint32_t>(ad) + ((kk * 32) >> 4);
+                        bv[kk] = static_cast<uint32_t>(bd) + ((KMAJOR_B ? kk * 32 : kk * 2048) >> 4);
+                    }
+                    if (elect_one()) {
+                        umma_ss_x4_pair(d, av, static_cast<uint32_t>(ad >> 32), bv, static_cast<uint32_t>(bd >> 32),
+                                        IDESC, k > 0 ? 1u : 0u);
+                        // the stage is free in both CTAs once these MMAs are done
+                        umma_commit_pair(rank_bar(B_EMPTY + s, 0));
+                        umma_commit_pair(rank_bar(B_EMPTY + s, 1));
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (elect_one()) {
+                    umma_commit_pair(rank_bar(B_ACC_FULL + acc, 0));
+                    umma_commit_pair(rank_bar(B_ACC_FULL + acc, 1));
+                }
+                __syncwarp();
+                ++items;
+            }
+            if (elect_one()) umma_commit_pair(rank_bar(B_MMADONE, 0));
+            __syncwarp();
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar(B_MMADONE), 0) &&
+                   global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue warps (both CTAs)
+        const int q = warp % 4;           // TMEM lane quarter
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t cstage = sbase + CSTAGE_OFF + (warp - WARP_EPI) * 2 * C_BOX_BYTES;
+        uint8_t *cstage_ptr = smem + CSTAGE_OFF + (warp - WARP_EPI) * 2 * C_BOX_BYTES;
+        uint32_t items = 0, boxes = 0;
+        bool ok = true;
+        for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+            const uint32_t acc = items & 1;
+            const uint32_t ph = (items >> 1) & 1;
+            bool done = mbar_try_wait_cluster(bar(B_ACC_FULL + acc), ph);
+            const uint64_t t0 = global_timer_ns();
+            while (!done) {
+                done = mbar_try_wait_cluster(bar(B_ACC_FULL + acc), ph);
+                if (!done && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) {
+                    if (!*abort_flag)
+                        record_timeout((ROLE_GEMM_EPILOGUE << 24) | ((B_ACC_FULL + acc) << 16) | (items & 0xFFFF));
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            tc_fence_after_sync();
+            ++items;
+            const uint32_t d = lane_base + acc * BN;
+            int tm, tn;
+            tile_coords(tile, p, tm, tn);
+#pragma unroll 1
+            for (int h = 0; h < BN / 64; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v[32];
+                    tmem_ld32(d + (2 * h + c2) * 32, v);
+                    if (h == BN / 64 - 1 && c2 == 1) {
+                        // accumulator free (in this CTA) for the leader's MMAs
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(lead_bar(B_ACC_EMPTY + acc));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[c2 * 16 + e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                }
+                const uint32_t b = boxes & 1;
+                ++boxes;
+                if (lane == 0) tma_store_wait_read_all();  // box b free again
+                __syncwarp();
+                uint8_t *box = cstage_ptr + b * C_BOX_BYTES;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&p.tmC, cstage + b * C_BOX_BYTES, tn * BN + h * 64,
+                                 tm * (2 * BM) + static_cast<int>(rank) * BM + q * 32, 0);
+                    tma_store_commit();
+                }
+            }
+        }
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal or read it
+    if (warp == WARP_MMA) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
 }  // namespace gemm
 
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream) {
@@ -403,7 +681,35 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream) {
         if ((err = cudaFuncSetAttribute(gemm::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         gemm::SMEM_ALLOC)) != cudaSuccess)
             return err;
+        if ((err = cudaFuncSetAttribute(gemm::gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        gemm::pair::SMEM_ALLOC)) != cudaSuccess)
+            return err;
+        if ((err = cudaFuncSetAttribute(gemm::gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        gemm::pair::SMEM_ALLOC)) != cudaSuccess)
+            return err;
         configured_device = dev;
+    }
+    if (p.pair) {
+        if (grid < 2 || grid % 2 != 0 || p.sk_tiles != 0) return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // clusters of two (compile-time dims)
+        cfg.blockDim = dim3(gemm::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = gemm::pair::SMEM_ALLOC;
+        cfg.stream = stream;
+        // The pairs are persistent: no more of them than can be resident at
+        // once (a GPC with an odd number of free SMs holds one pair fewer).
+        static thread_local int pairs_device = -1, max_pairs = 0;
+        if (pairs_device != dev) {
+            int n = 0;
+            err = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_pair_kernel<true>, &cfg);
+            if (err != cudaSuccess) return err;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+            max_pairs = n;
+            pairs_device = dev;
+        }
+        if (grid / 2 > max_pairs) cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs), 1, 1);
+        return p.b_kmajor ? cudaLaunchKernelEx(&cfg, gemm::gemm_pair_kernel<true>, p)
+                          : cudaLaunchKernelEx(&cfg, gemm::gemm_pair_kernel<false>, p);
     }
     if (p.sk_tiles > 0) {
         err = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(p.sk_tiles) * sizeof(unsigned), stream);

@@ -440,6 +440,7 @@ constexpr uint64_t kGemmSlotBytes = static_cast<uint64_t>(kGemmBM) * kGemmBN * 4
 struct GemmPlan {
     int tiles_m, tiles_n, k_iters, grid, dp_tiles, sk_tiles, sk_iters_per_cta;
     uint64_t workspace;  // bytes: partial slots, then the counters
+    int pair;            // CTA pairs on 256 x 256 tiles
 };
 
 int gemm_shape(int64_t M, int64_t N, int64_t K) {
@@ -450,12 +451,44 @@ int gemm_shape(int64_t M, int64_t N, int64_t K) {
     return TK_OK;
 }
 
+// CTA pairs (cta_group::2, 256 x 256 tiles) take a problem with at least a
+// full wave of pair tiles and K >= 1024: per tile they ran 15-27 % faster than
+// single CTAs on the GB300 (8192^3, 6144^3, 16384^3, 8192 x 8192 x 1024,
+// 2048 x 8192 x 2048) and lost with fewer tiles than pairs (2048 x 2048 x
+// 4096).  They have no stream-K, so where the single-CTA plan would split a
+// partial last wave in K, pairs are kept only while their own waves are at
+// least 80 % full (3000 x 5120 x 4096, 79 %, measured a tie and stays with
+// stream-K).
+bool use_pairs(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
+    const int64_t pairs = num_sms / 2;
+    const int64_t t2 = ((M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * ((N + kGemmBN - 1) / kGemmBN);
+    if (pairs < 1 || K < 16 * kGemmBK || t2 < pairs) return false;
+    const int64_t t1 = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
+    const int64_t k_iters = (K + kGemmBK - 1) / kGemmBK;
+    if (stream_k && k_iters >= kGemmSkMinKIters && t1 > num_sms && t1 % num_sms != 0) {
+        const int64_t waves = (t2 + pairs - 1) / pairs;
+        if (5 * t2 < 4 * waves * pairs) return false;
+    }
+    return true;
+}
+
 // Data-parallel waves of whole tiles; when the tiles do not fill the last
 // wave (and there is more than one wave), the last partial wave plus one full
 // wave are split in K over all CTAs (stream-K): every CTA gets at least one
 // tile's worth of K iterations, so a tile has at most two K segments.
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
     GemmPlan g = {};
+    if (use_pairs(M, N, K, num_sms, stream_k)) {
+        g.pair = 1;
+        g.tiles_m = static_cast<int>((M + 2 * kGemmBM - 1) / (2 * kGemmBM));
+        g.tiles_n = static_cast<int>((N + kGemmBN - 1) / kGemmBN);
+        g.k_iters = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
+        const int64_t T = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
+        const int64_t pairs = num_sms / 2;
+        g.dp_tiles = static_cast<int>(T);
+        g.grid = static_cast<int>(2 * (T < pairs ? T : pairs));
+        return g;
+    }
     g.tiles_m = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
     g.tiles_n = static_cast<int>((N + kGemmBN - 1) / kGemmBN);
     g.k_iters = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
@@ -487,6 +520,13 @@ size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k) {
     return static_cast<size_t>(plan_gemm(M, N, K, num_sms, stream_k).workspace);
 }
 
+int tk_gemm_uses_pairs(int64_t M, int64_t N, int64_t K, int stream_k) {
+    if (gemm_shape(M, N, K) != TK_OK || (stream_k != 0 && stream_k != 1)) return 0;
+    int num_sms = 0;
+    if (current_device(&num_sms) != TK_OK) return 0;
+    return plan_gemm(M, N, K, num_sms, stream_k).pair;
+}
+
 int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t workspace_bytes, int64_t M,
             int64_t N, int64_t K, int b_kmajor, int stream_k, cudaStream_t stream) {
     if (!A || !B || !C) return TK_ERR_NULL_PTR;
@@ -514,7 +554,7 @@ int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t works
     tk::GemmParams p;
     if ((rc = encode_matrix_map(&p.tmA, A, K, M, 64, 128)) != TK_OK) return rc;
     if (b_kmajor) {
-        if ((rc = encode_matrix_map(&p.tmB, B, K, N, 64, 256)) != TK_OK) return rc;
+        if ((rc = encode_matrix_map(&p.tmB, B, K, N, 64, g.pair ? 128 : 256)) != TK_OK) return rc;
     } else {
         if ((rc = encode_matrix_map(&p.tmB, B, N, K, 64, 64)) != TK_OK) return rc;
     }
@@ -536,6 +576,7 @@ int tk_gemm(const void *A, const void *B, void *C, void *workspace, size_t works
     p.dp_tiles = g.dp_tiles;
     p.sk_tiles = g.sk_tiles;
     p.sk_iters_per_cta = g.sk_iters_per_cta;
+    p.pair = g.pair;
     cudaError_t e = tk::launch_gemm(p, g.grid, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;

@@ -83,6 +83,8 @@ struct GemmParams {
     int dp_tiles;      // tiles [0, dp_tiles): whole tiles, round-robin over the CTAs
     int sk_tiles;      // tiles [dp_tiles, dp_tiles + sk_tiles): split in K (stream-K)
     int sk_iters_per_cta;  // K iterations of the stream-K range of each CTA
+    int pair;          // 1: CTA pairs (cta_group::2) on 256 x 256 tiles; tiles_m counts 256-row tiles,
+                       // tmB's box is {64, 128, 1} when b_kmajor, and there is no stream-K
 };
 
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream);
