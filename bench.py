@@ -130,9 +130,16 @@ def peaks(sustained: bool = False):
         (FALLBACK_BF16_TFLOPS, "of fallback")
 
 
-def traffic_for(workload_name: str):
+FWD256_SOURCES = ["tiled_attention_tk_gb300/csrc/attn_fwd256.cu", "tiled_attention_tk_gb300/csrc/tk_ptx.cuh",
+                  "tiled_attention_tk_gb300/csrc/tk_sync.cuh"]
+
+
+def traffic_for(workload_name: str, D: int = 128):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current source of the forward kernel that runs head dim D; else
+    None."""
+    if D == 256:
+        return sources_traffic_for(workload_name, FWD256_SOURCES)
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -663,7 +670,7 @@ def run_ours(args, w):
                      "rank0_heads": [run.first, run.first + run.count]},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": peak_label, "traffic": traffic_for(w.name) if ws == 1 else None,
+                     "peak_source": peak_label, "traffic": traffic_for(w.name, w.D) if ws == 1 else None,
                      "kernel": f"attn_fwd_kernel<{w.D}>" if w.D != 256 else f"attn_fwd256_kernel<256, {str(bool(w.causal)).lower()}>",
                      "kernel_ms": round(kernel_ms, 5)},
         "launch_ms": launch_stats,  # this rank's per-launch CUDA-event times

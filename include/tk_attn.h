@@ -72,7 +72,8 @@ enum {
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 1.
  *            Any N >= 1: the last key tile is masked, the last query tile's
  *            extra rows are neither computed into nor stored.
- *   D        head dimension: 32, 64, 96, 128 or 256 (the backward: 64 or 128).
+ *   D        head dimension: 32, 64, 96, 128 or 256 (the backward: 32, 64, 96
+ *            or 128).
  *   causal   0: every query sees every key; 1: query i sees keys j <= i.
  *   scale    multiplier of Q K^T, finite and > 0 (usually 1/sqrt(D)).
  *   stream   CUDA stream the kernel is enqueued on (0 = legacy default).
@@ -162,11 +163,13 @@ int tk_attn_fwd_ws(const void *Q, const void *K, const void *V, void *O, float *
 /*
  * tk_attn_bwd_workspace_bytes -- device workspace tk_attn_bwd needs for a
  * problem of this shape: an fp32 dQ accumulator over whole 128-row query
- * tiles (B*H*ceil(N/128)*128*D floats) and two fp32 row values over the
- * same padded rows, Delta_i = <dO_i, O_i> and -LSE_i*log2(e); each section
+ * tiles (B*H*ceil(N/128)*128*Dk floats, Dk = 64 for D = 32 or 64 and 128 for
+ * D = 96 or 128: head dims 32 and 96 run on the 64- and 128-column kernels,
+ * their missing columns read as zeros) and two fp32 row values over the same
+ * padded rows, Delta_i = <dO_i, O_i> and -LSE_i*log2(e); each section
  * 256-byte aligned.
  * Returns 0 for shapes tk_attn_bwd rejects: TK_ERR_BAD_SHAPE, or a head dim
- * other than 64 and 128 (TK_ERR_UNSUPPORTED_D).
+ * other than 32, 64, 96 and 128 (TK_ERR_UNSUPPORTED_D).
  */
 size_t tk_attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
 

@@ -148,15 +148,18 @@ def test_bwd_workspace_size():
     expect = -(-acc // 256) * 256 + 2 * (-(-padded // 256) * 256)
     assert lib.tk_attn_bwd_workspace_bytes(2, 3, 100, 64) == expect
     assert lib.tk_attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
-    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 96) == 0
+    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 256) == 0
+    # head dims 32 and 96 run on the 64- and 128-column kernels: their accumulator is padded
+    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 32) == lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 64) > 0
+    assert lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 96) == lib.tk_attn_bwd_workspace_bytes(1, 1, 16, 128) > 0
 
 
 @pytest.mark.parametrize("kwargs,code", [
     (dict(do=None), "TK_ERR_NULL_PTR"),
     (dict(ws=None), "TK_ERR_NULL_PTR"),
     (dict(N=0), "TK_ERR_BAD_SHAPE"),
-    (dict(D=32), "TK_ERR_UNSUPPORTED_D"),   # the forward takes 32 and 96; the backward does not
-    (dict(D=96), "TK_ERR_UNSUPPORTED_D"),
+    (dict(D=48), "TK_ERR_UNSUPPORTED_D"),
+    (dict(D=256), "TK_ERR_UNSUPPORTED_D"),  # the forward takes 256; the backward does not
     (dict(causal=3), "TK_ERR_BAD_FLAG"),
     (dict(scale=-0.5), "TK_ERR_BAD_SCALE"),
     (dict(dk=BdK + 8), "TK_ERR_MISALIGNED"),

@@ -48,7 +48,7 @@ def _check(oracle_mod, q, k, v, do, causal, scale, what):
     return got
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 17, 128, 129, 300])
 def test_bwd_shape_sweep(oracle_mod, N, D, causal):
@@ -110,7 +110,7 @@ def test_bwd_bench_workload_sampled(oracle_mod, idx, heads):
                 f"{w.name} head ({b},{h}) {name}: mean err {err.mean():.3e}")
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal, D):
     """Every dQ row is written and the accumulator is re-zeroed per call: dQ
@@ -118,7 +118,9 @@ def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal, D):
     in a row, and every dQ row must come out finite and equal to the
     oracle's, over several heads, six query tiles (a ragged last one) and,
     under the causal mask, 1 to 6 key tiles adding into a query tile; at
-    D = 64 (bulk reductions of staged tiles) and D = 128 (vector reductions)."""
+    D = 64 (bulk reductions of staged tiles) and D = 128 (vector reductions),
+    and at D = 32 and 96, which run on those kernels with their missing
+    columns read as zeros (dQ, dK and dV rows are exactly D wide here)."""
     B, H, N = 2, 3, 700
     scale = 1.0 / math.sqrt(D)
     q, k, v = make_qkv(B, H, N, D, 9400 + causal + D)
@@ -129,8 +131,7 @@ def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal, D):
     lib = tk.load()
     outs = []
     for _ in range(2):
-        dq = torch.full_like(qd, float("nan"))
-        dk, dv = torch.empty_like(qd), torch.empty_like(qd)
+        dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
         rc = lib.tk_attn_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), gd.data_ptr(),
                              lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
                              ws.numel(), B, H, N, D, int(causal), scale, None)
@@ -138,11 +139,12 @@ def test_bwd_dq_rows_all_written_over_poisoned_buffers(oracle_mod, causal, D):
         torch.cuda.synchronize()
         status, detail = tk.device_status()
         assert status == 0, f"device status {status} detail {detail:#x}"
-        outs.append(dq.cpu())
-    ref = oracle_mod.attn_bwd(q, k, v, do, causal, scale)[0]
-    for dq in outs:
-        g = dq.double().numpy()
-        assert np.all(np.isfinite(g)), f"dQ rows left unwritten: {np.argwhere(~np.isfinite(g))[:4]}"
-        err = np.abs(g - ref)
-        assert err.max() <= 0.02 * np.abs(ref).max() + 1e-4
-        assert err.mean() <= 0.01 * np.abs(ref).mean() + 1e-5
+        outs.append((dq.cpu(), dk.cpu(), dv.cpu()))
+    refs = oracle_mod.attn_bwd(q, k, v, do, causal, scale)
+    for got in outs:
+        for name, t, ref in zip(("dQ", "dK", "dV"), got, refs):
+            g = t.double().numpy()
+            assert np.all(np.isfinite(g)), f"{name} rows left unwritten: {np.argwhere(~np.isfinite(g))[:4]}"
+            err = np.abs(g - ref)
+            assert err.max() <= 0.02 * np.abs(ref).max() + 1e-4, name
+            assert err.mean() <= 0.01 * np.abs(ref).mean() + 1e-5, name

@@ -588,8 +588,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             const int key = kt * BT + t;
             const bool valid_key = key < p.N;
             const float scale = p.scale;
-            __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (valid_key ? key : 0)) * D;
-            __nv_bfloat16 *dvrow = static_cast<__nv_bfloat16 *>(p.dV) + (head_rows + (valid_key ? key : 0)) * D;
+            // rows of the tensors' head dim p.D (32 and 96 run on the 64- and
+            // 128-column kernel: the columns past p.D are not stored)
+            __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (valid_key ? key : 0)) * p.D;
+            __nv_bfloat16 *dvrow = static_cast<__nv_bfloat16 *>(p.dV) + (head_rows + (valid_key ? key : 0)) * p.D;
             // dK then dV, 32 columns at a time (one set of registers at once)
 #pragma unroll 1
             for (int q = 0; q < 2 * (D / 32); ++q) {
@@ -599,7 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 // every lane takes part in the TMEM loads; only the stores are guarded
                 uint32_t r[32];
                 tmem_ld32(lane_base + (is_v ? L::T_DV : L::T_DK) + c * 32, r);
-                if (valid_key) {
+                if (valid_key && c * 32 < p.D) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -623,14 +625,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 
 // Per padded query row (n_tiles * 128 rows per head): -Delta = -<dO, O> in
 // fp32 and -LSE * log2(e); rows past N get 0 and -inf.  D/8 lanes share a
-// row, 16 bytes of O and of dO each.  Also zeroes the dQ accumulator
-// (acc_vec4 float4s, grid-stride).
+// row (D the kernel's head dim), 16 bytes of O and of dO each, the lanes
+// past the tensors' head dim d reading nothing.  Also zeroes the dQ
+// accumulator (acc_vec4 float4s, grid-stride).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ LSE, float *__restrict__ neg_delta,
                                                       float *__restrict__ neg_lse2, float *__restrict__ dq_acc,
-                                                      int64_t padded_rows, int N, int n_tiles, int64_t acc_vec4) {
+                                                      int64_t padded_rows, int N, int d, int n_tiles,
+                                                      int64_t acc_vec4) {
     constexpr int LPR = D / 8;            // lanes per row
     constexpr int RPB = 256 / LPR;        // rows per block
     const int64_t prow = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / LPR;
@@ -639,10 +643,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
     const int64_t bh = prow / (static_cast<int64_t>(n_tiles) * BT);
     const int n = static_cast<int>(prow % (static_cast<int64_t>(n_tiles) * BT));
     float s = 0.0f;
-    if (live && n < N) {
+    if (live && n < N && sub * 8 < d) {
         const int64_t row = bh * N + n;
-        const uint4 o = reinterpret_cast<const uint4 *>(O + row * D)[sub];
-        const uint4 g = reinterpret_cast<const uint4 *>(dO + row * D)[sub];
+        const uint4 o = reinterpret_cast<const uint4 *>(O + row * d)[sub];
+        const uint4 g = reinterpret_cast<const uint4 *>(dO + row * d)[sub];
         const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -665,17 +669,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
 
 // dQ = bf16(scale * accumulator), one 128-row query tile per block.  The
 // accumulator of a tile is [D/4][128 rows][4 floats] (the order the main
-// kernel's vector reductions write): it is read with consecutive threads on
+// kernel's vector reductions write; D the kernel's head dim): its first d
+// columns (the tensors' head dim) are read with consecutive threads on
 // consecutive rows, turned into bf16 rows in shared memory, and written out
 // row by row, so both sides are coalesced.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dQ,
-                                                     int N, int n_tiles, float scale) {
+                                                     int N, int d, int n_tiles, float scale) {
     constexpr int STRIDE = D / 2 + 1;  // 32-bit words per staged row (odd: no bank conflicts)
     __shared__ uint32_t rows[BT * STRIDE];
     const int64_t tile = blockIdx.x;   // bh * n_tiles + qt
     const float4 *acc = reinterpret_cast<const float4 *>(dq_acc + tile * BT * D);
-    for (int i = threadIdx.x; i < BT * (D / 4); i += blockDim.x) {
+    for (int i = threadIdx.x; i < BT * (d / 4); i += blockDim.x) {
         const int t = i % BT, grp = i / BT;
         const float4 a = acc[i];  // columns 4*grp .. 4*grp+3 of row t
         rows[t * STRIDE + 2 * grp] = pack_bf16x2(scale * a.x, scale * a.y);
@@ -684,12 +689,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
     __syncthreads();
     const int qt = static_cast<int>(tile % n_tiles);
     const int64_t bh = tile / n_tiles;
-    for (int i = threadIdx.x; i < BT * (D / 8); i += blockDim.x) {
-        const int t = i / (D / 8), g = i % (D / 8);
+    for (int i = threadIdx.x; i < BT * (d / 8); i += blockDim.x) {
+        const int t = i / (d / 8), g = i % (d / 8);
         const int n = qt * BT + t;
         if (n >= N) continue;
         const uint32_t *r = rows + t * STRIDE + 4 * g;
-        reinterpret_cast<uint4 *>(dQ + (bh * N + n) * D)[g] = make_uint4(r[0], r[1], r[2], r[3]);
+        reinterpret_cast<uint4 *>(dQ + (bh * N + n) * d)[g] = make_uint4(r[0], r[1], r[2], r[3]);
     }
 }
 
@@ -710,7 +715,7 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     constexpr int RPB = 256 / (D / 8);  // rows per prep block
     bwd_prep_kernel<D><<<static_cast<unsigned>((padded_rows + RPB - 1) / RPB), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(p.O), static_cast<const __nv_bfloat16 *>(p.dO), p.LSE, p.neg_delta,
-        p.neg_lse2, p.dq_acc, padded_rows, p.N, p.n_tiles, acc_vec4);
+        p.neg_lse2, p.dq_acc, padded_rows, p.N, p.D, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // Causal: groups of L heads, L the largest divisor of B*H up to about
@@ -736,7 +741,7 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     if ((err = cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D>, p)) != cudaSuccess) return err;
 
     bwd_dq_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.n_tiles), 256, 0, stream>>>(
-        p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), p.N, p.n_tiles, p.scale);
+        p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), p.N, p.D, p.n_tiles, p.scale);
     return cudaGetLastError();
 }
 
@@ -744,8 +749,8 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
 
 cudaError_t launch_attn_bwd(int D, const BwdParams &p, int num_sms, cudaStream_t stream) {
     if (num_sms < 1) return cudaErrorInvalidValue;
-    if (D == 64) return bwd::launch_d<64>(p, num_sms, stream);
-    if (D == 128) return bwd::launch_d<128>(p, num_sms, stream);
+    if (D == 64 && p.D <= 64) return bwd::launch_d<64>(p, num_sms, stream);
+    if (D == 128 && p.D > 64 && p.D <= 128) return bwd::launch_d<128>(p, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

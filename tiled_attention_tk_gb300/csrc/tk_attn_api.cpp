@@ -156,10 +156,10 @@ int encode_out32_map(CUtensorMap *map, const void *ptr, int64_t N, int64_t BH) {
     return TK_OK;
 }
 
-// Shape checks shared by the forward and backward entry points.
+// Shape checks of the backward entry points.
 int check_shape(int64_t B, int64_t H, int64_t N, int64_t D) {
     if (B < 1 || H < 1 || N < 1) return TK_ERR_BAD_SHAPE;
-    if (D != 64 && D != 128) return TK_ERR_UNSUPPORTED_D;
+    if (D != 32 && D != 64 && D != 96 && D != 128) return TK_ERR_UNSUPPORTED_D;
     // TMA coordinates and the launch grid are 32-bit.
     if (N > INT32_MAX || B > INT32_MAX / H) return TK_ERR_BAD_SHAPE;
     const int64_t BH = B * H;
@@ -177,10 +177,15 @@ uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 extern "C" {
 
-// The fp32 dQ accumulator covers whole 128-row query tiles of every head.
+// The backward kernel's head dim: 32 and 96 run on the 64- and 128-column
+// kernels (their tensor maps read the missing columns as zeros).
+static int64_t bwd_kernel_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+
+// The fp32 dQ accumulator covers whole 128-row query tiles of every head, in
+// the kernel's head dim.
 static uint64_t dq_acc_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
     const uint64_t tiles = (static_cast<uint64_t>(N) + 127) / 128;
-    return static_cast<uint64_t>(B) * H * tiles * 128 * D * 4;
+    return static_cast<uint64_t>(B) * H * tiles * 128 * bwd_kernel_dim(D) * 4;
 }
 
 // One fp32 value per query row, over whole 128-row tiles of every head.
@@ -245,12 +250,13 @@ int tk_attn_bwd(const void *Q, const void *K, const void *V, const void *O, cons
     p.dK = dK;
     p.dV = dV;
     p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
     p.BH = static_cast<int>(BH);
     p.causal = causal;
     p.n_tiles = static_cast<int>((N + 127) / 128);
     p.scale = scale;
     p.scale_log2e = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    cudaError_t e = tk::launch_attn_bwd(static_cast<int>(D), p, num_sms, stream);
+    cudaError_t e = tk::launch_attn_bwd(static_cast<int>(bwd_kernel_dim(D)), p, num_sms, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return TK_OK;
 }

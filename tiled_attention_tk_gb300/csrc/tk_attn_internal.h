@@ -59,6 +59,7 @@ struct BwdParams {
     void *dK;
     void *dV;
     int N;
+    int D;             // head dim of the tensors (32, 64, 96, 128); the kernel's is 64 or 128
     int BH;
     int causal;
     int n_tiles;       // ceil(N / 128)
