@@ -259,7 +259,7 @@ int tk_gemm_uses_pairs(int64_t M, int64_t N, int64_t K, int stream_k);
  * as the cures for its L2 hit rate and wave quantisation
  * (10100.com/article/71410160, section on grid-level abstraction).
  * Large problems (at least one wave of 256 x 256 tiles over pairs of SMs,
- * K >= 1024) run on CTA pairs (two-SM tcgen05 products, each SM loading half
+ * K >= 768) run on CTA pairs (two-SM tcgen05 products, each SM loading half
  * of each operand tile), without stream-K, unless stream_k = 1 would split a
  * partial last wave and the pairs' waves would be less than 80 % full; the
  * pair path needs no workspace.  Either path gives the same C bit for bit

@@ -104,7 +104,7 @@ def test_gemm_bench_shape_sampled(oracle_mod):
 
 
 # ---------------------------------------------------------------- CTA pairs
-# At least one wave of 256 x 256 tiles over the SM pairs and K >= 1024 run on
+# At least one wave of 256 x 256 tiles over the SM pairs and K >= 768 run on
 # pairs of CTAs: the leader's MMAs read both CTAs' halves of A and B, and each
 # CTA writes its own 128 rows of every tile.
 
@@ -114,14 +114,15 @@ def _pair_shape_rows(M):
 
 
 @pytest.mark.parametrize("b_kmajor", [True, False])
-def test_gemm_pairs_ragged(oracle_mod, b_kmajor):
+@pytest.mark.parametrize("M,N,K", [(2148, 2632, 1032), (2304, 2064, 776)])
+def test_gemm_pairs_ragged(oracle_mod, b_kmajor, M, N, K):
     """9 x 11 pair tiles with M, N and K all ragged (the last tile's second
-    CTA holds no row of C), against the oracle on two rows of every 128-row
-    block; stream-K on or off takes the same path."""
-    M, N, K = 2148, 2632, 1032
+    CTA holds no row of C), and 9 x 9 with ragged N and the shortest K that
+    takes pairs; against the oracle on two rows of every 128-row block;
+    stream-K on or off takes the same path."""
     assert tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_uses_pairs(M, N, K, False)
     assert tk.gemm_workspace_bytes(M, N, K, True) == 0 and tk.gemm_workspace_bytes(M, N, K, False) == 0
-    a, b = _inputs(M, N, K, b_kmajor, 31)
+    a, b = _inputs(M, N, K, b_kmajor, 31 + K)
     rows = _pair_shape_rows(M)
     c1 = _run(a, b, b_kmajor, True)
     _check(oracle_mod, a, b, b_kmajor, c1, rows=rows, what=f"pairs {M}x{N}x{K} kmajor={b_kmajor}")

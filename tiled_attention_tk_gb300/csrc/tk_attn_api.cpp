@@ -458,17 +458,17 @@ int gemm_shape(int64_t M, int64_t N, int64_t K) {
 }
 
 // CTA pairs (cta_group::2, 256 x 256 tiles) take a problem with at least a
-// full wave of pair tiles and K >= 1024: per tile they ran 15-27 % faster than
-// single CTAs on the GB300 (8192^3, 6144^3, 16384^3, 8192 x 8192 x 1024,
-// 2048 x 8192 x 2048) and lost with fewer tiles than pairs (2048 x 2048 x
-// 4096).  They have no stream-K, so where the single-CTA plan would split a
+// full wave of pair tiles and K >= 768: per tile they ran 11-27 % faster than
+// single CTAs on the GB300 (8192^3, 6144^3, 16384^3, 8192 x 8192 x 1024 and
+// x 768, 2048 x 8192 x 2048), lost with fewer tiles than pairs (2048 x 2048 x
+// 4096) and at shorter K (8192 x 8192 x 512: -5 %; x 256: -13 %).  They have no stream-K, so where the single-CTA plan would split a
 // partial last wave in K, pairs are kept only while their own waves are at
 // least 80 % full (3000 x 5120 x 4096, 79 %, measured a tie and stays with
 // stream-K).
 bool use_pairs(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
     const int64_t pairs = num_sms / 2;
     const int64_t t2 = ((M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * ((N + kGemmBN - 1) / kGemmBN);
-    if (pairs < 1 || K < 16 * kGemmBK || t2 < pairs) return false;
+    if (pairs < 1 || K < 12 * kGemmBK || t2 < pairs) return false;
     const int64_t t1 = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
     const int64_t k_iters = (K + kGemmBK - 1) / kGemmBK;
     if (stream_k && k_iters >= kGemmSkMinKIters && t1 > num_sms && t1 % num_sms != 0) {
