@@ -140,6 +140,17 @@ def test_gemm_pairs_full_wave_multiple(oracle_mod):
     _check(oracle_mod, a, b, True, c, rows=_pair_shape_rows(M)[::3], what="pairs 4864x4096x2048")
 
 
+def test_gemm_pairs_second_cta_empty(oracle_mod):
+    """M = 100: every pair tile's second CTA lies wholly past M (its loads read
+    zeros, its stores are clipped away), across 76 pair tiles of N; every row
+    against the oracle."""
+    M, N, K = 100, 76 * 256, 1024
+    assert tk.gemm_uses_pairs(M, N, K, True)
+    a, b = _inputs(M, N, K, True, 34)
+    c = _run(a, b, True, True)
+    _check(oracle_mod, a, b, True, c, what="pairs M=100")
+
+
 def test_gemm_pairs_deterministic():
     a, b = _inputs(2148, 2632, 1032, True, 33)
     c1 = _run(a, b, True, True)

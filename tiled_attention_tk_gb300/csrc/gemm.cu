@@ -11,16 +11,19 @@
 //   B  bf16 [N, K] row-major (C = A B^T, "b_kmajor")  or  [K, N] (C = A B)
 //   fp32 accumulation in TMEM, C rounded to bf16 (round to nearest even).
 //
-// One persistent CTA per SM, 192 threads: a TMA producer warp, an MMA warp
-// and four epilogue warps (one per 32 TMEM lanes).  Output tiles are 128 x 256
+// Two kernels.  Large problems run on CTA pairs (gemm_pair_kernel, below:
+// 256 x 256 tiles, M = 256 products shared by two SMs, each loading half of
+// the operand tiles).  The rest run on single CTAs (gemm_kernel): one
+// persistent CTA per SM, 192 threads: a TMA producer warp, an MMA warp and
+// four epilogue warps (one per 32 TMEM lanes).  Output tiles are 128 x 256
 // (tcgen05 M = 128, N = 256), the K loop runs in steps of 64 through a
 // four-stage shared-memory ring, and the accumulator is double-buffered in
 // TMEM (2 x 256 columns) so the epilogue of one tile overlaps the main loop of
-// the next.
+// the next.  The pair kernel keeps the same roles, tile order and epilogue.
 //
-// Schedule.  Tiles are numbered in groups of group_m tile rows, column by
-// column inside a group, so the CTAs running at the same time share rows of
-// A and columns of B in L2 (the threadblock swizzle).  The first dp_tiles
+// Schedule (single CTAs).  Tiles are numbered in groups of group_m tile
+// rows, column by column inside a group, so the CTAs running at the same
+// time share rows of A and columns of B in L2 (the threadblock swizzle).  The first dp_tiles
 // tiles are handed out whole, round-robin over the CTAs (data-parallel
 // waves).  When the tile count is not a multiple of the CTA count, the last
 // sk_tiles tiles (the partial wave plus one full wave) are split in K: their
