@@ -63,6 +63,33 @@ def test_d256_queries_against_longer_keys(oracle_mod, Nq, Nkv, causal):
     _check(oracle_mod, q, k, v, causal, 1.0 / math.sqrt(D), f"Nq={Nq} Nkv={Nkv}")
 
 
+def test_d256_causal_mirrored_pairs(oracle_mod):
+    """Under the causal mask with more query-tile pairs than CTAs, the first
+    heads run their Q tiles in mirrored pairs (tile n-1-i, then tile i, on one
+    CTA) and the rest heaviest first.  B1 H40 N2048 (16 Q tiles, 8 pairs per
+    head): 21 heads in pairs on the device's 152 SMs.  Heads on both sides of
+    that boundary, and the first and last, in full against the oracle; the
+    whole launch finite."""
+    H, N = 40, 2048
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hp = N // 128 // 2
+    paired = max(0, (H * hp - min(H * 2 * hp, sms)) // hp)
+    assert 0 < paired < H, paired
+    q, k, v = make_qkv(1, H, N, D, 8100)
+    scale = 1.0 / 16.0
+    o, lse = tk.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    status, detail = tk.device_status()
+    assert status == 0, f"device status {status} detail {detail:#x}"
+    o, lse = o.cpu().double().numpy(), lse.cpu().double().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    for h in sorted({0, paired - 1, paired, H - 1}):
+        O_ref, L_ref = oracle_mod.attn_fwd(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], True, scale)
+        err = np.abs(o[:, h:h + 1] - O_ref)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (h, err.max(), err.mean())
+        assert np.abs(lse[:, h:h + 1] - L_ref).max() <= 1e-3, h
+
+
 def test_d256_deterministic():
     q, k, v = (t.cuda() for t in make_qkv(2, 4, 1500, D, 9000))
     o1, l1 = tk.fwd(q, k, v, causal=True)
