@@ -237,10 +237,10 @@ int tk_attn_bwd_noalloc(const void *Q, const void *K, const void *V, const void 
 
 /*
  * tk_gemm_workspace_bytes -- device workspace tk_gemm needs on the current
- * device for this shape: 0 when the schedule has no stream-K part (the pair
- * path never has; also for a shape tk_gemm rejects), else one 128 x 256 fp32
- * partial-sum slot per SM plus one counter per stream-K tile, each section
- * 256-byte aligned.
+ * device for this shape: 0 when the schedule has no stream-K part (also for a
+ * shape tk_gemm rejects), else one 128 x 256 fp32 partial-sum slot per CTA of
+ * the grid (a pair of CTAs shares a 256 x 256 slot) plus one counter per
+ * stream-K tile, each section 256-byte aligned.
  */
 size_t tk_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int stream_k);
 
@@ -260,11 +260,9 @@ int tk_gemm_uses_pairs(int64_t M, int64_t N, int64_t K, int stream_k);
  * (10100.com/article/71410160, section on grid-level abstraction).
  * Large problems (at least one wave of 256 x 256 tiles over pairs of SMs,
  * K >= 768) run on CTA pairs (two-SM tcgen05 products, each SM loading half
- * of each operand tile), without stream-K, unless stream_k = 1 would split a
- * partial last wave and the pairs' waves would be less than 80 % full; the
- * pair path needs no workspace.  Either path gives the same C bit for bit
- * when no tile is split in K (each output element is one fp32 dot product in
- * k order).
+ * of each operand tile); there stream-K splits the last waves only below four
+ * waves of pair tiles.  Either path gives the same C bit for bit when no tile
+ * is split in K (each output element is one fp32 dot product in k order).
  *
  *   C[m,n] = sum_k A[m,k] * B'[k,n],  fp32 accumulation, C rounded to bf16
  *            (round to nearest even), where B' = B^T if b_kmajor else B.

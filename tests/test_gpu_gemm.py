@@ -72,14 +72,16 @@ def test_gemm_fewer_tiles_than_sms(oracle_mod, b_kmajor):
 
 @pytest.mark.parametrize("b_kmajor", [True, False])
 def test_gemm_stream_k_partial_wave(oracle_mod, b_kmajor):
-    """24 x 20 = 480 tiles, K = 4096: whole-tile waves, then the partial wave
-    plus one wave split in K.  Checked on two rows of every 128-row block (so
-    every tile), for stream-K on and off."""
+    """12 x 20 = 240 pair tiles, K = 4096: whole-tile waves, then the partial
+    wave plus one wave split in K over the pairs (each CTA of a pair writes its
+    128 rows of the partial).  Checked on two rows of every 128-row block (so
+    every tile and both CTAs' halves), for stream-K on and off."""
     M, N, K = 3000, 5120, 4096
     a, b = _inputs(M, N, K, b_kmajor, 22)
     assert tk.gemm_workspace_bytes(M, N, K, True) > 0
-    # with stream-K the pairs' waves would be 79 % full: single CTAs and stream-K
-    assert not tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_uses_pairs(M, N, K, False)
+    # 12 x 20 = 240 pair tiles: 3.2 waves over the pairs, the last partial
+    # wave plus one split in K
+    assert tk.gemm_uses_pairs(M, N, K, True) and tk.gemm_uses_pairs(M, N, K, False)
     rows = sorted({r for blk in range(0, M, 128) for r in (blk + 3, min(blk + 127, M - 1))})
     for stream_k in (True, False):
         c = _run(a, b, b_kmajor, stream_k)

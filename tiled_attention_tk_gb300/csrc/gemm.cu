@@ -403,8 +403,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 // rows of the accumulator.  The peer's TMA loads complete on the leader's
 // stage barrier (which expects both CTAs' bytes); the leader's commits
 // arrive on the barriers of both CTAs, one commit per CTA; the epilogue warps
-// of both CTAs free an accumulator on the leader's barrier.  Tiles go whole
-// and round-robin over the pairs (no stream-K).
+// of both CTAs free an accumulator on the leader's barrier.  The schedule is
+// the single-CTA kernel's with pairs in place of CTAs: whole tiles round-robin
+// over the pairs, then, when the tiles do not fill whole waves, the partial
+// wave plus one full wave split in K over all pairs (stream-K; a pair's
+// partial goes to its own 256 x 256 slot, each CTA its 128 rows, and each of
+// the pair's eight epilogue warps counts it on the tile's counter).
 namespace pair {
 
 constexpr int BM = 128;            // output rows per CTA (256 per pair)
@@ -478,7 +482,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const int pair_id = static_cast<int>(blockIdx.x) / 2;
     const int n_pairs = static_cast<int>(gridDim.x) / 2;
-    const int n_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == WARP_TMA) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -487,10 +490,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tma_prefetch_desc(&p.tmB);
             uint32_t n = 0;  // stages filled so far
             bool ok = true;
-            for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+            Schedule sched(p, pair_id, n_pairs);
+            Item it;
+            while (ok && sched.next(it)) {
                 int tm, tn;
-                tile_coords(tile, p, tm, tn);
-                for (int k = 0; k < p.k_iters; ++k, ++n) {
+                tile_coords(it.tile, p, tm, tn);
+                for (int k = it.kb; k < it.ke; ++k, ++n) {
                     const uint32_t s = n % STAGES;
                     if (n >= STAGES &&
                         !(ok = wait_bounded(bar(B_EMPTY + s), ((n / STAGES) - 1) & 1, abort_flag,
@@ -530,7 +535,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             uint32_t n = 0;      // stages consumed
             uint32_t items = 0;  // accumulators used
             bool ok = true;
-            for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+            Schedule sched(p, pair_id, n_pairs);
+            Item it;
+            while (ok && sched.next(it)) {
                 const uint32_t acc = items & 1;
                 // both CTAs' epilogues have read this accumulator's previous tile
                 if (items >= 2) {
@@ -551,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d = tmem + acc * BN;
-                for (int k = 0; k < p.k_iters; ++k, ++n) {
+                for (int k = it.kb; k < it.ke; ++k, ++n) {
                     const uint32_t s = n % STAGES;
                     if (!(ok = wait_bounded(bar(B_FULL + s), (n / STAGES) & 1, abort_flag,
                                             (ROLE_GEMM_MMA << 24) | ((B_FULL + s) << 16) | (n & 0xFFFF))))
@@ -570,7 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (elect_one()) {
                         umma_ss_x4_pair(d, av, static_cast<uint32_t>(ad >> 32), bv, static_cast<uint32_t>(bd >> 32),
-                                        IDESC, k > 0 ? 1u : 0u);
+                                        IDESC, k > it.kb ? 1u : 0u);
                         // the stage is free in both CTAs once these MMAs are done
                         umma_commit_pair(rank_bar(B_EMPTY + s, 0));
                         umma_commit_pair(rank_bar(B_EMPTY + s, 1));
@@ -599,9 +606,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const uint32_t cstage = sbase + CSTAGE_OFF + (warp - WARP_EPI) * 2 * C_BOX_BYTES;
         uint8_t *cstage_ptr = smem + CSTAGE_OFF + (warp - WARP_EPI) * 2 * C_BOX_BYTES;
+        const int row = static_cast<int>(rank) * BM + q * 32 + lane;  // row of the pair's 256-row tile
+        // this CTA's accumulator is free again for the leader's MMAs
+        auto free_acc = [&](uint32_t acc) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead_bar(B_ACC_EMPTY + acc));
+        };
         uint32_t items = 0, boxes = 0;
         bool ok = true;
-        for (int tile = pair_id; ok && tile < n_tiles; tile += n_pairs) {
+        Schedule sched(p, pair_id, n_pairs);
+        Item it;
+        while (ok && sched.next(it)) {
             const uint32_t acc = items & 1;
             const uint32_t ph = (items >> 1) & 1;
             bool done = mbar_try_wait_cluster(bar(B_ACC_FULL + acc), ph);
@@ -621,23 +637,79 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             ++items;
             const uint32_t d = lane_base + acc * BN;
             int tm, tn;
-            tile_coords(tile, p, tm, tn);
+            tile_coords(it.tile, p, tm, tn);
+            if (it.kb > 0) {
+                // --- stream-K partial: fp32 into the pair's slot, [64 column
+                // groups][256 rows][4] (each CTA its 128 rows), then counted
+                // on the tile's counter by each of the pair's eight warps.
+                float4 *slot = reinterpret_cast<float4 *>(p.partials) + static_cast<size_t>(pair_id) * (2 * BM * BN / 4);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(d + c * 32, v);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        __stcg(slot + (c * 8 + g) * (2 * BM) + row,
+                               make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                           __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+                }
+                free_acc(acc);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.counters + (it.tile - p.dp_tiles), 1u);
+                continue;
+            }
+            // --- the tile's result: this accumulator plus, for a stream-K
+            // tile, the partials of the pairs that hold its later K ranges.
+            int first_peer = 0, last_peer = -1;
+            if (it.ke < p.k_iters) {
+                const int64_t start = static_cast<int64_t>(it.tile - p.dp_tiles) * p.k_iters;
+                const int64_t end = start + p.k_iters;
+                first_peer = pair_id + 1;
+                last_peer = static_cast<int>((end - 1) / p.sk_iters_per_cta);
+                const uint32_t want = 8u * static_cast<uint32_t>(last_peer - pair_id);
+                if (lane == 0) {
+                    const unsigned *ctr = p.counters + (it.tile - p.dp_tiles);
+                    const uint64_t tw = global_timer_ns();
+                    while (ld_acquire_u32(ctr) < want) {
+                        if (*abort_flag) { ok = false; break; }
+                        if (global_timer_ns() - tw > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            record_timeout((ROLE_GEMM_EPILOGUE << 24) | (0xFFu << 16) | (it.tile & 0xFFFF));
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                __threadfence();
+            }
 #pragma unroll 1
             for (int h = 0; h < BN / 64; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
+                    const int c = 2 * h + c2;
                     uint32_t v[32];
-                    tmem_ld32(d + (2 * h + c2) * 32, v);
-                    if (h == BN / 64 - 1 && c2 == 1) {
-                        // accumulator free (in this CTA) for the leader's MMAs
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(lead_bar(B_ACC_EMPTY + acc));
+                    tmem_ld32(d + c * 32, v);
+                    if (h == BN / 64 - 1 && c2 == 1) free_acc(acc);
+                    float f[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(v[e]);
+                    for (int peer = first_peer; ok && peer <= last_peer; ++peer) {
+                        const float4 *slot =
+                            reinterpret_cast<const float4 *>(p.partials) + static_cast<size_t>(peer) * (2 * BM * BN / 4);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const float4 x = __ldcg(slot + (c * 8 + g) * (2 * BM) + row);
+                            f[4 * g] += x.x;
+                            f[4 * g + 1] += x.y;
+                            f[4 * g + 2] += x.z;
+                            f[4 * g + 3] += x.w;
+                        }
                     }
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[c2 * 16 + e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                    for (int e = 0; e < 16; ++e) pk[c2 * 16 + e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
                 }
                 const uint32_t b = boxes & 1;
                 ++boxes;
@@ -672,6 +744,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace gemm
 
+// Pairs of CTAs of the pair kernel that can be resident at once on the
+// current device (a GPC with an odd number of free SMs holds one pair fewer
+// than half its SMs); cached per device.
+cudaError_t gemm_pair_capacity(int *pairs) {
+    static thread_local int cached_device = -1, cached_pairs = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (cached_device != dev) {
+        for (auto kern : {gemm::gemm_pair_kernel<true>, gemm::gemm_pair_kernel<false>})
+            if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            gemm::pair::SMEM_ALLOC)) != cudaSuccess)
+                return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(gemm::NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = gemm::pair::SMEM_ALLOC;
+        int n = 0;
+        if ((err = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_pair_kernel<true>, &cfg)) != cudaSuccess)
+            return err;
+        cached_pairs = n;
+        cached_device = dev;
+    }
+    *pairs = cached_pairs;
+    return cudaSuccess;
+}
+
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream) {
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -693,24 +792,20 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream) {
         configured_device = dev;
     }
     if (p.pair) {
-        if (grid < 2 || grid % 2 != 0 || p.sk_tiles != 0) return cudaErrorInvalidValue;
+        // The pairs are persistent and the stream-K ranges were planned for
+        // this many of them: all must be resident at once.
+        int max_pairs = 0;
+        if ((err = gemm_pair_capacity(&max_pairs)) != cudaSuccess) return err;
+        if (grid < 2 || grid % 2 != 0 || grid / 2 > max_pairs) return cudaErrorInvalidConfiguration;
+        if (p.sk_tiles > 0) {
+            err = cudaMemsetAsync(p.counters, 0, static_cast<size_t>(p.sk_tiles) * sizeof(unsigned), stream);
+            if (err != cudaSuccess) return err;
+        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // clusters of two (compile-time dims)
         cfg.blockDim = dim3(gemm::NUM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = gemm::pair::SMEM_ALLOC;
         cfg.stream = stream;
-        // The pairs are persistent: no more of them than can be resident at
-        // once (a GPC with an odd number of free SMs holds one pair fewer).
-        static thread_local int pairs_device = -1, max_pairs = 0;
-        if (pairs_device != dev) {
-            int n = 0;
-            err = cudaOccupancyMaxActiveClusters(&n, gemm::gemm_pair_kernel<true>, &cfg);
-            if (err != cudaSuccess) return err;
-            if (n < 1) return cudaErrorInvalidConfiguration;
-            max_pairs = n;
-            pairs_device = dev;
-        }
-        if (grid / 2 > max_pairs) cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs), 1, 1);
         return p.b_kmajor ? cudaLaunchKernelEx(&cfg, gemm::gemm_pair_kernel<true>, p)
                           : cudaLaunchKernelEx(&cfg, gemm::gemm_pair_kernel<false>, p);
     }

@@ -461,48 +461,46 @@ int gemm_shape(int64_t M, int64_t N, int64_t K) {
 // full wave of pair tiles and K >= 768: per tile they ran 11-27 % faster than
 // single CTAs on the GB300 (8192^3, 6144^3, 16384^3, 8192 x 8192 x 1024 and
 // x 768, 2048 x 8192 x 2048), lost with fewer tiles than pairs (2048 x 2048 x
-// 4096) and at shorter K (8192 x 8192 x 512: -5 %; x 256: -13 %).  They have no stream-K, so where the single-CTA plan would split a
-// partial last wave in K, pairs are kept only while their own waves are at
-// least 80 % full (3000 x 5120 x 4096, 79 %, measured a tie and stays with
-// stream-K).
-bool use_pairs(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
-    const int64_t pairs = num_sms / 2;
+// 4096) and at shorter K (8192 x 8192 x 512: -5 %; x 256: -13 %).  `pairs` is
+// the number of pairs that can be resident at once.
+bool use_pairs(int64_t M, int64_t N, int64_t K, int64_t pairs) {
     const int64_t t2 = ((M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * ((N + kGemmBN - 1) / kGemmBN);
-    if (pairs < 1 || K < 12 * kGemmBK || t2 < pairs) return false;
-    const int64_t t1 = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
-    const int64_t k_iters = (K + kGemmBK - 1) / kGemmBK;
-    if (stream_k && k_iters >= kGemmSkMinKIters && t1 > num_sms && t1 % num_sms != 0) {
-        const int64_t waves = (t2 + pairs - 1) / pairs;
-        if (5 * t2 < 4 * waves * pairs) return false;
+    return pairs >= 1 && K >= 12 * kGemmBK && t2 >= pairs;
+}
+
+// The pairs the device can hold at once (0 if the query fails: single CTAs).
+int64_t resident_pairs(int num_sms) {
+    int n = 0;
+    if (tk::gemm_pair_capacity(&n) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
     }
-    return true;
+    return n < num_sms / 2 ? n : num_sms / 2;
 }
 
 // Data-parallel waves of whole tiles; when the tiles do not fill the last
 // wave (and there is more than one wave), the last partial wave plus one full
-// wave are split in K over all CTAs (stream-K): every CTA gets at least one
-// tile's worth of K iterations, so a tile has at most two K segments.
+// wave are split in K over all workers (stream-K): every worker gets at least
+// one tile's worth of K iterations, so a tile has at most two K segments.  A
+// worker is a CTA, or a pair of CTAs on the pair path (256 x 256 tiles, a
+// 256 x 256 partial slot per pair).  Pairs split only below four waves: there
+// stream-K gained (3000 x 5120 x 4096, 3.2 waves: 1474 -> 1581 TFLOP/s against
+// single CTAs with stream-K), beyond it the partials cost what the last wave
+// loses (8192^3, 13.5 waves: 1894 vs 1885; 6144^3, 7.6 waves: 1886 vs 1856).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
     GemmPlan g = {};
-    if (use_pairs(M, N, K, num_sms, stream_k)) {
-        g.pair = 1;
-        g.tiles_m = static_cast<int>((M + 2 * kGemmBM - 1) / (2 * kGemmBM));
-        g.tiles_n = static_cast<int>((N + kGemmBN - 1) / kGemmBN);
-        g.k_iters = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
-        const int64_t T = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
-        const int64_t pairs = num_sms / 2;
-        g.dp_tiles = static_cast<int>(T);
-        g.grid = static_cast<int>(2 * (T < pairs ? T : pairs));
-        return g;
-    }
-    g.tiles_m = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
+    const int64_t pairs = resident_pairs(num_sms);
+    g.pair = use_pairs(M, N, K, pairs) ? 1 : 0;
+    const int64_t bm = g.pair ? 2 * kGemmBM : kGemmBM;
+    g.tiles_m = static_cast<int>((M + bm - 1) / bm);
     g.tiles_n = static_cast<int>((N + kGemmBN - 1) / kGemmBN);
     g.k_iters = static_cast<int>((K + kGemmBK - 1) / kGemmBK);
     const int64_t T = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
-    const int P = num_sms;
-    if (!stream_k || g.k_iters < kGemmSkMinKIters || T <= P || T % P == 0) {
+    const int64_t P = g.pair ? pairs : num_sms;  // workers
+    const int per_worker = g.pair ? 2 : 1;       // CTAs per worker
+    if (!stream_k || g.k_iters < kGemmSkMinKIters || T <= P || T % P == 0 || (g.pair && T >= 4 * P)) {
         g.dp_tiles = static_cast<int>(T);
-        g.grid = static_cast<int>(T < P ? T : P);
+        g.grid = static_cast<int>(per_worker * (T < P ? T : P));
         return g;
     }
     g.sk_tiles = static_cast<int>(P + T % P);  // the partial wave plus one full wave
@@ -511,8 +509,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int stream_k) {
     int64_t L = (total + P - 1) / P;
     if (L < kGemmMinSkIters) L = kGemmMinSkIters;
     g.sk_iters_per_cta = static_cast<int>(L);
-    g.grid = P;
-    g.workspace = round_up(static_cast<uint64_t>(P) * kGemmSlotBytes, kWorkspaceAlign) +
+    g.grid = static_cast<int>(per_worker * P);
+    // one 128 x 256 fp32 slot per CTA (a pair's 256 x 256 slot is its two CTAs' slots)
+    g.workspace = round_up(static_cast<uint64_t>(g.grid) * kGemmSlotBytes, kWorkspaceAlign) +
                   round_up(static_cast<uint64_t>(g.sk_tiles) * 4, kWorkspaceAlign);
     return g;
 }

@@ -85,10 +85,13 @@ struct GemmParams {
     int sk_tiles;      // tiles [dp_tiles, dp_tiles + sk_tiles): split in K (stream-K)
     int sk_iters_per_cta;  // K iterations of the stream-K range of each CTA
     int pair;          // 1: CTA pairs (cta_group::2) on 256 x 256 tiles; tiles_m counts 256-row tiles,
-                       // tmB's box is {64, 128, 1} when b_kmajor, and there is no stream-K
+                       // tmB's box is {64, 128, 1} when b_kmajor, the schedule's CTAs are pairs
+                       // (grid = 2 x pairs) and a partial slot is 256 x 256
 };
 
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t stream);
+// CTA pairs of the GEMM's pair kernel that can be resident at once on the current device.
+cudaError_t gemm_pair_capacity(int *pairs);
 cudaError_t read_and_clear_gemm_status(uint32_t *status, uint32_t *detail);
 
 // Everything the Based linear-attention kernel needs (Dqk = 16, Dv = 64).
