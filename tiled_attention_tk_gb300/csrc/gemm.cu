@@ -84,8 +84,9 @@ struct Item {
     int tile, kb, ke;
 };
 
-// Walks the work of CTA `cta`: its data-parallel tiles, then its stream-K
-// range.  Every role of the CTA walks the same sequence.
+// Walks the work of worker `cta` of `grid` (a CTA, or on the pair path a pair
+// of CTAs): its data-parallel tiles, then its stream-K range.  Every role of
+// the worker walks the same sequence.
 struct Schedule {
     const GemmParams &p;
     int cta, grid;

@@ -83,7 +83,7 @@ struct GemmParams {
     int group_m;       // tile rows per L2 group of the tile order
     int dp_tiles;      // tiles [0, dp_tiles): whole tiles, round-robin over the CTAs
     int sk_tiles;      // tiles [dp_tiles, dp_tiles + sk_tiles): split in K (stream-K)
-    int sk_iters_per_cta;  // K iterations of the stream-K range of each CTA
+    int sk_iters_per_cta;  // K iterations of the stream-K range of each worker (CTA, or pair)
     int pair;          // 1: CTA pairs (cta_group::2) on 256 x 256 tiles; tiles_m counts 256-row tiles,
                        // tmB's box is {64, 128, 1} when b_kmajor, the schedule's CTAs are pairs
                        // (grid = 2 x pairs) and a partial slot is 256 x 256
