@@ -94,7 +94,9 @@ struct Layout {
     static constexpr int B_MMADONE = 17;
     static constexpr int B_STAGED = 18;    // + buffer (2): dQ_part staged (dQ warps, 4)
     static constexpr int B_STAGEFREE = 20; // + buffer (2): its bulk reduction has read it (one thread)
-    static constexpr int NUM_BARS = 22;
+    static constexpr int B_KVFREE = 22;    // a unit's K and V are no longer read (MMA commit)
+    static constexpr int B_DKVREAD = 23;   // a unit's dK and dV have left TMEM (dQ warps, 4)
+    static constexpr int NUM_BARS = 24;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     // No alignment slack: the dynamic shared memory of a kernel without
     // static shared memory starts 1024-byte aligned (the kernel checks).
@@ -151,6 +153,34 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
 
 __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
+// Work units: key tile kt of head bh.  Without the mask every unit costs the
+// same and the grid is persistent (at most one CTA per SM): CTA c takes the
+// head-major units c, c + grid, ..., so the CTAs running together hold a few
+// heads' key tiles and share their Q and dO through L2, and a CTA's next unit
+// loads while its last one finishes.  Under the mask key tile kt sees n_tiles
+// - kt query tiles: the grid is (L, n_tiles, B*H / L), one unit per block,
+// and blocks start roughly in launch order (x fastest), so heads run in
+// groups of L whose key tiles launch tile by tile across the group, heaviest
+// first, and the SMs take the next block as they free (which balances unequal
+// units better than a fixed assignment).
+struct BwdUnit {
+    int kt, bh;
+};
+
+template <bool PERSIST>
+__device__ __forceinline__ int bwd_units_of_cta(const BwdParams &p) {
+    if (!PERSIST) return 1;
+    const int total = p.BH * p.n_tiles, grid = gridDim.x;
+    return (total - static_cast<int>(blockIdx.x) + grid - 1) / grid;
+}
+
+template <bool PERSIST>
+__device__ __forceinline__ BwdUnit bwd_unit(int k, const BwdParams &p) {
+    if (!PERSIST) return {static_cast<int>(blockIdx.y), static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x)};
+    const int idx = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    return {idx % p.n_tiles, idx / p.n_tiles};
+}
+
 // Keys sit on the TMEM lanes: the MMA warp forms S^T = K Q^T and
 // dP^T = V dO^T, so that each key row of the tile belongs to one TMEM lane.
 // Two groups of four compute warps (queries 0..63 and 64..127) write P^T
@@ -164,7 +194,9 @@ __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.
 //
 // The unscaled dS' = P (dP - Delta) is what the products see; dK and dQ are
 // multiplied by `scale` when they are rounded to bf16.
-template <int D>
+// PERSIST is !p.causal: each launch shape has its own instantiation (the
+// one-unit blocks of the causal grid then carry no unit loop).
+template <int D, bool PERSIST>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = Layout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -180,18 +212,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    // Work: key tile kt of head bh.  The grid is (L, n_tiles, B*H / L) and
-    // blocks start roughly in launch order (x fastest): the heads run in
-    // groups of L, and a group's key tiles launch tile by tile across its
-    // heads.  The blocks running together then share a few heads' Q and dO
-    // through L2, and under the causal mask, where key tile kt sees n_tiles
-    // - kt query tiles, each group goes heaviest first (L = 1 without it).
-    const int kt = blockIdx.y;
-    const int bh = blockIdx.z * gridDim.x + blockIdx.x;
-    const int qt_first = p.causal ? kt : 0;
-    const int n_q = p.n_tiles - qt_first;
-    const size_t head_rows = static_cast<size_t>(bh) * p.N;
-    const size_t head_tiles = static_cast<size_t>(bh) * p.n_tiles;
+    const int my_units = bwd_units_of_cta<PERSIST>(p);
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -212,6 +233,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         mbar_init(bar(L::B_GDONE), 1);
         mbar_init(bar(L::B_DQREAD), 4);
         mbar_init(bar(L::B_MMADONE), 1);
+        mbar_init(bar(L::B_KVFREE), 1);
+        mbar_init(bar(L::B_DKVREAD), 4);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_STAGED + b), 4);
             mbar_init(bar(L::B_STAGEFREE + b), 1);
@@ -231,39 +254,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             tma_prefetch_desc(&p.tmK);
             tma_prefetch_desc(&p.tmV);
             tma_prefetch_desc(&p.tmDO);
-            mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
-            for (int c = 0; c < L::KATOMS; ++c) {
-                tma_load_3d(sbase + L::K_OFF + c * L::BOX, &p.tmK, bar(L::B_KVFULL), c * 64, kt * BT, bh);
-                tma_load_3d(sbase + L::V_OFF + c * L::BOX, &p.tmV, bar(L::B_KVFULL), c * 64, kt * BT, bh);
-            }
-            int issued = 0;
-            for (int it = 0; it < n_q; ++it) {
-                const int b = it & 1;
-                // Buffer b was last used by query tile it-2.
-                if (it >= 2 && !wait_bounded(bar(L::B_QEMPTY + b), ((it >> 1) - 1) & 1, abort_flag,
-                                             (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | it)) {
-                    // Let the copies in flight land before the CTA exits.
-                    const uint64_t t0 = global_timer_ns();
-                    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-                        while (!mbar_try_wait(bar(L::B_QFULL + (j & 1)), (j >> 1) & 1) &&
-                               global_timer_ns() - t0 < kDrainLimitNs) {
-                        }
-                    while (!mbar_try_wait(bar(L::B_KVFULL), 0) && global_timer_ns() - t0 < kDrainLimitNs) {
-                    }
-                    break;
-                }
-                const int qt = qt_first + it;
-                const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                const uint32_t rb = sbase + L::RB_OFF + b * 1024;
-                const size_t row0 = (head_tiles + qt) * BT;
-                mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
+            uint32_t g = 0;          // query tiles loaded (all units of the CTA)
+            uint32_t kv_loads = 0;   // units whose K and V were loaded
+            bool ok = true;
+            auto load_kv = [&](const BwdUnit &u) {
+                mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
                 for (int c = 0; c < L::KATOMS; ++c) {
-                    tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
-                    tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, bh);
+                    tma_load_3d(sbase + L::K_OFF + c * L::BOX, &p.tmK, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
+                    tma_load_3d(sbase + L::V_OFF + c * L::BOX, &p.tmV, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
                 }
-                bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
-                bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
-                ++issued;
+                ++kv_loads;
+            };
+            for (int k = 0; ok && k < my_units; ++k) {
+                const BwdUnit u = bwd_unit<PERSIST>(k, p);
+                const int qt_first = p.causal ? u.kt : 0;
+                const int n_q = p.n_tiles - qt_first;
+                const size_t head_tiles = static_cast<size_t>(u.bh) * p.n_tiles;
+                if (k == 0) load_kv(u);  // the first unit's K and V lead
+                for (int it = 0; it < n_q; ++it) {
+                    const int b = g & 1;
+                    // Buffer b was last used by query tile g-2.
+                    if (g >= 2 && !(ok = wait_bounded(bar(L::B_QEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                      (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | (g & 0xFFFF))))
+                        break;
+                    const int qt = qt_first + it;
+                    const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                    const uint32_t rb = sbase + L::RB_OFF + b * 1024;
+                    const size_t row0 = (head_tiles + qt) * BT;
+                    mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
+                    for (int c = 0; c < L::KATOMS; ++c) {
+                        tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                        tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                    }
+                    bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
+                    bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
+                    ++g;
+                    if (it == 0 && k > 0) {
+                        // a later unit's K and V, once the unit before no longer reads
+                        // them (its first Q and dO went ahead into the free buffer)
+                        if (!(ok = wait_bounded(bar(L::B_KVFREE), (k - 1) & 1, abort_flag,
+                                                (ROLE_BWD_PRODUCER << 24) | (L::B_KVFREE << 16) | k)))
+                            break;
+                        load_kv(u);
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the copies in flight land before the CTA exits.
+                const uint64_t t0 = global_timer_ns();
+                for (uint32_t j = g >= 2 ? g - 2 : 0; j < g; ++j)
+                    while (!mbar_try_wait(bar(L::B_QFULL + (j & 1)), (j >> 1) & 1) &&
+                           global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
+                if (kv_loads > 0)
+                    while (!mbar_try_wait(bar(L::B_KVFULL), (kv_loads - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    }
             }
         }
         __syncwarp();
@@ -306,82 +351,104 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             };
             auto issue_s = [&](uint32_t qb) { issue_kmajor(tmem + L::T_S, sbase + L::K_OFF, qb, L::B_SFULL); };     // S^T = K Q^T
             auto issue_dp = [&](uint32_t dob) { issue_kmajor(tmem + L::T_DP, sbase + L::V_OFF, dob, L::B_DPFULL); };  // dP^T = V dO^T
-            bool ok = wait_bounded(bar(L::B_KVFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16)) &&
-                      wait_bounded(bar(L::B_QFULL), 0, abort_flag, (ROLE_BWD_MMA << 24) | (L::B_QFULL << 16));
-            if (ok) {
-                tc_fence_after_sync();
-                issue_s(sbase + L::QB_OFF);
-                issue_dp(sbase + L::QB_OFF + L::TILE);
-            }
-            for (int it = 0; ok && it < n_q; ++it) {
-                const int b = it & 1;
-                const uint32_t ph = it & 1;
-                const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                const uint32_t dob = qb + L::TILE;
-                const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
-                const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
-                // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
-                // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
-                for (int c = 0; ok && c < 4; ++c) {
-                    if (!(ok = wait_bounded(bar(L::B_PRDY + c), ph, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | it)))
-                        break;
-                    tc_fence_after_sync();
-                    const uint32_t b0 = static_cast<uint32_t>(dob_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
-                    if (elect_one()) {
-                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
-                        umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
-                    }
-                    __syncwarp();
-                }
-                // dK += dS'^T Q likewise.
-                for (int c = 0; ok && c < 4; ++c) {
-                    if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | it)))
-                        break;
-                    tc_fence_after_sync();
-                    const uint32_t b0 = static_cast<uint32_t>(qb_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
-                    if (elect_one()) {
-                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
-                        umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
-                    }
-                    __syncwarp();
-                }
-                if (!ok) break;
-                commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
-                const bool has_next = it + 1 < n_q;
-                const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
-                if (has_next) {
-                    if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((it + 1) >> 1) & 1, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | it)))
-                        break;
-                    tc_fence_after_sync();
-                    issue_s(qn);
-                }
-                // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
-                // the dS^T buffer (MN-major A) and K MN-major.
+            uint32_t g = 0;  // query tiles (all units of the CTA)
+            bool ok = true;
+            for (int k = 0; ok && k < my_units; ++k) {
+                const int n_q = p.n_tiles - (p.causal ? bwd_unit<PERSIST>(k, p).kt : 0);
+                // The unit's first S^T and dP^T: its K and V loaded, its first Q and dO
+                // loaded, and (dP^T lies over dQ_part) the previous tile's dQ_part read.
                 {
-                    const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
-                                   kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
-                    const uint32_t hi = static_cast<uint32_t>(dsd >> 32);
-                    uint32_t av[BT / 16], bv[BT / 16];
-#pragma unroll
-                    for (int k = 0; k < BT / 16; ++k) {
-                        av[k] = static_cast<uint32_t>(dsd) + ((k * 2048) >> 4);
-                        bv[k] = static_cast<uint32_t>(kmd) + ((k * 2048) >> 4);
-                    }
-                    if (elect_one()) {
-                        umma_ss_steps<BT / 16>(tmem + L::T_DQ, av, hi, bv, hi, IDESC_MM, 0u);
-                        umma_commit(bar(L::B_GDONE));
-                    }
-                    __syncwarp();
-                }
-                if (has_next) {
-                    if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | it)))
+                    const uint32_t q0 = sbase + L::QB_OFF + (g & 1) * 2 * L::TILE;
+                    if (!(ok = wait_bounded(bar(L::B_KVFULL), k & 1, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16) | k) &&
+                               wait_bounded(bar(L::B_QFULL + (g & 1)), (g >> 1) & 1, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (g & 1)) << 16) | (g & 0xFFFF))))
                         break;
                     tc_fence_after_sync();
-                    issue_dp(qn + L::TILE);
+                    issue_s(q0);
+                    if (g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
+                                                     (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                        break;
+                    tc_fence_after_sync();
+                    issue_dp(q0 + L::TILE);
+                }
+                for (int it = 0; ok && it < n_q; ++it, ++g) {
+                    const int b = g & 1;
+                    const uint32_t ph = g & 1;
+                    const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                    const uint32_t dob = qb + L::TILE;
+                    const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
+                    const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
+                    // The unit's first dV and dK products start the accumulators
+                    // over: the previous unit's dK and dV must have left TMEM.
+                    if (it == 0 && k > 0 &&
+                        !(ok = wait_bounded(bar(L::B_DKVREAD), (k - 1) & 1, abort_flag,
+                                            (ROLE_BWD_MMA << 24) | (L::B_DKVREAD << 16) | k)))
+                        break;
+                    // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
+                    // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
+                    for (int c = 0; ok && c < 4; ++c) {
+                        if (!(ok = wait_bounded(bar(L::B_PRDY + c), ph, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        const uint32_t b0 = static_cast<uint32_t>(dob_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                        if (elect_one()) {
+                            umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                            umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                        }
+                        __syncwarp();
+                    }
+                    // dK += dS'^T Q likewise.
+                    for (int c = 0; ok && c < 4; ++c) {
+                        if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        const uint32_t b0 = static_cast<uint32_t>(qb_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                        if (elect_one()) {
+                            umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                            umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
+                    const bool has_next = it + 1 < n_q;
+                    const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
+                    if (has_next) {
+                        if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        issue_s(qn);
+                    }
+                    // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
+                    // the dS^T buffer (MN-major A) and K MN-major.
+                    {
+                        const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
+                                       kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
+                        const uint32_t hi = static_cast<uint32_t>(dsd >> 32);
+                        uint32_t av[BT / 16], bv[BT / 16];
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk) {
+                            av[kk] = static_cast<uint32_t>(dsd) + ((kk * 2048) >> 4);
+                            bv[kk] = static_cast<uint32_t>(kmd) + ((kk * 2048) >> 4);
+                        }
+                        if (elect_one()) {
+                            umma_ss_steps<BT / 16>(tmem + L::T_DQ, av, hi, bv, hi, IDESC_MM, 0u);
+                            umma_commit(bar(L::B_GDONE));
+                            if (!has_next) umma_commit(bar(L::B_KVFREE));  // the unit's K and V are no longer read
+                        }
+                        __syncwarp();
+                    }
+                    if (has_next) {
+                        if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        issue_dp(qn + L::TILE);
+                    }
                 }
             }
             commit(L::B_MMADONE);
@@ -397,23 +464,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         const int t = (warp % 4) * 32 + lane;  // TMEM lane: key row t of the key tile
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const float2 c2 = make_float2(p.scale_log2e, p.scale_log2e);
-        const int key = kt * BT + t;
         bool ok = true;
-        for (int it = 0; it < n_q; ++it) {
-            const int qt = qt_first + it;
-            const uint32_t ph = it & 1;
+        uint32_t g = 0;  // query tiles (all units of the CTA)
+        for (int k = 0; ok && k < my_units; ++k) {
+        const BwdUnit u = bwd_unit<PERSIST>(k, p);
+        const int n_q = p.n_tiles - (p.causal ? u.kt : 0);
+        const bool key_out = u.kt * BT + t >= p.N;  // this lane's key is past N
+        const bool ragged = u.kt * BT + BT > p.N;   // the key tile holds keys past N
+        for (int it = 0; it < n_q; ++it, ++g) {
+            const uint32_t ph = g & 1;
             // -LSE*log2(e) and -Delta of this group's 64 queries, loaded with
             // Q and dO (padded rows: -inf and 0, so their weights and
             // gradients are 0)
-            const float *rows = reinterpret_cast<const float *>(smem + L::RB_OFF + (it & 1) * 1024) + grp * 64;
+            const float *rows = reinterpret_cast<const float *>(smem + L::RB_OFF + (g & 1) * 1024) + grp * 64;
             const float4 *nl4 = reinterpret_cast<const float4 *>(rows);
             const float4 *dl4 = reinterpret_cast<const float4 *>(rows + 128);
-            // Only the causal diagonal tile and a ragged last key tile hold
-            // weights to zero: the queries below qmin do not see this key
-            // (keys past N are seen by none).
-            const bool diag = p.causal && qt == kt;
-            const bool masked = diag || kt * BT + BT > p.N;
-            const int qmin = key >= p.N ? BT : (diag ? key - qt * BT : 0);
+            // Only the causal diagonal tile (a unit's first query tile under
+            // the mask) and a ragged last key tile hold weights to zero: the
+            // queries below qmin do not see this key (keys past N are seen by
+            // none).
+            const bool diag = p.causal && it == 0;
+            const bool masked = diag || ragged;
+            const int qmin = key_out ? BT : (diag ? t : 0);
 
             // P^T = exp2(S^T c - LSE log2 e), bf16, 32 queries per chunk
             auto p_chunk = [&](const uint32_t(&sr)[32], int cc, uint32_t(&pp)[16], auto mask_tag) {
@@ -456,7 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             };
 
             if (!(ok = wait_bounded(bar(L::B_SFULL), ph, abort_flag,
-                                    (ROLE_BWD_COMPUTE << 24) | (L::B_SFULL << 16) | it)))
+                                    (ROLE_BWD_COMPUTE << 24) | (L::B_SFULL << 16) | (g & 0xFFFF))))
                 break;
             tc_fence_after_sync();
             {
@@ -477,7 +549,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             }
 
             if (!(ok = wait_bounded(bar(L::B_DPFULL), ph, abort_flag,
-                                    (ROLE_BWD_COMPUTE << 24) | (L::B_DPFULL << 16) | it)))
+                                    (ROLE_BWD_COMPUTE << 24) | (L::B_DPFULL << 16) | (g & 0xFFFF))))
                 break;
             tc_fence_after_sync();
 #pragma unroll
@@ -504,6 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             warp_arrive(bar(L::B_DSRDY + 2 * grp), lane);
             warp_arrive(bar(L::B_DSRDY + 2 * grp + 1), lane);
         }
+        }
     } else {
         // ------------------------------------------------ dQ warps
         const int t = (warp - WARP_DQ) * 32 + lane;  // TMEM lane: query row t (dQ_part), key row t (dK, dV)
@@ -511,83 +584,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         const bool issuer = warp == WARP_DQ && lane == 0;  // issues the bulk reductions (D = 64)
         int bulk_issued = 0;
         bool ok = true;
-        for (int it = 0; it < n_q; ++it) {
-            const int qt = qt_first + it;
-            if (!(ok = wait_bounded(bar(L::B_GDONE), it & 1, abort_flag,
-                                    (ROLE_BWD_COMPUTE << 24) | (L::B_GDONE << 16) | it)))
-                break;
-            tc_fence_after_sync();
-            if constexpr (L::DQ_BULK) {
-                // dQ_part into staging buffer it & 1 ([D/4][128 rows][4], the
-                // accumulator's layout), then one bulk reduction of the tile.
-                uint32_t r0[32], r1[32];
-                tmem_ld32_async(lane_base + L::T_DQ, r0);
-                tmem_ld32_async(lane_base + L::T_DQ + 32, r1);
-                tmem_ld_wait();
-                reg_fence(r0);
-                reg_fence(r1);
-                tc_fence_before_sync();
-                warp_arrive(bar(L::B_DQREAD), lane);
-                const int b = it & 1;
-                if (it >= 2 && !(ok = wait_bounded(bar(L::B_STAGEFREE + b), ((it >> 1) - 1) & 1, abort_flag,
-                                                   (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGEFREE + b) << 16) | it)))
+        uint32_t g = 0;  // query tiles (all units of the CTA)
+        for (int k = 0; ok && k < my_units; ++k) {
+            const BwdUnit u = bwd_unit<PERSIST>(k, p);
+            const int qt_first = p.causal ? u.kt : 0;
+            const int n_q = p.n_tiles - qt_first;
+            // the accumulator tile of the unit's first query tile
+            float *const dq_first = p.dq_acc + (static_cast<size_t>(u.bh) * p.n_tiles + qt_first) * BT * D;
+            for (int it = 0; it < n_q; ++it, ++g) {
+                if (!(ok = wait_bounded(bar(L::B_GDONE), g & 1, abort_flag,
+                                        (ROLE_BWD_COMPUTE << 24) | (L::B_GDONE << 16) | (g & 0xFFFF))))
                     break;
-                const uint32_t stage = sbase + L::DQST_OFF + b * L::DQST_BYTES + t * 16;
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    st_shared_v4(stage + g * BT * 16, r0[4 * g], r0[4 * g + 1], r0[4 * g + 2], r0[4 * g + 3]);
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    st_shared_v4(stage + (8 + g) * BT * 16, r1[4 * g], r1[4 * g + 1], r1[4 * g + 2], r1[4 * g + 3]);
-                fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk-copy unit
-                warp_arrive(bar(L::B_STAGED + b), lane);
-                if (issuer) {
-                    if ((ok = wait_bounded(bar(L::B_STAGED + b), (it >> 1) & 1, abort_flag,
-                                           (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGED + b) << 16) | it))) {
-                        bulk_reduce_add_f32(p.dq_acc + (head_tiles + qt) * BT * D,
-                                            sbase + L::DQST_OFF + b * L::DQST_BYTES, L::DQST_BYTES);
-                        tma_store_commit();
-                        ++bulk_issued;
-                        if (it >= 1) {
-                            // the previous tile's reduction has read its buffer
-                            bulk_wait_read_all_but_one();
-                            mbar_arrive(bar(L::B_STAGEFREE + (b ^ 1)));
-                        }
-                    }
-                }
-                __syncwarp();
-                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the issuer's verdict holds for its warp
-                if (!ok) break;
-            } else {
-                // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
-                // reduction of one 4-column group covers 512 contiguous bytes.
-                float *dq_tile = p.dq_acc + (head_tiles + qt) * BT * D + t * 4;
-#pragma unroll
-                for (int h = 0; h < D / 32; ++h) {
-                    uint32_t r0[32];
-                    tmem_ld32_async(lane_base + L::T_DQ + 32 * h, r0);
+                tc_fence_after_sync();
+                if constexpr (L::DQ_BULK) {
+                    // dQ_part into staging buffer g & 1 ([D/4][128 rows][4], the
+                    // accumulator's layout), then one bulk reduction of the tile.
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32_async(lane_base + L::T_DQ, r0);
+                    tmem_ld32_async(lane_base + L::T_DQ + 32, r1);
                     tmem_ld_wait();
                     reg_fence(r0);
-                    if (h == D / 32 - 1) {
-                        tc_fence_before_sync();
-                        warp_arrive(bar(L::B_DQREAD), lane);
-                    }
+                    reg_fence(r1);
+                    tc_fence_before_sync();
+                    warp_arrive(bar(L::B_DQREAD), lane);
+                    const int b = g & 1;
+                    if (g >= 2 && !(ok = wait_bounded(bar(L::B_STAGEFREE + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                      (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGEFREE + b) << 16) |
+                                                          (g & 0xFFFF))))
+                        break;
+                    const uint32_t stage = sbase + L::DQST_OFF + b * L::DQST_BYTES + t * 16;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        red_add_v4(dq_tile + (8 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
-                                   r0[4 * j + 3]);
+                        st_shared_v4(stage + j * BT * 16, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stage + (8 + j) * BT * 16, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2], r1[4 * j + 3]);
+                    fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk-copy unit
+                    warp_arrive(bar(L::B_STAGED + b), lane);
+                    if (issuer) {
+                        if ((ok = wait_bounded(bar(L::B_STAGED + b), (g >> 1) & 1, abort_flag,
+                                               (ROLE_BWD_COMPUTE << 24) | ((L::B_STAGED + b) << 16) | (g & 0xFFFF)))) {
+                            bulk_reduce_add_f32(dq_first + static_cast<size_t>(it) * BT * D,
+                                                sbase + L::DQST_OFF + b * L::DQST_BYTES, L::DQST_BYTES);
+                            tma_store_commit();
+                            ++bulk_issued;
+                            if (g >= 1) {
+                                // the previous tile's reduction has read its buffer
+                                bulk_wait_read_all_but_one();
+                                mbar_arrive(bar(L::B_STAGEFREE + (b ^ 1)));
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the issuer's verdict holds for its warp
+                    if (!ok) break;
+                } else {
+                    // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
+                    // reduction of one 4-column group covers 512 contiguous bytes.
+                    float *dq_tile = dq_first + static_cast<size_t>(it) * BT * D + t * 4;
+#pragma unroll
+                    for (int h = 0; h < D / 32; ++h) {
+                        uint32_t r0[32];
+                        tmem_ld32_async(lane_base + L::T_DQ + 32 * h, r0);
+                        tmem_ld_wait();
+                        reg_fence(r0);
+                        if (h == D / 32 - 1) {
+                            tc_fence_before_sync();
+                            warp_arrive(bar(L::B_DQREAD), lane);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            red_add_v4(dq_tile + (8 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
+                                       r0[4 * j + 3]);
+                    }
                 }
             }
-        }
-        // The bulk reductions complete before the CTA (and its shared memory) goes away.
-        if (issuer && bulk_issued > 0) tma_store_wait_all();
-        __syncwarp();
-        if (ok) {
-            // dK = scale * (dS'^T Q), dV of this key tile (lane t = key).
-            // The last GDONE wait covers every product.
-            const int key = kt * BT + t;
+            if (!ok) break;
+            // dK = scale * (dS'^T Q), dV of this key tile (lane t = key).  The
+            // unit's last GDONE wait covers every product; once both are read
+            // the next unit's products may start them over.
+            const int key = u.kt * BT + t;
             const bool valid_key = key < p.N;
             const float scale = p.scale;
+            const size_t head_rows = static_cast<size_t>(u.bh) * p.N;
             // rows of the tensors' head dim p.D (32 and 96 run on the 64- and
             // 128-column kernel: the columns past p.D are not stored)
             __nv_bfloat16 *dkrow = static_cast<__nv_bfloat16 *>(p.dK) + (head_rows + (valid_key ? key : 0)) * p.D;
@@ -601,6 +680,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 // every lane takes part in the TMEM loads; only the stores are guarded
                 uint32_t r[32];
                 tmem_ld32(lane_base + (is_v ? L::T_DV : L::T_DK) + c * 32, r);
+                if (q == 2 * (D / 32) - 1) {
+                    tc_fence_before_sync();
+                    warp_arrive(bar(L::B_DKVREAD), lane);
+                }
                 if (valid_key && c * 32 < p.D) {
                     uint32_t pk[16];
 #pragma unroll
@@ -613,6 +696,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
             }
         }
+        // The bulk reductions complete before the CTA (and its shared memory) goes away.
+        if (issuer && bulk_issued > 0) tma_store_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -706,8 +792,10 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        err = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
-        if (err != cudaSuccess) return err;
+        for (auto kern : {attn_bwd_kernel<D, true>, attn_bwd_kernel<D, false>}) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+            if (err != cudaSuccess) return err;
+        }
         configured_device = dev;
     }
     const int64_t padded_rows = static_cast<int64_t>(p.BH) * p.n_tiles * BT;
@@ -718,8 +806,10 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         p.neg_lse2, p.dq_acc, padded_rows, p.N, p.D, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
-    // Causal: groups of L heads, L the largest divisor of B*H up to about
-    // three waves of blocks; the grid's z extent stays within its limit.
+    // Without the mask: a persistent grid, at most one CTA per SM, each taking
+    // units round-robin.  Causal: one block per unit, in groups of L heads, L
+    // the largest divisor of B*H up to about three waves of blocks; the grid's
+    // z extent stays within its limit.
     int64_t group = 1;
     if (p.causal) {
         const int64_t want = (3 * static_cast<int64_t>(num_sms) + p.n_tiles - 1) / p.n_tiles;
@@ -733,12 +823,16 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         for (++group; p.BH % group != 0; ++group) {
         }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(group), static_cast<unsigned>(p.n_tiles),
-                       static_cast<unsigned>(p.BH / group));
+    const int64_t units = static_cast<int64_t>(p.BH) * p.n_tiles;
+    cfg.gridDim = p.causal ? dim3(static_cast<unsigned>(group), static_cast<unsigned>(p.n_tiles),
+                                  static_cast<unsigned>(p.BH / group))
+                           : dim3(static_cast<unsigned>(units < num_sms ? units : num_sms), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM_ALLOC;
     cfg.stream = stream;
-    if ((err = cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D>, p)) != cudaSuccess) return err;
+    err = p.causal ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D, false>, p)
+                   : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D, true>, p);
+    if (err != cudaSuccess) return err;
 
     bwd_dq_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.n_tiles), 256, 0, stream>>>(
         p.dq_acc, static_cast<__nv_bfloat16 *>(p.dQ), p.N, p.D, p.n_tiles, p.scale);
