@@ -86,6 +86,32 @@ def test_bwd_invariants_and_determinism():
     assert (dq.double() - dq2.double()).abs().max().item() <= 1e-2
 
 
+@pytest.mark.parametrize("D", [32, 64, 96, 128])
+def test_bwd_persistent_units(oracle_mod, D):
+    """Without the mask the grid is persistent: B2 H40 N1000 has 80 heads x 8
+    key tiles = 640 units, about four per CTA on 152 SMs, so every CTA runs
+    several units in a row (the next unit's Q and dO loading while the last
+    one finishes, K and V reloaded, dK and dV reused).  The first, a middle
+    and the last head against the oracle's backward; dK and dV bitwise the
+    same in a second launch."""
+    B, H, N = 2, 40, 1000
+    q, k, v = make_qkv(B, H, N, D, 9600 + D)
+    do = make_qkv(B, H, N, D, 9601 + D)[0]
+    scale = 1.0 / math.sqrt(D)
+    got = _run(q, k, v, do, False, scale)
+    for b, h in [(0, 0), (1, 7), (1, H - 1)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle_mod.attn_bwd(q[sl].contiguous(), k[sl].contiguous(), v[sl].contiguous(),
+                                  do[sl].contiguous(), False, scale)
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            g = g[sl].double().numpy()
+            err = np.abs(g - r)
+            assert err.max() <= 0.02 * np.abs(r).max() + 1e-4, (D, b, h, name, err.max())
+            assert err.mean() <= 0.01 * np.abs(r).mean() + 1e-5, (D, b, h, name, err.mean())
+    again = _run(q, k, v, do, False, scale)
+    assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2])
+
+
 @pytest.mark.parametrize("idx,heads", [(4, [(0, 0), (15, 31)]), (3, [(3, 15)])])
 def test_bwd_bench_workload_sampled(oracle_mod, idx, heads):
     """The benchmark's backward launches at full size (B16 H32 N1024 D128 wide
