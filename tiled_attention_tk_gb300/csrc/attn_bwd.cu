@@ -153,32 +153,75 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
 
 __device__ __forceinline__ uint32_t pack2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
-// Work units: key tile kt of head bh.  Without the mask every unit costs the
-// same and the grid is persistent (at most one CTA per SM): CTA c takes the
-// head-major units c, c + grid, ..., so the CTAs running together hold a few
-// heads' key tiles and share their Q and dO through L2, and a CTA's next unit
-// loads while its last one finishes.  Under the mask key tile kt sees n_tiles
-// - kt query tiles: the grid is (L, n_tiles, B*H / L), one unit per block,
-// and blocks start roughly in launch order (x fastest), so heads run in
-// groups of L whose key tiles launch tile by tile across the group, heaviest
-// first, and the SMs take the next block as they free (which balances unequal
-// units better than a fixed assignment).
+// Work units: key tile kt of head bh.  The grid is persistent (at most one
+// CTA per SM), and a CTA starts its next unit while its last one finishes.
+// Without the mask every unit costs the same: CTA c takes the head-major
+// units c, c + grid, ..., so the CTAs running together hold a few heads' key
+// tiles and share their Q and dO through L2.  Under the mask key tile kt sees
+// n_tiles - kt query tiles; see bwd_sched.
 struct BwdUnit {
     int kt, bh;
 };
 
-template <bool PERSIST>
-__device__ __forceinline__ int bwd_units_of_cta(const BwdParams &p) {
-    if (!PERSIST) return 1;
-    const int total = p.BH * p.n_tiles, grid = gridDim.x;
-    return (total - static_cast<int>(blockIdx.x) + grid - 1) / grid;
+__device__ __forceinline__ int bwd_slot_index(int round, int cta, int grid) {
+    return round * grid + ((round & 1) ? grid - 1 - cta : cta);
 }
 
-template <bool PERSIST>
+// The schedule under the mask: slots, one per CTA per round, odd rounds in
+// reverse CTA order (snake).  The first heads run their key tiles in mirrored
+// pairs (key tile i, which sees n_tiles - i query tiles, then key tile
+// n_tiles-1-i, which sees i + 1: n_tiles + 1 together, whatever i is), head by
+// head, so these slots are balanced as they come and the CTAs running together
+// share a few heads' Q and dO; the heads left once fewer than two rounds of
+// pairs would remain run one key tile per slot, heaviest first, which evens
+// out the last rounds.  Odd tile counts run that way throughout.
+struct BwdSched {
+    int heads_paired, pair_slots, slots;
+};
+
+__device__ __forceinline__ BwdSched bwd_sched(const BwdParams &p) {
+    BwdSched s{0, 0, p.BH * p.n_tiles};
+    if (p.causal && p.n_tiles % 2 == 0) {
+        const int hp = p.n_tiles / 2;
+        s.heads_paired = max(0, (p.BH * hp - 2 * static_cast<int>(gridDim.x)) / hp);
+        s.pair_slots = s.heads_paired * hp;
+        s.slots = s.pair_slots + (p.BH - s.heads_paired) * p.n_tiles;
+    }
+    return s;
+}
+
+// Units this CTA runs (two per slot of a mirrored pair).
+__device__ __forceinline__ int bwd_units_of_cta(const BwdParams &p) {
+    const int grid = gridDim.x;
+    if (!p.causal) {
+        const int total = p.BH * p.n_tiles;
+        return (total - static_cast<int>(blockIdx.x) + grid - 1) / grid;
+    }
+    const BwdSched s = bwd_sched(p);
+    const int rounds = (s.slots + grid - 1) / grid;
+    const int r0 = s.pair_slots / grid;
+    const int pair_rounds = r0 + (bwd_slot_index(r0, blockIdx.x, grid) < s.pair_slots ? 1 : 0);
+    return rounds - (bwd_slot_index(rounds - 1, blockIdx.x, grid) >= s.slots ? 1 : 0) + pair_rounds;
+}
+
+// The k-th unit of this CTA (k < bwd_units_of_cta).
 __device__ __forceinline__ BwdUnit bwd_unit(int k, const BwdParams &p) {
-    if (!PERSIST) return {static_cast<int>(blockIdx.y), static_cast<int>(blockIdx.z * gridDim.x + blockIdx.x)};
-    const int idx = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-    return {idx % p.n_tiles, idx / p.n_tiles};
+    const int grid = gridDim.x;
+    if (!p.causal) {
+        const int idx = static_cast<int>(blockIdx.x) + k * grid;
+        return {idx % p.n_tiles, idx / p.n_tiles};
+    }
+    const BwdSched s = bwd_sched(p);
+    const int r0 = s.pair_slots / grid;
+    const int pair_rounds = r0 + (bwd_slot_index(r0, blockIdx.x, grid) < s.pair_slots ? 1 : 0);
+    const int idx = k < 2 * pair_rounds ? bwd_slot_index(k >> 1, blockIdx.x, grid)
+                                        : bwd_slot_index(k - pair_rounds, blockIdx.x, grid);
+    if (idx < s.pair_slots) {
+        const int hp = p.n_tiles / 2, i = idx % hp;
+        return {(k < 2 * pair_rounds && (k & 1)) ? p.n_tiles - 1 - i : i, idx / hp};
+    }
+    const int j = idx - s.pair_slots, left = p.BH - s.heads_paired;
+    return {j / left, s.heads_paired + j % left};
 }
 
 // Keys sit on the TMEM lanes: the MMA warp forms S^T = K Q^T and
@@ -194,9 +237,7 @@ __device__ __forceinline__ BwdUnit bwd_unit(int k, const BwdParams &p) {
 //
 // The unscaled dS' = P (dP - Delta) is what the products see; dK and dQ are
 // multiplied by `scale` when they are rounded to bf16.
-// PERSIST is !p.causal: each launch shape has its own instantiation (the
-// one-unit blocks of the causal grid then carry no unit loop).
-template <int D, bool PERSIST>
+template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = Layout<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -212,7 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int my_units = bwd_units_of_cta<PERSIST>(p);
+    const int my_units = bwd_units_of_cta(p);
 
     if (warp == WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -266,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 ++kv_loads;
             };
             for (int k = 0; ok && k < my_units; ++k) {
-                const BwdUnit u = bwd_unit<PERSIST>(k, p);
+                const BwdUnit u = bwd_unit(k, p);
                 const int qt_first = p.causal ? u.kt : 0;
                 const int n_q = p.n_tiles - qt_first;
                 const size_t head_tiles = static_cast<size_t>(u.bh) * p.n_tiles;
@@ -354,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             uint32_t g = 0;  // query tiles (all units of the CTA)
             bool ok = true;
             for (int k = 0; ok && k < my_units; ++k) {
-                const int n_q = p.n_tiles - (p.causal ? bwd_unit<PERSIST>(k, p).kt : 0);
+                const int n_q = p.n_tiles - (p.causal ? bwd_unit(k, p).kt : 0);
                 // The unit's first S^T and dP^T: its K and V loaded, its first Q and dO
                 // loaded, and (dP^T lies over dQ_part) the previous tile's dQ_part read.
                 {
@@ -467,7 +508,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         bool ok = true;
         uint32_t g = 0;  // query tiles (all units of the CTA)
         for (int k = 0; ok && k < my_units; ++k) {
-        const BwdUnit u = bwd_unit<PERSIST>(k, p);
+        const BwdUnit u = bwd_unit(k, p);
         const int n_q = p.n_tiles - (p.causal ? u.kt : 0);
         const bool key_out = u.kt * BT + t >= p.N;  // this lane's key is past N
         const bool ragged = u.kt * BT + BT > p.N;   // the key tile holds keys past N
@@ -586,7 +627,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         bool ok = true;
         uint32_t g = 0;  // query tiles (all units of the CTA)
         for (int k = 0; ok && k < my_units; ++k) {
-            const BwdUnit u = bwd_unit<PERSIST>(k, p);
+            const BwdUnit u = bwd_unit(k, p);
             const int qt_first = p.causal ? u.kt : 0;
             const int n_q = p.n_tiles - qt_first;
             // the accumulator tile of the unit's first query tile
@@ -792,10 +833,8 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
-        for (auto kern : {attn_bwd_kernel<D, true>, attn_bwd_kernel<D, false>}) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
-            if (err != cudaSuccess) return err;
-        }
+        err = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+        if (err != cudaSuccess) return err;
         configured_device = dev;
     }
     const int64_t padded_rows = static_cast<int64_t>(p.BH) * p.n_tiles * BT;
@@ -806,32 +845,14 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
         p.neg_lse2, p.dq_acc, padded_rows, p.N, p.D, p.n_tiles, acc_vec4);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
-    // Without the mask: a persistent grid, at most one CTA per SM, each taking
-    // units round-robin.  Causal: one block per unit, in groups of L heads, L
-    // the largest divisor of B*H up to about three waves of blocks; the grid's
-    // z extent stays within its limit.
-    int64_t group = 1;
-    if (p.causal) {
-        const int64_t want = (3 * static_cast<int64_t>(num_sms) + p.n_tiles - 1) / p.n_tiles;
-        for (int64_t l = want < p.BH ? want : p.BH; l >= 1; --l)
-            if (p.BH % l == 0) {
-                group = l;
-                break;
-            }
-    }
-    while (p.BH / group > 65535)  // a divisor of B*H that keeps z in range (B*H itself at worst)
-        for (++group; p.BH % group != 0; ++group) {
-        }
-    cudaLaunchConfig_t cfg = {};
+    // A persistent grid: at most one CTA per SM (the units' order is the kernel's).
     const int64_t units = static_cast<int64_t>(p.BH) * p.n_tiles;
-    cfg.gridDim = p.causal ? dim3(static_cast<unsigned>(group), static_cast<unsigned>(p.n_tiles),
-                                  static_cast<unsigned>(p.BH / group))
-                           : dim3(static_cast<unsigned>(units < num_sms ? units : num_sms), 1, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units < num_sms ? units : num_sms), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM_ALLOC;
     cfg.stream = stream;
-    err = p.causal ? cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D, false>, p)
-                   : cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D, true>, p);
+    err = cudaLaunchKernelEx(&cfg, attn_bwd_kernel<D>, p);
     if (err != cudaSuccess) return err;
 
     bwd_dq_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(p.BH) * p.n_tiles), 256, 0, stream>>>(
