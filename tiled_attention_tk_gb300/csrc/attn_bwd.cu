@@ -683,21 +683,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
                     // reduction of one 4-column group covers 512 contiguous bytes.
                     float *dq_tile = dq_first + static_cast<size_t>(it) * BT * D + t * 4;
-#pragma unroll
-                    for (int h = 0; h < D / 32; ++h) {
-                        uint32_t r0[32];
-                        tmem_ld32_async(lane_base + L::T_DQ + 32 * h, r0);
-                        tmem_ld_wait();
-                        reg_fence(r0);
-                        if (h == D / 32 - 1) {
-                            tc_fence_before_sync();
-                            warp_arrive(bar(L::B_DQREAD), lane);
-                        }
+                    static_assert(D == 128, "the vector-reduction path runs at D = 128");
+                    auto red_chunk = [&](int h, uint32_t(&r)[32]) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            red_add_v4(dq_tile + (8 * h + j) * BT * 4, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2],
-                                       r0[4 * j + 3]);
-                    }
+                            red_add_v4(dq_tile + (8 * h + j) * BT * 4, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    };
+                    // The next dP^T waits for dQ_part to leave TMEM: two 32-column
+                    // blocks are read before the first reductions and each later
+                    // read is issued while the block before it is reduced, so only
+                    // 16 of the 32 reductions queue ahead of the release.
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_async(lane_base + L::T_DQ, ra);
+                    tmem_ld32_async(lane_base + L::T_DQ + 32, rb);
+                    tmem_ld_wait();
+                    reg_fence(ra);
+                    reg_fence(rb);
+                    red_chunk(0, ra);
+                    tmem_ld32_async(lane_base + L::T_DQ + 64, ra);
+                    red_chunk(1, rb);
+                    tmem_ld32_async(lane_base + L::T_DQ + 96, rb);
+                    tmem_ld_wait();
+                    reg_fence(ra);
+                    reg_fence(rb);
+                    tc_fence_before_sync();
+                    warp_arrive(bar(L::B_DQREAD), lane);
+                    red_chunk(2, ra);
+                    red_chunk(3, rb);
                 }
             }
             if (!ok) break;
