@@ -520,6 +520,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             const float *rows = reinterpret_cast<const float *>(smem + L::RB_OFF + (g & 1) * 1024) + grp * 64;
             const float4 *nl4 = reinterpret_cast<const float4 *>(rows);
             const float4 *dl4 = reinterpret_cast<const float4 *>(rows + 128);
+            // At D = 64 the row values are requested before the TMEM loads they
+            // go with (and both chunks of S^T at once), so their shared-memory
+            // latency overlaps the TMEM latency; at D = 128 this measured no
+            // faster and the values are read where they are used.
+            constexpr bool kEarlyRows = D == 64;
             // Only the causal diagonal tile (a unit's first query tile under
             // the mask) and a ragged last key tile hold weights to zero: the
             // queries below qmin do not see this key (keys past N are seen by
@@ -529,11 +534,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             const int qmin = key_out ? BT : (diag ? t : 0);
 
             // P^T = exp2(S^T c - LSE log2 e), bf16, 32 queries per chunk
-            auto p_chunk = [&](const uint32_t(&sr)[32], int cc, uint32_t(&pp)[16], auto mask_tag) {
+            // The row values of a chunk come from `lv`: shared memory, or (see
+            // kEarlyRows) registers loaded before the chunk's TMEM load.
+            auto p_chunk = [&](const uint32_t(&sr)[32], const float4 *lv, int cc, uint32_t(&pp)[16],
+                               auto mask_tag) {
                 const int q0 = (2 * grp + cc) * 32;
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 l4 = nl4[cc * 8 + e4];
+                    const float4 l4 = lv[e4];
                     float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * e4]), __uint_as_float(sr[4 * e4 + 1])),
                                            c2, make_float2(l4.x, l4.y));
                     float2 x1 = __ffma2_rn(
@@ -553,10 +561,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
             };
             // dS' = P (dP - Delta), bf16
-            auto ds_chunk = [&](const uint32_t(&dr)[32], const uint32_t(&pr)[16], int cc, uint32_t(&ds)[16]) {
+            auto ds_chunk = [&](const uint32_t(&dr)[32], const uint32_t(&pr)[16], const float4 *dv,
+                                uint32_t(&ds)[16]) {
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 d4 = dl4[cc * 8 + e4];
+                    const float4 d4 = dv[e4];
                     const float2 g0 = __fadd2_rn(
                         make_float2(__uint_as_float(dr[4 * e4]), __uint_as_float(dr[4 * e4 + 1])),
                         make_float2(d4.x, d4.y));
@@ -575,13 +584,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             {
                 const int ca = 2 * grp, cb = 2 * grp + 1;
                 uint32_t sr[32], pp[16];
-                tmem_ld32(lane_base + L::T_S + ca * 32, sr);
-                if (masked) p_chunk(sr, 0, pp, std::true_type());
-                else p_chunk(sr, 0, pp, std::false_type());
-                tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
-                tmem_ld32(lane_base + L::T_S + cb * 32, sr);
-                if (masked) p_chunk(sr, 1, pp, std::true_type());
-                else p_chunk(sr, 1, pp, std::false_type());
+                if constexpr (kEarlyRows) {
+                    // both chunks of S^T and the first chunk's row values at once
+                    uint32_t sr2[32];
+                    float4 lv[8];
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) lv[e4] = nl4[e4];
+                    tmem_ld32_async(lane_base + L::T_S + ca * 32, sr);
+                    tmem_ld32_async(lane_base + L::T_S + cb * 32, sr2);
+                    tmem_ld_wait();
+                    reg_fence(sr);
+                    reg_fence(sr2);
+                    if (masked) p_chunk(sr, lv, 0, pp, std::true_type());
+                    else p_chunk(sr, lv, 0, pp, std::false_type());
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) lv[e4] = nl4[8 + e4];
+                    tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
+                    if (masked) p_chunk(sr2, lv, 1, pp, std::true_type());
+                    else p_chunk(sr2, lv, 1, pp, std::false_type());
+                } else {
+                    tmem_ld32(lane_base + L::T_S + ca * 32, sr);
+                    if (masked) p_chunk(sr, nl4, 0, pp, std::true_type());
+                    else p_chunk(sr, nl4, 0, pp, std::false_type());
+                    tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
+                    tmem_ld32(lane_base + L::T_S + cb * 32, sr);
+                    if (masked) p_chunk(sr, nl4 + 8, 1, pp, std::true_type());
+                    else p_chunk(sr, nl4 + 8, 1, pp, std::false_type());
+                }
                 tmem_st16(lane_base + L::T_S + L::pcol(cb), pp);
                 tmem_st_wait();
                 tc_fence_before_sync();
@@ -597,12 +626,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
             for (int cc = 0; cc < 2; ++cc) {
                 const int ch = 2 * grp + cc;
                 uint32_t dr[32], pr[16], ds[16];
+                float4 dv[8];
+                if constexpr (kEarlyRows) {
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) dv[e4] = dl4[cc * 8 + e4];
+                }
                 tmem_ld32_async(lane_base + L::T_DP + ch * 32, dr);
                 tmem_ld16_async(lane_base + L::T_S + L::pcol(ch), pr);
                 tmem_ld_wait();
                 reg_fence(dr);
                 reg_fence(pr);
-                ds_chunk(dr, pr, cc, ds);
+                ds_chunk(dr, pr, kEarlyRows ? dv : dl4 + cc * 8, ds);
                 tmem_st16(lane_base + L::T_DP + L::pcol(ch), ds);
                 // dS'^T row t (key), queries ch*32 .. ch*32+31 = pieces 4cc.. of box grp
                 const uint32_t dbox = sbase + L::DS_OFF + grp * L::BOX;
