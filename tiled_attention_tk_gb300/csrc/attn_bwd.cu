@@ -355,10 +355,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------ MMA issuer
-        // Per query tile i: dV(i) and dK(i) chunk by chunk, S^T(i+1),
-        // dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.  Each
-        // product that overwrites TMEM columns an earlier product reads (S^T
-        // over P^T, dQ_part over dS^T) is issued after it; the tensor core
+        // Per query tile i: dV(i) chunk by chunk, S^T(i+1), dK(i) chunk by
+        // chunk, dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.
+        // Each product that overwrites TMEM columns an earlier product reads
+        // (S^T over P^T, dQ_part over dS^T) is issued after it; the tensor core
         // runs one thread's products in issue order.  The whole warp runs
         // the loop (operands stay warp-uniform); one elected lane sends each
         // block of products and each commit.
@@ -440,6 +440,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                         }
                         __syncwarp();
                     }
+                    if (!ok) break;
+                    // S^T of the next query tile over P^T: the dV products above
+                    // were the last to read P^T (the compute warps keep their own
+                    // copy for dS^T), so the next P^T pass can start as soon as
+                    // this tile's dS^T pass ends.
+                    const bool has_next = it + 1 < n_q;
+                    const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
+                    if (has_next) {
+                        if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        issue_s(qn);
+                    }
                     // dK += dS'^T Q likewise.
                     for (int c = 0; ok && c < 4; ++c) {
                         if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
@@ -455,15 +469,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     }
                     if (!ok) break;
                     commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
-                    const bool has_next = it + 1 < n_q;
-                    const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
-                    if (has_next) {
-                        if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
-                                                (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
-                            break;
-                        tc_fence_after_sync();
-                        issue_s(qn);
-                    }
                     // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
                     // the dS^T buffer (MN-major A) and K MN-major.
                     {
@@ -581,9 +586,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                                     (ROLE_BWD_COMPUTE << 24) | (L::B_SFULL << 16) | (g & 0xFFFF))))
                 break;
             tc_fence_after_sync();
+            // This group's two chunks of bf16 P^T, kept for dS^T (the next S^T
+            // overwrites them in TMEM once the dV products have read them).
+            uint32_t ppa[16], ppb[16];
             {
                 const int ca = 2 * grp, cb = 2 * grp + 1;
-                uint32_t sr[32], pp[16];
+                uint32_t sr[32];
                 if constexpr (kEarlyRows) {
                     // both chunks of S^T and the first chunk's row values at once
                     uint32_t sr2[32];
@@ -595,23 +603,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     tmem_ld_wait();
                     reg_fence(sr);
                     reg_fence(sr2);
-                    if (masked) p_chunk(sr, lv, 0, pp, std::true_type());
-                    else p_chunk(sr, lv, 0, pp, std::false_type());
+                    if (masked) p_chunk(sr, lv, 0, ppa, std::true_type());
+                    else p_chunk(sr, lv, 0, ppa, std::false_type());
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) lv[e4] = nl4[8 + e4];
-                    tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
-                    if (masked) p_chunk(sr2, lv, 1, pp, std::true_type());
-                    else p_chunk(sr2, lv, 1, pp, std::false_type());
+                    tmem_st16(lane_base + L::T_S + L::pcol(ca), ppa);
+                    if (masked) p_chunk(sr2, lv, 1, ppb, std::true_type());
+                    else p_chunk(sr2, lv, 1, ppb, std::false_type());
                 } else {
                     tmem_ld32(lane_base + L::T_S + ca * 32, sr);
-                    if (masked) p_chunk(sr, nl4, 0, pp, std::true_type());
-                    else p_chunk(sr, nl4, 0, pp, std::false_type());
-                    tmem_st16(lane_base + L::T_S + L::pcol(ca), pp);
+                    if (masked) p_chunk(sr, nl4, 0, ppa, std::true_type());
+                    else p_chunk(sr, nl4, 0, ppa, std::false_type());
+                    tmem_st16(lane_base + L::T_S + L::pcol(ca), ppa);
                     tmem_ld32(lane_base + L::T_S + cb * 32, sr);
-                    if (masked) p_chunk(sr, nl4 + 8, 1, pp, std::true_type());
-                    else p_chunk(sr, nl4 + 8, 1, pp, std::false_type());
+                    if (masked) p_chunk(sr, nl4 + 8, 1, ppb, std::true_type());
+                    else p_chunk(sr, nl4 + 8, 1, ppb, std::false_type());
                 }
-                tmem_st16(lane_base + L::T_S + L::pcol(cb), pp);
+                tmem_st16(lane_base + L::T_S + L::pcol(cb), ppb);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 warp_arrive(bar(L::B_PRDY + ca), lane);
@@ -625,17 +633,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int ch = 2 * grp + cc;
-                uint32_t dr[32], pr[16], ds[16];
+                uint32_t dr[32], ds[16];
+                const uint32_t(&pr)[16] = cc == 0 ? ppa : ppb;
                 float4 dv[8];
                 if constexpr (kEarlyRows) {
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) dv[e4] = dl4[cc * 8 + e4];
                 }
                 tmem_ld32_async(lane_base + L::T_DP + ch * 32, dr);
-                tmem_ld16_async(lane_base + L::T_S + L::pcol(ch), pr);
                 tmem_ld_wait();
                 reg_fence(dr);
-                reg_fence(pr);
                 ds_chunk(dr, pr, kEarlyRows ? dv : dl4 + cc * 8, ds);
                 tmem_st16(lane_base + L::T_DP + L::pcol(ch), ds);
                 // dS'^T row t (key), queries ch*32 .. ch*32+31 = pieces 4cc.. of box grp
