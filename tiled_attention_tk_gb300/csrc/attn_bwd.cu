@@ -54,11 +54,21 @@ namespace tk {
 namespace bwd {
 
 constexpr int BT = 128;             // rows per query tile and per key tile
-constexpr int NUM_THREADS = 448;    // 8 compute warps, 4 dQ warps, TMA warp, MMA warp
+constexpr int NUM_THREADS = 512;    // 8 compute warps, 4 dQ warps, TMA warp, MMA warp, 2 set-up warps
 constexpr int WARP_DQ = 8;          // first of the four dQ warps
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
 constexpr uint32_t TMEM_COLS = 512;
+// Registers per thread and warpgroup: the compute warpgroups keep the launch
+// budget, the dQ warpgroup takes what the control warpgroup (TMA, MMA and two
+// set-up warps) gives up, so that it can hold a whole dQ_part row (128 fp32)
+// before its reductions.  The shares add up to the launch budget (checked on
+// the host against the compiled kernel), else the growing warpgroup would wait.
+constexpr int LAUNCH_REGS = 128;
+constexpr uint32_t REGS_DQ = 168;
+constexpr uint32_t REGS_CTRL = 88;
+static_assert(2 * LAUNCH_REGS + REGS_DQ + REGS_CTRL == 4 * LAUNCH_REGS, "register split = launch budget");
+static_assert(NUM_THREADS == 512, "four whole warpgroups");
 
 template <int D>
 struct Layout {
@@ -288,222 +298,225 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_TMA) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.tmQ);
-            tma_prefetch_desc(&p.tmK);
-            tma_prefetch_desc(&p.tmV);
-            tma_prefetch_desc(&p.tmDO);
-            uint32_t g = 0;          // query tiles loaded (all units of the CTA)
-            uint32_t kv_loads = 0;   // units whose K and V were loaded
-            bool ok = true;
-            auto load_kv = [&](const BwdUnit &u) {
-                mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
-                for (int c = 0; c < L::KATOMS; ++c) {
-                    tma_load_3d(sbase + L::K_OFF + c * L::BOX, &p.tmK, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
-                    tma_load_3d(sbase + L::V_OFF + c * L::BOX, &p.tmV, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
-                }
-                ++kv_loads;
-            };
-            for (int k = 0; ok && k < my_units; ++k) {
-                const BwdUnit u = bwd_unit(k, p);
-                const int qt_first = p.causal ? u.kt : 0;
-                const int n_q = p.n_tiles - qt_first;
-                const size_t head_tiles = static_cast<size_t>(u.bh) * p.n_tiles;
-                if (k == 0) load_kv(u);  // the first unit's K and V lead
-                for (int it = 0; it < n_q; ++it) {
-                    const int b = g & 1;
-                    // Buffer b was last used by query tile g-2.
-                    if (g >= 2 && !(ok = wait_bounded(bar(L::B_QEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
-                                                      (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | (g & 0xFFFF))))
-                        break;
-                    const int qt = qt_first + it;
-                    const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                    const uint32_t rb = sbase + L::RB_OFF + b * 1024;
-                    const size_t row0 = (head_tiles + qt) * BT;
-                    mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
+    if (warp >= WARP_TMA) {
+        regs_dealloc<REGS_CTRL>();
+        if (warp == WARP_TMA) {
+            // ------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tmQ);
+                tma_prefetch_desc(&p.tmK);
+                tma_prefetch_desc(&p.tmV);
+                tma_prefetch_desc(&p.tmDO);
+                uint32_t g = 0;          // query tiles loaded (all units of the CTA)
+                uint32_t kv_loads = 0;   // units whose K and V were loaded
+                bool ok = true;
+                auto load_kv = [&](const BwdUnit &u) {
+                    mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
                     for (int c = 0; c < L::KATOMS; ++c) {
-                        tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
-                        tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                        tma_load_3d(sbase + L::K_OFF + c * L::BOX, &p.tmK, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
+                        tma_load_3d(sbase + L::V_OFF + c * L::BOX, &p.tmV, bar(L::B_KVFULL), c * 64, u.kt * BT, u.bh);
                     }
-                    bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
-                    bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
-                    ++g;
-                    if (it == 0 && k > 0) {
-                        // a later unit's K and V, once the unit before no longer reads
-                        // them (its first Q and dO went ahead into the free buffer)
-                        if (!(ok = wait_bounded(bar(L::B_KVFREE), (k - 1) & 1, abort_flag,
-                                                (ROLE_BWD_PRODUCER << 24) | (L::B_KVFREE << 16) | k)))
+                    ++kv_loads;
+                };
+                for (int k = 0; ok && k < my_units; ++k) {
+                    const BwdUnit u = bwd_unit(k, p);
+                    const int qt_first = p.causal ? u.kt : 0;
+                    const int n_q = p.n_tiles - qt_first;
+                    const size_t head_tiles = static_cast<size_t>(u.bh) * p.n_tiles;
+                    if (k == 0) load_kv(u);  // the first unit's K and V lead
+                    for (int it = 0; it < n_q; ++it) {
+                        const int b = g & 1;
+                        // Buffer b was last used by query tile g-2.
+                        if (g >= 2 && !(ok = wait_bounded(bar(L::B_QEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                          (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | (g & 0xFFFF))))
                             break;
-                        load_kv(u);
+                        const int qt = qt_first + it;
+                        const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                        const uint32_t rb = sbase + L::RB_OFF + b * 1024;
+                        const size_t row0 = (head_tiles + qt) * BT;
+                        mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
+                        for (int c = 0; c < L::KATOMS; ++c) {
+                            tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                            tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                        }
+                        bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
+                        bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
+                        ++g;
+                        if (it == 0 && k > 0) {
+                            // a later unit's K and V, once the unit before no longer reads
+                            // them (its first Q and dO went ahead into the free buffer)
+                            if (!(ok = wait_bounded(bar(L::B_KVFREE), (k - 1) & 1, abort_flag,
+                                                    (ROLE_BWD_PRODUCER << 24) | (L::B_KVFREE << 16) | k)))
+                                break;
+                            load_kv(u);
+                        }
                     }
+                }
+                if (!ok) {
+                    // Let the copies in flight land before the CTA exits.
+                    const uint64_t t0 = global_timer_ns();
+                    for (uint32_t j = g >= 2 ? g - 2 : 0; j < g; ++j)
+                        while (!mbar_try_wait(bar(L::B_QFULL + (j & 1)), (j >> 1) & 1) &&
+                               global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    if (kv_loads > 0)
+                        while (!mbar_try_wait(bar(L::B_KVFULL), (kv_loads - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
                 }
             }
-            if (!ok) {
-                // Let the copies in flight land before the CTA exits.
-                const uint64_t t0 = global_timer_ns();
-                for (uint32_t j = g >= 2 ? g - 2 : 0; j < g; ++j)
-                    while (!mbar_try_wait(bar(L::B_QFULL + (j & 1)), (j >> 1) & 1) &&
-                           global_timer_ns() - t0 < kDrainLimitNs) {
+            __syncwarp();
+        } else if (warp == WARP_MMA) {
+            // ------------------------------------------------ MMA issuer
+            // Per query tile i: dV(i) chunk by chunk, S^T(i+1), dK(i) chunk by
+            // chunk, dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.
+            // Each product that overwrites TMEM columns an earlier product reads
+            // (S^T over P^T, dQ_part over dS^T) is issued after it; the tensor core
+            // runs one thread's products in issue order.  The whole warp runs
+            // the loop (operands stay warp-uniform); one elected lane sends each
+            // block of products and each commit.
+            {
+                constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S^T, dP^T: K-major A and B
+                constexpr uint32_t IDESC_TS = idesc_bf16_f32(BT, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
+                constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dQ_part: MN-major A and B
+                // Descriptors are formed once per operand tile; a k step adds its
+                // compile-time offset to the start-address field, which cannot
+                // carry out of its 14 bits (shared memory is below 256 KB).
+                auto commit = [&](int b) {
+                    if (elect_one()) umma_commit(bar(b));
+                    __syncwarp();
+                };
+                // A = (K or V) x B = (Q or dO), both K-major over D, into `dst`.
+                auto issue_kmajor = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile, int done_bar) {
+                    const uint64_t ad = smem_desc_sw128(a_tile, 16, 1024), bd = smem_desc_sw128(b_tile, 16, 1024);
+                    const uint32_t hi = static_cast<uint32_t>(ad >> 32);
+                    uint32_t av[D / 16], bv[D / 16];
+    #pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
+                        av[k] = static_cast<uint32_t>(ad) + off;
+                        bv[k] = static_cast<uint32_t>(bd) + off;
                     }
-                if (kv_loads > 0)
-                    while (!mbar_try_wait(bar(L::B_KVFULL), (kv_loads - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                    if (elect_one()) {
+                        umma_ss_steps<D / 16>(dst, av, hi, bv, hi, IDESC_KK, 0u);
+                        umma_commit(bar(done_bar));
                     }
-            }
-        }
-        __syncwarp();
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ MMA issuer
-        // Per query tile i: dV(i) chunk by chunk, S^T(i+1), dK(i) chunk by
-        // chunk, dQ_part(i), then dP^T(i+1) once dQ_part(i) has been read.
-        // Each product that overwrites TMEM columns an earlier product reads
-        // (S^T over P^T, dQ_part over dS^T) is issued after it; the tensor core
-        // runs one thread's products in issue order.  The whole warp runs
-        // the loop (operands stay warp-uniform); one elected lane sends each
-        // block of products and each commit.
-        {
-            constexpr uint32_t IDESC_KK = idesc_bf16_f32(BT, BT, 0, 0);  // S^T, dP^T: K-major A and B
-            constexpr uint32_t IDESC_TS = idesc_bf16_f32(BT, D, 0, 1);   // dV, dK: A from TMEM, B MN-major
-            constexpr uint32_t IDESC_MM = idesc_bf16_f32(BT, D, 1, 1);   // dQ_part: MN-major A and B
-            // Descriptors are formed once per operand tile; a k step adds its
-            // compile-time offset to the start-address field, which cannot
-            // carry out of its 14 bits (shared memory is below 256 KB).
-            auto commit = [&](int b) {
-                if (elect_one()) umma_commit(bar(b));
-                __syncwarp();
-            };
-            // A = (K or V) x B = (Q or dO), both K-major over D, into `dst`.
-            auto issue_kmajor = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile, int done_bar) {
-                const uint64_t ad = smem_desc_sw128(a_tile, 16, 1024), bd = smem_desc_sw128(b_tile, 16, 1024);
-                const uint32_t hi = static_cast<uint32_t>(ad >> 32);
-                uint32_t av[D / 16], bv[D / 16];
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = ((k / 4) * L::BOX + (k % 4) * 32) >> 4;
-                    av[k] = static_cast<uint32_t>(ad) + off;
-                    bv[k] = static_cast<uint32_t>(bd) + off;
-                }
-                if (elect_one()) {
-                    umma_ss_steps<D / 16>(dst, av, hi, bv, hi, IDESC_KK, 0u);
-                    umma_commit(bar(done_bar));
-                }
-                __syncwarp();
-            };
-            auto issue_s = [&](uint32_t qb) { issue_kmajor(tmem + L::T_S, sbase + L::K_OFF, qb, L::B_SFULL); };     // S^T = K Q^T
-            auto issue_dp = [&](uint32_t dob) { issue_kmajor(tmem + L::T_DP, sbase + L::V_OFF, dob, L::B_DPFULL); };  // dP^T = V dO^T
-            uint32_t g = 0;  // query tiles (all units of the CTA)
-            bool ok = true;
-            for (int k = 0; ok && k < my_units; ++k) {
-                const int n_q = p.n_tiles - (p.causal ? bwd_unit(k, p).kt : 0);
-                // The unit's first S^T and dP^T: its K and V loaded, its first Q and dO
-                // loaded, and (dP^T lies over dQ_part) the previous tile's dQ_part read.
-                {
-                    const uint32_t q0 = sbase + L::QB_OFF + (g & 1) * 2 * L::TILE;
-                    if (!(ok = wait_bounded(bar(L::B_KVFULL), k & 1, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16) | k) &&
-                               wait_bounded(bar(L::B_QFULL + (g & 1)), (g >> 1) & 1, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (g & 1)) << 16) | (g & 0xFFFF))))
-                        break;
-                    tc_fence_after_sync();
-                    issue_s(q0);
-                    if (g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
-                                                     (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
-                        break;
-                    tc_fence_after_sync();
-                    issue_dp(q0 + L::TILE);
-                }
-                for (int it = 0; ok && it < n_q; ++it, ++g) {
-                    const int b = g & 1;
-                    const uint32_t ph = g & 1;
-                    const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                    const uint32_t dob = qb + L::TILE;
-                    const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
-                    const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
-                    // The unit's first dV and dK products start the accumulators
-                    // over: the previous unit's dK and dV must have left TMEM.
-                    if (it == 0 && k > 0 &&
-                        !(ok = wait_bounded(bar(L::B_DKVREAD), (k - 1) & 1, abort_flag,
-                                            (ROLE_BWD_MMA << 24) | (L::B_DKVREAD << 16) | k)))
-                        break;
-                    // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
-                    // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
-                    for (int c = 0; ok && c < 4; ++c) {
-                        if (!(ok = wait_bounded(bar(L::B_PRDY + c), ph, abort_flag,
-                                                (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | (g & 0xFFFF))))
-                            break;
-                        tc_fence_after_sync();
-                        const uint32_t b0 = static_cast<uint32_t>(dob_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
-                        if (elect_one()) {
-                            umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
-                            umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
-                        }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
-                    // S^T of the next query tile over P^T: the dV products above
-                    // were the last to read P^T (the compute warps keep their own
-                    // copy for dS^T), so the next P^T pass can start as soon as
-                    // this tile's dS^T pass ends.
-                    const bool has_next = it + 1 < n_q;
-                    const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
-                    if (has_next) {
-                        if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
-                                                (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
-                            break;
-                        tc_fence_after_sync();
-                        issue_s(qn);
-                    }
-                    // dK += dS'^T Q likewise.
-                    for (int c = 0; ok && c < 4; ++c) {
-                        if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
-                                                (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | (g & 0xFFFF))))
-                            break;
-                        tc_fence_after_sync();
-                        const uint32_t b0 = static_cast<uint32_t>(qb_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
-                        if (elect_one()) {
-                            umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
-                            umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
-                        }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
-                    commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
-                    // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
-                    // the dS^T buffer (MN-major A) and K MN-major.
+                    __syncwarp();
+                };
+                auto issue_s = [&](uint32_t qb) { issue_kmajor(tmem + L::T_S, sbase + L::K_OFF, qb, L::B_SFULL); };     // S^T = K Q^T
+                auto issue_dp = [&](uint32_t dob) { issue_kmajor(tmem + L::T_DP, sbase + L::V_OFF, dob, L::B_DPFULL); };  // dP^T = V dO^T
+                uint32_t g = 0;  // query tiles (all units of the CTA)
+                bool ok = true;
+                for (int k = 0; ok && k < my_units; ++k) {
+                    const int n_q = p.n_tiles - (p.causal ? bwd_unit(k, p).kt : 0);
+                    // The unit's first S^T and dP^T: its K and V loaded, its first Q and dO
+                    // loaded, and (dP^T lies over dQ_part) the previous tile's dQ_part read.
                     {
-                        const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
-                                       kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
-                        const uint32_t hi = static_cast<uint32_t>(dsd >> 32);
-                        uint32_t av[BT / 16], bv[BT / 16];
-#pragma unroll
-                        for (int kk = 0; kk < BT / 16; ++kk) {
-                            av[kk] = static_cast<uint32_t>(dsd) + ((kk * 2048) >> 4);
-                            bv[kk] = static_cast<uint32_t>(kmd) + ((kk * 2048) >> 4);
-                        }
-                        if (elect_one()) {
-                            umma_ss_steps<BT / 16>(tmem + L::T_DQ, av, hi, bv, hi, IDESC_MM, 0u);
-                            umma_commit(bar(L::B_GDONE));
-                            if (!has_next) umma_commit(bar(L::B_KVFREE));  // the unit's K and V are no longer read
-                        }
-                        __syncwarp();
-                    }
-                    if (has_next) {
-                        if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
-                                                (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                        const uint32_t q0 = sbase + L::QB_OFF + (g & 1) * 2 * L::TILE;
+                        if (!(ok = wait_bounded(bar(L::B_KVFULL), k & 1, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16) | k) &&
+                                   wait_bounded(bar(L::B_QFULL + (g & 1)), (g >> 1) & 1, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (g & 1)) << 16) | (g & 0xFFFF))))
                             break;
                         tc_fence_after_sync();
-                        issue_dp(qn + L::TILE);
+                        issue_s(q0);
+                        if (g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
+                                                         (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        issue_dp(q0 + L::TILE);
+                    }
+                    for (int it = 0; ok && it < n_q; ++it, ++g) {
+                        const int b = g & 1;
+                        const uint32_t ph = g & 1;
+                        const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                        const uint32_t dob = qb + L::TILE;
+                        const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
+                        const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
+                        // The unit's first dV and dK products start the accumulators
+                        // over: the previous unit's dK and dV must have left TMEM.
+                        if (it == 0 && k > 0 &&
+                            !(ok = wait_bounded(bar(L::B_DKVREAD), (k - 1) & 1, abort_flag,
+                                                (ROLE_BWD_MMA << 24) | (L::B_DKVREAD << 16) | k)))
+                            break;
+                        // dV += P^T dO as the P^T chunks arrive: 16 queries per step,
+                        // 8 TMEM columns of P^T, dO rows advance by 16 * 128 bytes.
+                        for (int c = 0; ok && c < 4; ++c) {
+                            if (!(ok = wait_bounded(bar(L::B_PRDY + c), ph, abort_flag,
+                                                    (ROLE_BWD_MMA << 24) | ((L::B_PRDY + c) << 16) | (g & 0xFFFF))))
+                                break;
+                            tc_fence_after_sync();
+                            const uint32_t b0 = static_cast<uint32_t>(dob_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                            if (elect_one()) {
+                                umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                                umma_ts_lo(tmem + L::T_DV, tmem + L::T_S + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                            }
+                            __syncwarp();
+                        }
+                        if (!ok) break;
+                        // S^T of the next query tile over P^T: the dV products above
+                        // were the last to read P^T (the compute warps keep their own
+                        // copy for dS^T), so the next P^T pass can start as soon as
+                        // this tile's dS^T pass ends.
+                        const bool has_next = it + 1 < n_q;
+                        const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
+                        if (has_next) {
+                            if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
+                                                    (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
+                                break;
+                            tc_fence_after_sync();
+                            issue_s(qn);
+                        }
+                        // dK += dS'^T Q likewise.
+                        for (int c = 0; ok && c < 4; ++c) {
+                            if (!(ok = wait_bounded(bar(L::B_DSRDY + c), ph, abort_flag,
+                                                    (ROLE_BWD_MMA << 24) | ((L::B_DSRDY + c) << 16) | (g & 0xFFFF))))
+                                break;
+                            tc_fence_after_sync();
+                            const uint32_t b0 = static_cast<uint32_t>(qb_mn) + ((2 * c * 2048) >> 4), b1 = b0 + (2048 >> 4);
+                            if (elect_one()) {
+                                umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c), b0, mn_hi, IDESC_TS, (it > 0 || c > 0) ? 1u : 0u);
+                                umma_ts_lo(tmem + L::T_DK, tmem + L::T_DP + L::pcol(c) + 8, b1, mn_hi, IDESC_TS, 1u);
+                            }
+                            __syncwarp();
+                        }
+                        if (!ok) break;
+                        commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
+                        // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
+                        // the dS^T buffer (MN-major A) and K MN-major.
+                        {
+                            const uint64_t dsd = smem_desc_sw128(sbase + L::DS_OFF, L::BOX, 1024),
+                                           kmd = smem_desc_sw128(sbase + L::K_OFF, L::BOX, 1024);
+                            const uint32_t hi = static_cast<uint32_t>(dsd >> 32);
+                            uint32_t av[BT / 16], bv[BT / 16];
+    #pragma unroll
+                            for (int kk = 0; kk < BT / 16; ++kk) {
+                                av[kk] = static_cast<uint32_t>(dsd) + ((kk * 2048) >> 4);
+                                bv[kk] = static_cast<uint32_t>(kmd) + ((kk * 2048) >> 4);
+                            }
+                            if (elect_one()) {
+                                umma_ss_steps<BT / 16>(tmem + L::T_DQ, av, hi, bv, hi, IDESC_MM, 0u);
+                                umma_commit(bar(L::B_GDONE));
+                                if (!has_next) umma_commit(bar(L::B_KVFREE));  // the unit's K and V are no longer read
+                            }
+                            __syncwarp();
+                        }
+                        if (has_next) {
+                            if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
+                                                    (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                                break;
+                            tc_fence_after_sync();
+                            issue_dp(qn + L::TILE);
+                        }
                     }
                 }
+                commit(L::B_MMADONE);
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
+                       global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+                }
             }
-            commit(L::B_MMADONE);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(bar(L::B_MMADONE), 0) &&
-                   global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
-            }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp < WARP_DQ) {
         // ------------------------------------------------ compute warps
         const int grp = warp / 4;              // queries 64*grp .. 64*grp + 63
@@ -661,6 +674,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         }
     } else {
         // ------------------------------------------------ dQ warps
+        regs_alloc<REGS_DQ>();
         const int t = (warp - WARP_DQ) * 32 + lane;  // TMEM lane: query row t (dQ_part), key row t (dK, dV)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - WARP_DQ) * 32) << 16);
         const bool issuer = warp == WARP_DQ && lane == 0;  // issues the bulk reductions (D = 64)
@@ -730,27 +744,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                         for (int j = 0; j < 8; ++j)
                             red_add_v4(dq_tile + (8 * h + j) * BT * 4, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                     };
-                    // The next dP^T waits for dQ_part to leave TMEM: two 32-column
-                    // blocks are read before the first reductions and each later
-                    // read is issued while the block before it is reduced, so only
-                    // 16 of the 32 reductions queue ahead of the release.
-                    uint32_t ra[32], rb[32];
+                    // The next dP^T waits for dQ_part to leave TMEM: the whole row
+                    // is read (the dQ warpgroup's larger register share) and TMEM
+                    // released before the first reduction.
+                    uint32_t ra[32], rb[32], rc[32], rd[32];
                     tmem_ld32_async(lane_base + L::T_DQ, ra);
                     tmem_ld32_async(lane_base + L::T_DQ + 32, rb);
+                    tmem_ld32_async(lane_base + L::T_DQ + 64, rc);
+                    tmem_ld32_async(lane_base + L::T_DQ + 96, rd);
                     tmem_ld_wait();
                     reg_fence(ra);
                     reg_fence(rb);
-                    red_chunk(0, ra);
-                    tmem_ld32_async(lane_base + L::T_DQ + 64, ra);
-                    red_chunk(1, rb);
-                    tmem_ld32_async(lane_base + L::T_DQ + 96, rb);
-                    tmem_ld_wait();
-                    reg_fence(ra);
-                    reg_fence(rb);
+                    reg_fence(rc);
+                    reg_fence(rd);
                     tc_fence_before_sync();
                     warp_arrive(bar(L::B_DQREAD), lane);
-                    red_chunk(2, ra);
-                    red_chunk(3, rb);
+                    red_chunk(0, ra);
+                    red_chunk(1, rb);
+                    red_chunk(2, rc);
+                    red_chunk(3, rd);
                 }
             }
             if (!ok) break;
@@ -886,6 +898,13 @@ static cudaError_t launch_d(const BwdParams &p, int num_sms, cudaStream_t stream
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (configured_device != dev) {
+        // The warpgroups' register shares add up to a launch budget of 128 per
+        // thread; a build compiled to fewer would leave the dQ warpgroup
+        // waiting for registers, so it is refused here.
+        cudaFuncAttributes attr;
+        err = cudaFuncGetAttributes(&attr, attn_bwd_kernel<D>);
+        if (err != cudaSuccess) return err;
+        if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
         err = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
         if (err != cudaSuccess) return err;
         configured_device = dev;
