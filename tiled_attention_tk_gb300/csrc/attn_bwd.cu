@@ -28,9 +28,10 @@
 //                      accumulates dV += P^T dO and dK += dS^T Q chunk by
 //                      chunk with P^T and dS^T read from TMEM, then forms
 //                      dQ_part = dS K, which four dQ warps add into the fp32
-//                      accumulator with vector reductions (at D = 64: staged
-//                      in shared memory, one bulk reduction per tile); at the
-//                      end they write dK and dV as bf16.
+//                      accumulator (at D = 64 staged in shared memory, one bulk
+//                      reduction per tile; at D = 128 half staged for one bulk
+//                      reduction, half as vector reductions); at the end they
+//                      write dK and dV as bf16.
 //   bwd_dq_kernel      dQ = bf16(scale * accumulator).
 // The same shared-memory tiles serve as K-major and MN-major MMA operands
 // through different descriptors (Q and dO are K-major B operands of S^T and
@@ -65,8 +66,8 @@ constexpr uint32_t TMEM_COLS = 512;
 // before its reductions.  The shares add up to the launch budget (checked on
 // the host against the compiled kernel), else the growing warpgroup would wait.
 constexpr int LAUNCH_REGS = 128;
-constexpr uint32_t REGS_DQ = 168;
-constexpr uint32_t REGS_CTRL = 88;
+constexpr uint32_t REGS_DQ = 160;
+constexpr uint32_t REGS_CTRL = 96;
 static_assert(2 * LAUNCH_REGS + REGS_DQ + REGS_CTRL == 4 * LAUNCH_REGS, "register split = launch budget");
 static_assert(NUM_THREADS == 512, "four whole warpgroups");
 
@@ -77,9 +78,19 @@ struct Layout {
     static constexpr uint32_t TILE = BT * D * 2;         // a 128 x D tile
     static constexpr uint32_t K_OFF = 0;
     static constexpr uint32_t V_OFF = K_OFF + TILE;
-    // Q and dO of a query tile, double-buffered: buffer b holds Q at
-    // QB_OFF + b * 2 * TILE and dO right after it.
+    // Q and dO of a query tile.  At D = 64 both are double-buffered: buffer b
+    // holds Q at QB_OFF + b * 2 * TILE and dO right after it.  At D = 128 Q is
+    // double-buffered and dO single: the dV products are the last to read a
+    // tile's dO, and the next tile's dO is first read by its dP^T, after the dK
+    // and dQ_part products; the tile this frees stages half a dQ_part block.
     static constexpr uint32_t QB_OFF = V_OFF + TILE;
+    static constexpr bool DO_SINGLE = D == 128;
+    __host__ __device__ static constexpr uint32_t q_off(int b) {
+        return DO_SINGLE ? QB_OFF + b * TILE : QB_OFF + b * 2 * TILE;
+    }
+    __host__ __device__ static constexpr uint32_t do_off(int b) {
+        return DO_SINGLE ? QB_OFF + 2 * TILE : QB_OFF + b * 2 * TILE + TILE;
+    }
     static constexpr uint32_t DS_OFF = QB_OFF + 4 * TILE;   // dS^T: 128 keys x 128 queries bf16 (2 boxes)
     // Per Q/dO buffer b, the query tile's row values: -LSE*log2(e) at
     // RB_OFF + b * 1024 and -Delta 512 bytes further (128 floats each).
@@ -89,9 +100,12 @@ struct Layout {
     // reduction (the TMA unit adds it into L2) instead of the dQ warps'
     // vector reductions.  D = 128 has no room and keeps the vector reductions.
     static constexpr bool DQ_BULK = D == 64;
-    static constexpr uint32_t DQST_BYTES = BT * D * 4;
-    static constexpr uint32_t DQST_OFF = RB_OFF + 2048;
-    static constexpr uint32_t BAR_OFF = DQST_OFF + (DQ_BULK ? 2 * DQST_BYTES : 0);
+    // D = 128 stages half of dQ_part (64 columns, 32 KB, the size of a bf16
+    // tile) in the tile the single dO buffer leaves free.
+    static constexpr uint32_t DQST_BYTES = DO_SINGLE ? BT * 64 * 4 : BT * D * 4;
+    static constexpr uint32_t DQST_OFF = DO_SINGLE ? QB_OFF + 3 * TILE : RB_OFF + 2048;
+    static_assert(!DO_SINGLE || DQST_BYTES == TILE, "the staged half fills the freed tile");
+    static constexpr uint32_t BAR_OFF = RB_OFF + 2048 + (DQ_BULK ? 2 * DQST_BYTES : 0);
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;      // + buffer (2): Q and dO loaded
     static constexpr int B_QEMPTY = 3;     // + buffer (2): the products that read them are done (MMA commit)
@@ -106,7 +120,9 @@ struct Layout {
     static constexpr int B_STAGEFREE = 20; // + buffer (2): its bulk reduction has read it (one thread)
     static constexpr int B_KVFREE = 22;    // a unit's K and V are no longer read (MMA commit)
     static constexpr int B_DKVREAD = 23;   // a unit's dK and dV have left TMEM (dQ warps, 4)
-    static constexpr int NUM_BARS = 24;
+    static constexpr int B_DOFULL = 24;    // dO loaded (single buffer)
+    static constexpr int B_DOEMPTY = 25;   // the dV products that read dO are done (MMA commit)
+    static constexpr int NUM_BARS = 26;
     static constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
     // No alignment slack: the dynamic shared memory of a kernel without
     // static shared memory starts 1024-byte aligned (the kernel checks).
@@ -286,6 +302,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         mbar_init(bar(L::B_MMADONE), 1);
         mbar_init(bar(L::B_KVFREE), 1);
         mbar_init(bar(L::B_DKVREAD), 4);
+        mbar_init(bar(L::B_DOFULL), 1);
+        mbar_init(bar(L::B_DOEMPTY), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_STAGED + b), 4);
             mbar_init(bar(L::B_STAGEFREE + b), 1);
@@ -309,6 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                 tma_prefetch_desc(&p.tmDO);
                 uint32_t g = 0;          // query tiles loaded (all units of the CTA)
                 uint32_t kv_loads = 0;   // units whose K and V were loaded
+                uint32_t do_loads = 0;   // dO loads into the single buffer
                 bool ok = true;
                 auto load_kv = [&](const BwdUnit &u) {
                     mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
@@ -331,17 +350,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                                                           (ROLE_BWD_PRODUCER << 24) | ((L::B_QEMPTY + b) << 16) | (g & 0xFFFF))))
                             break;
                         const int qt = qt_first + it;
-                        const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
+                        const uint32_t qb = sbase + L::q_off(b), dob = sbase + L::do_off(b);
                         const uint32_t rb = sbase + L::RB_OFF + b * 1024;
                         const size_t row0 = (head_tiles + qt) * BT;
-                        mbar_arrive_expect_tx(bar(L::B_QFULL + b), 2 * L::TILE + 1024);
-                        for (int c = 0; c < L::KATOMS; ++c) {
+                        mbar_arrive_expect_tx(bar(L::B_QFULL + b), (L::DO_SINGLE ? 1 : 2) * L::TILE + 1024);
+                        for (int c = 0; c < L::KATOMS; ++c)
                             tma_load_3d(qb + c * L::BOX, &p.tmQ, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
-                            tma_load_3d(qb + L::TILE + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
-                        }
                         bulk_load(rb, p.neg_lse2 + row0, 512, bar(L::B_QFULL + b));
                         bulk_load(rb + 512, p.neg_delta + row0, 512, bar(L::B_QFULL + b));
-                        ++g;
+                        if constexpr (L::DO_SINGLE) {
+                            ++g;  // counted before the wait below, so that the drain covers Q
+                            // the single dO buffer, once the previous tile's dV products are done
+                            if (g >= 2 && !(ok = wait_bounded(bar(L::B_DOEMPTY), (g - 2) & 1, abort_flag,
+                                                              (ROLE_BWD_PRODUCER << 24) | (L::B_DOEMPTY << 16) | (g & 0xFFFF))))
+                                break;
+                            mbar_arrive_expect_tx(bar(L::B_DOFULL), L::TILE);
+                            for (int c = 0; c < L::KATOMS; ++c)
+                                tma_load_3d(dob + c * L::BOX, &p.tmDO, bar(L::B_DOFULL), c * 64, qt * BT, u.bh);
+                            ++do_loads;
+                        } else {
+                            for (int c = 0; c < L::KATOMS; ++c)
+                                tma_load_3d(dob + c * L::BOX, &p.tmDO, bar(L::B_QFULL + b), c * 64, qt * BT, u.bh);
+                            ++g;
+                        }
                         if (it == 0 && k > 0) {
                             // a later unit's K and V, once the unit before no longer reads
                             // them (its first Q and dO went ahead into the free buffer)
@@ -361,6 +392,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                         }
                     if (kv_loads > 0)
                         while (!mbar_try_wait(bar(L::B_KVFULL), (kv_loads - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    if (do_loads > 0)
+                        while (!mbar_try_wait(bar(L::B_DOFULL), (do_loads - 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
                         }
                 }
             }
@@ -411,7 +445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     // The unit's first S^T and dP^T: its K and V loaded, its first Q and dO
                     // loaded, and (dP^T lies over dQ_part) the previous tile's dQ_part read.
                     {
-                        const uint32_t q0 = sbase + L::QB_OFF + (g & 1) * 2 * L::TILE;
+                        const uint32_t q0 = sbase + L::q_off(g & 1);
                         if (!(ok = wait_bounded(bar(L::B_KVFULL), k & 1, abort_flag,
                                                 (ROLE_BWD_MMA << 24) | (L::B_KVFULL << 16) | k) &&
                                    wait_bounded(bar(L::B_QFULL + (g & 1)), (g >> 1) & 1, abort_flag,
@@ -422,14 +456,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                         if (g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
                                                          (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
                             break;
+                        if (L::DO_SINGLE && !(ok = wait_bounded(bar(L::B_DOFULL), g & 1, abort_flag,
+                                                                (ROLE_BWD_MMA << 24) | (L::B_DOFULL << 16) | (g & 0xFFFF))))
+                            break;
                         tc_fence_after_sync();
-                        issue_dp(q0 + L::TILE);
+                        issue_dp(sbase + L::do_off(g & 1));
                     }
                     for (int it = 0; ok && it < n_q; ++it, ++g) {
                         const int b = g & 1;
                         const uint32_t ph = g & 1;
-                        const uint32_t qb = sbase + L::QB_OFF + b * 2 * L::TILE;
-                        const uint32_t dob = qb + L::TILE;
+                        const uint32_t qb = sbase + L::q_off(b);
+                        const uint32_t dob = sbase + L::do_off(b);
                         const uint64_t qb_mn = smem_desc_sw128(qb, L::BOX, 1024), dob_mn = smem_desc_sw128(dob, L::BOX, 1024);
                         const uint32_t mn_hi = static_cast<uint32_t>(qb_mn >> 32);
                         // The unit's first dV and dK products start the accumulators
@@ -453,12 +490,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                             __syncwarp();
                         }
                         if (!ok) break;
+                        if constexpr (L::DO_SINGLE) commit(L::B_DOEMPTY);  // the single dO buffer may be reloaded
                         // S^T of the next query tile over P^T: the dV products above
                         // were the last to read P^T (the compute warps keep their own
                         // copy for dS^T), so the next P^T pass can start as soon as
                         // this tile's dS^T pass ends.
                         const bool has_next = it + 1 < n_q;
-                        const uint32_t qn = sbase + L::QB_OFF + (b ^ 1) * 2 * L::TILE;
+                        const uint32_t qn = sbase + L::q_off(b ^ 1);
                         if (has_next) {
                             if (!(ok = wait_bounded(bar(L::B_QFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
                                                     (ROLE_BWD_MMA << 24) | ((L::B_QFULL + (b ^ 1)) << 16) | (g & 0xFFFF))))
@@ -504,8 +542,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                             if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
                                                     (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
                                 break;
+                            if (L::DO_SINGLE && !(ok = wait_bounded(bar(L::B_DOFULL), (g + 1) & 1, abort_flag,
+                                                                    (ROLE_BWD_MMA << 24) | (L::B_DOFULL << 16) | (g & 0xFFFF))))
+                                break;
                             tc_fence_after_sync();
-                            issue_dp(qn + L::TILE);
+                            issue_dp(sbase + L::do_off(b ^ 1));
                         }
                     }
                 }
@@ -677,7 +718,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
         regs_alloc<REGS_DQ>();
         const int t = (warp - WARP_DQ) * 32 + lane;  // TMEM lane: query row t (dQ_part), key row t (dK, dV)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - WARP_DQ) * 32) << 16);
-        const bool issuer = warp == WARP_DQ && lane == 0;  // issues the bulk reductions (D = 64)
+        const bool issuer = warp == WARP_DQ && lane == 0;  // issues the bulk reductions
         int bulk_issued = 0;
         bool ok = true;
         uint32_t g = 0;  // query tiles (all units of the CTA)
@@ -735,18 +776,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the issuer's verdict holds for its warp
                     if (!ok) break;
                 } else {
-                    // Accumulator tile layout [D/4][128 rows][4]: a warp's vector
-                    // reduction of one 4-column group covers 512 contiguous bytes.
-                    float *dq_tile = dq_first + static_cast<size_t>(it) * BT * D + t * 4;
-                    static_assert(D == 128, "the vector-reduction path runs at D = 128");
-                    auto red_chunk = [&](int h, uint32_t(&r)[32]) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            red_add_v4(dq_tile + (8 * h + j) * BT * 4, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    };
                     // The next dP^T waits for dQ_part to leave TMEM: the whole row
                     // is read (the dQ warpgroup's larger register share) and TMEM
-                    // released before the first reduction.
+                    // released first.  Then columns 0..63 go through the staging tile,
+                    // laid out like the accumulator ([16 column groups][128 rows][4]),
+                    // as one bulk reduction by the TMA unit, and columns 64..127 as
+                    // vector reductions from the SM: the two paths share the traffic.
+                    static_assert(D == 128, "the split reduction runs at D = 128");
                     uint32_t ra[32], rb[32], rc[32], rd[32];
                     tmem_ld32_async(lane_base + L::T_DQ, ra);
                     tmem_ld32_async(lane_base + L::T_DQ + 32, rb);
@@ -759,10 +795,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                     reg_fence(rd);
                     tc_fence_before_sync();
                     warp_arrive(bar(L::B_DQREAD), lane);
-                    red_chunk(0, ra);
-                    red_chunk(1, rb);
-                    red_chunk(2, rc);
-                    red_chunk(3, rd);
+                    float *const dq_tile = dq_first + static_cast<size_t>(it) * BT * D;
+                    // the staging tile is free once the previous tile's bulk reduction has read it
+                    if (g >= 1 && !(ok = wait_bounded(bar(L::B_STAGEFREE), (g - 1) & 1, abort_flag,
+                                                      (ROLE_BWD_COMPUTE << 24) | (L::B_STAGEFREE << 16) | (g & 0xFFFF))))
+                        break;
+                    const uint32_t stage = sbase + L::DQST_OFF + t * 16;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stage + j * BT * 16, ra[4 * j], ra[4 * j + 1], ra[4 * j + 2], ra[4 * j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stage + (8 + j) * BT * 16, rb[4 * j], rb[4 * j + 1], rb[4 * j + 2], rb[4 * j + 3]);
+                    fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk-copy unit
+                    warp_arrive(bar(L::B_STAGED), lane);
+                    if (issuer) {
+                        if ((ok = wait_bounded(bar(L::B_STAGED), g & 1, abort_flag,
+                                               (ROLE_BWD_COMPUTE << 24) | (L::B_STAGED << 16) | (g & 0xFFFF)))) {
+                            bulk_reduce_add_f32(dq_tile, sbase + L::DQST_OFF, L::DQST_BYTES);
+                            tma_store_commit();
+                            ++bulk_issued;
+                            tma_store_wait_read_all();  // the staging tile may be rewritten
+                            mbar_arrive(bar(L::B_STAGEFREE));
+                        }
+                    }
+                    __syncwarp();
+                    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;  // the issuer's verdict holds for its warp
+                    if (!ok) break;
+                    float *const dq_row = dq_tile + t * 4;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        red_add_v4(dq_row + (16 + j) * BT * 4, rc[4 * j], rc[4 * j + 1], rc[4 * j + 2], rc[4 * j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        red_add_v4(dq_row + (24 + j) * BT * 4, rd[4 * j], rd[4 * j + 1], rd[4 * j + 2], rd[4 * j + 3]);
                 }
             }
             if (!ok) break;
