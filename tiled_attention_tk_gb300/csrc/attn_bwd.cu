@@ -938,19 +938,35 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
     __shared__ uint32_t rows[BT * STRIDE];
     const int64_t tile = blockIdx.x;   // bh * n_tiles + qt
     const float4 *acc = reinterpret_cast<const float4 *>(dq_acc + tile * BT * D);
-    for (int i = threadIdx.x; i < BT * (d / 4); i += blockDim.x) {
+    // Fixed trip counts for the 256-thread block: every load of a thread is in
+    // flight before the first is used.  Column groups past the tensors' head
+    // dim d (96 on the 128-column kernel) are not read.
+    constexpr int LOADS = BT * (D / 4) / 256;
+    static_assert(LOADS * 256 == BT * (D / 4), "whole loads per thread");
+    float4 a[LOADS];
+#pragma unroll
+    for (int k = 0; k < LOADS; ++k) {
+        const int i = static_cast<int>(threadIdx.x) + k * 256;
+        a[k] = i / BT < d / 4 ? acc[i] : make_float4(0.f, 0.f, 0.f, 0.f);  // columns 4*grp .. of row t
+    }
+#pragma unroll
+    for (int k = 0; k < LOADS; ++k) {
+        const int i = static_cast<int>(threadIdx.x) + k * 256;
         const int t = i % BT, grp = i / BT;
-        const float4 a = acc[i];  // columns 4*grp .. 4*grp+3 of row t
-        rows[t * STRIDE + 2 * grp] = pack_bf16x2(scale * a.x, scale * a.y);
-        rows[t * STRIDE + 2 * grp + 1] = pack_bf16x2(scale * a.z, scale * a.w);
+        rows[t * STRIDE + 2 * grp] = pack_bf16x2(scale * a[k].x, scale * a[k].y);
+        rows[t * STRIDE + 2 * grp + 1] = pack_bf16x2(scale * a[k].z, scale * a[k].w);
     }
     __syncthreads();
     const int qt = static_cast<int>(tile % n_tiles);
     const int64_t bh = tile / n_tiles;
-    for (int i = threadIdx.x; i < BT * (d / 8); i += blockDim.x) {
-        const int t = i / (d / 8), g = i % (d / 8);
+    constexpr int STORES = BT * (D / 8) / 256;
+    static_assert(STORES * 256 == BT * (D / 8), "whole stores per thread");
+#pragma unroll
+    for (int k = 0; k < STORES; ++k) {
+        const int i = static_cast<int>(threadIdx.x) + k * 256;
+        const int t = i / (D / 8), g = i % (D / 8);
         const int n = qt * BT + t;
-        if (n >= N) continue;
+        if (n >= N || g >= d / 8) continue;
         const uint32_t *r = rows + t * STRIDE + 4 * g;
         reinterpret_cast<uint4 *>(dQ + (bh * N + n) * d)[g] = make_uint4(r[0], r[1], r[2], r[3]);
     }
