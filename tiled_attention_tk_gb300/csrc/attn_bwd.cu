@@ -18,8 +18,9 @@
 //   bwd_prep_kernel    -Delta_i = -<dO_i, O_i> (fp32) and -LSE_i * log2(e)
 //                      per padded query row; zeroes the fp32 dQ accumulator.
 //   attn_bwd_kernel<D> one CTA per (head, 128-key tile).  K_j and V_j stay in
-//                      shared memory and Q_i, dO_i of the query tiles that
-//                      see the keys stream through two buffers.  The MMA
+//                      shared memory; Q_i of the query tiles that see the
+//                      keys streams through two buffers, dO_i through two
+//                      (D = 64) or one (D = 128).  The MMA
 //                      warp forms S^T = K Q^T and dP^T = V dO^T in TMEM (one
 //                      key per TMEM lane); two groups of four compute warps
 //                      turn them into P^T and then dS^T, 32 queries at a
@@ -92,13 +93,14 @@ struct Layout {
         return DO_SINGLE ? QB_OFF + 2 * TILE : QB_OFF + b * 2 * TILE + TILE;
     }
     static constexpr uint32_t DS_OFF = QB_OFF + 4 * TILE;   // dS^T: 128 keys x 128 queries bf16 (2 boxes)
-    // Per Q/dO buffer b, the query tile's row values: -LSE*log2(e) at
+    // Per Q buffer b, the query tile's row values: -LSE*log2(e) at
     // RB_OFF + b * 1024 and -Delta 512 bytes further (128 floats each).
     static constexpr uint32_t RB_OFF = DS_OFF + 2 * BOX;
     // D = 64 leaves room for two fp32 staging copies of dQ_part, laid out like
     // an accumulator tile ([D/4][128 rows][4]); each goes out as one bulk
     // reduction (the TMA unit adds it into L2) instead of the dQ warps'
-    // vector reductions.  D = 128 has no room and keeps the vector reductions.
+    // vector reductions.  D = 128 has room for one half (below); the other
+    // half goes out as vector reductions.
     static constexpr bool DQ_BULK = D == 64;
     // D = 128 stages half of dQ_part (64 columns, 32 KB, the size of a bf16
     // tile) in the tile the single dO buffer leaves free.
@@ -926,8 +928,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
 }
 
 // dQ = bf16(scale * accumulator), one 128-row query tile per block.  The
-// accumulator of a tile is [D/4][128 rows][4 floats] (the order the main
-// kernel's vector reductions write; D the kernel's head dim): its first d
+// accumulator of a tile is [D/4][128 rows][4 floats] (the layout the main
+// kernel's reductions add into; D the kernel's head dim): its first d
 // columns (the tensors' head dim) are read with consecutive threads on
 // consecutive rows, turned into bf16 rows in shared memory, and written out
 // row by row, so both sides are coalesced.
