@@ -21,9 +21,10 @@
 //   state:  S^T += [V | 1]^T phi(K)                                 (tensor core)
 //   O_i = num_i / den_i.
 //
-// 320 threads: two compute warpgroups over the same 128 rows (row i of the
-// chunk = TMEM lane i; they split the columns of every step), a TMA warp and
-// an MMA warp.  The tensor core forms chunk c+1's Q K^T right after chunk
+// 512 threads: two compute warpgroups over the same 128 rows (row i of the
+// chunk = TMEM lane i; they split the columns of every step), an epilogue
+// warpgroup that writes O and DEN, a TMA warp and an MMA warp (and two warps
+// that only take part in set-up).  The tensor core forms chunk c+1's Q K^T right after chunk
 // c's P [V|1], so the compute warps form P of c+1 while the rest of chunk c's
 // products run.  Q and K arrive as 128 x 64 boxes of which the first
 // 16 columns are the tensor (the rest zero-filled by TMA), so the same
@@ -48,9 +49,23 @@ constexpr int DQK = 16;
 constexpr int DV = 64;
 constexpr int F = 160;             // feature columns (153 live; ten 16-feature steps)
 constexpr int NV = 80;             // [num | den] columns (64 + 1, padded to a multiple of 16)
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 320;   // the segment-state kernel: 8 compute warps, TMA warp, MMA warp
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
+// The main kernel: 8 compute warps, an epilogue warpgroup that writes O, and a
+// control warpgroup (TMA warp, MMA warp, two set-up warps).  Registers per
+// thread and warpgroup (setmaxnreg) add up to the launch budget of 128: the
+// host refuses a build compiled to any other count, else the growing
+// warpgroups would wait for registers.
+constexpr int MAIN_THREADS = 512;
+constexpr int M_WARP_EPI = 8;
+constexpr int M_WARP_TMA = 12;
+constexpr int M_WARP_MMA = 13;
+constexpr int LAUNCH_REGS = 128;
+constexpr uint32_t REGS_COMPUTE = 168;
+constexpr uint32_t REGS_EPI = 88;
+constexpr uint32_t REGS_CTRL = 88;
+static_assert(2 * REGS_COMPUTE + REGS_EPI + REGS_CTRL == 4 * LAUNCH_REGS, "register split = launch budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ROLE_BASED_PRODUCER = 12;
 constexpr uint32_t ROLE_BASED_MMA = 13;
@@ -64,7 +79,7 @@ constexpr uint32_t PHIK_OFF = ONES_OFF + BOX;         // phi(K): 128 rows x 160 
 constexpr uint32_t SBOX = NV * 128;                   // 80 rows x 128 bytes
 constexpr uint32_t SPREV_OFF = PHIK_OFF + 3 * BOX;    // S (bf16, K-major): 80 rows x 160 features (3 boxes, the last half used)
 constexpr uint32_t OBOX = 32 * DV;                    // 32 rows x 64 bytes: one warp's O columns
-constexpr uint32_t OST_OFF = SPREV_OFF + 3 * SBOX;    // O staging: one 32 x 32 box per compute warp
+constexpr uint32_t OST_OFF = SPREV_OFF + 3 * SBOX;    // O staging: two 32 x 32 boxes per epilogue warp
 constexpr uint32_t BAR_OFF = OST_OFF + 8 * OBOX;
 constexpr int B_QKFULL = 0;        // + buffer (2): Q, K of a chunk loaded
 constexpr int B_QKEMPTY = 2;       // + buffer (2): its Q K^T and feature maps formed (8 warps)
@@ -72,13 +87,14 @@ constexpr int B_VFULL = 4;         // + buffer (2): V of a chunk loaded
 constexpr int B_VEMPTY = 6;        // + buffer (2): its P [V|1] and state products done
 constexpr int B_SFULL = 8;         // Q K^T in TMEM
 constexpr int B_SREAD = 9;         // both groups hold their half of S in registers (8 warps)
-constexpr int B_PREADY = 10;       // P in TMEM, the last O read out (8 warps)
+constexpr int B_PREADY = 10;       // P in TMEM (8 warps)
 constexpr int B_PHIQREADY = 11;    // phi(Q) in TMEM, the bf16 state of the chunks before in smem (8 warps)
 constexpr int B_PHIKREADY = 12;    // phi(K) in smem (8 warps)
 constexpr int B_ODONE = 13;        // [num | den] of the chunk complete
 constexpr int B_STDONE = 14;       // state product done
 constexpr int B_MMADONE = 15;
-constexpr int NUM_BARS = 16;
+constexpr int B_OFREE = 16;        // [num | den] of the chunk read out (epilogue, 4)
+constexpr int NUM_BARS = 17;
 constexpr uint32_t SMEM_USED = BAR_OFF + NUM_BARS * 8 + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 227u * 1024u, "shared memory per CTA");
@@ -252,7 +268,7 @@ struct Piece {
 // it published.  Compiled apart, so the whole-head kernel carries none of the
 // bookkeeping.
 template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
+__global__ void __launch_bounds__(MAIN_THREADS, 1) based_kernel(const __grid_constant__ BasedParams p) {
     constexpr bool SEG = MODE == 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         return {hs, cs, n_ch - cs, 2, 0, 0};  // the end of the head the run starts in
     };
 
-    if (warp == WARP_MMA) {
+    if (warp == M_WARP_MMA) {
         tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
@@ -310,6 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_STDONE), 1);
         mbar_init(bar(B_MMADONE), 1);
+        mbar_init(bar(B_OFREE), 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -326,179 +343,216 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_TMA) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.tmQ);
-            tma_prefetch_desc(&p.tmK);
-            tma_prefetch_desc(&p.tmV);
-            // Q, K of chunk c into buffer c & 1 once chunk c-2's Q K^T and
-            // feature maps are formed (early, so the next S never waits on
-            // HBM); V of chunk c once chunk c-2's products are done.
-            int qk_issued = 0, v_issued = 0;
-            bool ok = true;
-            int g0 = 0;  // chunks of earlier pieces
-            for (int k = 0; ok && k < n_pieces; ++k) {
-            const Piece pc = piece(k);
-            for (int c = 0; c < pc.n; ++c) {
-                const int g = g0 + c;
-                const int b = g & 1;
-                if (g >= 2 && !(ok = wait_bounded(bar(B_QKEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
-                                                  (ROLE_BASED_PRODUCER << 24) | ((B_QKEMPTY + b) << 16) | (g & 0xFFFF))))
-                    break;
-                // Q and K boxes carry 16 real columns; TMA fills the rest with 0
-                // but still counts the full box.
-                const uint32_t dst = sbase + QK_OFF + b * 2 * BOX;
-                mbar_arrive_expect_tx(bar(B_QKFULL + b), 2 * BOX);
-                tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
-                tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
-                ++qk_issued;
-                if (g >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
-                                                  (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | (g & 0xFFFF))))
-                    break;
-                mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
-                tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (pc.c0 + c) * C, pc.bh);
-                ++v_issued;
-            }
-            g0 += pc.n;
-            }
-            if (!ok) {
-                // let the loads in flight land before the CTA's shared memory goes away
-                const uint64_t t0 = global_timer_ns();
-                for (int j = qk_issued - 2 < 0 ? 0 : qk_issued - 2; j < qk_issued; ++j)
-                    while (!mbar_try_wait(bar(B_QKFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
-                    }
-                for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
-                    while (!mbar_try_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
-                    }
-            }
-        }
-        __syncwarp();
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------ MMA issuer
-        // The whole warp runs the loop (operands stay warp-uniform); one
-        // elected lane sends each block of products and each commit.
-        {
-            constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);       // Q K^T
-            constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
-            constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
-            constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
-            // Per chunk c: Q K^T of chunk c+1 as soon as both groups hold S of
-            // chunk c in registers; then P [V|1], phi(Q) S_{<c} and the state
-            // update, each once its operands are in place.
-            auto issue_s = [&](int c) {
-                const uint32_t qb = sbase + QK_OFF + (c & 1) * 2 * BOX;
-                const uint64_t qd = smem_desc_sw128(qb, 16, 1024), kd = smem_desc_sw128(qb + BOX, 16, 1024);
-                if (elect_one()) {
-                    umma_ss(tmem + T_S, qd, kd, ID_S, 0);
-                    umma_commit(bar(B_SFULL));
+    if (warp >= M_WARP_TMA) {
+        regs_dealloc<REGS_CTRL>();
+        if (warp == M_WARP_TMA) {
+            // ------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tmQ);
+                tma_prefetch_desc(&p.tmK);
+                tma_prefetch_desc(&p.tmV);
+                // Q, K of chunk c into buffer c & 1 once chunk c-2's Q K^T and
+                // feature maps are formed (early, so the next S never waits on
+                // HBM); V of chunk c once chunk c-2's products are done.
+                int qk_issued = 0, v_issued = 0;
+                bool ok = true;
+                int g0 = 0;  // chunks of earlier pieces
+                for (int k = 0; ok && k < n_pieces; ++k) {
+                const Piece pc = piece(k);
+                for (int c = 0; c < pc.n; ++c) {
+                    const int g = g0 + c;
+                    const int b = g & 1;
+                    if (g >= 2 && !(ok = wait_bounded(bar(B_QKEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                      (ROLE_BASED_PRODUCER << 24) | ((B_QKEMPTY + b) << 16) | (g & 0xFFFF))))
+                        break;
+                    // Q and K boxes carry 16 real columns; TMA fills the rest with 0
+                    // but still counts the full box.
+                    const uint32_t dst = sbase + QK_OFF + b * 2 * BOX;
+                    mbar_arrive_expect_tx(bar(B_QKFULL + b), 2 * BOX);
+                    tma_load_3d(dst, &p.tmQ, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
+                    tma_load_3d(dst + BOX, &p.tmK, bar(B_QKFULL + b), 0, (pc.c0 + c) * C, pc.bh);
+                    ++qk_issued;
+                    if (g >= 2 && !(ok = wait_bounded(bar(B_VEMPTY + b), ((g >> 1) - 1) & 1, abort_flag,
+                                                      (ROLE_BASED_PRODUCER << 24) | ((B_VEMPTY + b) << 16) | (g & 0xFFFF))))
+                        break;
+                    mbar_arrive_expect_tx(bar(B_VFULL + b), BOX);
+                    tma_load_3d(sbase + V_OFF + b * BOX, &p.tmV, bar(B_VFULL + b), 0, (pc.c0 + c) * C, pc.bh);
+                    ++v_issued;
                 }
-                __syncwarp();
-            };
-            bool ok = true;
-            int g0 = 0;  // chunks of earlier pieces
-            for (int k = 0; ok && k < n_pieces; ++k) {
-            const Piece pc = piece(k);
-            const bool has_prev = pc.carry != 0;
-            if (k == 0) {  // the first S (a later piece's was issued during the piece before it)
-                ok = wait_bounded(bar(B_QKFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag,
-                                  (ROLE_BASED_MMA << 24) | ((B_QKFULL + (g0 & 1)) << 16) | (g0 & 0xFFFF));
-                if (ok) {
-                    tc_fence_after_sync();
-                    issue_s(g0);
+                g0 += pc.n;
+                }
+                if (!ok) {
+                    // let the loads in flight land before the CTA's shared memory goes away
+                    const uint64_t t0 = global_timer_ns();
+                    for (int j = qk_issued - 2 < 0 ? 0 : qk_issued - 2; j < qk_issued; ++j)
+                        while (!mbar_try_wait(bar(B_QKFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
+                    for (int j = v_issued - 2 < 0 ? 0 : v_issued - 2; j < v_issued; ++j)
+                        while (!mbar_try_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1) && global_timer_ns() - t0 < kDrainLimitNs) {
+                        }
                 }
             }
-            for (int c = 0; ok && c < pc.n; ++c) {
-                const int g = g0 + c;
-                const int b = g & 1;
-                const uint32_t ph = g & 1;
-                const uint32_t vb = sbase + V_OFF + b * BOX;
-                if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | (g & 0xFFFF))))
-                    break;
-                if (c + 1 < pc.n || k + 1 < n_pieces) {  // S of the next chunk, in this piece or the next
-                    if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
-                                            (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | ((g + 1) & 0xFFFF))))
+            __syncwarp();
+        } else if (warp == M_WARP_MMA) {
+            // ------------------------------------------------ MMA issuer
+            // The whole warp runs the loop (operands stay warp-uniform); one
+            // elected lane sends each block of products and each commit.
+            {
+                constexpr uint32_t ID_S = idesc_bf16_f32(C, C, 0, 0);       // Q K^T
+                constexpr uint32_t ID_INTRA = idesc_bf16_f32(C, NV, 0, 1);  // P [V | 1]: A in TMEM, B MN-major
+                constexpr uint32_t ID_INTER = idesc_bf16_f32(C, NV, 0, 0);  // phi(Q) S: A in TMEM, B K-major
+                constexpr uint32_t ID_STATE = idesc_bf16_f32(C, F, 1, 1);   // [V | 1]^T phi(K): both MN-major
+                // Per chunk c: Q K^T of chunk c+1 as soon as both groups hold S of
+                // chunk c in registers; then P [V|1], phi(Q) S_{<c} and the state
+                // update, each once its operands are in place.
+                auto issue_s = [&](int c) {
+                    const uint32_t qb = sbase + QK_OFF + (c & 1) * 2 * BOX;
+                    const uint64_t qd = smem_desc_sw128(qb, 16, 1024), kd = smem_desc_sw128(qb + BOX, 16, 1024);
+                    if (elect_one()) {
+                        umma_ss(tmem + T_S, qd, kd, ID_S, 0);
+                        umma_commit(bar(B_SFULL));
+                    }
+                    __syncwarp();
+                };
+                bool ok = true;
+                int g0 = 0;  // chunks of earlier pieces
+                for (int k = 0; ok && k < n_pieces; ++k) {
+                const Piece pc = piece(k);
+                const bool has_prev = pc.carry != 0;
+                if (k == 0) {  // the first S (a later piece's was issued during the piece before it)
+                    ok = wait_bounded(bar(B_QKFULL + (g0 & 1)), (g0 >> 1) & 1, abort_flag,
+                                      (ROLE_BASED_MMA << 24) | ((B_QKFULL + (g0 & 1)) << 16) | (g0 & 0xFFFF));
+                    if (ok) {
+                        tc_fence_after_sync();
+                        issue_s(g0);
+                    }
+                }
+                for (int c = 0; ok && c < pc.n; ++c) {
+                    const int g = g0 + c;
+                    const int b = g & 1;
+                    const uint32_t ph = g & 1;
+                    const uint32_t vb = sbase + V_OFF + b * BOX;
+                    if (!(ok = wait_bounded(bar(B_SREAD), ph, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | (B_SREAD << 16) | (g & 0xFFFF))))
+                        break;
+                    if (c + 1 < pc.n || k + 1 < n_pieces) {  // S of the next chunk, in this piece or the next
+                        if (!(ok = wait_bounded(bar(B_QKFULL + (b ^ 1)), ((g + 1) >> 1) & 1, abort_flag,
+                                                (ROLE_BASED_MMA << 24) | ((B_QKFULL + (b ^ 1)) << 16) | ((g + 1) & 0xFFFF))))
+                            break;
+                        tc_fence_after_sync();
+                        issue_s(g + 1);
+                    }
+                    if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | (g & 0xFFFF))))
+                        break;
+                    if (!(ok = wait_bounded(bar(B_VFULL + b), (g >> 1) & 1, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | ((B_VFULL + b) << 16) | (g & 0xFFFF))))
+                        break;
+                    // the epilogue has read the previous chunk's [num | den]
+                    if (g > 0 && !(ok = wait_bounded(bar(B_OFREE), (g - 1) & 1, abort_flag,
+                                                     (ROLE_BASED_MMA << 24) | (B_OFREE << 16) | (g & 0xFFFF))))
                         break;
                     tc_fence_after_sync();
-                    issue_s(g + 1);
+                    // intra: [num | den] = P [V | 1]; 16 chunk rows per step.  Descriptors
+                    // are formed once per operand; a k step adds its compile-time
+                    // offset to the start-address field (no carry: smem < 256 KB).
+                    const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
+                    const uint32_t v1_lo = static_cast<uint32_t>(v1d), hi = static_cast<uint32_t>(v1d >> 32);
+                    uint32_t v1v[C / 16];
+    #pragma unroll
+                    for (int k = 0; k < C / 16; ++k) v1v[k] = v1_lo + ((k * 2048) >> 4);
+                    if (elect_one()) umma_ts_steps<C / 16, 8>(tmem + T_O, tmem + T_P, v1v, hi, ID_INTRA, 0u);
+                    __syncwarp();
+                    // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
+                    if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | (g & 0xFFFF))))
+                        break;
+                    tc_fence_after_sync();
+                    const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
+                    uint32_t sv[F / 16];
+    #pragma unroll
+                    for (int k = 0; k < F / 16; ++k) sv[k] = s_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4);
+                    if (elect_one()) {
+                        if (c > 0 || has_prev) umma_ts_steps<F / 16, 8>(tmem + T_O, tmem + T_PHIQ, sv, hi, ID_INTER, 1u);
+                        umma_commit(bar(B_ODONE));
+                    }
+                    __syncwarp();
+                    // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
+                    if (!(ok = wait_bounded(bar(B_PHIKREADY), ph, abort_flag,
+                                            (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | (g & 0xFFFF))))
+                        break;
+                    tc_fence_after_sync();
+                    const uint32_t pk_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024));
+                    uint32_t pkv[C / 16];
+    #pragma unroll
+                    for (int k = 0; k < C / 16; ++k) pkv[k] = pk_lo + ((k * 2048) >> 4);
+                    if (elect_one()) {
+                        umma_ss_steps<C / 16>(tmem + T_ST, v1v, hi, pkv, hi, ID_STATE, (c > 0 || has_prev) ? 1u : 0u);
+                        umma_commit(bar(B_STDONE));
+                        umma_commit(bar(B_VEMPTY + b));
+                    }
+                    __syncwarp();
                 }
-                if (!(ok = wait_bounded(bar(B_PREADY), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_PREADY << 16) | (g & 0xFFFF))))
-                    break;
-                if (!(ok = wait_bounded(bar(B_VFULL + b), (g >> 1) & 1, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | ((B_VFULL + b) << 16) | (g & 0xFFFF))))
+                g0 += pc.n;
+                }
+                if (elect_one()) umma_commit(bar(B_MMADONE));
+                __syncwarp();
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp >= M_WARP_EPI) {
+        // ------------------------------------------------ epilogue warps
+        // O = num / den and DEN of every chunk, once its [num | den] is
+        // complete: warp w writes rows 32w .. 32w + 31 of the chunk, both
+        // 32-column halves, and releases the accumulator for the next chunk's
+        // first product.
+        regs_dealloc<REGS_EPI>();
+        const int ew = warp - M_WARP_EPI;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+        const uint32_t obox0 = sbase + OST_OFF + (2 * ew) * OBOX, obox1 = obox0 + OBOX;
+        bool ok = true;
+        int g0 = 0;  // chunks of earlier pieces
+        for (int k = 0; ok && k < n_pieces; ++k) {
+            const Piece pc = piece(k);
+            for (int c = 0; c < pc.n; ++c) {
+                const int gc = g0 + c;
+                if (!(ok = wait_bounded(bar(B_ODONE), gc & 1, abort_flag,
+                                        (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (gc & 0xFFFF))))
                     break;
                 tc_fence_after_sync();
-                // intra: [num | den] = P [V | 1]; 16 chunk rows per step.  Descriptors
-                // are formed once per operand; a k step adds its compile-time
-                // offset to the start-address field (no carry: smem < 256 KB).
-                const uint64_t v1d = smem_desc_sw128(vb, ONES_OFF - (vb - sbase), 1024);
-                const uint32_t v1_lo = static_cast<uint32_t>(v1d), hi = static_cast<uint32_t>(v1d >> 32);
-                uint32_t v1v[C / 16];
-#pragma unroll
-                for (int k = 0; k < C / 16; ++k) v1v[k] = v1_lo + ((k * 2048) >> 4);
-                if (elect_one()) umma_ts_steps<C / 16, 8>(tmem + T_O, tmem + T_P, v1v, hi, ID_INTRA, 0u);
-                __syncwarp();
-                // inter: [num | den] += phi(Q) S_{<c}; 16 features per step
-                if (!(ok = wait_bounded(bar(B_PHIQREADY), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_PHIQREADY << 16) | (g & 0xFFFF))))
-                    break;
-                tc_fence_after_sync();
-                const uint32_t s_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + SPREV_OFF, 16, 1024));
-                uint32_t sv[F / 16];
-#pragma unroll
-                for (int k = 0; k < F / 16; ++k) sv[k] = s_lo + (((k / 4) * SBOX + (k % 4) * 32) >> 4);
-                if (elect_one()) {
-                    if (c > 0 || has_prev) umma_ts_steps<F / 16, 8>(tmem + T_O, tmem + T_PHIQ, sv, hi, ID_INTER, 1u);
-                    umma_commit(bar(B_ODONE));
-                }
-                __syncwarp();
-                // state: S^T += [V | 1]^T phi(K); 16 chunk rows per step
-                if (!(ok = wait_bounded(bar(B_PHIKREADY), ph, abort_flag,
-                                        (ROLE_BASED_MMA << 24) | (B_PHIKREADY << 16) | (g & 0xFFFF))))
-                    break;
-                tc_fence_after_sync();
-                const uint32_t pk_lo = static_cast<uint32_t>(smem_desc_sw128(sbase + PHIK_OFF, BOX, 1024));
-                uint32_t pkv[C / 16];
-#pragma unroll
-                for (int k = 0; k < C / 16; ++k) pkv[k] = pk_lo + ((k * 2048) >> 4);
-                if (elect_one()) {
-                    umma_ss_steps<C / 16>(tmem + T_ST, v1v, hi, pkv, hi, ID_STATE, (c > 0 || has_prev) ? 1u : 0u);
-                    umma_commit(bar(B_STDONE));
-                    umma_commit(bar(B_VEMPTY + b));
-                }
-                __syncwarp();
+                const int row0 = (pc.c0 + c) * C + ew * 32;  // this warp's first row in the head
+                write_o(lane_base, 0, lane, obox0, &p.tmO, row0, pc.bh, p.N,
+                        p.DEN + static_cast<size_t>(pc.bh) * p.N + row0 + lane);
+                write_o(lane_base, 1, lane, obox1, &p.tmO, row0, pc.bh, p.N, nullptr);
+                tc_fence_before_sync();
+                warp_arrive(bar(B_OFREE), lane);
             }
             g0 += pc.n;
-            }
-            if (elect_one()) umma_commit(bar(B_MMADONE));
-            __syncwarp();
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(bar(B_MMADONE), 0) && global_timer_ns() - t0 < (ok ? kWaitLimitNs : kDrainLimitNs)) {
-            }
         }
-        __syncwarp();
+        if (lane == 0) tma_store_wait_all();
     } else {
         // ------------------------------------------------ compute warps
+        regs_alloc<REGS_COMPUTE>();
         // Two warpgroups over the same 128 rows (warp w reads TMEM lanes
         // 32 (w % 4) ..); each takes half of every step.  Per chunk c: S(c)
         // into registers (the tensor core may then form S(c+1)); P(c) once
-        // chunk c-1's [num | den] is complete; O of chunk c-1; PREADY; the
-        // bf16 state copy of chunk c-1 and phi(Q) of chunk c; PHIQREADY;
-        // phi(K) of chunk c; PHIKREADY.
+        // chunk c-1's [num | den] is complete; PREADY; the bf16 state copy of
+        // chunk c-1 and phi(Q) of chunk c; PHIQREADY; phi(K) of chunk c;
+        // PHIKREADY.  The epilogue warps write O.
         const int i = threadIdx.x % 128;  // row of the chunk = TMEM lane; also row i of S^T
         const int grp = warp / 4;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
         const float scale = p.scale;
         const float r = sqrtf(scale), h = scale * 0.70710678118654752f, g = scale;
-        const uint32_t obox = sbase + OST_OFF + warp * OBOX;
         const int col0 = grp == 0 ? 0 : 64, ncol = grp == 0 ? 64 : F - 64;  // this group's state columns
         bool ok = true;
         int g0 = 0;  // chunks of earlier pieces
         // The chunk before the current one (possibly the previous piece's
         // last): its O is written while the current chunk's products run.
-        int prev_bh = 0, prev_row0 = 0, prev_publish = 0, pc_prev_bh = 0;
+        int prev_bh = 0, prev_publish = 0, pc_prev_bh = 0;
         // --- this warp's rows and columns of S^T (fp32), once a piece's last
         // state product is done, for the CTA that walks the rest of the head;
         // then this warp's flag
@@ -647,11 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
                 tc_fence_after_sync();
             }
             tmem_st32(lane_base + T_P + grp * 32, pk);
-            if (gc > 0)  // --- O of the previous chunk, this group's 32 columns
-                write_o(lane_base, grp, lane, obox, &p.tmO, prev_row0 + (warp % 4) * 32, prev_bh, p.N,
-                        grp == 0 ? p.DEN + static_cast<size_t>(prev_bh) * p.N + prev_row0 + i : nullptr);
             prev_bh = bh;
-            prev_row0 = (c0 + c) * C;
             tmem_st_wait();
             tc_fence_before_sync();
             warp_arrive(bar(B_PREADY), lane);
@@ -722,26 +772,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) based_kernel(const __grid_cons
         // of a head)
         if (ok && g0 > 0) {
             const int g_last = g0 - 1;
-            ok = wait_bounded(bar(B_ODONE), g_last & 1, abort_flag,
-                              (ROLE_BASED_COMPUTE << 24) | (B_ODONE << 16) | (g_last & 0xFFFF));
-            if (ok) {
-                tc_fence_after_sync();
-                write_o(lane_base, grp, lane, obox, &p.tmO, prev_row0 + (warp % 4) * 32, prev_bh, p.N,
-                        grp == 0 ? p.DEN + static_cast<size_t>(prev_bh) * p.N + prev_row0 + i : nullptr);
-            }
-            if (ok && MODE == 2 && prev_publish &&
+            if (MODE == 2 && prev_publish &&
                 (ok = wait_bounded(bar(B_STDONE), g_last & 1, abort_flag,
                                    (ROLE_BASED_COMPUTE << 24) | (B_STDONE << 16) | (g_last & 0xFFFF)))) {
                 tc_fence_after_sync();
                 publish(pc_prev_bh);
             }
         }
-        if (lane == 0) tma_store_wait_all();
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == WARP_MMA) {
+    if (warp == M_WARP_MMA) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -936,10 +978,15 @@ cudaError_t launch_based(const BasedParams &p, cudaStream_t stream) {
             (err = cudaFuncSetAttribute(based::based_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         based::SMEM_ALLOC)) != cudaSuccess)
             return err;
+        for (auto kern : {based::based_kernel<0>, based::based_kernel<1>, based::based_kernel<2>}) {
+            cudaFuncAttributes attr;
+            if ((err = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return err;
+            if (attr.numRegs != based::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        }
         configured_device = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(based::NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(based::MAIN_THREADS, 1, 1);
     cfg.dynamicSmemBytes = based::SMEM_ALLOC;
     cfg.stream = stream;
     if (p.balanced) {
