@@ -134,7 +134,10 @@ struct Layout {
     // (lane = query of the current query tile).
     static constexpr uint32_t T_S = 0;           // S^T, then bf16 P^T (see pcol)
     static constexpr uint32_t T_DP = 128;        // dP^T, then bf16 dS^T (see pcol); then dQ_part
-    static constexpr uint32_t T_DQ = T_DP + 128 - D;  // dQ_part (D columns)
+    // dQ_part (D columns): at D = 64 in columns of its own (the next dP^T need
+    // not wait for it to be read), at D = 128 over the dP^T block
+    static constexpr bool DQ_OWN = D == 64;
+    static constexpr uint32_t T_DQ = DQ_OWN ? 384 : T_DP + 128 - D;
     static constexpr uint32_t T_DV = 256;        // dV accumulator (D columns)
     static constexpr uint32_t T_DK = 256 + D;    // dK accumulator (D columns)
     // Column (within the S^T / dP^T block) of the bf16 results of query
@@ -455,7 +458,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                             break;
                         tc_fence_after_sync();
                         issue_s(q0);
-                        if (g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
+                        if (!L::DQ_OWN && g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
                                                          (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
                             break;
                         if (L::DO_SINGLE && !(ok = wait_bounded(bar(L::B_DOFULL), g & 1, abort_flag,
@@ -521,6 +524,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                         }
                         if (!ok) break;
                         commit(L::B_QEMPTY + b);  // Q, dO of this tile are no longer read
+                        // with its own columns, the previous tile's dQ_part must have been read first
+                        if (L::DQ_OWN && g > 0 && !(ok = wait_bounded(bar(L::B_DQREAD), (g - 1) & 1, abort_flag,
+                                                                      (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
+                            break;
                         // dQ_part = dS' K (lane = query), 16 keys per step, dS' from
                         // the dS^T buffer (MN-major A) and K MN-major.
                         {
@@ -541,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_bwd_kernel(const __grid_c
                             __syncwarp();
                         }
                         if (has_next) {
-                            if (!(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
+                            if (!L::DQ_OWN && !(ok = wait_bounded(bar(L::B_DQREAD), ph, abort_flag,
                                                     (ROLE_BWD_MMA << 24) | (L::B_DQREAD << 16) | (g & 0xFFFF))))
                                 break;
                             if (L::DO_SINGLE && !(ok = wait_bounded(bar(L::B_DOFULL), (g + 1) & 1, abort_flag,
