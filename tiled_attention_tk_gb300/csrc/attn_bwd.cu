@@ -133,7 +133,7 @@ struct Layout {
     // TMEM columns; lane = key of this CTA's key tile, except dQ_part
     // (lane = query of the current query tile).
     static constexpr uint32_t T_S = 0;           // S^T, then bf16 P^T (see pcol)
-    static constexpr uint32_t T_DP = 128;        // dP^T, then bf16 dS^T (see pcol); then dQ_part
+    static constexpr uint32_t T_DP = 128;        // dP^T, then bf16 dS^T (see pcol); then dQ_part at D = 128
     // dQ_part (D columns): at D = 64 in columns of its own (the next dP^T need
     // not wait for it to be read), at D = 128 over the dP^T block
     static constexpr bool DQ_OWN = D == 64;
